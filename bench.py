@@ -1,0 +1,502 @@
+#!/usr/bin/env python
+"""Benchmark of the FP8 delayed-scaling linear layer on one GB300 per rank.
+
+One step = one mixed-precision training step of the proj linear of the
+transformer workload (M = 8192 tokens, K = N = 4096, bf16 activations with
+0.1 % outliers, fp32 master weights ~ N(0, 0.02), bf16 output gradient), run
+through the library's entry points on one CUDA stream:
+  fp8_quantize(x  -> X8, X8^T, amax)           E4M3
+  fp8_quantize(W  -> W8, W8^T, amax)           E4M3 (fp32 master in)
+  fp8_linear_fwd(X8, W8 -> Y bf16, amax_y)
+  fp8_quantize(dY -> dY8, dY8^T, amax)         E5M2
+  fp8_linear_dgrad(dY8, W8^T -> dX bf16)
+  fp8_linear_wgrad(dY8^T, X8^T -> dW bf16)
+  mp_master_step(dW -> master, momentum, w8)   SGD-momentum, loss scale 2^16
+  delayed_scaling_update(x, w, y, dy metas)    L = 1024, most_recent
+The metric counts the FLOPs the FP8 tensor cores perform, 3 * 2 * M * N * K,
+per step time. Multi-GPU runs are independent replicas (weak scaling).
+
+--impl reference times the CPU oracle on a bounded sample of the same step.
+"""
+
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+M_TOK, K_IN, N_OUT = 8192, 4096, 4096
+HIST_LEN = 1024
+LR, MU, S0 = 1e-4, 0.9, 2.0 ** 16
+METRIC = "FP8 linear fwd+bwd TFLOP/s at M=8192,K=N=4096; % of GB300 dense FP8 peak"
+WORKLOAD = "transformer proj linear 4096->4096, M=8192 tokens (seq 2048 x batch 4), bf16 in, FP8 HYBRID delayed scaling"
+GEMM_SRC = os.path.join(ROOT, "fp8_mixed_precision_reduce_gb300", "csrc", "gemm.cu")
+PROFILE = os.path.join(ROOT, "profiles", "gemm_fp8_kernel_proj_8192x4096x4096.md")
+FALLBACK_BF16_TFLOPS = 1900.0
+FP8_OVER_BF16 = 4.5 / 2.25  # nominal dense ratio
+
+
+def flops_per_step(m=M_TOK, n=N_OUT, k=K_IN) -> float:
+    return 3.0 * 2.0 * m * n * k
+
+
+# ------------------------------------------------------------------ peaks
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return p, "measured"
+    except (OSError, ValueError):
+        return {"bf16_tflops": FALLBACK_BF16_TFLOPS, "hbm_gbs": 6800.0}, "fallback"
+
+
+def gemm_traffic_from_profile():
+    """DRAM bytes per launch from the committed ncu summary, if it was taken
+    on the current gemm.cu (its sha256 is recorded there); else None."""
+    try:
+        text = open(PROFILE).read()
+    except OSError:
+        return None
+    sha = hashlib.sha256(open(GEMM_SRC, "rb").read()).hexdigest()
+    vals = {}
+    for line in text.splitlines():
+        line = line.strip().strip("-").strip()
+        if ":" in line:
+            k, v = line.split(":", 1)
+            vals[k.strip().strip("`")] = v.strip().strip("`")
+    if vals.get("gemm_cu_sha256") != sha:
+        return None
+    try:
+        return float(vals["dram_bytes_per_launch"])
+    except (KeyError, ValueError):
+        return None
+
+
+# ------------------------------------------------------------------ clocks
+
+
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons during a region."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+            time.sleep(0.3)
+        except OSError:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            time.sleep(0.2)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+        return False
+
+    def summary(self):
+        sm, mx, reasons = [], [], set()
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 7:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx.append(float(parts[1]))
+            except ValueError:
+                continue
+            for nm, v in zip(names, parts[3:7]):
+                if v.lower() == "active":
+                    reasons.add(nm)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ------------------------------------------------------------ distributed
+
+
+def dist_setup():
+    import torch
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if torch.cuda.is_available():
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend=backend)
+    elif torch.cuda.is_available():
+        torch.cuda.set_device(local)
+    return world, rank, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.barrier()
+
+
+def max_over_ranks(value: float, world: int) -> float:
+    """Max of a host float over all ranks (plain float when world == 1)."""
+    if world <= 1:
+        return float(value)
+    import torch
+    import torch.distributed as dist
+
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([float(value)], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ------------------------------------------------------------ our step
+
+
+class LinearStep:
+    """Device state and the step of the proj linear, through the library."""
+
+    def __init__(self, m=M_TOK, k=K_IN, n=N_OUT, seed=3):
+        import torch
+
+        import fp8_mixed_precision_reduce_gb300 as fp8mp
+        import workloads
+
+        self.fp8mp = fp8mp
+        self.m, self.k, self.n = m, k, n
+        dev = "cuda"
+        tb = workloads.transformer_block(seed=seed, m=m, d=k, device=dev)
+        self.x = tb.x                                                     # (M, K) bf16
+        self.dy = tb.dy_proj[:, :n].contiguous() if n != k else tb.dy_proj  # (M, N) bf16
+        self.master = workloads.master_weights(n * k, seed=seed, device=dev).view(n, k)
+        del tb
+        u8 = torch.uint8
+        self.X8 = torch.empty((m, k), dtype=u8, device=dev)
+        self.X8t = torch.empty((k, m), dtype=u8, device=dev)
+        self.W8 = torch.empty((n, k), dtype=u8, device=dev)
+        self.W8t = torch.empty((k, n), dtype=u8, device=dev)
+        self.D8 = torch.empty((m, n), dtype=u8, device=dev)
+        self.D8t = torch.empty((n, m), dtype=u8, device=dev)
+        self.y = torch.empty((m, n), dtype=torch.bfloat16, device=dev)
+        self.dx = torch.empty((m, k), dtype=torch.bfloat16, device=dev)
+        self.dw = torch.empty((n, k), dtype=torch.bfloat16, device=dev)
+        self.mom = torch.zeros((n, k), dtype=torch.float32, device=dev)
+        self.w8_next = torch.empty((n, k), dtype=u8, device=dev)
+        self.S = torch.tensor([S0], dtype=torch.float32, device=dev)
+        self.growth = torch.zeros(1, dtype=torch.int32, device=dev)
+        self.found = torch.zeros(1, dtype=torch.int32, device=dev)
+        E4, E5 = fp8mp.E4M3, fp8mp.E5M2
+        self.mx, self.mw, self.my = (fp8mp.Meta(HIST_LEN, E4) for _ in range(3))
+        self.md = fp8mp.Meta(HIST_LEN, E5)
+        self.launches_per_step = 10  # 3 casts, 3 GEMMs, 3 master-step kernels, 1 scale update
+
+    def step(self, gemm_events=None):
+        f = self.fp8mp
+        f.fp8_quantize(self.x, f.E4M3, self.mx.scale, self.X8, self.X8t, self.mx.cur_amax)
+        f.fp8_quantize(self.master, f.E4M3, self.mw.scale, self.W8, self.W8t, self.mw.cur_amax)
+        ev = gemm_events
+        if ev is not None:
+            ev[0].record()
+        f.fp8_linear_fwd(self.X8, self.W8, self.mx.scale_inv, self.mw.scale_inv, self.y, y_amax=self.my.cur_amax)
+        if ev is not None:
+            ev[1].record()
+        f.fp8_quantize(self.dy, f.E5M2, self.md.scale, self.D8, self.D8t, self.md.cur_amax)
+        if ev is not None:
+            ev[2].record()
+        f.fp8_linear_dgrad(self.D8, self.W8t, self.md.scale_inv, self.mw.scale_inv, self.dx)
+        if ev is not None:
+            ev[3].record()
+        f.fp8_linear_wgrad(self.D8t, self.X8t, self.md.scale_inv, self.mx.scale_inv, self.dw)
+        if ev is not None:
+            ev[4].record()
+        f.mp_master_step(self.dw, self.master, self.mom, self.w8_next, self.mw.scale, self.mw.cur_amax, self.S,
+                         self.growth, self.found, LR, MU)
+        f.delayed_scaling_update([self.mx, self.mw, self.my, self.md], f.AMAX_MOST_RECENT, 0)
+
+
+def run_ours(args, world, rank, local):
+    import torch
+
+    peaks, peak_kind = load_peaks()
+    st = LinearStep()
+    torch.cuda.synchronize()
+    flush = torch.empty(int(2 * 129e6 // 4) + 1, dtype=torch.float32, device="cuda")  # > 2x L2
+
+    for _ in range(args.warmup):
+        st.step()
+    torch.cuda.synchronize()
+    rc = st.fp8mp.fp8mp_check()
+    if rc != 0:
+        raise RuntimeError(f"warm-up failed: {st.fp8mp.last_error()}")
+
+    E = torch.cuda.Event
+    starts = [E(enable_timing=True) for _ in range(args.steps)]
+    ends = [E(enable_timing=True) for _ in range(args.steps)]
+    gev = [[E(enable_timing=True) for _ in range(5)] for _ in range(args.steps)]
+    barrier(world)
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clocks:
+        for i in range(args.steps):
+            flush.fill_(float(i))  # L2 flush between timed steps (outside the step events)
+            starts[i].record()
+            st.step(gev[i])
+            ends[i].record()
+        torch.cuda.synchronize()
+    barrier(world)
+    rc = st.fp8mp.fp8mp_check()
+    if rc != 0:
+        raise RuntimeError(f"timed steps failed: {st.fp8mp.last_error()}")
+    step_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+    gemm_ms = [[g[0].elapsed_time(g[1]), g[2].elapsed_time(g[3]), g[3].elapsed_time(g[4])] for g in gev]
+    ms_per_step = max_over_ranks(statistics.mean(step_ms), world)
+    gemm_step_ms = max_over_ranks(statistics.mean(sum(g) for g in gemm_ms), world)
+    gemm_launch_ms = statistics.mean(x for g in gemm_ms for x in g)
+
+    # end to end through the public API: pinned host x, dY in; y, dX out
+    x_h = st.x.cpu().pin_memory()
+    dy_h = st.dy.cpu().pin_memory()
+    y_h = torch.empty(st.y.shape, dtype=st.y.dtype).pin_memory()
+    dx_h = torch.empty(st.dx.shape, dtype=st.dx.dtype).pin_memory()
+    e2e_steps = max(3, min(args.steps, 10))
+    torch.cuda.synchronize()
+    barrier(world)
+    e0, e1 = E(enable_timing=True), E(enable_timing=True)
+    e0.record()
+    for _ in range(e2e_steps):
+        st.x.copy_(x_h, non_blocking=True)
+        st.dy.copy_(dy_h, non_blocking=True)
+        st.step()
+        y_h.copy_(st.y, non_blocking=True)
+        dx_h.copy_(st.dx, non_blocking=True)
+    e1.record()
+    torch.cuda.synchronize()
+    barrier(world)
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1) / e2e_steps, world)
+    h2d = x_h.numel() * x_h.element_size() + dy_h.numel() * dy_h.element_size()
+    d2h = y_h.numel() * y_h.element_size() + dx_h.numel() * dx_h.element_size()
+
+    fl = flops_per_step()
+    value = world * fl / (ms_per_step * 1e-3) / 1e12
+    fp8_peak = float(peaks["bf16_tflops"]) * FP8_OVER_BF16
+    achieved = 2.0 * M_TOK * N_OUT * K_IN / (gemm_launch_ms * 1e-3) / 1e12
+    traffic = gemm_traffic_from_profile()
+    clk = clocks.summary()
+    out = {
+        "metric": METRIC,
+        "value": round(value, 2),
+        "unit": "TFLOP/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(ms_per_step, 5),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "fp8 (e4m3/e5m2) x fp8 -> fp32 accumulate; bf16/fp32 tensors",
+        "data": "synthetic (seeded; shapes and distributions of the transformer proj workload)",
+        "config": {"workload": WORKLOAD, "M": M_TOK, "K": K_IN, "N": N_OUT, "history_len": HIST_LEN,
+                   "amax_compute_algo": "most_recent", "recipe": "HYBRID", "parallelism": f"replicas x{world}",
+                   "l2": "flushed (2x L2 write) between timed steps"},
+        "gemm_only": {"tflops": round(world * fl / (gemm_step_ms * 1e-3) / 1e12, 2), "ms_per_step": round(gemm_step_ms, 5)},
+        "roofline": {"kernel": "gemm_fp8_kernel", "bound": "tensor", "achieved": round(achieved, 2),
+                     "peak": round(fp8_peak, 1), "unit": "TFLOP/s", "frac": round(achieved / fp8_peak, 4),
+                     "traffic": traffic,
+                     "peak_source": f"{peak_kind} bf16 burst x {FP8_OVER_BF16:g} (nominal fp8/bf16 dense ratio)"},
+        "e2e": {"value": round(world * fl / (e2e_ms * 1e-3) / 1e12, 2), "unit": "TFLOP/s",
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 5)},
+        "gpu_launches": st.launches_per_step * args.steps,
+        "clocks": {"sm_mhz": clk["sm_mhz"], "sm_max_mhz": clk["sm_max_mhz"], "reasons": clk["reasons"]},
+    }
+    del flush
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        out["cpu_baseline"] = cpu_baseline(args.baseline_tokens)
+    return out
+
+
+# --------------------------------------------------- the oracle (CPU) arm
+
+
+def oracle_step_sample(tokens: int, seed=3):
+    """Inputs of a `tokens`-row sample of the step, prepared outside timing."""
+    import numpy as np
+
+    import workloads
+
+    tb = workloads.transformer_block(seed=seed, m=tokens, d=K_IN)
+    x = tb.x.view(__import__("torch").int16).numpy().view(np.uint16)
+    dy = tb.dy_proj.view(__import__("torch").int16).numpy().view(np.uint16)
+    w = workloads.master_weights(N_OUT * K_IN, seed=seed).numpy().reshape(N_OUT, K_IN)
+    return x, dy, w
+
+
+def oracle_step(orc, x, dy, w, mom, metas):
+    """The same step on the CPU oracle (codes, GEMMs in fp64, master step)."""
+    import numpy as np
+
+    E4, E5 = orc.E4M3, orc.E5M2
+    mx, mw, my, md = metas
+    X8 = orc.cast(x, float(mx.scale[0]), E4)
+    mx.record_amax(orc.amax(x))
+    W8 = orc.cast(w, float(mw.scale[0]), E4)
+    mw.record_amax(orc.amax(w))
+    y, _ = orc.gemm_ref(X8, E4, W8, E4, float(mx.scale_inv[0]), float(mw.scale_inv[0]), with_abs=False)
+    my.record_amax(np.float32(np.abs(y).max()))
+    D8 = orc.cast(dy, float(md.scale[0]), E5)
+    md.record_amax(orc.amax(dy))
+    W8t = orc.transpose_u8(W8)
+    dx, _ = orc.gemm_ref(D8, E5, W8t, E4, float(md.scale_inv[0]), float(mw.scale_inv[0]), with_abs=False)
+    D8t, X8t = orc.transpose_u8(D8), orc.transpose_u8(X8)
+    dw, _ = orc.gemm_ref(D8t, E5, X8t, E4, float(md.scale_inv[0]), float(mx.scale_inv[0]), with_abs=False)
+    import torch
+
+    g = torch.from_numpy(dw.astype(np.float32)).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    w8 = np.empty(w.size, dtype=np.uint8)
+    st = orc.LossScaleState(S0)
+    orc.master_step(g.reshape(-1), w.reshape(-1), mom.reshape(-1), w8, float(mw.scale[0]), mw.cur_amax, st, LR, MU)
+    for m, f in zip(metas, (E4, E4, E4, E5)):
+        orc.scale_update(m, f, orc.AMAX_MOST_RECENT, 0)
+
+
+def cpu_baseline(tokens: int):
+    import numpy as np
+
+    import oracle as orc
+
+    orc.build()
+    x, dy, w = oracle_step_sample(tokens)
+    mom = np.zeros_like(w)
+    metas = [orc.Meta(HIST_LEN) for _ in range(4)]
+    t0 = time.perf_counter()
+    oracle_step(orc, x, dy, w, mom, metas)
+    dt = time.perf_counter() - t0
+    fl = flops_per_step(m=tokens)
+    return {"value": round(fl / dt / 1e12, 6), "unit": "TFLOP/s", "cores": orc.num_threads(), "kind": "oracle",
+            "sample": f"one full step on a {tokens}-token sample (x {tokens}x{K_IN}, dY {tokens}x{N_OUT}, "
+                      f"full {N_OUT}x{K_IN} weight and master step), {dt:.2f} s"}
+
+
+def run_reference(args, world, rank):
+    if rank != 0:
+        return None
+    import numpy as np
+
+    import oracle as orc
+
+    orc.build()
+    x, dy, w = oracle_step_sample(args.cpu_tokens)
+    mom = np.zeros_like(w)
+    metas = [orc.Meta(HIST_LEN) for _ in range(4)]
+    for _ in range(args.warmup):
+        oracle_step(orc, x, dy, w.copy(), mom.copy(), [m.copy() for m in metas])
+    times = []
+    for _ in range(args.steps):
+        t0 = time.perf_counter()
+        oracle_step(orc, x, dy, w, mom, metas)
+        times.append(time.perf_counter() - t0)
+    ms = statistics.mean(times) * 1e3
+    fl = flops_per_step(m=args.cpu_tokens)
+    value = fl / (ms * 1e-3) / 1e12
+    return {
+        "impl": "reference",
+        "metric": METRIC,
+        "value": round(value, 6),
+        "unit": "TFLOP/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(ms, 3),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "fp64 accumulate over decoded fp8 codes; fp32 casts and master step",
+        "data": "synthetic (seeded)",
+        "config": {"workload": WORKLOAD, "M": M_TOK, "K": K_IN, "N": N_OUT, "history_len": HIST_LEN,
+                   "parallelism": "host cores", "sample_tokens": args.cpu_tokens},
+        "cpu_baseline": {"value": round(value, 6), "unit": "TFLOP/s", "cores": orc.num_threads(), "kind": "oracle",
+                         "sample": f"each step: the full step on a {args.cpu_tokens}-token sample of the "
+                                   f"{M_TOK}-token workload"},
+        "e2e": {"value": round(value, 6), "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
+    ap.add_argument("--cpu-tokens", type=int, default=96,
+                    help="tokens of the oracle's bounded sample per step of --impl reference")
+    ap.add_argument("--baseline-tokens", type=int, default=1024,
+                    help="tokens of the oracle sample timed as cpu_baseline (about 10-30 s)")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+
+    if args.impl == "reference":
+        world = int(os.environ.get("WORLD_SIZE", "1"))
+        rank = int(os.environ.get("RANK", "0"))
+        out = run_reference(args, world, rank)
+        if out is not None:
+            print(json.dumps(out), flush=True)
+        return 0
+
+    import torch
+
+    if not torch.cuda.is_available():
+        print(json.dumps({"error": "no CUDA device"}), flush=True)
+        return 1
+    import fp8_mixed_precision_reduce_gb300 as fp8mp
+
+    fp8mp.load()  # raises when the library is missing: no fallback
+    world, rank, local = dist_setup()
+    out = run_ours(args, world, rank, local)
+    if rank == 0:
+        print(json.dumps(out), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

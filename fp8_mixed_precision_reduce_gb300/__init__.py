@@ -1,0 +1,205 @@
+"""Python binding of libfp8mp, the GB300 FP8 delayed-scaling linear layer.
+
+Argument marshalling only: every function below forwards to the C entry
+point of the same name in ``libfp8mp.so`` (declared in ``include/fp8mp.h``),
+passing device pointers, sizes and the CUDA stream. All computation runs in
+the library's CUDA kernels. torch is used for device memory and streams.
+If the library has not been built, ``load()`` raises: there is no fallback.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+E4M3, E5M2 = 0, 1
+F32, BF16 = 0, 1
+AMAX_MAX, AMAX_MOST_RECENT = 0, 1
+MAX_HISTORY = 8192
+FMT_MAX = {E4M3: 448.0, E5M2: 57344.0}
+
+OK, ERR_INVALID, ERR_DEVICE, ERR_LAUNCH, ERR_TIMEOUT = 0, -1, -2, -3, -4
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libfp8mp.so")
+EXPORTS = ("fp8_quantize", "fp8_linear_fwd", "fp8_linear_dgrad", "fp8_linear_wgrad",
+           "delayed_scaling_update", "mp_master_step", "fp8mp_check", "fp8mp_last_error",
+           "fp8mp_version")
+
+_lib = None
+
+
+class Fp8mpError(RuntimeError):
+    def __init__(self, code: int, msg: str):
+        super().__init__(f"libfp8mp error {code}: {msg}")
+        self.code = code
+
+
+class fp8mp_meta(ctypes.Structure):
+    """Mirror of the C struct fp8mp_meta (device pointers + two int32)."""
+
+    _fields_ = [("amax_history", ctypes.c_void_p), ("scale", ctypes.c_void_p),
+                ("scale_inv", ctypes.c_void_p), ("cur_amax", ctypes.c_void_p),
+                ("history_len", ctypes.c_int32), ("fmt", ctypes.c_int32)]
+
+
+def build(force: bool = False) -> str:
+    from . import buildlib
+
+    return buildlib.build(force=force)
+
+
+def load(path: str | None = None):
+    """Loads libfp8mp.so (raises if it is missing) and declares the signatures."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    path = path or LIB_PATH
+    if not os.path.exists(path):
+        raise Fp8mpError(ERR_LAUNCH, f"{path} is missing: build it with "
+                         "fp8_mixed_precision_reduce_gb300.build() (no CPU fallback exists)")
+    L = ctypes.CDLL(path)
+    P, I64, I32, F = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int32, ctypes.c_float
+    L.fp8_quantize.argtypes = [P, I32, I64, I64, I32, P, P, P, P, P]
+    L.fp8_linear_fwd.argtypes = [P, P, I64, I64, I64, P, P, P, I32, P, I32, P, P]
+    L.fp8_linear_dgrad.argtypes = [P, P, I64, I64, I64, I32, P, P, P, I32, P]
+    L.fp8_linear_wgrad.argtypes = [P, P, I64, I64, I64, I32, P, P, P, I32, P]
+    L.delayed_scaling_update.argtypes = [ctypes.POINTER(fp8mp_meta), I32, I32, I32, P]
+    L.mp_master_step.argtypes = [P, I64, P, P, P, P, P, P, P, P, F, F, F, F, I32, P]
+    L.fp8mp_check.argtypes = [P]
+    L.fp8mp_last_error.restype = ctypes.c_char_p
+    L.fp8mp_version.restype = I32
+    for name in ("fp8_quantize", "fp8_linear_fwd", "fp8_linear_dgrad", "fp8_linear_wgrad",
+                 "delayed_scaling_update", "mp_master_step", "fp8mp_check"):
+        getattr(L, name).restype = ctypes.c_int
+    _lib = L
+    return L
+
+
+def last_error() -> str:
+    return load().fp8mp_last_error().decode()
+
+
+def _check(rc: int) -> None:
+    if rc != OK:
+        raise Fp8mpError(rc, last_error())
+
+
+def _ptr(t) -> int | None:
+    if t is None:
+        return None
+    if isinstance(t, int):
+        return t
+    return t.data_ptr()
+
+
+def _stream(stream) -> int | None:
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+def _dtype_code(t: torch.Tensor) -> int:
+    if t.dtype == torch.float32:
+        return F32
+    if t.dtype == torch.bfloat16:
+        return BF16
+    raise TypeError(f"unsupported dtype {t.dtype}")
+
+
+def _rows_cols(t: torch.Tensor):
+    if t.dim() == 2:
+        return t.shape[0], t.shape[1]
+    return 1, t.numel()
+
+
+# ------------------------------------------------------------- entry points
+
+
+def fp8_quantize(x: torch.Tensor, fmt: int, scale: torch.Tensor, out: torch.Tensor,
+                 out_t: torch.Tensor | None = None, amax: torch.Tensor | None = None,
+                 stream=None) -> None:
+    """out = sat_rne(x * scale) as FP8 codes (uint8), out_t its transpose,
+    amax = max(amax, max|x|). x is 2-D (rows, cols) or flat, contiguous."""
+    rows, cols = _rows_cols(x)
+    _check(load().fp8_quantize(_ptr(x), _dtype_code(x), rows, cols, fmt, _ptr(scale), _ptr(out),
+                               _ptr(out_t), _ptr(amax), _stream(stream)))
+
+
+def fp8_linear_fwd(x8: torch.Tensor, w8: torch.Tensor, sinv_x: torch.Tensor, sinv_w: torch.Tensor,
+                   y: torch.Tensor, bias: torch.Tensor | None = None,
+                   y_amax: torch.Tensor | None = None, stream=None) -> None:
+    """y[M, N] = (x8[M, K] . w8[N, K]^T) * sinv_x * sinv_w + bias."""
+    M, K = x8.shape
+    N = w8.shape[0]
+    _check(load().fp8_linear_fwd(_ptr(x8), _ptr(w8), M, N, K, _ptr(sinv_x), _ptr(sinv_w), _ptr(bias),
+                                 _dtype_code(bias) if bias is not None else F32, _ptr(y), _dtype_code(y),
+                                 _ptr(y_amax), _stream(stream)))
+
+
+def fp8_linear_dgrad(dy8: torch.Tensor, w8t: torch.Tensor, sinv_dy: torch.Tensor,
+                     sinv_w: torch.Tensor, dx: torch.Tensor, dy_fmt: int = E5M2, stream=None) -> None:
+    """dx[M, K] = (dy8[M, N] . w8t[K, N]^T) * sinv_dy * sinv_w."""
+    M, N = dy8.shape
+    K = w8t.shape[0]
+    _check(load().fp8_linear_dgrad(_ptr(dy8), _ptr(w8t), M, N, K, dy_fmt, _ptr(sinv_dy), _ptr(sinv_w),
+                                   _ptr(dx), _dtype_code(dx), _stream(stream)))
+
+
+def fp8_linear_wgrad(dy8t: torch.Tensor, x8t: torch.Tensor, sinv_dy: torch.Tensor,
+                     sinv_x: torch.Tensor, dw: torch.Tensor, dy_fmt: int = E5M2, stream=None) -> None:
+    """dw[N, K] = (dy8t[N, M] . x8t[K, M]^T) * sinv_dy * sinv_x."""
+    N, M = dy8t.shape
+    K = x8t.shape[0]
+    _check(load().fp8_linear_wgrad(_ptr(dy8t), _ptr(x8t), M, N, K, dy_fmt, _ptr(sinv_dy), _ptr(sinv_x),
+                                   _ptr(dw), _dtype_code(dw), _stream(stream)))
+
+
+class Meta:
+    """One tensor's delayed-scaling state in device memory (fp32)."""
+
+    def __init__(self, history_len: int, fmt: int, device="cuda"):
+        self.fmt = fmt
+        self.history_len = history_len
+        self.amax_history = torch.zeros(history_len, dtype=torch.float32, device=device)
+        self.scale = torch.ones(1, dtype=torch.float32, device=device)
+        self.scale_inv = torch.ones(1, dtype=torch.float32, device=device)
+        self.cur_amax = torch.zeros(1, dtype=torch.float32, device=device)
+
+    def c_struct(self) -> fp8mp_meta:
+        return fp8mp_meta(self.amax_history.data_ptr(), self.scale.data_ptr(),
+                          self.scale_inv.data_ptr(), self.cur_amax.data_ptr(),
+                          self.history_len, self.fmt)
+
+
+def delayed_scaling_update(metas, algo: int, margin: int = 0, stream=None) -> None:
+    """Rolls each meta's history, picks the amax and refreshes scale/scale_inv."""
+    metas = list(metas)
+    arr = (fp8mp_meta * max(1, len(metas)))(*[m.c_struct() for m in metas])
+    _check(load().delayed_scaling_update(arr, len(metas), algo, margin, _stream(stream)))
+
+
+def mp_master_step(grad_bf16: torch.Tensor, master: torch.Tensor, momentum: torch.Tensor,
+                   w8: torch.Tensor, scale_w: torch.Tensor, amax_w: torch.Tensor,
+                   loss_scale: torch.Tensor, growth_tracker: torch.Tensor, found_inf: torch.Tensor,
+                   lr: float, momentum_coef: float, backoff: float = 0.5, growth_factor: float = 2.0,
+                   growth_interval: int = 2000, stream=None) -> None:
+    """Unscale, overflow skip, FP32 SGD-momentum update and E4M3 re-cast, in place."""
+    n = grad_bf16.numel()
+    _check(load().mp_master_step(_ptr(grad_bf16), n, _ptr(master), _ptr(momentum), _ptr(w8),
+                                 _ptr(scale_w), _ptr(amax_w), _ptr(loss_scale), _ptr(growth_tracker),
+                                 _ptr(found_inf), float(lr), float(momentum_coef), float(backoff),
+                                 float(growth_factor), int(growth_interval), _stream(stream)))
+
+
+def fp8mp_check(stream=None) -> int:
+    """Synchronises the stream and returns the library's check code (0 = OK)."""
+    return int(load().fp8mp_check(_stream(stream)))
+
+
+def fp8mp_version() -> int:
+    return int(load().fp8mp_version())

@@ -1,0 +1,272 @@
+// api.cu -- the extern "C" entry points of libfp8mp declared in
+// include/fp8mp.h: argument validation, device check, error reporting, and
+// dispatch to the kernels' launchers. No computation happens here.
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+
+#include "fp8mp_internal.cuh"
+
+namespace fp8mp {
+
+namespace {
+thread_local char g_last_error[512] = {0};
+}
+
+const char *last_error_message() { return g_last_error; }
+
+int fail(int code, const char *fmt, ...) {
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(g_last_error, sizeof g_last_error, fmt, ap);
+    va_end(ap);
+    return code;
+}
+
+void clear_error() { g_last_error[0] = 0; }
+
+int current_device(DeviceInfo *info) {
+    int dev = -1;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return fail(FP8MP_ERR_LAUNCH, "cudaGetDevice failed: %s", cudaGetErrorString(e));
+    static DeviceInfo cache[64];
+    static bool have[64] = {false};
+    if (dev >= 0 && dev < 64 && have[dev]) {
+        *info = cache[dev];
+    } else {
+        DeviceInfo d;
+        d.device = dev;
+        e = cudaDeviceGetAttribute(&d.cc_major, cudaDevAttrComputeCapabilityMajor, dev);
+        if (e == cudaSuccess) e = cudaDeviceGetAttribute(&d.cc_minor, cudaDevAttrComputeCapabilityMinor, dev);
+        if (e == cudaSuccess) e = cudaDeviceGetAttribute(&d.num_sms, cudaDevAttrMultiProcessorCount, dev);
+        if (e != cudaSuccess)
+            return fail(FP8MP_ERR_LAUNCH, "cudaDeviceGetAttribute failed: %s", cudaGetErrorString(e));
+        if (dev >= 0 && dev < 64) {
+            cache[dev] = d;
+            have[dev] = true;
+        }
+        *info = d;
+    }
+    if (info->cc_major != 10 || info->cc_minor != 3)
+        return fail(FP8MP_ERR_DEVICE, "device %d is sm_%d%d; libfp8mp is built for sm_103a only", info->device,
+                    info->cc_major, info->cc_minor);
+    return FP8MP_OK;
+}
+
+}  // namespace fp8mp
+
+using namespace fp8mp;
+
+namespace {
+
+bool valid_fmt(int32_t f) { return f == FP8MP_E4M3 || f == FP8MP_E5M2; }
+bool valid_dtype(int32_t d) { return d == FP8MP_F32 || d == FP8MP_BF16; }
+
+#define REQUIRE(cond, ...)                                        \
+    do {                                                          \
+        if (!(cond)) return fail(FP8MP_ERR_INVALID, __VA_ARGS__); \
+    } while (0)
+
+int check_ptr(const void *p, const char *fn, const char *name, bool required) {
+    if (p == nullptr) {
+        if (required) return fail(FP8MP_ERR_INVALID, "%s: %s is NULL", fn, name);
+        return FP8MP_OK;
+    }
+    if (!aligned16(p)) return fail(FP8MP_ERR_INVALID, "%s: %s is not 16-byte aligned", fn, name);
+    return FP8MP_OK;
+}
+
+#define CHECK_PTR(p, required)                              \
+    do {                                                    \
+        const int rc_ = check_ptr((p), fn, #p, (required)); \
+        if (rc_) return rc_;                                \
+    } while (0)
+
+// Scalars (scales, amax slots, S, counters) only need 4-byte alignment.
+int check_scalar(const void *p, const char *fn, const char *name, bool required) {
+    if (p == nullptr) {
+        if (required) return fail(FP8MP_ERR_INVALID, "%s: %s is NULL", fn, name);
+        return FP8MP_OK;
+    }
+    if ((reinterpret_cast<uintptr_t>(p) & 3u) != 0) return fail(FP8MP_ERR_INVALID, "%s: %s is misaligned", fn, name);
+    return FP8MP_OK;
+}
+
+#define CHECK_SCALAR(p, required)                              \
+    do {                                                       \
+        const int rc_ = check_scalar((p), fn, #p, (required)); \
+        if (rc_) return rc_;                                   \
+    } while (0)
+
+int check_gemm_dims(const char *fn, int64_t M, int64_t N, int64_t K) {
+    REQUIRE(M >= 0 && N >= 0 && K >= 0, "%s: negative dimension", fn);
+    REQUIRE(M % 16 == 0 && N % 16 == 0 && K % 16 == 0,
+            "%s: M, N and K must be multiples of 16 (got %lld, %lld, %lld)", fn, (long long)M, (long long)N,
+            (long long)K);
+    REQUIRE(M <= (1ll << 30) && N <= (1ll << 30) && K <= (1ll << 30), "%s: dimension above 2^30", fn);
+    return FP8MP_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int32_t fp8mp_version(void) { return 1; }
+
+const char *fp8mp_last_error(void) { return last_error_message(); }
+
+int fp8_quantize(const void *x, int32_t x_dtype, int64_t rows, int64_t cols, int32_t fmt, const float *scale,
+                 uint8_t *out, uint8_t *out_t, float *amax, void *stream) {
+    const char *fn = "fp8_quantize";
+    clear_error();
+    REQUIRE(valid_dtype(x_dtype), "%s: x_dtype %d is not FP8MP_F32 or FP8MP_BF16", fn, x_dtype);
+    REQUIRE(valid_fmt(fmt), "%s: fmt %d is not FP8MP_E4M3 or FP8MP_E5M2", fn, fmt);
+    REQUIRE(rows >= 0 && cols >= 0, "%s: negative size", fn);
+    REQUIRE(rows <= (1ll << 40) / (cols > 0 ? cols : 1), "%s: tensor too large", fn);
+    if (out_t != nullptr)
+        REQUIRE(rows % 16 == 0 && cols % 16 == 0,
+                "%s: with a transposed output rows and cols must be multiples of 16 (got %lld x %lld)", fn,
+                (long long)rows, (long long)cols);
+    if (rows == 0 || cols == 0) return FP8MP_OK;
+    CHECK_PTR(x, true);
+    CHECK_PTR(out, true);
+    CHECK_PTR(out_t, false);
+    CHECK_SCALAR(scale, true);
+    CHECK_SCALAR(amax, false);
+    DeviceInfo dev;
+    int rc = current_device(&dev);
+    if (rc) return rc;
+    return launch_quantize(x, x_dtype, rows, cols, fmt, scale, out, out_t, amax, static_cast<cudaStream_t>(stream),
+                           dev);
+}
+
+int fp8_linear_fwd(const uint8_t *x8, const uint8_t *w8, int64_t M, int64_t N, int64_t K, const float *sinv_x,
+                   const float *sinv_w, const void *bias, int32_t bias_dtype, void *y, int32_t y_dtype,
+                   float *y_amax, void *stream) {
+    const char *fn = "fp8_linear_fwd";
+    clear_error();
+    int rc = check_gemm_dims(fn, M, N, K);
+    if (rc) return rc;
+    REQUIRE(valid_dtype(y_dtype), "%s: y_dtype %d invalid", fn, y_dtype);
+    REQUIRE(bias == nullptr || valid_dtype(bias_dtype), "%s: bias_dtype %d invalid", fn, bias_dtype);
+    if (M == 0 || N == 0) return FP8MP_OK;
+    CHECK_PTR(y, true);
+    CHECK_PTR(bias, false);
+    CHECK_SCALAR(y_amax, false);
+    CHECK_SCALAR(sinv_x, true);
+    CHECK_SCALAR(sinv_w, true);
+    if (K > 0) {
+        CHECK_PTR(x8, true);
+        CHECK_PTR(w8, true);
+    }
+    DeviceInfo dev;
+    rc = current_device(&dev);
+    if (rc) return rc;
+    return launch_gemm(x8, FP8MP_E4M3, w8, FP8MP_E4M3, M, N, K, sinv_x, sinv_w, bias, bias_dtype, y, y_dtype,
+                       y_amax, static_cast<cudaStream_t>(stream), dev);
+}
+
+int fp8_linear_dgrad(const uint8_t *dy8, const uint8_t *w8t, int64_t M, int64_t N, int64_t K, int32_t dy_fmt,
+                     const float *sinv_dy, const float *sinv_w, void *dx, int32_t dx_dtype, void *stream) {
+    const char *fn = "fp8_linear_dgrad";
+    clear_error();
+    int rc = check_gemm_dims(fn, M, N, K);
+    if (rc) return rc;
+    REQUIRE(valid_fmt(dy_fmt), "%s: dy_fmt %d invalid", fn, dy_fmt);
+    REQUIRE(valid_dtype(dx_dtype), "%s: dx_dtype %d invalid", fn, dx_dtype);
+    if (M == 0 || K == 0) return FP8MP_OK;
+    CHECK_PTR(dx, true);
+    CHECK_SCALAR(sinv_dy, true);
+    CHECK_SCALAR(sinv_w, true);
+    if (N > 0) {
+        CHECK_PTR(dy8, true);
+        CHECK_PTR(w8t, true);
+    }
+    DeviceInfo dev;
+    rc = current_device(&dev);
+    if (rc) return rc;
+    return launch_gemm(dy8, dy_fmt, w8t, FP8MP_E4M3, M, K, N, sinv_dy, sinv_w, nullptr, FP8MP_F32, dx, dx_dtype,
+                       nullptr, static_cast<cudaStream_t>(stream), dev);
+}
+
+int fp8_linear_wgrad(const uint8_t *dy8t, const uint8_t *x8t, int64_t M, int64_t N, int64_t K, int32_t dy_fmt,
+                     const float *sinv_dy, const float *sinv_x, void *dw, int32_t dw_dtype, void *stream) {
+    const char *fn = "fp8_linear_wgrad";
+    clear_error();
+    int rc = check_gemm_dims(fn, M, N, K);
+    if (rc) return rc;
+    REQUIRE(valid_fmt(dy_fmt), "%s: dy_fmt %d invalid", fn, dy_fmt);
+    REQUIRE(valid_dtype(dw_dtype), "%s: dw_dtype %d invalid", fn, dw_dtype);
+    if (N == 0 || K == 0) return FP8MP_OK;
+    CHECK_PTR(dw, true);
+    CHECK_SCALAR(sinv_dy, true);
+    CHECK_SCALAR(sinv_x, true);
+    if (M > 0) {
+        CHECK_PTR(dy8t, true);
+        CHECK_PTR(x8t, true);
+    }
+    DeviceInfo dev;
+    rc = current_device(&dev);
+    if (rc) return rc;
+    return launch_gemm(dy8t, dy_fmt, x8t, FP8MP_E4M3, N, K, M, sinv_dy, sinv_x, nullptr, FP8MP_F32, dw, dw_dtype,
+                       nullptr, static_cast<cudaStream_t>(stream), dev);
+}
+
+int delayed_scaling_update(const fp8mp_meta *metas, int32_t n, int32_t algo, int32_t margin, void *stream) {
+    const char *fn = "delayed_scaling_update";
+    clear_error();
+    REQUIRE(n >= 0, "%s: negative count", fn);
+    if (n == 0) return FP8MP_OK;
+    REQUIRE(metas != nullptr, "%s: metas is NULL", fn);
+    REQUIRE(algo == FP8MP_AMAX_MAX || algo == FP8MP_AMAX_MOST_RECENT, "%s: algo %d invalid", fn, algo);
+    REQUIRE(margin >= 0 && margin <= 126, "%s: margin %d outside 0..126", fn, margin);
+    for (int32_t i = 0; i < n; ++i) {
+        const fp8mp_meta &m = metas[i];
+        REQUIRE(m.history_len >= 1 && m.history_len <= FP8MP_MAX_HISTORY, "%s: meta %d history_len %d outside 1..%d",
+                fn, i, m.history_len, FP8MP_MAX_HISTORY);
+        REQUIRE(valid_fmt(m.fmt), "%s: meta %d fmt %d invalid", fn, i, m.fmt);
+        REQUIRE(m.amax_history && m.scale && m.scale_inv && m.cur_amax, "%s: meta %d has a NULL pointer", fn, i);
+    }
+    DeviceInfo dev;
+    const int rc = current_device(&dev);
+    if (rc) return rc;
+    return launch_scale_update(metas, n, algo, margin, static_cast<cudaStream_t>(stream));
+}
+
+int mp_master_step(const uint16_t *grad_bf16, int64_t n, float *master, float *momentum, uint8_t *w8,
+                   const float *scale_w, float *amax_w, float *loss_scale, int32_t *growth_tracker,
+                   int32_t *found_inf, float lr, float momentum_coef, float backoff, float growth_factor,
+                   int32_t growth_interval, void *stream) {
+    const char *fn = "mp_master_step";
+    clear_error();
+    REQUIRE(n >= 0 && n <= (1ll << 40), "%s: n = %lld out of range", fn, (long long)n);
+    REQUIRE(growth_interval >= 1, "%s: growth_interval must be >= 1", fn);
+    CHECK_PTR(grad_bf16, n > 0);
+    CHECK_PTR(master, n > 0);
+    CHECK_PTR(momentum, n > 0);
+    CHECK_PTR(w8, n > 0);
+    CHECK_SCALAR(scale_w, true);
+    CHECK_SCALAR(amax_w, true);
+    CHECK_SCALAR(loss_scale, true);
+    CHECK_SCALAR(growth_tracker, true);
+    CHECK_SCALAR(found_inf, true);
+    DeviceInfo dev;
+    const int rc = current_device(&dev);
+    if (rc) return rc;
+    return launch_master_step(grad_bf16, n, master, momentum, w8, scale_w, amax_w, loss_scale, growth_tracker,
+                              found_inf, lr, momentum_coef, backoff, growth_factor, growth_interval,
+                              static_cast<cudaStream_t>(stream), dev);
+}
+
+int fp8mp_check(void *stream) {
+    clear_error();
+    cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return fail(FP8MP_ERR_LAUNCH, "stream synchronize failed: %s", cudaGetErrorString(e));
+    unsigned int flag = 0;
+    const int rc = read_and_clear_timeout_flag(&flag);
+    if (rc) return rc;
+    if (flag) return fail(FP8MP_ERR_TIMEOUT, "a GEMM kernel's bounded wait expired; its output is undefined");
+    return FP8MP_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,107 @@
+// fp8mp_internal.cuh -- device helpers (inline PTX for sm_103a) and host
+// plumbing shared by the libfp8mp translation units. Not part of the ABI.
+#pragma once
+
+#include <cstdint>
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+
+#include "../../include/fp8mp.h"
+
+namespace fp8mp {
+
+// ---------------------------------------------------------------- host side
+
+// Records a thread-local message and returns `code`.
+int fail(int code, const char *fmt, ...);
+// Clears the thread-local message.
+void clear_error();
+
+struct DeviceInfo {
+    int device;
+    int num_sms;
+    int cc_major, cc_minor;
+};
+// Fills `info` for the current device; returns FP8MP_ERR_DEVICE if it is not
+// an sm_103 GPU, FP8MP_ERR_LAUNCH on a CUDA error.
+int current_device(DeviceInfo *info);
+
+inline bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Launchers (return FP8MP_* codes; arguments already validated).
+int launch_quantize(const void *x, int x_dtype, int64_t rows, int64_t cols, int fmt,
+                    const float *scale, uint8_t *out, uint8_t *out_t, float *amax,
+                    cudaStream_t s, const DeviceInfo &dev);
+int launch_gemm(const uint8_t *a, int fmt_a, const uint8_t *b, int fmt_b, int64_t rows_a,
+                int64_t rows_b, int64_t kc, const float *sinv_a, const float *sinv_b,
+                const void *bias, int bias_dtype, void *out, int out_dtype, float *out_amax,
+                cudaStream_t s, const DeviceInfo &dev);
+int launch_scale_update(const fp8mp_meta *metas, int32_t n, int32_t algo, int32_t margin,
+                        cudaStream_t s);
+int launch_master_step(const uint16_t *g, int64_t n, float *w, float *v, uint8_t *w8,
+                       const float *scale_w, float *amax_w, float *loss_scale, int32_t *growth,
+                       int32_t *found_inf, float lr, float mu, float backoff, float growth_factor,
+                       int32_t growth_interval, cudaStream_t s, const DeviceInfo &dev);
+// Reads and clears the GEMM wait-timeout flag (after a stream sync).
+int read_and_clear_timeout_flag(unsigned int *value);
+const char *last_error_message();
+
+// -------------------------------------------------------------- device side
+
+// Largest finite value of each format.
+__host__ __device__ constexpr float fmt_max(int fmt) { return fmt == FP8MP_E4M3 ? 448.0f : 57344.0f; }
+
+__device__ __forceinline__ float bf16_bits_to_f32(uint32_t h16) { return __uint_as_float(h16 << 16); }
+
+// Two fp32 values -> two FP8 codes with round-to-nearest-even and
+// saturation to the largest finite value (PTX cvt .satfinite). `lo` lands in
+// the low byte. A NaN input is mapped to 0x7F explicitly.
+template <int FMT>
+__device__ __forceinline__ uint32_t cvt_pair(float lo, float hi) {
+    uint16_t r;
+    if constexpr (FMT == FP8MP_E4M3)
+        asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
+    else
+        asm("cvt.rn.satfinite.e5m2x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
+    uint32_t v = r;
+    if (lo != lo) v = (v & 0xFF00u) | 0x7Fu;
+    if (hi != hi) v = (v & 0x00FFu) | 0x7F00u;
+    return v;
+}
+
+// Four fp32 values -> four codes packed little-endian in a 32-bit word.
+template <int FMT>
+__device__ __forceinline__ uint32_t cvt_quad(float a, float b, float c, float d) {
+    return cvt_pair<FMT>(a, b) | (cvt_pair<FMT>(c, d) << 16);
+}
+
+// max that never lets a NaN win (the NaN operand is ignored).
+__device__ __forceinline__ float max_ignore_nan(float acc, float v) { return v > acc ? v : acc; }
+
+__device__ __forceinline__ float warp_max(float v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+    return v;
+}
+
+// Block-wide max of a non-negative value, then one atomic max into *dst by
+// thread 0 (integer order equals float order for values >= +0).
+__device__ __forceinline__ void block_amax_atomic(float v, float *dst) {
+    __shared__ float red[32];
+    v = warp_max(v);
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    if (lane == 0) red[warp] = v;
+    __syncthreads();
+    if (warp == 0) {
+        const int nw = (blockDim.x + 31) >> 5;
+        float t = lane < nw ? red[lane] : 0.0f;
+        t = warp_max(t);
+        if (lane == 0 && dst != nullptr) atomicMax(reinterpret_cast<int *>(dst), __float_as_int(t));
+    }
+}
+
+__device__ __forceinline__ uint32_t smem_u32(const void *p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+}  // namespace fp8mp

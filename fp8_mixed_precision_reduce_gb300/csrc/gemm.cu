@@ -1,0 +1,553 @@
+// gemm.cu -- FP8 x FP8 -> fp32-accumulated GEMM on the sm_103a tensor cores
+// (tcgen05 + TMEM + TMA), the engine of the forward, dgrad and wgrad GEMMs
+// of the FP8 linear layer.
+//
+// Pages: "Các kiểu dữ liệu FP8 gốc của PyTorch ..." (hotroai.com), the
+// torch._scaled_mm listing (two FP8 operands with their scales, a bias, the
+// output and its amax); "LLM) Mixed-Precision 개념 및 학습 방법 알아보기"
+// (data-newbie.tistory.com) "Accumulation into FP32" (products accumulated in
+// single precision, converted on the way out); "Как работает FP8
+// quantization на H100 (Transformer Engine)?" (aivaro.ru) section 3, step 4
+// (the GEMM result is divided by the scaling factors); "Transformer
+// Engine으로 FP8 사용하기" (coniverse.tistory.com) "Introduction to FP8" and
+// "FP8 사용방안(recipe)" (HYBRID: E5M2 gradients against E4M3 operands).
+//
+// Computes out[i, j] = (sum_k A[i, k] * B[j, k]) * sinv_a * sinv_b + bias[j]
+// with A (rows_a x kc) and B (rows_b x kc) both contiguous along k.
+//
+// Design (one CTA per SM, persistent over 128 x 256 output tiles):
+//   warp 0, one lane  : TMA producer -- 128-byte-swizzled 128 x 128 B tiles of
+//                       A and 256 x 128 B tiles of B into a 4-stage ring of
+//                       shared-memory buffers, each guarded by a full/empty
+//                       mbarrier pair;
+//   warp 1, one lane  : MMA issuer -- 4 x tcgen05.mma.kind::f8f6f4
+//                       (M 128, N 256, K 32) per stage into a TMEM accumulator,
+//                       tcgen05.commit frees the stage; two accumulators
+//                       (2 x 256 of the 512 TMEM columns) let the next tile's
+//                       mainloop run while the previous tile drains;
+//   warps 2-5         : epilogue -- tcgen05.ld of the warp's 32 TMEM lanes,
+//                       y = acc * (sinv_a * sinv_b) + bias, rounding to the
+//                       output type, 16-byte stores, running max |y|; one
+//                       atomic max per warp at the end.
+// Every mbarrier wait is bounded (about 2 s of %globaltimer); on expiry the
+// thread raises a device flag that fp8mp_check() reports, tells the other
+// roles to stop, waits (bounded) for its own copies / MMAs in flight, and the
+// CTA frees its TMEM and returns.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include <mutex>
+
+#include "fp8mp_internal.cuh"
+
+namespace fp8mp {
+
+__device__ unsigned int g_gemm_timeout_flag = 0;
+
+namespace {
+
+constexpr int BM = 128;           // rows of A per tile (TMEM lanes)
+constexpr int BN = 256;           // rows of B per tile (TMEM columns per accumulator)
+constexpr int BK = 128;           // bytes of k per stage = one 128-byte swizzle row
+constexpr int UMMA_K = 32;        // k of one kind::f8f6f4 MMA (32 bytes)
+constexpr int STAGES = 4;
+constexpr int NUM_EPI_WARPS = 4;
+constexpr int NUM_THREADS = 64 + 32 * NUM_EPI_WARPS;
+constexpr int GROUP_M = 16;       // tile raster: 16 row-blocks of A per group
+constexpr uint32_t TMEM_COLS = 2 * BN;
+constexpr uint64_t kWaitLimitNs = 2000000000ull;
+
+constexpr int A_BYTES = BM * BK;
+constexpr int B_BYTES = BN * BK;
+constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+constexpr int BAR_OFFSET = STAGES * STAGE_BYTES;
+constexpr int NUM_BARS = 2 * STAGES + 5;  // full, empty, tmem_full[2], tmem_empty[2], drain
+constexpr int SLOT_OFFSET = BAR_OFFSET + NUM_BARS * 8;
+constexpr int FLAG_OFFSET = SLOT_OFFSET + 8;
+constexpr int SMEM_USED = FLAG_OFFSET + 8;
+constexpr int SMEM_ALLOC = SMEM_USED + 1024;  // slack to align the base to 1024 bytes
+static_assert(STAGE_BYTES % 1024 == 0 && A_BYTES % 1024 == 0, "swizzle atoms need 1 KB alignment");
+
+struct GemmParams {
+    int rows_a, rows_b, num_kb;
+    int tiles_m, tiles_n;
+    const float *sinv_a, *sinv_b;
+    const void *bias;
+    int bias_bf16;
+    void *out;
+    int out_bf16;
+    float *out_amax;
+};
+
+// ------------------------------------------------------------ PTX wrappers
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+__device__ __forceinline__ void fence_mbar_init() {
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+__device__ __forceinline__ uint64_t global_timer_ns() {
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+// Waits until the phase of parity `parity` of `bar` has completed. Returns
+// false if another role has raised `abort_flag` or if about kWaitLimitNs
+// elapse (then raises both flags).
+__device__ __noinline__ bool wait_bounded(uint32_t bar, uint32_t parity, volatile int *abort_flag) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = global_timer_ns();
+    for (uint32_t i = 1;; ++i) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if ((i & 63u) == 0u) {
+            if (*abort_flag) return false;
+            if (global_timer_ns() - t0 > kWaitLimitNs) {
+                *abort_flag = 1;
+                atomicOr(&g_gemm_timeout_flag, 1u);
+                return false;
+            }
+        }
+    }
+}
+
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *map, uint32_t bar, int32_t c0,
+                                            int32_t c1) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%3, %4}], [%2];" ::"r"(
+            dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(c0), "r"(c1)
+        : "memory");
+}
+__device__ __forceinline__ void prefetch_tmap(const CUtensorMap *map) {
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
+}
+
+__device__ __forceinline__ void tmem_alloc(uint32_t slot, uint32_t ncols) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(slot), "r"(ncols)
+                 : "memory");
+}
+__device__ __forceinline__ void tmem_relinquish() {
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
+}
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+
+__device__ __forceinline__ void umma_f8f6f4(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                            uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+__device__ __forceinline__ void umma_commit(uint32_t bar) {
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+                 : "memory");
+}
+
+// 32 consecutive fp32 columns of this warp's 32 TMEM lanes (lane i of the
+// warp gets TMEM lane base+i); the wait is in the same asm so the registers
+// are valid when it returns.
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+        "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
+        "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];\n\t"
+        "tcgen05.wait::ld.sync.aligned;"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
+          "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]),
+          "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]),
+          "=r"(r[30]), "=r"(r[31])
+        : "r"(taddr)
+        : "memory");
+}
+
+// Shared-memory matrix descriptor of a K-major operand tile stored as rows of
+// 128 bytes with the 128-byte swizzle (the layout TMA writes with
+// CU_TENSOR_MAP_SWIZZLE_128B): 8-row atoms of 1024 bytes stacked along M/N.
+__device__ __forceinline__ uint64_t sw128_kmajor_desc(uint32_t saddr) {
+    uint64_t d = 0;
+    d |= static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4);  // start address, bits 0-13
+    d |= static_cast<uint64_t>(1u) << 16;                 // leading byte offset (unused here), bits 16-29
+    d |= static_cast<uint64_t>(1024u >> 4) << 32;         // stride byte offset: one 8-row atom, bits 32-45
+    d |= static_cast<uint64_t>(1u) << 46;                 // descriptor version for tcgen05, bits 46-47
+    d |= static_cast<uint64_t>(2u) << 61;                 // swizzle mode: 128 bytes, bits 61-63
+    return d;
+}
+
+// Tile index -> (row-block of A, row-block of B), grouped so that the CTAs
+// working at the same time share GROUP_M A panels and a few B panels in L2.
+__device__ __forceinline__ void tile_coords(int t, int tiles_m, int tiles_n, int &mb, int &nb) {
+    const int group = GROUP_M * tiles_n;
+    const int g = t / group;
+    const int first = g * GROUP_M;
+    const int gm = min(tiles_m - first, GROUP_M);
+    const int local = t - g * group;
+    mb = first + local % gm;
+    nb = local / gm;
+}
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float a, float b) {
+    const __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
+    return *reinterpret_cast<const uint32_t *>(&h);
+}
+
+// ------------------------------------------------------------------ kernel
+
+__global__ void __launch_bounds__(NUM_THREADS, 1)
+gemm_fp8_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CUtensorMap tmap_b,
+                const GemmParams p, const uint32_t idesc) {
+    extern __shared__ uint8_t smem_raw[];
+    uint32_t base = smem_u32(smem_raw);
+    const uint32_t pad = (1024u - (base & 1023u)) & 1023u;
+    uint8_t *smem = smem_raw + pad;
+    base += pad;
+
+    const uint32_t bar0 = base + BAR_OFFSET;
+    auto full_bar = [&](int s) { return bar0 + 8u * s; };
+    auto empty_bar = [&](int s) { return bar0 + 8u * (STAGES + s); };
+    auto tfull_bar = [&](int a) { return bar0 + 8u * (2 * STAGES + a); };
+    auto tempty_bar = [&](int a) { return bar0 + 8u * (2 * STAGES + 2 + a); };
+    const uint32_t drain_bar = bar0 + 8u * (2 * STAGES + 4);
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + SLOT_OFFSET);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + FLAG_OFFSET);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < STAGES; ++s) {
+            mbar_init(full_bar(s), 1);
+            mbar_init(empty_bar(s), 1);
+        }
+        for (int a = 0; a < 2; ++a) {
+            mbar_init(tfull_bar(a), 1);
+            mbar_init(tempty_bar(a), NUM_EPI_WARPS);
+        }
+        mbar_init(drain_bar, 1);
+        *abort_flag = 0;
+        fence_mbar_init();
+        prefetch_tmap(&tmap_a);
+        prefetch_tmap(&tmap_b);
+    }
+    if (warp == 1) {
+        tmem_alloc(smem_u32(tmem_slot), TMEM_COLS);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = *tmem_slot;
+
+    const int num_tiles = p.tiles_m * p.tiles_n;
+
+    if (warp == 0) {
+        if (lane == 0) {
+            // ---------------- TMA producer
+            uint32_t it = 0;
+            int issued_stages = 0;  // stages that have received at least one load
+            bool ok = true;
+            for (int tile = blockIdx.x; ok && tile < num_tiles; tile += gridDim.x) {
+                int mb, nb;
+                tile_coords(tile, p.tiles_m, p.tiles_n, mb, nb);
+                for (int kb = 0; kb < p.num_kb; ++kb, ++it) {
+                    const int s = static_cast<int>(it % STAGES);
+                    const uint32_t ph = (it / STAGES) & 1u;
+                    if (!wait_bounded(empty_bar(s), ph ^ 1u, abort_flag)) {
+                        ok = false;
+                        break;
+                    }
+                    const uint32_t sa = base + s * STAGE_BYTES;
+                    mbar_arrive_expect_tx(full_bar(s), STAGE_BYTES);
+                    tma_load_2d(sa, &tmap_a, full_bar(s), kb * BK, mb * BM);
+                    tma_load_2d(sa + A_BYTES, &tmap_b, full_bar(s), kb * BK, nb * BN);
+                    if (issued_stages < STAGES) ++issued_stages;
+                }
+            }
+            if (!ok) {
+                // let the loads already issued land before the CTA goes away
+                for (int j = 1; j <= issued_stages && j <= static_cast<int>(it); ++j) {
+                    const uint32_t last = it - static_cast<uint32_t>(j);
+                    volatile int never = 0;
+                    wait_bounded(full_bar(static_cast<int>(last % STAGES)), (last / STAGES) & 1u, &never);
+                }
+            }
+        }
+    } else if (warp == 1) {
+        if (lane == 0) {
+            // ---------------- MMA issuer
+            uint32_t it = 0;
+            int lt = 0;
+            bool ok = true;
+            for (int tile = blockIdx.x; ok && tile < num_tiles; tile += gridDim.x, ++lt) {
+                const int acc = lt & 1;
+                const uint32_t aph = (static_cast<uint32_t>(lt) >> 1) & 1u;
+                if (!wait_bounded(tempty_bar(acc), aph ^ 1u, abort_flag)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * BN);
+                for (int kb = 0; kb < p.num_kb; ++kb, ++it) {
+                    const int s = static_cast<int>(it % STAGES);
+                    const uint32_t ph = (it / STAGES) & 1u;
+                    if (!wait_bounded(full_bar(s), ph, abort_flag)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t sa = base + s * STAGE_BYTES;
+#pragma unroll
+                    for (int k = 0; k < BK / UMMA_K; ++k) {
+                        umma_f8f6f4(d_tmem, sw128_kmajor_desc(sa + k * UMMA_K),
+                                    sw128_kmajor_desc(sa + A_BYTES + k * UMMA_K), idesc,
+                                    (kb > 0 || k > 0) ? 1u : 0u);
+                    }
+                    umma_commit(empty_bar(s));
+                }
+                if (!ok) break;
+                umma_commit(tfull_bar(acc));
+            }
+            if (!ok) {
+                // wait for the MMAs in flight before TMEM is released
+                umma_commit(drain_bar);
+                volatile int never = 0;
+                wait_bounded(drain_bar, 0u, &never);
+            }
+        }
+    } else {
+        // ---------------- epilogue warps
+        const int q = warp & 3;  // this warp may access TMEM lanes 32q .. 32q+31
+        const int row_in_tile = q * 32 + lane;
+        const float scale = __fmul_rn(__ldg(p.sinv_a), __ldg(p.sinv_b));
+        float am = 0.0f;
+        int lt = 0;
+        for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x, ++lt) {
+            const int acc = lt & 1;
+            const uint32_t aph = (static_cast<uint32_t>(lt) >> 1) & 1u;
+            int ok = 1;
+            if (lane == 0) ok = wait_bounded(tfull_bar(acc), aph, abort_flag) ? 1 : 0;
+            ok = __shfl_sync(0xffffffffu, ok, 0);
+            if (!ok) break;
+            tc_fence_after();
+            int mb, nb;
+            tile_coords(tile, p.tiles_m, p.tiles_n, mb, nb);
+            const int64_t m = static_cast<int64_t>(mb) * BM + row_in_tile;
+            const bool row_ok = m < p.rows_a;
+#pragma unroll 1
+            for (int c = 0; c < BN; c += 32) {
+                uint32_t r[32];
+                tmem_ld32(tmem_base + static_cast<uint32_t>(acc * BN + c) + (static_cast<uint32_t>(q * 32) << 16),
+                          r);
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    const int n = nb * BN + c + 16 * h;
+                    if (!row_ok || n >= p.rows_b) continue;
+                    float y[16];
+                    if (p.bias == nullptr) {
+#pragma unroll
+                        for (int j = 0; j < 16; ++j) y[j] = __fmul_rn(__uint_as_float(r[16 * h + j]), scale);
+                    } else if (p.bias_bf16) {
+                        const uint4 *bp = reinterpret_cast<const uint4 *>(static_cast<const uint16_t *>(p.bias) + n);
+                        const uint4 b0 = __ldg(bp), b1 = __ldg(bp + 1);
+                        const uint32_t bw[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
+#pragma unroll
+                        for (int j = 0; j < 8; ++j) {
+                            y[2 * j] = __fmaf_rn(__uint_as_float(r[16 * h + 2 * j]), scale, __uint_as_float(bw[j] << 16));
+                            y[2 * j + 1] = __fmaf_rn(__uint_as_float(r[16 * h + 2 * j + 1]), scale,
+                                                     __uint_as_float(bw[j] & 0xFFFF0000u));
+                        }
+                    } else {
+                        const float4 *bp = reinterpret_cast<const float4 *>(static_cast<const float *>(p.bias) + n);
+#pragma unroll
+                        for (int j = 0; j < 4; ++j) {
+                            const float4 b = __ldg(bp + j);
+                            y[4 * j] = __fmaf_rn(__uint_as_float(r[16 * h + 4 * j]), scale, b.x);
+                            y[4 * j + 1] = __fmaf_rn(__uint_as_float(r[16 * h + 4 * j + 1]), scale, b.y);
+                            y[4 * j + 2] = __fmaf_rn(__uint_as_float(r[16 * h + 4 * j + 2]), scale, b.z);
+                            y[4 * j + 3] = __fmaf_rn(__uint_as_float(r[16 * h + 4 * j + 3]), scale, b.w);
+                        }
+                    }
+#pragma unroll
+                    for (int j = 0; j < 16; ++j) am = max_ignore_nan(am, fabsf(y[j]));
+                    if (p.out_bf16) {
+                        uint4 *dst = reinterpret_cast<uint4 *>(static_cast<uint16_t *>(p.out) + m * p.rows_b + n);
+                        dst[0] = make_uint4(pack_bf16x2(y[0], y[1]), pack_bf16x2(y[2], y[3]), pack_bf16x2(y[4], y[5]),
+                                            pack_bf16x2(y[6], y[7]));
+                        dst[1] = make_uint4(pack_bf16x2(y[8], y[9]), pack_bf16x2(y[10], y[11]),
+                                            pack_bf16x2(y[12], y[13]), pack_bf16x2(y[14], y[15]));
+                    } else {
+                        float4 *dst = reinterpret_cast<float4 *>(static_cast<float *>(p.out) + m * p.rows_b + n);
+#pragma unroll
+                        for (int j = 0; j < 4; ++j)
+                            dst[j] = make_float4(y[4 * j], y[4 * j + 1], y[4 * j + 2], y[4 * j + 3]);
+                    }
+                }
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(tempty_bar(acc));
+        }
+        if (p.out_amax != nullptr) {
+            am = warp_max(am);
+            if (p.out_bf16) am = __bfloat162float(__float2bfloat16_rn(am));  // max of the stored values
+            if (lane == 0) atomicMax(reinterpret_cast<int *>(p.out_amax), __float_as_int(am));
+        }
+    }
+
+    __syncwarp();
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 1) tmem_dealloc(tmem_base, TMEM_COLS);
+}
+
+// out = bias (or 0) broadcast over rows: the GEMM of an empty contraction.
+__global__ void fill_bias_kernel(int64_t rows, int64_t cols, const void *bias, int bias_bf16, void *out,
+                                 int out_bf16, float *out_amax) {
+    float am = 0.0f;
+    const int64_t n = rows * cols;
+    for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n;
+         i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+        const int64_t j = i % cols;
+        float y = 0.0f;
+        if (bias != nullptr)
+            y = bias_bf16 ? bf16_bits_to_f32(static_cast<const uint16_t *>(bias)[j]) : static_cast<const float *>(bias)[j];
+        if (out_bf16) {
+            const __nv_bfloat16 h = __float2bfloat16_rn(y);
+            static_cast<__nv_bfloat16 *>(out)[i] = h;
+            y = __bfloat162float(h);
+        } else {
+            static_cast<float *>(out)[i] = y;
+        }
+        am = max_ignore_nan(am, fabsf(y));
+    }
+    block_amax_atomic(am, out_amax);
+}
+
+// ------------------------------------------------------------- host side
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *ptr = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+    });
+    return fn;
+}
+
+// 2-D byte tensor [outer x inner], inner contiguous; box box_outer x 128 bytes.
+int make_tmap(CUtensorMap *map, const void *ptr, uint64_t inner, uint64_t outer, uint32_t box_outer) {
+    auto enc = encode_fn();
+    if (enc == nullptr) return fail(FP8MP_ERR_LAUNCH, "cuTensorMapEncodeTiled is not available");
+    const cuuint64_t dims[2] = {inner, outer};
+    const cuuint64_t strides[1] = {inner};
+    const cuuint32_t box[2] = {static_cast<cuuint32_t>(BK), box_outer};
+    const cuuint32_t estr[2] = {1, 1};
+    const CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void *>(ptr), dims, strides, box, estr,
+                           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                           CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return fail(FP8MP_ERR_LAUNCH, "cuTensorMapEncodeTiled failed (%d)", static_cast<int>(r));
+    return FP8MP_OK;
+}
+
+constexpr uint32_t make_idesc(int fmt_a, int fmt_b) {
+    return (1u << 4)                                    // accumulator: f32
+           | (static_cast<uint32_t>(fmt_a) << 7)        // A: 0 = E4M3, 1 = E5M2
+           | (static_cast<uint32_t>(fmt_b) << 10)       // B: 0 = E4M3, 1 = E5M2
+           | (0u << 15) | (0u << 16)                    // A and B K-major
+           | (static_cast<uint32_t>(BN >> 3) << 17)     // N / 8
+           | (static_cast<uint32_t>(BM >> 4) << 24);    // M / 16
+}
+
+}  // namespace
+
+int launch_gemm(const uint8_t *a, int fmt_a, const uint8_t *b, int fmt_b, int64_t rows_a, int64_t rows_b,
+                int64_t kc, const float *sinv_a, const float *sinv_b, const void *bias, int bias_dtype, void *out,
+                int out_dtype, float *out_amax, cudaStream_t s, const DeviceInfo &dev) {
+    if (rows_a == 0 || rows_b == 0) return FP8MP_OK;
+    if (rows_a > (1ll << 30) || rows_b > (1ll << 30) || kc > (1ll << 30))
+        return fail(FP8MP_ERR_INVALID, "GEMM dimension above 2^30");
+    if (kc == 0) {
+        int64_t blocks = (rows_a * rows_b + 255) / 256;
+        if (blocks > dev.num_sms * 8) blocks = dev.num_sms * 8;
+        fill_bias_kernel<<<static_cast<unsigned>(blocks), 256, 0, s>>>(rows_a, rows_b, bias, bias_dtype == FP8MP_BF16,
+                                                                      out, out_dtype == FP8MP_BF16, out_amax);
+        const cudaError_t e = cudaGetLastError();
+        if (e != cudaSuccess) return fail(FP8MP_ERR_LAUNCH, "GEMM fill launch failed: %s", cudaGetErrorString(e));
+        return FP8MP_OK;
+    }
+    CUtensorMap ta, tb;
+    int rc = make_tmap(&ta, a, static_cast<uint64_t>(kc), static_cast<uint64_t>(rows_a), BM);
+    if (rc) return rc;
+    rc = make_tmap(&tb, b, static_cast<uint64_t>(kc), static_cast<uint64_t>(rows_b), BN);
+    if (rc) return rc;
+
+    GemmParams p;
+    p.rows_a = static_cast<int>(rows_a);
+    p.rows_b = static_cast<int>(rows_b);
+    p.num_kb = static_cast<int>((kc + BK - 1) / BK);
+    p.tiles_m = static_cast<int>((rows_a + BM - 1) / BM);
+    p.tiles_n = static_cast<int>((rows_b + BN - 1) / BN);
+    p.sinv_a = sinv_a;
+    p.sinv_b = sinv_b;
+    p.bias = bias;
+    p.bias_bf16 = bias_dtype == FP8MP_BF16;
+    p.out = out;
+    p.out_bf16 = out_dtype == FP8MP_BF16;
+    p.out_amax = out_amax;
+    const int64_t num_tiles = static_cast<int64_t>(p.tiles_m) * p.tiles_n;
+    if (num_tiles > 0x7FFFFFFF) return fail(FP8MP_ERR_INVALID, "GEMM has too many tiles");
+    const int grid = static_cast<int>(num_tiles < dev.num_sms ? num_tiles : dev.num_sms);
+
+    static int attr_done[64] = {0};
+    if (dev.device >= 0 && dev.device < 64 && !attr_done[dev.device]) {
+        const cudaError_t e =
+            cudaFuncSetAttribute(gemm_fp8_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_ALLOC);
+        if (e != cudaSuccess)
+            return fail(FP8MP_ERR_LAUNCH, "GEMM smem attribute failed: %s", cudaGetErrorString(e));
+        attr_done[dev.device] = 1;
+    }
+    gemm_fp8_kernel<<<grid, NUM_THREADS, SMEM_ALLOC, s>>>(ta, tb, p, make_idesc(fmt_a, fmt_b));
+    const cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return fail(FP8MP_ERR_LAUNCH, "GEMM launch failed: %s", cudaGetErrorString(e));
+    return FP8MP_OK;
+}
+
+int read_and_clear_timeout_flag(unsigned int *value) {
+    unsigned int v = 0, zero = 0;
+    cudaError_t e = cudaMemcpyFromSymbol(&v, g_gemm_timeout_flag, sizeof v);
+    if (e == cudaSuccess) e = cudaMemcpyToSymbol(g_gemm_timeout_flag, &zero, sizeof zero);
+    if (e != cudaSuccess) return fail(FP8MP_ERR_LAUNCH, "reading the timeout flag failed: %s", cudaGetErrorString(e));
+    *value = v;
+    return FP8MP_OK;
+}
+
+}  // namespace fp8mp

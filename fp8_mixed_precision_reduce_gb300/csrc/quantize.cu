@@ -1,0 +1,218 @@
+// quantize.cu -- scaled, saturating round-to-nearest-even cast of bf16/fp32
+// tensors to E4M3/E5M2 with the fused per-tensor amax, and the variant that
+// also writes the transposed copy the backward GEMMs consume.
+//
+// Pages: "Как работает FP8 quantization на H100 (Transformer Engine)?"
+// (aivaro.ru) section 3, steps 2-3 -- the amax of the tensor and the cast of
+// the scaled tensor; "Transformer Engine으로 FP8 사용하기" (coniverse.tistory.com)
+// "Scaling factor 선택 전략" -- the per-tensor amax delayed scaling records.
+//
+// Both kernels are HBM-bound streams (algorithmic bytes per element: input
+// 2 or 4, output 1, transposed output 1). Loads and stores are 16 bytes wide
+// and coalesced; the amax is a per-thread max, a warp-shuffle max and one
+// atomic max per block.
+#include "fp8mp_internal.cuh"
+
+namespace fp8mp {
+namespace {
+
+constexpr int kThreads = 256;
+
+// 16 consecutive input elements starting at element 16*chunk, widened to fp32.
+template <bool BF16>
+__device__ __forceinline__ void load16(const void *x, int64_t chunk, float f[16]) {
+    if constexpr (BF16) {
+        const uint4 *p = reinterpret_cast<const uint4 *>(x) + 2 * chunk;
+        const uint4 a = __ldcs(p), b = __ldcs(p + 1);
+        const uint32_t w[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            f[2 * i] = __uint_as_float(w[i] << 16);
+            f[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
+        }
+    } else {
+        const float4 *p = reinterpret_cast<const float4 *>(x) + 4 * chunk;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const float4 v = __ldcs(p + i);
+            f[4 * i] = v.x;
+            f[4 * i + 1] = v.y;
+            f[4 * i + 2] = v.z;
+            f[4 * i + 3] = v.w;
+        }
+    }
+}
+
+// 8 consecutive elements of row `r` starting at column `c`.
+template <bool BF16>
+__device__ __forceinline__ void load8(const void *x, int64_t cols, int64_t r, int64_t c, float f[8]) {
+    const int64_t e = r * cols + c;
+    if constexpr (BF16) {
+        const uint4 a = __ldcs(reinterpret_cast<const uint4 *>(reinterpret_cast<const uint16_t *>(x) + e));
+        const uint32_t w[4] = {a.x, a.y, a.z, a.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            f[2 * i] = __uint_as_float(w[i] << 16);
+            f[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
+        }
+    } else {
+        const float4 *p = reinterpret_cast<const float4 *>(reinterpret_cast<const float *>(x) + e);
+        const float4 a = __ldcs(p), b = __ldcs(p + 1);
+        f[0] = a.x; f[1] = a.y; f[2] = a.z; f[3] = a.w;
+        f[4] = b.x; f[5] = b.y; f[6] = b.z; f[7] = b.w;
+    }
+}
+
+template <bool BF16>
+__device__ __forceinline__ float load1(const void *x, int64_t i) {
+    if constexpr (BF16)
+        return bf16_bits_to_f32(reinterpret_cast<const uint16_t *>(x)[i]);
+    else
+        return reinterpret_cast<const float *>(x)[i];
+}
+
+// Row-major cast of a flat array of n elements: chunks of 16 elements give
+// one 16-byte store; the n % 16 tail is done element by element.
+template <int FMT, bool BF16>
+__global__ void __launch_bounds__(kThreads)
+cast_rows_kernel(const void *__restrict__ x, int64_t n, const float *__restrict__ scale_p,
+                 uint8_t *__restrict__ out, float *__restrict__ amax_p) {
+    const float scale = __ldg(scale_p);
+    float am = 0.0f;
+    const int64_t nchunk = n >> 4;
+    const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+    for (int64_t c = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; c < nchunk; c += stride) {
+        float f[16];
+        load16<BF16>(x, c, f);
+        uint32_t o[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            o[j] = cvt_quad<FMT>(__fmul_rn(f[4 * j], scale), __fmul_rn(f[4 * j + 1], scale),
+                                 __fmul_rn(f[4 * j + 2], scale), __fmul_rn(f[4 * j + 3], scale));
+        }
+#pragma unroll
+        for (int j = 0; j < 16; ++j) am = max_ignore_nan(am, fabsf(f[j]));
+        reinterpret_cast<uint4 *>(out)[c] = make_uint4(o[0], o[1], o[2], o[3]);
+    }
+    if (blockIdx.x == gridDim.x - 1) {
+        for (int64_t i = (nchunk << 4) + threadIdx.x; i < n; i += blockDim.x) {
+            const float v = load1<BF16>(x, i);
+            out[i] = static_cast<uint8_t>(cvt_pair<FMT>(__fmul_rn(v, scale), 0.0f) & 0xFFu);
+            am = max_ignore_nan(am, fabsf(v));
+        }
+    }
+    if (amax_p != nullptr) block_amax_atomic(am, amax_p);
+}
+
+// Row-major + transposed cast of one 128 x 128 tile per block.
+// Phase 1: each thread converts a 4-row x 8-column patch (16-byte loads),
+// stores its row-major bytes, transposes the 4 x 8 bytes in registers into
+// eight 4-byte column words and parks them in shared memory, where word
+// (column cc, row-group g) sits at index cc * 32 + (g ^ 2 * ((cc >> 3) & 15))
+// -- the XOR spreads one store instruction of a warp over all 32 banks.
+// Phase 2: each thread reads 16 consecutive row bytes of one column (one
+// 16-byte shared load, un-permuting the XOR) and writes them to out_t, so a
+// warp writes four full 128-byte rows of out_t.
+template <int FMT, bool BF16>
+__global__ void __launch_bounds__(kThreads)
+cast_rows_t_kernel(const void *__restrict__ x, int64_t rows, int64_t cols, const float *__restrict__ scale_p,
+                   uint8_t *__restrict__ out, uint8_t *__restrict__ out_t, float *__restrict__ amax_p) {
+    __shared__ __align__(16) uint32_t sT[128 * 32];
+    const int64_t tiles_c = (cols + 127) >> 7;
+    const int64_t r0 = (blockIdx.x / tiles_c) * 128, c0 = (blockIdx.x % tiles_c) * 128;
+    const int tx = threadIdx.x & 15, ty = threadIdx.x >> 4;
+    const float scale = __ldg(scale_p);
+    float am = 0.0f;
+    const int64_t c = c0 + 8 * tx;
+    const int sw1 = 2 * tx;
+#pragma unroll
+    for (int it = 0; it < 2; ++it) {
+        const int g = ty + 16 * it;  // 4-row group within the tile
+        const int64_t r = r0 + 4 * g;
+        if (c < cols && r < rows) {
+            uint32_t lo[4], hi[4];
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                float f[8];
+                load8<BF16>(x, cols, r + q, c, f);
+                lo[q] = cvt_quad<FMT>(__fmul_rn(f[0], scale), __fmul_rn(f[1], scale),
+                                      __fmul_rn(f[2], scale), __fmul_rn(f[3], scale));
+                hi[q] = cvt_quad<FMT>(__fmul_rn(f[4], scale), __fmul_rn(f[5], scale),
+                                      __fmul_rn(f[6], scale), __fmul_rn(f[7], scale));
+#pragma unroll
+                for (int j = 0; j < 8; ++j) am = max_ignore_nan(am, fabsf(f[j]));
+                *reinterpret_cast<uint2 *>(out + (r + q) * cols + c) = make_uint2(lo[q], hi[q]);
+            }
+            // 4 x 4 byte transposes: word j holds column (c + j), rows r .. r+3.
+            uint32_t wcol[8];
+            {
+                const uint32_t t0 = __byte_perm(lo[0], lo[1], 0x5140), t1 = __byte_perm(lo[0], lo[1], 0x7362);
+                const uint32_t t2 = __byte_perm(lo[2], lo[3], 0x5140), t3 = __byte_perm(lo[2], lo[3], 0x7362);
+                wcol[0] = __byte_perm(t0, t2, 0x5410);
+                wcol[1] = __byte_perm(t0, t2, 0x7632);
+                wcol[2] = __byte_perm(t1, t3, 0x5410);
+                wcol[3] = __byte_perm(t1, t3, 0x7632);
+            }
+            {
+                const uint32_t t0 = __byte_perm(hi[0], hi[1], 0x5140), t1 = __byte_perm(hi[0], hi[1], 0x7362);
+                const uint32_t t2 = __byte_perm(hi[2], hi[3], 0x5140), t3 = __byte_perm(hi[2], hi[3], 0x7362);
+                wcol[4] = __byte_perm(t0, t2, 0x5410);
+                wcol[5] = __byte_perm(t0, t2, 0x7632);
+                wcol[6] = __byte_perm(t1, t3, 0x5410);
+                wcol[7] = __byte_perm(t1, t3, 0x7632);
+            }
+#pragma unroll
+            for (int j = 0; j < 8; ++j) sT[(8 * tx + j) * 32 + (g ^ sw1)] = wcol[j];
+        }
+    }
+    __syncthreads();
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const int id = threadIdx.x + kThreads * i;  // 0 .. 1023
+        const int cc = id >> 3, k = id & 7;          // tile column, 16-row chunk
+        const int64_t col = c0 + cc, row = r0 + 16 * k;
+        if (col < cols && row < rows) {
+            const int sw = 2 * ((cc >> 3) & 15);
+            const uint4 P = *reinterpret_cast<const uint4 *>(&sT[cc * 32 + ((4 * k) ^ (sw & ~3))]);
+            const uint4 o = (sw & 2) ? make_uint4(P.z, P.w, P.x, P.y) : P;
+            *reinterpret_cast<uint4 *>(out_t + col * rows + row) = o;
+        }
+    }
+    if (amax_p != nullptr) block_amax_atomic(am, amax_p);
+}
+
+template <int FMT, bool BF16>
+int launch_typed(const void *x, int64_t rows, int64_t cols, const float *scale, uint8_t *out,
+                 uint8_t *out_t, float *amax, cudaStream_t s, const DeviceInfo &dev) {
+    if (out_t == nullptr) {
+        const int64_t n = rows * cols;
+        const int64_t nchunk = n >> 4;
+        int64_t blocks = (nchunk + kThreads - 1) / kThreads;
+        const int64_t cap = static_cast<int64_t>(dev.num_sms) * 8;
+        if (blocks > cap) blocks = cap;
+        if (blocks < 1) blocks = 1;
+        cast_rows_kernel<FMT, BF16><<<static_cast<unsigned>(blocks), kThreads, 0, s>>>(x, n, scale, out, amax);
+    } else {
+        const int64_t tiles = ((rows + 127) >> 7) * ((cols + 127) >> 7);
+        if (tiles > 0x7FFFFFFF) return fail(FP8MP_ERR_INVALID, "fp8_quantize: tensor too large");
+        cast_rows_t_kernel<FMT, BF16><<<static_cast<unsigned>(tiles), kThreads, 0, s>>>(x, rows, cols, scale, out,
+                                                                                       out_t, amax);
+    }
+    const cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return fail(FP8MP_ERR_LAUNCH, "fp8_quantize: launch failed: %s", cudaGetErrorString(e));
+    return FP8MP_OK;
+}
+
+}  // namespace
+
+int launch_quantize(const void *x, int x_dtype, int64_t rows, int64_t cols, int fmt, const float *scale,
+                    uint8_t *out, uint8_t *out_t, float *amax, cudaStream_t s, const DeviceInfo &dev) {
+    const bool bf16 = x_dtype == FP8MP_BF16;
+    if (fmt == FP8MP_E4M3)
+        return bf16 ? launch_typed<FP8MP_E4M3, true>(x, rows, cols, scale, out, out_t, amax, s, dev)
+                    : launch_typed<FP8MP_E4M3, false>(x, rows, cols, scale, out, out_t, amax, s, dev);
+    return bf16 ? launch_typed<FP8MP_E5M2, true>(x, rows, cols, scale, out, out_t, amax, s, dev)
+                : launch_typed<FP8MP_E5M2, false>(x, rows, cols, scale, out, out_t, amax, s, dev);
+}
+
+}  // namespace fp8mp

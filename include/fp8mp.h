@@ -1,0 +1,230 @@
+/*
+ * fp8mp.h -- C ABI of libfp8mp, the GB300 (sm_103a) hot path of an FP8
+ * delayed-scaling linear layer used in mixed-precision training.
+ *
+ * Pages this interface follows (title -- site):
+ *   [TE-FP8]  "Transformer Engine으로 FP8 사용하기" -- coniverse.tistory.com
+ *   [MP]      "LLM) Mixed-Precision 개념 및 학습 방법 알아보기"
+ *             -- data-newbie.tistory.com
+ *   [PT-FP8]  "Các kiểu dữ liệu FP8 gốc của PyTorch ..." (PyTorch native FP8
+ *             data types) -- hotroai.com
+ *   [H100-Q]  "Как работает FP8 quantization на H100 (Transformer Engine)?"
+ *             -- aivaro.ru
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ * Layout. Every matrix is row-major and dense (leading dimension = number of
+ *   columns). M = tokens, K = in_features, N = out_features; the weight W is
+ *   N x K, as a linear layer stores it.
+ * Pointers. Every tensor argument is a DEVICE pointer of the current CUDA
+ *   device, owned by the caller, which must keep it alive until the work on
+ *   `stream` has finished. The library allocates no device memory and keeps
+ *   no pointer after a call returns. Tensor pointers must be 16-byte aligned.
+ * Stream. `stream` is a cudaStream_t passed as void* (NULL = the legacy
+ *   default stream). Every call only enqueues work on it and returns; no call
+ *   synchronises with the host, and no data-dependent decision (the overflow
+ *   skip of mp_master_step, the scale update) leaves the device.
+ * Aliasing. Inputs are read-only; outputs must not overlap inputs, except
+ *   the in-place state of mp_master_step and delayed_scaling_update.
+ * Return value. 0 on success, otherwise a negative code:
+ *   FP8MP_ERR_INVALID (-1): a required pointer is NULL or not 16-byte
+ *     aligned, a size is negative or too large, an enum is out of range, or
+ *     a GEMM dimension is not a multiple of 16 ([TE-FP8] "주의!" restricts
+ *     FP8 linears to shapes whose dimensions divide by 16). Nothing was
+ *     enqueued.
+ *   FP8MP_ERR_DEVICE (-2): the current device is not an sm_103 GPU.
+ *   FP8MP_ERR_LAUNCH (-3): a CUDA call or kernel launch failed.
+ *   FP8MP_ERR_TIMEOUT (-4): returned by fp8mp_check(): a bounded wait inside
+ *     a GEMM kernel ran out (a wedged pipeline); that kernel's output is
+ *     undefined, the CUDA context stays usable.
+ *   fp8mp_last_error() then describes the failure (thread-local).
+ */
+#ifndef FP8MP_H
+#define FP8MP_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* FP8 formats ([TE-FP8] "Introduction to FP8"; [PT-FP8] finfo table).
+ * E4M3: largest finite 448, no infinities; E5M2: largest finite 57344. */
+typedef enum { FP8MP_E4M3 = 0, FP8MP_E5M2 = 1 } fp8mp_fmt;
+
+/* High-precision element types of inputs and outputs. */
+typedef enum { FP8MP_F32 = 0, FP8MP_BF16 = 1 } fp8mp_dtype;
+
+/* amax_compute_algo of the DelayedScaling recipe ([TE-FP8] "FP8
+ * 사용방안(recipe)"): the largest amax of the history, or the newest one. */
+typedef enum { FP8MP_AMAX_MAX = 0, FP8MP_AMAX_MOST_RECENT = 1 } fp8mp_algo;
+
+enum {
+    FP8MP_OK = 0,
+    FP8MP_ERR_INVALID = -1,
+    FP8MP_ERR_DEVICE = -2,
+    FP8MP_ERR_LAUNCH = -3,
+    FP8MP_ERR_TIMEOUT = -4
+};
+
+/* Largest history a meta may have (floats per tensor). */
+#define FP8MP_MAX_HISTORY 8192
+
+/*
+ * Per-tensor FP8 bookkeeping ([TE-FP8] "Scaling factor 선택 전략": each FP8
+ * tensor keeps its own factor and a record of past amaxes; [H100-Q]
+ * section 3). All four pointers are device pointers to fp32 values.
+ * Initial state expected by delayed_scaling_update: history all 0,
+ * scale = scale_inv = 1, cur_amax = 0.
+ */
+typedef struct fp8mp_meta {
+    float *amax_history; /* [history_len], newest amax at index 0 */
+    float *scale;        /* 1 value: multiplies the tensor before the cast */
+    float *scale_inv;    /* 1 value: 1 / scale, multiplies GEMM results */
+    float *cur_amax;     /* 1 value: amax of the current step; the casts and
+                            the forward GEMM raise it with an atomic max */
+    int32_t history_len; /* 1 .. FP8MP_MAX_HISTORY */
+    int32_t fmt;         /* fp8mp_fmt of the tensor this meta scales */
+} fp8mp_meta;
+
+/*
+ * fp8_quantize -- scaled, saturating round-to-nearest-even cast of a bf16 or
+ * fp32 matrix to FP8, with the tensor's amax and an optional transposed copy.
+ *
+ * Defines ([H100-Q] section 3, steps 2-3; [TE-FP8] "Scaling factor 선택 전략"):
+ *   out[r, c]   = sat_rne_fmt(fl32(x[r, c]) * scale[0])      (one fp32 multiply)
+ *   out_t[c, r] = out[r, c]                                  (when out_t != NULL)
+ *   *amax       = max(*amax, max_{r,c} |x[r, c]|)           (when amax != NULL)
+ * Saturation: finite values beyond the format and +-Inf become +-largest
+ * finite; NaN becomes 0x7F; subnormal FP8 results are kept (no flush).
+ * The amax is over the UNSCALED input, NaN elements ignored; it is merged
+ * into *amax with an atomic max, so *amax must hold a value >= +0 (the scale
+ * update leaves 0 there).
+ *
+ * x      [rows x cols] of x_dtype (FP8MP_F32 or FP8MP_BF16).
+ * scale  device pointer to one fp32 value (the tensor's meta->scale).
+ * out    [rows x cols] bytes, required.
+ * out_t  [cols x rows] bytes or NULL. When given, rows and cols must be
+ *        multiples of 16; without it any rows x cols is accepted.
+ * amax   device fp32 or NULL.
+ * rows == 0 or cols == 0 is a no-op returning 0.
+ */
+int fp8_quantize(const void *x, int32_t x_dtype, int64_t rows, int64_t cols, int32_t fmt,
+                 const float *scale, uint8_t *out, uint8_t *out_t, float *amax, void *stream);
+
+/*
+ * fp8_linear_fwd -- forward FP8 GEMM of a linear layer, E4M3 x E4M3.
+ *
+ * Defines ([PT-FP8] the torch._scaled_mm listing: two FP8 operands, their
+ * scales, an optional bias and the output amax; [MP] "Accumulation into
+ * FP32"; [H100-Q] section 3, step 4: the product is divided by the scales):
+ *   y[m, n] = (sum_k x8[m, k] * w8[n, k]) * sinv_x[0] * sinv_w[0] + bias[n]
+ * accumulated in fp32 on the tensor cores, rounded once to y_dtype.
+ *   *y_amax = max(*y_amax, max |y as stored|)                (when y_amax != NULL)
+ *
+ * x8  [M x K] E4M3 codes;  w8 [N x K] E4M3 codes (the weight, K contiguous).
+ * sinv_x, sinv_w  device pointers to one fp32 each (metas' scale_inv).
+ * bias  [N] of bias_dtype, or NULL.   y  [M x N] of y_dtype.
+ * M, N, K multiples of 16. M == 0 or N == 0: no-op. K == 0: y = bias (or 0).
+ */
+int fp8_linear_fwd(const uint8_t *x8, const uint8_t *w8, int64_t M, int64_t N, int64_t K,
+                   const float *sinv_x, const float *sinv_w, const void *bias, int32_t bias_dtype,
+                   void *y, int32_t y_dtype, float *y_amax, void *stream);
+
+/*
+ * fp8_linear_dgrad -- input gradient of the linear layer (HYBRID recipe:
+ * E5M2 gradient against the E4M3 weight; [TE-FP8] "Introduction to FP8" and
+ * "FP8 사용방안(recipe)", Format.HYBRID; "Backward Pass 처리").
+ *   dx[m, k] = (sum_n dy8[m, n] * w8t[k, n]) * sinv_dy[0] * sinv_w[0]
+ *
+ * dy8  [M x N] codes of dy_fmt (E5M2 under HYBRID, E4M3 allowed).
+ * w8t  [K x N] E4M3 codes: the transposed copy fp8_quantize writes to out_t
+ *      when casting the weight.
+ * dx   [M x K] of dx_dtype.  M, N, K multiples of 16; N == 0 gives dx = 0.
+ */
+int fp8_linear_dgrad(const uint8_t *dy8, const uint8_t *w8t, int64_t M, int64_t N, int64_t K,
+                     int32_t dy_fmt, const float *sinv_dy, const float *sinv_w, void *dx,
+                     int32_t dx_dtype, void *stream);
+
+/*
+ * fp8_linear_wgrad -- weight gradient of the linear layer (HYBRID recipe as
+ * above), contracting over the M tokens:
+ *   dw[n, k] = (sum_m dy8t[n, m] * x8t[k, m]) * sinv_dy[0] * sinv_x[0]
+ *
+ * dy8t [N x M] codes of dy_fmt: the transposed copy of the output gradient.
+ * x8t  [K x M] E4M3 codes: the transposed copy of the layer input.
+ * dw   [N x K] of dw_dtype.  M, N, K multiples of 16; M == 0 gives dw = 0.
+ */
+int fp8_linear_wgrad(const uint8_t *dy8t, const uint8_t *x8t, int64_t M, int64_t N, int64_t K,
+                     int32_t dy_fmt, const float *sinv_dy, const float *sinv_x, void *dw,
+                     int32_t dw_dtype, void *stream);
+
+/*
+ * delayed_scaling_update -- the DelayedScaling bookkeeping of one step for a
+ * batch of tensors ([TE-FP8] "Scaling factor 선택 전략", "FP8 사용방안(recipe)":
+ * amax_history_len, amax_compute_algo; [PT-FP8] amax and scale history
+ * synchronised once per step after backward; [H100-Q] section 3, step 2, and
+ * section 10). For each meta, in this order:
+ *   1. history[j] = history[j-1] for j = L-1 .. 1; history[0] = cur_amax;
+ *   2. a = max_j history[j] (FP8MP_AMAX_MAX) or history[0] (MOST_RECENT);
+ *   3. if a > 0 and finite: s = fl32(fmt_max / a) * 2^-margin; the scale
+ *      becomes s when s is finite and > 0, otherwise it keeps its value;
+ *   4. scale_inv = fl32(1 / scale); cur_amax = 0.
+ * fmt_max is 448 (E4M3) or 57344 (E5M2) after meta->fmt.
+ *
+ * metas   HOST array of n structs whose pointers are device pointers; read
+ *         during the call only (the values travel as kernel parameters).
+ * algo    fp8mp_algo.   margin  0 .. 126.   n == 0 is a no-op.
+ */
+int delayed_scaling_update(const fp8mp_meta *metas, int32_t n, int32_t algo, int32_t margin,
+                           void *stream);
+
+/*
+ * mp_master_step -- one mixed-precision optimizer step on a flat parameter
+ * buffer: loss unscale, overflow check with dynamic loss scaling, FP32
+ * master-weight SGD-momentum update and E4M3 re-cast ([MP] "FP32 Master Copy
+ * of Weights", "Mixed-Precision Training Iteration" steps 5-7, and the
+ * dynamic loss-scale procedure: skip the update and lower S when a gradient
+ * is Inf/NaN, raise S after a run of clean steps; [H100-Q] section 7).
+ *   found_inf = any grad is Inf or NaN                        (pass 1)
+ *   if found_inf: S = S * backoff; growth = 0; nothing else changes.
+ *   else, for every i (fp32; fmaf is one correctly rounded fused op):
+ *     u = fp32(grad[i]) * fl32(1 / S)
+ *     momentum[i] = fmaf(momentum_coef, momentum[i], u)
+ *     master[i]   = fmaf(-lr, momentum[i], master[i])
+ *     w8[i]       = sat_rne_E4M3(master[i] * scale_w[0])
+ *     *amax_w     = max(*amax_w, |master[i]|)
+ *   then growth += 1; if growth >= growth_interval: S = S * growth_factor,
+ *   growth = 0.
+ *
+ * grad_bf16 [n] bf16 bits (gradients of the loss multiplied by S).
+ * master, momentum [n] fp32 (in place);  w8 [n] E4M3 codes (written).
+ * scale_w   device fp32: the weight meta's scale (delayed: this step's).
+ * amax_w    device fp32: the weight meta's cur_amax (atomic max target).
+ * loss_scale device fp32 S;  growth_tracker device int32;  both in place.
+ * found_inf device int32 written with 0 or 1 (the step's overflow flag).
+ * growth_interval >= 1. n == 0 still counts a clean step.
+ */
+int mp_master_step(const uint16_t *grad_bf16, int64_t n, float *master, float *momentum,
+                   uint8_t *w8, const float *scale_w, float *amax_w, float *loss_scale,
+                   int32_t *growth_tracker, int32_t *found_inf, float lr, float momentum_coef,
+                   float backoff, float growth_factor, int32_t growth_interval, void *stream);
+
+/*
+ * fp8mp_check -- synchronises `stream`, then reports and clears the device
+ * flag a GEMM kernel sets when one of its bounded waits runs out:
+ * FP8MP_ERR_TIMEOUT if it was set, FP8MP_ERR_LAUNCH on a CUDA error, else 0.
+ */
+int fp8mp_check(void *stream);
+
+/* Thread-local description of the last nonzero return ("" if none). */
+const char *fp8mp_last_error(void);
+
+/* Interface version (incremented on any ABI change). */
+int32_t fp8mp_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FP8MP_H */

@@ -1,0 +1,156 @@
+"""GPU parity of the three FP8 GEMMs (fwd, dgrad, wgrad) against the oracle's
+fp64 reference, per element within |err| <= 2^-8 |ref| + 1e-5 sum|a b|, and
+of the forward GEMM's output amax (bit-exact against a host reduction of the
+stored output, within tolerance against the reference)."""
+
+import numpy as np
+import pytest
+import torch
+
+import workloads
+from gpu_util import E4M3, E5M2, dev, finite_codes, gemm_tolerance_check, np_view
+
+pytestmark = pytest.mark.gpu
+
+TORCH_DT = {"f32": torch.float32, "bf16": torch.bfloat16}
+
+
+def sc(v):
+    return torch.tensor([v], dtype=torch.float32, device="cuda")
+
+
+def fwd(fp8mp, A, B, sa, sb, bias=None, out="bf16", amax0=None):
+    M, N = A.shape[0], B.shape[0]
+    y = torch.empty((M, N), dtype=TORCH_DT[out], device="cuda")
+    am = torch.tensor([amax0], dtype=torch.float32, device="cuda") if amax0 is not None else None
+    fp8mp.fp8_linear_fwd(dev(A), dev(B), sc(sa), sc(sb), y, bias=bias, y_amax=am)
+    assert fp8mp.fp8mp_check() == 0
+    return y, am
+
+
+# (M, N, K): single tile, several tiles, ragged in every dimension, tiny,
+# the 768 layer, a long contraction
+SHAPES = [(128, 256, 128), (256, 512, 256), (1040, 784, 784), (16, 16, 16), (1024, 768, 768),
+          (128, 256, 16384), (384, 1280, 1152)]
+
+
+@pytest.mark.parametrize("M,N,K", SHAPES)
+@pytest.mark.parametrize("out", ["bf16", "f32"])
+def test_fwd_random_codes(cuda_lib, orc, M, N, K, out):
+    rng = np.random.default_rng(M * 31 + N * 7 + K)
+    A = finite_codes(rng, (M, K), E4M3)
+    B = finite_codes(rng, (N, K), E4M3)
+    sa, sb = 2.0 ** -6, 0.37
+    y, _ = fwd(cuda_lib, A, B, sa, sb, out=out)
+    ref, ab = orc.gemm_ref(A, E4M3, B, E4M3, float(np.float32(sa)), float(np.float32(sb)))
+    gemm_tolerance_check(np_view(y.float()).astype(np.float64), ref, ab, f"fwd {M}x{N}x{K}")
+
+
+@pytest.mark.parametrize("bias_dt", ["f32", "bf16"])
+@pytest.mark.parametrize("out", ["bf16", "f32"])
+def test_fwd_bias_and_output_amax(cuda_lib, orc, bias_dt, out):
+    M, N, K = 1040, 784, 512
+    rng = np.random.default_rng(5)
+    A = finite_codes(rng, (M, K), E4M3)
+    B = finite_codes(rng, (N, K), E4M3)
+    bias = (torch.randn(N, generator=workloads.gen(9)) * 50).to(TORCH_DT[bias_dt])
+    y, am = fwd(cuda_lib, A, B, 1e-3, 2e-3, bias=bias.cuda(), out=out, amax0=0.0)
+    ref, ab = orc.gemm_ref(A, E4M3, B, E4M3, float(np.float32(1e-3)), float(np.float32(2e-3)),
+                           bias=bias.double().numpy())
+    yh = np_view(y.float()).astype(np.float64)
+    gemm_tolerance_check(yh, ref, ab, "fwd+bias")
+    # amax: exactly the max |.| of what was stored, and close to the reference's
+    assert am.item() == np.abs(np_view(y.float())).max()
+    assert abs(am.item() - np.abs(ref).max()) <= 2.0 ** -8 * np.abs(ref).max() + 1e-5 * ab.max()
+
+
+@pytest.mark.parametrize("dy_fmt", [E5M2, E4M3])
+@pytest.mark.parametrize("M,N,K", [(256, 512, 256), (1040, 784, 784), (1024, 768, 768)])
+def test_dgrad_and_wgrad(cuda_lib, orc, dy_fmt, M, N, K):
+    rng = np.random.default_rng(M + 2 * N + 3 * K + dy_fmt)
+    dy8 = finite_codes(rng, (M, N), dy_fmt)
+    w8t = finite_codes(rng, (K, N), E4M3)
+    x8t = finite_codes(rng, (K, M), E4M3)
+    dy8t = np.ascontiguousarray(dy8.T)
+    s_dy, s_w, s_x = 2.0 ** -12, 0.5, 0.125
+    for out in ("bf16", "f32"):
+        dx = torch.empty((M, K), dtype=TORCH_DT[out], device="cuda")
+        cuda_lib.fp8_linear_dgrad(dev(dy8), dev(w8t), sc(s_dy), sc(s_w), dx, dy_fmt=dy_fmt)
+        dw = torch.empty((N, K), dtype=TORCH_DT[out], device="cuda")
+        cuda_lib.fp8_linear_wgrad(dev(dy8t), dev(x8t), sc(s_dy), sc(s_x), dw, dy_fmt=dy_fmt)
+        assert cuda_lib.fp8mp_check() == 0
+        ref, ab = orc.gemm_ref(dy8, dy_fmt, w8t, E4M3, s_dy, s_w)
+        gemm_tolerance_check(np_view(dx.float()).astype(np.float64), ref, ab, "dgrad")
+        ref, ab = orc.gemm_ref(dy8t, dy_fmt, x8t, E4M3, s_dy, s_x)
+        gemm_tolerance_check(np_view(dw.float()).astype(np.float64), ref, ab, "wgrad")
+
+
+def test_long_contraction_e5m2_wgrad(cuda_lib, orc):
+    """wgrad contracts over all tokens: 16384 here (the MLP workload's M)."""
+    N, K, M = 256, 384, 16384
+    rng = np.random.default_rng(77)
+    dy8t = finite_codes(rng, (N, M), E5M2)
+    x8t = finite_codes(rng, (K, M), E4M3)
+    dw = torch.empty((N, K), dtype=torch.float32, device="cuda")
+    cuda_lib.fp8_linear_wgrad(dev(dy8t), dev(x8t), sc(1.0), sc(1.0), dw, dy_fmt=E5M2)
+    assert cuda_lib.fp8mp_check() == 0
+    ref, ab = orc.gemm_ref(dy8t, E5M2, x8t, E4M3, 1.0, 1.0)
+    gemm_tolerance_check(np_view(dw).astype(np.float64), ref, ab, "wgrad K=16384")
+
+
+def test_empty_contraction_and_empty_output(cuda_lib):
+    bias = torch.arange(32, dtype=torch.float32, device="cuda")
+    y = torch.full((16, 32), 7.0, dtype=torch.float32, device="cuda")
+    am = torch.zeros(1, device="cuda")
+    e = torch.empty((16, 0), dtype=torch.uint8, device="cuda")
+    w = torch.empty((32, 0), dtype=torch.uint8, device="cuda")
+    cuda_lib.fp8_linear_fwd(e, w, sc(1.0), sc(1.0), y, bias=bias, y_amax=am)
+    assert cuda_lib.fp8mp_check() == 0
+    assert (y.cpu() == bias.cpu()[None, :]).all() and am.item() == 31.0
+    dw = torch.full((32, 48), 3.0, dtype=torch.bfloat16, device="cuda")
+    cuda_lib.fp8_linear_wgrad(torch.empty((32, 0), dtype=torch.uint8, device="cuda"),
+                              torch.empty((48, 0), dtype=torch.uint8, device="cuda"), sc(1.0), sc(1.0), dw)
+    assert cuda_lib.fp8mp_check() == 0
+    assert (dw.float().cpu() == 0).all()
+
+
+def test_metric_shape_full_size_sampled(cuda_lib, orc):
+    """M = 8192, N = K = 4096 (the proj linear of the transformer workload),
+    realistic codes cast by the oracle, every output of 40 sampled rows and of
+    one whole 128 x 256 tile checked, for fwd, dgrad and wgrad."""
+    tb = workloads.transformer_block(device="cuda")
+    M, K, N = 8192, 4096, 4096
+    xn, wn, dyn = np_view(tb.x), np_view(tb.w_proj), np_view(tb.dy_proj)
+    metas = {}
+    codes = {}
+    for name, arr, fmt in (("x", xn, E4M3), ("w", wn, E4M3), ("dy", dyn, E5M2)):
+        m = orc.Meta(1024)
+        m.record_amax(orc.amax(arr))
+        orc.scale_update(m, fmt, 1, 0)
+        metas[name] = m
+        codes[name] = orc.cast(arr, float(m.scale[0]), fmt)
+    sinv = {k: float(m.scale_inv[0]) for k, m in metas.items()}
+    rng = np.random.default_rng(8192)
+    rows = np.unique(np.concatenate([rng.integers(0, M, 40), np.arange(128 * 37, 128 * 38)])).astype(np.int64)
+
+    y, _ = fwd(cuda_lib, codes["x"], codes["w"], sinv["x"], sinv["w"], out="bf16")
+    ref, ab = orc.gemm_ref(codes["x"], E4M3, codes["w"], E4M3, sinv["x"], sinv["w"], rows=rows)
+    gemm_tolerance_check(np_view(y.float())[rows].astype(np.float64), ref, ab, "fwd 8192x4096x4096")
+    del y
+
+    w8t = orc.transpose_u8(codes["w"])
+    dx = torch.empty((M, K), dtype=torch.bfloat16, device="cuda")
+    cuda_lib.fp8_linear_dgrad(dev(codes["dy"]), dev(w8t), sc(sinv["dy"]), sc(sinv["w"]), dx)
+    assert cuda_lib.fp8mp_check() == 0
+    ref, ab = orc.gemm_ref(codes["dy"], E5M2, w8t, E4M3, sinv["dy"], sinv["w"], rows=rows)
+    gemm_tolerance_check(np_view(dx.float())[rows].astype(np.float64), ref, ab, "dgrad 8192x4096x4096")
+    del dx
+
+    dy8t = orc.transpose_u8(codes["dy"])
+    x8t = orc.transpose_u8(codes["x"])
+    dw = torch.empty((N, K), dtype=torch.bfloat16, device="cuda")
+    cuda_lib.fp8_linear_wgrad(dev(dy8t), dev(x8t), sc(sinv["dy"]), sc(sinv["x"]), dw)
+    assert cuda_lib.fp8mp_check() == 0
+    wrows = rows[rows < N]
+    ref, ab = orc.gemm_ref(dy8t, E5M2, x8t, E4M3, sinv["dy"], sinv["x"], rows=wrows)
+    gemm_tolerance_check(np_view(dw.float())[wrows].astype(np.float64), ref, ab, "wgrad 8192x4096x4096")

@@ -1,0 +1,130 @@
+"""The C-ABI library on the CPU host: it builds, loads, exports every entry
+point include/fp8mp.h declares, and its argument validation (which runs before
+any CUDA call) rejects bad input with FP8MP_ERR_INVALID. No compute calls."""
+
+import ctypes
+import os
+import re
+
+import pytest
+
+import fp8_mixed_precision_reduce_gb300 as fp8mp
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "fp8mp.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    fp8mp.build()
+    return fp8mp.load()
+
+
+def declared_functions():
+    src = open(HEADER).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    names = re.findall(r"^\s*(?:const\s+)?[a-z_0-9]+\s*\*?\s*([a-z_0-9]+)\s*\(", src, flags=re.M)
+    return sorted(set(n for n in names if n not in ("if", "while")))
+
+
+def test_header_declares_the_boundary():
+    names = declared_functions()
+    for n in ("fp8_quantize", "fp8_linear_fwd", "fp8_linear_dgrad", "fp8_linear_wgrad",
+              "delayed_scaling_update", "mp_master_step", "fp8mp_check", "fp8mp_last_error",
+              "fp8mp_version"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for n in declared_functions():
+        assert hasattr(lib, n), n
+    assert set(fp8mp.EXPORTS) <= set(declared_functions())
+
+
+def test_version_and_empty_error(lib):
+    assert fp8mp.fp8mp_version() == 1
+    assert fp8mp.last_error() == ""
+
+
+def test_ctypes_meta_layout_matches_header():
+    # four pointers then two int32: 40 bytes with 8-byte alignment
+    assert ctypes.sizeof(fp8mp.fp8mp_meta) == 40
+    assert fp8mp.fp8mp_meta.history_len.offset == 32
+
+
+def test_quantize_rejects_bad_arguments(lib):
+    P = 4096  # a fake, aligned address: never dereferenced, validation fails first
+    assert lib.fp8_quantize(P, 7, 16, 16, 0, P, P, None, None, None) == fp8mp.ERR_INVALID
+    assert "x_dtype" in fp8mp.last_error()
+    assert lib.fp8_quantize(P, 1, 16, 16, 5, P, P, None, None, None) == fp8mp.ERR_INVALID
+    assert lib.fp8_quantize(P, 1, -1, 16, 0, P, P, None, None, None) == fp8mp.ERR_INVALID
+    # a transposed output needs both dims divisible by 16
+    assert lib.fp8_quantize(P, 1, 24, 16, 0, P, P, P, None, None) == fp8mp.ERR_INVALID
+    assert "multiples of 16" in fp8mp.last_error()
+    # misaligned / missing pointers
+    assert lib.fp8_quantize(P + 2, 1, 16, 16, 0, P, P, None, None, None) == fp8mp.ERR_INVALID
+    assert "aligned" in fp8mp.last_error()
+    assert lib.fp8_quantize(None, 1, 16, 16, 0, P, P, None, None, None) == fp8mp.ERR_INVALID
+    assert lib.fp8_quantize(P, 1, 16, 16, 0, None, P, None, None, None) == fp8mp.ERR_INVALID
+    # an empty tensor is a no-op that needs no pointer and no device
+    assert lib.fp8_quantize(None, 1, 0, 16, 0, None, None, None, None, None) == fp8mp.OK
+
+
+def test_gemms_reject_bad_shapes(lib):
+    P = 4096
+    for fn in (lambda M, N, K: lib.fp8_linear_fwd(P, P, M, N, K, P, P, None, 0, P, 1, None, None),
+               lambda M, N, K: lib.fp8_linear_dgrad(P, P, M, N, K, 1, P, P, P, 1, None),
+               lambda M, N, K: lib.fp8_linear_wgrad(P, P, M, N, K, 1, P, P, P, 1, None)):
+        assert fn(24, 32, 32) == fp8mp.ERR_INVALID
+        assert fn(32, 40, 32) == fp8mp.ERR_INVALID
+        assert fn(32, 32, 8) == fp8mp.ERR_INVALID
+        assert fn(-16, 32, 32) == fp8mp.ERR_INVALID
+        assert fn(1 << 31, 32, 32) == fp8mp.ERR_INVALID
+    # empty outputs are no-ops
+    assert lib.fp8_linear_fwd(None, None, 0, 32, 32, None, None, None, 0, None, 1, None, None) == fp8mp.OK
+    assert lib.fp8_linear_dgrad(None, None, 32, 32, 0, 1, None, None, None, 1, None) == fp8mp.OK
+    assert lib.fp8_linear_wgrad(None, None, 32, 0, 32, 1, None, None, None, 1, None) == fp8mp.OK
+    # bad enums
+    assert lib.fp8_linear_fwd(P, P, 32, 32, 32, P, P, None, 0, P, 9, None, None) == fp8mp.ERR_INVALID
+    assert lib.fp8_linear_dgrad(P, P, 32, 32, 32, 3, P, P, P, 1, None) == fp8mp.ERR_INVALID
+
+
+def test_scale_update_rejects_bad_metas(lib):
+    P = 4096
+    good = fp8mp.fp8mp_meta(P, P, P, P, 16, 0)
+    arr = (fp8mp.fp8mp_meta * 1)(good)
+    assert lib.delayed_scaling_update(arr, 0, 0, 0, None) == fp8mp.OK
+    assert lib.delayed_scaling_update(arr, 1, 2, 0, None) == fp8mp.ERR_INVALID
+    assert lib.delayed_scaling_update(arr, 1, 0, -1, None) == fp8mp.ERR_INVALID
+    assert lib.delayed_scaling_update(arr, 1, 0, 127, None) == fp8mp.ERR_INVALID
+    for bad in (fp8mp.fp8mp_meta(P, P, P, P, 0, 0), fp8mp.fp8mp_meta(P, P, P, P, 8193, 0),
+                fp8mp.fp8mp_meta(P, P, P, P, 16, 2), fp8mp.fp8mp_meta(None, P, P, P, 16, 0)):
+        arr = (fp8mp.fp8mp_meta * 1)(bad)
+        assert lib.delayed_scaling_update(arr, 1, 0, 0, None) == fp8mp.ERR_INVALID
+
+
+def test_master_step_rejects_bad_arguments(lib):
+    P = 4096
+    args = [P, 1024, P, P, P, P, P, P, P, P, 1e-4, 0.9, 0.5, 2.0, 2000, None]
+    bad = list(args)
+    bad[14] = 0  # growth_interval
+    assert lib.mp_master_step(*bad) == fp8mp.ERR_INVALID
+    bad = list(args)
+    bad[2] = P + 8  # master misaligned
+    assert lib.mp_master_step(*bad) == fp8mp.ERR_INVALID
+    bad = list(args)
+    bad[7] = None  # loss_scale
+    assert lib.mp_master_step(*bad) == fp8mp.ERR_INVALID
+    bad = list(args)
+    bad[1] = -5
+    assert lib.mp_master_step(*bad) == fp8mp.ERR_INVALID
+
+
+def test_missing_library_fails_loudly(tmp_path):
+    with pytest.raises(fp8mp.Fp8mpError):
+        saved = fp8mp._lib
+        fp8mp._lib = None
+        try:
+            fp8mp.load(str(tmp_path / "nope.so"))
+        finally:
+            fp8mp._lib = saved
