@@ -462,9 +462,9 @@ def main(argv=None):
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
-    ap.add_argument("--cpu-tokens", type=int, default=96,
+    ap.add_argument("--cpu-tokens", type=int, default=256,
                     help="tokens of the oracle's bounded sample per step of --impl reference")
-    ap.add_argument("--baseline-tokens", type=int, default=1024,
+    ap.add_argument("--baseline-tokens", type=int, default=4096,
                     help="tokens of the oracle sample timed as cpu_baseline (about 10-30 s)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args(argv)
