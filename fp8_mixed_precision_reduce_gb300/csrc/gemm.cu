@@ -15,27 +15,39 @@
 // Computes out[i, j] = (sum_k A[i, k] * B[j, k]) * sinv_a * sinv_b + bias[j]
 // with A (rows_a x kc) and B (rows_b x kc) both contiguous along k.
 //
-// Design (one CTA per SM, persistent over 128 x 256 output tiles):
-//   warp 0, one lane  : TMA producer -- 128-byte-swizzled 128 x 128 B tiles of
-//                       A and 256 x 128 B tiles of B into a 4-stage ring of
-//                       shared-memory buffers, each guarded by a full/empty
-//                       mbarrier pair;
-//   warp 1, one lane  : MMA issuer -- 4 x tcgen05.mma.kind::f8f6f4
-//                       (M 128, N 256, K 32) per stage into a TMEM accumulator,
-//                       tcgen05.commit frees the stage; two accumulators
-//                       (2 x 256 of the 512 TMEM columns) let the next tile's
-//                       mainloop run while the previous tile drains;
+// Two tile engines share this file:
+//   PAIR = true  -- a cluster of two CTAs on the two SMs of a TPC computes a
+//                   256 x 256 tile with tcgen05.mma.cta_group::2 (M 256,
+//                   N 256, K 32): each CTA stages its own 128 rows of A and
+//                   its own 128 rows of B (32 KB per 128-byte k-block, a
+//                   6-stage ring); the even CTA issues the MMAs, which read
+//                   both CTAs' shared memory and write 128 TMEM lanes in each
+//                   CTA. Staging half of B per SM cuts the shared-memory
+//                   traffic per MMA by a third against a 128 x 256 tile.
+//   PAIR = false -- one CTA computes a 128 x 256 tile with
+//                   tcgen05.mma.cta_group::1 (4-stage, 48 KB ring); used when
+//                   a problem has too few 256 x 256 tiles to fill the GPU.
+// In both, one CTA per SM runs persistently over tiles:
+//   warp 0, one lane  : TMA producer (128-byte-swizzled boxes), waits on the
+//                       stage's empty mbarrier, arms / signals its full one;
+//   warp 1, one lane  : MMA issuer (even CTA only with PAIR), 4 MMAs per
+//                       stage, tcgen05.commit frees the stage (multicast to
+//                       both CTAs with PAIR); two TMEM accumulators of 256
+//                       columns let the next tile's mainloop overlap the
+//                       previous tile's epilogue;
 //   warps 2-5         : epilogue -- tcgen05.ld of the warp's 32 TMEM lanes,
 //                       y = acc * (sinv_a * sinv_b) + bias, rounding to the
 //                       output type, 16-byte stores, running max |y|; one
 //                       atomic max per warp at the end.
 // Every mbarrier wait is bounded (about 2 s of %globaltimer); on expiry the
 // thread raises a device flag that fp8mp_check() reports, tells the other
-// roles to stop, waits (bounded) for its own copies / MMAs in flight, and the
-// CTA frees its TMEM and returns.
+// roles of its CTA to stop, waits (bounded) for its own copies / MMAs in
+// flight, and the CTA frees its TMEM and returns.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
+#include <cstdlib>
+#include <cstring>
 #include <mutex>
 
 #include "fp8mp_internal.cuh"
@@ -46,27 +58,35 @@ __device__ unsigned int g_gemm_timeout_flag = 0;
 
 namespace {
 
-constexpr int BM = 128;           // rows of A per tile (TMEM lanes)
-constexpr int BN = 256;           // rows of B per tile (TMEM columns per accumulator)
 constexpr int BK = 128;           // bytes of k per stage = one 128-byte swizzle row
 constexpr int UMMA_K = 32;        // k of one kind::f8f6f4 MMA (32 bytes)
-constexpr int STAGES = 4;
+constexpr int TILE_N = 256;       // output columns per tile (TMEM columns per accumulator)
+constexpr int ROWS_A = 128;       // rows of A each CTA stages (TMEM lanes)
 constexpr int NUM_EPI_WARPS = 4;
 constexpr int NUM_THREADS = 64 + 32 * NUM_EPI_WARPS;
-constexpr int GROUP_M = 16;       // tile raster: 16 row-blocks of A per group
-constexpr uint32_t TMEM_COLS = 2 * BN;
+constexpr int GROUP_M = 16;       // tile raster: 16 row-blocks per group
+constexpr uint32_t TMEM_COLS = 2 * TILE_N;
 constexpr uint64_t kWaitLimitNs = 2000000000ull;
 
-constexpr int A_BYTES = BM * BK;
-constexpr int B_BYTES = BN * BK;
-constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
-constexpr int BAR_OFFSET = STAGES * STAGE_BYTES;
-constexpr int NUM_BARS = 2 * STAGES + 5;  // full, empty, tmem_full[2], tmem_empty[2], drain
-constexpr int SLOT_OFFSET = BAR_OFFSET + NUM_BARS * 8;
-constexpr int FLAG_OFFSET = SLOT_OFFSET + 8;
-constexpr int SMEM_USED = FLAG_OFFSET + 8;
-constexpr int SMEM_ALLOC = SMEM_USED + 1024;  // slack to align the base to 1024 bytes
-static_assert(STAGE_BYTES % 1024 == 0 && A_BYTES % 1024 == 0, "swizzle atoms need 1 KB alignment");
+template <bool PAIR>
+struct Cfg {
+    static constexpr int TILE_M = PAIR ? 256 : 128;   // output rows per tile
+    static constexpr int ROWS_B = PAIR ? 128 : 256;   // rows of B each CTA stages
+    static constexpr int STAGES = PAIR ? 6 : 4;
+    static constexpr int A_BYTES = ROWS_A * BK;
+    static constexpr int B_BYTES = ROWS_B * BK;
+    static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+    static constexpr int TX_BYTES = PAIR ? 2 * STAGE_BYTES : STAGE_BYTES;  // bytes one full phase waits for
+    static constexpr int BAR_OFFSET = STAGES * STAGE_BYTES;
+    static constexpr int NUM_BARS = 2 * STAGES + 5;  // full, empty, tmem_full[2], tmem_empty[2], drain
+    static constexpr int SLOT_OFFSET = BAR_OFFSET + NUM_BARS * 8;
+    static constexpr int FLAG_OFFSET = SLOT_OFFSET + 8;
+    static constexpr int SMEM_USED = FLAG_OFFSET + 8;
+    static constexpr int SMEM_ALLOC = SMEM_USED + 1024;  // slack to align the base to 1024 bytes
+    static constexpr uint32_t TEMPTY_COUNT = PAIR ? 2 * NUM_EPI_WARPS : NUM_EPI_WARPS;
+    static_assert(STAGE_BYTES % 1024 == 0 && A_BYTES % 1024 == 0, "swizzle atoms need 1 KB alignment");
+    static_assert(SMEM_ALLOC <= 232448, "shared memory budget");
+};
 
 struct GemmParams {
     int rows_a, rows_b, num_kb;
@@ -93,6 +113,10 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t byt
 __device__ __forceinline__ void mbar_arrive(uint32_t bar) {
     asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
 }
+// Arrive on an mbarrier given by its shared::cluster address (any CTA of the cluster).
+__device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr) {
+    asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
+}
 __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
     uint32_t ok;
     asm volatile(
@@ -108,6 +132,20 @@ __device__ __forceinline__ uint64_t global_timer_ns() {
     uint64_t t;
     asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
     return t;
+}
+__device__ __forceinline__ uint32_t cluster_ctarank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+// shared::cluster address of the variable at local shared address `addr` in CTA `rank`.
+__device__ __forceinline__ uint32_t mapa_shared(uint32_t addr, uint32_t rank) {
+    uint32_t r;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(addr), "r"(rank));
+    return r;
+}
+__device__ __forceinline__ void cluster_sync_all() {
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
 
 // Waits until the phase of parity `parity` of `bar` has completed. Returns
@@ -129,43 +167,98 @@ __device__ __noinline__ bool wait_bounded(uint32_t bar, uint32_t parity, volatil
     }
 }
 
+// TMA 2-D tile load into this CTA's shared memory; completion is counted on
+// the mbarrier at shared::cluster address `bar` (with PAIR it may sit in the
+// peer CTA of the pair).
+template <bool PAIR>
 __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *map, uint32_t bar, int32_t c0,
                                             int32_t c1) {
-    asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%3, %4}], [%2];" ::"r"(
-            dst),
-        "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(c0), "r"(c1)
-        : "memory");
+    if constexpr (PAIR)
+        asm volatile(
+            "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes"
+            " [%0], [%1, {%3, %4}], [%2];" ::"r"(dst),
+            "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(c0), "r"(c1)
+            : "memory");
+    else
+        asm volatile(
+            "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes"
+            " [%0], [%1, {%3, %4}], [%2];" ::"r"(dst),
+            "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(c0), "r"(c1)
+            : "memory");
 }
 __device__ __forceinline__ void prefetch_tmap(const CUtensorMap *map) {
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
 }
 
+template <bool PAIR>
 __device__ __forceinline__ void tmem_alloc(uint32_t slot, uint32_t ncols) {
-    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(slot), "r"(ncols)
-                 : "memory");
+    if constexpr (PAIR)
+        asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(slot), "r"(ncols)
+                     : "memory");
+    else
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(slot), "r"(ncols)
+                     : "memory");
 }
+template <bool PAIR>
 __device__ __forceinline__ void tmem_relinquish() {
-    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    if constexpr (PAIR)
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+    else
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
 }
+template <bool PAIR>
 __device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
-    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
+    if constexpr (PAIR)
+        asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
+    else
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
 }
 __device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
 __device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
 
+template <bool PAIR>
 __device__ __forceinline__ void umma_f8f6f4(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
                                             uint32_t accumulate) {
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "setp.ne.b32 p, %4, 0;\n\t"
-        "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
-        : "memory");
+    if constexpr (PAIR)
+        asm volatile(
+            "{\n\t.reg .pred p;\n\t"
+            "setp.ne.b32 p, %4, 0;\n\t"
+            "tcgen05.mma.cta_group::2.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+            "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+            : "memory");
+    else
+        asm volatile(
+            "{\n\t.reg .pred p;\n\t"
+            "setp.ne.b32 p, %4, 0;\n\t"
+            "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+            "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+            : "memory");
 }
-__device__ __forceinline__ void umma_commit(uint32_t bar) {
-    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
-                 : "memory");
+// Arrive once on `bar` when all MMAs this thread issued so far complete: in
+// this CTA (PAIR = false), or at the same offset in both CTAs of the pair.
+template <bool PAIR>
+__device__ __forceinline__ void umma_commit_all(uint32_t bar) {
+    if constexpr (PAIR) {
+        const uint16_t mask = 0x3;
+        asm volatile(
+            "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(
+                bar),
+            "h"(mask)
+            : "memory");
+    } else {
+        asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+                     : "memory");
+    }
+}
+// Arrive once on this CTA's `bar` when the MMAs issued so far complete.
+template <bool PAIR>
+__device__ __forceinline__ void umma_commit_local(uint32_t bar) {
+    if constexpr (PAIR)
+        asm volatile("tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+                     : "memory");
+    else
+        asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+                     : "memory");
 }
 
 // 32 consecutive fp32 columns of this warp's 32 TMEM lanes (lane i of the
@@ -218,33 +311,39 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float a, float b) {
 
 // ------------------------------------------------------------------ kernel
 
+template <bool PAIR>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
 gemm_fp8_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CUtensorMap tmap_b,
                 const GemmParams p, const uint32_t idesc) {
+    using C = Cfg<PAIR>;
     extern __shared__ uint8_t smem_raw[];
     uint32_t base = smem_u32(smem_raw);
     const uint32_t pad = (1024u - (base & 1023u)) & 1023u;
     uint8_t *smem = smem_raw + pad;
     base += pad;
 
-    const uint32_t bar0 = base + BAR_OFFSET;
+    const uint32_t bar0 = base + C::BAR_OFFSET;
     auto full_bar = [&](int s) { return bar0 + 8u * s; };
-    auto empty_bar = [&](int s) { return bar0 + 8u * (STAGES + s); };
-    auto tfull_bar = [&](int a) { return bar0 + 8u * (2 * STAGES + a); };
-    auto tempty_bar = [&](int a) { return bar0 + 8u * (2 * STAGES + 2 + a); };
-    const uint32_t drain_bar = bar0 + 8u * (2 * STAGES + 4);
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + SLOT_OFFSET);
-    volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + FLAG_OFFSET);
+    auto empty_bar = [&](int s) { return bar0 + 8u * (C::STAGES + s); };
+    auto tfull_bar = [&](int a) { return bar0 + 8u * (2 * C::STAGES + a); };
+    auto tempty_bar = [&](int a) { return bar0 + 8u * (2 * C::STAGES + 2 + a); };
+    const uint32_t drain_bar = bar0 + 8u * (2 * C::STAGES + 4);
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + C::SLOT_OFFSET);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + C::FLAG_OFFSET);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const uint32_t rank = PAIR ? cluster_ctarank() : 0u;  // 0 = the CTA that issues the MMAs
+    const int cluster_id = PAIR ? static_cast<int>(blockIdx.x >> 1) : static_cast<int>(blockIdx.x);
+    const int num_clusters = PAIR ? static_cast<int>(gridDim.x >> 1) : static_cast<int>(gridDim.x);
+
     if (threadIdx.x == 0) {
-        for (int s = 0; s < STAGES; ++s) {
+        for (int s = 0; s < C::STAGES; ++s) {
             mbar_init(full_bar(s), 1);
             mbar_init(empty_bar(s), 1);
         }
         for (int a = 0; a < 2; ++a) {
             mbar_init(tfull_bar(a), 1);
-            mbar_init(tempty_bar(a), NUM_EPI_WARPS);
+            mbar_init(tempty_bar(a), C::TEMPTY_COUNT);
         }
         mbar_init(drain_bar, 1);
         *abort_flag = 0;
@@ -253,11 +352,14 @@ gemm_fp8_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constan
         prefetch_tmap(&tmap_b);
     }
     if (warp == 1) {
-        tmem_alloc(smem_u32(tmem_slot), TMEM_COLS);
-        tmem_relinquish();
+        tmem_alloc<PAIR>(smem_u32(tmem_slot), TMEM_COLS);
+        tmem_relinquish<PAIR>();
     }
     tc_fence_before();
-    __syncthreads();
+    if constexpr (PAIR)
+        cluster_sync_all();  // the peer's barriers are initialised before anyone signals them
+    else
+        __syncthreads();
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
 
@@ -265,43 +367,47 @@ gemm_fp8_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constan
 
     if (warp == 0) {
         if (lane == 0) {
-            // ---------------- TMA producer
+            // ---------------- TMA producer (both CTAs of a pair)
             uint32_t it = 0;
-            int issued_stages = 0;  // stages that have received at least one load
+            int issued_stages = 0;
             bool ok = true;
-            for (int tile = blockIdx.x; ok && tile < num_tiles; tile += gridDim.x) {
+            for (int tile = cluster_id; ok && tile < num_tiles; tile += num_clusters) {
                 int mb, nb;
                 tile_coords(tile, p.tiles_m, p.tiles_n, mb, nb);
+                const int a_row = mb * C::TILE_M + static_cast<int>(rank) * ROWS_A;
+                const int b_row = nb * TILE_N + static_cast<int>(rank) * C::ROWS_B;
                 for (int kb = 0; kb < p.num_kb; ++kb, ++it) {
-                    const int s = static_cast<int>(it % STAGES);
-                    const uint32_t ph = (it / STAGES) & 1u;
+                    const int s = static_cast<int>(it % C::STAGES);
+                    const uint32_t ph = (it / C::STAGES) & 1u;
                     if (!wait_bounded(empty_bar(s), ph ^ 1u, abort_flag)) {
                         ok = false;
                         break;
                     }
-                    const uint32_t sa = base + s * STAGE_BYTES;
-                    mbar_arrive_expect_tx(full_bar(s), STAGE_BYTES);
-                    tma_load_2d(sa, &tmap_a, full_bar(s), kb * BK, mb * BM);
-                    tma_load_2d(sa + A_BYTES, &tmap_b, full_bar(s), kb * BK, nb * BN);
-                    if (issued_stages < STAGES) ++issued_stages;
+                    const uint32_t sa = base + s * C::STAGE_BYTES;
+                    // the full barrier of a pair lives in the MMA-issuing CTA
+                    const uint32_t fb = PAIR ? mapa_shared(full_bar(s), 0) : full_bar(s);
+                    if (rank == 0) mbar_arrive_expect_tx(full_bar(s), C::TX_BYTES);
+                    tma_load_2d<PAIR>(sa, &tmap_a, fb, kb * BK, a_row);
+                    tma_load_2d<PAIR>(sa + C::A_BYTES, &tmap_b, fb, kb * BK, b_row);
+                    if (issued_stages < C::STAGES) ++issued_stages;
                 }
             }
-            if (!ok) {
+            if (!ok && rank == 0) {
                 // let the loads already issued land before the CTA goes away
                 for (int j = 1; j <= issued_stages && j <= static_cast<int>(it); ++j) {
                     const uint32_t last = it - static_cast<uint32_t>(j);
                     volatile int never = 0;
-                    wait_bounded(full_bar(static_cast<int>(last % STAGES)), (last / STAGES) & 1u, &never);
+                    wait_bounded(full_bar(static_cast<int>(last % C::STAGES)), (last / C::STAGES) & 1u, &never);
                 }
             }
         }
     } else if (warp == 1) {
-        if (lane == 0) {
+        if (lane == 0 && rank == 0) {
             // ---------------- MMA issuer
             uint32_t it = 0;
             int lt = 0;
             bool ok = true;
-            for (int tile = blockIdx.x; ok && tile < num_tiles; tile += gridDim.x, ++lt) {
+            for (int tile = cluster_id; ok && tile < num_tiles; tile += num_clusters, ++lt) {
                 const int acc = lt & 1;
                 const uint32_t aph = (static_cast<uint32_t>(lt) >> 1) & 1u;
                 if (!wait_bounded(tempty_bar(acc), aph ^ 1u, abort_flag)) {
@@ -309,42 +415,42 @@ gemm_fp8_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constan
                     break;
                 }
                 tc_fence_after();
-                const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * BN);
+                const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * TILE_N);
                 for (int kb = 0; kb < p.num_kb; ++kb, ++it) {
-                    const int s = static_cast<int>(it % STAGES);
-                    const uint32_t ph = (it / STAGES) & 1u;
+                    const int s = static_cast<int>(it % C::STAGES);
+                    const uint32_t ph = (it / C::STAGES) & 1u;
                     if (!wait_bounded(full_bar(s), ph, abort_flag)) {
                         ok = false;
                         break;
                     }
                     tc_fence_after();
-                    const uint32_t sa = base + s * STAGE_BYTES;
+                    const uint32_t sa = base + s * C::STAGE_BYTES;
 #pragma unroll
                     for (int k = 0; k < BK / UMMA_K; ++k) {
-                        umma_f8f6f4(d_tmem, sw128_kmajor_desc(sa + k * UMMA_K),
-                                    sw128_kmajor_desc(sa + A_BYTES + k * UMMA_K), idesc,
-                                    (kb > 0 || k > 0) ? 1u : 0u);
+                        umma_f8f6f4<PAIR>(d_tmem, sw128_kmajor_desc(sa + k * UMMA_K),
+                                          sw128_kmajor_desc(sa + C::A_BYTES + k * UMMA_K), idesc,
+                                          (kb > 0 || k > 0) ? 1u : 0u);
                     }
-                    umma_commit(empty_bar(s));
+                    umma_commit_all<PAIR>(empty_bar(s));
                 }
                 if (!ok) break;
-                umma_commit(tfull_bar(acc));
+                umma_commit_all<PAIR>(tfull_bar(acc));
             }
             if (!ok) {
                 // wait for the MMAs in flight before TMEM is released
-                umma_commit(drain_bar);
+                umma_commit_local<PAIR>(drain_bar);
                 volatile int never = 0;
                 wait_bounded(drain_bar, 0u, &never);
             }
         }
     } else {
-        // ---------------- epilogue warps
+        // ---------------- epilogue warps (both CTAs of a pair)
         const int q = warp & 3;  // this warp may access TMEM lanes 32q .. 32q+31
-        const int row_in_tile = q * 32 + lane;
+        const int row_in_tile = static_cast<int>(rank) * ROWS_A + q * 32 + lane;
         const float scale = __fmul_rn(__ldg(p.sinv_a), __ldg(p.sinv_b));
         float am = 0.0f;
         int lt = 0;
-        for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x, ++lt) {
+        for (int tile = cluster_id; tile < num_tiles; tile += num_clusters, ++lt) {
             const int acc = lt & 1;
             const uint32_t aph = (static_cast<uint32_t>(lt) >> 1) & 1u;
             int ok = 1;
@@ -354,16 +460,16 @@ gemm_fp8_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constan
             tc_fence_after();
             int mb, nb;
             tile_coords(tile, p.tiles_m, p.tiles_n, mb, nb);
-            const int64_t m = static_cast<int64_t>(mb) * BM + row_in_tile;
+            const int64_t m = static_cast<int64_t>(mb) * C::TILE_M + row_in_tile;
             const bool row_ok = m < p.rows_a;
 #pragma unroll 1
-            for (int c = 0; c < BN; c += 32) {
+            for (int c = 0; c < TILE_N; c += 32) {
                 uint32_t r[32];
-                tmem_ld32(tmem_base + static_cast<uint32_t>(acc * BN + c) + (static_cast<uint32_t>(q * 32) << 16),
+                tmem_ld32(tmem_base + static_cast<uint32_t>(acc * TILE_N + c) + (static_cast<uint32_t>(q * 32) << 16),
                           r);
 #pragma unroll
                 for (int h = 0; h < 2; ++h) {
-                    const int n = nb * BN + c + 16 * h;
+                    const int n = nb * TILE_N + c + 16 * h;
                     if (!row_ok || n >= p.rows_b) continue;
                     float y[16];
                     if (p.bias == nullptr) {
@@ -408,7 +514,12 @@ gemm_fp8_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constan
             }
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(tempty_bar(acc));
+            if (lane == 0) {
+                if constexpr (PAIR)
+                    mbar_arrive_cluster(mapa_shared(tempty_bar(acc), 0));  // the MMA issuer's barrier
+                else
+                    mbar_arrive(tempty_bar(acc));
+            }
         }
         if (p.out_amax != nullptr) {
             am = warp_max(am);
@@ -419,9 +530,12 @@ gemm_fp8_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constan
 
     __syncwarp();
     tc_fence_before();
-    __syncthreads();
+    if constexpr (PAIR)
+        cluster_sync_all();  // no CTA leaves while its peer may still touch its shared memory
+    else
+        __syncthreads();
     tc_fence_after();
-    if (warp == 1) tmem_dealloc(tmem_base, TMEM_COLS);
+    if (warp == 1) tmem_dealloc<PAIR>(tmem_base, TMEM_COLS);
 }
 
 // out = bias (or 0) broadcast over rows: the GEMM of an empty contraction.
@@ -478,13 +592,71 @@ int make_tmap(CUtensorMap *map, const void *ptr, uint64_t inner, uint64_t outer,
     return FP8MP_OK;
 }
 
-constexpr uint32_t make_idesc(int fmt_a, int fmt_b) {
+constexpr uint32_t make_idesc(int fmt_a, int fmt_b, int m) {
     return (1u << 4)                                    // accumulator: f32
            | (static_cast<uint32_t>(fmt_a) << 7)        // A: 0 = E4M3, 1 = E5M2
            | (static_cast<uint32_t>(fmt_b) << 10)       // B: 0 = E4M3, 1 = E5M2
            | (0u << 15) | (0u << 16)                    // A and B K-major
-           | (static_cast<uint32_t>(BN >> 3) << 17)     // N / 8
-           | (static_cast<uint32_t>(BM >> 4) << 24);    // M / 16
+           | (static_cast<uint32_t>(TILE_N >> 3) << 17) // N / 8
+           | (static_cast<uint32_t>(m >> 4) << 24);     // M / 16
+}
+
+struct PerDevice {
+    bool attr_done[2] = {false, false};
+    int max_pairs = 0;
+};
+PerDevice g_dev[64];
+
+template <bool PAIR>
+int launch_engine(const CUtensorMap &ta, const CUtensorMap &tb, const GemmParams &p, int grid, uint32_t idesc,
+                  cudaStream_t s) {
+    using C = Cfg<PAIR>;
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1];
+    cfg.gridDim = dim3(static_cast<unsigned>(grid));
+    cfg.blockDim = dim3(NUM_THREADS);
+    cfg.dynamicSmemBytes = C::SMEM_ALLOC;
+    cfg.stream = s;
+    if (PAIR) {
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = 2;
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+    }
+    const cudaError_t e = cudaLaunchKernelEx(&cfg, gemm_fp8_kernel<PAIR>, ta, tb, p, idesc);
+    if (e != cudaSuccess) return fail(FP8MP_ERR_LAUNCH, "GEMM launch failed: %s", cudaGetErrorString(e));
+    return FP8MP_OK;
+}
+
+template <bool PAIR>
+int prepare_engine(const DeviceInfo &dev) {
+    using C = Cfg<PAIR>;
+    PerDevice &pd = g_dev[dev.device & 63];
+    if (pd.attr_done[PAIR]) return FP8MP_OK;
+    cudaError_t e =
+        cudaFuncSetAttribute(gemm_fp8_kernel<PAIR>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_ALLOC);
+    if (e != cudaSuccess) return fail(FP8MP_ERR_LAUNCH, "GEMM smem attribute failed: %s", cudaGetErrorString(e));
+    if (PAIR) {
+        cudaLaunchConfig_t cfg = {};
+        cudaLaunchAttribute attr[1];
+        cfg.gridDim = dim3(static_cast<unsigned>(dev.num_sms & ~1));
+        cfg.blockDim = dim3(NUM_THREADS);
+        cfg.dynamicSmemBytes = C::SMEM_ALLOC;
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = 2;
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        int n = 0;
+        e = cudaOccupancyMaxActiveClusters(&n, gemm_fp8_kernel<true>, &cfg);
+        if (e != cudaSuccess || n < 1) n = dev.num_sms / 2;
+        pd.max_pairs = n;
+    }
+    pd.attr_done[PAIR] = true;
+    return FP8MP_OK;
 }
 
 }  // namespace
@@ -504,18 +676,11 @@ int launch_gemm(const uint8_t *a, int fmt_a, const uint8_t *b, int fmt_b, int64_
         if (e != cudaSuccess) return fail(FP8MP_ERR_LAUNCH, "GEMM fill launch failed: %s", cudaGetErrorString(e));
         return FP8MP_OK;
     }
-    CUtensorMap ta, tb;
-    int rc = make_tmap(&ta, a, static_cast<uint64_t>(kc), static_cast<uint64_t>(rows_a), BM);
-    if (rc) return rc;
-    rc = make_tmap(&tb, b, static_cast<uint64_t>(kc), static_cast<uint64_t>(rows_b), BN);
-    if (rc) return rc;
-
     GemmParams p;
     p.rows_a = static_cast<int>(rows_a);
     p.rows_b = static_cast<int>(rows_b);
     p.num_kb = static_cast<int>((kc + BK - 1) / BK);
-    p.tiles_m = static_cast<int>((rows_a + BM - 1) / BM);
-    p.tiles_n = static_cast<int>((rows_b + BN - 1) / BN);
+    p.tiles_n = static_cast<int>((rows_b + TILE_N - 1) / TILE_N);
     p.sinv_a = sinv_a;
     p.sinv_b = sinv_b;
     p.bias = bias;
@@ -523,22 +688,40 @@ int launch_gemm(const uint8_t *a, int fmt_a, const uint8_t *b, int fmt_b, int64_
     p.out = out;
     p.out_bf16 = out_dtype == FP8MP_BF16;
     p.out_amax = out_amax;
-    const int64_t num_tiles = static_cast<int64_t>(p.tiles_m) * p.tiles_n;
-    if (num_tiles > 0x7FFFFFFF) return fail(FP8MP_ERR_INVALID, "GEMM has too many tiles");
-    const int grid = static_cast<int>(num_tiles < dev.num_sms ? num_tiles : dev.num_sms);
 
-    static int attr_done[64] = {0};
-    if (dev.device >= 0 && dev.device < 64 && !attr_done[dev.device]) {
-        const cudaError_t e =
-            cudaFuncSetAttribute(gemm_fp8_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_ALLOC);
-        if (e != cudaSuccess)
-            return fail(FP8MP_ERR_LAUNCH, "GEMM smem attribute failed: %s", cudaGetErrorString(e));
-        attr_done[dev.device] = 1;
+    // Pairs of SMs on 256 x 256 tiles when there are enough tiles to occupy
+    // most SMs; otherwise single-SM 128 x 256 tiles (twice as many tiles).
+    // FP8MP_GEMM_ENGINE=pair|single overrides the choice (used by the tests
+    // to run both engines on every shape).
+    const int64_t pair_tiles = ((rows_a + 255) / 256) * p.tiles_n;
+    bool pair = pair_tiles * 2 >= dev.num_sms;
+    if (const char *force = std::getenv("FP8MP_GEMM_ENGINE")) {
+        if (std::strcmp(force, "pair") == 0) pair = true;
+        if (std::strcmp(force, "single") == 0) pair = false;
     }
-    gemm_fp8_kernel<<<grid, NUM_THREADS, SMEM_ALLOC, s>>>(ta, tb, p, make_idesc(fmt_a, fmt_b));
-    const cudaError_t e = cudaGetLastError();
-    if (e != cudaSuccess) return fail(FP8MP_ERR_LAUNCH, "GEMM launch failed: %s", cudaGetErrorString(e));
-    return FP8MP_OK;
+    int rc = pair ? prepare_engine<true>(dev) : prepare_engine<false>(dev);
+    if (rc) return rc;
+
+    CUtensorMap ta, tb;
+    rc = make_tmap(&ta, a, static_cast<uint64_t>(kc), static_cast<uint64_t>(rows_a), ROWS_A);
+    if (rc) return rc;
+    rc = make_tmap(&tb, b, static_cast<uint64_t>(kc), static_cast<uint64_t>(rows_b),
+                   pair ? Cfg<true>::ROWS_B : Cfg<false>::ROWS_B);
+    if (rc) return rc;
+
+    if (pair) {
+        p.tiles_m = static_cast<int>((rows_a + 255) / 256);
+        const int64_t tiles = static_cast<int64_t>(p.tiles_m) * p.tiles_n;
+        if (tiles > 0x7FFFFFFF) return fail(FP8MP_ERR_INVALID, "GEMM has too many tiles");
+        const int max_pairs = g_dev[dev.device & 63].max_pairs;
+        const int clusters = static_cast<int>(tiles < max_pairs ? tiles : max_pairs);
+        return launch_engine<true>(ta, tb, p, 2 * clusters, make_idesc(fmt_a, fmt_b, 256), s);
+    }
+    p.tiles_m = static_cast<int>((rows_a + 127) / 128);
+    const int64_t tiles = static_cast<int64_t>(p.tiles_m) * p.tiles_n;
+    if (tiles > 0x7FFFFFFF) return fail(FP8MP_ERR_INVALID, "GEMM has too many tiles");
+    const int grid = static_cast<int>(tiles < dev.num_sms ? tiles : dev.num_sms);
+    return launch_engine<false>(ta, tb, p, grid, make_idesc(fmt_a, fmt_b, 128), s);
 }
 
 int read_and_clear_timeout_flag(unsigned int *value) {

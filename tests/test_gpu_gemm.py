@@ -15,6 +15,14 @@ pytestmark = pytest.mark.gpu
 TORCH_DT = {"f32": torch.float32, "bf16": torch.bfloat16}
 
 
+@pytest.fixture(params=["single", "pair"])
+def engine(request, monkeypatch):
+    """Runs a test on both tile engines: single-SM 128x256 tiles and
+    SM-pair 256x256 tiles (the library reads FP8MP_GEMM_ENGINE per call)."""
+    monkeypatch.setenv("FP8MP_GEMM_ENGINE", request.param)
+    return request.param
+
+
 def sc(v):
     return torch.tensor([v], dtype=torch.float32, device="cuda")
 
@@ -31,12 +39,12 @@ def fwd(fp8mp, A, B, sa, sb, bias=None, out="bf16", amax0=None):
 # (M, N, K): single tile, several tiles, ragged in every dimension, tiny,
 # the 768 layer, a long contraction
 SHAPES = [(128, 256, 128), (256, 512, 256), (1040, 784, 784), (16, 16, 16), (1024, 768, 768),
-          (128, 256, 16384), (384, 1280, 1152)]
+          (128, 256, 16384), (384, 1280, 1152), (144, 272, 2064), (2304, 2560, 1024)]
 
 
 @pytest.mark.parametrize("M,N,K", SHAPES)
 @pytest.mark.parametrize("out", ["bf16", "f32"])
-def test_fwd_random_codes(cuda_lib, orc, M, N, K, out):
+def test_fwd_random_codes(cuda_lib, orc, engine, M, N, K, out):
     rng = np.random.default_rng(M * 31 + N * 7 + K)
     A = finite_codes(rng, (M, K), E4M3)
     B = finite_codes(rng, (N, K), E4M3)
@@ -48,7 +56,7 @@ def test_fwd_random_codes(cuda_lib, orc, M, N, K, out):
 
 @pytest.mark.parametrize("bias_dt", ["f32", "bf16"])
 @pytest.mark.parametrize("out", ["bf16", "f32"])
-def test_fwd_bias_and_output_amax(cuda_lib, orc, bias_dt, out):
+def test_fwd_bias_and_output_amax(cuda_lib, orc, engine, bias_dt, out):
     M, N, K = 1040, 784, 512
     rng = np.random.default_rng(5)
     A = finite_codes(rng, (M, K), E4M3)
@@ -66,7 +74,7 @@ def test_fwd_bias_and_output_amax(cuda_lib, orc, bias_dt, out):
 
 @pytest.mark.parametrize("dy_fmt", [E5M2, E4M3])
 @pytest.mark.parametrize("M,N,K", [(256, 512, 256), (1040, 784, 784), (1024, 768, 768)])
-def test_dgrad_and_wgrad(cuda_lib, orc, dy_fmt, M, N, K):
+def test_dgrad_and_wgrad(cuda_lib, orc, engine, dy_fmt, M, N, K):
     rng = np.random.default_rng(M + 2 * N + 3 * K + dy_fmt)
     dy8 = finite_codes(rng, (M, N), dy_fmt)
     w8t = finite_codes(rng, (K, N), E4M3)
@@ -85,7 +93,7 @@ def test_dgrad_and_wgrad(cuda_lib, orc, dy_fmt, M, N, K):
         gemm_tolerance_check(np_view(dw.float()).astype(np.float64), ref, ab, "wgrad")
 
 
-def test_long_contraction_e5m2_wgrad(cuda_lib, orc):
+def test_long_contraction_e5m2_wgrad(cuda_lib, orc, engine):
     """wgrad contracts over all tokens: 16384 here (the MLP workload's M)."""
     N, K, M = 256, 384, 16384
     rng = np.random.default_rng(77)
@@ -98,7 +106,7 @@ def test_long_contraction_e5m2_wgrad(cuda_lib, orc):
     gemm_tolerance_check(np_view(dw).astype(np.float64), ref, ab, "wgrad K=16384")
 
 
-def test_empty_contraction_and_empty_output(cuda_lib):
+def test_empty_contraction_and_empty_output(cuda_lib, engine):
     bias = torch.arange(32, dtype=torch.float32, device="cuda")
     y = torch.full((16, 32), 7.0, dtype=torch.float32, device="cuda")
     am = torch.zeros(1, device="cuda")
