@@ -66,7 +66,8 @@ constexpr int NUM_EPI_WARPS = 4;
 constexpr int NUM_THREADS = 64 + 32 * NUM_EPI_WARPS;
 constexpr int GROUP_M = 16;       // tile raster: 16 row-blocks per group
 constexpr uint32_t TMEM_COLS = 2 * TILE_N;
-constexpr uint64_t kWaitLimitNs = 2000000000ull;
+constexpr long long kWaitLimitCycles = 4000000000ll;  // about 2 s at the SM clock
+constexpr uint32_t kSuspendHintNs = 1000000u;          // longest single sleep inside try_wait
 
 template <bool PAIR>
 struct Cfg {
@@ -77,7 +78,11 @@ struct Cfg {
     static constexpr int B_BYTES = ROWS_B * BK;
     static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
     static constexpr int TX_BYTES = PAIR ? 2 * STAGE_BYTES : STAGE_BYTES;  // bytes one full phase waits for
-    static constexpr int BAR_OFFSET = STAGES * STAGE_BYTES;
+    // output staging: per epilogue warp two 32-row x 128-byte boxes (4 KB each)
+    static constexpr int EPI_OFFSET = STAGES * STAGE_BYTES;
+    static constexpr int EPI_BOX_BYTES = 32 * 128;
+    static constexpr int EPI_BYTES = NUM_EPI_WARPS * 2 * EPI_BOX_BYTES;
+    static constexpr int BAR_OFFSET = EPI_OFFSET + EPI_BYTES;
     static constexpr int NUM_BARS = 2 * STAGES + 5;  // full, empty, tmem_full[2], tmem_empty[2], drain
     static constexpr int SLOT_OFFSET = BAR_OFFSET + NUM_BARS * 8;
     static constexpr int FLAG_OFFSET = SLOT_OFFSET + 8;
@@ -117,21 +122,18 @@ __device__ __forceinline__ void mbar_arrive(uint32_t bar) {
 __device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr) {
     asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
 }
+// Tests the phase; if it is not complete the thread sleeps in hardware until
+// it completes or kSuspendHintNs pass (no spinning on the issue slots).
 __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
     uint32_t ok;
     asm volatile(
         "{\n\t.reg .pred p;\n\t"
-        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
         "selp.u32 %0, 1, 0, p;\n\t}"
         : "=r"(ok)
-        : "r"(bar), "r"(parity)
+        : "r"(bar), "r"(parity), "r"(kSuspendHintNs)
         : "memory");
     return ok != 0;
-}
-__device__ __forceinline__ uint64_t global_timer_ns() {
-    uint64_t t;
-    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
-    return t;
 }
 __device__ __forceinline__ uint32_t cluster_ctarank() {
     uint32_t r;
@@ -149,22 +151,23 @@ __device__ __forceinline__ void cluster_sync_all() {
 }
 
 // Waits until the phase of parity `parity` of `bar` has completed. Returns
-// false if another role has raised `abort_flag` or if about kWaitLimitNs
-// elapse (then raises both flags).
-__device__ __noinline__ bool wait_bounded(uint32_t bar, uint32_t parity, volatile int *abort_flag) {
-    if (mbar_try_wait(bar, parity)) return true;
-    const uint64_t t0 = global_timer_ns();
-    for (uint32_t i = 1;; ++i) {
+// false if another role has raised `abort_flag` or if about kWaitLimitCycles
+// SM cycles elapse (then raises both flags).
+__device__ __noinline__ bool wait_bounded_slow(uint32_t bar, uint32_t parity, volatile int *abort_flag) {
+    const long long t0 = clock64();
+    for (;;) {
         if (mbar_try_wait(bar, parity)) return true;
-        if ((i & 63u) == 0u) {
-            if (*abort_flag) return false;
-            if (global_timer_ns() - t0 > kWaitLimitNs) {
-                *abort_flag = 1;
-                atomicOr(&g_gemm_timeout_flag, 1u);
-                return false;
-            }
+        if (*abort_flag) return false;
+        if (clock64() - t0 > kWaitLimitCycles) {
+            *abort_flag = 1;
+            atomicOr(&g_gemm_timeout_flag, 1u);
+            return false;
         }
     }
+}
+__device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity, volatile int *abort_flag) {
+    if (mbar_try_wait(bar, parity)) return true;
+    return wait_bounded_slow(bar, parity, abort_flag);
 }
 
 // TMA 2-D tile load into this CTA's shared memory; completion is counted on
@@ -185,6 +188,24 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *map
             " [%0], [%1, {%3, %4}], [%2];" ::"r"(dst),
             "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(c0), "r"(c1)
             : "memory");
+}
+// TMA 2-D tile store from this CTA's shared memory (rows / columns outside
+// the tensor are not written), tracked as a bulk async-group of the thread.
+__device__ __forceinline__ void tma_store_2d(const CUtensorMap *map, uint32_t src, int32_t c0, int32_t c1) {
+    asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%2, %3}], [%1];" ::"l"(
+                     reinterpret_cast<uint64_t>(map)),
+                 "r"(src), "r"(c0), "r"(c1)
+                 : "memory");
+}
+__device__ __forceinline__ void bulk_commit_group() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+// Waits until at most one bulk group of this thread still reads shared memory.
+__device__ __forceinline__ void bulk_wait_read_le1() { asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory"); }
+// Waits until every bulk group of this thread has completed.
+__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+// Orders this thread's generic-proxy shared-memory writes before later async-proxy reads (TMA).
+__device__ __forceinline__ void fence_proxy_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
+__device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
+    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d) : "memory");
 }
 __device__ __forceinline__ void prefetch_tmap(const CUtensorMap *map) {
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
@@ -314,7 +335,7 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float a, float b) {
 template <bool PAIR>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
 gemm_fp8_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CUtensorMap tmap_b,
-                const GemmParams p, const uint32_t idesc) {
+                const __grid_constant__ CUtensorMap tmap_out, const GemmParams p, const uint32_t idesc) {
     using C = Cfg<PAIR>;
     extern __shared__ uint8_t smem_raw[];
     uint32_t base = smem_u32(smem_raw);
@@ -350,6 +371,7 @@ gemm_fp8_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constan
         fence_mbar_init();
         prefetch_tmap(&tmap_a);
         prefetch_tmap(&tmap_b);
+        prefetch_tmap(&tmap_out);
     }
     if (warp == 1) {
         tmem_alloc<PAIR>(smem_u32(tmem_slot), TMEM_COLS);
@@ -445,11 +467,19 @@ gemm_fp8_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constan
         }
     } else {
         // ---------------- epilogue warps (both CTAs of a pair)
+        // Each warp drains its 32 TMEM lanes (32 output rows) in chunks of
+        // 128 bytes per row (64 bf16 or 32 fp32 columns): tcgen05.ld, scale,
+        // bias and rounding in registers, the row written into a 128-byte-
+        // swizzled 32 x 128 B staging box, then one TMA store per box. Two
+        // boxes per warp alternate so the next chunk overlaps the store.
         const int q = warp & 3;  // this warp may access TMEM lanes 32q .. 32q+31
         const int row_in_tile = static_cast<int>(rank) * ROWS_A + q * 32 + lane;
         const float scale = __fmul_rn(__ldg(p.sinv_a), __ldg(p.sinv_b));
+        const int box_cols = p.out_bf16 ? 64 : 32;
+        const uint32_t stage_box = base + C::EPI_OFFSET + static_cast<uint32_t>((warp - 2) * 2 * C::EPI_BOX_BYTES);
         float am = 0.0f;
         int lt = 0;
+        uint32_t chunk_no = 0;
         for (int tile = cluster_id; tile < num_tiles; tile += num_clusters, ++lt) {
             const int acc = lt & 1;
             const uint32_t aph = (static_cast<uint32_t>(lt) >> 1) & 1u;
@@ -462,54 +492,76 @@ gemm_fp8_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constan
             tile_coords(tile, p.tiles_m, p.tiles_n, mb, nb);
             const int64_t m = static_cast<int64_t>(mb) * C::TILE_M + row_in_tile;
             const bool row_ok = m < p.rows_a;
+            const int warp_row0 = mb * C::TILE_M + static_cast<int>(rank) * ROWS_A + q * 32;
 #pragma unroll 1
-            for (int c = 0; c < TILE_N; c += 32) {
-                uint32_t r[32];
-                tmem_ld32(tmem_base + static_cast<uint32_t>(acc * TILE_N + c) + (static_cast<uint32_t>(q * 32) << 16),
-                          r);
+            for (int c = 0; c < TILE_N; c += box_cols, ++chunk_no) {
+                uint32_t packed[32];  // this lane's 128-byte row of the box
 #pragma unroll
-                for (int h = 0; h < 2; ++h) {
-                    const int n = nb * TILE_N + c + 16 * h;
-                    if (!row_ok || n >= p.rows_b) continue;
-                    float y[16];
-                    if (p.bias == nullptr) {
+                for (int half = 0; half < 2; ++half) {
+                    if (half == 1 && !p.out_bf16) break;
+                    uint32_t r[32];
+                    const int c32 = c + 32 * half;
+                    tmem_ld32(tmem_base + static_cast<uint32_t>(acc * TILE_N + c32) +
+                                  (static_cast<uint32_t>(q * 32) << 16),
+                              r);
 #pragma unroll
-                        for (int j = 0; j < 16; ++j) y[j] = __fmul_rn(__uint_as_float(r[16 * h + j]), scale);
-                    } else if (p.bias_bf16) {
-                        const uint4 *bp = reinterpret_cast<const uint4 *>(static_cast<const uint16_t *>(p.bias) + n);
-                        const uint4 b0 = __ldg(bp), b1 = __ldg(bp + 1);
-                        const uint32_t bw[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
+                    for (int g = 0; g < 2; ++g) {  // 16-column groups
+                        const int n = nb * TILE_N + c32 + 16 * g;
+                        const bool col_ok = n < p.rows_b;
+                        float y[16];
+                        if (p.bias == nullptr || !col_ok) {
 #pragma unroll
-                        for (int j = 0; j < 8; ++j) {
-                            y[2 * j] = __fmaf_rn(__uint_as_float(r[16 * h + 2 * j]), scale, __uint_as_float(bw[j] << 16));
-                            y[2 * j + 1] = __fmaf_rn(__uint_as_float(r[16 * h + 2 * j + 1]), scale,
-                                                     __uint_as_float(bw[j] & 0xFFFF0000u));
+                            for (int j = 0; j < 16; ++j) y[j] = __fmul_rn(__uint_as_float(r[16 * g + j]), scale);
+                        } else if (p.bias_bf16) {
+                            const uint4 *bp = reinterpret_cast<const uint4 *>(static_cast<const uint16_t *>(p.bias) + n);
+                            const uint4 b0 = __ldg(bp), b1 = __ldg(bp + 1);
+                            const uint32_t bw[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
+#pragma unroll
+                            for (int j = 0; j < 8; ++j) {
+                                y[2 * j] = __fmaf_rn(__uint_as_float(r[16 * g + 2 * j]), scale,
+                                                     __uint_as_float(bw[j] << 16));
+                                y[2 * j + 1] = __fmaf_rn(__uint_as_float(r[16 * g + 2 * j + 1]), scale,
+                                                         __uint_as_float(bw[j] & 0xFFFF0000u));
+                            }
+                        } else {
+                            const float4 *bp = reinterpret_cast<const float4 *>(static_cast<const float *>(p.bias) + n);
+#pragma unroll
+                            for (int j = 0; j < 4; ++j) {
+                                const float4 bb = __ldg(bp + j);
+                                y[4 * j] = __fmaf_rn(__uint_as_float(r[16 * g + 4 * j]), scale, bb.x);
+                                y[4 * j + 1] = __fmaf_rn(__uint_as_float(r[16 * g + 4 * j + 1]), scale, bb.y);
+                                y[4 * j + 2] = __fmaf_rn(__uint_as_float(r[16 * g + 4 * j + 2]), scale, bb.z);
+                                y[4 * j + 3] = __fmaf_rn(__uint_as_float(r[16 * g + 4 * j + 3]), scale, bb.w);
+                            }
                         }
-                    } else {
-                        const float4 *bp = reinterpret_cast<const float4 *>(static_cast<const float *>(p.bias) + n);
+                        if (row_ok && col_ok) {
 #pragma unroll
-                        for (int j = 0; j < 4; ++j) {
-                            const float4 b = __ldg(bp + j);
-                            y[4 * j] = __fmaf_rn(__uint_as_float(r[16 * h + 4 * j]), scale, b.x);
-                            y[4 * j + 1] = __fmaf_rn(__uint_as_float(r[16 * h + 4 * j + 1]), scale, b.y);
-                            y[4 * j + 2] = __fmaf_rn(__uint_as_float(r[16 * h + 4 * j + 2]), scale, b.z);
-                            y[4 * j + 3] = __fmaf_rn(__uint_as_float(r[16 * h + 4 * j + 3]), scale, b.w);
+                            for (int j = 0; j < 16; ++j) am = max_ignore_nan(am, fabsf(y[j]));
+                        }
+                        if (p.out_bf16) {
+#pragma unroll
+                            for (int j = 0; j < 8; ++j) packed[16 * half + 8 * g + j] = pack_bf16x2(y[2 * j], y[2 * j + 1]);
+                        } else {
+#pragma unroll
+                            for (int j = 0; j < 16; ++j) packed[16 * g + j] = __float_as_uint(y[j]);
                         }
                     }
+                }
+                // the staging box written two chunks ago must have been read by its TMA store
+                const uint32_t box = stage_box + (chunk_no & 1u) * C::EPI_BOX_BYTES;
+                if (lane == 0 && chunk_no >= 2) bulk_wait_read_le1();
+                __syncwarp();
+                const uint32_t row_addr = box + static_cast<uint32_t>(lane) * 128u;
 #pragma unroll
-                    for (int j = 0; j < 16; ++j) am = max_ignore_nan(am, fabsf(y[j]));
-                    if (p.out_bf16) {
-                        uint4 *dst = reinterpret_cast<uint4 *>(static_cast<uint16_t *>(p.out) + m * p.rows_b + n);
-                        dst[0] = make_uint4(pack_bf16x2(y[0], y[1]), pack_bf16x2(y[2], y[3]), pack_bf16x2(y[4], y[5]),
-                                            pack_bf16x2(y[6], y[7]));
-                        dst[1] = make_uint4(pack_bf16x2(y[8], y[9]), pack_bf16x2(y[10], y[11]),
-                                            pack_bf16x2(y[12], y[13]), pack_bf16x2(y[14], y[15]));
-                    } else {
-                        float4 *dst = reinterpret_cast<float4 *>(static_cast<float *>(p.out) + m * p.rows_b + n);
-#pragma unroll
-                        for (int j = 0; j < 4; ++j)
-                            dst[j] = make_float4(y[4 * j], y[4 * j + 1], y[4 * j + 2], y[4 * j + 3]);
-                    }
+                for (int j = 0; j < 8; ++j)
+                    st_shared_v4(row_addr + ((static_cast<uint32_t>(j) ^ (static_cast<uint32_t>(lane) & 7u)) << 4),
+                                 packed[4 * j], packed[4 * j + 1], packed[4 * j + 2], packed[4 * j + 3]);
+                fence_proxy_async_smem();
+                __syncwarp();
+                // boxes that start outside the output (ragged last tiles) are not stored
+                if (lane == 0 && nb * TILE_N + c < p.rows_b && warp_row0 < p.rows_a) {
+                    tma_store_2d(&tmap_out, box, nb * TILE_N + c, warp_row0);
+                    bulk_commit_group();
                 }
             }
             tc_fence_before();
@@ -521,6 +573,7 @@ gemm_fp8_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constan
                     mbar_arrive(tempty_bar(acc));
             }
         }
+        if (lane == 0) bulk_wait_all();  // stores done before the CTA's shared memory goes away
         if (p.out_amax != nullptr) {
             am = warp_max(am);
             if (p.out_bf16) am = __bfloat162float(__float2bfloat16_rn(am));  // max of the stored values
@@ -577,6 +630,23 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
     return fn;
 }
 
+// Output tensor [rows x cols] of bf16 or fp32, box 32 rows x 128 bytes, 128-byte swizzle.
+int make_out_tmap(CUtensorMap *map, void *ptr, uint64_t cols, uint64_t rows, bool bf16) {
+    auto enc = encode_fn();
+    if (enc == nullptr) return fail(FP8MP_ERR_LAUNCH, "cuTensorMapEncodeTiled is not available");
+    const uint64_t esize = bf16 ? 2 : 4;
+    const cuuint64_t dims[2] = {cols, rows};
+    const cuuint64_t strides[1] = {cols * esize};
+    const cuuint32_t box[2] = {static_cast<cuuint32_t>(128 / esize), 32};
+    const cuuint32_t estr[2] = {1, 1};
+    const CUresult r = enc(map, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, ptr,
+                           dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                           CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS)
+        return fail(FP8MP_ERR_LAUNCH, "cuTensorMapEncodeTiled (output) failed (%d)", static_cast<int>(r));
+    return FP8MP_OK;
+}
+
 // 2-D byte tensor [outer x inner], inner contiguous; box box_outer x 128 bytes.
 int make_tmap(CUtensorMap *map, const void *ptr, uint64_t inner, uint64_t outer, uint32_t box_outer) {
     auto enc = encode_fn();
@@ -608,8 +678,8 @@ struct PerDevice {
 PerDevice g_dev[64];
 
 template <bool PAIR>
-int launch_engine(const CUtensorMap &ta, const CUtensorMap &tb, const GemmParams &p, int grid, uint32_t idesc,
-                  cudaStream_t s) {
+int launch_engine(const CUtensorMap &ta, const CUtensorMap &tb, const CUtensorMap &to, const GemmParams &p, int grid,
+                  uint32_t idesc, cudaStream_t s) {
     using C = Cfg<PAIR>;
     cudaLaunchConfig_t cfg = {};
     cudaLaunchAttribute attr[1];
@@ -625,7 +695,7 @@ int launch_engine(const CUtensorMap &ta, const CUtensorMap &tb, const GemmParams
         cfg.attrs = attr;
         cfg.numAttrs = 1;
     }
-    const cudaError_t e = cudaLaunchKernelEx(&cfg, gemm_fp8_kernel<PAIR>, ta, tb, p, idesc);
+    const cudaError_t e = cudaLaunchKernelEx(&cfg, gemm_fp8_kernel<PAIR>, ta, tb, to, p, idesc);
     if (e != cudaSuccess) return fail(FP8MP_ERR_LAUNCH, "GEMM launch failed: %s", cudaGetErrorString(e));
     return FP8MP_OK;
 }
@@ -708,6 +778,9 @@ int launch_gemm(const uint8_t *a, int fmt_a, const uint8_t *b, int fmt_b, int64_
     rc = make_tmap(&tb, b, static_cast<uint64_t>(kc), static_cast<uint64_t>(rows_b),
                    pair ? Cfg<true>::ROWS_B : Cfg<false>::ROWS_B);
     if (rc) return rc;
+    CUtensorMap to;
+    rc = make_out_tmap(&to, out, static_cast<uint64_t>(rows_b), static_cast<uint64_t>(rows_a), p.out_bf16 != 0);
+    if (rc) return rc;
 
     if (pair) {
         p.tiles_m = static_cast<int>((rows_a + 255) / 256);
@@ -715,13 +788,13 @@ int launch_gemm(const uint8_t *a, int fmt_a, const uint8_t *b, int fmt_b, int64_
         if (tiles > 0x7FFFFFFF) return fail(FP8MP_ERR_INVALID, "GEMM has too many tiles");
         const int max_pairs = g_dev[dev.device & 63].max_pairs;
         const int clusters = static_cast<int>(tiles < max_pairs ? tiles : max_pairs);
-        return launch_engine<true>(ta, tb, p, 2 * clusters, make_idesc(fmt_a, fmt_b, 256), s);
+        return launch_engine<true>(ta, tb, to, p, 2 * clusters, make_idesc(fmt_a, fmt_b, 256), s);
     }
     p.tiles_m = static_cast<int>((rows_a + 127) / 128);
     const int64_t tiles = static_cast<int64_t>(p.tiles_m) * p.tiles_n;
     if (tiles > 0x7FFFFFFF) return fail(FP8MP_ERR_INVALID, "GEMM has too many tiles");
     const int grid = static_cast<int>(tiles < dev.num_sms ? tiles : dev.num_sms);
-    return launch_engine<false>(ta, tb, p, grid, make_idesc(fmt_a, fmt_b, 128), s);
+    return launch_engine<false>(ta, tb, to, p, grid, make_idesc(fmt_a, fmt_b, 128), s);
 }
 
 int read_and_clear_timeout_flag(unsigned int *value) {
