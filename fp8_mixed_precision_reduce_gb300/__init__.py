@@ -26,7 +26,7 @@ _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "libfp8mp.so")
 EXPORTS = ("fp8_quantize", "fp8_linear_fwd", "fp8_linear_dgrad", "fp8_linear_wgrad",
            "delayed_scaling_update", "mp_master_step", "fp8mp_check", "fp8mp_last_error",
-           "fp8mp_version")
+           "fp8mp_version", "fp8mp_selftest_timeout")
 
 _lib = None
 
@@ -69,10 +69,11 @@ def load(path: str | None = None):
     L.delayed_scaling_update.argtypes = [ctypes.POINTER(fp8mp_meta), I32, I32, I32, P]
     L.mp_master_step.argtypes = [P, I64, P, P, P, P, P, P, P, P, F, F, F, F, I32, P]
     L.fp8mp_check.argtypes = [P]
+    L.fp8mp_selftest_timeout.argtypes = [P]
     L.fp8mp_last_error.restype = ctypes.c_char_p
     L.fp8mp_version.restype = I32
     for name in ("fp8_quantize", "fp8_linear_fwd", "fp8_linear_dgrad", "fp8_linear_wgrad",
-                 "delayed_scaling_update", "mp_master_step", "fp8mp_check"):
+                 "delayed_scaling_update", "mp_master_step", "fp8mp_check", "fp8mp_selftest_timeout"):
         getattr(L, name).restype = ctypes.c_int
     _lib = L
     return L
@@ -199,6 +200,12 @@ def mp_master_step(grad_bf16: torch.Tensor, master: torch.Tensor, momentum: torc
 def fp8mp_check(stream=None) -> int:
     """Synchronises the stream and returns the library's check code (0 = OK)."""
     return int(load().fp8mp_check(_stream(stream)))
+
+
+def fp8mp_selftest_timeout(stream=None) -> None:
+    """Enqueues the kernel whose bounded wait runs out (about 2 s); the next
+    fp8mp_check() on the stream then returns ERR_TIMEOUT."""
+    _check(load().fp8mp_selftest_timeout(_stream(stream)))
 
 
 def fp8mp_version() -> int:

@@ -258,6 +258,14 @@ int mp_master_step(const uint16_t *grad_bf16, int64_t n, float *master, float *m
                               static_cast<cudaStream_t>(stream), dev);
 }
 
+int fp8mp_selftest_timeout(void *stream) {
+    clear_error();
+    DeviceInfo dev;
+    const int rc = current_device(&dev);
+    if (rc) return rc;
+    return launch_timeout_selftest(static_cast<cudaStream_t>(stream));
+}
+
 int fp8mp_check(void *stream) {
     clear_error();
     cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));

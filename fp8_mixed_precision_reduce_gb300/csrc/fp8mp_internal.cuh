@@ -42,6 +42,8 @@ int launch_master_step(const uint16_t *g, int64_t n, float *w, float *v, uint8_t
                        const float *scale_w, float *amax_w, float *loss_scale, int32_t *growth,
                        int32_t *found_inf, float lr, float mu, float backoff, float growth_factor,
                        int32_t growth_interval, cudaStream_t s, const DeviceInfo &dev);
+// Enqueues the one-thread kernel whose bounded wait is meant to run out.
+int launch_timeout_selftest(cudaStream_t s);
 // Reads and clears the GEMM wait-timeout flag (after a stream sync).
 int read_and_clear_timeout_flag(unsigned int *value);
 const char *last_error_message();

@@ -591,6 +591,22 @@ gemm_fp8_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constan
     if (warp == 1) tmem_dealloc<PAIR>(tmem_base, TMEM_COLS);
 }
 
+// Diagnostic of the failure path: one thread waits, with the same bounded
+// wait the GEMM roles use, on an mbarrier that nothing ever signals. The wait
+// gives up after kWaitLimitCycles and raises the device timeout flag; the
+// kernel then returns normally.
+__global__ void timeout_selftest_kernel() {
+    __shared__ __align__(8) uint64_t bar;
+    __shared__ int abort_flag;
+    if (threadIdx.x == 0) {
+        mbar_init(smem_u32(&bar), 1);
+        abort_flag = 0;
+        fence_mbar_init();
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) wait_bounded(smem_u32(&bar), 0u, &abort_flag);
+}
+
 // out = bias (or 0) broadcast over rows: the GEMM of an empty contraction.
 __global__ void fill_bias_kernel(int64_t rows, int64_t cols, const void *bias, int bias_bf16, void *out,
                                  int out_bf16, float *out_amax) {
@@ -795,6 +811,13 @@ int launch_gemm(const uint8_t *a, int fmt_a, const uint8_t *b, int fmt_b, int64_
     if (tiles > 0x7FFFFFFF) return fail(FP8MP_ERR_INVALID, "GEMM has too many tiles");
     const int grid = static_cast<int>(tiles < dev.num_sms ? tiles : dev.num_sms);
     return launch_engine<false>(ta, tb, to, p, grid, make_idesc(fmt_a, fmt_b, 128), s);
+}
+
+int launch_timeout_selftest(cudaStream_t s) {
+    timeout_selftest_kernel<<<1, 32, 0, s>>>();
+    const cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return fail(FP8MP_ERR_LAUNCH, "self-test launch failed: %s", cudaGetErrorString(e));
+    return FP8MP_OK;
 }
 
 int read_and_clear_timeout_flag(unsigned int *value) {

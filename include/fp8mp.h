@@ -217,6 +217,17 @@ int mp_master_step(const uint16_t *grad_bf16, int64_t n, float *master, float *m
  */
 int fp8mp_check(void *stream);
 
+/*
+ * fp8mp_selftest_timeout -- diagnostic of the failure path. Enqueues on
+ * `stream` a one-thread kernel that waits, with the bounded wait the GEMM
+ * kernels use, on an mbarrier nothing ever signals. After about 2 s the wait
+ * gives up and raises the device timeout flag, the kernel returns normally,
+ * and the next fp8mp_check(stream) returns FP8MP_ERR_TIMEOUT (and clears the
+ * flag). No fault, trap or hang is involved; the context stays usable.
+ * Returns 0 when enqueued.
+ */
+int fp8mp_selftest_timeout(void *stream);
+
 /* Thread-local description of the last nonzero return ("" if none). */
 const char *fp8mp_last_error(void);
 
