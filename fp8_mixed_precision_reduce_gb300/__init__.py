@@ -24,7 +24,8 @@ OK, ERR_INVALID, ERR_DEVICE, ERR_LAUNCH, ERR_TIMEOUT = 0, -1, -2, -3, -4
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "libfp8mp.so")
-EXPORTS = ("fp8_quantize", "fp8_linear_fwd", "fp8_linear_dgrad", "fp8_linear_wgrad",
+EXPORTS = ("fp8_quantize", "fp8_quantize_current", "fp8_quantize_dbias",
+           "fp8_quantize_dbias_workspace_bytes", "fp8_linear_fwd", "fp8_linear_dgrad", "fp8_linear_wgrad",
            "delayed_scaling_update", "mp_master_step", "fp8mp_check", "fp8mp_last_error",
            "fp8mp_version", "fp8mp_selftest_timeout")
 
@@ -63,6 +64,10 @@ def load(path: str | None = None):
     L = ctypes.CDLL(path)
     P, I64, I32, F = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int32, ctypes.c_float
     L.fp8_quantize.argtypes = [P, I32, I64, I64, I32, P, P, P, P, P]
+    L.fp8_quantize_current.argtypes = [P, I32, I64, I64, I32, I32, P, P, P, P, P, P]
+    L.fp8_quantize_dbias.argtypes = [P, I32, I64, I64, I32, P, P, P, P, P, I32, P, I64, P]
+    L.fp8_quantize_dbias_workspace_bytes.argtypes = [I64, I64]
+    L.fp8_quantize_dbias_workspace_bytes.restype = I64
     L.fp8_linear_fwd.argtypes = [P, P, I64, I64, I64, P, P, P, I32, P, I32, P, P]
     L.fp8_linear_dgrad.argtypes = [P, P, I64, I64, I64, I32, P, P, P, I32, P]
     L.fp8_linear_wgrad.argtypes = [P, P, I64, I64, I64, I32, P, P, P, I32, P]
@@ -72,7 +77,8 @@ def load(path: str | None = None):
     L.fp8mp_selftest_timeout.argtypes = [P]
     L.fp8mp_last_error.restype = ctypes.c_char_p
     L.fp8mp_version.restype = I32
-    for name in ("fp8_quantize", "fp8_linear_fwd", "fp8_linear_dgrad", "fp8_linear_wgrad",
+    for name in ("fp8_quantize", "fp8_quantize_current", "fp8_quantize_dbias",
+                 "fp8_linear_fwd", "fp8_linear_dgrad", "fp8_linear_wgrad",
                  "delayed_scaling_update", "mp_master_step", "fp8mp_check", "fp8mp_selftest_timeout"):
         getattr(L, name).restype = ctypes.c_int
     _lib = L
@@ -129,6 +135,33 @@ def fp8_quantize(x: torch.Tensor, fmt: int, scale: torch.Tensor, out: torch.Tens
     rows, cols = _rows_cols(x)
     _check(load().fp8_quantize(_ptr(x), _dtype_code(x), rows, cols, fmt, _ptr(scale), _ptr(out),
                                _ptr(out_t), _ptr(amax), _stream(stream)))
+
+
+def fp8_quantize_current(x: torch.Tensor, fmt: int, scale: torch.Tensor, scale_inv: torch.Tensor,
+                         amax: torch.Tensor, out: torch.Tensor, out_t: torch.Tensor | None = None,
+                         margin: int = 0, stream=None) -> None:
+    """Just-in-time scaling: amax = max|x|, scale from it (kept when the amax
+    is 0 / not finite), then out = sat_rne(x * scale) and its transpose."""
+    rows, cols = _rows_cols(x)
+    _check(load().fp8_quantize_current(_ptr(x), _dtype_code(x), rows, cols, fmt, margin, _ptr(scale),
+                                       _ptr(scale_inv), _ptr(amax), _ptr(out), _ptr(out_t), _stream(stream)))
+
+
+def fp8_quantize_dbias_workspace_bytes(rows: int, cols: int) -> int:
+    return int(load().fp8_quantize_dbias_workspace_bytes(rows, cols))
+
+
+def fp8_quantize_dbias(dy: torch.Tensor, fmt: int, scale: torch.Tensor, out: torch.Tensor,
+                       out_t: torch.Tensor, dbias: torch.Tensor, workspace: torch.Tensor,
+                       amax: torch.Tensor | None = None, stream=None) -> None:
+    """Cast of an output gradient (+ transposed copy, + amax) that also writes
+    the bias gradient dbias = column sums of dy. `workspace` is a device
+    buffer of at least fp8_quantize_dbias_workspace_bytes(rows, cols) bytes."""
+    rows, cols = _rows_cols(dy)
+    _check(load().fp8_quantize_dbias(_ptr(dy), _dtype_code(dy), rows, cols, fmt, _ptr(scale), _ptr(out),
+                                     _ptr(out_t), _ptr(amax), _ptr(dbias), _dtype_code(dbias),
+                                     _ptr(workspace), workspace.numel() * workspace.element_size(),
+                                     _stream(stream)))
 
 
 def fp8_linear_fwd(x8: torch.Tensor, w8: torch.Tensor, sinv_x: torch.Tensor, sinv_w: torch.Tensor,

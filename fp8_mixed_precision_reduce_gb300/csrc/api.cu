@@ -140,6 +140,78 @@ int fp8_quantize(const void *x, int32_t x_dtype, int64_t rows, int64_t cols, int
                            dev);
 }
 
+int fp8_quantize_current(const void *x, int32_t x_dtype, int64_t rows, int64_t cols, int32_t fmt, int32_t margin,
+                         float *scale, float *scale_inv, float *amax, uint8_t *out, uint8_t *out_t, void *stream) {
+    const char *fn = "fp8_quantize_current";
+    clear_error();
+    REQUIRE(valid_dtype(x_dtype), "%s: x_dtype %d is not FP8MP_F32 or FP8MP_BF16", fn, x_dtype);
+    REQUIRE(valid_fmt(fmt), "%s: fmt %d is not FP8MP_E4M3 or FP8MP_E5M2", fn, fmt);
+    REQUIRE(margin >= 0 && margin <= 126, "%s: margin %d outside 0..126", fn, margin);
+    REQUIRE(rows >= 0 && cols >= 0, "%s: negative size", fn);
+    REQUIRE(rows <= (1ll << 40) / (cols > 0 ? cols : 1), "%s: tensor too large", fn);
+    if (out_t != nullptr)
+        REQUIRE(rows % 16 == 0 && cols % 16 == 0,
+                "%s: with a transposed output rows and cols must be multiples of 16 (got %lld x %lld)", fn,
+                (long long)rows, (long long)cols);
+    CHECK_SCALAR(scale, true);
+    CHECK_SCALAR(scale_inv, true);
+    CHECK_SCALAR(amax, true);
+    if (rows > 0 && cols > 0) {
+        CHECK_PTR(x, true);
+        CHECK_PTR(out, true);
+        CHECK_PTR(out_t, false);
+    }
+    DeviceInfo dev;
+    const int rc = current_device(&dev);
+    if (rc) return rc;
+    return launch_quantize_current(x, x_dtype, rows, cols, fmt, margin, scale, scale_inv, amax, out, out_t,
+                                   static_cast<cudaStream_t>(stream), dev);
+}
+
+int64_t fp8_quantize_dbias_workspace_bytes(int64_t rows, int64_t cols) {
+    if (rows < 0 || cols < 0) return -1;
+    return ((rows + 127) / 128) * cols * static_cast<int64_t>(sizeof(float));
+}
+
+int fp8_quantize_dbias(const void *x, int32_t x_dtype, int64_t rows, int64_t cols, int32_t fmt, const float *scale,
+                       uint8_t *out, uint8_t *out_t, float *amax, void *dbias, int32_t dbias_dtype, float *workspace,
+                       int64_t workspace_bytes, void *stream) {
+    const char *fn = "fp8_quantize_dbias";
+    clear_error();
+    REQUIRE(valid_dtype(x_dtype), "%s: x_dtype %d is not FP8MP_F32 or FP8MP_BF16", fn, x_dtype);
+    REQUIRE(valid_dtype(dbias_dtype), "%s: dbias_dtype %d invalid", fn, dbias_dtype);
+    REQUIRE(valid_fmt(fmt), "%s: fmt %d is not FP8MP_E4M3 or FP8MP_E5M2", fn, fmt);
+    REQUIRE(rows >= 0 && cols >= 0, "%s: negative size", fn);
+    REQUIRE(rows <= (1ll << 40) / (cols > 0 ? cols : 1), "%s: tensor too large", fn);
+    REQUIRE(rows % 16 == 0 && cols % 16 == 0, "%s: rows and cols must be multiples of 16 (got %lld x %lld)", fn,
+            (long long)rows, (long long)cols);
+    if (cols == 0) return FP8MP_OK;
+    CHECK_PTR(dbias, true);
+    const int64_t need = fp8_quantize_dbias_workspace_bytes(rows, cols);
+    if (rows > 0) {
+        CHECK_PTR(x, true);
+        CHECK_PTR(out, true);
+        CHECK_PTR(out_t, true);
+        CHECK_SCALAR(scale, true);
+        CHECK_SCALAR(amax, false);
+        CHECK_PTR(workspace, true);
+        REQUIRE(workspace_bytes >= need, "%s: workspace of %lld bytes, %lld needed", fn, (long long)workspace_bytes,
+                (long long)need);
+    }
+    DeviceInfo dev;
+    const int rc = current_device(&dev);
+    if (rc) return rc;
+    if (rows == 0) {
+        const cudaError_t e =
+            cudaMemsetAsync(dbias, 0, static_cast<size_t>(cols) * (dbias_dtype == FP8MP_BF16 ? 2 : 4),
+                            static_cast<cudaStream_t>(stream));
+        if (e != cudaSuccess) return fail(FP8MP_ERR_LAUNCH, "%s: memset failed: %s", fn, cudaGetErrorString(e));
+        return FP8MP_OK;
+    }
+    return launch_quantize_dbias(x, x_dtype, rows, cols, fmt, scale, out, out_t, amax, dbias, dbias_dtype, workspace,
+                                 static_cast<cudaStream_t>(stream), dev);
+}
+
 int fp8_linear_fwd(const uint8_t *x8, const uint8_t *w8, int64_t M, int64_t N, int64_t K, const float *sinv_x,
                    const float *sinv_w, const void *bias, int32_t bias_dtype, void *y, int32_t y_dtype,
                    float *y_amax, void *stream) {

@@ -29,6 +29,12 @@ int current_device(DeviceInfo *info);
 inline bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 // Launchers (return FP8MP_* codes; arguments already validated).
+int launch_quantize_current(const void *x, int x_dtype, int64_t rows, int64_t cols, int fmt, int margin,
+                            float *scale, float *scale_inv, float *amax, uint8_t *out, uint8_t *out_t,
+                            cudaStream_t s, const DeviceInfo &dev);
+int launch_quantize_dbias(const void *x, int x_dtype, int64_t rows, int64_t cols, int fmt, const float *scale,
+                          uint8_t *out, uint8_t *out_t, float *amax, void *dbias, int dbias_dtype, float *ws,
+                          cudaStream_t s, const DeviceInfo &dev);
 int launch_quantize(const void *x, int x_dtype, int64_t rows, int64_t cols, int fmt,
                     const float *scale, uint8_t *out, uint8_t *out_t, float *amax,
                     cudaStream_t s, const DeviceInfo &dev);
@@ -53,7 +59,22 @@ const char *last_error_message();
 // Largest finite value of each format.
 __host__ __device__ constexpr float fmt_max(int fmt) { return fmt == FP8MP_E4M3 ? 448.0f : 57344.0f; }
 
+
 __device__ __forceinline__ float bf16_bits_to_f32(uint32_t h16) { return __uint_as_float(h16 << 16); }
+
+// The scale rule of delayed / current scaling: with a > 0 and finite,
+// s = fl32(fmt_max / a) * 2^-margin (one IEEE division, one exact multiply by
+// a power of two, margin 0..126); the new scale is s when s is finite and
+// > 0, otherwise the old scale is kept.
+__device__ __forceinline__ float scale_from_amax(float a, float old_scale, int fmt, int margin) {
+    float sc = old_scale;
+    if (a > 0.0f && isfinite(a)) {
+        const float s = __fdiv_rn(fmt_max(fmt), a);
+        const float s2 = __fmul_rn(s, __int_as_float((127 - margin) << 23));
+        if (isfinite(s2) && s2 > 0.0f) sc = s2;
+    }
+    return sc;
+}
 
 // Two fp32 values -> two FP8 codes with round-to-nearest-even and
 // saturation to the largest finite value (PTX cvt .satfinite). `lo` lands in

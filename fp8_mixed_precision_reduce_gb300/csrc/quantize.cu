@@ -113,11 +113,17 @@ cast_rows_kernel(const void *__restrict__ x, int64_t n, const float *__restrict_
 // Phase 2: each thread reads 16 consecutive row bytes of one column (one
 // 16-byte shared load, un-permuting the XOR) and writes them to out_t, so a
 // warp writes four full 128-byte rows of out_t.
-template <int FMT, bool BF16>
+// With DBIAS the kernel also sums its 128 rows per column (fp32, fixed order:
+// each thread its 8 rows in row order, then the 16 row groups in order) and
+// writes the 128 column sums of its tile to ws[tile_row * cols + col].
+template <int FMT, bool BF16, bool DBIAS>
 __global__ void __launch_bounds__(kThreads)
 cast_rows_t_kernel(const void *__restrict__ x, int64_t rows, int64_t cols, const float *__restrict__ scale_p,
-                   uint8_t *__restrict__ out, uint8_t *__restrict__ out_t, float *__restrict__ amax_p) {
+                   uint8_t *__restrict__ out, uint8_t *__restrict__ out_t, float *__restrict__ amax_p,
+                   float *__restrict__ ws) {
     __shared__ __align__(16) uint32_t sT[128 * 32];
+    __shared__ float s_colsum[DBIAS ? 16 * 128 : 1];
+    float csum[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
     const int64_t tiles_c = (cols + 127) >> 7;
     const int64_t r0 = (blockIdx.x / tiles_c) * 128, c0 = (blockIdx.x % tiles_c) * 128;
     const int tx = threadIdx.x & 15, ty = threadIdx.x >> 4;
@@ -141,6 +147,10 @@ cast_rows_t_kernel(const void *__restrict__ x, int64_t rows, int64_t cols, const
                                       __fmul_rn(f[6], scale), __fmul_rn(f[7], scale));
 #pragma unroll
                 for (int j = 0; j < 8; ++j) am = max_ignore_nan(am, fabsf(f[j]));
+                if constexpr (DBIAS) {
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) csum[j] = __fadd_rn(csum[j], f[j]);
+                }
                 *reinterpret_cast<uint2 *>(out + (r + q) * cols + c) = make_uint2(lo[q], hi[q]);
             }
             // 4 x 4 byte transposes: word j holds column (c + j), rows r .. r+3.
@@ -165,7 +175,18 @@ cast_rows_t_kernel(const void *__restrict__ x, int64_t rows, int64_t cols, const
             for (int j = 0; j < 8; ++j) sT[(8 * tx + j) * 32 + (g ^ sw1)] = wcol[j];
         }
     }
+    if constexpr (DBIAS) {
+#pragma unroll
+        for (int j = 0; j < 8; ++j) s_colsum[ty * 128 + 8 * tx + j] = csum[j];
+    }
     __syncthreads();
+    if constexpr (DBIAS) {
+        if (threadIdx.x < 128 && c0 + threadIdx.x < cols) {
+            float t = 0.0f;
+            for (int g = 0; g < 16; ++g) t = __fadd_rn(t, s_colsum[g * 128 + threadIdx.x]);
+            ws[(r0 >> 7) * cols + c0 + threadIdx.x] = t;
+        }
+    }
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
         const int id = threadIdx.x + kThreads * i;  // 0 .. 1023
@@ -181,9 +202,23 @@ cast_rows_t_kernel(const void *__restrict__ x, int64_t rows, int64_t cols, const
     if (amax_p != nullptr) block_amax_atomic(am, amax_p);
 }
 
+// dbias[n] = sum over tile rows t (in order) of ws[t * cols + n].
+__global__ void __launch_bounds__(kThreads)
+dbias_reduce_kernel(const float *__restrict__ ws, int64_t tile_rows, int64_t cols, void *__restrict__ dbias,
+                    int bf16_out) {
+    const int64_t n = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+    if (n >= cols) return;
+    float t = 0.0f;
+    for (int64_t r = 0; r < tile_rows; ++r) t = __fadd_rn(t, ws[r * cols + n]);
+    if (bf16_out)
+        static_cast<__nv_bfloat16 *>(dbias)[n] = __float2bfloat16_rn(t);
+    else
+        static_cast<float *>(dbias)[n] = t;
+}
+
 template <int FMT, bool BF16>
 int launch_typed(const void *x, int64_t rows, int64_t cols, const float *scale, uint8_t *out,
-                 uint8_t *out_t, float *amax, cudaStream_t s, const DeviceInfo &dev) {
+                 uint8_t *out_t, float *amax, cudaStream_t s, const DeviceInfo &dev, float *ws = nullptr) {
     if (out_t == nullptr) {
         const int64_t n = rows * cols;
         const int64_t nchunk = n >> 4;
@@ -195,15 +230,89 @@ int launch_typed(const void *x, int64_t rows, int64_t cols, const float *scale, 
     } else {
         const int64_t tiles = ((rows + 127) >> 7) * ((cols + 127) >> 7);
         if (tiles > 0x7FFFFFFF) return fail(FP8MP_ERR_INVALID, "fp8_quantize: tensor too large");
-        cast_rows_t_kernel<FMT, BF16><<<static_cast<unsigned>(tiles), kThreads, 0, s>>>(x, rows, cols, scale, out,
-                                                                                       out_t, amax);
+        if (ws != nullptr)
+            cast_rows_t_kernel<FMT, BF16, true>
+                <<<static_cast<unsigned>(tiles), kThreads, 0, s>>>(x, rows, cols, scale, out, out_t, amax, ws);
+        else
+            cast_rows_t_kernel<FMT, BF16, false>
+                <<<static_cast<unsigned>(tiles), kThreads, 0, s>>>(x, rows, cols, scale, out, out_t, amax, nullptr);
     }
     const cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return fail(FP8MP_ERR_LAUNCH, "fp8_quantize: launch failed: %s", cudaGetErrorString(e));
     return FP8MP_OK;
 }
 
+// amax pass of current scaling: max |x| over a flat array, one atomic max
+// per block into *amax (zeroed by the caller's stream just before).
+template <bool BF16>
+__global__ void __launch_bounds__(kThreads)
+amax_kernel(const void *__restrict__ x, int64_t n, float *__restrict__ amax_p) {
+    float am = 0.0f;
+    const int64_t nchunk = n >> 4;
+    const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+    for (int64_t c = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; c < nchunk; c += stride) {
+        float f[16];
+        load16<BF16>(x, c, f);
+#pragma unroll
+        for (int j = 0; j < 16; ++j) am = max_ignore_nan(am, fabsf(f[j]));
+    }
+    if (blockIdx.x == gridDim.x - 1)
+        for (int64_t i = (nchunk << 4) + threadIdx.x; i < n; i += blockDim.x) am = max_ignore_nan(am, fabsf(load1<BF16>(x, i)));
+    block_amax_atomic(am, amax_p);
+}
+
+// scale and scale_inv from this tensor's amax (the current-scaling rule).
+__global__ void current_scale_kernel(const float *__restrict__ amax, float *__restrict__ scale,
+                                     float *__restrict__ scale_inv, int fmt, int margin) {
+    const float sc = scale_from_amax(*amax, *scale, fmt, margin);
+    *scale = sc;
+    *scale_inv = __fdiv_rn(1.0f, sc);
+}
+
 }  // namespace
+
+int launch_quantize_current(const void *x, int x_dtype, int64_t rows, int64_t cols, int fmt, int margin,
+                            float *scale, float *scale_inv, float *amax, uint8_t *out, uint8_t *out_t,
+                            cudaStream_t s, const DeviceInfo &dev) {
+    cudaError_t e = cudaMemsetAsync(amax, 0, sizeof(float), s);
+    if (e != cudaSuccess) return fail(FP8MP_ERR_LAUNCH, "fp8_quantize_current: memset failed: %s", cudaGetErrorString(e));
+    const int64_t n = rows * cols;
+    int64_t blocks = ((n >> 4) + kThreads - 1) / kThreads;
+    const int64_t cap = static_cast<int64_t>(dev.num_sms) * 8;
+    if (blocks > cap) blocks = cap;
+    if (blocks < 1) blocks = 1;
+    if (x_dtype == FP8MP_BF16)
+        amax_kernel<true><<<static_cast<unsigned>(blocks), kThreads, 0, s>>>(x, n, amax);
+    else
+        amax_kernel<false><<<static_cast<unsigned>(blocks), kThreads, 0, s>>>(x, n, amax);
+    current_scale_kernel<<<1, 1, 0, s>>>(amax, scale, scale_inv, fmt, margin);
+    e = cudaGetLastError();
+    if (e != cudaSuccess)
+        return fail(FP8MP_ERR_LAUNCH, "fp8_quantize_current: launch failed: %s", cudaGetErrorString(e));
+    if (n == 0) return FP8MP_OK;
+    return launch_quantize(x, x_dtype, rows, cols, fmt, scale, out, out_t, nullptr, s, dev);
+}
+
+int launch_quantize_dbias(const void *x, int x_dtype, int64_t rows, int64_t cols, int fmt, const float *scale,
+                          uint8_t *out, uint8_t *out_t, float *amax, void *dbias, int dbias_dtype, float *ws,
+                          cudaStream_t s, const DeviceInfo &dev) {
+    const bool bf16 = x_dtype == FP8MP_BF16;
+    int rc;
+    if (fmt == FP8MP_E4M3)
+        rc = bf16 ? launch_typed<FP8MP_E4M3, true>(x, rows, cols, scale, out, out_t, amax, s, dev, ws)
+                  : launch_typed<FP8MP_E4M3, false>(x, rows, cols, scale, out, out_t, amax, s, dev, ws);
+    else
+        rc = bf16 ? launch_typed<FP8MP_E5M2, true>(x, rows, cols, scale, out, out_t, amax, s, dev, ws)
+                  : launch_typed<FP8MP_E5M2, false>(x, rows, cols, scale, out, out_t, amax, s, dev, ws);
+    if (rc) return rc;
+    const int64_t tile_rows = (rows + 127) >> 7;
+    dbias_reduce_kernel<<<static_cast<unsigned>((cols + kThreads - 1) / kThreads), kThreads, 0, s>>>(
+        ws, tile_rows, cols, dbias, dbias_dtype == FP8MP_BF16);
+    const cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess)
+        return fail(FP8MP_ERR_LAUNCH, "fp8_quantize_dbias: launch failed: %s", cudaGetErrorString(e));
+    return FP8MP_OK;
+}
 
 int launch_quantize(const void *x, int x_dtype, int64_t rows, int64_t cols, int fmt, const float *scale,
                     uint8_t *out, uint8_t *out_t, float *amax, cudaStream_t s, const DeviceInfo &dev) {

@@ -59,13 +59,7 @@ __global__ void __launch_bounds__(kThreads) scale_update_kernel(const __grid_con
         float all = 0.0f;
         for (int w = 0; w < kThreads / 32; ++w) all = fmaxf(all, red[w]);
         const float a = (b.algo == FP8MP_AMAX_MAX) ? all : cur;
-        float sc = *m.scale;
-        if (a > 0.0f && isfinite(a)) {
-            const float s = __fdiv_rn(fmt_max(m.fmt), a);
-            const float pow2 = __int_as_float((127 - b.margin) << 23);  // 2^-margin, exact
-            const float s2 = __fmul_rn(s, pow2);
-            if (isfinite(s2) && s2 > 0.0f) sc = s2;
-        }
+        const float sc = scale_from_amax(a, *m.scale, m.fmt, b.margin);
         *m.scale = sc;
         *m.scale_inv = __fdiv_rn(1.0f, sc);
         *m.cur_amax = 0.0f;

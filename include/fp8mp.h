@@ -113,6 +113,49 @@ int fp8_quantize(const void *x, int32_t x_dtype, int64_t rows, int64_t cols, int
                  const float *scale, uint8_t *out, uint8_t *out_t, float *amax, void *stream);
 
 /*
+ * fp8_quantize_current -- the same cast under just-in-time ("current")
+ * scaling ([TE-FP8] "Scaling factor 선택 전략", the just-in-time strategy:
+ * the factor comes from the amax of the tensor being cast, measured each
+ * time, instead of from the history). Three passes on `stream`:
+ *   *amax = max_{r,c} |x[r, c]|                  (over the unscaled input)
+ *   if *amax > 0 and finite: s = fl32(fmt_max / *amax) * 2^-margin, and
+ *      *scale = s when s is finite and > 0 (else *scale keeps its value);
+ *   *scale_inv = fl32(1 / *scale)
+ *   out = sat_rne_fmt(fl32(x) * *scale); out_t = its transpose (optional)
+ * This is delayed scaling with a one-entry history applied before the cast.
+ * Arguments as fp8_quantize, plus: margin 0..126; scale (in/out, device fp32,
+ * the fallback when the amax is zero or not finite); scale_inv and amax
+ * (out, device fp32; *amax is overwritten, not max-merged).
+ * Traffic: the amax pass reads x once more (bf16 + transpose: 6 B/elem).
+ */
+int fp8_quantize_current(const void *x, int32_t x_dtype, int64_t rows, int64_t cols, int32_t fmt,
+                         int32_t margin, float *scale, float *scale_inv, float *amax, uint8_t *out,
+                         uint8_t *out_t, void *stream);
+
+/*
+ * fp8_quantize_dbias -- fp8_quantize of a layer's output gradient dY, with
+ * its transposed copy, that also returns the bias gradient of the linear
+ * layer ([TE-FP8] the te.Linear(768, 768, bias=True) example under "FP8
+ * 사용방안(recipe)" and its backward under "Backward Pass 처리"; the bias
+ * gradient of y = x W^T + b is the column sum of dY):
+ *   out, out_t, *amax    exactly as fp8_quantize (out_t required here);
+ *   dbias[c] = sum_r x[r, c]  over the unscaled input, fp32 accumulation in
+ *                             a fixed order (deterministic): each 128-row
+ *                             block's column sums, then the blocks in order;
+ *                             rounded once to dbias_dtype.
+ * workspace  device scratch of at least fp8_quantize_dbias_workspace_bytes
+ *            (rows, cols) bytes, 16-byte aligned, owned by the caller; its
+ *            contents on entry do not matter and on exit are unspecified.
+ * rows, cols multiples of 16; rows == 0 gives dbias = 0.
+ */
+int fp8_quantize_dbias(const void *x, int32_t x_dtype, int64_t rows, int64_t cols, int32_t fmt,
+                       const float *scale, uint8_t *out, uint8_t *out_t, float *amax, void *dbias,
+                       int32_t dbias_dtype, float *workspace, int64_t workspace_bytes, void *stream);
+
+/* Workspace bytes fp8_quantize_dbias needs: ceil(rows / 128) * cols * 4. */
+int64_t fp8_quantize_dbias_workspace_bytes(int64_t rows, int64_t cols);
+
+/*
  * fp8_linear_fwd -- forward FP8 GEMM of a linear layer, E4M3 x E4M3.
  *
  * Defines ([PT-FP8] the torch._scaled_mm listing: two FP8 operands, their

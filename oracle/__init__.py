@@ -16,6 +16,8 @@ passage):
 * ``scale_update(hist, scale, scale_inv, cur_amax, fmt, algo, margin)``.
 * ``gemm_ref(A, fa, B, fb, sinv_a, sinv_b, bias, rows)``: fp64 reference.
 * ``master_step(...)``: unscale, overflow skip, SGD-momentum, E4M3 re-cast.
+* ``dbias(dy)``: the bias gradient (fp64 column sums) and column abs sums.
+* ``cast_current(x, fmt, margin)``: just-in-time scaling then the cast.
 """
 
 from __future__ import annotations
@@ -75,6 +77,7 @@ def _bind(path: str):
     L.orc_gemm_ref.argtypes = [P, ctypes.c_int, P, ctypes.c_int, I64, I64, I64, P, I64, D, D,
                                P, P, P]
     L.orc_master_step.argtypes = [P, I64, P, P, P, F, P, P, P, P, F, F, F, F, I32]
+    L.orc_dbias.argtypes = [P, ctypes.c_int, I64, I64, P, P]
     return L
 
 
@@ -222,6 +225,30 @@ def gemm_ref(A: np.ndarray, fmt_a: int, B: np.ndarray, fmt_b: int, sinv_a: float
                        _ptr(bias) if bias is not None else None, _ptr(out),
                        _ptr(abs_out) if abs_out is not None else None)
     return out, abs_out
+
+
+def dbias(dy: np.ndarray):
+    """(column sums, column abs sums) in fp64; dy is float32 or bf16 bits."""
+    dy = np.ascontiguousarray(dy)
+    rows, cols = dy.shape
+    out = np.empty(cols, dtype=np.float64)
+    ab = np.empty(cols, dtype=np.float64)
+    is_bf16 = 1 if dy.dtype in (np.uint16, np.int16) else 0
+    assert is_bf16 or dy.dtype == np.float32
+    lib().orc_dbias(_ptr(dy), is_bf16, rows, cols, _ptr(out), _ptr(ab))
+    return out, ab
+
+
+def cast_current(x: np.ndarray, fmt: int, margin: int = 0, scale0: float = 1.0):
+    """Just-in-time scaling: amax of this tensor, the scale rule on a one-entry
+    history (most_recent), then the cast. Returns (codes, meta)."""
+    m = Meta(1)
+    m.scale[0] = scale0
+    m.record_amax(amax(x))
+    a = np.float32(m.cur_amax[0])
+    scale_update(m, fmt, AMAX_MOST_RECENT, margin)
+    m.cur_amax[0] = a  # report this tensor's amax, as the cast does
+    return cast(x, float(m.scale[0]), fmt), m
 
 
 class LossScaleState:

@@ -403,3 +403,29 @@ void orc_master_step(const uint16_t *g, int64_t n, float *w, float *v, uint8_t *
         *growth = 0;
     }
 }
+
+/* ------------------------------------------------------------------------ */
+/* Bias gradient of the linear layer y = x W^T + b (the te.Linear example   */
+/* with bias=True under [TE-FP8] "FP8 사용방안(recipe)", backward under      */
+/* "Backward Pass 처리"): db[c] = sum_r dy[r, c], a plain fp64 column sum of */
+/* the unscaled gradient; abs_out[c] = sum_r |dy[r, c]| bounds the rounding  */
+/* error of any fp32 summation order. dy is fp32 (is_bf16 = 0) or bf16 bits. */
+/* ------------------------------------------------------------------------ */
+
+void orc_dbias(const void *dy, int is_bf16, int64_t rows, int64_t cols, double *out, double *abs_out)
+{
+    int64_t c;
+#pragma omp parallel for schedule(static)
+    for (c = 0; c < cols; ++c) {
+        double s = 0.0, a = 0.0;
+        for (int64_t r = 0; r < rows; ++r) {
+            const double v = is_bf16 ? (double)bf16_to_f32(((const uint16_t *)dy)[r * cols + c])
+                                     : (double)((const float *)dy)[r * cols + c];
+            s += v;
+            a += fabs(v);
+        }
+        out[c] = s;
+        if (abs_out)
+            abs_out[c] = a;
+    }
+}

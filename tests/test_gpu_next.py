@@ -1,0 +1,98 @@
+"""GPU parity of the widened rows: just-in-time (current) scaling and the
+bias gradient fused into the output-gradient cast."""
+
+import numpy as np
+import pytest
+import torch
+
+import workloads
+from gpu_util import E4M3, E5M2, assert_same_bits, np_view
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.mark.parametrize("rows,cols", [(16, 16), (1040, 784), (1024, 768), (4096, 4096)])
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
+@pytest.mark.parametrize("fmt", [E4M3, E5M2])
+def test_current_scaling(cuda_lib, orc, rows, cols, dtype, fmt):
+    g = workloads.gen(rows + cols + fmt)
+    x = (torch.randn((rows, cols), generator=g) * 5).to(dtype)
+    xn = np_view(x)
+    for margin in (0, 2):
+        scale = torch.tensor([0.5], device="cuda")
+        sinv = torch.empty(1, device="cuda")
+        am = torch.full((1,), 123.0, device="cuda")
+        out = torch.empty((rows, cols), dtype=torch.uint8, device="cuda")
+        out_t = torch.empty((cols, rows), dtype=torch.uint8, device="cuda")
+        cuda_lib.fp8_quantize_current(x.cuda(), fmt, scale, sinv, am, out, out_t, margin=margin)
+        assert cuda_lib.fp8mp_check() == 0
+        q, m = orc.cast_current(xn, fmt, margin=margin, scale0=0.5)
+        assert_same_bits(out.cpu().numpy(), q, "codes")
+        assert_same_bits(out_t.cpu().numpy(), orc.transpose_u8(q), "transposed")
+        assert_same_bits(np_view(scale), m.scale, "scale")
+        assert_same_bits(np_view(sinv), m.scale_inv, "scale_inv")
+        assert_same_bits(np_view(am), m.cur_amax, "amax")
+
+
+def test_current_scaling_degenerate(cuda_lib, orc):
+    for fill in (0.0, float("inf"), float("nan")):
+        x = torch.full((32, 32), fill, dtype=torch.float32)
+        scale = torch.tensor([3.0], device="cuda")
+        sinv = torch.empty(1, device="cuda")
+        am = torch.empty(1, device="cuda")
+        out = torch.empty((32, 32), dtype=torch.uint8, device="cuda")
+        cuda_lib.fp8_quantize_current(x.cuda(), E4M3, scale, sinv, am, out)
+        assert cuda_lib.fp8mp_check() == 0
+        q, m = orc.cast_current(np_view(x), E4M3, scale0=3.0)
+        assert scale.item() == 3.0 and m.scale[0] == 3.0
+        assert_same_bits(out.cpu().numpy(), q, f"codes fill={fill}")
+        assert_same_bits(np_view(am), m.cur_amax, "amax")
+
+
+def dbias_check(got, ref, ab, rows, bf16):
+    """fp32 summation of `rows` terms in any order is off by at most
+    rows * 2^-24 * sum|x|; a bf16 result adds one round-to-nearest of a value
+    with an 8-bit significand: at most 2^-8 |ref| (its unit roundoff)."""
+    err = np.abs(got.astype(np.float64) - ref)
+    bound = rows * 2.0 ** -24 * ab + (2.0 ** -8 * (np.abs(ref) + rows * 2.0 ** -24 * ab) if bf16 else 0.0) + 1e-30
+    assert (err <= bound).all(), (err / bound).max()
+
+
+@pytest.mark.parametrize("rows,cols", [(16, 16), (144, 272), (1040, 784), (8192, 4096)])
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
+@pytest.mark.parametrize("db_dtype", [torch.float32, torch.bfloat16])
+def test_dbias_fused_in_gradient_cast(cuda_lib, orc, rows, cols, dtype, db_dtype):
+    g = workloads.gen(7 * rows + cols)
+    dy = (torch.randn((rows, cols), generator=g) * 1e-3 + 2e-4).to(dtype)
+    dyn = np_view(dy)
+    scale = torch.tensor([4096.0], device="cuda")
+    out = torch.empty((rows, cols), dtype=torch.uint8, device="cuda")
+    out_t = torch.empty((cols, rows), dtype=torch.uint8, device="cuda")
+    am = torch.zeros(1, device="cuda")
+    db = torch.empty(cols, dtype=db_dtype, device="cuda")
+    ws = torch.empty(cuda_lib.fp8_quantize_dbias_workspace_bytes(rows, cols) // 4, dtype=torch.float32,
+                     device="cuda")
+    cuda_lib.fp8_quantize_dbias(dy.cuda(), E5M2, scale, out, out_t, db, ws, amax=am)
+    assert cuda_lib.fp8mp_check() == 0
+    q = orc.cast(dyn, 4096.0, E5M2)
+    assert_same_bits(out.cpu().numpy(), q, "codes")
+    assert_same_bits(out_t.cpu().numpy(), orc.transpose_u8(q), "transposed")
+    assert_same_bits(np_view(am), np.array([orc.amax(dyn)], np.float32), "amax")
+    ref, ab = orc.dbias(dyn)
+    dbias_check(np_view(db.float()), ref, ab, rows, db_dtype == torch.bfloat16)
+    # deterministic: a second call gives the same bits
+    db2 = torch.empty_like(db)
+    cuda_lib.fp8_quantize_dbias(dy.cuda(), E5M2, scale, out, out_t, db2, ws, amax=am)
+    assert cuda_lib.fp8mp_check() == 0
+    assert torch.equal(db.view(torch.uint8) if db.dtype == torch.uint8 else db, db2)
+
+
+def test_dbias_rejects_small_workspace(cuda_lib):
+    dy = torch.ones((256, 64), dtype=torch.bfloat16, device="cuda")
+    out = torch.empty((256, 64), dtype=torch.uint8, device="cuda")
+    out_t = torch.empty((64, 256), dtype=torch.uint8, device="cuda")
+    db = torch.empty(64, device="cuda")
+    ws = torch.empty(16, device="cuda")
+    with pytest.raises(cuda_lib.Fp8mpError) as e:
+        cuda_lib.fp8_quantize_dbias(dy, E5M2, torch.ones(1, device="cuda"), out, out_t, db, ws)
+    assert e.value.code == cuda_lib.ERR_INVALID and "workspace" in cuda_lib.last_error()

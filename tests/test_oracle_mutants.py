@@ -51,6 +51,9 @@ MUTANTS = [
     ("recast ignores scale_w", "orc_encode(ORC_E4M3, wn * scale_w)", "orc_encode(ORC_E4M3, wn)"),
     ("recast as E5M2", "orc_encode(ORC_E4M3, wn * scale_w)", "orc_encode(ORC_E5M2, wn * scale_w)"),
     ("NaN gradient missed", "if ((g[i] & 0x7F80u) == 0x7F80u)", "if (g[i] == 0x7F80u)"),
+    ("dbias sums a transposed view", "((const uint16_t *)dy)[r * cols + c]", "((const uint16_t *)dy)[c * rows + r]"),
+    ("dbias drops its last row", "for (int64_t r = 0; r < rows; ++r) {\n            const double v = is_bf16",
+     "for (int64_t r = 0; r + 1 < rows; ++r) {\n            const double v = is_bf16"),
 ]
 
 
@@ -81,6 +84,8 @@ def _pins():
         ("master_nan_alone", lambda: gm.test_master_step_each_nonfinite_kind_alone_skips(oracle, 0xFFC1)),
         ("master_neginf_alone", lambda: gm.test_master_step_each_nonfinite_kind_alone_skips(oracle, 0xFF80)),
         ("master_torch_sgd", lambda: gm.test_master_step_vs_torch_sgd_momentum(oracle)),
+        ("dbias", lambda: sc.test_dbias_definition(oracle)),
+        ("current_scaling", lambda: sc.test_current_scaling_maps_amax_to_fmt_max(oracle)),
     ]
     return p
 

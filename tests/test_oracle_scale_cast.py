@@ -142,3 +142,35 @@ def test_history_window_is_last_L(orc):
         scales.append(float(m.scale[0]))
     assert scales[:L] == [44.8 if False else float(np.float32(448.0) / np.float32(10.0))] * L
     assert scales[L] == 448.0 and scales[L + 1] == 448.0
+
+
+# ------------------------------------------------------ current scaling, dbias
+
+
+def test_current_scaling_maps_amax_to_fmt_max(orc):
+    rng = np.random.default_rng(31)
+    for fmt in (E4M3, E5M2):
+        x = (rng.standard_normal((64, 48)) * 7).astype(np.float32)
+        q, m = orc.cast_current(x, fmt)
+        i = np.unravel_index(np.argmax(np.abs(x)), x.shape)
+        assert orc.decode(fmt, q[i]) == np.sign(x[i]) * orc.fmt_max(fmt)
+        assert m.cur_amax[0] == np.abs(x).max()
+        assert m.scale[0] == np.float32(orc.fmt_max(fmt)) / np.float32(np.abs(x).max())
+    q, m = orc.cast_current(np.zeros((16, 16), np.float32), E4M3, scale0=3.0)
+    assert m.scale[0] == 3.0 and (q == 0).all()
+
+
+def test_dbias_definition(orc):
+    rng = np.random.default_rng(32)
+    # small integers: every summation order is exact
+    dy = rng.integers(-40, 40, (300, 48)).astype(np.float32)
+    s, a = orc.dbias(dy)
+    assert (s == dy.astype(np.int64).sum(axis=0)).all()
+    assert (a == np.abs(dy).sum(axis=0)).all()
+    # bf16 bits against a library fp64 sum of the widened values
+    xb = torch.from_numpy(rng.standard_normal((257, 33)).astype(np.float32)).to(torch.bfloat16)
+    bits = xb.view(torch.int16).numpy().view(np.uint16)
+    s, _ = orc.dbias(bits)
+    np.testing.assert_allclose(s, xb.double().sum(0).numpy(), rtol=1e-13, atol=1e-13)
+    # columns, not rows
+    assert not np.allclose(s[:33], xb.double().sum(1).numpy()[:33])
