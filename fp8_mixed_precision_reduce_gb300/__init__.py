@@ -25,7 +25,7 @@ OK, ERR_INVALID, ERR_DEVICE, ERR_LAUNCH, ERR_TIMEOUT = 0, -1, -2, -3, -4
 _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "libfp8mp.so")
 EXPORTS = ("fp8_quantize", "fp8_quantize_current", "fp8_quantize_dbias",
-           "fp8_quantize_dbias_workspace_bytes", "fp8_linear_fwd", "fp8_linear_dgrad", "fp8_linear_wgrad",
+           "fp8_quantize_dbias_workspace_bytes", "fp8_quantize_dbias_noalloc", "fp8_linear_fwd", "fp8_linear_dgrad", "fp8_linear_wgrad",
            "delayed_scaling_update", "mp_master_step", "fp8mp_check", "fp8mp_last_error",
            "fp8mp_version", "fp8mp_selftest_timeout")
 
@@ -66,6 +66,7 @@ def load(path: str | None = None):
     L.fp8_quantize.argtypes = [P, I32, I64, I64, I32, P, P, P, P, P]
     L.fp8_quantize_current.argtypes = [P, I32, I64, I64, I32, I32, P, P, P, P, P, P]
     L.fp8_quantize_dbias.argtypes = [P, I32, I64, I64, I32, P, P, P, P, P, I32, P, I64, P]
+    L.fp8_quantize_dbias_noalloc.argtypes = [P, I32, I64, I64, I32, P, P, P, P, P, I32, P]
     L.fp8_quantize_dbias_workspace_bytes.argtypes = [I64, I64]
     L.fp8_quantize_dbias_workspace_bytes.restype = I64
     L.fp8_linear_fwd.argtypes = [P, P, I64, I64, I64, P, P, P, I32, P, I32, P, P]
@@ -77,7 +78,7 @@ def load(path: str | None = None):
     L.fp8mp_selftest_timeout.argtypes = [P]
     L.fp8mp_last_error.restype = ctypes.c_char_p
     L.fp8mp_version.restype = I32
-    for name in ("fp8_quantize", "fp8_quantize_current", "fp8_quantize_dbias",
+    for name in ("fp8_quantize", "fp8_quantize_current", "fp8_quantize_dbias", "fp8_quantize_dbias_noalloc",
                  "fp8_linear_fwd", "fp8_linear_dgrad", "fp8_linear_wgrad",
                  "delayed_scaling_update", "mp_master_step", "fp8mp_check", "fp8mp_selftest_timeout"):
         getattr(L, name).restype = ctypes.c_int
@@ -162,6 +163,22 @@ def fp8_quantize_dbias(dy: torch.Tensor, fmt: int, scale: torch.Tensor, out: tor
                                      _ptr(out_t), _ptr(amax), _ptr(dbias), _dtype_code(dbias),
                                      _ptr(workspace), workspace.numel() * workspace.element_size(),
                                      _stream(stream)))
+
+
+NOALLOC_DBIAS_SCRATCH_FLOATS = 1 << 20
+
+
+def fp8_quantize_dbias_noalloc(dy: torch.Tensor, fmt: int, scale: torch.Tensor, out: torch.Tensor,
+                               out_t: torch.Tensor, dbias: torch.Tensor, amax: torch.Tensor | None = None,
+                               stream=None) -> None:
+    """fp8_quantize_dbias without a workspace, for callers that cannot
+    allocate device memory: the partial sums live in a fixed 4 MiB array in
+    the library (ceil(rows/128) * cols <= 2^20). The first call on a device
+    looks up that array's address; calls that overlap on the GPU race on it."""
+    rows, cols = _rows_cols(dy)
+    _check(load().fp8_quantize_dbias_noalloc(_ptr(dy), _dtype_code(dy), rows, cols, fmt, _ptr(scale), _ptr(out),
+                                             _ptr(out_t), _ptr(amax), _ptr(dbias), _dtype_code(dbias),
+                                             _stream(stream)))
 
 
 def fp8_linear_fwd(x8: torch.Tensor, w8: torch.Tensor, sinv_x: torch.Tensor, sinv_w: torch.Tensor,

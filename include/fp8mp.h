@@ -155,6 +155,37 @@ int fp8_quantize_dbias(const void *x, int32_t x_dtype, int64_t rows, int64_t col
 /* Workspace bytes fp8_quantize_dbias needs: ceil(rows / 128) * cols * 4. */
 int64_t fp8_quantize_dbias_workspace_bytes(int64_t rows, int64_t cols);
 
+/* Floats in the fixed scratch array of fp8_quantize_dbias_noalloc (4 MiB). */
+#define FP8MP_NOALLOC_DBIAS_SCRATCH_FLOATS (1 << 20)
+
+/*
+ * fp8_quantize_dbias_noalloc -- fp8_quantize_dbias for callers that cannot
+ * allocate device memory. The pages have no counterpart: this entry point
+ * exists for callers that are not allowed to call cudaMalloc -- code running
+ * inside a framework whose memory pool owns the device, plugin code handed
+ * only input and output pointers, and latency-critical paths that cannot
+ * take the implicit device synchronisation of cudaMalloc / cudaFree.
+ *
+ * Same arguments and results as fp8_quantize_dbias, minus the workspace:
+ * the per-block partial sums live in a file-scope device array of
+ * FP8MP_NOALLOC_DBIAS_SCRATCH_FLOATS floats inside the library, which every
+ * GPU that loads the library holds until the process exits. The call
+ * allocates nothing (no cudaMalloc, cudaFree or allocating library routine).
+ *   - Limit: ceil(rows / 128) * cols <= FP8MP_NOALLOC_DBIAS_SCRATCH_FLOATS
+ *     (for example rows 16384 with cols up to 8192); larger shapes return
+ *     FP8MP_ERR_INVALID with a message naming the limit.
+ *   - The first call on a device looks up the array's device address
+ *     (cudaGetSymbolAddress, with that device current) and caches it; make
+ *     that first call before any stream capture.
+ *   - Every call shares the one array and leaves its partial sums there
+ *     (each call writes every entry it reads, so nothing needs clearing).
+ *     Calls whose work overlaps on the GPU (other streams, other threads)
+ *     race on the array: serialise them, e.g. on one stream.
+ */
+int fp8_quantize_dbias_noalloc(const void *x, int32_t x_dtype, int64_t rows, int64_t cols, int32_t fmt,
+                               const float *scale, uint8_t *out, uint8_t *out_t, float *amax, void *dbias,
+                               int32_t dbias_dtype, void *stream);
+
 /*
  * fp8_linear_fwd -- forward FP8 GEMM of a linear layer, E4M3 x E4M3.
  *
