@@ -25,8 +25,8 @@ OK, ERR_INVALID, ERR_DEVICE, ERR_LAUNCH, ERR_TIMEOUT = 0, -1, -2, -3, -4
 _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "libfp8mp.so")
 EXPORTS = ("fp8_quantize", "fp8_quantize_current", "fp8_quantize_dbias",
-           "fp8_quantize_dbias_workspace_bytes", "fp8_quantize_dbias_noalloc", "fp8_linear_fwd", "fp8_linear_dgrad", "fp8_linear_wgrad",
-           "delayed_scaling_update", "mp_master_step", "fp8mp_check", "fp8mp_last_error",
+           "fp8_quantize_dbias_workspace_bytes", "fp8_quantize_dbias_noalloc", "fp8_linear_fwd", "fp8_linear_fwd_fp8out", "fp8_linear_dgrad", "fp8_linear_wgrad",
+           "delayed_scaling_update", "mp_master_step", "mp_master_step_adam", "fp8mp_check", "fp8mp_last_error",
            "fp8mp_version", "fp8mp_selftest_timeout")
 
 _lib = None
@@ -70,17 +70,20 @@ def load(path: str | None = None):
     L.fp8_quantize_dbias_workspace_bytes.argtypes = [I64, I64]
     L.fp8_quantize_dbias_workspace_bytes.restype = I64
     L.fp8_linear_fwd.argtypes = [P, P, I64, I64, I64, P, P, P, I32, P, I32, P, P]
+    L.fp8_linear_fwd_fp8out.argtypes = [P, P, I64, I64, I64, P, P, P, I32, P, I32, P, P, P]
     L.fp8_linear_dgrad.argtypes = [P, P, I64, I64, I64, I32, P, P, P, I32, P]
     L.fp8_linear_wgrad.argtypes = [P, P, I64, I64, I64, I32, P, P, P, I32, P]
     L.delayed_scaling_update.argtypes = [ctypes.POINTER(fp8mp_meta), I32, I32, I32, P]
     L.mp_master_step.argtypes = [P, I64, P, P, P, P, P, P, P, P, F, F, F, F, I32, P]
+    L.mp_master_step_adam.argtypes = [P, I64, P, P, P, P, P, P, P, P, P, P, F, F, F, F, F, F, I32, P]
     L.fp8mp_check.argtypes = [P]
     L.fp8mp_selftest_timeout.argtypes = [P]
     L.fp8mp_last_error.restype = ctypes.c_char_p
     L.fp8mp_version.restype = I32
     for name in ("fp8_quantize", "fp8_quantize_current", "fp8_quantize_dbias", "fp8_quantize_dbias_noalloc",
-                 "fp8_linear_fwd", "fp8_linear_dgrad", "fp8_linear_wgrad",
-                 "delayed_scaling_update", "mp_master_step", "fp8mp_check", "fp8mp_selftest_timeout"):
+                 "fp8_linear_fwd", "fp8_linear_fwd_fp8out", "fp8_linear_dgrad", "fp8_linear_wgrad",
+                 "delayed_scaling_update", "mp_master_step", "mp_master_step_adam", "fp8mp_check",
+                 "fp8mp_selftest_timeout"):
         getattr(L, name).restype = ctypes.c_int
     _lib = L
     return L
@@ -192,6 +195,18 @@ def fp8_linear_fwd(x8: torch.Tensor, w8: torch.Tensor, sinv_x: torch.Tensor, sin
                                  _ptr(y_amax), _stream(stream)))
 
 
+def fp8_linear_fwd_fp8out(x8: torch.Tensor, w8: torch.Tensor, sinv_x: torch.Tensor, sinv_w: torch.Tensor,
+                          y_scale: torch.Tensor, y8: torch.Tensor, y_fmt: int = E4M3,
+                          bias: torch.Tensor | None = None, y_amax: torch.Tensor | None = None,
+                          stream=None) -> None:
+    """y8 = FP8 codes of ((x8 . w8^T) * sinv_x * sinv_w + bias) * y_scale."""
+    M, K = x8.shape
+    N = w8.shape[0]
+    _check(load().fp8_linear_fwd_fp8out(_ptr(x8), _ptr(w8), M, N, K, _ptr(sinv_x), _ptr(sinv_w), _ptr(bias),
+                                        _dtype_code(bias) if bias is not None else F32, _ptr(y_scale), y_fmt,
+                                        _ptr(y8), _ptr(y_amax), _stream(stream)))
+
+
 def fp8_linear_dgrad(dy8: torch.Tensor, w8t: torch.Tensor, sinv_dy: torch.Tensor,
                      sinv_w: torch.Tensor, dx: torch.Tensor, dy_fmt: int = E5M2, stream=None) -> None:
     """dx[M, K] = (dy8[M, N] . w8t[K, N]^T) * sinv_dy * sinv_w."""
@@ -245,6 +260,21 @@ def mp_master_step(grad_bf16: torch.Tensor, master: torch.Tensor, momentum: torc
                                  _ptr(scale_w), _ptr(amax_w), _ptr(loss_scale), _ptr(growth_tracker),
                                  _ptr(found_inf), float(lr), float(momentum_coef), float(backoff),
                                  float(growth_factor), int(growth_interval), _stream(stream)))
+
+
+def mp_master_step_adam(grad_bf16: torch.Tensor, master: torch.Tensor, exp_avg: torch.Tensor,
+                        exp_avg_sq: torch.Tensor, w8: torch.Tensor, scale_w: torch.Tensor, amax_w: torch.Tensor,
+                        loss_scale: torch.Tensor, growth_tracker: torch.Tensor, found_inf: torch.Tensor,
+                        beta_pows: torch.Tensor, lr: float, beta1: float = 0.9, beta2: float = 0.999,
+                        eps: float = 1e-8, backoff: float = 0.5, growth_factor: float = 2.0,
+                        growth_interval: int = 2000, stream=None) -> None:
+    """Unscale, overflow skip, FP32 Adam update and E4M3 re-cast, in place."""
+    n = grad_bf16.numel()
+    _check(load().mp_master_step_adam(_ptr(grad_bf16), n, _ptr(master), _ptr(exp_avg), _ptr(exp_avg_sq), _ptr(w8),
+                                      _ptr(scale_w), _ptr(amax_w), _ptr(loss_scale), _ptr(growth_tracker),
+                                      _ptr(found_inf), _ptr(beta_pows), float(lr), float(beta1), float(beta2),
+                                      float(eps), float(backoff), float(growth_factor), int(growth_interval),
+                                      _stream(stream)))
 
 
 def fp8mp_check(stream=None) -> int:

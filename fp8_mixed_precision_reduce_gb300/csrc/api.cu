@@ -238,6 +238,33 @@ int fp8_linear_fwd(const uint8_t *x8, const uint8_t *w8, int64_t M, int64_t N, i
                        y_amax, static_cast<cudaStream_t>(stream), dev);
 }
 
+int fp8_linear_fwd_fp8out(const uint8_t *x8, const uint8_t *w8, int64_t M, int64_t N, int64_t K, const float *sinv_x,
+                          const float *sinv_w, const void *bias, int32_t bias_dtype, const float *y_scale,
+                          int32_t y_fmt, uint8_t *y8, float *y_amax, void *stream) {
+    const char *fn = "fp8_linear_fwd_fp8out";
+    clear_error();
+    int rc = check_gemm_dims(fn, M, N, K);
+    if (rc) return rc;
+    REQUIRE(valid_fmt(y_fmt), "%s: y_fmt %d invalid", fn, y_fmt);
+    REQUIRE(bias == nullptr || valid_dtype(bias_dtype), "%s: bias_dtype %d invalid", fn, bias_dtype);
+    if (M == 0 || N == 0) return FP8MP_OK;
+    CHECK_PTR(y8, true);
+    CHECK_PTR(bias, false);
+    CHECK_SCALAR(y_amax, false);
+    CHECK_SCALAR(y_scale, true);
+    CHECK_SCALAR(sinv_x, true);
+    CHECK_SCALAR(sinv_w, true);
+    if (K > 0) {
+        CHECK_PTR(x8, true);
+        CHECK_PTR(w8, true);
+    }
+    DeviceInfo dev;
+    rc = current_device(&dev);
+    if (rc) return rc;
+    return launch_gemm(x8, FP8MP_E4M3, w8, FP8MP_E4M3, M, N, K, sinv_x, sinv_w, bias, bias_dtype, y8, FP8MP_F32,
+                       y_amax, static_cast<cudaStream_t>(stream), dev, y_scale, y_fmt);
+}
+
 int fp8_linear_dgrad(const uint8_t *dy8, const uint8_t *w8t, int64_t M, int64_t N, int64_t K, int32_t dy_fmt,
                      const float *sinv_dy, const float *sinv_w, void *dx, int32_t dx_dtype, void *stream) {
     const char *fn = "fp8_linear_dgrad";
@@ -328,6 +355,34 @@ int mp_master_step(const uint16_t *grad_bf16, int64_t n, float *master, float *m
     return launch_master_step(grad_bf16, n, master, momentum, w8, scale_w, amax_w, loss_scale, growth_tracker,
                               found_inf, lr, momentum_coef, backoff, growth_factor, growth_interval,
                               static_cast<cudaStream_t>(stream), dev);
+}
+
+int mp_master_step_adam(const uint16_t *grad_bf16, int64_t n, float *master, float *exp_avg, float *exp_avg_sq,
+                        uint8_t *w8, const float *scale_w, float *amax_w, float *loss_scale, int32_t *growth_tracker,
+                        int32_t *found_inf, float *beta_pows, float lr, float beta1, float beta2, float eps,
+                        float backoff, float growth_factor, int32_t growth_interval, void *stream) {
+    const char *fn = "mp_master_step_adam";
+    clear_error();
+    REQUIRE(n >= 0 && n <= (1ll << 40), "%s: n = %lld out of range", fn, (long long)n);
+    REQUIRE(growth_interval >= 1, "%s: growth_interval must be >= 1", fn);
+    REQUIRE(beta1 >= 0.0f && beta1 < 1.0f && beta2 >= 0.0f && beta2 < 1.0f, "%s: betas must lie in [0, 1)", fn);
+    CHECK_PTR(grad_bf16, n > 0);
+    CHECK_PTR(master, n > 0);
+    CHECK_PTR(exp_avg, n > 0);
+    CHECK_PTR(exp_avg_sq, n > 0);
+    CHECK_PTR(w8, n > 0);
+    CHECK_SCALAR(scale_w, true);
+    CHECK_SCALAR(amax_w, true);
+    CHECK_SCALAR(loss_scale, true);
+    CHECK_SCALAR(growth_tracker, true);
+    CHECK_SCALAR(found_inf, true);
+    CHECK_SCALAR(beta_pows, true);
+    DeviceInfo dev;
+    const int rc = current_device(&dev);
+    if (rc) return rc;
+    return launch_adam_step(grad_bf16, n, master, exp_avg, exp_avg_sq, w8, scale_w, amax_w, loss_scale,
+                            growth_tracker, found_inf, beta_pows, lr, beta1, beta2, eps, backoff, growth_factor,
+                            growth_interval, static_cast<cudaStream_t>(stream), dev);
 }
 
 int fp8mp_selftest_timeout(void *stream) {

@@ -41,13 +41,18 @@ int launch_quantize(const void *x, int x_dtype, int64_t rows, int64_t cols, int 
 int launch_gemm(const uint8_t *a, int fmt_a, const uint8_t *b, int fmt_b, int64_t rows_a,
                 int64_t rows_b, int64_t kc, const float *sinv_a, const float *sinv_b,
                 const void *bias, int bias_dtype, void *out, int out_dtype, float *out_amax,
-                cudaStream_t s, const DeviceInfo &dev);
+                cudaStream_t s, const DeviceInfo &dev, const float *out_scale = nullptr,
+                int out_fmt = FP8MP_E4M3);
 int launch_scale_update(const fp8mp_meta *metas, int32_t n, int32_t algo, int32_t margin,
                         cudaStream_t s);
 int launch_master_step(const uint16_t *g, int64_t n, float *w, float *v, uint8_t *w8,
                        const float *scale_w, float *amax_w, float *loss_scale, int32_t *growth,
                        int32_t *found_inf, float lr, float mu, float backoff, float growth_factor,
                        int32_t growth_interval, cudaStream_t s, const DeviceInfo &dev);
+int launch_adam_step(const uint16_t *g, int64_t n, float *w, float *m, float *v, uint8_t *w8, const float *scale_w,
+                     float *amax_w, float *loss_scale, int32_t *growth, int32_t *found_inf, float *beta_pows,
+                     float lr, float b1, float b2, float eps, float backoff, float growth_factor,
+                     int32_t growth_interval, cudaStream_t s, const DeviceInfo &dev);
 // Enqueues the one-thread kernel whose bounded wait is meant to run out.
 int launch_timeout_selftest(cudaStream_t s);
 // Reads and clears the GEMM wait-timeout flag (after a stream sync).

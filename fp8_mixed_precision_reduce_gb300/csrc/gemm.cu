@@ -101,6 +101,9 @@ struct GemmParams {
     int bias_bf16;
     void *out;
     int out_bf16;
+    int out_fp8;              // output as FP8 codes of out_fmt under *out_scale
+    int out_fmt;
+    const float *out_scale;
     float *out_amax;
 };
 
@@ -475,7 +478,9 @@ gemm_fp8_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constan
         const int q = warp & 3;  // this warp may access TMEM lanes 32q .. 32q+31
         const int row_in_tile = static_cast<int>(rank) * ROWS_A + q * 32 + lane;
         const float scale = __fmul_rn(__ldg(p.sinv_a), __ldg(p.sinv_b));
-        const int box_cols = p.out_bf16 ? 64 : 32;
+        const int box_cols = p.out_fp8 ? 128 : (p.out_bf16 ? 64 : 32);  // 128 bytes per row either way
+        const int parts = box_cols / 32;                                 // tcgen05.ld of 32 columns each
+        const float out_scale = p.out_fp8 ? __ldg(p.out_scale) : 1.0f;
         const uint32_t stage_box = base + C::EPI_OFFSET + static_cast<uint32_t>((warp - 2) * 2 * C::EPI_BOX_BYTES);
         float am = 0.0f;
         int lt = 0;
@@ -497,8 +502,8 @@ gemm_fp8_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constan
             for (int c = 0; c < TILE_N; c += box_cols, ++chunk_no) {
                 uint32_t packed[32];  // this lane's 128-byte row of the box
 #pragma unroll
-                for (int half = 0; half < 2; ++half) {
-                    if (half == 1 && !p.out_bf16) break;
+                for (int half = 0; half < 4; ++half) {
+                    if (half >= parts) break;
                     uint32_t r[32];
                     const int c32 = c + 32 * half;
                     tmem_ld32(tmem_base + static_cast<uint32_t>(acc * TILE_N + c32) +
@@ -538,7 +543,15 @@ gemm_fp8_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constan
 #pragma unroll
                             for (int j = 0; j < 16; ++j) am = max_ignore_nan(am, fabsf(y[j]));
                         }
-                        if (p.out_bf16) {
+                        if (p.out_fp8) {
+#pragma unroll
+                            for (int j = 0; j < 4; ++j) {
+                                const float a0 = __fmul_rn(y[4 * j], out_scale), a1 = __fmul_rn(y[4 * j + 1], out_scale);
+                                const float a2 = __fmul_rn(y[4 * j + 2], out_scale), a3 = __fmul_rn(y[4 * j + 3], out_scale);
+                                packed[8 * half + 4 * g + j] = p.out_fmt == FP8MP_E4M3 ? cvt_quad<FP8MP_E4M3>(a0, a1, a2, a3)
+                                                                                      : cvt_quad<FP8MP_E5M2>(a0, a1, a2, a3);
+                            }
+                        } else if (p.out_bf16) {
 #pragma unroll
                             for (int j = 0; j < 8; ++j) packed[16 * half + 8 * g + j] = pack_bf16x2(y[2 * j], y[2 * j + 1]);
                         } else {
@@ -576,7 +589,7 @@ gemm_fp8_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constan
         if (lane == 0) bulk_wait_all();  // stores done before the CTA's shared memory goes away
         if (p.out_amax != nullptr) {
             am = warp_max(am);
-            if (p.out_bf16) am = __bfloat162float(__float2bfloat16_rn(am));  // max of the stored values
+            if (p.out_bf16 && !p.out_fp8) am = __bfloat162float(__float2bfloat16_rn(am));  // max of the stored values
             if (lane == 0) atomicMax(reinterpret_cast<int *>(p.out_amax), __float_as_int(am));
         }
     }
@@ -609,7 +622,7 @@ __global__ void timeout_selftest_kernel() {
 
 // out = bias (or 0) broadcast over rows: the GEMM of an empty contraction.
 __global__ void fill_bias_kernel(int64_t rows, int64_t cols, const void *bias, int bias_bf16, void *out,
-                                 int out_bf16, float *out_amax) {
+                                 int out_bf16, float *out_amax, const float *out_scale, int out_fmt) {
     float am = 0.0f;
     const int64_t n = rows * cols;
     for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n;
@@ -618,7 +631,11 @@ __global__ void fill_bias_kernel(int64_t rows, int64_t cols, const void *bias, i
         float y = 0.0f;
         if (bias != nullptr)
             y = bias_bf16 ? bf16_bits_to_f32(static_cast<const uint16_t *>(bias)[j]) : static_cast<const float *>(bias)[j];
-        if (out_bf16) {
+        if (out_scale != nullptr) {
+            const float a = __fmul_rn(y, *out_scale);
+            static_cast<uint8_t *>(out)[i] = static_cast<uint8_t>(
+                (out_fmt == FP8MP_E4M3 ? cvt_pair<FP8MP_E4M3>(a, 0.0f) : cvt_pair<FP8MP_E5M2>(a, 0.0f)) & 0xFFu);
+        } else if (out_bf16) {
             const __nv_bfloat16 h = __float2bfloat16_rn(y);
             static_cast<__nv_bfloat16 *>(out)[i] = h;
             y = __bfloat162float(h);
@@ -646,16 +663,20 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
     return fn;
 }
 
-// Output tensor [rows x cols] of bf16 or fp32, box 32 rows x 128 bytes, 128-byte swizzle.
-int make_out_tmap(CUtensorMap *map, void *ptr, uint64_t cols, uint64_t rows, bool bf16) {
+// Output tensor [rows x cols] of bf16, fp32 or FP8 bytes, box 32 rows x 128
+// bytes, 128-byte swizzle.
+int make_out_tmap(CUtensorMap *map, void *ptr, uint64_t cols, uint64_t rows, bool bf16, bool fp8 = false) {
     auto enc = encode_fn();
     if (enc == nullptr) return fail(FP8MP_ERR_LAUNCH, "cuTensorMapEncodeTiled is not available");
-    const uint64_t esize = bf16 ? 2 : 4;
+    const uint64_t esize = fp8 ? 1 : (bf16 ? 2 : 4);
     const cuuint64_t dims[2] = {cols, rows};
     const cuuint64_t strides[1] = {cols * esize};
     const cuuint32_t box[2] = {static_cast<cuuint32_t>(128 / esize), 32};
     const cuuint32_t estr[2] = {1, 1};
-    const CUresult r = enc(map, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, ptr,
+    const CUresult r = enc(map,
+                           fp8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8
+                               : (bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32),
+                           2, ptr,
                            dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                            CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS)
@@ -749,7 +770,8 @@ int prepare_engine(const DeviceInfo &dev) {
 
 int launch_gemm(const uint8_t *a, int fmt_a, const uint8_t *b, int fmt_b, int64_t rows_a, int64_t rows_b,
                 int64_t kc, const float *sinv_a, const float *sinv_b, const void *bias, int bias_dtype, void *out,
-                int out_dtype, float *out_amax, cudaStream_t s, const DeviceInfo &dev) {
+                int out_dtype, float *out_amax, cudaStream_t s, const DeviceInfo &dev, const float *out_scale,
+                int out_fmt) {
     if (rows_a == 0 || rows_b == 0) return FP8MP_OK;
     if (rows_a > (1ll << 30) || rows_b > (1ll << 30) || kc > (1ll << 30))
         return fail(FP8MP_ERR_INVALID, "GEMM dimension above 2^30");
@@ -757,7 +779,8 @@ int launch_gemm(const uint8_t *a, int fmt_a, const uint8_t *b, int fmt_b, int64_
         int64_t blocks = (rows_a * rows_b + 255) / 256;
         if (blocks > dev.num_sms * 8) blocks = dev.num_sms * 8;
         fill_bias_kernel<<<static_cast<unsigned>(blocks), 256, 0, s>>>(rows_a, rows_b, bias, bias_dtype == FP8MP_BF16,
-                                                                      out, out_dtype == FP8MP_BF16, out_amax);
+                                                                      out, out_dtype == FP8MP_BF16, out_amax,
+                                                                      out_scale, out_fmt);
         const cudaError_t e = cudaGetLastError();
         if (e != cudaSuccess) return fail(FP8MP_ERR_LAUNCH, "GEMM fill launch failed: %s", cudaGetErrorString(e));
         return FP8MP_OK;
@@ -773,6 +796,9 @@ int launch_gemm(const uint8_t *a, int fmt_a, const uint8_t *b, int fmt_b, int64_
     p.bias_bf16 = bias_dtype == FP8MP_BF16;
     p.out = out;
     p.out_bf16 = out_dtype == FP8MP_BF16;
+    p.out_fp8 = out_scale != nullptr;
+    p.out_fmt = out_fmt;
+    p.out_scale = out_scale;
     p.out_amax = out_amax;
 
     // Pairs of SMs on 256 x 256 tiles when there are enough tiles to occupy
@@ -795,7 +821,8 @@ int launch_gemm(const uint8_t *a, int fmt_a, const uint8_t *b, int fmt_b, int64_
                    pair ? Cfg<true>::ROWS_B : Cfg<false>::ROWS_B);
     if (rc) return rc;
     CUtensorMap to;
-    rc = make_out_tmap(&to, out, static_cast<uint64_t>(rows_b), static_cast<uint64_t>(rows_a), p.out_bf16 != 0);
+    rc = make_out_tmap(&to, out, static_cast<uint64_t>(rows_b), static_cast<uint64_t>(rows_a), p.out_bf16 != 0,
+                       p.out_fp8 != 0);
     if (rc) return rc;
 
     if (pair) {

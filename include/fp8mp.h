@@ -206,6 +206,22 @@ int fp8_linear_fwd(const uint8_t *x8, const uint8_t *w8, int64_t M, int64_t N, i
                    void *y, int32_t y_dtype, float *y_amax, void *stream);
 
 /*
+ * fp8_linear_fwd_fp8out -- fp8_linear_fwd whose output is written directly as
+ * FP8 codes for the next layer ([PT-FP8] the torch._scaled_mm listing with
+ * out_dtype=e4m3_type, returning the output and its amax). With y computed
+ * in fp32 exactly as fp8_linear_fwd computes it before rounding:
+ *   y8[m, n] = sat_rne_{y_fmt}(fl32(y[m, n] * y_scale[0]))
+ *   *y_amax  = max(*y_amax, max |y|)     (fp32 y, unscaled: the amax delayed
+ *                                         scaling records for that tensor)
+ * y_scale is the consumer tensor's meta->scale. Saves the separate cast
+ * pass of the next layer's input (its transposed copy is not produced).
+ * Arguments otherwise as fp8_linear_fwd; y8 is [M x N] bytes.
+ */
+int fp8_linear_fwd_fp8out(const uint8_t *x8, const uint8_t *w8, int64_t M, int64_t N, int64_t K,
+                          const float *sinv_x, const float *sinv_w, const void *bias, int32_t bias_dtype,
+                          const float *y_scale, int32_t y_fmt, uint8_t *y8, float *y_amax, void *stream);
+
+/*
  * fp8_linear_dgrad -- input gradient of the linear layer (HYBRID recipe:
  * E5M2 gradient against the E4M3 weight; [TE-FP8] "Introduction to FP8" and
  * "FP8 사용방안(recipe)", Format.HYBRID; "Backward Pass 처리").
@@ -283,6 +299,30 @@ int mp_master_step(const uint16_t *grad_bf16, int64_t n, float *master, float *m
                    uint8_t *w8, const float *scale_w, float *amax_w, float *loss_scale,
                    int32_t *growth_tracker, int32_t *found_inf, float lr, float momentum_coef,
                    float backoff, float growth_factor, int32_t growth_interval, void *stream);
+
+/*
+ * mp_master_step_adam -- mp_master_step with an Adam update of the FP32
+ * master weights ([PT-FP8]: the float8_experimental training loop uses
+ * torch.optim.Adam; the loss-scale, skip and re-cast frame is [MP]'s as
+ * above). Pass 1 and the skip rule are mp_master_step's; otherwise, per
+ * element, each operation one correctly rounded fp32 operation:
+ *   u  = fp32(grad[i]) * fl32(1 / S)
+ *   b1t = fl32(beta_pows[0] * beta1),  b2t = fl32(beta_pows[1] * beta2)
+ *   exp_avg[i]    = fmaf(beta1, exp_avg[i], fl32(1 - beta1) * u)
+ *   exp_avg_sq[i] = fmaf(beta2, exp_avg_sq[i], fl32(1 - beta2) * fl32(u * u))
+ *   master[i] = fmaf(-lr, (exp_avg[i] / fl32(1 - b1t)) /
+ *                         (sqrt(exp_avg_sq[i] / fl32(1 - b2t)) + eps), master[i])
+ *   w8[i], *amax_w as mp_master_step.
+ * beta_pows  device float[2] = (beta1^(t-1), beta2^(t-1)), both 1 before the
+ *            first step; advanced to (b1t, b2t) on clean steps only.
+ * exp_avg, exp_avg_sq  [n] fp32, zero before the first step (in place).
+ * Traffic: 2 + (2 + 12) + (12 + 1) = 29 bytes per parameter.
+ */
+int mp_master_step_adam(const uint16_t *grad_bf16, int64_t n, float *master, float *exp_avg,
+                        float *exp_avg_sq, uint8_t *w8, const float *scale_w, float *amax_w,
+                        float *loss_scale, int32_t *growth_tracker, int32_t *found_inf, float *beta_pows,
+                        float lr, float beta1, float beta2, float eps, float backoff, float growth_factor,
+                        int32_t growth_interval, void *stream);
 
 /*
  * fp8mp_check -- synchronises `stream`, then reports and clears the device

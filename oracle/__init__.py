@@ -17,6 +17,7 @@ passage):
 * ``gemm_ref(A, fa, B, fb, sinv_a, sinv_b, bias, rows)``: fp64 reference.
 * ``master_step(...)``: unscale, overflow skip, SGD-momentum, E4M3 re-cast.
 * ``dbias(dy)``: the bias gradient (fp64 column sums) and column abs sums.
+* ``adam_step(...)``: the Adam variant of the master step.
 * ``cast_current(x, fmt, margin)``: just-in-time scaling then the cast.
 """
 
@@ -78,6 +79,7 @@ def _bind(path: str):
                                P, P, P]
     L.orc_master_step.argtypes = [P, I64, P, P, P, F, P, P, P, P, F, F, F, F, I32]
     L.orc_dbias.argtypes = [P, ctypes.c_int, I64, I64, P, P]
+    L.orc_adam_step.argtypes = [P, I64, P, P, P, P, F, P, P, P, P, P, P, F, F, F, F, F, F, I32]
     return L
 
 
@@ -249,6 +251,27 @@ def cast_current(x: np.ndarray, fmt: int, margin: int = 0, scale0: float = 1.0):
     scale_update(m, fmt, AMAX_MOST_RECENT, margin)
     m.cur_amax[0] = a  # report this tensor's amax, as the cast does
     return cast(x, float(m.scale[0]), fmt), m
+
+
+class AdamState:
+    """Adam's beta powers beta1^(t-1), beta2^(t-1) (both start at 1)."""
+
+    def __init__(self):
+        self.b1p = np.ones(1, dtype=np.float32)
+        self.b2p = np.ones(1, dtype=np.float32)
+
+
+def adam_step(g_bits, w, m, v, w8, scale_w, cur_amax_w, st, ad: AdamState, lr, beta1=0.9, beta2=0.999,
+              eps=1e-8, backoff=0.5, growth_factor=2.0, growth_interval=2000):
+    """In-place reference of one Adam master step (w, m, v, w8, amax, st, ad)."""
+    n = g_bits.size
+    for a in (w, m, v):
+        assert a.dtype == np.float32 and a.size == n and a.flags["C_CONTIGUOUS"]
+    lib().orc_adam_step(_ptr(g_bits), n, _ptr(w), _ptr(m), _ptr(v), _ptr(w8), ctypes.c_float(scale_w),
+                        _ptr(cur_amax_w), _ptr(st.S), _ptr(st.growth), _ptr(st.found_inf), _ptr(ad.b1p),
+                        _ptr(ad.b2p), ctypes.c_float(lr), ctypes.c_float(beta1), ctypes.c_float(beta2),
+                        ctypes.c_float(eps), ctypes.c_float(backoff), ctypes.c_float(growth_factor),
+                        int(growth_interval))
 
 
 class LossScaleState:

@@ -429,3 +429,71 @@ void orc_dbias(const void *dy, int is_bf16, int64_t rows, int64_t cols, double *
             abs_out[c] = a;
     }
 }
+
+/* ------------------------------------------------------------------------ */
+/* Adam master step. The PyTorch-native FP8 page trains its model with      */
+/* torch.optim.Adam ([PT-FP8], the float8_experimental training loop); the  */
+/* mixed-precision frame is the SGD step's ([MP]: unscale by 1/S, skip on   */
+/* Inf/NaN and lower S, FP32 master, low-precision copy). The update, each  */
+/* operation one correctly rounded fp32 operation in this order:            */
+/*   u   = fp32(g) * fl32(1 / S)                                            */
+/*   b1t = fl32(b1p * beta1),  b2t = fl32(b2p * beta2)  (beta^t; b1p, b2p   */
+/*         hold beta^(t-1), start at 1, advance on clean steps only)        */
+/*   m   = fmaf(beta1, m, fl32(1 - beta1) * u)                              */
+/*   v   = fmaf(beta2, v, fl32(1 - beta2) * fl32(u * u))                    */
+/*   mh  = m / fl32(1 - b1t),  vh = v / fl32(1 - b2t)                       */
+/*   w   = fmaf(-lr, mh / (sqrtf(vh) + eps), w)                             */
+/*   w8  = encode_E4M3(fl32(w * scale_w)); cur_amax_w = max(.., |w|)        */
+/* then, on a clean step, b1p = b1t, b2p = b2t and the loss-scale update.   */
+/* ------------------------------------------------------------------------ */
+
+void orc_adam_step(const uint16_t *g, int64_t n, float *w, float *m, float *v, uint8_t *w8, float scale_w,
+                   float *cur_amax_w, float *S, int32_t *growth, int32_t *found_inf, float *b1p, float *b2p,
+                   float lr, float beta1, float beta2, float eps, float backoff, float growth_factor,
+                   int32_t growth_interval)
+{
+    int found = 0;
+    int64_t i;
+#pragma omp parallel for reduction(| : found) schedule(static)
+    for (i = 0; i < n; ++i)
+        if ((g[i] & 0x7F80u) == 0x7F80u)
+            found |= 1;
+    *found_inf = found;
+    if (found) {
+        *S = *S * backoff;
+        *growth = 0;
+        return;
+    }
+    const float inv_s = 1.0f / *S;
+    const float b1t = *b1p * beta1, b2t = *b2p * beta2;
+    const float c1 = 1.0f - beta1, c2 = 1.0f - beta2;
+    const float bc1 = 1.0f - b1t, bc2 = 1.0f - b2t;
+    const float neg_lr = -lr;
+    float am = *cur_amax_w;
+#pragma omp parallel for reduction(max : am) schedule(static)
+    for (i = 0; i < n; ++i) {
+        const float u = bf16_to_f32(g[i]) * inv_s;
+        const float mn = fmaf(beta1, m[i], c1 * u);
+        const float uu = u * u;
+        const float vn = fmaf(beta2, v[i], c2 * uu);
+        const float mh = mn / bc1;
+        const float vh = vn / bc2;
+        const float den = sqrtf(vh) + eps;
+        const float wn = fmaf(neg_lr, mh / den, w[i]);
+        m[i] = mn;
+        v[i] = vn;
+        w[i] = wn;
+        w8[i] = orc_encode(ORC_E4M3, wn * scale_w);
+        const float a = fabsf(wn);
+        if (a > am)
+            am = a;
+    }
+    *cur_amax_w = am;
+    *b1p = b1t;
+    *b2p = b2t;
+    *growth += 1;
+    if (*growth >= growth_interval) {
+        *S = *S * growth_factor;
+        *growth = 0;
+    }
+}

@@ -93,3 +93,28 @@ def test_1e9_parameters(cuda_lib, orc):
         del g
         compare(ds, hs, f"1e9 step={step}")
     assert hs["st"].found_inf[0] == 0 and hs["st"].S[0] == 2.0 ** 15
+
+
+# ------------------------------------------------------------- Adam variant
+
+
+@pytest.mark.parametrize("n", [0, 1, 9, 4096, (1 << 20) + 5])
+def test_adam_steps_bit_exact(cuda_lib, orc, n):
+    w = workloads.master_weights(n, seed=n + 1)
+    ds = DevState(w, 2.0 ** 16, 0)
+    m = torch.zeros(n, dtype=torch.float32, device="cuda")
+    bp = torch.ones(2, dtype=torch.float32, device="cuda")
+    hs = host_state(w, 2.0 ** 16, 0, orc)
+    hm = np.zeros(n, np.float32)
+    ad = orc.AdamState()
+    for step in range(4):
+        g = workloads.master_step(n, step, seed=n + 1, inject=(step == 2 and n > 0), inject_frac=1e-3)
+        ds.scale_w.fill_(64.0)
+        cuda_lib.mp_master_step_adam(g.cuda(), ds.w, m, ds.v, ds.w8, ds.scale_w, ds.amax_w, ds.S, ds.growth,
+                                     ds.found, bp, lr=1e-3, beta1=0.9, beta2=0.999, eps=1e-8)
+        assert cuda_lib.fp8mp_check() == 0
+        orc.adam_step(np_view(g), hs["w"], hm, hs["v"], hs["w8"], 64.0, hs["am"], hs["st"], ad, lr=1e-3,
+                      beta1=0.9, beta2=0.999, eps=1e-8)
+        compare(ds, hs, f"adam n={n} step={step}")
+        assert_same_bits(np_view(m), hm, "exp_avg")
+        assert_same_bits(np_view(bp), np.array([ad.b1p[0], ad.b2p[0]], np.float32), "beta powers")

@@ -96,3 +96,50 @@ def test_dbias_rejects_small_workspace(cuda_lib):
     with pytest.raises(cuda_lib.Fp8mpError) as e:
         cuda_lib.fp8_quantize_dbias(dy, E5M2, torch.ones(1, device="cuda"), out, out_t, db, ws)
     assert e.value.code == cuda_lib.ERR_INVALID and "workspace" in cuda_lib.last_error()
+
+
+@pytest.mark.parametrize("engine", ["single", "pair"])
+@pytest.mark.parametrize("M,N,K", [(256, 512, 256), (1040, 784, 784), (2304, 2560, 1024)])
+@pytest.mark.parametrize("y_fmt", [E4M3, E5M2])
+def test_fwd_with_fp8_output(cuda_lib, orc, monkeypatch, engine, M, N, K, y_fmt):
+    """FP8 codes written by the GEMM epilogue: (a) the same codes a plain cast
+    of the GEMM's own fp32 output gives (torch's float8 cast, a library
+    routine, with saturation beyond the range); (b) every code inside the
+    band of values that the GEMM tolerance around the oracle's reference
+    allows; (c) the amax is the fp32 output's, close to the reference's."""
+    from gpu_util import dev, finite_codes, gemm_tolerance_check
+
+    monkeypatch.setenv("FP8MP_GEMM_ENGINE", engine)
+    rng = np.random.default_rng(M + N + K + y_fmt)
+    A = finite_codes(rng, (M, K), E4M3)
+    B = finite_codes(rng, (N, K), E4M3)
+    sa, sb = 2.0 ** -7, 0.05
+    bias = (torch.randn(N, generator=workloads.gen(5)) * 10).to(torch.bfloat16)
+    ref, ab = orc.gemm_ref(A, E4M3, B, E4M3, float(np.float32(sa)), float(np.float32(sb)),
+                           bias=bias.double().numpy())
+    ys = np.float32(orc.fmt_max(y_fmt) / (np.abs(ref).max() * 0.8))  # the top 20 % saturates
+    one = lambda v: torch.tensor([v], dtype=torch.float32, device="cuda")
+    y8 = torch.empty((M, N), dtype=torch.uint8, device="cuda")
+    am = torch.zeros(1, device="cuda")
+    cuda_lib.fp8_linear_fwd_fp8out(dev(A), dev(B), one(sa), one(sb), one(ys), y8, y_fmt=y_fmt,
+                                   bias=bias.cuda(), y_amax=am)
+    y32 = torch.empty((M, N), dtype=torch.float32, device="cuda")
+    cuda_lib.fp8_linear_fwd(dev(A), dev(B), one(sa), one(sb), y32, bias=bias.cuda())
+    assert cuda_lib.fp8mp_check() == 0
+    codes = y8.cpu().numpy()
+    yh = np_view(y32)
+    gemm_tolerance_check(yh.astype(np.float64), ref, ab, "fp32 output")
+    # (a) the epilogue's cast of its own fp32 y
+    tfmt = torch.float8_e4m3fn if y_fmt == E4M3 else torch.float8_e5m2
+    prod = torch.from_numpy(yh) * torch.tensor(ys)
+    vmax = orc.fmt_max(y_fmt)
+    expect = prod.clamp(-vmax, vmax).to(tfmt).view(torch.uint8).numpy()
+    assert (codes == expect).all()
+    # (b) the band allowed by the tolerance around the fp64 reference
+    tol = 2.0 ** -8 * np.abs(ref) + 1e-5 * ab
+    lo = orc.decode(y_fmt, orc.cast(((ref - tol) * ys).astype(np.float32), 1.0, y_fmt))
+    hi = orc.decode(y_fmt, orc.cast(((ref + tol) * ys).astype(np.float32), 1.0, y_fmt))
+    val = orc.decode(y_fmt, codes)
+    assert ((val >= lo) & (val <= hi)).all()
+    # (c) amax of the fp32 output
+    assert am.item() == np.abs(yh).max()

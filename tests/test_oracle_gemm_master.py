@@ -210,3 +210,72 @@ def test_master_step_unscale_exact_for_power_of_two(orc):
     assert (w == -v).all()
     # the FP8 copy is the E4M3 cast of the new master weights at scale_w
     assert (w8 == orc.cast(w, 1.0, E4M3)).all()
+
+
+# ------------------------------------------------------------- Adam step
+
+
+def test_adam_first_step_is_sign_descent(orc):
+    """At t = 1 the bias corrections cancel: mh = u, vh = u^2, so with a tiny
+    eps each weight moves by lr * sign(u) (worked from the update rule)."""
+    g = bf16_bits([2.0 ** 16, -(2.0 ** 15), 3.0 * 2 ** 16])
+    w = np.array([1.0, 1.0, -0.5], dtype=np.float32)
+    m = np.zeros(3, np.float32)
+    v = np.zeros(3, np.float32)
+    w8 = np.zeros(3, np.uint8)
+    am = np.zeros(1, np.float32)
+    st = orc.LossScaleState(2.0 ** 16)
+    ad = orc.AdamState()
+    orc.adam_step(g, w, m, v, w8, 1.0, am, st, ad, lr=2.0 ** -7, eps=1e-30)
+    np.testing.assert_allclose(w, [1.0 - 2 ** -7, 1.0 + 2 ** -7, -0.5 - 2 ** -7], rtol=0, atol=2e-7)
+    np.testing.assert_allclose(m, np.float32(0.1) * np.array([1.0, -0.5, 3.0], np.float32), rtol=1e-6)
+    assert ad.b1p[0] == np.float32(0.9) and ad.b2p[0] == np.float32(0.999)
+    assert st.growth[0] == 1
+
+
+def test_adam_vs_torch_optim_adam(orc):
+    """torch.optim.Adam (the optimizer the PyTorch-native FP8 page uses) on the
+    unscaled gradients: same trajectory within a few fp32 roundings. beta2 =
+    1 - 2^-10 is exact in fp32, so both sides use the same 1 - beta2 (with
+    0.999 the fp32 complement 1 - fl32(0.999) differs from fl32(0.001) by
+    1.3e-5 relative, which would show in every v)."""
+    rng = np.random.default_rng(41)
+    n, S = 20_000, 2.0 ** 16
+    w = (rng.standard_normal(n) * 0.02).astype(np.float32)
+    m = np.zeros(n, np.float32)
+    v = np.zeros(n, np.float32)
+    w8 = np.zeros(n, np.uint8)
+    am = np.zeros(1, np.float32)
+    st = orc.LossScaleState(S)
+    ad = orc.AdamState()
+    p = torch.nn.Parameter(torch.from_numpy(w.copy()))
+    b2 = 1.0 - 2.0 ** -10
+    opt = torch.optim.Adam([p], lr=1e-3, betas=(0.9, b2), eps=1e-8)
+    for step in range(4):
+        gt = torch.from_numpy((rng.standard_normal(n) * 1e-4 * S).astype(np.float32)).to(torch.bfloat16)
+        g = gt.view(torch.int16).numpy().view(np.uint16).copy()
+        orc.adam_step(g, w, m, v, w8, 1.0, am, st, ad, lr=1e-3, beta2=b2)
+        p.grad = gt.float() / S
+        opt.step()
+    np.testing.assert_allclose(w, p.detach().numpy(), rtol=0, atol=2e-8)
+    # torch forms m with lerp (another rounding order); where 0.9 m and 0.1 u
+    # nearly cancel the two differ by a few roundings of the terms, not of m
+    np.testing.assert_allclose(m, opt.state[p]["exp_avg"].numpy(), rtol=2e-6, atol=1e-6 * np.abs(m).max())
+    np.testing.assert_allclose(v, opt.state[p]["exp_avg_sq"].numpy(), rtol=2e-6, atol=1e-20)
+
+
+def test_adam_skip_step_keeps_everything(orc):
+    g = bf16_bits(np.ones(64))
+    g[5] = 0xFFC0
+    w = np.ones(64, np.float32)
+    m = np.full(64, 0.5, np.float32)
+    v = np.full(64, 0.25, np.float32)
+    w8 = np.zeros(64, np.uint8)
+    am = np.zeros(1, np.float32)
+    st = orc.LossScaleState(8.0, growth=7)
+    ad = orc.AdamState()
+    ad.b1p[0], ad.b2p[0] = 0.81, 0.998
+    orc.adam_step(g, w, m, v, w8, 1.0, am, st, ad, lr=0.1)
+    assert st.found_inf[0] == 1 and st.S[0] == 4.0 and st.growth[0] == 0
+    assert (w == 1).all() and (m == 0.5).all() and (v == 0.25).all() and (w8 == 0).all()
+    assert ad.b1p[0] == np.float32(0.81) and ad.b2p[0] == np.float32(0.998)

@@ -51,6 +51,11 @@ MUTANTS = [
     ("recast ignores scale_w", "orc_encode(ORC_E4M3, wn * scale_w)", "orc_encode(ORC_E4M3, wn)"),
     ("recast as E5M2", "orc_encode(ORC_E4M3, wn * scale_w)", "orc_encode(ORC_E5M2, wn * scale_w)"),
     ("NaN gradient missed", "if ((g[i] & 0x7F80u) == 0x7F80u)", "if (g[i] == 0x7F80u)"),
+    ("Adam second moment uses u", "const float uu = u * u;", "const float uu = u;"),
+    ("Adam without bias correction", "const float mh = mn / bc1;", "const float mh = mn;"),
+    ("Adam eps inside the sqrt", "const float den = sqrtf(vh) + eps;", "const float den = sqrtf(vh + eps);"),
+    ("Adam step count advances on skips", "        *S = *S * backoff;\n        *growth = 0;\n        return;\n    }\n    const float inv_s = 1.0f / *S;\n    const float b1t",
+     "        *S = *S * backoff;\n        *growth = 0;\n        *b1p = *b1p * beta1;\n        return;\n    }\n    const float inv_s = 1.0f / *S;\n    const float b1t"),
     ("dbias sums a transposed view", "((const uint16_t *)dy)[r * cols + c]", "((const uint16_t *)dy)[c * rows + r]"),
     ("dbias drops its last row", "for (int64_t r = 0; r < rows; ++r) {\n            const double v = is_bf16",
      "for (int64_t r = 0; r + 1 < rows; ++r) {\n            const double v = is_bf16"),
@@ -85,6 +90,9 @@ def _pins():
         ("master_neginf_alone", lambda: gm.test_master_step_each_nonfinite_kind_alone_skips(oracle, 0xFF80)),
         ("master_torch_sgd", lambda: gm.test_master_step_vs_torch_sgd_momentum(oracle)),
         ("dbias", lambda: sc.test_dbias_definition(oracle)),
+        ("adam_first", lambda: gm.test_adam_first_step_is_sign_descent(oracle)),
+        ("adam_torch", lambda: gm.test_adam_vs_torch_optim_adam(oracle)),
+        ("adam_skip", lambda: gm.test_adam_skip_step_keeps_everything(oracle)),
         ("current_scaling", lambda: sc.test_current_scaling_maps_amax_to_fmt_max(oracle)),
     ]
     return p
