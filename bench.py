@@ -16,6 +16,11 @@ through the library's entry points on one CUDA stream:
 The metric counts the FLOPs the FP8 tensor cores perform, 3 * 2 * M * N * K,
 per step time. Multi-GPU runs are independent replicas (weak scaling).
 
+The timed steps replay CUDA graphs of those ten library calls (captured after
+the eager warm-up; one graph per timed step, each with its own event-record
+nodes around the three GEMMs), as a training loop that captures its step
+would; --eager launches every call from Python instead.
+
 --impl reference times the CPU oracle on a bounded sample of the same step.
 """
 
@@ -254,6 +259,35 @@ class LinearStep:
         f.delayed_scaling_update([self.mx, self.mw, self.my, self.md], f.AMAX_MOST_RECENT, 0)
 
 
+def capture_step_graphs(st, count):
+    """`count` CUDA graphs of one step each, or None when this torch cannot
+    record timing events inside a graph. Each graph carries its own five
+    event-record nodes around the GEMMs so that every timed step's GEMM
+    launches are timed on the device. Capture runs on a side stream after
+    the eager warm-up (which made the library's one-time attribute and
+    occupancy queries)."""
+    import torch
+
+    try:
+        probe = torch.cuda.Event(enable_timing=True, external=True)
+    except TypeError:
+        return None
+    del probe
+    graphs, events = [], []
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    for _ in range(count):
+        ev = [torch.cuda.Event(enable_timing=True, external=True) for _ in range(5)]
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=side):
+            st.step(ev)
+        graphs.append(g)
+        events.append(ev)
+    torch.cuda.current_stream().wait_stream(side)
+    torch.cuda.synchronize()
+    return graphs, events
+
+
 def run_e2e(st, steps, world):
     import torch
 
@@ -320,14 +354,26 @@ def run_ours(args, world, rank, local):
     E = torch.cuda.Event
     starts = [E(enable_timing=True) for _ in range(args.steps)]
     ends = [E(enable_timing=True) for _ in range(args.steps)]
-    gev = [[E(enable_timing=True) for _ in range(5)] for _ in range(args.steps)]
+    graphs = None if args.eager else capture_step_graphs(st, args.steps)
+    if graphs is None:
+        gev = [[E(enable_timing=True) for _ in range(5)] for _ in range(args.steps)]
+        launch = "eager (one host launch per library call)"
+    else:
+        graphs, gev = graphs
+        for g in graphs:  # first replay uploads the graph: keep it out of the timed region
+            g.replay()
+        torch.cuda.synchronize()
+        launch = "CUDA graph per step (the ten library calls captured, replayed)"
     barrier(world)
     torch.cuda.synchronize()
     with ClockSampler(local) as clocks:
         for i in range(args.steps):
             flush.fill_(float(i))  # L2 flush between timed steps (outside the step events)
             starts[i].record()
-            st.step(gev[i])
+            if graphs is None:
+                st.step(gev[i])
+            else:
+                graphs[i].replay()
             ends[i].record()
         torch.cuda.synchronize()
     barrier(world)
@@ -366,7 +412,7 @@ def run_ours(args, world, rank, local):
         "data": "synthetic (seeded; shapes and distributions of the transformer proj workload)",
         "config": {"workload": WORKLOAD, "M": M_TOK, "K": K_IN, "N": N_OUT, "history_len": HIST_LEN,
                    "amax_compute_algo": "most_recent", "recipe": "HYBRID", "parallelism": f"replicas x{world}",
-                   "l2": "flushed (2x L2 write) between timed steps"},
+                   "l2": "flushed (2x L2 write) between timed steps", "launch": launch},
         "gemm_only": {"tflops": round(world * fl / (gemm_step_ms * 1e-3) / 1e12, 2), "ms_per_step": round(gemm_step_ms, 5)},
         "roofline": {"kernel": "gemm_fp8_kernel", "bound": "tensor", "achieved": round(achieved, 2),
                      "peak": round(fp8_peak, 1), "unit": "TFLOP/s", "frac": round(achieved / fp8_peak, 4),
@@ -501,6 +547,8 @@ def main(argv=None):
     ap.add_argument("--baseline-tokens", type=int, default=4096,
                     help="tokens of the oracle sample timed as cpu_baseline (about 10-30 s)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--eager", action="store_true",
+                    help="launch every library call from Python in the timed steps instead of replaying graphs")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
