@@ -9,16 +9,16 @@ through the library's entry points on one CUDA stream:
   fp8_quantize(W  -> W8, W8^T, amax)           E4M3 (fp32 master in)
   fp8_linear_fwd(X8, W8 -> Y bf16, amax_y)
   fp8_quantize(dY -> dY8, dY8^T, amax)         E5M2
-  fp8_linear_dgrad(dY8, W8^T -> dX bf16)
-  fp8_linear_wgrad(dY8^T, X8^T -> dW bf16)
+  fp8_linear_bwd(dY8, W8^T -> dX bf16;         dgrad and wgrad GEMMs in
+                 dY8^T, X8^T -> dW bf16)        one launch
   mp_master_step(dW -> master, momentum, w8)   SGD-momentum, loss scale 2^16
   delayed_scaling_update(x, w, y, dy metas)    L = 1024, most_recent
 The metric counts the FLOPs the FP8 tensor cores perform, 3 * 2 * M * N * K,
 per step time. Multi-GPU runs are independent replicas (weak scaling).
 
-The timed steps replay CUDA graphs of those ten library calls (captured after
-the eager warm-up; one graph per timed step, each with its own event-record
-nodes around the three GEMMs), as a training loop that captures its step
+The timed steps replay CUDA graphs of those library calls (captured after the
+eager warm-up; one graph per timed step, each with its own event-record nodes
+around the two GEMM launches), as a training loop that captures its step
 would; --eager launches every call from Python instead.
 
 --impl reference times the CPU oracle on a bounded sample of the same step.
@@ -230,7 +230,8 @@ class LinearStep:
         E4, E5 = fp8mp.E4M3, fp8mp.E5M2
         self.mx, self.mw, self.my = (fp8mp.Meta(HIST_LEN, E4) for _ in range(3))
         self.md = fp8mp.Meta(HIST_LEN, E5)
-        self.launches_per_step = 10  # 3 casts, 3 GEMMs, 3 master-step kernels, 1 scale update
+        # 3 casts, the fwd GEMM, the fused dgrad + wgrad GEMM, 3 master-step kernels, 1 scale update
+        self.launches_per_step = 9
 
     def step(self, gemm_events=None, io=None):
         """One training step. `io` = (x, dy, y, dx) device buffers to use
@@ -248,12 +249,10 @@ class LinearStep:
         f.fp8_quantize(dy, f.E5M2, self.md.scale, self.D8, self.D8t, self.md.cur_amax)
         if ev is not None:
             ev[2].record()
-        f.fp8_linear_dgrad(self.D8, self.W8t, self.md.scale_inv, self.mw.scale_inv, dx)
+        f.fp8_linear_bwd(self.D8, self.D8t, self.W8t, self.X8t, self.md.scale_inv, self.mw.scale_inv,
+                         self.mx.scale_inv, dx, self.dw)
         if ev is not None:
             ev[3].record()
-        f.fp8_linear_wgrad(self.D8t, self.X8t, self.md.scale_inv, self.mx.scale_inv, self.dw)
-        if ev is not None:
-            ev[4].record()
         f.mp_master_step(self.dw, self.master, self.mom, self.w8_next, self.mw.scale, self.mw.cur_amax, self.S,
                          self.growth, self.found, LR, MU)
         f.delayed_scaling_update([self.mx, self.mw, self.my, self.md], f.AMAX_MOST_RECENT, 0)
@@ -261,8 +260,8 @@ class LinearStep:
 
 def capture_step_graphs(st, count):
     """`count` CUDA graphs of one step each, or None when this torch cannot
-    record timing events inside a graph. Each graph carries its own five
-    event-record nodes around the GEMMs so that every timed step's GEMM
+    record timing events inside a graph. Each graph carries its own four
+    event-record nodes around the GEMM launches so that every timed step's GEMM
     launches are timed on the device. Capture runs on a side stream after
     the eager warm-up (which made the library's one-time attribute and
     occupancy queries)."""
@@ -277,7 +276,7 @@ def capture_step_graphs(st, count):
     side = torch.cuda.Stream()
     side.wait_stream(torch.cuda.current_stream())
     for _ in range(count):
-        ev = [torch.cuda.Event(enable_timing=True, external=True) for _ in range(5)]
+        ev = [torch.cuda.Event(enable_timing=True, external=True) for _ in range(4)]
         g = torch.cuda.CUDAGraph()
         with torch.cuda.graph(g, stream=side):
             st.step(ev)
@@ -356,14 +355,14 @@ def run_ours(args, world, rank, local):
     ends = [E(enable_timing=True) for _ in range(args.steps)]
     graphs = None if args.eager else capture_step_graphs(st, args.steps)
     if graphs is None:
-        gev = [[E(enable_timing=True) for _ in range(5)] for _ in range(args.steps)]
+        gev = [[E(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
         launch = "eager (one host launch per library call)"
     else:
         graphs, gev = graphs
         for g in graphs:  # first replay uploads the graph: keep it out of the timed region
             g.replay()
         torch.cuda.synchronize()
-        launch = "CUDA graph per step (the ten library calls captured, replayed)"
+        launch = "CUDA graph per step (the step's library calls captured, replayed)"
     barrier(world)
     torch.cuda.synchronize()
     with ClockSampler(local) as clocks:
@@ -381,10 +380,11 @@ def run_ours(args, world, rank, local):
     if rc != 0:
         raise RuntimeError(f"timed steps failed: {st.fp8mp.last_error()}")
     step_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
-    gemm_ms = [[g[0].elapsed_time(g[1]), g[2].elapsed_time(g[3]), g[3].elapsed_time(g[4])] for g in gev]
+    gemm_ms = [[g[0].elapsed_time(g[1]), g[2].elapsed_time(g[3])] for g in gev]  # fwd, fused bwd
     ms_per_step = max_over_ranks(statistics.mean(step_ms), world)
     gemm_step_ms = max_over_ranks(statistics.mean(sum(g) for g in gemm_ms), world)
-    gemm_launch_ms = statistics.mean(x for g in gemm_ms for x in g)
+    fwd_ms = statistics.mean(g[0] for g in gemm_ms)
+    bwd_ms = statistics.mean(g[1] for g in gemm_ms)
 
     # end to end through the public API: every step copies its x and dY in
     # from pinned host memory and its y and dX back out. Copies run on their
@@ -394,7 +394,9 @@ def run_ours(args, world, rank, local):
     fl = flops_per_step()
     value = world * fl / (ms_per_step * 1e-3) / 1e12
     fp8_peak = float(peaks["bf16_tflops"]) * FP8_OVER_BF16
-    achieved = 2.0 * M_TOK * N_OUT * K_IN / (gemm_launch_ms * 1e-3) / 1e12
+    # the GEMM kernel's two launches per step do 2MNK (fwd) and 4MNK (dgrad +
+    # wgrad) FLOPs: achieved = their FLOPs / their summed device time
+    achieved = fl / ((fwd_ms + bwd_ms) * 1e-3) / 1e12
     traffic = gemm_traffic_from_profile()
     clk = clocks.summary()
     out = {
@@ -413,7 +415,8 @@ def run_ours(args, world, rank, local):
         "config": {"workload": WORKLOAD, "M": M_TOK, "K": K_IN, "N": N_OUT, "history_len": HIST_LEN,
                    "amax_compute_algo": "most_recent", "recipe": "HYBRID", "parallelism": f"replicas x{world}",
                    "l2": "flushed (2x L2 write) between timed steps", "launch": launch},
-        "gemm_only": {"tflops": round(world * fl / (gemm_step_ms * 1e-3) / 1e12, 2), "ms_per_step": round(gemm_step_ms, 5)},
+        "gemm_only": {"tflops": round(world * fl / (gemm_step_ms * 1e-3) / 1e12, 2), "ms_per_step": round(gemm_step_ms, 5),
+                      "fwd_ms": round(fwd_ms, 5), "bwd_ms": round(bwd_ms, 5)},
         "roofline": {"kernel": "gemm_fp8_kernel", "bound": "tensor", "achieved": round(achieved, 2),
                      "peak": round(fp8_peak, 1), "unit": "TFLOP/s", "frac": round(achieved / fp8_peak, 4),
                      "traffic": traffic,

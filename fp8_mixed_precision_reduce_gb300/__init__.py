@@ -26,7 +26,7 @@ _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "libfp8mp.so")
 EXPORTS = ("fp8_quantize", "fp8_quantize_current", "fp8_quantize_dbias",
            "fp8_quantize_dbias_workspace_bytes", "fp8_quantize_dbias_noalloc", "fp8_linear_fwd", "fp8_linear_fwd_fp8out", "fp8_linear_dgrad", "fp8_linear_wgrad",
-           "delayed_scaling_update", "mp_master_step", "mp_master_step_adam", "fp8mp_check", "fp8mp_last_error",
+           "fp8_linear_bwd", "delayed_scaling_update", "mp_master_step", "mp_master_step_adam", "fp8mp_check", "fp8mp_last_error",
            "fp8mp_version", "fp8mp_selftest_timeout")
 
 _lib = None
@@ -73,6 +73,7 @@ def load(path: str | None = None):
     L.fp8_linear_fwd_fp8out.argtypes = [P, P, I64, I64, I64, P, P, P, I32, P, I32, P, P, P]
     L.fp8_linear_dgrad.argtypes = [P, P, I64, I64, I64, I32, P, P, P, I32, P]
     L.fp8_linear_wgrad.argtypes = [P, P, I64, I64, I64, I32, P, P, P, I32, P]
+    L.fp8_linear_bwd.argtypes = [P, P, P, P, I64, I64, I64, I32, P, P, P, P, I32, P, I32, P]
     L.delayed_scaling_update.argtypes = [ctypes.POINTER(fp8mp_meta), I32, I32, I32, P]
     L.mp_master_step.argtypes = [P, I64, P, P, P, P, P, P, P, P, F, F, F, F, I32, P]
     L.mp_master_step_adam.argtypes = [P, I64, P, P, P, P, P, P, P, P, P, P, F, F, F, F, F, F, I32, P]
@@ -82,7 +83,7 @@ def load(path: str | None = None):
     L.fp8mp_version.restype = I32
     for name in ("fp8_quantize", "fp8_quantize_current", "fp8_quantize_dbias", "fp8_quantize_dbias_noalloc",
                  "fp8_linear_fwd", "fp8_linear_fwd_fp8out", "fp8_linear_dgrad", "fp8_linear_wgrad",
-                 "delayed_scaling_update", "mp_master_step", "mp_master_step_adam", "fp8mp_check",
+                 "fp8_linear_bwd", "delayed_scaling_update", "mp_master_step", "mp_master_step_adam", "fp8mp_check",
                  "fp8mp_selftest_timeout"):
         getattr(L, name).restype = ctypes.c_int
     _lib = L
@@ -223,6 +224,18 @@ def fp8_linear_wgrad(dy8t: torch.Tensor, x8t: torch.Tensor, sinv_dy: torch.Tenso
     K = x8t.shape[0]
     _check(load().fp8_linear_wgrad(_ptr(dy8t), _ptr(x8t), M, N, K, dy_fmt, _ptr(sinv_dy), _ptr(sinv_x),
                                    _ptr(dw), _dtype_code(dw), _stream(stream)))
+
+
+def fp8_linear_bwd(dy8: torch.Tensor, dy8t: torch.Tensor, w8t: torch.Tensor, x8t: torch.Tensor,
+                   sinv_dy: torch.Tensor, sinv_w: torch.Tensor, sinv_x: torch.Tensor, dx: torch.Tensor,
+                   dw: torch.Tensor, dy_fmt: int = E5M2, stream=None) -> None:
+    """fp8_linear_dgrad and fp8_linear_wgrad in one launch:
+    dx[M, K] = (dy8 . w8t^T) * sinv_dy * sinv_w, dw[N, K] = (dy8t . x8t^T) * sinv_dy * sinv_x."""
+    M, N = dy8.shape
+    K = w8t.shape[0]
+    _check(load().fp8_linear_bwd(_ptr(dy8), _ptr(dy8t), _ptr(w8t), _ptr(x8t), M, N, K, dy_fmt, _ptr(sinv_dy),
+                                 _ptr(sinv_w), _ptr(sinv_x), _ptr(dx), _dtype_code(dx), _ptr(dw), _dtype_code(dw),
+                                 _stream(stream)))
 
 
 class Meta:

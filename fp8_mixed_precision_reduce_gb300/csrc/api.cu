@@ -311,6 +311,47 @@ int fp8_linear_wgrad(const uint8_t *dy8t, const uint8_t *x8t, int64_t M, int64_t
                        nullptr, static_cast<cudaStream_t>(stream), dev);
 }
 
+int fp8_linear_bwd(const uint8_t *dy8, const uint8_t *dy8t, const uint8_t *w8t, const uint8_t *x8t, int64_t M,
+                   int64_t N, int64_t K, int32_t dy_fmt, const float *sinv_dy, const float *sinv_w,
+                   const float *sinv_x, void *dx, int32_t dx_dtype, void *dw, int32_t dw_dtype, void *stream) {
+    const char *fn = "fp8_linear_bwd";
+    clear_error();
+    int rc = check_gemm_dims(fn, M, N, K);
+    if (rc) return rc;
+    REQUIRE(valid_fmt(dy_fmt), "%s: dy_fmt %d invalid", fn, dy_fmt);
+    REQUIRE(valid_dtype(dx_dtype), "%s: dx_dtype %d invalid", fn, dx_dtype);
+    REQUIRE(valid_dtype(dw_dtype), "%s: dw_dtype %d invalid", fn, dw_dtype);
+    if (K == 0 || (M == 0 && N == 0)) return FP8MP_OK;
+    CHECK_SCALAR(sinv_dy, true);
+    if (M > 0) {
+        CHECK_PTR(dx, true);
+        CHECK_SCALAR(sinv_w, true);
+    }
+    if (N > 0) {
+        CHECK_PTR(dw, true);
+        CHECK_SCALAR(sinv_x, true);
+    }
+    if (M > 0 && N > 0) {
+        CHECK_PTR(dy8, true);
+        CHECK_PTR(dy8t, true);
+        CHECK_PTR(w8t, true);
+        CHECK_PTR(x8t, true);
+        const uintptr_t a = reinterpret_cast<uintptr_t>(dx), b = reinterpret_cast<uintptr_t>(dw);
+        const uintptr_t na = static_cast<uintptr_t>(M * K) * (dx_dtype == FP8MP_BF16 ? 2 : 4);
+        const uintptr_t nb = static_cast<uintptr_t>(N * K) * (dw_dtype == FP8MP_BF16 ? 2 : 4);
+        REQUIRE(a + na <= b || b + nb <= a, "%s: dx and dw overlap", fn);
+    }
+    DeviceInfo dev;
+    rc = current_device(&dev);
+    if (rc) return rc;
+    const GemmDesc d[2] = {
+        {dy8, dy_fmt, w8t, FP8MP_E4M3, M, K, N, sinv_dy, sinv_w, nullptr, FP8MP_F32, dx, dx_dtype, nullptr, nullptr,
+         FP8MP_E4M3},
+        {dy8t, dy_fmt, x8t, FP8MP_E4M3, N, K, M, sinv_dy, sinv_x, nullptr, FP8MP_F32, dw, dw_dtype, nullptr, nullptr,
+         FP8MP_E4M3}};
+    return launch_gemms(d, 2, static_cast<cudaStream_t>(stream), dev);
+}
+
 int delayed_scaling_update(const fp8mp_meta *metas, int32_t n, int32_t algo, int32_t margin, void *stream) {
     const char *fn = "delayed_scaling_update";
     clear_error();

@@ -38,6 +38,25 @@ int launch_quantize_dbias(const void *x, int x_dtype, int64_t rows, int64_t cols
 int launch_quantize(const void *x, int x_dtype, int64_t rows, int64_t cols, int fmt,
                     const float *scale, uint8_t *out, uint8_t *out_t, float *amax,
                     cudaStream_t s, const DeviceInfo &dev);
+// One GEMM out[rows_a x rows_b] = (A B^T) * sinv_a * sinv_b (+ bias), A and B
+// contiguous along the contraction of length kc.
+struct GemmDesc {
+    const uint8_t *a;
+    int fmt_a;
+    const uint8_t *b;
+    int fmt_b;
+    int64_t rows_a, rows_b, kc;
+    const float *sinv_a, *sinv_b;
+    const void *bias;
+    int bias_dtype;
+    void *out;
+    int out_dtype;
+    float *out_amax;
+    const float *out_scale;  // non-null: FP8 output of out_fmt under *out_scale
+    int out_fmt;
+};
+// Runs 1 or 2 independent GEMMs in one persistent launch.
+int launch_gemms(const GemmDesc *descs, int n, cudaStream_t s, const DeviceInfo &dev);
 int launch_gemm(const uint8_t *a, int fmt_a, const uint8_t *b, int fmt_b, int64_t rows_a,
                 int64_t rows_b, int64_t kc, const float *sinv_a, const float *sinv_b,
                 const void *bias, int bias_dtype, void *out, int out_dtype, float *out_amax,

@@ -96,6 +96,7 @@ struct Cfg {
 struct GemmParams {
     int rows_a, rows_b, num_kb;
     int tiles_m, tiles_n;
+    uint32_t idesc;           // tcgen05 instruction descriptor (operand formats, M, N)
     const float *sinv_a, *sinv_b;
     const void *bias;
     int bias_bf16;
@@ -105,6 +106,23 @@ struct GemmParams {
     int out_fmt;
     const float *out_scale;
     float *out_amax;
+};
+
+// One GEMM of a launch: its operand and output tensor maps and parameters.
+struct GemmProblem {
+    CUtensorMap ta, tb, to;
+    GemmParams p;
+};
+
+// Up to two independent GEMMs share one launch (the dgrad and wgrad GEMMs of
+// a layer's backward pass). Their tiles form one list, problem 0's first;
+// the host puts the problem with the longer contraction first.
+constexpr int MAX_PROBLEMS = 2;
+struct GemmBatch {
+    GemmProblem prob[MAX_PROBLEMS];
+    int nprob;
+    int tiles0;     // tiles of problem 0; problem 1's follow
+    int num_tiles;  // tiles of all problems
 };
 
 // ------------------------------------------------------------ PTX wrappers
@@ -316,6 +334,25 @@ __device__ __forceinline__ uint64_t sw128_kmajor_desc(uint32_t saddr) {
     return d;
 }
 
+// Tile of round `r` for cluster `c` of `nc`: one tile per cluster per round,
+// dealt forwards in even rounds and backwards in odd ones (serpentine). With
+// the tiles sorted by contraction length, longest first, the clusters that
+// got the last long tiles get the first short ones, which keeps the
+// per-cluster sums of k-blocks within one short tile of each other.
+__device__ __forceinline__ int serpentine_tile(int r, int c, int nc) {
+    return r * nc + ((r & 1) ? nc - 1 - c : c);
+}
+
+// The problem a tile of the batch belongs to, and its index within it.
+__device__ __forceinline__ int tile_problem(const GemmBatch &b, int t, int &local) {
+    if (t < b.tiles0) {
+        local = t;
+        return 0;
+    }
+    local = t - b.tiles0;
+    return 1;
+}
+
 // Tile index -> (row-block of A, row-block of B), grouped so that the CTAs
 // working at the same time share GROUP_M A panels and a few B panels in L2.
 __device__ __forceinline__ void tile_coords(int t, int tiles_m, int tiles_n, int &mb, int &nb) {
@@ -337,8 +374,7 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float a, float b) {
 
 template <bool PAIR>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
-gemm_fp8_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CUtensorMap tmap_b,
-                const __grid_constant__ CUtensorMap tmap_out, const GemmParams p, const uint32_t idesc) {
+gemm_fp8_kernel(const __grid_constant__ GemmBatch batch) {
     using C = Cfg<PAIR>;
     extern __shared__ uint8_t smem_raw[];
     uint32_t base = smem_u32(smem_raw);
@@ -372,9 +408,11 @@ gemm_fp8_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constan
         mbar_init(drain_bar, 1);
         *abort_flag = 0;
         fence_mbar_init();
-        prefetch_tmap(&tmap_a);
-        prefetch_tmap(&tmap_b);
-        prefetch_tmap(&tmap_out);
+        for (int i = 0; i < batch.nprob; ++i) {
+            prefetch_tmap(&batch.prob[i].ta);
+            prefetch_tmap(&batch.prob[i].tb);
+            prefetch_tmap(&batch.prob[i].to);
+        }
     }
     if (warp == 1) {
         tmem_alloc<PAIR>(smem_u32(tmem_slot), TMEM_COLS);
@@ -388,7 +426,8 @@ gemm_fp8_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constan
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
 
-    const int num_tiles = p.tiles_m * p.tiles_n;
+    const int num_tiles = batch.num_tiles;
+    const int rounds = (num_tiles + num_clusters - 1) / num_clusters;
 
     if (warp == 0) {
         if (lane == 0) {
@@ -396,12 +435,17 @@ gemm_fp8_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constan
             uint32_t it = 0;
             int issued_stages = 0;
             bool ok = true;
-            for (int tile = cluster_id; ok && tile < num_tiles; tile += num_clusters) {
+            for (int r = 0; ok && r < rounds; ++r) {
+                const int tile = serpentine_tile(r, cluster_id, num_clusters);
+                if (tile >= num_tiles) continue;
+                int local;
+                const GemmProblem &P = batch.prob[tile_problem(batch, tile, local)];
                 int mb, nb;
-                tile_coords(tile, p.tiles_m, p.tiles_n, mb, nb);
+                tile_coords(local, P.p.tiles_m, P.p.tiles_n, mb, nb);
                 const int a_row = mb * C::TILE_M + static_cast<int>(rank) * ROWS_A;
                 const int b_row = nb * TILE_N + static_cast<int>(rank) * C::ROWS_B;
-                for (int kb = 0; kb < p.num_kb; ++kb, ++it) {
+                const int num_kb = P.p.num_kb;
+                for (int kb = 0; kb < num_kb; ++kb, ++it) {
                     const int s = static_cast<int>(it % C::STAGES);
                     const uint32_t ph = (it / C::STAGES) & 1u;
                     if (!wait_bounded(empty_bar(s), ph ^ 1u, abort_flag)) {
@@ -412,8 +456,8 @@ gemm_fp8_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constan
                     // the full barrier of a pair lives in the MMA-issuing CTA
                     const uint32_t fb = PAIR ? mapa_shared(full_bar(s), 0) : full_bar(s);
                     if (rank == 0) mbar_arrive_expect_tx(full_bar(s), C::TX_BYTES);
-                    tma_load_2d<PAIR>(sa, &tmap_a, fb, kb * BK, a_row);
-                    tma_load_2d<PAIR>(sa + C::A_BYTES, &tmap_b, fb, kb * BK, b_row);
+                    tma_load_2d<PAIR>(sa, &P.ta, fb, kb * BK, a_row);
+                    tma_load_2d<PAIR>(sa + C::A_BYTES, &P.tb, fb, kb * BK, b_row);
                     if (issued_stages < C::STAGES) ++issued_stages;
                 }
             }
@@ -432,16 +476,23 @@ gemm_fp8_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constan
             uint32_t it = 0;
             int lt = 0;
             bool ok = true;
-            for (int tile = cluster_id; ok && tile < num_tiles; tile += num_clusters, ++lt) {
+            for (int r = 0; ok && r < rounds; ++r) {
+                const int tile = serpentine_tile(r, cluster_id, num_clusters);
+                if (tile >= num_tiles) continue;
+                int local;
+                const GemmProblem &P = batch.prob[tile_problem(batch, tile, local)];
+                const uint32_t idesc = P.p.idesc;
+                const int num_kb = P.p.num_kb;
                 const int acc = lt & 1;
                 const uint32_t aph = (static_cast<uint32_t>(lt) >> 1) & 1u;
+                ++lt;
                 if (!wait_bounded(tempty_bar(acc), aph ^ 1u, abort_flag)) {
                     ok = false;
                     break;
                 }
                 tc_fence_after();
                 const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * TILE_N);
-                for (int kb = 0; kb < p.num_kb; ++kb, ++it) {
+                for (int kb = 0; kb < num_kb; ++kb, ++it) {
                     const int s = static_cast<int>(it % C::STAGES);
                     const uint32_t ph = (it / C::STAGES) & 1u;
                     if (!wait_bounded(full_bar(s), ph, abort_flag)) {
@@ -471,87 +522,99 @@ gemm_fp8_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constan
     } else {
         // ---------------- epilogue warps (both CTAs of a pair)
         // Each warp drains its 32 TMEM lanes (32 output rows) in chunks of
-        // 128 bytes per row (64 bf16 or 32 fp32 columns): tcgen05.ld, scale,
-        // bias and rounding in registers, the row written into a 128-byte-
-        // swizzled 32 x 128 B staging box, then one TMA store per box. Two
-        // boxes per warp alternate so the next chunk overlaps the store.
+        // 128 bytes per row (64 bf16, 32 fp32 or 128 FP8 columns): tcgen05.ld,
+        // scale, bias and rounding in registers, the row written into a
+        // 128-byte-swizzled 32 x 128 B staging box, then one TMA store per
+        // box. Two boxes per warp alternate so the next chunk overlaps the
+        // store.
         const int q = warp & 3;  // this warp may access TMEM lanes 32q .. 32q+31
         const int row_in_tile = static_cast<int>(rank) * ROWS_A + q * 32 + lane;
-        const float scale = __fmul_rn(__ldg(p.sinv_a), __ldg(p.sinv_b));
-        const int box_cols = p.out_fp8 ? 128 : (p.out_bf16 ? 64 : 32);  // 128 bytes per row either way
-        const int parts = box_cols / 32;                                 // tcgen05.ld of 32 columns each
-        const float out_scale = p.out_fp8 ? __ldg(p.out_scale) : 1.0f;
         const uint32_t stage_box = base + C::EPI_OFFSET + static_cast<uint32_t>((warp - 2) * 2 * C::EPI_BOX_BYTES);
-        float am = 0.0f;
+        float am0 = 0.0f, am1 = 0.0f;  // max |y| of problem 0 / 1
         int lt = 0;
         uint32_t chunk_no = 0;
-        for (int tile = cluster_id; tile < num_tiles; tile += num_clusters, ++lt) {
+        for (int r = 0; r < rounds; ++r) {
+            const int tile = serpentine_tile(r, cluster_id, num_clusters);
+            if (tile >= num_tiles) continue;
+            int local;
+            const int pi = tile_problem(batch, tile, local);
+            const GemmProblem &P = batch.prob[pi];
             const int acc = lt & 1;
             const uint32_t aph = (static_cast<uint32_t>(lt) >> 1) & 1u;
+            ++lt;
             int ok = 1;
             if (lane == 0) ok = wait_bounded(tfull_bar(acc), aph, abort_flag) ? 1 : 0;
             ok = __shfl_sync(0xffffffffu, ok, 0);
             if (!ok) break;
             tc_fence_after();
+            const float scale = __fmul_rn(__ldg(P.p.sinv_a), __ldg(P.p.sinv_b));
+            const int out_fp8 = P.p.out_fp8, out_bf16 = P.p.out_bf16, out_fmt = P.p.out_fmt;
+            const int box_cols = out_fp8 ? 128 : (out_bf16 ? 64 : 32);  // 128 bytes per row either way
+            const int parts = box_cols / 32;                             // tcgen05.ld of 32 columns each
+            const float out_scale = out_fp8 ? __ldg(P.p.out_scale) : 1.0f;
+            const void *bias = P.p.bias;
+            const int bias_bf16 = P.p.bias_bf16;
+            const int rows_a = P.p.rows_a, rows_b = P.p.rows_b;
             int mb, nb;
-            tile_coords(tile, p.tiles_m, p.tiles_n, mb, nb);
+            tile_coords(local, P.p.tiles_m, P.p.tiles_n, mb, nb);
             const int64_t m = static_cast<int64_t>(mb) * C::TILE_M + row_in_tile;
-            const bool row_ok = m < p.rows_a;
+            const bool row_ok = m < rows_a;
             const int warp_row0 = mb * C::TILE_M + static_cast<int>(rank) * ROWS_A + q * 32;
+            float am = 0.0f;
 #pragma unroll 1
             for (int c = 0; c < TILE_N; c += box_cols, ++chunk_no) {
                 uint32_t packed[32];  // this lane's 128-byte row of the box
 #pragma unroll
                 for (int half = 0; half < 4; ++half) {
                     if (half >= parts) break;
-                    uint32_t r[32];
+                    uint32_t r32[32];
                     const int c32 = c + 32 * half;
                     tmem_ld32(tmem_base + static_cast<uint32_t>(acc * TILE_N + c32) +
                                   (static_cast<uint32_t>(q * 32) << 16),
-                              r);
+                              r32);
 #pragma unroll
                     for (int g = 0; g < 2; ++g) {  // 16-column groups
                         const int n = nb * TILE_N + c32 + 16 * g;
-                        const bool col_ok = n < p.rows_b;
+                        const bool col_ok = n < rows_b;
                         float y[16];
-                        if (p.bias == nullptr || !col_ok) {
+                        if (bias == nullptr || !col_ok) {
 #pragma unroll
-                            for (int j = 0; j < 16; ++j) y[j] = __fmul_rn(__uint_as_float(r[16 * g + j]), scale);
-                        } else if (p.bias_bf16) {
-                            const uint4 *bp = reinterpret_cast<const uint4 *>(static_cast<const uint16_t *>(p.bias) + n);
+                            for (int j = 0; j < 16; ++j) y[j] = __fmul_rn(__uint_as_float(r32[16 * g + j]), scale);
+                        } else if (bias_bf16) {
+                            const uint4 *bp = reinterpret_cast<const uint4 *>(static_cast<const uint16_t *>(bias) + n);
                             const uint4 b0 = __ldg(bp), b1 = __ldg(bp + 1);
                             const uint32_t bw[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
 #pragma unroll
                             for (int j = 0; j < 8; ++j) {
-                                y[2 * j] = __fmaf_rn(__uint_as_float(r[16 * g + 2 * j]), scale,
+                                y[2 * j] = __fmaf_rn(__uint_as_float(r32[16 * g + 2 * j]), scale,
                                                      __uint_as_float(bw[j] << 16));
-                                y[2 * j + 1] = __fmaf_rn(__uint_as_float(r[16 * g + 2 * j + 1]), scale,
+                                y[2 * j + 1] = __fmaf_rn(__uint_as_float(r32[16 * g + 2 * j + 1]), scale,
                                                          __uint_as_float(bw[j] & 0xFFFF0000u));
                             }
                         } else {
-                            const float4 *bp = reinterpret_cast<const float4 *>(static_cast<const float *>(p.bias) + n);
+                            const float4 *bp = reinterpret_cast<const float4 *>(static_cast<const float *>(bias) + n);
 #pragma unroll
                             for (int j = 0; j < 4; ++j) {
                                 const float4 bb = __ldg(bp + j);
-                                y[4 * j] = __fmaf_rn(__uint_as_float(r[16 * g + 4 * j]), scale, bb.x);
-                                y[4 * j + 1] = __fmaf_rn(__uint_as_float(r[16 * g + 4 * j + 1]), scale, bb.y);
-                                y[4 * j + 2] = __fmaf_rn(__uint_as_float(r[16 * g + 4 * j + 2]), scale, bb.z);
-                                y[4 * j + 3] = __fmaf_rn(__uint_as_float(r[16 * g + 4 * j + 3]), scale, bb.w);
+                                y[4 * j] = __fmaf_rn(__uint_as_float(r32[16 * g + 4 * j]), scale, bb.x);
+                                y[4 * j + 1] = __fmaf_rn(__uint_as_float(r32[16 * g + 4 * j + 1]), scale, bb.y);
+                                y[4 * j + 2] = __fmaf_rn(__uint_as_float(r32[16 * g + 4 * j + 2]), scale, bb.z);
+                                y[4 * j + 3] = __fmaf_rn(__uint_as_float(r32[16 * g + 4 * j + 3]), scale, bb.w);
                             }
                         }
                         if (row_ok && col_ok) {
 #pragma unroll
                             for (int j = 0; j < 16; ++j) am = max_ignore_nan(am, fabsf(y[j]));
                         }
-                        if (p.out_fp8) {
+                        if (out_fp8) {
 #pragma unroll
                             for (int j = 0; j < 4; ++j) {
                                 const float a0 = __fmul_rn(y[4 * j], out_scale), a1 = __fmul_rn(y[4 * j + 1], out_scale);
                                 const float a2 = __fmul_rn(y[4 * j + 2], out_scale), a3 = __fmul_rn(y[4 * j + 3], out_scale);
-                                packed[8 * half + 4 * g + j] = p.out_fmt == FP8MP_E4M3 ? cvt_quad<FP8MP_E4M3>(a0, a1, a2, a3)
-                                                                                      : cvt_quad<FP8MP_E5M2>(a0, a1, a2, a3);
+                                packed[8 * half + 4 * g + j] = out_fmt == FP8MP_E4M3 ? cvt_quad<FP8MP_E4M3>(a0, a1, a2, a3)
+                                                                                    : cvt_quad<FP8MP_E5M2>(a0, a1, a2, a3);
                             }
-                        } else if (p.out_bf16) {
+                        } else if (out_bf16) {
 #pragma unroll
                             for (int j = 0; j < 8; ++j) packed[16 * half + 8 * g + j] = pack_bf16x2(y[2 * j], y[2 * j + 1]);
                         } else {
@@ -572,11 +635,15 @@ gemm_fp8_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constan
                 fence_proxy_async_smem();
                 __syncwarp();
                 // boxes that start outside the output (ragged last tiles) are not stored
-                if (lane == 0 && nb * TILE_N + c < p.rows_b && warp_row0 < p.rows_a) {
-                    tma_store_2d(&tmap_out, box, nb * TILE_N + c, warp_row0);
+                if (lane == 0 && nb * TILE_N + c < rows_b && warp_row0 < rows_a) {
+                    tma_store_2d(&P.to, box, nb * TILE_N + c, warp_row0);
                     bulk_commit_group();
                 }
             }
+            if (pi == 0)
+                am0 = max_ignore_nan(am0, am);
+            else
+                am1 = max_ignore_nan(am1, am);
             tc_fence_before();
             __syncwarp();
             if (lane == 0) {
@@ -587,10 +654,12 @@ gemm_fp8_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constan
             }
         }
         if (lane == 0) bulk_wait_all();  // stores done before the CTA's shared memory goes away
-        if (p.out_amax != nullptr) {
-            am = warp_max(am);
-            if (p.out_bf16 && !p.out_fp8) am = __bfloat162float(__float2bfloat16_rn(am));  // max of the stored values
-            if (lane == 0) atomicMax(reinterpret_cast<int *>(p.out_amax), __float_as_int(am));
+        for (int i = 0; i < batch.nprob; ++i) {
+            const GemmParams &pp = batch.prob[i].p;
+            if (pp.out_amax == nullptr) continue;
+            float a = warp_max(i == 0 ? am0 : am1);
+            if (pp.out_bf16 && !pp.out_fp8) a = __bfloat162float(__float2bfloat16_rn(a));  // max of the stored values
+            if (lane == 0) atomicMax(reinterpret_cast<int *>(pp.out_amax), __float_as_int(a));
         }
     }
 
@@ -715,8 +784,7 @@ struct PerDevice {
 PerDevice g_dev[64];
 
 template <bool PAIR>
-int launch_engine(const CUtensorMap &ta, const CUtensorMap &tb, const CUtensorMap &to, const GemmParams &p, int grid,
-                  uint32_t idesc, cudaStream_t s) {
+int launch_engine(const GemmBatch &batch, int grid, cudaStream_t s) {
     using C = Cfg<PAIR>;
     cudaLaunchConfig_t cfg = {};
     cudaLaunchAttribute attr[1];
@@ -732,7 +800,7 @@ int launch_engine(const CUtensorMap &ta, const CUtensorMap &tb, const CUtensorMa
         cfg.attrs = attr;
         cfg.numAttrs = 1;
     }
-    const cudaError_t e = cudaLaunchKernelEx(&cfg, gemm_fp8_kernel<PAIR>, ta, tb, to, p, idesc);
+    const cudaError_t e = cudaLaunchKernelEx(&cfg, gemm_fp8_kernel<PAIR>, batch);
     if (e != cudaSuccess) return fail(FP8MP_ERR_LAUNCH, "GEMM launch failed: %s", cudaGetErrorString(e));
     return FP8MP_OK;
 }
@@ -768,44 +836,42 @@ int prepare_engine(const DeviceInfo &dev) {
 
 }  // namespace
 
-int launch_gemm(const uint8_t *a, int fmt_a, const uint8_t *b, int fmt_b, int64_t rows_a, int64_t rows_b,
-                int64_t kc, const float *sinv_a, const float *sinv_b, const void *bias, int bias_dtype, void *out,
-                int out_dtype, float *out_amax, cudaStream_t s, const DeviceInfo &dev, const float *out_scale,
-                int out_fmt) {
-    if (rows_a == 0 || rows_b == 0) return FP8MP_OK;
-    if (rows_a > (1ll << 30) || rows_b > (1ll << 30) || kc > (1ll << 30))
-        return fail(FP8MP_ERR_INVALID, "GEMM dimension above 2^30");
-    if (kc == 0) {
-        int64_t blocks = (rows_a * rows_b + 255) / 256;
-        if (blocks > dev.num_sms * 8) blocks = dev.num_sms * 8;
-        fill_bias_kernel<<<static_cast<unsigned>(blocks), 256, 0, s>>>(rows_a, rows_b, bias, bias_dtype == FP8MP_BF16,
-                                                                      out, out_dtype == FP8MP_BF16, out_amax,
-                                                                      out_scale, out_fmt);
-        const cudaError_t e = cudaGetLastError();
-        if (e != cudaSuccess) return fail(FP8MP_ERR_LAUNCH, "GEMM fill launch failed: %s", cudaGetErrorString(e));
-        return FP8MP_OK;
+int launch_gemms(const GemmDesc *descs, int n, cudaStream_t s, const DeviceInfo &dev) {
+    if (n < 1 || n > MAX_PROBLEMS) return fail(FP8MP_ERR_INVALID, "a GEMM launch takes 1 or 2 problems");
+    const GemmDesc *work[MAX_PROBLEMS];
+    int nw = 0;
+    for (int i = 0; i < n; ++i) {
+        const GemmDesc &d = descs[i];
+        if (d.rows_a == 0 || d.rows_b == 0) continue;
+        if (d.rows_a > (1ll << 30) || d.rows_b > (1ll << 30) || d.kc > (1ll << 30))
+            return fail(FP8MP_ERR_INVALID, "GEMM dimension above 2^30");
+        if (d.kc == 0) {
+            int64_t blocks = (d.rows_a * d.rows_b + 255) / 256;
+            if (blocks > dev.num_sms * 8) blocks = dev.num_sms * 8;
+            fill_bias_kernel<<<static_cast<unsigned>(blocks), 256, 0, s>>>(
+                d.rows_a, d.rows_b, d.bias, d.bias_dtype == FP8MP_BF16, d.out, d.out_dtype == FP8MP_BF16,
+                d.out_amax, d.out_scale, d.out_fmt);
+            const cudaError_t e = cudaGetLastError();
+            if (e != cudaSuccess) return fail(FP8MP_ERR_LAUNCH, "GEMM fill launch failed: %s", cudaGetErrorString(e));
+            continue;
+        }
+        work[nw++] = &d;
     }
-    GemmParams p;
-    p.rows_a = static_cast<int>(rows_a);
-    p.rows_b = static_cast<int>(rows_b);
-    p.num_kb = static_cast<int>((kc + BK - 1) / BK);
-    p.tiles_n = static_cast<int>((rows_b + TILE_N - 1) / TILE_N);
-    p.sinv_a = sinv_a;
-    p.sinv_b = sinv_b;
-    p.bias = bias;
-    p.bias_bf16 = bias_dtype == FP8MP_BF16;
-    p.out = out;
-    p.out_bf16 = out_dtype == FP8MP_BF16;
-    p.out_fp8 = out_scale != nullptr;
-    p.out_fmt = out_fmt;
-    p.out_scale = out_scale;
-    p.out_amax = out_amax;
+    if (nw == 0) return FP8MP_OK;
+    // longest contraction first: the serpentine deal then balances the
+    // clusters' k-blocks (see serpentine_tile)
+    if (nw == 2 && work[1]->kc > work[0]->kc) {
+        const GemmDesc *t = work[0];
+        work[0] = work[1];
+        work[1] = t;
+    }
 
     // Pairs of SMs on 256 x 256 tiles when there are enough tiles to occupy
     // most SMs; otherwise single-SM 128 x 256 tiles (twice as many tiles).
     // FP8MP_GEMM_ENGINE=pair|single overrides the choice (used by the tests
     // to run both engines on every shape).
-    const int64_t pair_tiles = ((rows_a + 255) / 256) * p.tiles_n;
+    int64_t pair_tiles = 0;
+    for (int i = 0; i < nw; ++i) pair_tiles += ((work[i]->rows_a + 255) / 256) * ((work[i]->rows_b + TILE_N - 1) / TILE_N);
     bool pair = pair_tiles * 2 >= dev.num_sms;
     if (const char *force = std::getenv("FP8MP_GEMM_ENGINE")) {
         if (std::strcmp(force, "pair") == 0) pair = true;
@@ -814,30 +880,61 @@ int launch_gemm(const uint8_t *a, int fmt_a, const uint8_t *b, int fmt_b, int64_
     int rc = pair ? prepare_engine<true>(dev) : prepare_engine<false>(dev);
     if (rc) return rc;
 
-    CUtensorMap ta, tb;
-    rc = make_tmap(&ta, a, static_cast<uint64_t>(kc), static_cast<uint64_t>(rows_a), ROWS_A);
-    if (rc) return rc;
-    rc = make_tmap(&tb, b, static_cast<uint64_t>(kc), static_cast<uint64_t>(rows_b),
-                   pair ? Cfg<true>::ROWS_B : Cfg<false>::ROWS_B);
-    if (rc) return rc;
-    CUtensorMap to;
-    rc = make_out_tmap(&to, out, static_cast<uint64_t>(rows_b), static_cast<uint64_t>(rows_a), p.out_bf16 != 0,
-                       p.out_fp8 != 0);
-    if (rc) return rc;
+    GemmBatch batch;
+    std::memset(&batch, 0, sizeof batch);
+    batch.nprob = nw;
+    int64_t tiles = 0;
+    for (int i = 0; i < nw; ++i) {
+        const GemmDesc &d = *work[i];
+        GemmProblem &P = batch.prob[i];
+        GemmParams &p = P.p;
+        p.rows_a = static_cast<int>(d.rows_a);
+        p.rows_b = static_cast<int>(d.rows_b);
+        p.num_kb = static_cast<int>((d.kc + BK - 1) / BK);
+        p.tiles_n = static_cast<int>((d.rows_b + TILE_N - 1) / TILE_N);
+        p.tiles_m = static_cast<int>(pair ? (d.rows_a + 255) / 256 : (d.rows_a + 127) / 128);
+        p.idesc = make_idesc(d.fmt_a, d.fmt_b, pair ? 256 : 128);
+        p.sinv_a = d.sinv_a;
+        p.sinv_b = d.sinv_b;
+        p.bias = d.bias;
+        p.bias_bf16 = d.bias_dtype == FP8MP_BF16;
+        p.out = d.out;
+        p.out_bf16 = d.out_dtype == FP8MP_BF16;
+        p.out_fp8 = d.out_scale != nullptr;
+        p.out_fmt = d.out_fmt;
+        p.out_scale = d.out_scale;
+        p.out_amax = d.out_amax;
+        rc = make_tmap(&P.ta, d.a, static_cast<uint64_t>(d.kc), static_cast<uint64_t>(d.rows_a), ROWS_A);
+        if (rc) return rc;
+        rc = make_tmap(&P.tb, d.b, static_cast<uint64_t>(d.kc), static_cast<uint64_t>(d.rows_b),
+                       pair ? Cfg<true>::ROWS_B : Cfg<false>::ROWS_B);
+        if (rc) return rc;
+        rc = make_out_tmap(&P.to, d.out, static_cast<uint64_t>(d.rows_b), static_cast<uint64_t>(d.rows_a),
+                           p.out_bf16 != 0, p.out_fp8 != 0);
+        if (rc) return rc;
+        const int64_t t = static_cast<int64_t>(p.tiles_m) * p.tiles_n;
+        if (i == 0) batch.tiles0 = static_cast<int>(t < 0x7FFFFFFF ? t : 0x7FFFFFFF);
+        tiles += t;
+    }
+    if (tiles > 0x7FFFFFFF) return fail(FP8MP_ERR_INVALID, "GEMM has too many tiles");
+    batch.num_tiles = static_cast<int>(tiles);
 
     if (pair) {
-        p.tiles_m = static_cast<int>((rows_a + 255) / 256);
-        const int64_t tiles = static_cast<int64_t>(p.tiles_m) * p.tiles_n;
-        if (tiles > 0x7FFFFFFF) return fail(FP8MP_ERR_INVALID, "GEMM has too many tiles");
         const int max_pairs = g_dev[dev.device & 63].max_pairs;
         const int clusters = static_cast<int>(tiles < max_pairs ? tiles : max_pairs);
-        return launch_engine<true>(ta, tb, to, p, 2 * clusters, make_idesc(fmt_a, fmt_b, 256), s);
+        return launch_engine<true>(batch, 2 * clusters, s);
     }
-    p.tiles_m = static_cast<int>((rows_a + 127) / 128);
-    const int64_t tiles = static_cast<int64_t>(p.tiles_m) * p.tiles_n;
-    if (tiles > 0x7FFFFFFF) return fail(FP8MP_ERR_INVALID, "GEMM has too many tiles");
     const int grid = static_cast<int>(tiles < dev.num_sms ? tiles : dev.num_sms);
-    return launch_engine<false>(ta, tb, to, p, grid, make_idesc(fmt_a, fmt_b, 128), s);
+    return launch_engine<false>(batch, grid, s);
+}
+
+int launch_gemm(const uint8_t *a, int fmt_a, const uint8_t *b, int fmt_b, int64_t rows_a, int64_t rows_b,
+                int64_t kc, const float *sinv_a, const float *sinv_b, const void *bias, int bias_dtype, void *out,
+                int out_dtype, float *out_amax, cudaStream_t s, const DeviceInfo &dev, const float *out_scale,
+                int out_fmt) {
+    const GemmDesc d = {a,    fmt_a,      b,   fmt_b,     rows_a,   rows_b,    kc,     sinv_a,
+                        sinv_b, bias, bias_dtype, out, out_dtype, out_amax, out_scale, out_fmt};
+    return launch_gemms(&d, 1, s, dev);
 }
 
 int launch_timeout_selftest(cudaStream_t s) {

@@ -7,7 +7,8 @@ DelayedScaling recipe with the HYBRID format: E4M3 for the input and the
 weight in the forward GEMM, E5M2 for the output gradient in dgrad and wgrad.
 
 Every step of the layer is a call into libfp8mp (casts with transposed
-copies and amaxes, the three FP8 GEMMs, the fused bias gradient); this file
+copies and amaxes, the forward GEMM, the fused dgrad + wgrad launch, the
+fused bias gradient); this file
 only allocates the outputs through torch and passes pointers. Like
 sync_float8_amax_and_scale_history after backward in the pages' training
 loop, ``update_scales()`` runs the delayed-scaling update of the layer's
@@ -18,8 +19,8 @@ from __future__ import annotations
 
 import torch
 
-from . import (AMAX_MAX, E4M3, E5M2, Meta, delayed_scaling_update, fp8_linear_dgrad, fp8_linear_fwd,
-               fp8_linear_wgrad, fp8_quantize, fp8_quantize_dbias, fp8_quantize_dbias_workspace_bytes)
+from . import (AMAX_MAX, E4M3, E5M2, Meta, delayed_scaling_update, fp8_linear_bwd, fp8_linear_fwd, fp8_quantize,
+               fp8_quantize_dbias, fp8_quantize_dbias_workspace_bytes)
 
 __all__ = ["FP8Linear"]
 
@@ -75,9 +76,9 @@ class _FP8LinearFn(torch.autograd.Function):
             fp8_quantize(dy2, E5M2, md.scale, D8, D8t, md.cur_amax)
         sinv_dy = md.scale_inv.clone()
         dx = torch.empty((M, K), dtype=x_dtype, device=dev)
-        fp8_linear_dgrad(D8, W8t, sinv_dy, sinv_w, dx, dy_fmt=E5M2)
         dw = torch.empty((N, K), dtype=w_dtype, device=dev)
-        fp8_linear_wgrad(D8t, X8t, sinv_dy, sinv_x, dw, dy_fmt=E5M2)
+        # dgrad and wgrad in one launch
+        fp8_linear_bwd(D8, D8t, W8t, X8t, sinv_dy, sinv_w, sinv_x, dx, dw, dy_fmt=E5M2)
         return dx.reshape(x_shape), dw, db, None
 
 

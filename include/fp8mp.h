@@ -250,6 +250,29 @@ int fp8_linear_wgrad(const uint8_t *dy8t, const uint8_t *x8t, int64_t M, int64_t
                      int32_t dw_dtype, void *stream);
 
 /*
+ * fp8_linear_bwd -- both backward GEMMs of the linear layer in one launch:
+ * exactly fp8_linear_dgrad and fp8_linear_wgrad above on the same arguments
+ * (same per-element sums in the same order, so the results are bitwise those
+ * of the two separate calls):
+ *   dx[m, k] = (sum_n dy8[m, n]  * w8t[k, n]) * sinv_dy[0] * sinv_w[0]
+ *   dw[n, k] = (sum_m dy8t[n, m] * x8t[k, m]) * sinv_dy[0] * sinv_x[0]
+ * The two GEMMs are independent ([TE-FP8] "Backward Pass 처리": the input
+ * gradient and the weight gradient both come from the one output gradient),
+ * so their output tiles share one persistent grid, which keeps every SM busy
+ * through the tail of the shorter GEMM instead of idling at each launch's
+ * last partial wave.
+ *
+ * dy8 [M x N] and dy8t [N x M]: codes of dy_fmt (the output gradient and its
+ * transposed copy, as fp8_quantize writes them); w8t [K x N], x8t [K x M]:
+ * E4M3 codes. dx [M x K] of dx_dtype, dw [N x K] of dw_dtype, both required
+ * when non-empty and not overlapping. M, N, K multiples of 16. Empty cases
+ * follow the separate calls: N == 0 gives dx = 0, M == 0 gives dw = 0.
+ */
+int fp8_linear_bwd(const uint8_t *dy8, const uint8_t *dy8t, const uint8_t *w8t, const uint8_t *x8t, int64_t M,
+                   int64_t N, int64_t K, int32_t dy_fmt, const float *sinv_dy, const float *sinv_w,
+                   const float *sinv_x, void *dx, int32_t dx_dtype, void *dw, int32_t dw_dtype, void *stream);
+
+/*
  * delayed_scaling_update -- the DelayedScaling bookkeeping of one step for a
  * batch of tensors ([TE-FP8] "Scaling factor 선택 전략", "FP8 사용방안(recipe)":
  * amax_history_len, amax_compute_algo; [PT-FP8] amax and scale history

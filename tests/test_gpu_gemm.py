@@ -93,6 +93,56 @@ def test_dgrad_and_wgrad(cuda_lib, orc, engine, dy_fmt, M, N, K):
         gemm_tolerance_check(np_view(dw.float()).astype(np.float64), ref, ab, "wgrad")
 
 
+# (M, N, K): wgrad contracts over M, dgrad over N, so these put either GEMM
+# in the longer-contraction (first) slot, and include ragged tiles
+BWD_SHAPES = [(256, 512, 256), (1040, 784, 784), (2048, 256, 1024), (256, 2048, 528), (16, 16, 16),
+              (1024, 768, 768)]
+
+
+@pytest.mark.parametrize("M,N,K", BWD_SHAPES)
+@pytest.mark.parametrize("dy_fmt,dx_dt,dw_dt", [(E5M2, "bf16", "f32"), (E4M3, "f32", "bf16")])
+def test_fused_backward_equals_separate_calls(cuda_lib, orc, engine, M, N, K, dy_fmt, dx_dt, dw_dt):
+    """fp8_linear_bwd gives bitwise the results of fp8_linear_dgrad and
+    fp8_linear_wgrad (same sums in the same order per element), and both are
+    within the GEMM tolerance of the oracle."""
+    rng = np.random.default_rng(3 * M + 5 * N + 7 * K + dy_fmt)
+    dy8 = finite_codes(rng, (M, N), dy_fmt)
+    dy8t = np.ascontiguousarray(dy8.T)
+    w8t = finite_codes(rng, (K, N), E4M3)
+    x8t = finite_codes(rng, (K, M), E4M3)
+    s_dy, s_w, s_x = 2.0 ** -10, 0.75, 0.0625
+    dx = torch.full((M, K), 5.0, dtype=TORCH_DT[dx_dt], device="cuda")
+    dw = torch.full((N, K), 5.0, dtype=TORCH_DT[dw_dt], device="cuda")
+    cuda_lib.fp8_linear_bwd(dev(dy8), dev(dy8t), dev(w8t), dev(x8t), sc(s_dy), sc(s_w), sc(s_x), dx, dw,
+                            dy_fmt=dy_fmt)
+    dx1, dw1 = torch.empty_like(dx), torch.empty_like(dw)
+    cuda_lib.fp8_linear_dgrad(dev(dy8), dev(w8t), sc(s_dy), sc(s_w), dx1, dy_fmt=dy_fmt)
+    cuda_lib.fp8_linear_wgrad(dev(dy8t), dev(x8t), sc(s_dy), sc(s_x), dw1, dy_fmt=dy_fmt)
+    assert cuda_lib.fp8mp_check() == 0
+    assert torch.equal(dx.view(torch.int16) if dx_dt == "bf16" else dx.view(torch.int32),
+                       dx1.view(torch.int16) if dx_dt == "bf16" else dx1.view(torch.int32))
+    assert torch.equal(dw.view(torch.int16) if dw_dt == "bf16" else dw.view(torch.int32),
+                       dw1.view(torch.int16) if dw_dt == "bf16" else dw1.view(torch.int32))
+    ref, ab = orc.gemm_ref(dy8, dy_fmt, w8t, E4M3, s_dy, s_w)
+    gemm_tolerance_check(np_view(dx.float()).astype(np.float64), ref, ab, f"bwd dx {M}x{N}x{K}")
+    ref, ab = orc.gemm_ref(dy8t, dy_fmt, x8t, E4M3, s_dy, s_x)
+    gemm_tolerance_check(np_view(dw.float()).astype(np.float64), ref, ab, f"bwd dw {M}x{N}x{K}")
+
+
+def test_fused_backward_empty_sides(cuda_lib, engine):
+    """N == 0: dx is the empty sum (0) and dw is empty; M == 0: dw = 0."""
+    one = sc(1.0)
+    u8 = lambda r, c: torch.empty((r, c), dtype=torch.uint8, device="cuda")
+    dx = torch.full((32, 48), 3.0, device="cuda")
+    cuda_lib.fp8_linear_bwd(u8(32, 0), u8(0, 32), u8(48, 0), u8(48, 32), one, one, one, dx,
+                            torch.empty((0, 48), device="cuda"))
+    dw = torch.full((64, 48), 3.0, dtype=torch.bfloat16, device="cuda")
+    cuda_lib.fp8_linear_bwd(u8(0, 64), u8(64, 0), u8(48, 64), u8(48, 0), one, one, one,
+                            torch.empty((0, 48), device="cuda"), dw)
+    assert cuda_lib.fp8mp_check() == 0
+    assert (dx.cpu() == 0).all() and (dw.float().cpu() == 0).all()
+
+
 def test_long_contraction_e5m2_wgrad(cuda_lib, orc, engine):
     """wgrad contracts over all tokens: 16384 here (the MLP workload's M)."""
     N, K, M = 256, 384, 16384
@@ -162,3 +212,14 @@ def test_metric_shape_full_size_sampled(cuda_lib, orc):
     wrows = rows[rows < N]
     ref, ab = orc.gemm_ref(dy8t, E5M2, x8t, E4M3, sinv["dy"], sinv["x"], rows=wrows)
     gemm_tolerance_check(np_view(dw.float())[wrows].astype(np.float64), ref, ab, "wgrad 8192x4096x4096")
+
+    # the fused backward launch (the bench step's) gives the same bits
+    dx = torch.empty((M, K), dtype=torch.bfloat16, device="cuda")
+    dx1 = torch.empty((M, K), dtype=torch.bfloat16, device="cuda")
+    dw1 = torch.empty((N, K), dtype=torch.bfloat16, device="cuda")
+    d8, d8t, w8t_d, x8t_d = dev(codes["dy"]), dev(dy8t), dev(w8t), dev(x8t)
+    cuda_lib.fp8_linear_bwd(d8, d8t, w8t_d, x8t_d, sc(sinv["dy"]), sc(sinv["w"]), sc(sinv["x"]), dx1, dw1)
+    cuda_lib.fp8_linear_dgrad(d8, w8t_d, sc(sinv["dy"]), sc(sinv["w"]), dx)
+    assert cuda_lib.fp8mp_check() == 0
+    assert torch.equal(dx1.view(torch.int16), dx.view(torch.int16))
+    assert torch.equal(dw1.view(torch.int16), dw.view(torch.int16))

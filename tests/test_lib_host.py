@@ -29,7 +29,7 @@ def declared_functions():
 
 def test_header_declares_the_boundary():
     names = declared_functions()
-    for n in ("fp8_quantize", "fp8_linear_fwd", "fp8_linear_dgrad", "fp8_linear_wgrad",
+    for n in ("fp8_quantize", "fp8_linear_fwd", "fp8_linear_dgrad", "fp8_linear_wgrad", "fp8_linear_bwd",
               "delayed_scaling_update", "mp_master_step", "fp8mp_check", "fp8mp_last_error",
               "fp8mp_version"):
         assert n in names
@@ -87,6 +87,26 @@ def test_gemms_reject_bad_shapes(lib):
     # bad enums
     assert lib.fp8_linear_fwd(P, P, 32, 32, 32, P, P, None, 0, P, 9, None, None) == fp8mp.ERR_INVALID
     assert lib.fp8_linear_dgrad(P, P, 32, 32, 32, 3, P, P, P, 1, None) == fp8mp.ERR_INVALID
+
+
+def test_fused_backward_rejects_bad_arguments(lib):
+    P = 1 << 20  # fake, aligned addresses: never dereferenced, validation fails first
+    bwd = lambda M, N, K, dx=P, dw=2 * P, fmt=1, dxt=1, dwt=1: lib.fp8_linear_bwd(
+        P, P, P, P, M, N, K, fmt, P, P, P, dx, dxt, dw, dwt, None)
+    for shape in ((24, 32, 32), (32, 40, 32), (32, 32, 8), (-16, 32, 32), (1 << 31, 32, 32)):
+        assert bwd(*shape) == fp8mp.ERR_INVALID
+    assert bwd(32, 32, 32, fmt=2) == fp8mp.ERR_INVALID
+    assert bwd(32, 32, 32, dxt=5) == fp8mp.ERR_INVALID and "dx_dtype" in fp8mp.last_error()
+    assert bwd(32, 32, 32, dwt=5) == fp8mp.ERR_INVALID and "dw_dtype" in fp8mp.last_error()
+    assert bwd(32, 32, 32, dw=None) == fp8mp.ERR_INVALID
+    assert bwd(32, 32, 32, dx=P + 4) == fp8mp.ERR_INVALID and "aligned" in fp8mp.last_error()
+    # dx (32 x 32 bf16 = 2 KiB) and dw must not overlap
+    assert bwd(32, 32, 32, dx=P, dw=P + 1024) == fp8mp.ERR_INVALID and "overlap" in fp8mp.last_error()
+    # empty outputs are no-ops needing no pointer and no device
+    assert lib.fp8_linear_bwd(None, None, None, None, 32, 32, 0, 1, None, None, None, None, 1, None, 1,
+                              None) == fp8mp.OK
+    assert lib.fp8_linear_bwd(None, None, None, None, 0, 0, 32, 1, None, None, None, None, 1, None, 1,
+                              None) == fp8mp.OK
 
 
 def test_scale_update_rejects_bad_metas(lib):
