@@ -67,9 +67,9 @@ def load_peaks():
         return {"bf16_tflops": FALLBACK_BF16_TFLOPS, "hbm_gbs": 6800.0}, "fallback"
 
 
-def gemm_traffic_from_profile():
-    """DRAM bytes per launch from the committed ncu summary, if it was taken
-    on the current gemm.cu (its sha256 is recorded there); else None."""
+def gemm_traffic_from_profile(key="dram_bytes_per_launch"):
+    """DRAM bytes per launch (`key`) from the committed ncu summary, if it was
+    taken on the current gemm.cu (its sha256 is recorded there); else None."""
     try:
         text = open(PROFILE).read()
     except OSError:
@@ -84,7 +84,7 @@ def gemm_traffic_from_profile():
     if vals.get("gemm_cu_sha256") != sha:
         return None
     try:
-        return float(vals["dram_bytes_per_launch"])
+        return float(vals[key])
     except (KeyError, ValueError):
         return None
 
@@ -420,6 +420,8 @@ def run_ours(args, world, rank, local):
         "roofline": {"kernel": "gemm_fp8_kernel", "bound": "tensor", "achieved": round(achieved, 2),
                      "peak": round(fp8_peak, 1), "unit": "TFLOP/s", "frac": round(achieved / fp8_peak, 4),
                      "traffic": traffic,
+                     "traffic_by_launch": {"fwd": gemm_traffic_from_profile("dram_bytes_fwd_launch"),
+                                           "bwd": gemm_traffic_from_profile("dram_bytes_bwd_launch")},
                      "peak_source": f"{peak_kind} bf16 burst x {FP8_OVER_BF16:g} (nominal fp8/bf16 dense ratio)"},
         "e2e": {"value": round(world * fl / (e2e_ms * 1e-3) / 1e12, 2), "unit": "TFLOP/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 5),

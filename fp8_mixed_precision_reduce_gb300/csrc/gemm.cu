@@ -13,7 +13,9 @@
 // "FP8 사용방안(recipe)" (HYBRID: E5M2 gradients against E4M3 operands).
 //
 // Computes out[i, j] = (sum_k A[i, k] * B[j, k]) * sinv_a * sinv_b + bias[j]
-// with A (rows_a x kc) and B (rows_b x kc) both contiguous along k.
+// with A (rows_a x kc) and B (rows_b x kc) both contiguous along k. One
+// launch runs one such GEMM, or two independent ones (the dgrad and wgrad
+// GEMMs of a backward pass) whose tiles share the persistent grid.
 //
 // Two tile engines share this file:
 //   PAIR = true  -- a cluster of two CTAs on the two SMs of a TPC computes a
@@ -27,7 +29,8 @@
 //   PAIR = false -- one CTA computes a 128 x 256 tile with
 //                   tcgen05.mma.cta_group::1 (4-stage, 48 KB ring); used when
 //                   a problem has too few 256 x 256 tiles to fill the GPU.
-// In both, one CTA per SM runs persistently over tiles:
+// In both, one CTA per SM runs persistently over tiles, dealt one per
+// cluster per round in serpentine order (longest contraction first):
 //   warp 0, one lane  : TMA producer (128-byte-swizzled boxes), waits on the
 //                       stage's empty mbarrier, arms / signals its full one;
 //   warp 1, one lane  : MMA issuer (even CTA only with PAIR), 4 MMAs per
@@ -37,12 +40,14 @@
 //                       previous tile's epilogue;
 //   warps 2-5         : epilogue -- tcgen05.ld of the warp's 32 TMEM lanes,
 //                       y = acc * (sinv_a * sinv_b) + bias, rounding to the
-//                       output type, 16-byte stores, running max |y|; one
-//                       atomic max per warp at the end.
-// Every mbarrier wait is bounded (about 2 s of %globaltimer); on expiry the
-// thread raises a device flag that fp8mp_check() reports, tells the other
-// roles of its CTA to stop, waits (bounded) for its own copies / MMAs in
-// flight, and the CTA frees its TMEM and returns.
+//                       output type into 128-byte-swizzled staging boxes in
+//                       shared memory, one TMA bulk store per 32-row box,
+//                       running max |y|; one atomic max per warp at the end.
+// Every mbarrier wait sleeps in mbarrier.try_wait and is bounded (about 2 s
+// of SM clock cycles, read with clock64); on expiry the thread raises a
+// device flag that fp8mp_check() reports, tells the other roles of its CTA
+// to stop, waits (bounded) for its own copies / MMAs in flight, and the CTA
+// frees its TMEM and returns.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
