@@ -5,14 +5,19 @@ One step = one mixed-precision training step of the proj linear of the
 transformer workload (M = 8192 tokens, K = N = 4096, bf16 activations with
 0.1 % outliers, fp32 master weights ~ N(0, 0.02), bf16 output gradient), run
 through the library's entry points on one CUDA stream:
-  fp8_quantize(x  -> X8, X8^T, amax)           E4M3
-  fp8_quantize(W  -> W8, W8^T, amax)           E4M3 (fp32 master in)
-  fp8_linear_fwd(X8, W8 -> Y bf16, amax_y)
-  fp8_quantize(dY -> dY8, dY8^T, amax)         E5M2
-  fp8_linear_bwd(dY8, W8^T -> dX bf16;         dgrad and wgrad GEMMs in
-                 dY8^T, X8^T -> dW bf16)        one launch
-  mp_master_step(dW -> master, momentum, w8)   SGD-momentum, loss scale 2^16
-  delayed_scaling_update(x, w, y, dy metas)    L = 1024, most_recent
+  fp8_quantize(x -> X8, amax)                    E4M3, row-major only
+  fp8_linear_fwd(X8, W8 -> Y bf16, amax_y)       W8: the weight's E4M3 copy
+  fp8_quantize(dY -> dY8, amax)                  E5M2, row-major only
+  fp8_linear_bwd_rowmajor(dY8, W8, X8            dgrad and wgrad GEMMs in one
+                          -> dX bf16, dW bf16)   launch, no transposed copies
+  delayed_scaling_update(x, w, y, dy metas)      L = 1024, most_recent
+  mp_master_step(dW -> master, momentum, W8)     SGD-momentum, loss scale 2^16;
+                                                 re-casts W8 under the updated
+                                                 weight scale for the next step
+The weight's first E4M3 copy is cast once before the first step; from then
+on each step's master step writes the next step's W8 (and records the amax
+of the new master weights for the next scale update), so the weight is cast
+once per optimizer step, inside the fused update pass.
 The metric counts the FLOPs the FP8 tensor cores perform, 3 * 2 * M * N * K,
 per step time. Multi-GPU runs are independent replicas (weak scaling).
 
@@ -214,48 +219,45 @@ class LinearStep:
         del tb
         u8 = torch.uint8
         self.X8 = torch.empty((m, k), dtype=u8, device=dev)
-        self.X8t = torch.empty((k, m), dtype=u8, device=dev)
         self.W8 = torch.empty((n, k), dtype=u8, device=dev)
-        self.W8t = torch.empty((k, n), dtype=u8, device=dev)
         self.D8 = torch.empty((m, n), dtype=u8, device=dev)
-        self.D8t = torch.empty((n, m), dtype=u8, device=dev)
         self.y = torch.empty((m, n), dtype=torch.bfloat16, device=dev)
         self.dx = torch.empty((m, k), dtype=torch.bfloat16, device=dev)
         self.dw = torch.empty((n, k), dtype=torch.bfloat16, device=dev)
         self.mom = torch.zeros((n, k), dtype=torch.float32, device=dev)
-        self.w8_next = torch.empty((n, k), dtype=u8, device=dev)
         self.S = torch.tensor([S0], dtype=torch.float32, device=dev)
         self.growth = torch.zeros(1, dtype=torch.int32, device=dev)
         self.found = torch.zeros(1, dtype=torch.int32, device=dev)
         E4, E5 = fp8mp.E4M3, fp8mp.E5M2
         self.mx, self.mw, self.my = (fp8mp.Meta(HIST_LEN, E4) for _ in range(3))
         self.md = fp8mp.Meta(HIST_LEN, E5)
-        # 3 casts, the fwd GEMM, the fused dgrad + wgrad GEMM, 3 master-step kernels, 1 scale update
-        self.launches_per_step = 9
+        # the weight's first E4M3 copy (and its amax for the first update)
+        fp8mp.fp8_quantize(self.master, E4, self.mw.scale, self.W8, None, self.mw.cur_amax)
+        # 2 casts, the fwd GEMM, the fused dgrad + wgrad GEMM, 1 scale update, 3 master-step kernels
+        self.launches_per_step = 8
 
     def step(self, gemm_events=None, io=None):
         """One training step. `io` = (x, dy, y, dx) device buffers to use
         instead of the step's own (the end-to-end leg double-buffers them)."""
         f = self.fp8mp
         x, dy, y, dx = io if io is not None else (self.x, self.dy, self.y, self.dx)
-        f.fp8_quantize(x, f.E4M3, self.mx.scale, self.X8, self.X8t, self.mx.cur_amax)
-        f.fp8_quantize(self.master, f.E4M3, self.mw.scale, self.W8, self.W8t, self.mw.cur_amax)
+        f.fp8_quantize(x, f.E4M3, self.mx.scale, self.X8, None, self.mx.cur_amax)
         ev = gemm_events
         if ev is not None:
             ev[0].record()
         f.fp8_linear_fwd(self.X8, self.W8, self.mx.scale_inv, self.mw.scale_inv, y, y_amax=self.my.cur_amax)
         if ev is not None:
             ev[1].record()
-        f.fp8_quantize(dy, f.E5M2, self.md.scale, self.D8, self.D8t, self.md.cur_amax)
+        f.fp8_quantize(dy, f.E5M2, self.md.scale, self.D8, None, self.md.cur_amax)
         if ev is not None:
             ev[2].record()
-        f.fp8_linear_bwd(self.D8, self.D8t, self.W8t, self.X8t, self.md.scale_inv, self.mw.scale_inv,
-                         self.mx.scale_inv, dx, self.dw)
+        f.fp8_linear_bwd_rowmajor(self.D8, self.W8, self.X8, self.md.scale_inv, self.mw.scale_inv,
+                                  self.mx.scale_inv, dx, self.dw)
         if ev is not None:
             ev[3].record()
-        f.mp_master_step(self.dw, self.master, self.mom, self.w8_next, self.mw.scale, self.mw.cur_amax, self.S,
-                         self.growth, self.found, LR, MU)
         f.delayed_scaling_update([self.mx, self.mw, self.my, self.md], f.AMAX_MOST_RECENT, 0)
+        f.mp_master_step(self.dw, self.master, self.mom, self.W8, self.mw.scale, self.mw.cur_amax, self.S,
+                         self.growth, self.found, LR, MU)
 
 
 def capture_step_graphs(st, count):
@@ -451,32 +453,41 @@ def oracle_step_sample(tokens: int, seed=3):
     return x, dy, w
 
 
-def oracle_step(orc, x, dy, w, mom, metas):
-    """The same step on the CPU oracle (codes, GEMMs in fp64, master step)."""
+def oracle_step(orc, x, dy, w, mom, w8, metas):
+    """The same step on the CPU oracle: codes, GEMMs in fp64 over decoded
+    codes (the oracle takes both operands contiguous along the contraction,
+    so it forms the transposes itself), the scale update, then the master
+    step re-casting `w8` under the updated weight scale."""
     import numpy as np
+    import torch
 
     E4, E5 = orc.E4M3, orc.E5M2
     mx, mw, my, md = metas
     X8 = orc.cast(x, float(mx.scale[0]), E4)
     mx.record_amax(orc.amax(x))
-    W8 = orc.cast(w, float(mw.scale[0]), E4)
-    mw.record_amax(orc.amax(w))
+    W8 = w8.reshape(w.shape)
     y, _ = orc.gemm_ref(X8, E4, W8, E4, float(mx.scale_inv[0]), float(mw.scale_inv[0]), with_abs=False)
     my.record_amax(np.float32(np.abs(y).max()))
     D8 = orc.cast(dy, float(md.scale[0]), E5)
     md.record_amax(orc.amax(dy))
-    W8t = orc.transpose_u8(W8)
-    dx, _ = orc.gemm_ref(D8, E5, W8t, E4, float(md.scale_inv[0]), float(mw.scale_inv[0]), with_abs=False)
-    D8t, X8t = orc.transpose_u8(D8), orc.transpose_u8(X8)
-    dw, _ = orc.gemm_ref(D8t, E5, X8t, E4, float(md.scale_inv[0]), float(mx.scale_inv[0]), with_abs=False)
-    import torch
-
-    g = torch.from_numpy(dw.astype(np.float32)).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
-    w8 = np.empty(w.size, dtype=np.uint8)
-    st = orc.LossScaleState(S0)
-    orc.master_step(g.reshape(-1), w.reshape(-1), mom.reshape(-1), w8, float(mw.scale[0]), mw.cur_amax, st, LR, MU)
+    dx, _ = orc.gemm_ref(D8, E5, orc.transpose_u8(W8), E4, float(md.scale_inv[0]), float(mw.scale_inv[0]),
+                         with_abs=False)
+    dw, _ = orc.gemm_ref(orc.transpose_u8(D8), E5, orc.transpose_u8(X8), E4, float(md.scale_inv[0]),
+                         float(mx.scale_inv[0]), with_abs=False)
     for m, f in zip(metas, (E4, E4, E4, E5)):
         orc.scale_update(m, f, orc.AMAX_MOST_RECENT, 0)
+    g = torch.from_numpy(dw.astype(np.float32)).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    st = orc.LossScaleState(S0)
+    orc.master_step(g.reshape(-1), w.reshape(-1), mom.reshape(-1), w8.reshape(-1), float(mw.scale[0]),
+                    mw.cur_amax, st, LR, MU)
+
+
+def oracle_initial_weight_copy(orc, w, metas):
+    """The weight's first E4M3 copy, cast once before the first step."""
+    mw = metas[1]
+    w8 = orc.cast(w, float(mw.scale[0]), orc.E4M3).reshape(-1).copy()
+    mw.record_amax(orc.amax(w))
+    return w8
 
 
 def cpu_baseline(tokens: int):
@@ -488,13 +499,14 @@ def cpu_baseline(tokens: int):
     x, dy, w = oracle_step_sample(tokens)
     mom = np.zeros_like(w)
     metas = [orc.Meta(HIST_LEN) for _ in range(4)]
+    w8 = oracle_initial_weight_copy(orc, w, metas)
     t0 = time.perf_counter()
-    oracle_step(orc, x, dy, w, mom, metas)
+    oracle_step(orc, x, dy, w, mom, w8, metas)
     dt = time.perf_counter() - t0
     fl = flops_per_step(m=tokens)
     return {"value": round(fl / dt / 1e12, 6), "unit": "TFLOP/s", "cores": orc.num_threads(), "kind": "oracle",
             "sample": f"one full step on a {tokens}-token sample (x {tokens}x{K_IN}, dY {tokens}x{N_OUT}, "
-                      f"full {N_OUT}x{K_IN} weight and master step), {dt:.2f} s"}
+                      f"full {N_OUT}x{K_IN} weight, scale update and master step), {dt:.2f} s"}
 
 
 def run_reference(args, world, rank):
@@ -508,12 +520,13 @@ def run_reference(args, world, rank):
     x, dy, w = oracle_step_sample(args.cpu_tokens)
     mom = np.zeros_like(w)
     metas = [orc.Meta(HIST_LEN) for _ in range(4)]
+    w8 = oracle_initial_weight_copy(orc, w, metas)
     for _ in range(args.warmup):
-        oracle_step(orc, x, dy, w.copy(), mom.copy(), [m.copy() for m in metas])
+        oracle_step(orc, x, dy, w.copy(), mom.copy(), w8.copy(), [m.copy() for m in metas])
     times = []
     for _ in range(args.steps):
         t0 = time.perf_counter()
-        oracle_step(orc, x, dy, w, mom, metas)
+        oracle_step(orc, x, dy, w, mom, w8, metas)
         times.append(time.perf_counter() - t0)
     ms = statistics.mean(times) * 1e3
     fl = flops_per_step(m=args.cpu_tokens)

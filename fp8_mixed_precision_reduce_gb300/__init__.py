@@ -26,7 +26,7 @@ _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "libfp8mp.so")
 EXPORTS = ("fp8_quantize", "fp8_quantize_current", "fp8_quantize_dbias",
            "fp8_quantize_dbias_workspace_bytes", "fp8_quantize_dbias_noalloc", "fp8_linear_fwd", "fp8_linear_fwd_fp8out", "fp8_linear_dgrad", "fp8_linear_wgrad",
-           "fp8_linear_bwd", "delayed_scaling_update", "mp_master_step", "mp_master_step_adam", "fp8mp_check", "fp8mp_last_error",
+           "fp8_linear_bwd", "fp8_linear_bwd_rowmajor", "delayed_scaling_update", "mp_master_step", "mp_master_step_adam", "fp8mp_check", "fp8mp_last_error",
            "fp8mp_version", "fp8mp_selftest_timeout")
 
 _lib = None
@@ -74,6 +74,7 @@ def load(path: str | None = None):
     L.fp8_linear_dgrad.argtypes = [P, P, I64, I64, I64, I32, P, P, P, I32, P]
     L.fp8_linear_wgrad.argtypes = [P, P, I64, I64, I64, I32, P, P, P, I32, P]
     L.fp8_linear_bwd.argtypes = [P, P, P, P, I64, I64, I64, I32, P, P, P, P, I32, P, I32, P]
+    L.fp8_linear_bwd_rowmajor.argtypes = [P, P, P, I64, I64, I64, I32, P, P, P, P, I32, P, I32, P]
     L.delayed_scaling_update.argtypes = [ctypes.POINTER(fp8mp_meta), I32, I32, I32, P]
     L.mp_master_step.argtypes = [P, I64, P, P, P, P, P, P, P, P, F, F, F, F, I32, P]
     L.mp_master_step_adam.argtypes = [P, I64, P, P, P, P, P, P, P, P, P, P, F, F, F, F, F, F, I32, P]
@@ -83,7 +84,7 @@ def load(path: str | None = None):
     L.fp8mp_version.restype = I32
     for name in ("fp8_quantize", "fp8_quantize_current", "fp8_quantize_dbias", "fp8_quantize_dbias_noalloc",
                  "fp8_linear_fwd", "fp8_linear_fwd_fp8out", "fp8_linear_dgrad", "fp8_linear_wgrad",
-                 "fp8_linear_bwd", "delayed_scaling_update", "mp_master_step", "mp_master_step_adam", "fp8mp_check",
+                 "fp8_linear_bwd", "fp8_linear_bwd_rowmajor", "delayed_scaling_update", "mp_master_step", "mp_master_step_adam", "fp8mp_check",
                  "fp8mp_selftest_timeout"):
         getattr(L, name).restype = ctypes.c_int
     _lib = L
@@ -157,11 +158,12 @@ def fp8_quantize_dbias_workspace_bytes(rows: int, cols: int) -> int:
 
 
 def fp8_quantize_dbias(dy: torch.Tensor, fmt: int, scale: torch.Tensor, out: torch.Tensor,
-                       out_t: torch.Tensor, dbias: torch.Tensor, workspace: torch.Tensor,
+                       out_t: torch.Tensor | None, dbias: torch.Tensor, workspace: torch.Tensor,
                        amax: torch.Tensor | None = None, stream=None) -> None:
-    """Cast of an output gradient (+ transposed copy, + amax) that also writes
-    the bias gradient dbias = column sums of dy. `workspace` is a device
-    buffer of at least fp8_quantize_dbias_workspace_bytes(rows, cols) bytes."""
+    """Cast of an output gradient (+ optional transposed copy, + amax) that
+    also writes the bias gradient dbias = column sums of dy. `workspace` is a
+    device buffer of at least fp8_quantize_dbias_workspace_bytes(rows, cols)
+    bytes."""
     rows, cols = _rows_cols(dy)
     _check(load().fp8_quantize_dbias(_ptr(dy), _dtype_code(dy), rows, cols, fmt, _ptr(scale), _ptr(out),
                                      _ptr(out_t), _ptr(amax), _ptr(dbias), _dtype_code(dbias),
@@ -236,6 +238,21 @@ def fp8_linear_bwd(dy8: torch.Tensor, dy8t: torch.Tensor, w8t: torch.Tensor, x8t
     _check(load().fp8_linear_bwd(_ptr(dy8), _ptr(dy8t), _ptr(w8t), _ptr(x8t), M, N, K, dy_fmt, _ptr(sinv_dy),
                                  _ptr(sinv_w), _ptr(sinv_x), _ptr(dx), _dtype_code(dx), _ptr(dw), _dtype_code(dw),
                                  _stream(stream)))
+
+
+def fp8_linear_bwd_rowmajor(dy8: torch.Tensor, w8: torch.Tensor | None, x8: torch.Tensor | None,
+                            sinv_dy: torch.Tensor, sinv_w: torch.Tensor | None, sinv_x: torch.Tensor | None,
+                            dx: torch.Tensor | None, dw: torch.Tensor | None, dy_fmt: int = E5M2,
+                            stream=None) -> None:
+    """Both backward GEMMs from the forward's row-major FP8 copies, one launch:
+    dx[M, K] = (dy8 . w8) * sinv_dy * sinv_w, dw[N, K] = (dy8^T . x8) * sinv_dy * sinv_x.
+    dx or dw may be None to skip that gradient."""
+    M, N = dy8.shape
+    K = (w8 if w8 is not None else x8).shape[1]
+    _check(load().fp8_linear_bwd_rowmajor(_ptr(dy8), _ptr(w8), _ptr(x8), M, N, K, dy_fmt, _ptr(sinv_dy),
+                                          _ptr(sinv_w), _ptr(sinv_x), _ptr(dx),
+                                          _dtype_code(dx) if dx is not None else F32, _ptr(dw),
+                                          _dtype_code(dw) if dw is not None else F32, _stream(stream)))
 
 
 class Meta:

@@ -191,7 +191,7 @@ int fp8_quantize_dbias(const void *x, int32_t x_dtype, int64_t rows, int64_t col
     if (rows > 0) {
         CHECK_PTR(x, true);
         CHECK_PTR(out, true);
-        CHECK_PTR(out_t, true);
+        CHECK_PTR(out_t, false);
         CHECK_SCALAR(scale, true);
         CHECK_SCALAR(amax, false);
         CHECK_PTR(workspace, true);
@@ -346,10 +346,56 @@ int fp8_linear_bwd(const uint8_t *dy8, const uint8_t *dy8t, const uint8_t *w8t, 
     if (rc) return rc;
     const GemmDesc d[2] = {
         {dy8, dy_fmt, w8t, FP8MP_E4M3, M, K, N, sinv_dy, sinv_w, nullptr, FP8MP_F32, dx, dx_dtype, nullptr, nullptr,
-         FP8MP_E4M3},
+         FP8MP_E4M3, 0, 0},
         {dy8t, dy_fmt, x8t, FP8MP_E4M3, N, K, M, sinv_dy, sinv_x, nullptr, FP8MP_F32, dw, dw_dtype, nullptr, nullptr,
-         FP8MP_E4M3}};
+         FP8MP_E4M3, 0, 0}};
     return launch_gemms(d, 2, static_cast<cudaStream_t>(stream), dev);
+}
+
+int fp8_linear_bwd_rowmajor(const uint8_t *dy8, const uint8_t *w8, const uint8_t *x8, int64_t M, int64_t N,
+                            int64_t K, int32_t dy_fmt, const float *sinv_dy, const float *sinv_w,
+                            const float *sinv_x, void *dx, int32_t dx_dtype, void *dw, int32_t dw_dtype,
+                            void *stream) {
+    const char *fn = "fp8_linear_bwd_rowmajor";
+    clear_error();
+    int rc = check_gemm_dims(fn, M, N, K);
+    if (rc) return rc;
+    REQUIRE(valid_fmt(dy_fmt), "%s: dy_fmt %d invalid", fn, dy_fmt);
+    REQUIRE(dx == nullptr || valid_dtype(dx_dtype), "%s: dx_dtype %d invalid", fn, dx_dtype);
+    REQUIRE(dw == nullptr || valid_dtype(dw_dtype), "%s: dw_dtype %d invalid", fn, dw_dtype);
+    const bool want_dx = dx != nullptr && M > 0 && K > 0;
+    const bool want_dw = dw != nullptr && N > 0 && K > 0;
+    if (!want_dx && !want_dw) return FP8MP_OK;
+    CHECK_PTR(dx, false);
+    CHECK_PTR(dw, false);
+    CHECK_SCALAR(sinv_dy, true);
+    if (want_dx) CHECK_SCALAR(sinv_w, true);
+    if (want_dw) CHECK_SCALAR(sinv_x, true);
+    if (M > 0 && N > 0) {
+        CHECK_PTR(dy8, true);
+        if (want_dx) CHECK_PTR(w8, true);
+        if (want_dw) CHECK_PTR(x8, true);
+    }
+    if (want_dx && want_dw) {
+        const uintptr_t a = reinterpret_cast<uintptr_t>(dx), b = reinterpret_cast<uintptr_t>(dw);
+        const uintptr_t na = static_cast<uintptr_t>(M * K) * (dx_dtype == FP8MP_BF16 ? 2 : 4);
+        const uintptr_t nb = static_cast<uintptr_t>(N * K) * (dw_dtype == FP8MP_BF16 ? 2 : 4);
+        REQUIRE(a + na <= b || b + nb <= a, "%s: dx and dw overlap", fn);
+    }
+    DeviceInfo dev;
+    rc = current_device(&dev);
+    if (rc) return rc;
+    GemmDesc d[2];
+    int n = 0;
+    // dgrad: A = dY8 [M x N] K-major, B = W8 [N x K] read MN-major (rows_b = K, kc = N)
+    if (want_dx)
+        d[n++] = {dy8, dy_fmt, w8, FP8MP_E4M3, M, K, N, sinv_dy, sinv_w, nullptr, FP8MP_F32, dx, dx_dtype, nullptr,
+                  nullptr, FP8MP_E4M3, 0, 1};
+    // wgrad: A = dY8 [M x N] read MN-major (rows_a = N, kc = M), B = X8 [M x K] read MN-major
+    if (want_dw)
+        d[n++] = {dy8, dy_fmt, x8, FP8MP_E4M3, N, K, M, sinv_dy, sinv_x, nullptr, FP8MP_F32, dw, dw_dtype, nullptr,
+                  nullptr, FP8MP_E4M3, 1, 1};
+    return launch_gemms(d, n, static_cast<cudaStream_t>(stream), dev);
 }
 
 int delayed_scaling_update(const fp8mp_meta *metas, int32_t n, int32_t algo, int32_t margin, void *stream) {

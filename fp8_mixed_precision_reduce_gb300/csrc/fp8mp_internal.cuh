@@ -38,8 +38,9 @@ int launch_quantize_dbias(const void *x, int x_dtype, int64_t rows, int64_t cols
 int launch_quantize(const void *x, int x_dtype, int64_t rows, int64_t cols, int fmt,
                     const float *scale, uint8_t *out, uint8_t *out_t, float *amax,
                     cudaStream_t s, const DeviceInfo &dev);
-// One GEMM out[rows_a x rows_b] = (A B^T) * sinv_a * sinv_b (+ bias), A and B
-// contiguous along the contraction of length kc.
+// One GEMM out[rows_a x rows_b] = (A B^T) * sinv_a * sinv_b (+ bias) over a
+// contraction of length kc. A is [rows_a x kc] (K-major) or, with a_mn,
+// [kc x rows_a] (MN-major); likewise B with rows_b and b_mn.
 struct GemmDesc {
     const uint8_t *a;
     int fmt_a;
@@ -54,6 +55,7 @@ struct GemmDesc {
     float *out_amax;
     const float *out_scale;  // non-null: FP8 output of out_fmt under *out_scale
     int out_fmt;
+    int a_mn, b_mn;
 };
 // Runs 1 or 2 independent GEMMs in one persistent launch.
 int launch_gemms(const GemmDesc *descs, int n, cudaStream_t s, const DeviceInfo &dev);

@@ -101,7 +101,8 @@ struct Cfg {
 struct GemmParams {
     int rows_a, rows_b, num_kb;
     int tiles_m, tiles_n;
-    uint32_t idesc;           // tcgen05 instruction descriptor (operand formats, M, N)
+    int a_mn, b_mn;           // operand stored MN-major ([kc x rows], contiguous along M / N)
+    uint32_t idesc;           // tcgen05 instruction descriptor (operand formats, majors, M, N)
     const float *sinv_a, *sinv_b;
     const void *bias;
     int bias_bf16;
@@ -339,6 +340,23 @@ __device__ __forceinline__ uint64_t sw128_kmajor_desc(uint32_t saddr) {
     return d;
 }
 
+// Shared-memory matrix descriptor of an MN-major operand tile: one
+// 128-byte row of 128 M/N elements per k (the layout TMA writes for a box
+// whose inner dimension runs along M/N, with CU_TENSOR_MAP_SWIZZLE_128B),
+// 8-row atoms of 1024 bytes stacked along k. The stride byte offset is the
+// step between those 8-row groups along k; the leading byte offset is the
+// step between 128-element atoms along M/N (a 256-wide tile is staged as
+// two 128-wide halves `lbo` bytes apart; a 128-wide tile has one atom).
+__device__ __forceinline__ uint64_t sw128_mnmajor_desc(uint32_t saddr, uint32_t lbo) {
+    uint64_t d = 0;
+    d |= static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4);  // start address, bits 0-13
+    d |= static_cast<uint64_t>(lbo >> 4) << 16;           // leading byte offset: next M/N atom, bits 16-29
+    d |= static_cast<uint64_t>(1024u >> 4) << 32;         // stride byte offset: next 8 k-rows, bits 32-45
+    d |= static_cast<uint64_t>(1u) << 46;                 // descriptor version for tcgen05, bits 46-47
+    d |= static_cast<uint64_t>(2u) << 61;                 // swizzle mode: 128 bytes, bits 61-63
+    return d;
+}
+
 // Tile of round `r` for cluster `c` of `nc`: one tile per cluster per round,
 // dealt forwards in even rounds and backwards in odd ones (serpentine). With
 // the tiles sorted by contraction length, longest first, the clusters that
@@ -450,6 +468,7 @@ gemm_fp8_kernel(const __grid_constant__ GemmBatch batch) {
                 const int a_row = mb * C::TILE_M + static_cast<int>(rank) * ROWS_A;
                 const int b_row = nb * TILE_N + static_cast<int>(rank) * C::ROWS_B;
                 const int num_kb = P.p.num_kb;
+                const int a_mn = P.p.a_mn, b_mn = P.p.b_mn;
                 for (int kb = 0; kb < num_kb; ++kb, ++it) {
                     const int s = static_cast<int>(it % C::STAGES);
                     const uint32_t ph = (it / C::STAGES) & 1u;
@@ -461,8 +480,19 @@ gemm_fp8_kernel(const __grid_constant__ GemmBatch batch) {
                     // the full barrier of a pair lives in the MMA-issuing CTA
                     const uint32_t fb = PAIR ? mapa_shared(full_bar(s), 0) : full_bar(s);
                     if (rank == 0) mbar_arrive_expect_tx(full_bar(s), C::TX_BYTES);
-                    tma_load_2d<PAIR>(sa, &P.ta, fb, kb * BK, a_row);
-                    tma_load_2d<PAIR>(sa + C::A_BYTES, &P.tb, fb, kb * BK, b_row);
+                    // K-major: box of rows x 128 bytes of k at (k, row); MN-major:
+                    // box of 128 k-rows x 128 bytes of M/N at (row, k)
+                    if (a_mn)
+                        tma_load_2d<PAIR>(sa, &P.ta, fb, a_row, kb * BK);
+                    else
+                        tma_load_2d<PAIR>(sa, &P.ta, fb, kb * BK, a_row);
+                    if (!b_mn) {
+                        tma_load_2d<PAIR>(sa + C::A_BYTES, &P.tb, fb, kb * BK, b_row);
+                    } else {
+#pragma unroll
+                        for (int h = 0; h < C::ROWS_B / 128; ++h)
+                            tma_load_2d<PAIR>(sa + C::A_BYTES + h * (BK * 128), &P.tb, fb, b_row + 128 * h, kb * BK);
+                    }
                     if (issued_stages < C::STAGES) ++issued_stages;
                 }
             }
@@ -488,6 +518,7 @@ gemm_fp8_kernel(const __grid_constant__ GemmBatch batch) {
                 const GemmProblem &P = batch.prob[tile_problem(batch, tile, local)];
                 const uint32_t idesc = P.p.idesc;
                 const int num_kb = P.p.num_kb;
+                const int a_mn = P.p.a_mn, b_mn = P.p.b_mn;
                 const int acc = lt & 1;
                 const uint32_t aph = (static_cast<uint32_t>(lt) >> 1) & 1u;
                 ++lt;
@@ -508,9 +539,15 @@ gemm_fp8_kernel(const __grid_constant__ GemmBatch batch) {
                     const uint32_t sa = base + s * C::STAGE_BYTES;
 #pragma unroll
                     for (int k = 0; k < BK / UMMA_K; ++k) {
-                        umma_f8f6f4<PAIR>(d_tmem, sw128_kmajor_desc(sa + k * UMMA_K),
-                                          sw128_kmajor_desc(sa + C::A_BYTES + k * UMMA_K), idesc,
-                                          (kb > 0 || k > 0) ? 1u : 0u);
+                        // the k-th 32-element slice: 32 bytes into each K-major row,
+                        // or 32 rows (4 KB) into an MN-major tile
+                        const uint32_t a_addr = sa + (a_mn ? k * UMMA_K * 128 : k * UMMA_K);
+                        const uint32_t b_addr = sa + C::A_BYTES + (b_mn ? k * UMMA_K * 128 : k * UMMA_K);
+                        const uint64_t a_desc = a_mn ? sw128_mnmajor_desc(a_addr, 1024u) : sw128_kmajor_desc(a_addr);
+                        const uint64_t b_desc =
+                            b_mn ? sw128_mnmajor_desc(b_addr, C::ROWS_B > 128 ? BK * 128u : 1024u)
+                                 : sw128_kmajor_desc(b_addr);
+                        umma_f8f6f4<PAIR>(d_tmem, a_desc, b_desc, idesc, (kb > 0 || k > 0) ? 1u : 0u);
                     }
                     umma_commit_all<PAIR>(empty_bar(s));
                 }
@@ -759,6 +796,8 @@ int make_out_tmap(CUtensorMap *map, void *ptr, uint64_t cols, uint64_t rows, boo
 }
 
 // 2-D byte tensor [outer x inner], inner contiguous; box box_outer x 128 bytes.
+// A K-major operand has inner = kc, outer = its rows (box: the tile's rows);
+// an MN-major one has inner = its rows, outer = kc (box: 128 k-rows).
 int make_tmap(CUtensorMap *map, const void *ptr, uint64_t inner, uint64_t outer, uint32_t box_outer) {
     auto enc = encode_fn();
     if (enc == nullptr) return fail(FP8MP_ERR_LAUNCH, "cuTensorMapEncodeTiled is not available");
@@ -773,11 +812,12 @@ int make_tmap(CUtensorMap *map, const void *ptr, uint64_t inner, uint64_t outer,
     return FP8MP_OK;
 }
 
-constexpr uint32_t make_idesc(int fmt_a, int fmt_b, int m) {
+constexpr uint32_t make_idesc(int fmt_a, int fmt_b, int m, int a_mn, int b_mn) {
     return (1u << 4)                                    // accumulator: f32
            | (static_cast<uint32_t>(fmt_a) << 7)        // A: 0 = E4M3, 1 = E5M2
            | (static_cast<uint32_t>(fmt_b) << 10)       // B: 0 = E4M3, 1 = E5M2
-           | (0u << 15) | (0u << 16)                    // A and B K-major
+           | (static_cast<uint32_t>(a_mn) << 15)        // A: 0 = K-major, 1 = MN-major
+           | (static_cast<uint32_t>(b_mn) << 16)        // B: 0 = K-major, 1 = MN-major
            | (static_cast<uint32_t>(TILE_N >> 3) << 17) // N / 8
            | (static_cast<uint32_t>(m >> 4) << 24);     // M / 16
 }
@@ -898,7 +938,9 @@ int launch_gemms(const GemmDesc *descs, int n, cudaStream_t s, const DeviceInfo 
         p.num_kb = static_cast<int>((d.kc + BK - 1) / BK);
         p.tiles_n = static_cast<int>((d.rows_b + TILE_N - 1) / TILE_N);
         p.tiles_m = static_cast<int>(pair ? (d.rows_a + 255) / 256 : (d.rows_a + 127) / 128);
-        p.idesc = make_idesc(d.fmt_a, d.fmt_b, pair ? 256 : 128);
+        p.a_mn = d.a_mn;
+        p.b_mn = d.b_mn;
+        p.idesc = make_idesc(d.fmt_a, d.fmt_b, pair ? 256 : 128, d.a_mn, d.b_mn);
         p.sinv_a = d.sinv_a;
         p.sinv_b = d.sinv_b;
         p.bias = d.bias;
@@ -909,10 +951,12 @@ int launch_gemms(const GemmDesc *descs, int n, cudaStream_t s, const DeviceInfo 
         p.out_fmt = d.out_fmt;
         p.out_scale = d.out_scale;
         p.out_amax = d.out_amax;
-        rc = make_tmap(&P.ta, d.a, static_cast<uint64_t>(d.kc), static_cast<uint64_t>(d.rows_a), ROWS_A);
+        const uint64_t kc = static_cast<uint64_t>(d.kc);
+        const uint64_t ra = static_cast<uint64_t>(d.rows_a), rb = static_cast<uint64_t>(d.rows_b);
+        rc = d.a_mn ? make_tmap(&P.ta, d.a, ra, kc, BK) : make_tmap(&P.ta, d.a, kc, ra, ROWS_A);
         if (rc) return rc;
-        rc = make_tmap(&P.tb, d.b, static_cast<uint64_t>(d.kc), static_cast<uint64_t>(d.rows_b),
-                       pair ? Cfg<true>::ROWS_B : Cfg<false>::ROWS_B);
+        rc = d.b_mn ? make_tmap(&P.tb, d.b, rb, kc, BK)
+                    : make_tmap(&P.tb, d.b, kc, rb, pair ? Cfg<true>::ROWS_B : Cfg<false>::ROWS_B);
         if (rc) return rc;
         rc = make_out_tmap(&P.to, d.out, static_cast<uint64_t>(d.rows_b), static_cast<uint64_t>(d.rows_a),
                            p.out_bf16 != 0, p.out_fp8 != 0);
@@ -938,7 +982,7 @@ int launch_gemm(const uint8_t *a, int fmt_a, const uint8_t *b, int fmt_b, int64_
                 int out_dtype, float *out_amax, cudaStream_t s, const DeviceInfo &dev, const float *out_scale,
                 int out_fmt) {
     const GemmDesc d = {a,    fmt_a,      b,   fmt_b,     rows_a,   rows_b,    kc,     sinv_a,
-                        sinv_b, bias, bias_dtype, out, out_dtype, out_amax, out_scale, out_fmt};
+                        sinv_b, bias, bias_dtype, out, out_dtype, out_amax, out_scale, out_fmt, 0, 0};
     return launch_gemms(&d, 1, s, dev);
 }
 

@@ -115,7 +115,8 @@ cast_rows_kernel(const void *__restrict__ x, int64_t n, const float *__restrict_
 // warp writes four full 128-byte rows of out_t.
 // With DBIAS the kernel also sums its 128 rows per column (fp32, fixed order:
 // each thread its 8 rows in row order, then the 16 row groups in order) and
-// writes the 128 column sums of its tile to ws[tile_row * cols + col].
+// writes the 128 column sums of its tile to ws[tile_row * cols + col]; then
+// out_t may be NULL (no transposed copy: phase 2 is skipped).
 template <int FMT, bool BF16, bool DBIAS>
 __global__ void __launch_bounds__(kThreads)
 cast_rows_t_kernel(const void *__restrict__ x, int64_t rows, int64_t cols, const float *__restrict__ scale_p,
@@ -171,8 +172,10 @@ cast_rows_t_kernel(const void *__restrict__ x, int64_t rows, int64_t cols, const
                 wcol[6] = __byte_perm(t1, t3, 0x5410);
                 wcol[7] = __byte_perm(t1, t3, 0x7632);
             }
+            if (out_t != nullptr) {
 #pragma unroll
-            for (int j = 0; j < 8; ++j) sT[(8 * tx + j) * 32 + (g ^ sw1)] = wcol[j];
+                for (int j = 0; j < 8; ++j) sT[(8 * tx + j) * 32 + (g ^ sw1)] = wcol[j];
+            }
         }
     }
     if constexpr (DBIAS) {
@@ -189,6 +192,7 @@ cast_rows_t_kernel(const void *__restrict__ x, int64_t rows, int64_t cols, const
     }
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
+        if (out_t == nullptr) break;
         const int id = threadIdx.x + kThreads * i;  // 0 .. 1023
         const int cc = id >> 3, k = id & 7;          // tile column, 16-row chunk
         const int64_t col = c0 + cc, row = r0 + 16 * k;
@@ -219,7 +223,7 @@ dbias_reduce_kernel(const float *__restrict__ ws, int64_t tile_rows, int64_t col
 template <int FMT, bool BF16>
 int launch_typed(const void *x, int64_t rows, int64_t cols, const float *scale, uint8_t *out,
                  uint8_t *out_t, float *amax, cudaStream_t s, const DeviceInfo &dev, float *ws = nullptr) {
-    if (out_t == nullptr) {
+    if (out_t == nullptr && ws == nullptr) {
         const int64_t n = rows * cols;
         const int64_t nchunk = n >> 4;
         int64_t blocks = (nchunk + kThreads - 1) / kThreads;

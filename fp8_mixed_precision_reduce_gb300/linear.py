@@ -6,10 +6,10 @@ Engine으로 FP8 사용하기", the te.Linear(768, 768, bias=True) example under
 DelayedScaling recipe with the HYBRID format: E4M3 for the input and the
 weight in the forward GEMM, E5M2 for the output gradient in dgrad and wgrad.
 
-Every step of the layer is a call into libfp8mp (casts with transposed
-copies and amaxes, the forward GEMM, the fused dgrad + wgrad launch, the
-fused bias gradient); this file
-only allocates the outputs through torch and passes pointers. Like
+Every step of the layer is a call into libfp8mp (casts to row-major FP8
+copies with their amaxes, the forward GEMM, the fused dgrad + wgrad launch
+that reads those copies as they are, the fused bias gradient); this file only
+allocates the outputs through torch and passes pointers. Like
 sync_float8_amax_and_scale_history after backward in the pages' training
 loop, ``update_scales()`` runs the delayed-scaling update of the layer's
 four tensors (input, weight, output, output gradient) once per step.
@@ -19,8 +19,8 @@ from __future__ import annotations
 
 import torch
 
-from . import (AMAX_MAX, E4M3, E5M2, Meta, delayed_scaling_update, fp8_linear_bwd, fp8_linear_fwd, fp8_quantize,
-               fp8_quantize_dbias, fp8_quantize_dbias_workspace_bytes)
+from . import (AMAX_MAX, E4M3, E5M2, Meta, delayed_scaling_update, fp8_linear_bwd_rowmajor, fp8_linear_fwd,
+               fp8_quantize, fp8_quantize_dbias, fp8_quantize_dbias_workspace_bytes)
 
 __all__ = ["FP8Linear"]
 
@@ -36,28 +36,27 @@ class _FP8LinearFn(torch.autograd.Function):
         M = x2.shape[0]
         dev = x.device
         u8 = torch.uint8
-        X8t = torch.empty((K, M), dtype=u8, device=dev)
         X8 = torch.empty((M, K), dtype=u8, device=dev)
         W8 = torch.empty((N, K), dtype=u8, device=dev)
-        W8t = torch.empty((K, N), dtype=u8, device=dev)
-        fp8_quantize(x2, E4M3, layer.meta_x.scale, X8, X8t, layer.meta_x.cur_amax)
-        fp8_quantize(weight.detach(), E4M3, layer.meta_w.scale, W8, W8t, layer.meta_w.cur_amax)
+        # row-major copies only: the backward GEMMs read them along their rows
+        fp8_quantize(x2, E4M3, layer.meta_x.scale, X8, None, layer.meta_x.cur_amax)
+        fp8_quantize(weight.detach(), E4M3, layer.meta_w.scale, W8, None, layer.meta_w.cur_amax)
         y = torch.empty((M, N), dtype=x.dtype, device=dev)
         fp8_linear_fwd(X8, W8, layer.meta_x.scale_inv, layer.meta_w.scale_inv, y,
                        bias=bias.detach() if bias is not None else None, y_amax=layer.meta_y.cur_amax)
         # the codes were made with this step's scales: keep those for backward
-        ctx.save_for_backward(X8t, W8t, layer.meta_x.scale_inv.clone(), layer.meta_w.scale_inv.clone())
+        ctx.save_for_backward(X8, W8, layer.meta_x.scale_inv.clone(), layer.meta_w.scale_inv.clone())
         ctx.layer = layer
         ctx.shapes = (x.shape, x.dtype, weight.dtype, None if bias is None else bias.dtype)
         return y.reshape(*x.shape[:-1], N)
 
     @staticmethod
     def backward(ctx, dy):
-        X8t, W8t, sinv_x, sinv_w = ctx.saved_tensors
+        X8, W8, sinv_x, sinv_w = ctx.saved_tensors
         layer = ctx.layer
         x_shape, x_dtype, w_dtype, b_dtype = ctx.shapes
-        K, M = X8t.shape
-        N = W8t.shape[1]
+        M, K = X8.shape
+        N = W8.shape[0]
         dy2 = dy.reshape(-1, N)
         if dy2.dtype != x_dtype:
             dy2 = dy2.to(x_dtype)
@@ -65,21 +64,20 @@ class _FP8LinearFn(torch.autograd.Function):
             dy2 = dy2.contiguous()
         dev = dy.device
         D8 = torch.empty((M, N), dtype=torch.uint8, device=dev)
-        D8t = torch.empty((N, M), dtype=torch.uint8, device=dev)
         md = layer.meta_dy
         db = None
-        if b_dtype is not None:
+        if b_dtype is not None and ctx.needs_input_grad[2]:
             db = torch.empty(N, dtype=b_dtype, device=dev)
             ws = torch.empty(max(1, fp8_quantize_dbias_workspace_bytes(M, N) // 4), dtype=torch.float32, device=dev)
-            fp8_quantize_dbias(dy2, E5M2, md.scale, D8, D8t, db, ws, amax=md.cur_amax)
+            fp8_quantize_dbias(dy2, E5M2, md.scale, D8, None, db, ws, amax=md.cur_amax)
         else:
-            fp8_quantize(dy2, E5M2, md.scale, D8, D8t, md.cur_amax)
+            fp8_quantize(dy2, E5M2, md.scale, D8, None, md.cur_amax)
         sinv_dy = md.scale_inv.clone()
-        dx = torch.empty((M, K), dtype=x_dtype, device=dev)
-        dw = torch.empty((N, K), dtype=w_dtype, device=dev)
-        # dgrad and wgrad in one launch
-        fp8_linear_bwd(D8, D8t, W8t, X8t, sinv_dy, sinv_w, sinv_x, dx, dw, dy_fmt=E5M2)
-        return dx.reshape(x_shape), dw, db, None
+        dx = torch.empty((M, K), dtype=x_dtype, device=dev) if ctx.needs_input_grad[0] else None
+        dw = torch.empty((N, K), dtype=w_dtype, device=dev) if ctx.needs_input_grad[1] else None
+        # dgrad and wgrad in one launch, from the row-major copies
+        fp8_linear_bwd_rowmajor(D8, W8, X8, sinv_dy, sinv_w, sinv_x, dx, dw, dy_fmt=E5M2)
+        return (dx.reshape(x_shape) if dx is not None else None), dw, db, None
 
 
 class FP8Linear(torch.nn.Module):

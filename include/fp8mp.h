@@ -138,7 +138,9 @@ int fp8_quantize_current(const void *x, int32_t x_dtype, int64_t rows, int64_t c
  * layer ([TE-FP8] the te.Linear(768, 768, bias=True) example under "FP8
  * 사용방안(recipe)" and its backward under "Backward Pass 처리"; the bias
  * gradient of y = x W^T + b is the column sum of dY):
- *   out, out_t, *amax    exactly as fp8_quantize (out_t required here);
+ *   out, out_t, *amax    exactly as fp8_quantize (out_t may be NULL: a
+ *                        layer whose backward reads dY8 row-major through
+ *                        fp8_linear_bwd_rowmajor needs no transposed copy);
  *   dbias[c] = sum_r x[r, c]  over the unscaled input, fp32 accumulation in
  *                             a fixed order (deterministic): each 128-row
  *                             block's column sums, then the blocks in order;
@@ -271,6 +273,28 @@ int fp8_linear_wgrad(const uint8_t *dy8t, const uint8_t *x8t, int64_t M, int64_t
 int fp8_linear_bwd(const uint8_t *dy8, const uint8_t *dy8t, const uint8_t *w8t, const uint8_t *x8t, int64_t M,
                    int64_t N, int64_t K, int32_t dy_fmt, const float *sinv_dy, const float *sinv_w,
                    const float *sinv_x, void *dx, int32_t dx_dtype, void *dw, int32_t dw_dtype, void *stream);
+
+/*
+ * fp8_linear_bwd_rowmajor -- the backward GEMMs of the linear layer from the
+ * row-major FP8 copies the forward pass already has, with no transposed
+ * copies: the same results as fp8_linear_dgrad / fp8_linear_wgrad
+ *   dx[m, k] = (sum_n dy8[m, n] * w8[n, k]) * sinv_dy[0] * sinv_w[0]
+ *   dw[n, k] = (sum_m dy8[m, n] * x8[m, k]) * sinv_dy[0] * sinv_x[0]
+ * (each sum in fp32 on the tensor cores, rounded once to the output type),
+ * both in one launch ([TE-FP8] "Backward Pass 처리"). The tensor cores read
+ * w8 and x8, and for dw also dy8, along their rows (MN-major shared-memory
+ * operands), so casts for this layer need no transposed outputs.
+ *
+ * dy8 [M x N] codes of dy_fmt; w8 [N x K] and x8 [M x K] E4M3 codes (the
+ * forward's operands). dx [M x K] of dx_dtype or NULL (no input gradient,
+ * e.g. a first layer); dw [N x K] of dw_dtype or NULL (frozen weight); they
+ * must not overlap. M, N, K multiples of 16. N == 0 gives dx = 0, M == 0
+ * gives dw = 0.
+ */
+int fp8_linear_bwd_rowmajor(const uint8_t *dy8, const uint8_t *w8, const uint8_t *x8, int64_t M, int64_t N,
+                            int64_t K, int32_t dy_fmt, const float *sinv_dy, const float *sinv_w,
+                            const float *sinv_x, void *dx, int32_t dx_dtype, void *dw, int32_t dw_dtype,
+                            void *stream);
 
 /*
  * delayed_scaling_update -- the DelayedScaling bookkeeping of one step for a

@@ -143,6 +143,52 @@ def test_fused_backward_empty_sides(cuda_lib, engine):
     assert (dx.cpu() == 0).all() and (dw.float().cpu() == 0).all()
 
 
+@pytest.mark.parametrize("M,N,K", BWD_SHAPES + [(128, 256, 384), (4096, 1024, 2048)])
+@pytest.mark.parametrize("dy_fmt,dx_dt,dw_dt", [(E5M2, "bf16", "f32"), (E4M3, "f32", "bf16")])
+def test_backward_from_rowmajor_copies(cuda_lib, orc, engine, M, N, K, dy_fmt, dx_dt, dw_dt):
+    """fp8_linear_bwd_rowmajor reads dY8, W8 and X8 as the forward has them
+    (the tensor cores take W8, X8 and, for dW, dY8 along their rows): within
+    the GEMM tolerance of the oracle, and equal to the transposed-copy path."""
+    rng = np.random.default_rng(11 * M + 13 * N + 17 * K + dy_fmt)
+    dy8 = finite_codes(rng, (M, N), dy_fmt)
+    w8 = finite_codes(rng, (N, K), E4M3)
+    x8 = finite_codes(rng, (M, K), E4M3)
+    s_dy, s_w, s_x = 2.0 ** -9, 0.625, 0.125
+    dx = torch.full((M, K), 5.0, dtype=TORCH_DT[dx_dt], device="cuda")
+    dw = torch.full((N, K), 5.0, dtype=TORCH_DT[dw_dt], device="cuda")
+    d_dy8, d_w8, d_x8 = dev(dy8), dev(w8), dev(x8)
+    cuda_lib.fp8_linear_bwd_rowmajor(d_dy8, d_w8, d_x8, sc(s_dy), sc(s_w), sc(s_x), dx, dw, dy_fmt=dy_fmt)
+    assert cuda_lib.fp8mp_check() == 0
+    w8t, x8t, dy8t = (np.ascontiguousarray(a.T) for a in (w8, x8, dy8))
+    ref, ab = orc.gemm_ref(dy8, dy_fmt, w8t, E4M3, s_dy, s_w)
+    gemm_tolerance_check(np_view(dx.float()).astype(np.float64), ref, ab, f"rowmajor dx {M}x{N}x{K}")
+    ref, ab = orc.gemm_ref(dy8t, dy_fmt, x8t, E4M3, s_dy, s_x)
+    gemm_tolerance_check(np_view(dw.float()).astype(np.float64), ref, ab, f"rowmajor dw {M}x{N}x{K}")
+    dx1, dw1 = torch.empty_like(dx), torch.empty_like(dw)
+    cuda_lib.fp8_linear_bwd(d_dy8, dev(dy8t), dev(w8t), dev(x8t), sc(s_dy), sc(s_w), sc(s_x), dx1, dw1,
+                            dy_fmt=dy_fmt)
+    assert cuda_lib.fp8mp_check() == 0
+    assert torch.equal(dx.float(), dx1.float()) and torch.equal(dw.float(), dw1.float())
+
+
+def test_backward_from_rowmajor_copies_one_side(cuda_lib, orc, engine):
+    """dx or dw None: only the other gradient is computed (and written)."""
+    M, N, K = 272, 400, 528
+    rng = np.random.default_rng(99)
+    dy8 = finite_codes(rng, (M, N), E5M2)
+    w8 = finite_codes(rng, (N, K), E4M3)
+    x8 = finite_codes(rng, (M, K), E4M3)
+    dx = torch.empty((M, K), dtype=torch.float32, device="cuda")
+    cuda_lib.fp8_linear_bwd_rowmajor(dev(dy8), dev(w8), None, sc(1.0), sc(1.0), None, dx, None)
+    dw = torch.empty((N, K), dtype=torch.float32, device="cuda")
+    cuda_lib.fp8_linear_bwd_rowmajor(dev(dy8), None, dev(x8), sc(1.0), None, sc(1.0), None, dw)
+    assert cuda_lib.fp8mp_check() == 0
+    ref, ab = orc.gemm_ref(dy8, E5M2, np.ascontiguousarray(w8.T), E4M3, 1.0, 1.0)
+    gemm_tolerance_check(np_view(dx).astype(np.float64), ref, ab, "rowmajor dx only")
+    ref, ab = orc.gemm_ref(np.ascontiguousarray(dy8.T), E5M2, np.ascontiguousarray(x8.T), E4M3, 1.0, 1.0)
+    gemm_tolerance_check(np_view(dw).astype(np.float64), ref, ab, "rowmajor dw only")
+
+
 def test_long_contraction_e5m2_wgrad(cuda_lib, orc, engine):
     """wgrad contracts over all tokens: 16384 here (the MLP workload's M)."""
     N, K, M = 256, 384, 16384

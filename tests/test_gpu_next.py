@@ -87,6 +87,29 @@ def test_dbias_fused_in_gradient_cast(cuda_lib, orc, rows, cols, dtype, db_dtype
     assert torch.equal(db.view(torch.uint8) if db.dtype == torch.uint8 else db, db2)
 
 
+@pytest.mark.parametrize("rows,cols", [(144, 272), (8192, 4096)])
+def test_dbias_without_transposed_copy(cuda_lib, orc, rows, cols):
+    """out_t = NULL: the same codes, amax and bias gradient, no transposed
+    copy (for a backward that reads dY8 row-major)."""
+    g = workloads.gen(3 * rows + cols)
+    dy = (torch.randn((rows, cols), generator=g) * 1e-3).to(torch.bfloat16).cuda()
+    scale = torch.tensor([8192.0], device="cuda")
+    ws = torch.empty(cuda_lib.fp8_quantize_dbias_workspace_bytes(rows, cols) // 4, dtype=torch.float32,
+                     device="cuda")
+    out, am, db = (torch.empty((rows, cols), dtype=torch.uint8, device="cuda"), torch.zeros(1, device="cuda"),
+                   torch.empty(cols, device="cuda"))
+    cuda_lib.fp8_quantize_dbias(dy, E5M2, scale, out, None, db, ws, amax=am)
+    out2, am2, db2 = torch.empty_like(out), torch.zeros(1, device="cuda"), torch.empty_like(db)
+    out_t = torch.empty((cols, rows), dtype=torch.uint8, device="cuda")
+    cuda_lib.fp8_quantize_dbias(dy, E5M2, scale, out2, out_t, db2, ws, amax=am2)
+    assert cuda_lib.fp8mp_check() == 0
+    dyn = np_view(dy)
+    assert_same_bits(out.cpu().numpy(), orc.cast(dyn, 8192.0, E5M2), "codes")
+    assert torch.equal(out, out2) and torch.equal(am, am2) and torch.equal(db, db2)
+    ref, ab = orc.dbias(dyn)
+    dbias_check(np_view(db), ref, ab, rows, False)
+
+
 def test_dbias_rejects_small_workspace(cuda_lib):
     dy = torch.ones((256, 64), dtype=torch.bfloat16, device="cuda")
     out = torch.empty((256, 64), dtype=torch.uint8, device="cuda")

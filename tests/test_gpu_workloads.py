@@ -134,10 +134,10 @@ def test_mlp_16_steps(cuda_lib, orc):
         sinv = {k: dm[k].scale_inv for k in fmt}
         f.fp8_linear_fwd(XU, WU, sinv["x_up"], sinv["w_up"], h, y_amax=dm["h"].cur_amax)
         f.fp8_linear_fwd(XD, WD, sinv["x_down"], sinv["w_down"], y, y_amax=dm["y"].cur_amax)
-        f.fp8_linear_dgrad(DY, WDt, sinv["dy"], sinv["w_down"], dxd)
-        f.fp8_linear_wgrad(DYt, XDt, sinv["dy"], sinv["x_down"], dwd)
-        f.fp8_linear_dgrad(DH, WUt, sinv["dh"], sinv["w_up"], dxu)
-        f.fp8_linear_wgrad(DHt, XUt, sinv["dh"], sinv["x_up"], dwu)
+        # the down projection's backward from transposed copies, the up
+        # projection's from the row-major copies (both fused launches)
+        f.fp8_linear_bwd(DY, DYt, WDt, XDt, sinv["dy"], sinv["w_down"], sinv["x_down"], dxd, dwd)
+        f.fp8_linear_bwd_rowmajor(DH, WU, XU, sinv["dh"], sinv["w_up"], sinv["x_up"], dxu, dwu)
         assert f.fp8mp_check() == 0
         hh, yy = np_view(h.float()), np_view(y.float())
         # per-step output amax: exactly the max |.| of what was stored

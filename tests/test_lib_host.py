@@ -109,6 +109,22 @@ def test_fused_backward_rejects_bad_arguments(lib):
                               None) == fp8mp.OK
 
 
+def test_rowmajor_backward_rejects_bad_arguments(lib):
+    P = 1 << 20
+    bwd = lambda M, N, K, dx=P, dw=2 * P, fmt=1, dxt=1, dwt=1, w8=P, x8=P: lib.fp8_linear_bwd_rowmajor(
+        P, w8, x8, M, N, K, fmt, P, P, P, dx, dxt, dw, dwt, None)
+    for shape in ((24, 32, 32), (32, 40, 32), (32, 32, 8), (-16, 32, 32)):
+        assert bwd(*shape) == fp8mp.ERR_INVALID
+    assert bwd(32, 32, 32, fmt=3) == fp8mp.ERR_INVALID
+    assert bwd(32, 32, 32, dwt=7) == fp8mp.ERR_INVALID and "dw_dtype" in fp8mp.last_error()
+    assert bwd(32, 32, 32, w8=None) == fp8mp.ERR_INVALID and "w8" in fp8mp.last_error()
+    assert bwd(32, 32, 32, x8=P + 3) == fp8mp.ERR_INVALID and "aligned" in fp8mp.last_error()
+    assert bwd(32, 32, 32, dx=P, dw=P + 64) == fp8mp.ERR_INVALID and "overlap" in fp8mp.last_error()
+    # nothing requested: a no-op needing no pointer and no device
+    assert lib.fp8_linear_bwd_rowmajor(None, None, None, 32, 32, 32, 1, None, None, None, None, 1, None, 1,
+                                       None) == fp8mp.OK
+
+
 def test_scale_update_rejects_bad_metas(lib):
     P = 4096
     good = fp8mp.fp8mp_meta(P, P, P, P, 16, 0)
