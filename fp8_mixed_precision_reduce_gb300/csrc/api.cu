@@ -3,6 +3,7 @@
 // dispatch to the kernels' launchers. No computation happens here.
 #include <cstdarg>
 #include <cstdio>
+#include <cstdlib>
 #include <cstring>
 
 #include "fp8mp_internal.cuh"
@@ -24,6 +25,14 @@ int fail(int code, const char *fmt, ...) {
 }
 
 void clear_error() { g_last_error[0] = 0; }
+
+bool pdl_enabled() {
+    static const bool on = [] {
+        const char *v = std::getenv("FP8MP_PDL");
+        return !(v != nullptr && std::strcmp(v, "0") == 0);
+    }();
+    return on;
+}
 
 int current_device(DeviceInfo *info) {
     int dev = -1;

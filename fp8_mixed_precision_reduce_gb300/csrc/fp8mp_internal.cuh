@@ -28,6 +28,30 @@ int current_device(DeviceInfo *info);
 
 inline bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
+// Kernels of the library are launched with programmatic stream
+// serialization (programmatic dependent launch): a kernel may be scheduled
+// while the previous kernel on the stream drains, runs what touches no
+// global memory, and waits in griddepcontrol.wait for the previous grids to
+// complete (and their writes to be visible) before any global load or store.
+// FP8MP_PDL=0 in the environment launches them plainly (read once).
+bool pdl_enabled();
+
+template <typename... KArgs, typename... Args>
+cudaError_t launch_kernel(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                          Args &&...args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = pdl_enabled() ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, kernel, static_cast<Args &&>(args)...);
+}
+
 // Launchers (return FP8MP_* codes; arguments already validated).
 int launch_quantize_current(const void *x, int x_dtype, int64_t rows, int64_t cols, int fmt, int margin,
                             float *scale, float *scale_inv, float *amax, uint8_t *out, uint8_t *out_t,
@@ -81,6 +105,14 @@ int read_and_clear_timeout_flag(unsigned int *value);
 const char *last_error_message();
 
 // -------------------------------------------------------------- device side
+
+// Waits until the grids this one depends on (the previous kernel on the
+// stream) have completed and their memory is visible; returns at once when
+// the kernel was launched without programmatic serialization.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+// Lets the next kernel on the stream be scheduled (it still waits in
+// pdl_wait for this grid to complete before touching memory).
+__device__ __forceinline__ void pdl_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 
 // Largest finite value of each format.
 __host__ __device__ constexpr float fmt_max(int fmt) { return fmt == FP8MP_E4M3 ? 448.0f : 57344.0f; }

@@ -448,6 +448,9 @@ gemm_fp8_kernel(const __grid_constant__ GemmBatch batch) {
         __syncthreads();
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
+    // everything above touched only this CTA's shared memory and TMEM: it
+    // overlaps the previous kernel's tail; global memory waits for its end
+    pdl_wait();
 
     const int num_tiles = batch.num_tiles;
     const int rounds = (num_tiles + num_clusters - 1) / num_clusters;
@@ -496,6 +499,8 @@ gemm_fp8_kernel(const __grid_constant__ GemmBatch batch) {
                     if (issued_stages < C::STAGES) ++issued_stages;
                 }
             }
+            // the last loads are issued: the next kernel may be scheduled
+            pdl_launch_dependents();
             if (!ok && rank == 0) {
                 // let the loads already issued land before the CTA goes away
                 for (int j = 1; j <= issued_stages && j <= static_cast<int>(it); ++j) {
@@ -734,6 +739,8 @@ __global__ void timeout_selftest_kernel() {
 // out = bias (or 0) broadcast over rows: the GEMM of an empty contraction.
 __global__ void fill_bias_kernel(int64_t rows, int64_t cols, const void *bias, int bias_bf16, void *out,
                                  int out_bf16, float *out_amax, const float *out_scale, int out_fmt) {
+    pdl_wait();
+    pdl_launch_dependents();
     float am = 0.0f;
     const int64_t n = rows * cols;
     for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n;
@@ -832,18 +839,23 @@ template <bool PAIR>
 int launch_engine(const GemmBatch &batch, int grid, cudaStream_t s) {
     using C = Cfg<PAIR>;
     cudaLaunchConfig_t cfg = {};
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     cfg.gridDim = dim3(static_cast<unsigned>(grid));
     cfg.blockDim = dim3(NUM_THREADS);
     cfg.dynamicSmemBytes = C::SMEM_ALLOC;
     cfg.stream = s;
+    cfg.attrs = attr;
     if (PAIR) {
-        attr[0].id = cudaLaunchAttributeClusterDimension;
-        attr[0].val.clusterDim.x = 2;
-        attr[0].val.clusterDim.y = 1;
-        attr[0].val.clusterDim.z = 1;
-        cfg.attrs = attr;
-        cfg.numAttrs = 1;
+        attr[cfg.numAttrs].id = cudaLaunchAttributeClusterDimension;
+        attr[cfg.numAttrs].val.clusterDim.x = 2;
+        attr[cfg.numAttrs].val.clusterDim.y = 1;
+        attr[cfg.numAttrs].val.clusterDim.z = 1;
+        ++cfg.numAttrs;
+    }
+    if (pdl_enabled()) {
+        attr[cfg.numAttrs].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[cfg.numAttrs].val.programmaticStreamSerializationAllowed = 1;
+        ++cfg.numAttrs;
     }
     const cudaError_t e = cudaLaunchKernelEx(&cfg, gemm_fp8_kernel<PAIR>, batch);
     if (e != cudaSuccess) return fail(FP8MP_ERR_LAUNCH, "GEMM launch failed: %s", cudaGetErrorString(e));
@@ -893,10 +905,10 @@ int launch_gemms(const GemmDesc *descs, int n, cudaStream_t s, const DeviceInfo 
         if (d.kc == 0) {
             int64_t blocks = (d.rows_a * d.rows_b + 255) / 256;
             if (blocks > dev.num_sms * 8) blocks = dev.num_sms * 8;
-            fill_bias_kernel<<<static_cast<unsigned>(blocks), 256, 0, s>>>(
-                d.rows_a, d.rows_b, d.bias, d.bias_dtype == FP8MP_BF16, d.out, d.out_dtype == FP8MP_BF16,
-                d.out_amax, d.out_scale, d.out_fmt);
-            const cudaError_t e = cudaGetLastError();
+            const cudaError_t e = launch_kernel(fill_bias_kernel, dim3(static_cast<unsigned>(blocks)), dim3(256), 0,
+                                                s, d.rows_a, d.rows_b, d.bias, d.bias_dtype == FP8MP_BF16 ? 1 : 0,
+                                                d.out, d.out_dtype == FP8MP_BF16 ? 1 : 0, d.out_amax, d.out_scale,
+                                                d.out_fmt);
             if (e != cudaSuccess) return fail(FP8MP_ERR_LAUNCH, "GEMM fill launch failed: %s", cudaGetErrorString(e));
             continue;
         }

@@ -33,6 +33,8 @@ __device__ __forceinline__ bool has_nonfinite_bf16x2(uint32_t w) {
 
 __global__ void __launch_bounds__(kThreads)
 grad_scan_kernel(const uint16_t *__restrict__ g, int64_t n, int32_t *__restrict__ found_inf) {
+    pdl_wait();
+    pdl_launch_dependents();
     bool bad = false;
     const int64_t nvec = n >> 3;
     const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
@@ -63,6 +65,8 @@ master_update_kernel(const uint16_t *__restrict__ g, int64_t n, float *__restric
                      uint8_t *__restrict__ w8, const float *__restrict__ scale_w, float *__restrict__ amax_w,
                      const float *__restrict__ loss_scale, const int32_t *__restrict__ found_inf, float lr,
                      float mu) {
+    pdl_wait();
+    pdl_launch_dependents();
     if (*reinterpret_cast<const volatile int32_t *>(found_inf) != 0) return;  // skipped step
     const float inv_s = __fdiv_rn(1.0f, *loss_scale);
     const float sw = *scale_w;
@@ -116,6 +120,8 @@ master_update_kernel(const uint16_t *__restrict__ g, int64_t n, float *__restric
 __global__ void loss_scale_kernel(float *__restrict__ S, int32_t *__restrict__ growth,
                                   const int32_t *__restrict__ found_inf, float backoff, float growth_factor,
                                   int32_t interval) {
+    pdl_wait();
+    pdl_launch_dependents();
     if (*found_inf != 0) {
         *S = __fmul_rn(*S, backoff);
         *growth = 0;
@@ -140,6 +146,8 @@ adam_update_kernel(const uint16_t *__restrict__ g, int64_t n, float *__restrict_
                    float *__restrict__ amax_w, const float *__restrict__ loss_scale,
                    const int32_t *__restrict__ found_inf, const float *__restrict__ beta_pows, float lr, float b1,
                    float b2, float eps) {
+    pdl_wait();
+    pdl_launch_dependents();
     if (*reinterpret_cast<const volatile int32_t *>(found_inf) != 0) return;  // skipped step
     const float inv_s = __fdiv_rn(1.0f, *loss_scale);
     const float sw = *scale_w;
@@ -206,6 +214,8 @@ adam_update_kernel(const uint16_t *__restrict__ g, int64_t n, float *__restrict_
 __global__ void adam_bookkeeping_kernel(float *__restrict__ S, int32_t *__restrict__ growth,
                                         const int32_t *__restrict__ found_inf, float *__restrict__ beta_pows,
                                         float b1, float b2, float backoff, float growth_factor, int32_t interval) {
+    pdl_wait();
+    pdl_launch_dependents();
     if (*found_inf != 0) {
         *S = __fmul_rn(*S, backoff);
         *growth = 0;
@@ -236,13 +246,12 @@ int launch_adam_step(const uint16_t *g, int64_t n, float *w, float *m, float *v,
     if (blocks > cap) blocks = cap;
     if (blocks < 1) blocks = 1;
     if (n > 0) {
-        grad_scan_kernel<<<static_cast<unsigned>(blocks), kThreads, 0, s>>>(g, n, found_inf);
-        adam_update_kernel<<<static_cast<unsigned>(blocks), kThreads, 0, s>>>(g, n, w, m, v, w8, scale_w, amax_w,
-                                                                             loss_scale, found_inf, beta_pows, lr,
-                                                                             b1, b2, eps);
+        launch_kernel(grad_scan_kernel, dim3(static_cast<unsigned>(blocks)), dim3(kThreads), 0, s, g, n, found_inf);
+        launch_kernel(adam_update_kernel, dim3(static_cast<unsigned>(blocks)), dim3(kThreads), 0, s, g, n, w, m, v,
+                      w8, scale_w, amax_w, loss_scale, found_inf, beta_pows, lr, b1, b2, eps);
     }
-    adam_bookkeeping_kernel<<<1, 1, 0, s>>>(loss_scale, growth, found_inf, beta_pows, b1, b2, backoff,
-                                            growth_factor, growth_interval);
+    launch_kernel(adam_bookkeeping_kernel, dim3(1), dim3(1), 0, s, loss_scale, growth, found_inf, beta_pows, b1, b2,
+                  backoff, growth_factor, growth_interval);
     e = cudaGetLastError();
     if (e != cudaSuccess)
         return fail(FP8MP_ERR_LAUNCH, "mp_master_step_adam: launch failed: %s", cudaGetErrorString(e));
@@ -261,11 +270,12 @@ int launch_master_step(const uint16_t *g, int64_t n, float *w, float *v, uint8_t
     if (blocks > cap) blocks = cap;
     if (blocks < 1) blocks = 1;
     if (n > 0) {
-        grad_scan_kernel<<<static_cast<unsigned>(blocks), kThreads, 0, s>>>(g, n, found_inf);
-        master_update_kernel<<<static_cast<unsigned>(blocks), kThreads, 0, s>>>(g, n, w, v, w8, scale_w, amax_w,
-                                                                               loss_scale, found_inf, lr, mu);
+        launch_kernel(grad_scan_kernel, dim3(static_cast<unsigned>(blocks)), dim3(kThreads), 0, s, g, n, found_inf);
+        launch_kernel(master_update_kernel, dim3(static_cast<unsigned>(blocks)), dim3(kThreads), 0, s, g, n, w, v, w8,
+                      scale_w, amax_w, loss_scale, found_inf, lr, mu);
     }
-    loss_scale_kernel<<<1, 1, 0, s>>>(loss_scale, growth, found_inf, backoff, growth_factor, growth_interval);
+    launch_kernel(loss_scale_kernel, dim3(1), dim3(1), 0, s, loss_scale, growth, found_inf, backoff, growth_factor,
+                  growth_interval);
     e = cudaGetLastError();
     if (e != cudaSuccess) return fail(FP8MP_ERR_LAUNCH, "mp_master_step: launch failed: %s", cudaGetErrorString(e));
     return FP8MP_OK;

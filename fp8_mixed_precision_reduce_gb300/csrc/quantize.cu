@@ -77,6 +77,8 @@ template <int FMT, bool BF16>
 __global__ void __launch_bounds__(kThreads)
 cast_rows_kernel(const void *__restrict__ x, int64_t n, const float *__restrict__ scale_p,
                  uint8_t *__restrict__ out, float *__restrict__ amax_p) {
+    pdl_wait();
+    pdl_launch_dependents();
     const float scale = __ldg(scale_p);
     float am = 0.0f;
     const int64_t nchunk = n >> 4;
@@ -122,6 +124,8 @@ __global__ void __launch_bounds__(kThreads)
 cast_rows_t_kernel(const void *__restrict__ x, int64_t rows, int64_t cols, const float *__restrict__ scale_p,
                    uint8_t *__restrict__ out, uint8_t *__restrict__ out_t, float *__restrict__ amax_p,
                    float *__restrict__ ws) {
+    pdl_wait();
+    pdl_launch_dependents();
     __shared__ __align__(16) uint32_t sT[128 * 32];
     __shared__ float s_colsum[DBIAS ? 16 * 128 : 1];
     float csum[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
@@ -210,6 +214,8 @@ cast_rows_t_kernel(const void *__restrict__ x, int64_t rows, int64_t cols, const
 __global__ void __launch_bounds__(kThreads)
 dbias_reduce_kernel(const float *__restrict__ ws, int64_t tile_rows, int64_t cols, void *__restrict__ dbias,
                     int bf16_out) {
+    pdl_wait();
+    pdl_launch_dependents();
     const int64_t n = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
     if (n >= cols) return;
     float t = 0.0f;
@@ -230,16 +236,17 @@ int launch_typed(const void *x, int64_t rows, int64_t cols, const float *scale, 
         const int64_t cap = static_cast<int64_t>(dev.num_sms) * 8;
         if (blocks > cap) blocks = cap;
         if (blocks < 1) blocks = 1;
-        cast_rows_kernel<FMT, BF16><<<static_cast<unsigned>(blocks), kThreads, 0, s>>>(x, n, scale, out, amax);
+        launch_kernel(cast_rows_kernel<FMT, BF16>, dim3(static_cast<unsigned>(blocks)), dim3(kThreads), 0, s, x, n,
+                      scale, out, amax);
     } else {
         const int64_t tiles = ((rows + 127) >> 7) * ((cols + 127) >> 7);
         if (tiles > 0x7FFFFFFF) return fail(FP8MP_ERR_INVALID, "fp8_quantize: tensor too large");
         if (ws != nullptr)
-            cast_rows_t_kernel<FMT, BF16, true>
-                <<<static_cast<unsigned>(tiles), kThreads, 0, s>>>(x, rows, cols, scale, out, out_t, amax, ws);
+            launch_kernel(cast_rows_t_kernel<FMT, BF16, true>, dim3(static_cast<unsigned>(tiles)), dim3(kThreads), 0,
+                          s, x, rows, cols, scale, out, out_t, amax, ws);
         else
-            cast_rows_t_kernel<FMT, BF16, false>
-                <<<static_cast<unsigned>(tiles), kThreads, 0, s>>>(x, rows, cols, scale, out, out_t, amax, nullptr);
+            launch_kernel(cast_rows_t_kernel<FMT, BF16, false>, dim3(static_cast<unsigned>(tiles)), dim3(kThreads), 0,
+                          s, x, rows, cols, scale, out, out_t, amax, nullptr);
     }
     const cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return fail(FP8MP_ERR_LAUNCH, "fp8_quantize: launch failed: %s", cudaGetErrorString(e));
@@ -251,6 +258,8 @@ int launch_typed(const void *x, int64_t rows, int64_t cols, const float *scale, 
 template <bool BF16>
 __global__ void __launch_bounds__(kThreads)
 amax_kernel(const void *__restrict__ x, int64_t n, float *__restrict__ amax_p) {
+    pdl_wait();
+    pdl_launch_dependents();
     float am = 0.0f;
     const int64_t nchunk = n >> 4;
     const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
@@ -268,6 +277,8 @@ amax_kernel(const void *__restrict__ x, int64_t n, float *__restrict__ amax_p) {
 // scale and scale_inv from this tensor's amax (the current-scaling rule).
 __global__ void current_scale_kernel(const float *__restrict__ amax, float *__restrict__ scale,
                                      float *__restrict__ scale_inv, int fmt, int margin) {
+    pdl_wait();
+    pdl_launch_dependents();
     const float sc = scale_from_amax(*amax, *scale, fmt, margin);
     *scale = sc;
     *scale_inv = __fdiv_rn(1.0f, sc);
@@ -286,10 +297,10 @@ int launch_quantize_current(const void *x, int x_dtype, int64_t rows, int64_t co
     if (blocks > cap) blocks = cap;
     if (blocks < 1) blocks = 1;
     if (x_dtype == FP8MP_BF16)
-        amax_kernel<true><<<static_cast<unsigned>(blocks), kThreads, 0, s>>>(x, n, amax);
+        launch_kernel(amax_kernel<true>, dim3(static_cast<unsigned>(blocks)), dim3(kThreads), 0, s, x, n, amax);
     else
-        amax_kernel<false><<<static_cast<unsigned>(blocks), kThreads, 0, s>>>(x, n, amax);
-    current_scale_kernel<<<1, 1, 0, s>>>(amax, scale, scale_inv, fmt, margin);
+        launch_kernel(amax_kernel<false>, dim3(static_cast<unsigned>(blocks)), dim3(kThreads), 0, s, x, n, amax);
+    launch_kernel(current_scale_kernel, dim3(1), dim3(1), 0, s, amax, scale, scale_inv, fmt, margin);
     e = cudaGetLastError();
     if (e != cudaSuccess)
         return fail(FP8MP_ERR_LAUNCH, "fp8_quantize_current: launch failed: %s", cudaGetErrorString(e));
@@ -310,8 +321,8 @@ int launch_quantize_dbias(const void *x, int x_dtype, int64_t rows, int64_t cols
                   : launch_typed<FP8MP_E5M2, false>(x, rows, cols, scale, out, out_t, amax, s, dev, ws);
     if (rc) return rc;
     const int64_t tile_rows = (rows + 127) >> 7;
-    dbias_reduce_kernel<<<static_cast<unsigned>((cols + kThreads - 1) / kThreads), kThreads, 0, s>>>(
-        ws, tile_rows, cols, dbias, dbias_dtype == FP8MP_BF16);
+    launch_kernel(dbias_reduce_kernel, dim3(static_cast<unsigned>((cols + kThreads - 1) / kThreads)), dim3(kThreads),
+                  0, s, ws, tile_rows, cols, dbias, dbias_dtype == FP8MP_BF16 ? 1 : 0);
     const cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess)
         return fail(FP8MP_ERR_LAUNCH, "fp8_quantize_dbias: launch failed: %s", cudaGetErrorString(e));

@@ -38,6 +38,8 @@ struct MetaBatch {
 };
 
 __global__ void __launch_bounds__(kThreads) scale_update_kernel(const __grid_constant__ MetaBatch b) {
+    pdl_wait();
+    pdl_launch_dependents();
     extern __shared__ float old_hist[];
     const MetaArgs &m = b.m[blockIdx.x];
     const int L = m.len;
@@ -83,7 +85,7 @@ int launch_scale_update(const fp8mp_meta *metas, int32_t n, int32_t algo, int32_
         b.margin = margin;
         // at most FP8MP_MAX_HISTORY floats = 32 KB, inside the default 48 KB
         const size_t smem = static_cast<size_t>(max_len) * sizeof(float);
-        scale_update_kernel<<<cnt, kThreads, smem, s>>>(b);
+        launch_kernel(scale_update_kernel, dim3(static_cast<unsigned>(cnt)), dim3(kThreads), smem, s, b);
         const cudaError_t e = cudaGetLastError();
         if (e != cudaSuccess)
             return fail(FP8MP_ERR_LAUNCH, "delayed_scaling_update: launch failed: %s", cudaGetErrorString(e));
