@@ -493,10 +493,15 @@ int fp8mp_check(void *stream) {
     clear_error();
     cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return fail(FP8MP_ERR_LAUNCH, "stream synchronize failed: %s", cudaGetErrorString(e));
-    unsigned int flag = 0;
-    const int rc = read_and_clear_timeout_flag(&flag);
+    unsigned int flag = 0, mflag = 0;
+    int rc = read_and_clear_timeout_flag(&flag);
+    if (rc) return rc;
+    rc = read_and_clear_master_timeout_flag(&mflag);
     if (rc) return rc;
     if (flag) return fail(FP8MP_ERR_TIMEOUT, "a GEMM kernel's bounded wait expired; its output is undefined");
+    if (mflag)
+        return fail(FP8MP_ERR_TIMEOUT, "the master step's bounded grid barrier expired; the step's results are "
+                                       "undefined");
     return FP8MP_OK;
 }
 

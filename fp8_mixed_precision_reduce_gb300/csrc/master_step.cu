@@ -1,6 +1,7 @@
 // master_step.cu -- one mixed-precision optimizer step over a flat parameter
-// buffer: overflow scan, loss unscale, FP32 master SGD-momentum update, E4M3
-// re-cast of the weights and their amax, and the dynamic loss-scale update.
+// buffer: overflow scan, loss unscale, FP32 master update (SGD with momentum
+// or Adam), E4M3 re-cast of the weights and their amax, and the dynamic
+// loss-scale update.
 //
 // Pages: "LLM) Mixed-Precision 개념 및 학습 방법 알아보기" (data-newbie.tistory.com),
 // "FP32 Master Copy of Weights", "Mixed-Precision Training Iteration" (steps
@@ -8,189 +9,216 @@
 // the dynamic loss-scaling procedure (an Inf/NaN gradient lowers S and skips
 // the update; a run of clean steps raises S); "Как работает FP8 quantization
 // на H100 (Transformer Engine)?" (aivaro.ru) section 7 (FP32 master weights
-// with FP8 forward/backward copies).
+// with FP8 forward/backward copies); "Các kiểu dữ liệu FP8 gốc của PyTorch
+// ..." (hotroai.com), the float8_experimental training loop (torch.optim.Adam).
 //
-// Three launches on the caller's stream, no host round trip:
-//   1. grad_scan_kernel: reads the bf16 gradients once (2 B/param) and sets
-//      found_inf when any exponent field is all ones;
-//   2. master_update_kernel: every block first reads found_inf and leaves if
-//      it is set; otherwise one pass reads g, v, w (10 B/param) and writes
-//      v, w, w8 (9 B/param), fusing the unscale, the momentum and master
-//      updates, the E4M3 cast under the weight scale and the weight amax;
-//   3. loss_scale_kernel: one thread updates S and the growth counter after
-//      every block of pass 2 has read S.
+// The step is three passes: scan the bf16 gradients for Inf/NaN (2 B/param);
+// unless one was found, one fused pass per element (unscale, optimizer
+// update, E4M3 cast under the weight scale, weight amax); then S and the
+// growth counter (and Adam's beta powers) change by one thread, after every
+// element has read S. Two ways to run it, same arithmetic (the per-element
+// operations live once, in SgdOpt / AdamOpt):
+//   fused (default): one cooperative launch. Each block scans its slice,
+//     the blocks meet at a bounded grid barrier, each block updates its
+//     slice (re-reading the gradients it scanned, kept in L2 by an
+//     evict-last hint), and the last block to finish does the bookkeeping;
+//   three launches (FP8MP_FUSED_MASTER=0): grad_scan_kernel, the update
+//     kernel (every block leaves at once when found_inf is set), and a
+//     one-thread bookkeeping kernel.
+#include <cstdlib>
+#include <cstring>
+
 #include "fp8mp_internal.cuh"
 
 namespace fp8mp {
+
+__device__ unsigned int g_master_timeout_flag = 0;
+
 namespace {
 
 constexpr int kThreads = 256;
+constexpr long long kBarrierLimitCycles = 4000000000ll;  // about 2 s at the SM clock
 
 __device__ __forceinline__ bool has_nonfinite_bf16x2(uint32_t w) {
     const uint32_t t = (w & 0x7F807F80u) ^ 0x7F807F80u;  // a zero half <=> exponent all ones
     return (t & 0xFFFFu) == 0u || (t >> 16) == 0u;
 }
 
-__global__ void __launch_bounds__(kThreads)
-grad_scan_kernel(const uint16_t *__restrict__ g, int64_t n, int32_t *__restrict__ found_inf) {
-    pdl_wait();
-    pdl_launch_dependents();
+// L2 policy: keep the lines (the fused step re-reads the gradients).
+__device__ __forceinline__ uint64_t evict_last_policy() {
+    uint64_t p;
+    asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
+    return p;
+}
+__device__ __forceinline__ uint4 ld_with_policy(const uint4 *ptr, uint64_t pol) {
+    uint4 r;
+    asm volatile("ld.global.L2::cache_hint.v4.u32 {%0, %1, %2, %3}, [%4], %5;"
+                 : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+                 : "l"(ptr), "l"(pol)
+                 : "memory");
+    return r;
+}
+
+// Scans this thread's grid-stride share of the gradients (16-byte vectors,
+// the n % 8 tail by the last block).
+template <bool KEEP_IN_L2>
+__device__ __forceinline__ bool scan_share(const uint16_t *__restrict__ g, int64_t n) {
     bool bad = false;
     const int64_t nvec = n >> 3;
     const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
     const uint4 *g4 = reinterpret_cast<const uint4 *>(g);
+    uint64_t pol = 0;
+    if constexpr (KEEP_IN_L2) pol = evict_last_policy();
     for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < nvec; i += stride) {
-        const uint4 d = __ldcs(g4 + i);
+        uint4 d;
+        if constexpr (KEEP_IN_L2)
+            d = ld_with_policy(g4 + i, pol);
+        else
+            d = __ldcs(g4 + i);
         bad |= has_nonfinite_bf16x2(d.x) | has_nonfinite_bf16x2(d.y) | has_nonfinite_bf16x2(d.z) |
                has_nonfinite_bf16x2(d.w);
     }
     if (blockIdx.x == gridDim.x - 1)
         for (int64_t i = (nvec << 3) + threadIdx.x; i < n; i += blockDim.x) bad |= (g[i] & 0x7F80u) == 0x7F80u;
-    if (__syncthreads_or(bad) && threadIdx.x == 0) *found_inf = 1;
+    return bad;
 }
 
-struct Elem {
-    float v, w;
+// ---------------------------------------------------------- optimizers
+
+struct SgdArgs {
+    float *w, *v;
+    float lr, mu;
 };
 
-__device__ __forceinline__ Elem update_one(float g, float v, float w, float inv_s, float mu, float neg_lr) {
-    const float u = __fmul_rn(g, inv_s);
-    const float vn = __fmaf_rn(mu, v, u);
-    const float wn = __fmaf_rn(neg_lr, vn, w);
-    return Elem{vn, wn};
-}
-
-__global__ void __launch_bounds__(kThreads)
-master_update_kernel(const uint16_t *__restrict__ g, int64_t n, float *__restrict__ w, float *__restrict__ v,
-                     uint8_t *__restrict__ w8, const float *__restrict__ scale_w, float *__restrict__ amax_w,
-                     const float *__restrict__ loss_scale, const int32_t *__restrict__ found_inf, float lr,
-                     float mu) {
-    pdl_wait();
-    pdl_launch_dependents();
-    if (*reinterpret_cast<const volatile int32_t *>(found_inf) != 0) return;  // skipped step
-    const float inv_s = __fdiv_rn(1.0f, *loss_scale);
-    const float sw = *scale_w;
-    const float neg_lr = -lr;
-    float am = 0.0f;
-    const int64_t nvec = n >> 3;
-    const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
-    for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < nvec; i += stride) {
-        const uint4 gd = __ldcs(reinterpret_cast<const uint4 *>(g) + i);
+// SGD with momentum: u = g * fl32(1/S); v = fmaf(mu, v, u); w = fmaf(-lr, v, w).
+struct SgdOpt {
+    float *w, *v;
+    float inv_s, mu, neg_lr;
+    __device__ __forceinline__ float one(float g, float &vi, float wi) const {
+        const float u = __fmul_rn(g, inv_s);
+        vi = __fmaf_rn(mu, vi, u);
+        return __fmaf_rn(neg_lr, vi, wi);
+    }
+    // 8 parameters starting at 8*i; returns the 8 new master weights in wf.
+    __device__ __forceinline__ void vec8(int64_t i, const float gf[8], float wf[8]) const {
         float4 *v4 = reinterpret_cast<float4 *>(v) + 2 * i;
         float4 *w4 = reinterpret_cast<float4 *>(w) + 2 * i;
         const float4 va = __ldcs(v4), vb = __ldcs(v4 + 1);
         const float4 wa = __ldcs(w4), wb = __ldcs(w4 + 1);
-        const uint32_t gw[4] = {gd.x, gd.y, gd.z, gd.w};
-        float gf[8], vf[8] = {va.x, va.y, va.z, va.w, vb.x, vb.y, vb.z, vb.w},
-                     wf[8] = {wa.x, wa.y, wa.z, wa.w, wb.x, wb.y, wb.z, wb.w};
+        float vf[8] = {va.x, va.y, va.z, va.w, vb.x, vb.y, vb.z, vb.w};
+        const float wo[8] = {wa.x, wa.y, wa.z, wa.w, wb.x, wb.y, wb.z, wb.w};
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            gf[2 * j] = __uint_as_float(gw[j] << 16);
-            gf[2 * j + 1] = __uint_as_float(gw[j] & 0xFFFF0000u);
-        }
-#pragma unroll
-        for (int j = 0; j < 8; ++j) {
-            const Elem e = update_one(gf[j], vf[j], wf[j], inv_s, mu, neg_lr);
-            vf[j] = e.v;
-            wf[j] = e.w;
-            am = max_ignore_nan(am, fabsf(e.w));
-        }
+        for (int j = 0; j < 8; ++j) wf[j] = one(gf[j], vf[j], wo[j]);
         __stcs(v4, make_float4(vf[0], vf[1], vf[2], vf[3]));
         __stcs(v4 + 1, make_float4(vf[4], vf[5], vf[6], vf[7]));
         __stcs(w4, make_float4(wf[0], wf[1], wf[2], wf[3]));
         __stcs(w4 + 1, make_float4(wf[4], wf[5], wf[6], wf[7]));
-        const uint32_t q0 = cvt_quad<FP8MP_E4M3>(__fmul_rn(wf[0], sw), __fmul_rn(wf[1], sw), __fmul_rn(wf[2], sw),
-                                                 __fmul_rn(wf[3], sw));
-        const uint32_t q1 = cvt_quad<FP8MP_E4M3>(__fmul_rn(wf[4], sw), __fmul_rn(wf[5], sw), __fmul_rn(wf[6], sw),
-                                                 __fmul_rn(wf[7], sw));
-        reinterpret_cast<uint2 *>(w8)[i] = make_uint2(q0, q1);
     }
-    if (blockIdx.x == gridDim.x - 1) {
-        for (int64_t i = (nvec << 3) + threadIdx.x; i < n; i += blockDim.x) {
-            const Elem e = update_one(bf16_bits_to_f32(g[i]), v[i], w[i], inv_s, mu, neg_lr);
-            v[i] = e.v;
-            w[i] = e.w;
-            w8[i] = static_cast<uint8_t>(cvt_pair<FP8MP_E4M3>(__fmul_rn(e.w, sw), 0.0f) & 0xFFu);
-            am = max_ignore_nan(am, fabsf(e.w));
-        }
+    __device__ __forceinline__ float scalar(int64_t i, float g) const {
+        float vi = v[i];
+        const float wn = one(g, vi, w[i]);
+        v[i] = vi;
+        w[i] = wn;
+        return wn;
     }
-    block_amax_atomic(am, amax_w);
-}
+};
 
-__global__ void loss_scale_kernel(float *__restrict__ S, int32_t *__restrict__ growth,
-                                  const int32_t *__restrict__ found_inf, float backoff, float growth_factor,
-                                  int32_t interval) {
-    pdl_wait();
-    pdl_launch_dependents();
-    if (*found_inf != 0) {
-        *S = __fmul_rn(*S, backoff);
-        *growth = 0;
-    } else {
-        int32_t gr = *growth + 1;
-        if (gr >= interval) {
-            *S = __fmul_rn(*S, growth_factor);
-            gr = 0;
-        }
-        *growth = gr;
-    }
-}
+struct AdamArgs {
+    float *w, *m, *v;
+    float *beta_pows;
+    float lr, b1, b2, eps;
+};
 
-// Adam variant of pass 2 (same skip rule). Per element, each operation one
-// correctly rounded fp32 operation in this order:
-//   u = g * fl32(1/S); m = fmaf(b1, m, (1-b1) * u); v = fmaf(b2, v, (1-b2) * (u*u))
-//   w = fmaf(-lr, (m / (1 - b1^t)) / (sqrt(v / (1 - b2^t)) + eps), w)
-// with b^t = fl32(b^(t-1) * b) from the running powers in beta_pows.
-__global__ void __launch_bounds__(kThreads)
-adam_update_kernel(const uint16_t *__restrict__ g, int64_t n, float *__restrict__ w, float *__restrict__ m,
-                   float *__restrict__ v, uint8_t *__restrict__ w8, const float *__restrict__ scale_w,
-                   float *__restrict__ amax_w, const float *__restrict__ loss_scale,
-                   const int32_t *__restrict__ found_inf, const float *__restrict__ beta_pows, float lr, float b1,
-                   float b2, float eps) {
-    pdl_wait();
-    pdl_launch_dependents();
-    if (*reinterpret_cast<const volatile int32_t *>(found_inf) != 0) return;  // skipped step
-    const float inv_s = __fdiv_rn(1.0f, *loss_scale);
-    const float sw = *scale_w;
-    const float c1 = __fsub_rn(1.0f, b1), c2 = __fsub_rn(1.0f, b2);
-    const float bc1 = __fsub_rn(1.0f, __fmul_rn(beta_pows[0], b1));
-    const float bc2 = __fsub_rn(1.0f, __fmul_rn(beta_pows[1], b2));
-    const float neg_lr = -lr;
-    float am = 0.0f;
-    auto one = [&](float gf, float &mi, float &vi, float &wi) {
-        const float u = __fmul_rn(gf, inv_s);
+// Adam: u = g * fl32(1/S); m = fmaf(b1, m, (1-b1) * u); v = fmaf(b2, v, (1-b2) * (u*u));
+// w = fmaf(-lr, (m / (1 - b1^t)) / (sqrt(v / (1 - b2^t)) + eps), w), each operation one correctly
+// rounded fp32 operation in this order, with b^t = fl32(b^(t-1) * b) from the running powers.
+struct AdamOpt {
+    float *w, *m, *v;
+    float inv_s, b1, b2, c1, c2, bc1, bc2, eps, neg_lr;
+    __device__ __forceinline__ float one(float g, float &mi, float &vi, float wi) const {
+        const float u = __fmul_rn(g, inv_s);
         mi = __fmaf_rn(b1, mi, __fmul_rn(c1, u));
         vi = __fmaf_rn(b2, vi, __fmul_rn(c2, __fmul_rn(u, u)));
         const float mh = __fdiv_rn(mi, bc1);
         const float vh = __fdiv_rn(vi, bc2);
         const float den = __fadd_rn(__fsqrt_rn(vh), eps);
-        wi = __fmaf_rn(neg_lr, __fdiv_rn(mh, den), wi);
-        am = max_ignore_nan(am, fabsf(wi));
-    };
-    const int64_t nvec = n >> 3;
-    const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
-    for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < nvec; i += stride) {
-        const uint4 gd = __ldcs(reinterpret_cast<const uint4 *>(g) + i);
+        return __fmaf_rn(neg_lr, __fdiv_rn(mh, den), wi);
+    }
+    __device__ __forceinline__ void vec8(int64_t i, const float gf[8], float wf[8]) const {
         float4 *m4 = reinterpret_cast<float4 *>(m) + 2 * i;
         float4 *v4 = reinterpret_cast<float4 *>(v) + 2 * i;
         float4 *w4 = reinterpret_cast<float4 *>(w) + 2 * i;
         const float4 ma = __ldcs(m4), mb = __ldcs(m4 + 1);
         const float4 va = __ldcs(v4), vb = __ldcs(v4 + 1);
         const float4 wa = __ldcs(w4), wb = __ldcs(w4 + 1);
-        const uint32_t gw[4] = {gd.x, gd.y, gd.z, gd.w};
         float mf[8] = {ma.x, ma.y, ma.z, ma.w, mb.x, mb.y, mb.z, mb.w};
         float vf[8] = {va.x, va.y, va.z, va.w, vb.x, vb.y, vb.z, vb.w};
-        float wf[8] = {wa.x, wa.y, wa.z, wa.w, wb.x, wb.y, wb.z, wb.w};
+        const float wo[8] = {wa.x, wa.y, wa.z, wa.w, wb.x, wb.y, wb.z, wb.w};
 #pragma unroll
-        for (int j = 0; j < 8; ++j) {
-            const float gf = (j & 1) ? __uint_as_float(gw[j >> 1] & 0xFFFF0000u) : __uint_as_float(gw[j >> 1] << 16);
-            one(gf, mf[j], vf[j], wf[j]);
-        }
+        for (int j = 0; j < 8; ++j) wf[j] = one(gf[j], mf[j], vf[j], wo[j]);
         __stcs(m4, make_float4(mf[0], mf[1], mf[2], mf[3]));
         __stcs(m4 + 1, make_float4(mf[4], mf[5], mf[6], mf[7]));
         __stcs(v4, make_float4(vf[0], vf[1], vf[2], vf[3]));
         __stcs(v4 + 1, make_float4(vf[4], vf[5], vf[6], vf[7]));
         __stcs(w4, make_float4(wf[0], wf[1], wf[2], wf[3]));
         __stcs(w4 + 1, make_float4(wf[4], wf[5], wf[6], wf[7]));
+    }
+    __device__ __forceinline__ float scalar(int64_t i, float g) const {
+        float mi = m[i], vi = v[i];
+        const float wn = one(g, mi, vi, w[i]);
+        m[i] = mi;
+        v[i] = vi;
+        w[i] = wn;
+        return wn;
+    }
+};
+
+__device__ __forceinline__ SgdOpt make_opt(const SgdArgs &a, float inv_s) {
+    SgdOpt o;
+    o.w = a.w;
+    o.v = a.v;
+    o.inv_s = inv_s;
+    o.mu = a.mu;
+    o.neg_lr = -a.lr;
+    return o;
+}
+__device__ __forceinline__ AdamOpt make_opt(const AdamArgs &a, float inv_s) {
+    AdamOpt o;
+    o.w = a.w;
+    o.m = a.m;
+    o.v = a.v;
+    o.inv_s = inv_s;
+    o.b1 = a.b1;
+    o.b2 = a.b2;
+    o.c1 = __fsub_rn(1.0f, a.b1);
+    o.c2 = __fsub_rn(1.0f, a.b2);
+    o.bc1 = __fsub_rn(1.0f, __fmul_rn(a.beta_pows[0], a.b1));
+    o.bc2 = __fsub_rn(1.0f, __fmul_rn(a.beta_pows[1], a.b2));
+    o.eps = a.eps;
+    o.neg_lr = -a.lr;
+    return o;
+}
+
+// The update pass over this thread's grid-stride share: the optimizer, the
+// E4M3 re-cast of the new master weights under *scale_w, their max |w|.
+template <class Opt>
+__device__ __forceinline__ float update_share(const Opt &opt, const uint16_t *__restrict__ g, int64_t n,
+                                              uint8_t *__restrict__ w8, float sw) {
+    float am = 0.0f;
+    const int64_t nvec = n >> 3;
+    const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+    for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < nvec; i += stride) {
+        const uint4 gd = __ldcs(reinterpret_cast<const uint4 *>(g) + i);
+        const uint32_t gw[4] = {gd.x, gd.y, gd.z, gd.w};
+        float gf[8], wf[8];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            gf[2 * j] = __uint_as_float(gw[j] << 16);
+            gf[2 * j + 1] = __uint_as_float(gw[j] & 0xFFFF0000u);
+        }
+        opt.vec8(i, gf, wf);
+#pragma unroll
+        for (int j = 0; j < 8; ++j) am = max_ignore_nan(am, fabsf(wf[j]));
         const uint32_t q0 = cvt_quad<FP8MP_E4M3>(__fmul_rn(wf[0], sw), __fmul_rn(wf[1], sw), __fmul_rn(wf[2], sw),
                                                  __fmul_rn(wf[3], sw));
         const uint32_t q1 = cvt_quad<FP8MP_E4M3>(__fmul_rn(wf[4], sw), __fmul_rn(wf[5], sw), __fmul_rn(wf[6], sw),
@@ -199,29 +227,21 @@ adam_update_kernel(const uint16_t *__restrict__ g, int64_t n, float *__restrict_
     }
     if (blockIdx.x == gridDim.x - 1) {
         for (int64_t i = (nvec << 3) + threadIdx.x; i < n; i += blockDim.x) {
-            float mi = m[i], vi = v[i], wi = w[i];
-            one(bf16_bits_to_f32(g[i]), mi, vi, wi);
-            m[i] = mi;
-            v[i] = vi;
-            w[i] = wi;
-            w8[i] = static_cast<uint8_t>(cvt_pair<FP8MP_E4M3>(__fmul_rn(wi, sw), 0.0f) & 0xFFu);
+            const float wn = opt.scalar(i, bf16_bits_to_f32(g[i]));
+            w8[i] = static_cast<uint8_t>(cvt_pair<FP8MP_E4M3>(__fmul_rn(wn, sw), 0.0f) & 0xFFu);
+            am = max_ignore_nan(am, fabsf(wn));
         }
     }
-    block_amax_atomic(am, amax_w);
+    return am;
 }
 
-// Loss-scale update plus, on a clean step, beta_pows = (b1^t, b2^t).
-__global__ void adam_bookkeeping_kernel(float *__restrict__ S, int32_t *__restrict__ growth,
-                                        const int32_t *__restrict__ found_inf, float *__restrict__ beta_pows,
-                                        float b1, float b2, float backoff, float growth_factor, int32_t interval) {
-    pdl_wait();
-    pdl_launch_dependents();
-    if (*found_inf != 0) {
+// S and the growth counter after a step with overflow flag `found`.
+__device__ __forceinline__ void loss_scale_update(float *S, int32_t *growth, int found, float backoff,
+                                                  float growth_factor, int32_t interval) {
+    if (found) {
         *S = __fmul_rn(*S, backoff);
         *growth = 0;
     } else {
-        beta_pows[0] = __fmul_rn(beta_pows[0], b1);
-        beta_pows[1] = __fmul_rn(beta_pows[1], b2);
         int32_t gr = *growth + 1;
         if (gr >= interval) {
             *S = __fmul_rn(*S, growth_factor);
@@ -229,6 +249,171 @@ __global__ void adam_bookkeeping_kernel(float *__restrict__ S, int32_t *__restri
         }
         *growth = gr;
     }
+}
+
+struct NoExtra {
+    __device__ void clean_step() const {}
+};
+// Adam's beta powers advance on clean steps only.
+struct AdamExtra {
+    float *beta_pows;
+    float b1, b2;
+    __device__ void clean_step() const {
+        beta_pows[0] = __fmul_rn(beta_pows[0], b1);
+        beta_pows[1] = __fmul_rn(beta_pows[1], b2);
+    }
+};
+
+struct StepCommon {
+    const uint16_t *g;
+    int64_t n;
+    uint8_t *w8;
+    const float *scale_w;
+    float *amax_w;
+    float *loss_scale;
+    int32_t *growth;
+    int32_t *found_inf;
+    float backoff, growth_factor;
+    int32_t interval;
+};
+
+// ------------------------------------------------ three-launch version
+
+__global__ void __launch_bounds__(kThreads)
+grad_scan_kernel(const uint16_t *__restrict__ g, int64_t n, int32_t *__restrict__ found_inf) {
+    pdl_wait();
+    pdl_launch_dependents();
+    const bool bad = scan_share<false>(g, n);
+    if (__syncthreads_or(bad) && threadIdx.x == 0) *found_inf = 1;
+}
+
+template <class Opt, class Args>
+__global__ void __launch_bounds__(kThreads) update_kernel(const StepCommon c, const Args a) {
+    pdl_wait();
+    pdl_launch_dependents();
+    if (*reinterpret_cast<const volatile int32_t *>(c.found_inf) != 0) return;  // skipped step
+    const Opt opt = make_opt(a, __fdiv_rn(1.0f, *c.loss_scale));
+    const float am = update_share(opt, c.g, c.n, c.w8, *c.scale_w);
+    block_amax_atomic(am, c.amax_w);
+}
+
+template <class Extra>
+__global__ void bookkeeping_kernel(const StepCommon c, const Extra x) {
+    pdl_wait();
+    pdl_launch_dependents();
+    const int found = *c.found_inf != 0;
+    if (!found) x.clean_step();
+    loss_scale_update(c.loss_scale, c.growth, found, c.backoff, c.growth_factor, c.interval);
+}
+
+// ---------------------------------------------------- fused version
+
+// found_inf is 0 on entry (the launcher zeroes it on the stream first).
+// While the kernel runs, bit 0 of found_inf is the overflow flag (atomicOr)
+// and the bits above count block arrivals (atomicAdd of 2, which never
+// carries into bit 0): gridDim.x arrivals close the scan, 2 * gridDim.x the
+// step. The last block to arrive does the bookkeeping and leaves found_inf
+// holding the flag alone (0 or 1). The launch is cooperative, so every
+// block is resident and the barrier completes; its wait is still bounded
+// (about 2 s), after which the block sets a device flag that fp8mp_check()
+// reports and skips the update (the step's results are then undefined).
+template <class Opt, class Args, class Extra>
+__global__ void __launch_bounds__(kThreads) fused_step_kernel(const StepCommon c, const Args a, const Extra x) {
+    __shared__ int s_skip;
+    const bool bad = __syncthreads_or(scan_share<true>(c.g, c.n));
+    if (threadIdx.x == 0) {
+        volatile int32_t *fi = c.found_inf;
+        if (bad) atomicOr(c.found_inf, 1);
+        __threadfence();
+        atomicAdd(c.found_inf, 2);
+        const long long t0 = clock64();
+        int32_t f;
+        int timed_out = 0;
+        while (((f = *fi) >> 1) < static_cast<int32_t>(gridDim.x)) {
+            if (clock64() - t0 > kBarrierLimitCycles) {
+                atomicOr(&g_master_timeout_flag, 1u);
+                timed_out = 1;
+                break;
+            }
+            __nanosleep(128);
+        }
+        __threadfence();
+        s_skip = timed_out | (f & 1);
+    }
+    __syncthreads();
+    float am = 0.0f;
+    if (!s_skip) {
+        const Opt opt = make_opt(a, __fdiv_rn(1.0f, *c.loss_scale));
+        am = update_share(opt, c.g, c.n, c.w8, *c.scale_w);
+    }
+    block_amax_atomic(am, c.amax_w);  // a skipped block adds +0: no change
+    if (threadIdx.x == 0) {
+        __threadfence();
+        const int32_t prev = atomicAdd(c.found_inf, 2);
+        if ((prev >> 1) == 2 * static_cast<int32_t>(gridDim.x) - 1) {
+            __threadfence();
+            const int found = prev & 1;
+            if (!found) x.clean_step();
+            loss_scale_update(c.loss_scale, c.growth, found, c.backoff, c.growth_factor, c.interval);
+            *c.found_inf = found;
+        }
+    }
+}
+
+// FP8MP_FUSED_MASTER=0 selects the three-launch version (read per call, so
+// tests can run both).
+bool fused_enabled() {
+    const char *v = std::getenv("FP8MP_FUSED_MASTER");
+    return !(v != nullptr && std::strcmp(v, "0") == 0);
+}
+
+struct FusedGrid {
+    int blocks_per_sm[2] = {0, 0};  // SGD, Adam
+};
+FusedGrid g_fused[64];
+
+template <class Opt, class Args, class Extra>
+int launch_step(const StepCommon &c, const Args &a, const Extra &x, int which, cudaStream_t s, const DeviceInfo &dev,
+                const char *fn) {
+    cudaError_t e = cudaMemsetAsync(c.found_inf, 0, sizeof(int32_t), s);
+    if (e != cudaSuccess) return fail(FP8MP_ERR_LAUNCH, "%s: memset failed: %s", fn, cudaGetErrorString(e));
+    const int64_t nvec = c.n >> 3;
+    int64_t blocks = (nvec + kThreads - 1) / kThreads;
+    if (blocks < 1) blocks = 1;
+    if (c.n > 0 && fused_enabled()) {
+        int &per_sm = g_fused[dev.device & 63].blocks_per_sm[which];
+        if (per_sm == 0) {
+            e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, fused_step_kernel<Opt, Args, Extra>, kThreads,
+                                                              0);
+            if (e != cudaSuccess || per_sm < 1)
+                return fail(FP8MP_ERR_LAUNCH, "%s: occupancy query failed: %s", fn, cudaGetErrorString(e));
+        }
+        const int64_t cap = static_cast<int64_t>(dev.num_sms) * per_sm;
+        if (blocks > cap) blocks = cap;
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(static_cast<unsigned>(blocks));
+        cfg.blockDim = dim3(kThreads);
+        cfg.stream = s;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeCooperative;
+        attr[0].val.cooperative = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        e = cudaLaunchKernelEx(&cfg, fused_step_kernel<Opt, Args, Extra>, c, a, x);
+        if (e != cudaSuccess) return fail(FP8MP_ERR_LAUNCH, "%s: launch failed: %s", fn, cudaGetErrorString(e));
+        return FP8MP_OK;
+    }
+    const int64_t cap = static_cast<int64_t>(dev.num_sms) * 8;
+    if (blocks > cap) blocks = cap;
+    if (c.n > 0) {
+        launch_kernel(grad_scan_kernel, dim3(static_cast<unsigned>(blocks)), dim3(kThreads), 0, s, c.g, c.n,
+                      c.found_inf);
+        launch_kernel(update_kernel<Opt, Args>, dim3(static_cast<unsigned>(blocks)), dim3(kThreads), 0, s, c, a);
+    }
+    launch_kernel(bookkeeping_kernel<Extra>, dim3(1), dim3(1), 0, s, c, x);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return fail(FP8MP_ERR_LAUNCH, "%s: launch failed: %s", fn, cudaGetErrorString(e));
+    return FP8MP_OK;
 }
 
 }  // namespace
@@ -237,47 +422,29 @@ int launch_adam_step(const uint16_t *g, int64_t n, float *w, float *m, float *v,
                      float *amax_w, float *loss_scale, int32_t *growth, int32_t *found_inf, float *beta_pows,
                      float lr, float b1, float b2, float eps, float backoff, float growth_factor,
                      int32_t growth_interval, cudaStream_t s, const DeviceInfo &dev) {
-    cudaError_t e = cudaMemsetAsync(found_inf, 0, sizeof(int32_t), s);
-    if (e != cudaSuccess)
-        return fail(FP8MP_ERR_LAUNCH, "mp_master_step_adam: memset failed: %s", cudaGetErrorString(e));
-    const int64_t nvec = n >> 3;
-    int64_t blocks = (nvec + kThreads - 1) / kThreads;
-    const int64_t cap = static_cast<int64_t>(dev.num_sms) * 8;
-    if (blocks > cap) blocks = cap;
-    if (blocks < 1) blocks = 1;
-    if (n > 0) {
-        launch_kernel(grad_scan_kernel, dim3(static_cast<unsigned>(blocks)), dim3(kThreads), 0, s, g, n, found_inf);
-        launch_kernel(adam_update_kernel, dim3(static_cast<unsigned>(blocks)), dim3(kThreads), 0, s, g, n, w, m, v,
-                      w8, scale_w, amax_w, loss_scale, found_inf, beta_pows, lr, b1, b2, eps);
-    }
-    launch_kernel(adam_bookkeeping_kernel, dim3(1), dim3(1), 0, s, loss_scale, growth, found_inf, beta_pows, b1, b2,
-                  backoff, growth_factor, growth_interval);
-    e = cudaGetLastError();
-    if (e != cudaSuccess)
-        return fail(FP8MP_ERR_LAUNCH, "mp_master_step_adam: launch failed: %s", cudaGetErrorString(e));
-    return FP8MP_OK;
+    const StepCommon c = {g, n, w8, scale_w, amax_w, loss_scale, growth, found_inf, backoff, growth_factor,
+                          growth_interval};
+    const AdamArgs a = {w, m, v, beta_pows, lr, b1, b2, eps};
+    const AdamExtra x = {beta_pows, b1, b2};
+    return launch_step<AdamOpt>(c, a, x, 1, s, dev, "mp_master_step_adam");
 }
 
 int launch_master_step(const uint16_t *g, int64_t n, float *w, float *v, uint8_t *w8, const float *scale_w,
                        float *amax_w, float *loss_scale, int32_t *growth, int32_t *found_inf, float lr, float mu,
                        float backoff, float growth_factor, int32_t growth_interval, cudaStream_t s,
                        const DeviceInfo &dev) {
-    cudaError_t e = cudaMemsetAsync(found_inf, 0, sizeof(int32_t), s);
-    if (e != cudaSuccess) return fail(FP8MP_ERR_LAUNCH, "mp_master_step: memset failed: %s", cudaGetErrorString(e));
-    const int64_t nvec = n >> 3;
-    int64_t blocks = (nvec + kThreads - 1) / kThreads;
-    const int64_t cap = static_cast<int64_t>(dev.num_sms) * 8;
-    if (blocks > cap) blocks = cap;
-    if (blocks < 1) blocks = 1;
-    if (n > 0) {
-        launch_kernel(grad_scan_kernel, dim3(static_cast<unsigned>(blocks)), dim3(kThreads), 0, s, g, n, found_inf);
-        launch_kernel(master_update_kernel, dim3(static_cast<unsigned>(blocks)), dim3(kThreads), 0, s, g, n, w, v, w8,
-                      scale_w, amax_w, loss_scale, found_inf, lr, mu);
-    }
-    launch_kernel(loss_scale_kernel, dim3(1), dim3(1), 0, s, loss_scale, growth, found_inf, backoff, growth_factor,
-                  growth_interval);
-    e = cudaGetLastError();
-    if (e != cudaSuccess) return fail(FP8MP_ERR_LAUNCH, "mp_master_step: launch failed: %s", cudaGetErrorString(e));
+    const StepCommon c = {g, n, w8, scale_w, amax_w, loss_scale, growth, found_inf, backoff, growth_factor,
+                          growth_interval};
+    const SgdArgs a = {w, v, lr, mu};
+    return launch_step<SgdOpt>(c, a, NoExtra{}, 0, s, dev, "mp_master_step");
+}
+
+int read_and_clear_master_timeout_flag(unsigned int *value) {
+    unsigned int v = 0, zero = 0;
+    cudaError_t e = cudaMemcpyFromSymbol(&v, g_master_timeout_flag, sizeof v);
+    if (e == cudaSuccess) e = cudaMemcpyToSymbol(g_master_timeout_flag, &zero, sizeof zero);
+    if (e != cudaSuccess) return fail(FP8MP_ERR_LAUNCH, "reading the timeout flag failed: %s", cudaGetErrorString(e));
+    *value = v;
     return FP8MP_OK;
 }
 

@@ -13,6 +13,15 @@ from gpu_util import assert_same_bits, np_view
 pytestmark = pytest.mark.gpu
 
 
+@pytest.fixture(params=["fused", "three_launches"])
+def path(request, monkeypatch):
+    """Runs a test on both versions of the step: one cooperative launch
+    (scan, grid barrier, update, last-block bookkeeping) and three launches
+    (the library reads FP8MP_FUSED_MASTER per call)."""
+    monkeypatch.setenv("FP8MP_FUSED_MASTER", "1" if request.param == "fused" else "0")
+    return request.param
+
+
 class DevState:
     def __init__(self, w, S, growth, device="cuda"):
         n = w.numel()
@@ -52,7 +61,7 @@ def host_state(w, S, growth, orc):
 
 
 @pytest.mark.parametrize("n", [0, 1, 7, 8, 9, 1000, 12345, (1 << 20) + 3])
-def test_ragged_sizes_with_skip_and_growth(cuda_lib, orc, n):
+def test_ragged_sizes_with_skip_and_growth(cuda_lib, orc, path, n):
     w = workloads.master_weights(n, seed=n)
     ds = DevState(w, 2.0 ** 16, 1997)
     hs = host_state(w, 2.0 ** 16, 1997, orc)
@@ -65,13 +74,14 @@ def test_ragged_sizes_with_skip_and_growth(cuda_lib, orc, n):
         assert hs["st"].growth[0] == 2
 
 
-def test_growth_interval_doubles_S(cuda_lib, orc):
+def test_growth_interval_doubles_S(cuda_lib, orc, path):
     n = 4096
     w = workloads.master_weights(n)
     ds = DevState(w, 8.0, 0)
     hs = host_state(w, 8.0, 0, orc)
     for step in range(7):
         g = workloads.master_step(n, step)
+        ds.found.fill_(12345)  # found_inf's content on entry does not matter
         step_both(cuda_lib, orc, ds, hs, g, 1e-3, 0.5, 1.0, interval=3)
         compare(ds, hs, f"step={step}")
     assert ds.S.item() == 32.0 and ds.growth.item() == 1
@@ -99,7 +109,7 @@ def test_1e9_parameters(cuda_lib, orc):
 
 
 @pytest.mark.parametrize("n", [0, 1, 9, 4096, (1 << 20) + 5])
-def test_adam_steps_bit_exact(cuda_lib, orc, n):
+def test_adam_steps_bit_exact(cuda_lib, orc, path, n):
     w = workloads.master_weights(n, seed=n + 1)
     ds = DevState(w, 2.0 ** 16, 0)
     m = torch.zeros(n, dtype=torch.float32, device="cuda")
