@@ -27,7 +27,7 @@ LIB_PATH = os.path.join(_HERE, "libfp8mp.so")
 EXPORTS = ("fp8_quantize", "fp8_quantize_current", "fp8_quantize_dbias",
            "fp8_quantize_dbias_workspace_bytes", "fp8_quantize_dbias_noalloc", "fp8_linear_fwd", "fp8_linear_fwd_fp8out", "fp8_linear_dgrad", "fp8_linear_wgrad",
            "fp8_linear_bwd", "fp8_linear_bwd_rowmajor", "delayed_scaling_update", "mp_master_step", "mp_master_step_adam", "fp8mp_check", "fp8mp_last_error",
-           "fp8mp_version", "fp8mp_selftest_timeout")
+           "fp8mp_version", "fp8mp_selftest_timeout", "fp8mp_selftest_barrier_timeout")
 
 _lib = None
 
@@ -80,12 +80,13 @@ def load(path: str | None = None):
     L.mp_master_step_adam.argtypes = [P, I64, P, P, P, P, P, P, P, P, P, P, F, F, F, F, F, F, I32, P]
     L.fp8mp_check.argtypes = [P]
     L.fp8mp_selftest_timeout.argtypes = [P]
+    L.fp8mp_selftest_barrier_timeout.argtypes = [P]
     L.fp8mp_last_error.restype = ctypes.c_char_p
     L.fp8mp_version.restype = I32
     for name in ("fp8_quantize", "fp8_quantize_current", "fp8_quantize_dbias", "fp8_quantize_dbias_noalloc",
                  "fp8_linear_fwd", "fp8_linear_fwd_fp8out", "fp8_linear_dgrad", "fp8_linear_wgrad",
                  "fp8_linear_bwd", "fp8_linear_bwd_rowmajor", "delayed_scaling_update", "mp_master_step", "mp_master_step_adam", "fp8mp_check",
-                 "fp8mp_selftest_timeout"):
+                 "fp8mp_selftest_timeout", "fp8mp_selftest_barrier_timeout"):
         getattr(L, name).restype = ctypes.c_int
     _lib = L
     return L
@@ -316,6 +317,12 @@ def fp8mp_selftest_timeout(stream=None) -> None:
     """Enqueues the kernel whose bounded wait runs out (about 2 s); the next
     fp8mp_check() on the stream then returns ERR_TIMEOUT."""
     _check(load().fp8mp_selftest_timeout(_stream(stream)))
+
+
+def fp8mp_selftest_barrier_timeout(stream=None) -> None:
+    """Enqueues the one-block kernel whose grid-barrier wait (the master
+    step's) runs out (about 2 s); the next fp8mp_check() returns ERR_TIMEOUT."""
+    _check(load().fp8mp_selftest_barrier_timeout(_stream(stream)))
 
 
 def fp8mp_version() -> int:

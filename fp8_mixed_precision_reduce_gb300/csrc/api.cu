@@ -489,6 +489,14 @@ int fp8mp_selftest_timeout(void *stream) {
     return launch_timeout_selftest(static_cast<cudaStream_t>(stream));
 }
 
+int fp8mp_selftest_barrier_timeout(void *stream) {
+    clear_error();
+    DeviceInfo dev;
+    const int rc = current_device(&dev);
+    if (rc) return rc;
+    return launch_barrier_selftest(static_cast<cudaStream_t>(stream));
+}
+
 int fp8mp_check(void *stream) {
     clear_error();
     cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));

@@ -102,6 +102,8 @@ int launch_adam_step(const uint16_t *g, int64_t n, float *w, float *m, float *v,
 int launch_timeout_selftest(cudaStream_t s);
 // Reads and clears the GEMM wait-timeout flag (after a stream sync).
 int read_and_clear_timeout_flag(unsigned int *value);
+// Enqueues the one-block kernel whose grid-barrier wait is meant to run out.
+int launch_barrier_selftest(cudaStream_t s);
 // Reads and clears the fused master step's barrier-timeout flag.
 int read_and_clear_master_timeout_flag(unsigned int *value);
 const char *last_error_message();

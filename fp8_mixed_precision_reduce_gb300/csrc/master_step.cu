@@ -83,6 +83,27 @@ __device__ __forceinline__ bool scan_share(const uint16_t *__restrict__ g, int64
     return bad;
 }
 
+// Thread 0 of a block: counts the block's arrival (adds 2 to *word: bit 0 is
+// left to the overflow flag) and waits, bounded by about 2 s, until the
+// arrivals reach `expected`. Returns the word's last value, or -1 when the
+// wait ran out (then the device timeout flag is set).
+__device__ int32_t barrier_arrive_and_wait(int32_t *word, int32_t expected) {
+    volatile int32_t *vw = word;
+    __threadfence();
+    atomicAdd(word, 2);
+    const long long t0 = clock64();
+    int32_t f;
+    while (((f = *vw) >> 1) < expected) {
+        if (clock64() - t0 > kBarrierLimitCycles) {
+            atomicOr(&g_master_timeout_flag, 1u);
+            return -1;
+        }
+        __nanosleep(128);
+    }
+    __threadfence();
+    return f;
+}
+
 // ---------------------------------------------------------- optimizers
 
 struct SgdArgs {
@@ -322,23 +343,9 @@ __global__ void __launch_bounds__(kThreads) fused_step_kernel(const StepCommon c
     __shared__ int s_skip;
     const bool bad = __syncthreads_or(scan_share<true>(c.g, c.n));
     if (threadIdx.x == 0) {
-        volatile int32_t *fi = c.found_inf;
         if (bad) atomicOr(c.found_inf, 1);
-        __threadfence();
-        atomicAdd(c.found_inf, 2);
-        const long long t0 = clock64();
-        int32_t f;
-        int timed_out = 0;
-        while (((f = *fi) >> 1) < static_cast<int32_t>(gridDim.x)) {
-            if (clock64() - t0 > kBarrierLimitCycles) {
-                atomicOr(&g_master_timeout_flag, 1u);
-                timed_out = 1;
-                break;
-            }
-            __nanosleep(128);
-        }
-        __threadfence();
-        s_skip = timed_out | (f & 1);
+        const int32_t f = barrier_arrive_and_wait(c.found_inf, static_cast<int32_t>(gridDim.x));
+        s_skip = f < 0 ? 1 : (f & 1);  // a timed-out barrier skips the update
     }
     __syncthreads();
     float am = 0.0f;
@@ -362,6 +369,17 @@ __global__ void __launch_bounds__(kThreads) fused_step_kernel(const StepCommon c
 
 // FP8MP_FUSED_MASTER=0 selects the three-launch version (read per call, so
 // tests can run both).
+// Diagnostic of the barrier's failure path: one block arrives at a barrier
+// that waits for two arrivals, so the bounded wait runs out after about 2 s,
+// raises the device flag and returns; the kernel ends normally.
+__device__ int32_t g_selftest_word = 0;
+__global__ void barrier_selftest_kernel() {
+    if (threadIdx.x == 0) {
+        g_selftest_word = 0;
+        barrier_arrive_and_wait(&g_selftest_word, 2);
+    }
+}
+
 bool fused_enabled() {
     const char *v = std::getenv("FP8MP_FUSED_MASTER");
     return !(v != nullptr && std::strcmp(v, "0") == 0);
@@ -437,6 +455,13 @@ int launch_master_step(const uint16_t *g, int64_t n, float *w, float *v, uint8_t
                           growth_interval};
     const SgdArgs a = {w, v, lr, mu};
     return launch_step<SgdOpt>(c, a, NoExtra{}, 0, s, dev, "mp_master_step");
+}
+
+int launch_barrier_selftest(cudaStream_t s) {
+    barrier_selftest_kernel<<<1, 32, 0, s>>>();
+    const cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return fail(FP8MP_ERR_LAUNCH, "self-test launch failed: %s", cudaGetErrorString(e));
+    return FP8MP_OK;
 }
 
 int read_and_clear_master_timeout_flag(unsigned int *value) {

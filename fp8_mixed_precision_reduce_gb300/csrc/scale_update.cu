@@ -44,6 +44,8 @@ __global__ void __launch_bounds__(kThreads) scale_update_kernel(const __grid_con
     const MetaArgs &m = b.m[blockIdx.x];
     const int L = m.len;
     const float cur = *m.cur_amax;
+    // the old scale, loaded with the rest so the final step waits on nothing
+    const float old_scale = threadIdx.x == 0 ? *m.scale : 0.0f;
     for (int j = threadIdx.x; j < L; j += blockDim.x) old_hist[j] = m.hist[j];
     __syncthreads();
     // roll by one, newest first, and take the max of the new window
@@ -61,7 +63,7 @@ __global__ void __launch_bounds__(kThreads) scale_update_kernel(const __grid_con
         float all = 0.0f;
         for (int w = 0; w < kThreads / 32; ++w) all = fmaxf(all, red[w]);
         const float a = (b.algo == FP8MP_AMAX_MAX) ? all : cur;
-        const float sc = scale_from_amax(a, *m.scale, m.fmt, b.margin);
+        const float sc = scale_from_amax(a, old_scale, m.fmt, b.margin);
         *m.scale = sc;
         *m.scale_inv = __fdiv_rn(1.0f, sc);
         *m.cur_amax = 0.0f;

@@ -373,8 +373,9 @@ int mp_master_step_adam(const uint16_t *grad_bf16, int64_t n, float *master, flo
 
 /*
  * fp8mp_check -- synchronises `stream`, then reports and clears the device
- * flag a GEMM kernel sets when one of its bounded waits runs out:
- * FP8MP_ERR_TIMEOUT if it was set, FP8MP_ERR_LAUNCH on a CUDA error, else 0.
+ * flags a kernel sets when one of its bounded waits runs out (a GEMM's
+ * mbarrier wait, the master step's grid barrier): FP8MP_ERR_TIMEOUT if one
+ * was set, FP8MP_ERR_LAUNCH on a CUDA error, else 0.
  */
 int fp8mp_check(void *stream);
 
@@ -388,6 +389,16 @@ int fp8mp_check(void *stream);
  * Returns 0 when enqueued.
  */
 int fp8mp_selftest_timeout(void *stream);
+
+/*
+ * fp8mp_selftest_barrier_timeout -- the same diagnostic for the grid barrier
+ * of mp_master_step / mp_master_step_adam (which run as one cooperative
+ * launch): a one-block kernel arrives at a barrier that waits for two
+ * arrivals; after about 2 s the wait gives up, raises the device flag and
+ * the kernel returns normally; the next fp8mp_check(stream) returns
+ * FP8MP_ERR_TIMEOUT. Returns 0 when enqueued.
+ */
+int fp8mp_selftest_barrier_timeout(void *stream);
 
 /* Thread-local description of the last nonzero return ("" if none). */
 const char *fp8mp_last_error(void);
