@@ -235,8 +235,9 @@ class LinearStep:
         self.md = fp8mp.Meta(HIST_LEN, E5)
         # the weight's first E4M3 copy (and its amax for the first update)
         fp8mp.fp8_quantize(self.master, E4, self.mw.scale, self.W8, None, self.mw.cur_amax)
-        # 2 casts, the fwd GEMM, the fused dgrad + wgrad GEMM, 1 scale update, 3 master-step kernels
-        self.launches_per_step = 8
+        # 2 casts, the fwd GEMM, the fused dgrad + wgrad GEMM, 1 scale update, and the master step:
+        # one cooperative kernel (after a 4-byte memset), or three kernels with FP8MP_FUSED_MASTER=0
+        self.launches_per_step = 6 if os.environ.get("FP8MP_FUSED_MASTER", "1") != "0" else 8
 
     def step(self, gemm_events=None, io=None):
         """One training step. `io` = (x, dy, y, dx) device buffers to use
