@@ -295,7 +295,13 @@ def capture_step_graphs(st, count):
     return plain.replay, (graphs, events)
 
 
-def run_e2e(st, steps, world):
+def run_e2e(st, steps, world, with_outputs=False):
+    """The step end to end through the Python API: each step's inputs x and
+    dY are copied in from pinned host memory, and the step's result comes
+    back to pinned host memory: the loss scaler's overflow flag and loss
+    scale (8 bytes), and with `with_outputs` also Y and dX (128 MiB).
+    Copies run on their own streams against two sets of device buffers, so
+    step i+1's upload and step i-1's download overlap step i's kernels."""
     import torch
 
     E = torch.cuda.Event
@@ -303,13 +309,15 @@ def run_e2e(st, steps, world):
     up, down = torch.cuda.Stream(), torch.cuda.Stream()
     x_h = st.x.cpu().pin_memory()
     dy_h = st.dy.cpu().pin_memory()
-    y_h = [torch.empty(st.y.shape, dtype=st.y.dtype).pin_memory() for _ in range(2)]
-    dx_h = [torch.empty(st.dx.shape, dtype=st.dx.dtype).pin_memory() for _ in range(2)]
+    res_h = [torch.empty(2, dtype=torch.int32).pin_memory() for _ in range(2)]
+    res_d = [torch.empty(2, dtype=torch.int32, device="cuda") for _ in range(2)]
+    y_h = [torch.empty(st.y.shape, dtype=st.y.dtype).pin_memory() for _ in range(2)] if with_outputs else None
+    dx_h = [torch.empty(st.dx.shape, dtype=st.dx.dtype).pin_memory() for _ in range(2)] if with_outputs else None
     bufs = [(st.x, st.dy, st.y, st.dx),
             (torch.empty_like(st.x), torch.empty_like(st.dy), torch.empty_like(st.y), torch.empty_like(st.dx))]
     uploaded = [E() for _ in range(2)]    # inputs of buffer set b are on the device
     computed = [E() for _ in range(2)]    # the step using buffer set b has finished
-    downloaded = [E() for _ in range(2)]  # outputs of buffer set b are on the host
+    downloaded = [E() for _ in range(2)]  # results of buffer set b are on the host
     torch.cuda.synchronize()
     barrier(world)
     t0, t1 = E(enable_timing=True), E(enable_timing=True)
@@ -325,13 +333,18 @@ def run_e2e(st, steps, world):
             uploaded[b].record(up)
         comp.wait_event(uploaded[b])
         if i >= 2:
-            comp.wait_event(downloaded[b])    # step i-2's outputs have left these buffers
+            comp.wait_event(downloaded[b])    # step i-2's results have left these buffers
         st.step(io=bufs[b])
+        # this step's loss-scaler state, before the next step changes it
+        res_d[b][0:1].copy_(st.found, non_blocking=True)
+        res_d[b][1:2].copy_(st.S.view(torch.int32), non_blocking=True)
         computed[b].record(comp)
         with torch.cuda.stream(down):
             down.wait_event(computed[b])
-            y_h[b].copy_(y, non_blocking=True)
-            dx_h[b].copy_(dx, non_blocking=True)
+            res_h[b].copy_(res_d[b], non_blocking=True)
+            if with_outputs:
+                y_h[b].copy_(y, non_blocking=True)
+                dx_h[b].copy_(dx, non_blocking=True)
             downloaded[b].record(down)
     comp.wait_stream(down)
     t1.record(comp)
@@ -339,7 +352,9 @@ def run_e2e(st, steps, world):
     barrier(world)
     ms = max_over_ranks(t0.elapsed_time(t1) / steps, world)
     h2d = x_h.numel() * x_h.element_size() + dy_h.numel() * dy_h.element_size()
-    d2h = y_h[0].numel() * y_h[0].element_size() + dx_h[0].numel() * dx_h[0].element_size()
+    d2h = res_h[0].numel() * res_h[0].element_size()
+    if with_outputs:
+        d2h += y_h[0].numel() * y_h[0].element_size() + dx_h[0].numel() * dx_h[0].element_size()
     return ms, h2d, d2h
 
 
@@ -409,10 +424,10 @@ def run_ours(args, world, rank, local):
     bwd_ms = statistics.mean(g[1] for g in gemm_ms)
 
     # end to end through the public API: every step copies its x and dY in
-    # from pinned host memory and its y and dX back out. Copies run on their
-    # own streams against double-buffered device tensors, so step i+1's
-    # inputs upload and step i-1's outputs download while step i computes.
+    # from pinned host memory and reads its result (the loss scaler's state)
+    # back; the second run also reads back the outputs Y and dX.
     e2e_ms, h2d, d2h = run_e2e(st, max(10, args.steps), world)
+    e2e_out_ms, h2d_out, d2h_out = run_e2e(st, max(10, args.steps), world, with_outputs=True)
     fl = flops_per_step()
     value = world * fl / (ms_per_step * 1e-3) / 1e12
     fp8_peak = float(peaks["bf16_tflops"]) * FP8_OVER_BF16
@@ -449,7 +464,12 @@ def run_ours(args, world, rank, local):
                      "peak_source": f"{peak_kind} bf16 burst x {FP8_OVER_BF16:g} (nominal fp8/bf16 dense ratio)"},
         "e2e": {"value": round(world * fl / (e2e_ms * 1e-3) / 1e12, 2), "unit": "TFLOP/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 5),
+                "result_read_back": "overflow flag and loss scale (the loss scaler's state)",
                 "copies": "pinned host, own H2D/D2H streams, double-buffered device tensors"},
+        "e2e_with_outputs": {"value": round(world * fl / (e2e_out_ms * 1e-3) / 1e12, 2), "unit": "TFLOP/s",
+                             "h2d_bytes_per_step": h2d_out, "d2h_bytes_per_step": d2h_out,
+                             "ms_per_step": round(e2e_out_ms, 5),
+                             "result_read_back": "the above plus the outputs Y and dX (bf16)"},
         "gpu_launches": st.launches_per_step * args.steps,  # the step-time pass; the GEMM-timing pass repeats it
         "clocks": {"sm_mhz": clk["sm_mhz"], "sm_max_mhz": clk["sm_max_mhz"], "reasons": clk["reasons"]},
     }
