@@ -9,9 +9,12 @@ through the library's entry points on one CUDA stream:
   fp8_linear_fwd(X8, W8 -> Y bf16, amax_y)       W8: the weight's E4M3 copy
   fp8_quantize(dY -> dY8, amax)                  E5M2, row-major only
   fp8_linear_bwd_rowmajor(dY8, W8, X8            dgrad and wgrad GEMMs in one
-                          -> dX bf16, dW bf16)   launch, no transposed copies
+                          -> dX bf16, dW bf16)   launch, no transposed copies;
+                                                 the wgrad epilogue flags an
+                                                 Inf/NaN in the stored dW
   delayed_scaling_update(x, w, y, dy metas)      L = 1024, most_recent
-  mp_master_step(dW -> master, momentum, W8)     SGD-momentum, loss scale 2^16;
+  mp_master_step(dW -> master, momentum, W8)     SGD-momentum, loss scale 2^16,
+                                                 skip decided by that flag;
                                                  re-casts W8 under the updated
                                                  weight scale for the next step
 The weight's first E4M3 copy is cast once before the first step; from then
@@ -205,7 +208,7 @@ def max_over_ranks(value: float, world: int) -> float:
 class LinearStep:
     """Device state and the step of the proj linear, through the library."""
 
-    def __init__(self, m=M_TOK, k=K_IN, n=N_OUT, seed=3):
+    def __init__(self, m=M_TOK, k=K_IN, n=N_OUT, seed=3, prescanned=True):
         import torch
 
         import fp8_mixed_precision_reduce_gb300 as fp8mp
@@ -230,14 +233,18 @@ class LinearStep:
         self.S = torch.tensor([S0], dtype=torch.float32, device=dev)
         self.growth = torch.zeros(1, dtype=torch.int32, device=dev)
         self.found = torch.zeros(1, dtype=torch.int32, device=dev)
+        # dW's overflow flag: set by the wgrad epilogue, read and reset by the
+        # master step (with prescanned=False the master step scans dW itself)
+        self.prescanned = prescanned
+        self.gnf = torch.zeros(1, dtype=torch.int32, device=dev)
         E4, E5 = fp8mp.E4M3, fp8mp.E5M2
         self.mx, self.mw, self.my = (fp8mp.Meta(HIST_LEN, E4) for _ in range(3))
         self.md = fp8mp.Meta(HIST_LEN, E5)
         # the weight's first E4M3 copy (and its amax for the first update)
         fp8mp.fp8_quantize(self.master, E4, self.mw.scale, self.W8, None, self.mw.cur_amax)
-        # 2 casts, the fwd GEMM, the fused dgrad + wgrad GEMM, 1 scale update, and the master step:
-        # one cooperative kernel (after a 4-byte memset), or three kernels with FP8MP_FUSED_MASTER=0
-        self.launches_per_step = 6 if os.environ.get("FP8MP_FUSED_MASTER", "1") != "0" else 8
+        # 2 casts, the fwd GEMM, the fused dgrad + wgrad GEMM, 1 scale update, and the master step: one
+        # kernel after a 4-byte memset (three kernels when it scans dW itself with FP8MP_FUSED_MASTER=0)
+        self.launches_per_step = 6 if prescanned or os.environ.get("FP8MP_FUSED_MASTER", "1") != "0" else 8
 
     def step(self, gemm_events=None, io=None):
         """One training step. `io` = (x, dy, y, dx) device buffers to use
@@ -255,12 +262,13 @@ class LinearStep:
         if ev is not None:
             ev[2].record()
         f.fp8_linear_bwd_rowmajor(self.D8, self.W8, self.X8, self.md.scale_inv, self.mw.scale_inv,
-                                  self.mx.scale_inv, dx, self.dw)
+                                  self.mx.scale_inv, dx, self.dw,
+                                  dw_nonfinite=self.gnf if self.prescanned else None)
         if ev is not None:
             ev[3].record()
         f.delayed_scaling_update([self.mx, self.mw, self.my, self.md], f.AMAX_MOST_RECENT, 0)
         f.mp_master_step(self.dw, self.master, self.mom, self.W8, self.mw.scale, self.mw.cur_amax, self.S,
-                         self.growth, self.found, LR, MU)
+                         self.growth, self.found, LR, MU, grad_nonfinite=self.gnf if self.prescanned else None)
 
 
 def capture_step_graphs(st, count):
@@ -362,7 +370,7 @@ def run_ours(args, world, rank, local):
     import torch
 
     peaks, peak_kind = load_peaks()
-    st = LinearStep()
+    st = LinearStep(prescanned=not args.master_scans_dw)
     torch.cuda.synchronize()
     flush = torch.empty(int(2 * 129e6 // 4) + 1, dtype=torch.float32, device="cuda")  # > 2x L2
 
@@ -451,7 +459,9 @@ def run_ours(args, world, rank, local):
         "data": "synthetic (seeded; shapes and distributions of the transformer proj workload)",
         "config": {"workload": WORKLOAD, "M": M_TOK, "K": K_IN, "N": N_OUT, "history_len": HIST_LEN,
                    "amax_compute_algo": "most_recent", "recipe": "HYBRID", "parallelism": f"replicas x{world}",
-                   "l2": "flushed (2x L2 write) between timed steps", "launch": launch},
+                   "l2": "flushed (2x L2 write) between timed steps", "launch": launch,
+                   "overflow_check": "master step scans dW" if args.master_scans_dw
+                   else "wgrad epilogue flags Inf/NaN in the stored dW; the master step reads the flag"},
         "gemm_only": {"tflops": round(world * fl / (gemm_step_ms * 1e-3) / 1e12, 2), "ms_per_step": round(gemm_step_ms, 5),
                       "fwd_ms": round(fwd_ms, 5), "bwd_ms": round(bwd_ms, 5),
                       "from": "a second pass of K steps with timing events around the GEMM launches",
@@ -607,6 +617,8 @@ def main(argv=None):
     ap.add_argument("--baseline-tokens", type=int, default=4096,
                     help="tokens of the oracle sample timed as cpu_baseline (about 10-30 s)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--master-scans-dw", action="store_true",
+                    help="the master step scans dW for Inf/NaN itself instead of reading the wgrad epilogue's flag")
     ap.add_argument("--eager", action="store_true",
                     help="launch every library call from Python in the timed steps instead of replaying graphs")
     args = ap.parse_args(argv)

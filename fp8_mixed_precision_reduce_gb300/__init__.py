@@ -26,7 +26,8 @@ _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "libfp8mp.so")
 EXPORTS = ("fp8_quantize", "fp8_quantize_current", "fp8_quantize_dbias",
            "fp8_quantize_dbias_workspace_bytes", "fp8_quantize_dbias_noalloc", "fp8_linear_fwd", "fp8_linear_fwd_fp8out", "fp8_linear_dgrad", "fp8_linear_wgrad",
-           "fp8_linear_bwd", "fp8_linear_bwd_rowmajor", "delayed_scaling_update", "mp_master_step", "mp_master_step_adam", "fp8mp_check", "fp8mp_last_error",
+           "fp8_linear_bwd", "fp8_linear_bwd_rowmajor", "delayed_scaling_update", "mp_master_step", "mp_master_step_adam", "mp_master_step_prescanned",
+           "mp_master_step_adam_prescanned", "fp8mp_check", "fp8mp_last_error",
            "fp8mp_version", "fp8mp_selftest_timeout", "fp8mp_selftest_barrier_timeout")
 
 _lib = None
@@ -74,10 +75,12 @@ def load(path: str | None = None):
     L.fp8_linear_dgrad.argtypes = [P, P, I64, I64, I64, I32, P, P, P, I32, P]
     L.fp8_linear_wgrad.argtypes = [P, P, I64, I64, I64, I32, P, P, P, I32, P]
     L.fp8_linear_bwd.argtypes = [P, P, P, P, I64, I64, I64, I32, P, P, P, P, I32, P, I32, P]
-    L.fp8_linear_bwd_rowmajor.argtypes = [P, P, P, I64, I64, I64, I32, P, P, P, P, I32, P, I32, P]
+    L.fp8_linear_bwd_rowmajor.argtypes = [P, P, P, I64, I64, I64, I32, P, P, P, P, I32, P, I32, P, P]
     L.delayed_scaling_update.argtypes = [ctypes.POINTER(fp8mp_meta), I32, I32, I32, P]
     L.mp_master_step.argtypes = [P, I64, P, P, P, P, P, P, P, P, F, F, F, F, I32, P]
     L.mp_master_step_adam.argtypes = [P, I64, P, P, P, P, P, P, P, P, P, P, F, F, F, F, F, F, I32, P]
+    L.mp_master_step_prescanned.argtypes = [P, I64, P, P, P, P, P, P, P, P, P, F, F, F, F, I32, P]
+    L.mp_master_step_adam_prescanned.argtypes = [P, I64, P, P, P, P, P, P, P, P, P, P, P, F, F, F, F, F, F, I32, P]
     L.fp8mp_check.argtypes = [P]
     L.fp8mp_selftest_timeout.argtypes = [P]
     L.fp8mp_selftest_barrier_timeout.argtypes = [P]
@@ -85,7 +88,8 @@ def load(path: str | None = None):
     L.fp8mp_version.restype = I32
     for name in ("fp8_quantize", "fp8_quantize_current", "fp8_quantize_dbias", "fp8_quantize_dbias_noalloc",
                  "fp8_linear_fwd", "fp8_linear_fwd_fp8out", "fp8_linear_dgrad", "fp8_linear_wgrad",
-                 "fp8_linear_bwd", "fp8_linear_bwd_rowmajor", "delayed_scaling_update", "mp_master_step", "mp_master_step_adam", "fp8mp_check",
+                 "fp8_linear_bwd", "fp8_linear_bwd_rowmajor", "delayed_scaling_update", "mp_master_step", "mp_master_step_adam",
+                 "mp_master_step_prescanned", "mp_master_step_adam_prescanned", "fp8mp_check",
                  "fp8mp_selftest_timeout", "fp8mp_selftest_barrier_timeout"):
         getattr(L, name).restype = ctypes.c_int
     _lib = L
@@ -244,16 +248,18 @@ def fp8_linear_bwd(dy8: torch.Tensor, dy8t: torch.Tensor, w8t: torch.Tensor, x8t
 def fp8_linear_bwd_rowmajor(dy8: torch.Tensor, w8: torch.Tensor | None, x8: torch.Tensor | None,
                             sinv_dy: torch.Tensor, sinv_w: torch.Tensor | None, sinv_x: torch.Tensor | None,
                             dx: torch.Tensor | None, dw: torch.Tensor | None, dy_fmt: int = E5M2,
-                            stream=None) -> None:
+                            dw_nonfinite: torch.Tensor | None = None, stream=None) -> None:
     """Both backward GEMMs from the forward's row-major FP8 copies, one launch:
     dx[M, K] = (dy8 . w8) * sinv_dy * sinv_w, dw[N, K] = (dy8^T . x8) * sinv_dy * sinv_x.
-    dx or dw may be None to skip that gradient."""
+    dx or dw may be None to skip that gradient. dw_nonfinite (int32[1] on the
+    device) gets 1 OR-ed in when a stored element of dw is Inf or NaN."""
     M, N = dy8.shape
     K = (w8 if w8 is not None else x8).shape[1]
     _check(load().fp8_linear_bwd_rowmajor(_ptr(dy8), _ptr(w8), _ptr(x8), M, N, K, dy_fmt, _ptr(sinv_dy),
                                           _ptr(sinv_w), _ptr(sinv_x), _ptr(dx),
                                           _dtype_code(dx) if dx is not None else F32, _ptr(dw),
-                                          _dtype_code(dw) if dw is not None else F32, _stream(stream)))
+                                          _dtype_code(dw) if dw is not None else F32, _ptr(dw_nonfinite),
+                                          _stream(stream)))
 
 
 class Meta:
@@ -284,9 +290,19 @@ def mp_master_step(grad_bf16: torch.Tensor, master: torch.Tensor, momentum: torc
                    w8: torch.Tensor, scale_w: torch.Tensor, amax_w: torch.Tensor,
                    loss_scale: torch.Tensor, growth_tracker: torch.Tensor, found_inf: torch.Tensor,
                    lr: float, momentum_coef: float, backoff: float = 0.5, growth_factor: float = 2.0,
-                   growth_interval: int = 2000, stream=None) -> None:
-    """Unscale, overflow skip, FP32 SGD-momentum update and E4M3 re-cast, in place."""
+                   growth_interval: int = 2000, stream=None, grad_nonfinite: torch.Tensor | None = None) -> None:
+    """Unscale, overflow skip, FP32 SGD-momentum update and E4M3 re-cast, in place.
+    With grad_nonfinite (int32[1] on the device, set by the gradients' producer,
+    e.g. fp8_linear_bwd_rowmajor's dw_nonfinite) the step reads that flag
+    instead of scanning the gradients, and resets it to 0."""
     n = grad_bf16.numel()
+    if grad_nonfinite is not None:
+        _check(load().mp_master_step_prescanned(_ptr(grad_bf16), n, _ptr(master), _ptr(momentum), _ptr(w8),
+                                                _ptr(scale_w), _ptr(amax_w), _ptr(loss_scale), _ptr(growth_tracker),
+                                                _ptr(found_inf), _ptr(grad_nonfinite), float(lr),
+                                                float(momentum_coef), float(backoff), float(growth_factor),
+                                                int(growth_interval), _stream(stream)))
+        return
     _check(load().mp_master_step(_ptr(grad_bf16), n, _ptr(master), _ptr(momentum), _ptr(w8),
                                  _ptr(scale_w), _ptr(amax_w), _ptr(loss_scale), _ptr(growth_tracker),
                                  _ptr(found_inf), float(lr), float(momentum_coef), float(backoff),
@@ -298,9 +314,17 @@ def mp_master_step_adam(grad_bf16: torch.Tensor, master: torch.Tensor, exp_avg: 
                         loss_scale: torch.Tensor, growth_tracker: torch.Tensor, found_inf: torch.Tensor,
                         beta_pows: torch.Tensor, lr: float, beta1: float = 0.9, beta2: float = 0.999,
                         eps: float = 1e-8, backoff: float = 0.5, growth_factor: float = 2.0,
-                        growth_interval: int = 2000, stream=None) -> None:
-    """Unscale, overflow skip, FP32 Adam update and E4M3 re-cast, in place."""
+                        growth_interval: int = 2000, stream=None, grad_nonfinite: torch.Tensor | None = None) -> None:
+    """Unscale, overflow skip, FP32 Adam update and E4M3 re-cast, in place
+    (grad_nonfinite: as mp_master_step)."""
     n = grad_bf16.numel()
+    if grad_nonfinite is not None:
+        _check(load().mp_master_step_adam_prescanned(
+            _ptr(grad_bf16), n, _ptr(master), _ptr(exp_avg), _ptr(exp_avg_sq), _ptr(w8), _ptr(scale_w),
+            _ptr(amax_w), _ptr(loss_scale), _ptr(growth_tracker), _ptr(found_inf), _ptr(grad_nonfinite),
+            _ptr(beta_pows), float(lr), float(beta1), float(beta2), float(eps), float(backoff), float(growth_factor),
+            int(growth_interval), _stream(stream)))
+        return
     _check(load().mp_master_step_adam(_ptr(grad_bf16), n, _ptr(master), _ptr(exp_avg), _ptr(exp_avg_sq), _ptr(w8),
                                       _ptr(scale_w), _ptr(amax_w), _ptr(loss_scale), _ptr(growth_tracker),
                                       _ptr(found_inf), _ptr(beta_pows), float(lr), float(beta1), float(beta2),

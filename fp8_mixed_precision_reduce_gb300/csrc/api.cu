@@ -364,7 +364,7 @@ int fp8_linear_bwd(const uint8_t *dy8, const uint8_t *dy8t, const uint8_t *w8t, 
 int fp8_linear_bwd_rowmajor(const uint8_t *dy8, const uint8_t *w8, const uint8_t *x8, int64_t M, int64_t N,
                             int64_t K, int32_t dy_fmt, const float *sinv_dy, const float *sinv_w,
                             const float *sinv_x, void *dx, int32_t dx_dtype, void *dw, int32_t dw_dtype,
-                            void *stream) {
+                            int32_t *dw_nonfinite, void *stream) {
     const char *fn = "fp8_linear_bwd_rowmajor";
     clear_error();
     int rc = check_gemm_dims(fn, M, N, K);
@@ -380,6 +380,7 @@ int fp8_linear_bwd_rowmajor(const uint8_t *dy8, const uint8_t *w8, const uint8_t
     CHECK_SCALAR(sinv_dy, true);
     if (want_dx) CHECK_SCALAR(sinv_w, true);
     if (want_dw) CHECK_SCALAR(sinv_x, true);
+    CHECK_SCALAR(dw_nonfinite, false);
     if (M > 0 && N > 0) {
         CHECK_PTR(dy8, true);
         if (want_dx) CHECK_PTR(w8, true);
@@ -403,7 +404,7 @@ int fp8_linear_bwd_rowmajor(const uint8_t *dy8, const uint8_t *w8, const uint8_t
     // wgrad: A = dY8 [M x N] read MN-major (rows_a = N, kc = M), B = X8 [M x K] read MN-major
     if (want_dw)
         d[n++] = {dy8, dy_fmt, x8, FP8MP_E4M3, N, K, M, sinv_dy, sinv_x, nullptr, FP8MP_F32, dw, dw_dtype, nullptr,
-                  nullptr, FP8MP_E4M3, 1, 1};
+                  nullptr, FP8MP_E4M3, 1, 1, dw_nonfinite};
     return launch_gemms(d, n, static_cast<cudaStream_t>(stream), dev);
 }
 
@@ -428,11 +429,11 @@ int delayed_scaling_update(const fp8mp_meta *metas, int32_t n, int32_t algo, int
     return launch_scale_update(metas, n, algo, margin, static_cast<cudaStream_t>(stream));
 }
 
-int mp_master_step(const uint16_t *grad_bf16, int64_t n, float *master, float *momentum, uint8_t *w8,
-                   const float *scale_w, float *amax_w, float *loss_scale, int32_t *growth_tracker,
-                   int32_t *found_inf, float lr, float momentum_coef, float backoff, float growth_factor,
-                   int32_t growth_interval, void *stream) {
-    const char *fn = "mp_master_step";
+static int master_step_entry(const char *fn, const uint16_t *grad_bf16, int64_t n, float *master,
+                             float *momentum, uint8_t *w8, const float *scale_w, float *amax_w, float *loss_scale,
+                             int32_t *growth_tracker, int32_t *found_inf, int32_t *grad_nonfinite, bool prescanned,
+                             float lr, float momentum_coef, float backoff, float growth_factor,
+                             int32_t growth_interval, void *stream) {
     clear_error();
     REQUIRE(n >= 0 && n <= (1ll << 40), "%s: n = %lld out of range", fn, (long long)n);
     REQUIRE(growth_interval >= 1, "%s: growth_interval must be >= 1", fn);
@@ -445,19 +446,39 @@ int mp_master_step(const uint16_t *grad_bf16, int64_t n, float *master, float *m
     CHECK_SCALAR(loss_scale, true);
     CHECK_SCALAR(growth_tracker, true);
     CHECK_SCALAR(found_inf, true);
+    CHECK_SCALAR(grad_nonfinite, prescanned);
+    REQUIRE(grad_nonfinite != found_inf, "%s: grad_nonfinite and found_inf must be different words", fn);
     DeviceInfo dev;
     const int rc = current_device(&dev);
     if (rc) return rc;
     return launch_master_step(grad_bf16, n, master, momentum, w8, scale_w, amax_w, loss_scale, growth_tracker,
                               found_inf, lr, momentum_coef, backoff, growth_factor, growth_interval,
-                              static_cast<cudaStream_t>(stream), dev);
+                              static_cast<cudaStream_t>(stream), dev, grad_nonfinite);
 }
 
-int mp_master_step_adam(const uint16_t *grad_bf16, int64_t n, float *master, float *exp_avg, float *exp_avg_sq,
-                        uint8_t *w8, const float *scale_w, float *amax_w, float *loss_scale, int32_t *growth_tracker,
-                        int32_t *found_inf, float *beta_pows, float lr, float beta1, float beta2, float eps,
-                        float backoff, float growth_factor, int32_t growth_interval, void *stream) {
-    const char *fn = "mp_master_step_adam";
+int mp_master_step(const uint16_t *grad_bf16, int64_t n, float *master, float *momentum, uint8_t *w8,
+                   const float *scale_w, float *amax_w, float *loss_scale, int32_t *growth_tracker,
+                   int32_t *found_inf, float lr, float momentum_coef, float backoff, float growth_factor,
+                   int32_t growth_interval, void *stream) {
+    return master_step_entry("mp_master_step", grad_bf16, n, master, momentum, w8, scale_w, amax_w, loss_scale,
+                             growth_tracker, found_inf, nullptr, false, lr, momentum_coef, backoff, growth_factor,
+                             growth_interval, stream);
+}
+
+int mp_master_step_prescanned(const uint16_t *grad_bf16, int64_t n, float *master, float *momentum, uint8_t *w8,
+                              const float *scale_w, float *amax_w, float *loss_scale, int32_t *growth_tracker,
+                              int32_t *found_inf, int32_t *grad_nonfinite, float lr, float momentum_coef,
+                              float backoff, float growth_factor, int32_t growth_interval, void *stream) {
+    return master_step_entry("mp_master_step_prescanned", grad_bf16, n, master, momentum, w8, scale_w, amax_w,
+                             loss_scale, growth_tracker, found_inf, grad_nonfinite, true, lr, momentum_coef, backoff,
+                             growth_factor, growth_interval, stream);
+}
+
+static int adam_step_entry(const char *fn, const uint16_t *grad_bf16, int64_t n, float *master, float *exp_avg,
+                           float *exp_avg_sq, uint8_t *w8, const float *scale_w, float *amax_w, float *loss_scale,
+                           int32_t *growth_tracker, int32_t *found_inf, int32_t *grad_nonfinite, bool prescanned,
+                           float *beta_pows, float lr, float beta1, float beta2, float eps, float backoff,
+                           float growth_factor, int32_t growth_interval, void *stream) {
     clear_error();
     REQUIRE(n >= 0 && n <= (1ll << 40), "%s: n = %lld out of range", fn, (long long)n);
     REQUIRE(growth_interval >= 1, "%s: growth_interval must be >= 1", fn);
@@ -473,12 +494,34 @@ int mp_master_step_adam(const uint16_t *grad_bf16, int64_t n, float *master, flo
     CHECK_SCALAR(growth_tracker, true);
     CHECK_SCALAR(found_inf, true);
     CHECK_SCALAR(beta_pows, true);
+    CHECK_SCALAR(grad_nonfinite, prescanned);
+    REQUIRE(grad_nonfinite != found_inf, "%s: grad_nonfinite and found_inf must be different words", fn);
     DeviceInfo dev;
     const int rc = current_device(&dev);
     if (rc) return rc;
     return launch_adam_step(grad_bf16, n, master, exp_avg, exp_avg_sq, w8, scale_w, amax_w, loss_scale,
                             growth_tracker, found_inf, beta_pows, lr, beta1, beta2, eps, backoff, growth_factor,
-                            growth_interval, static_cast<cudaStream_t>(stream), dev);
+                            growth_interval, static_cast<cudaStream_t>(stream), dev, grad_nonfinite);
+}
+
+int mp_master_step_adam(const uint16_t *grad_bf16, int64_t n, float *master, float *exp_avg, float *exp_avg_sq,
+                        uint8_t *w8, const float *scale_w, float *amax_w, float *loss_scale, int32_t *growth_tracker,
+                        int32_t *found_inf, float *beta_pows, float lr, float beta1, float beta2, float eps,
+                        float backoff, float growth_factor, int32_t growth_interval, void *stream) {
+    return adam_step_entry("mp_master_step_adam", grad_bf16, n, master, exp_avg, exp_avg_sq, w8, scale_w, amax_w,
+                           loss_scale, growth_tracker, found_inf, nullptr, false, beta_pows, lr, beta1, beta2, eps,
+                           backoff, growth_factor, growth_interval, stream);
+}
+
+int mp_master_step_adam_prescanned(const uint16_t *grad_bf16, int64_t n, float *master, float *exp_avg,
+                                   float *exp_avg_sq, uint8_t *w8, const float *scale_w, float *amax_w,
+                                   float *loss_scale, int32_t *growth_tracker, int32_t *found_inf,
+                                   int32_t *grad_nonfinite, float *beta_pows, float lr, float beta1, float beta2,
+                                   float eps, float backoff, float growth_factor, int32_t growth_interval,
+                                   void *stream) {
+    return adam_step_entry("mp_master_step_adam_prescanned", grad_bf16, n, master, exp_avg, exp_avg_sq, w8, scale_w,
+                           amax_w, loss_scale, growth_tracker, found_inf, grad_nonfinite, true, beta_pows, lr, beta1,
+                           beta2, eps, backoff, growth_factor, growth_interval, stream);
 }
 
 int fp8mp_selftest_timeout(void *stream) {

@@ -80,6 +80,7 @@ struct GemmDesc {
     const float *out_scale;  // non-null: FP8 output of out_fmt under *out_scale
     int out_fmt;
     int a_mn, b_mn;
+    int32_t *out_nonfinite;  // non-null (bf16 / fp32 output): |= 1 when a stored element is Inf or NaN
 };
 // Runs 1 or 2 independent GEMMs in one persistent launch.
 int launch_gemms(const GemmDesc *descs, int n, cudaStream_t s, const DeviceInfo &dev);
@@ -93,11 +94,13 @@ int launch_scale_update(const fp8mp_meta *metas, int32_t n, int32_t algo, int32_
 int launch_master_step(const uint16_t *g, int64_t n, float *w, float *v, uint8_t *w8,
                        const float *scale_w, float *amax_w, float *loss_scale, int32_t *growth,
                        int32_t *found_inf, float lr, float mu, float backoff, float growth_factor,
-                       int32_t growth_interval, cudaStream_t s, const DeviceInfo &dev);
+                       int32_t growth_interval, cudaStream_t s, const DeviceInfo &dev,
+                       int32_t *grad_nonfinite = nullptr);
 int launch_adam_step(const uint16_t *g, int64_t n, float *w, float *m, float *v, uint8_t *w8, const float *scale_w,
                      float *amax_w, float *loss_scale, int32_t *growth, int32_t *found_inf, float *beta_pows,
                      float lr, float b1, float b2, float eps, float backoff, float growth_factor,
-                     int32_t growth_interval, cudaStream_t s, const DeviceInfo &dev);
+                     int32_t growth_interval, cudaStream_t s, const DeviceInfo &dev,
+                     int32_t *grad_nonfinite = nullptr);
 // Enqueues the one-thread kernel whose bounded wait is meant to run out.
 int launch_timeout_selftest(cudaStream_t s);
 // Reads and clears the GEMM wait-timeout flag (after a stream sync).

@@ -112,6 +112,7 @@ struct GemmParams {
     int out_fmt;
     const float *out_scale;
     float *out_amax;
+    int32_t *out_nonfinite;   // bf16 / fp32 output: |= 1 when a stored element is Inf or NaN
 };
 
 // One GEMM of a launch: its operand and output tensor maps and parameters.
@@ -388,6 +389,12 @@ __device__ __forceinline__ void tile_coords(int t, int tiles_m, int tiles_n, int
     nb = local / gm;
 }
 
+// A bf16 pair with an all-ones exponent field in either half (Inf or NaN).
+__device__ __forceinline__ bool has_nonfinite_bf16x2(uint32_t w) {
+    const uint32_t t = (w & 0x7F807F80u) ^ 0x7F807F80u;
+    return (t & 0xFFFFu) == 0u || (t >> 16) == 0u;
+}
+
 __device__ __forceinline__ uint32_t pack_bf16x2(float a, float b) {
     const __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
     return *reinterpret_cast<const uint32_t *>(&h);
@@ -578,6 +585,7 @@ gemm_fp8_kernel(const __grid_constant__ GemmBatch batch) {
         const int row_in_tile = static_cast<int>(rank) * ROWS_A + q * 32 + lane;
         const uint32_t stage_box = base + C::EPI_OFFSET + static_cast<uint32_t>((warp - 2) * 2 * C::EPI_BOX_BYTES);
         float am0 = 0.0f, am1 = 0.0f;  // max |y| of problem 0 / 1
+        bool bad0 = false, bad1 = false;  // a stored element of problem 0 / 1 is Inf or NaN
         int lt = 0;
         uint32_t chunk_no = 0;
         for (int r = 0; r < rounds; ++r) {
@@ -607,7 +615,9 @@ gemm_fp8_kernel(const __grid_constant__ GemmBatch batch) {
             const int64_t m = static_cast<int64_t>(mb) * C::TILE_M + row_in_tile;
             const bool row_ok = m < rows_a;
             const int warp_row0 = mb * C::TILE_M + static_cast<int>(rank) * ROWS_A + q * 32;
+            const bool scan_out = P.p.out_nonfinite != nullptr && !out_fp8 && row_ok;
             float am = 0.0f;
+            bool bad = false;
 #pragma unroll 1
             for (int c = 0; c < TILE_N; c += box_cols, ++chunk_no) {
                 uint32_t packed[32];  // this lane's 128-byte row of the box
@@ -670,6 +680,17 @@ gemm_fp8_kernel(const __grid_constant__ GemmBatch batch) {
                         }
                     }
                 }
+                // the overflow check of the values as stored (rows past the output
+                // are skipped; columns past it hold zeros from the zero-filled operand)
+                if (scan_out) {
+                    if (out_bf16) {
+#pragma unroll
+                        for (int j = 0; j < 32; ++j) bad |= has_nonfinite_bf16x2(packed[j]);
+                    } else {
+#pragma unroll
+                        for (int j = 0; j < 32; ++j) bad |= (packed[j] & 0x7F800000u) == 0x7F800000u;
+                    }
+                }
                 // the staging box written two chunks ago must have been read by its TMA store
                 const uint32_t box = stage_box + (chunk_no & 1u) * C::EPI_BOX_BYTES;
                 if (lane == 0 && chunk_no >= 2) bulk_wait_read_le1();
@@ -687,10 +708,13 @@ gemm_fp8_kernel(const __grid_constant__ GemmBatch batch) {
                     bulk_commit_group();
                 }
             }
-            if (pi == 0)
+            if (pi == 0) {
                 am0 = max_ignore_nan(am0, am);
-            else
+                bad0 |= bad;
+            } else {
                 am1 = max_ignore_nan(am1, am);
+                bad1 |= bad;
+            }
             tc_fence_before();
             __syncwarp();
             if (lane == 0) {
@@ -703,6 +727,8 @@ gemm_fp8_kernel(const __grid_constant__ GemmBatch batch) {
         if (lane == 0) bulk_wait_all();  // stores done before the CTA's shared memory goes away
         for (int i = 0; i < batch.nprob; ++i) {
             const GemmParams &pp = batch.prob[i].p;
+            if (pp.out_nonfinite != nullptr && __any_sync(0xffffffffu, i == 0 ? bad0 : bad1) && lane == 0)
+                atomicOr(pp.out_nonfinite, 1);
             if (pp.out_amax == nullptr) continue;
             float a = warp_max(i == 0 ? am0 : am1);
             if (pp.out_bf16 && !pp.out_fp8) a = __bfloat162float(__float2bfloat16_rn(a));  // max of the stored values
@@ -963,6 +989,7 @@ int launch_gemms(const GemmDesc *descs, int n, cudaStream_t s, const DeviceInfo 
         p.out_fmt = d.out_fmt;
         p.out_scale = d.out_scale;
         p.out_amax = d.out_amax;
+        p.out_nonfinite = d.out_nonfinite;
         const uint64_t kc = static_cast<uint64_t>(d.kc);
         const uint64_t ra = static_cast<uint64_t>(d.rows_a), rb = static_cast<uint64_t>(d.rows_b);
         rc = d.a_mn ? make_tmap(&P.ta, d.a, ra, kc, BK) : make_tmap(&P.ta, d.a, kc, ra, ROWS_A);

@@ -369,6 +369,41 @@ __global__ void __launch_bounds__(kThreads) fused_step_kernel(const StepCommon c
 
 // FP8MP_FUSED_MASTER=0 selects the three-launch version (read per call, so
 // tests can run both).
+// The step when the gradients' producer has already looked for Inf/NaN
+// (*grad_nonfinite nonzero iff it found one, e.g. the wgrad GEMM epilogue):
+// no scan pass and no barrier, so a plain launch. found_inf is 0 on entry
+// (zeroed on the stream); each block adds 2 when it is done, and the last
+// block does the bookkeeping, sets found_inf to the flag and resets
+// *grad_nonfinite to 0 for the next producer (every block read it before
+// its own arrival).
+template <class Opt, class Args, class Extra>
+__global__ void __launch_bounds__(kThreads)
+prescanned_step_kernel(const StepCommon c, const Args a, const Extra x, int32_t *grad_nonfinite) {
+    pdl_wait();
+    pdl_launch_dependents();
+    __shared__ int s_skip;
+    if (threadIdx.x == 0) s_skip = *reinterpret_cast<volatile int32_t *>(grad_nonfinite) != 0;
+    __syncthreads();
+    float am = 0.0f;
+    if (!s_skip) {
+        const Opt opt = make_opt(a, __fdiv_rn(1.0f, *c.loss_scale));
+        am = update_share(opt, c.g, c.n, c.w8, *c.scale_w);
+    }
+    block_amax_atomic(am, c.amax_w);
+    if (threadIdx.x == 0) {
+        __threadfence();
+        const int32_t prev = atomicAdd(c.found_inf, 2);
+        if ((prev >> 1) == static_cast<int32_t>(gridDim.x) - 1) {
+            __threadfence();
+            const int found = s_skip;
+            if (!found) x.clean_step();
+            loss_scale_update(c.loss_scale, c.growth, found, c.backoff, c.growth_factor, c.interval);
+            *c.found_inf = found;
+            *grad_nonfinite = 0;
+        }
+    }
+}
+
 // Diagnostic of the barrier's failure path: one block arrives at a barrier
 // that waits for two arrivals, so the bounded wait runs out after about 2 s,
 // raises the device flag and returns; the kernel ends normally.
@@ -392,12 +427,20 @@ FusedGrid g_fused[64];
 
 template <class Opt, class Args, class Extra>
 int launch_step(const StepCommon &c, const Args &a, const Extra &x, int which, cudaStream_t s, const DeviceInfo &dev,
-                const char *fn) {
+                const char *fn, int32_t *grad_nonfinite = nullptr) {
     cudaError_t e = cudaMemsetAsync(c.found_inf, 0, sizeof(int32_t), s);
     if (e != cudaSuccess) return fail(FP8MP_ERR_LAUNCH, "%s: memset failed: %s", fn, cudaGetErrorString(e));
     const int64_t nvec = c.n >> 3;
     int64_t blocks = (nvec + kThreads - 1) / kThreads;
     if (blocks < 1) blocks = 1;
+    if (grad_nonfinite != nullptr) {
+        const int64_t cap = static_cast<int64_t>(dev.num_sms) * 8;
+        if (blocks > cap) blocks = cap;
+        e = launch_kernel(prescanned_step_kernel<Opt, Args, Extra>, dim3(static_cast<unsigned>(blocks)),
+                          dim3(kThreads), 0, s, c, a, x, grad_nonfinite);
+        if (e != cudaSuccess) return fail(FP8MP_ERR_LAUNCH, "%s: launch failed: %s", fn, cudaGetErrorString(e));
+        return FP8MP_OK;
+    }
     if (c.n > 0 && fused_enabled()) {
         int &per_sm = g_fused[dev.device & 63].blocks_per_sm[which];
         if (per_sm == 0) {
@@ -439,22 +482,25 @@ int launch_step(const StepCommon &c, const Args &a, const Extra &x, int which, c
 int launch_adam_step(const uint16_t *g, int64_t n, float *w, float *m, float *v, uint8_t *w8, const float *scale_w,
                      float *amax_w, float *loss_scale, int32_t *growth, int32_t *found_inf, float *beta_pows,
                      float lr, float b1, float b2, float eps, float backoff, float growth_factor,
-                     int32_t growth_interval, cudaStream_t s, const DeviceInfo &dev) {
+                     int32_t growth_interval, cudaStream_t s, const DeviceInfo &dev, int32_t *grad_nonfinite) {
     const StepCommon c = {g, n, w8, scale_w, amax_w, loss_scale, growth, found_inf, backoff, growth_factor,
                           growth_interval};
     const AdamArgs a = {w, m, v, beta_pows, lr, b1, b2, eps};
     const AdamExtra x = {beta_pows, b1, b2};
-    return launch_step<AdamOpt>(c, a, x, 1, s, dev, "mp_master_step_adam");
+    return launch_step<AdamOpt>(c, a, x, 1, s, dev, grad_nonfinite ? "mp_master_step_adam_prescanned"
+                                                                   : "mp_master_step_adam",
+                                grad_nonfinite);
 }
 
 int launch_master_step(const uint16_t *g, int64_t n, float *w, float *v, uint8_t *w8, const float *scale_w,
                        float *amax_w, float *loss_scale, int32_t *growth, int32_t *found_inf, float lr, float mu,
                        float backoff, float growth_factor, int32_t growth_interval, cudaStream_t s,
-                       const DeviceInfo &dev) {
+                       const DeviceInfo &dev, int32_t *grad_nonfinite) {
     const StepCommon c = {g, n, w8, scale_w, amax_w, loss_scale, growth, found_inf, backoff, growth_factor,
                           growth_interval};
     const SgdArgs a = {w, v, lr, mu};
-    return launch_step<SgdOpt>(c, a, NoExtra{}, 0, s, dev, "mp_master_step");
+    return launch_step<SgdOpt>(c, a, NoExtra{}, 0, s, dev,
+                               grad_nonfinite ? "mp_master_step_prescanned" : "mp_master_step", grad_nonfinite);
 }
 
 int launch_barrier_selftest(cudaStream_t s) {

@@ -290,11 +290,20 @@ int fp8_linear_bwd(const uint8_t *dy8, const uint8_t *dy8t, const uint8_t *w8t, 
  * e.g. a first layer); dw [N x K] of dw_dtype or NULL (frozen weight); they
  * must not overlap. M, N, K multiples of 16. N == 0 gives dx = 0, M == 0
  * gives dw = 0.
+ *
+ * dw_nonfinite  device int32 or NULL. When given (and dw is computed), the
+ *   wgrad epilogue ORs 1 into it if any element of dw as stored is Inf or
+ *   NaN: the overflow check of the dynamic loss scaler ([MP], the loss-scale
+ *   procedure: inspect the gradients for Inf/NaN), made where the gradients
+ *   are produced, so mp_master_step_prescanned need not read them again.
+ *   The caller zeroes it before the first backward of a step (the
+ *   prescanned master step leaves it at 0); further backward passes of the
+ *   step (gradient accumulation) keep OR-ing into it.
  */
 int fp8_linear_bwd_rowmajor(const uint8_t *dy8, const uint8_t *w8, const uint8_t *x8, int64_t M, int64_t N,
                             int64_t K, int32_t dy_fmt, const float *sinv_dy, const float *sinv_w,
                             const float *sinv_x, void *dx, int32_t dx_dtype, void *dw, int32_t dw_dtype,
-                            void *stream);
+                            int32_t *dw_nonfinite, void *stream);
 
 /*
  * delayed_scaling_update -- the DelayedScaling bookkeeping of one step for a
@@ -370,6 +379,30 @@ int mp_master_step_adam(const uint16_t *grad_bf16, int64_t n, float *master, flo
                         float *loss_scale, int32_t *growth_tracker, int32_t *found_inf, float *beta_pows,
                         float lr, float beta1, float beta2, float eps, float backoff, float growth_factor,
                         int32_t growth_interval, void *stream);
+
+/*
+ * mp_master_step_prescanned, mp_master_step_adam_prescanned -- the two steps
+ * above when the gradients' producer has already looked for Inf/NaN in them
+ * (fp8_linear_bwd_rowmajor's dw_nonfinite): the same results bit for bit,
+ * with found_inf taken from the flag instead of a scan of the gradients
+ * (which saves a 2-byte-per-parameter pass and the grid barrier).
+ *   grad_nonfinite  device int32, in/out: nonzero iff some gradient element
+ *                   is Inf or NaN. The step copies it (as 0 / 1) into
+ *                   *found_inf and then sets it to 0 for the next producer.
+ *                   It must not be found_inf itself.
+ * Other arguments and results as mp_master_step / mp_master_step_adam.
+ */
+int mp_master_step_prescanned(const uint16_t *grad_bf16, int64_t n, float *master, float *momentum,
+                              uint8_t *w8, const float *scale_w, float *amax_w, float *loss_scale,
+                              int32_t *growth_tracker, int32_t *found_inf, int32_t *grad_nonfinite, float lr,
+                              float momentum_coef, float backoff, float growth_factor, int32_t growth_interval,
+                              void *stream);
+int mp_master_step_adam_prescanned(const uint16_t *grad_bf16, int64_t n, float *master, float *exp_avg,
+                                   float *exp_avg_sq, uint8_t *w8, const float *scale_w, float *amax_w,
+                                   float *loss_scale, int32_t *growth_tracker, int32_t *found_inf,
+                                   int32_t *grad_nonfinite, float *beta_pows, float lr, float beta1, float beta2,
+                                   float eps, float backoff, float growth_factor, int32_t growth_interval,
+                                   void *stream);
 
 /*
  * fp8mp_check -- synchronises `stream`, then reports and clears the device

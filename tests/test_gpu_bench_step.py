@@ -82,6 +82,7 @@ class OracleRun:
             meta_equal(dm_, om_, f"{label} meta {name}")
         assert st.S.item() == self.ls.S[0] and st.growth.item() == self.ls.growth[0]
         assert st.found.item() == self.ls.found_inf[0] == 0
+        assert st.gnf.item() == 0  # dW's overflow flag, consumed and reset by the master step
 
 
 def test_bench_step_matches_oracle(cuda_lib, orc):
@@ -113,3 +114,24 @@ def test_bench_step_full_size_eager_then_graph(cuda_lib, orc):
     g.replay()
     assert cuda_lib.fp8mp_check() == 0
     run.check_step("graph step")
+
+
+def test_bench_step_skips_on_a_nan_gradient(cuda_lib):
+    """A NaN in dY becomes an E5M2 NaN code, hence NaN in the stored dW; the
+    wgrad epilogue flags it and the master step skips on the flag: master
+    weights, momentum and W8 unchanged, S halved, growth reset, flag reset."""
+    st = bench.LinearStep(m=256, k=512, n=256)
+    st.step()
+    assert cuda_lib.fp8mp_check() == 0
+    master, mom, w8 = st.master.clone(), st.mom.clone(), st.W8.clone()
+    S, growth = st.S.item(), st.growth.item()
+    assert growth == 1
+    st.dy[17, 33] = float("nan")
+    st.step()
+    assert cuda_lib.fp8mp_check() == 0
+    assert st.found.item() == 1 and st.gnf.item() == 0
+    assert st.S.item() == S / 2 and st.growth.item() == 0
+    assert torch.equal(st.master.view(torch.int32), master.view(torch.int32))
+    assert torch.equal(st.mom.view(torch.int32), mom.view(torch.int32))
+    assert torch.equal(st.W8, w8)
+    assert not torch.isfinite(st.dw.float()).all()

@@ -189,6 +189,49 @@ def test_backward_from_rowmajor_copies_one_side(cuda_lib, orc, engine):
     gemm_tolerance_check(np_view(dw).astype(np.float64), ref, ab, "rowmajor dw only")
 
 
+@pytest.mark.parametrize("dw_dt", ["bf16", "f32"])
+def test_dw_nonfinite_flag_matches_a_scan_of_the_stored_dw(cuda_lib, orc, engine, dw_dt):
+    """fp8_linear_bwd_rowmajor's dw_nonfinite is 1 exactly when a stored dW
+    element is Inf or NaN: finite codes at ordinary scales; scales around the
+    output type's overflow (for bf16 a finite fp32 value can round to Inf);
+    and E5M2 Inf / NaN codes in dY8."""
+    M, N, K = 272, 400, 528
+    rng = np.random.default_rng(1234)
+    dy8 = finite_codes(rng, (M, N), E5M2)
+    x8 = finite_codes(rng, (M, K), E4M3)
+    ref, _ = orc.gemm_ref(np.ascontiguousarray(dy8.T), E5M2, np.ascontiguousarray(x8.T), E4M3, 1.0, 1.0)
+    big = float(np.abs(ref).max())
+    top = float(torch.finfo(TORCH_DT[dw_dt]).max)
+    dw = torch.empty((N, K), dtype=TORCH_DT[dw_dt], device="cuda")
+    flag = torch.zeros(1, dtype=torch.int32, device="cuda")
+    seen = []
+    for s_dy in (1.0, 0.5 * top / big, 0.999 * top / big, 1.001 * top / big, 4.0 * top / big):
+        s_dy = float(np.float32(s_dy))
+        if not np.isfinite(s_dy):
+            continue
+        flag.zero_()
+        cuda_lib.fp8_linear_bwd_rowmajor(dev(dy8), None, dev(x8), sc(s_dy), None, sc(1.0), None, dw,
+                                         dw_nonfinite=flag)
+        assert cuda_lib.fp8mp_check() == 0
+        expect = int(not torch.isfinite(dw.float()).all().item())
+        assert flag.item() == expect, (s_dy, expect)
+        seen.append(expect)
+    assert seen[0] == 0 and seen[-1] == 1
+    # Inf and NaN codes of E5M2 in the output gradient
+    for code in (0x7C, 0xFC, 0x7E):
+        bad = dy8.copy()
+        bad[rng.integers(0, M), rng.integers(0, N)] = code
+        flag.zero_()
+        cuda_lib.fp8_linear_bwd_rowmajor(dev(bad), None, dev(x8), sc(1.0), None, sc(1.0), None, dw,
+                                         dw_nonfinite=flag)
+        assert cuda_lib.fp8mp_check() == 0
+        assert not torch.isfinite(dw.float()).all().item()
+        assert flag.item() == 1, hex(code)
+    # the flag accumulates (OR) over calls and is left alone by clean ones
+    cuda_lib.fp8_linear_bwd_rowmajor(dev(dy8), None, dev(x8), sc(1.0), None, sc(1.0), None, dw, dw_nonfinite=flag)
+    assert cuda_lib.fp8mp_check() == 0 and flag.item() == 1
+
+
 def test_long_contraction_e5m2_wgrad(cuda_lib, orc, engine):
     """wgrad contracts over all tokens: 16384 here (the MLP workload's M)."""
     N, K, M = 256, 384, 16384

@@ -128,3 +128,43 @@ def test_adam_steps_bit_exact(cuda_lib, orc, path, n):
         compare(ds, hs, f"adam n={n} step={step}")
         assert_same_bits(np_view(m), hm, "exp_avg")
         assert_same_bits(np_view(bp), np.array([ad.b1p[0], ad.b2p[0]], np.float32), "beta powers")
+
+
+# ------------------------------------------- steps on a producer's flag
+
+
+@pytest.mark.parametrize("opt", ["sgd", "adam"])
+@pytest.mark.parametrize("n", [1, 9, 4096, (1 << 20) + 3])
+def test_prescanned_steps_bit_exact(cuda_lib, orc, opt, n):
+    """mp_master_step(_adam) with grad_nonfinite: the flag set from a host
+    scan of the gradients stands in for the producer's (the GEMM epilogue's
+    flag has its own test); results bit-exact against the oracle, found_inf
+    equal to the flag, the flag reset to 0."""
+    w = workloads.master_weights(n, seed=n + 7)
+    ds = DevState(w, 2.0 ** 16, 0)
+    hs = host_state(w, 2.0 ** 16, 0, orc)
+    m = torch.zeros(n, dtype=torch.float32, device="cuda")
+    bp = torch.ones(2, dtype=torch.float32, device="cuda")
+    hm = np.zeros(n, np.float32)
+    ad = orc.AdamState()
+    flag = torch.zeros(1, dtype=torch.int32, device="cuda")
+    for step in range(4):
+        g = workloads.master_step(n, step, seed=n + 7, inject=(step == 1), inject_frac=1e-3)
+        gb = np_view(g)
+        flag.fill_(int(((gb & 0x7F80) == 0x7F80).any()))
+        ds.scale_w.fill_(32.0)
+        if opt == "sgd":
+            cuda_lib.mp_master_step(g.cuda(), ds.w, ds.v, ds.w8, ds.scale_w, ds.amax_w, ds.S, ds.growth, ds.found,
+                                    1e-4, 0.9, grad_nonfinite=flag)
+            orc.master_step(gb, hs["w"], hs["v"], hs["w8"], 32.0, hs["am"], hs["st"], 1e-4, 0.9)
+        else:
+            cuda_lib.mp_master_step_adam(g.cuda(), ds.w, m, ds.v, ds.w8, ds.scale_w, ds.amax_w, ds.S, ds.growth,
+                                         ds.found, bp, lr=1e-3, grad_nonfinite=flag)
+            orc.adam_step(gb, hs["w"], hm, hs["v"], hs["w8"], 32.0, hs["am"], hs["st"], ad, lr=1e-3)
+        assert cuda_lib.fp8mp_check() == 0
+        compare(ds, hs, f"{opt} prescanned n={n} step={step}")
+        assert flag.item() == 0
+        if opt == "adam":
+            assert_same_bits(np_view(m), hm, "exp_avg")
+            assert_same_bits(np_view(bp), np.array([ad.b1p[0], ad.b2p[0]], np.float32), "beta powers")
+    assert hs["st"].S[0] == 2.0 ** 15  # the injected step backed off once

@@ -111,8 +111,8 @@ def test_fused_backward_rejects_bad_arguments(lib):
 
 def test_rowmajor_backward_rejects_bad_arguments(lib):
     P = 1 << 20
-    bwd = lambda M, N, K, dx=P, dw=2 * P, fmt=1, dxt=1, dwt=1, w8=P, x8=P: lib.fp8_linear_bwd_rowmajor(
-        P, w8, x8, M, N, K, fmt, P, P, P, dx, dxt, dw, dwt, None)
+    bwd = lambda M, N, K, dx=P, dw=2 * P, fmt=1, dxt=1, dwt=1, w8=P, x8=P, nf=None: lib.fp8_linear_bwd_rowmajor(
+        P, w8, x8, M, N, K, fmt, P, P, P, dx, dxt, dw, dwt, nf, None)
     for shape in ((24, 32, 32), (32, 40, 32), (32, 32, 8), (-16, 32, 32)):
         assert bwd(*shape) == fp8mp.ERR_INVALID
     assert bwd(32, 32, 32, fmt=3) == fp8mp.ERR_INVALID
@@ -120,9 +120,10 @@ def test_rowmajor_backward_rejects_bad_arguments(lib):
     assert bwd(32, 32, 32, w8=None) == fp8mp.ERR_INVALID and "w8" in fp8mp.last_error()
     assert bwd(32, 32, 32, x8=P + 3) == fp8mp.ERR_INVALID and "aligned" in fp8mp.last_error()
     assert bwd(32, 32, 32, dx=P, dw=P + 64) == fp8mp.ERR_INVALID and "overlap" in fp8mp.last_error()
+    assert bwd(32, 32, 32, nf=P + 2) == fp8mp.ERR_INVALID and "dw_nonfinite" in fp8mp.last_error()
     # nothing requested: a no-op needing no pointer and no device
     assert lib.fp8_linear_bwd_rowmajor(None, None, None, 32, 32, 32, 1, None, None, None, None, 1, None, 1,
-                                       None) == fp8mp.OK
+                                       None, None) == fp8mp.OK
 
 
 def test_scale_update_rejects_bad_metas(lib):
@@ -154,6 +155,26 @@ def test_master_step_rejects_bad_arguments(lib):
     bad = list(args)
     bad[1] = -5
     assert lib.mp_master_step(*bad) == fp8mp.ERR_INVALID
+
+
+def test_prescanned_master_steps_need_their_own_flag(lib):
+    P = 4096
+    sgd = [P, 1024, P, P, P, P, P, P, P, P, 2 * P, 1e-4, 0.9, 0.5, 2.0, 2000, None]
+    bad = list(sgd)
+    bad[10] = None  # grad_nonfinite is required
+    assert lib.mp_master_step_prescanned(*bad) == fp8mp.ERR_INVALID and "grad_nonfinite" in fp8mp.last_error()
+    bad = list(sgd)
+    bad[10] = P  # the same word as found_inf
+    assert lib.mp_master_step_prescanned(*bad) == fp8mp.ERR_INVALID and "different" in fp8mp.last_error()
+    bad = list(sgd)
+    bad[10] = 2 * P + 1  # misaligned
+    assert lib.mp_master_step_prescanned(*bad) == fp8mp.ERR_INVALID
+    adam = [P, 1024, P, P, P, P, P, P, P, P, P, None, P, 1e-4, 0.9, 0.999, 1e-8, 0.5, 2.0, 2000, None]
+    assert lib.mp_master_step_adam_prescanned(*adam) == fp8mp.ERR_INVALID and "grad_nonfinite" in fp8mp.last_error()
+    bad = list(adam)
+    bad[11] = 2 * P
+    bad[14] = 1.5  # beta1 outside [0, 1)
+    assert lib.mp_master_step_adam_prescanned(*bad) == fp8mp.ERR_INVALID and "betas" in fp8mp.last_error()
 
 
 def test_missing_library_fails_loudly(tmp_path):
