@@ -76,7 +76,8 @@ class _FP8LinearFn(torch.autograd.Function):
         dx = torch.empty((M, K), dtype=x_dtype, device=dev) if ctx.needs_input_grad[0] else None
         dw = torch.empty((N, K), dtype=w_dtype, device=dev) if ctx.needs_input_grad[1] else None
         # dgrad and wgrad in one launch, from the row-major copies
-        fp8_linear_bwd_rowmajor(D8, W8, X8, sinv_dy, sinv_w, sinv_x, dx, dw, dy_fmt=E5M2)
+        fp8_linear_bwd_rowmajor(D8, W8, X8, sinv_dy, sinv_w, sinv_x, dx, dw, dy_fmt=E5M2,
+                                dw_nonfinite=layer.dw_nonfinite if dw is not None else None)
         return (dx.reshape(x_shape) if dx is not None else None), dw, db, None
 
 
@@ -106,6 +107,10 @@ class FP8Linear(torch.nn.Module):
         self.meta_w = Meta(history_len, E4M3, device)
         self.meta_y = Meta(history_len, E4M3, device)
         self.meta_dy = Meta(history_len, E5M2, device)
+        # 1 once a weight gradient of this layer held an Inf or NaN (ORed by
+        # every backward); a master step given it as grad_nonfinite reads and
+        # clears it instead of scanning the gradient again
+        self.dw_nonfinite = torch.zeros(1, dtype=torch.int32, device=device)
 
     def metas(self):
         return [self.meta_x, self.meta_w, self.meta_y, self.meta_dy]

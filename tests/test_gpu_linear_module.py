@@ -59,6 +59,28 @@ def test_fp8linear_two_steps(cuda_lib, orc):
         for k, dm in zip(("x", "w", "y", "dy"), layer.metas()):
             assert_same_bits(np_view(dm.scale), om[k].scale, f"t={t} scale {k}")
             assert_same_bits(np_view(dm.amax_history), om[k].hist, f"t={t} history {k}")
+        assert layer.dw_nonfinite.item() == 0  # finite weight gradient
+
+
+def test_fp8linear_flags_a_nonfinite_weight_gradient(cuda_lib):
+    """The layer's dw_nonfinite turns 1 after a backward whose weight
+    gradient holds a NaN (a NaN in dY) and stays 1 over later clean ones."""
+    from fp8_mixed_precision_reduce_gb300.linear import FP8Linear
+
+    layer = FP8Linear(256, 128, bias=False)
+    x = torch.randn(64, 256, device="cuda")
+    dy = torch.randn(64, 128, device="cuda") * 1e-2
+    layer(x).backward(dy)
+    assert cuda_lib.fp8mp_check() == 0 and layer.dw_nonfinite.item() == 0
+    bad = dy.clone()
+    bad[3, 5] = float("nan")
+    layer.zero_grad(set_to_none=True)
+    layer(x).backward(bad)
+    assert cuda_lib.fp8mp_check() == 0
+    assert not torch.isfinite(layer.weight.grad).all() and layer.dw_nonfinite.item() == 1
+    layer.zero_grad(set_to_none=True)
+    layer(x).backward(dy)
+    assert cuda_lib.fp8mp_check() == 0 and layer.dw_nonfinite.item() == 1
 
 
 def test_fp8linear_rejects_unaligned_features(cuda_lib):
