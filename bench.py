@@ -366,10 +366,41 @@ def run_e2e(st, steps, world, with_outputs=False):
     return ms, h2d, d2h
 
 
+def library_fp8_gemm_tflops(n=8192):
+    """Context for the roofline: cuBLASLt's FP8 GEMM (torch._scaled_mm, E4M3 x
+    E4M3 -> bf16, n^3) back to back, measured before the timed steps. None
+    when this torch cannot run it."""
+    import torch
+
+    try:
+        a = torch.randn(n, n, device="cuda").to(torch.float8_e4m3fn)
+        b = torch.randn(n, n, device="cuda").to(torch.float8_e4m3fn)
+        one = torch.ones((), device="cuda")
+        fn = lambda: torch._scaled_mm(a, b.t(), scale_a=one, scale_b=one, out_dtype=torch.bfloat16)
+        for _ in range(3):
+            fn()
+        torch.cuda.synchronize()
+        best = 0.0
+        for _ in range(3):
+            t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            t0.record()
+            for _ in range(10):
+                fn()
+            t1.record()
+            torch.cuda.synchronize()
+            best = max(best, 2.0 * n ** 3 / (t0.elapsed_time(t1) / 10 * 1e-3) / 1e12)
+        del a, b
+        torch.cuda.empty_cache()
+        return round(best, 1)
+    except (RuntimeError, TypeError, AttributeError):
+        return None
+
+
 def run_ours(args, world, rank, local):
     import torch
 
     peaks, peak_kind = load_peaks()
+    lib_fp8 = library_fp8_gemm_tflops()
     st = LinearStep(prescanned=not args.master_scans_dw)
     torch.cuda.synchronize()
     flush = torch.empty(int(2 * 129e6 // 4) + 1, dtype=torch.float32, device="cuda")  # > 2x L2
@@ -471,7 +502,9 @@ def run_ours(args, world, rank, local):
                      "traffic": traffic,
                      "traffic_by_launch": {"fwd": gemm_traffic_from_profile("dram_bytes_fwd_launch"),
                                            "bwd": gemm_traffic_from_profile("dram_bytes_bwd_launch")},
-                     "peak_source": f"{peak_kind} bf16 burst x {FP8_OVER_BF16:g} (nominal fp8/bf16 dense ratio)"},
+                     "peak_source": f"{peak_kind} bf16 burst x {FP8_OVER_BF16:g} (nominal fp8/bf16 dense ratio)",
+                     "library_fp8_gemm_8192cubed": lib_fp8,
+                     "frac_of_library_fp8": round(achieved / lib_fp8, 4) if lib_fp8 else None},
         "e2e": {"value": round(world * fl / (e2e_ms * 1e-3) / 1e12, 2), "unit": "TFLOP/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 5),
                 "result_read_back": "overflow flag and loss scale (the loss scaler's state)",
