@@ -1,10 +1,12 @@
 // api.cu -- the extern "C" entry points of libfp8mp declared in
 // include/fp8mp.h: argument validation, device check, error reporting, and
 // dispatch to the kernels' launchers. No computation happens here.
+#include <atomic>
 #include <cstdarg>
 #include <cstdio>
 #include <cstdlib>
 #include <cstring>
+#include <mutex>
 
 #include "fp8mp_internal.cuh"
 
@@ -38,9 +40,11 @@ int current_device(DeviceInfo *info) {
     int dev = -1;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return fail(FP8MP_ERR_LAUNCH, "cudaGetDevice failed: %s", cudaGetErrorString(e));
+    // per-device attributes, queried once; the flag is published after the
+    // data (release) and checked before reading it (acquire)
     static DeviceInfo cache[64];
-    static bool have[64] = {false};
-    if (dev >= 0 && dev < 64 && have[dev]) {
+    static std::atomic<bool> have[64];
+    if (dev >= 0 && dev < 64 && have[dev].load(std::memory_order_acquire)) {
         *info = cache[dev];
     } else {
         DeviceInfo d;
@@ -50,9 +54,13 @@ int current_device(DeviceInfo *info) {
         if (e == cudaSuccess) e = cudaDeviceGetAttribute(&d.num_sms, cudaDevAttrMultiProcessorCount, dev);
         if (e != cudaSuccess)
             return fail(FP8MP_ERR_LAUNCH, "cudaDeviceGetAttribute failed: %s", cudaGetErrorString(e));
-        if (dev >= 0 && dev < 64) {
-            cache[dev] = d;
-            have[dev] = true;
+        if (dev >= 0 && dev < 64 && !have[dev].load(std::memory_order_acquire)) {
+            static std::mutex m;
+            std::lock_guard<std::mutex> lock(m);
+            if (!have[dev].load(std::memory_order_relaxed)) {
+                cache[dev] = d;
+                have[dev].store(true, std::memory_order_release);
+            }
         }
         *info = d;
     }

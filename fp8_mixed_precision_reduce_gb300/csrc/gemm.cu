@@ -51,6 +51,7 @@
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
+#include <atomic>
 #include <cstdlib>
 #include <cstring>
 #include <mutex>
@@ -855,11 +856,15 @@ constexpr uint32_t make_idesc(int fmt_a, int fmt_b, int m, int a_mn, int b_mn) {
            | (static_cast<uint32_t>(m >> 4) << 24);     // M / 16
 }
 
+// Per device: the kernels' shared-memory attribute set and the SM-pair
+// engine's resident cluster count, done once; `ready` is published after the
+// data (release) and checked before reading it (acquire).
 struct PerDevice {
-    bool attr_done[2] = {false, false};
+    std::atomic<bool> ready[2];
     int max_pairs = 0;
 };
 PerDevice g_dev[64];
+std::mutex g_dev_mutex;
 
 template <bool PAIR>
 int launch_engine(const GemmBatch &batch, int grid, cudaStream_t s) {
@@ -892,7 +897,9 @@ template <bool PAIR>
 int prepare_engine(const DeviceInfo &dev) {
     using C = Cfg<PAIR>;
     PerDevice &pd = g_dev[dev.device & 63];
-    if (pd.attr_done[PAIR]) return FP8MP_OK;
+    if (pd.ready[PAIR].load(std::memory_order_acquire)) return FP8MP_OK;
+    std::lock_guard<std::mutex> lock(g_dev_mutex);
+    if (pd.ready[PAIR].load(std::memory_order_relaxed)) return FP8MP_OK;
     cudaError_t e =
         cudaFuncSetAttribute(gemm_fp8_kernel<PAIR>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_ALLOC);
     if (e != cudaSuccess) return fail(FP8MP_ERR_LAUNCH, "GEMM smem attribute failed: %s", cudaGetErrorString(e));
@@ -913,7 +920,7 @@ int prepare_engine(const DeviceInfo &dev) {
         if (e != cudaSuccess || n < 1) n = dev.num_sms / 2;
         pd.max_pairs = n;
     }
-    pd.attr_done[PAIR] = true;
+    pd.ready[PAIR].store(true, std::memory_order_release);
     return FP8MP_OK;
 }
 

@@ -25,6 +25,7 @@
 //   three launches (FP8MP_FUSED_MASTER=0): grad_scan_kernel, the update
 //     kernel (every block leaves at once when found_inf is set), and a
 //     one-thread bookkeeping kernel.
+#include <atomic>
 #include <cstdlib>
 #include <cstring>
 
@@ -420,8 +421,10 @@ bool fused_enabled() {
     return !(v != nullptr && std::strcmp(v, "0") == 0);
 }
 
+// Resident blocks per SM of the fused kernel (SGD, Adam) per device, queried
+// once; a query that raced with another thread's stores the same value.
 struct FusedGrid {
-    int blocks_per_sm[2] = {0, 0};  // SGD, Adam
+    std::atomic<int> blocks_per_sm[2];
 };
 FusedGrid g_fused[64];
 
@@ -442,12 +445,14 @@ int launch_step(const StepCommon &c, const Args &a, const Extra &x, int which, c
         return FP8MP_OK;
     }
     if (c.n > 0 && fused_enabled()) {
-        int &per_sm = g_fused[dev.device & 63].blocks_per_sm[which];
-        if (per_sm == 0) {
+        std::atomic<int> &cached = g_fused[dev.device & 63].blocks_per_sm[which];
+        int per_sm = cached.load(std::memory_order_relaxed);
+        if (per_sm < 1) {
             e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, fused_step_kernel<Opt, Args, Extra>, kThreads,
                                                               0);
             if (e != cudaSuccess || per_sm < 1)
                 return fail(FP8MP_ERR_LAUNCH, "%s: occupancy query failed: %s", fn, cudaGetErrorString(e));
+            cached.store(per_sm, std::memory_order_relaxed);
         }
         const int64_t cap = static_cast<int64_t>(dev.num_sms) * per_sm;
         if (blocks > cap) blocks = cap;
