@@ -35,9 +35,17 @@
  *   FP8MP_ERR_DEVICE (-2): the current device is not an sm_103 GPU.
  *   FP8MP_ERR_LAUNCH (-3): a CUDA call or kernel launch failed.
  *   FP8MP_ERR_TIMEOUT (-4): returned by fp8mp_check(): a bounded wait inside
- *     a GEMM kernel ran out (a wedged pipeline); that kernel's output is
- *     undefined, the CUDA context stays usable.
+ *     a kernel ran out (a GEMM's wedged pipeline, the master step's grid
+ *     barrier); that kernel's output is undefined, the CUDA context stays
+ *     usable.
  *   fp8mp_last_error() then describes the failure (thread-local).
+ * Launch. Kernels are launched with programmatic stream serialization: one
+ *   may be scheduled while the previous kernel on the stream drains, and it
+ *   waits for that kernel to complete before it touches global memory, so
+ *   stream order holds as usual. Environment switches, read by the library:
+ *   FP8MP_PDL=0 (once per process) launches plainly; FP8MP_GEMM_ENGINE=pair
+ *   or single (per call) forces a GEMM tile engine; FP8MP_FUSED_MASTER=0
+ *   (per call) runs the self-scanning master steps as three launches.
  */
 #ifndef FP8MP_H
 #define FP8MP_H
