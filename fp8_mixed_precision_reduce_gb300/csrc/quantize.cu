@@ -71,10 +71,56 @@ __device__ __forceinline__ float load1(const void *x, int64_t i) {
         return reinterpret_cast<const float *>(x)[i];
 }
 
+// The casts' conversion step. cvt .satfinite rounds to nearest even and
+// saturates finite overflow and infinities to the largest finite code; a NaN
+// input gives a NaN code (E4M3 S.1111.111, E5M2 S.11111.mm with mm != 0) and
+// no other input does. So instead of testing every element for NaN the casts
+// test the packed codes: nan_probe sets bit 7 of every byte that holds a NaN
+// code (the byte's low 7 bits plus 1 (E4M3) or 3 (E5M2) reach 0x80 exactly
+// then, and no carry crosses a byte), and the rare words with one get their
+// NaN bytes rewritten to 0x7F -- the same codes cvt_quad gives.
+template <int FMT>
+__device__ __forceinline__ uint32_t nan_probe(uint32_t codes) {
+    return (codes & 0x7F7F7F7Fu) + (FMT == FP8MP_E4M3 ? 0x01010101u : 0x03030303u);
+}
+template <int FMT>
+__device__ __forceinline__ uint32_t canonical_nan(uint32_t codes) {
+    const uint32_t nan_bytes = ((nan_probe<FMT>(codes) & 0x80808080u) >> 7) * 0xFFu;
+    return (codes & ~nan_bytes) | (0x7F7F7F7Fu & nan_bytes);
+}
+template <int FMT>
+__device__ __forceinline__ uint32_t cvt_pair_raw(float lo, float hi) {
+    uint16_t r;
+    if constexpr (FMT == FP8MP_E4M3)
+        asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
+    else
+        asm("cvt.rn.satfinite.e5m2x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
+    return r;
+}
+// Four elements -> four codes (little-endian) under `scale`; their |x| joins
+// the running amax (fmaxf ignores a NaN operand, and the running value, which
+// starts at +0, is never NaN) and their codes join the NaN probe.
+template <int FMT>
+__device__ __forceinline__ uint32_t cast4(float f0, float f1, float f2, float f3, float scale, float &am,
+                                          uint32_t &probe) {
+    const uint32_t q = cvt_pair_raw<FMT>(__fmul_rn(f0, scale), __fmul_rn(f1, scale)) |
+                       (cvt_pair_raw<FMT>(__fmul_rn(f2, scale), __fmul_rn(f3, scale)) << 16);
+    probe |= nan_probe<FMT>(q);
+    am = fmaxf(fmaxf(am, fabsf(f0)), fmaxf(fabsf(f1), fmaxf(fabsf(f2), fabsf(f3))));
+    return q;
+}
+// Two bf16 words (four elements) -> four codes.
+template <int FMT>
+__device__ __forceinline__ uint32_t cast4_bf16(uint32_t w0, uint32_t w1, float scale, float &am, uint32_t &probe) {
+    return cast4<FMT>(__uint_as_float(w0 << 16), __uint_as_float(w0 & 0xFFFF0000u), __uint_as_float(w1 << 16),
+                      __uint_as_float(w1 & 0xFFFF0000u), scale, am, probe);
+}
+
 // Row-major cast of a flat array of n elements: chunks of 16 elements give
-// one 16-byte store; the n % 16 tail is done element by element.
+// one 16-byte store; the n % 16 tail is done element by element. Eight
+// blocks of 256 threads fit an SM (32 registers a thread).
 template <int FMT, bool BF16>
-__global__ void __launch_bounds__(kThreads)
+__global__ void __launch_bounds__(kThreads, 8)
 cast_rows_kernel(const void *__restrict__ x, int64_t n, const float *__restrict__ scale_p,
                  uint8_t *__restrict__ out, float *__restrict__ amax_p) {
     pdl_wait();
@@ -84,23 +130,33 @@ cast_rows_kernel(const void *__restrict__ x, int64_t n, const float *__restrict_
     const int64_t nchunk = n >> 4;
     const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
     for (int64_t c = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; c < nchunk; c += stride) {
-        float f[16];
-        load16<BF16>(x, c, f);
-        uint32_t o[4];
+        uint32_t o[4], probe = 0;
+        if constexpr (BF16) {
+            const uint4 *p = reinterpret_cast<const uint4 *>(x) + 2 * c;
+            const uint4 a = __ldcs(p), b = __ldcs(p + 1);
+            o[0] = cast4_bf16<FMT>(a.x, a.y, scale, am, probe);
+            o[1] = cast4_bf16<FMT>(a.z, a.w, scale, am, probe);
+            o[2] = cast4_bf16<FMT>(b.x, b.y, scale, am, probe);
+            o[3] = cast4_bf16<FMT>(b.z, b.w, scale, am, probe);
+        } else {
+            const float4 *p = reinterpret_cast<const float4 *>(x) + 4 * c;
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            o[j] = cvt_quad<FMT>(__fmul_rn(f[4 * j], scale), __fmul_rn(f[4 * j + 1], scale),
-                                 __fmul_rn(f[4 * j + 2], scale), __fmul_rn(f[4 * j + 3], scale));
+            for (int j = 0; j < 4; ++j) {
+                const float4 v = __ldcs(p + j);
+                o[j] = cast4<FMT>(v.x, v.y, v.z, v.w, scale, am, probe);
+            }
         }
+        if (probe & 0x80808080u) {
 #pragma unroll
-        for (int j = 0; j < 16; ++j) am = max_ignore_nan(am, fabsf(f[j]));
+            for (int j = 0; j < 4; ++j) o[j] = canonical_nan<FMT>(o[j]);
+        }
         reinterpret_cast<uint4 *>(out)[c] = make_uint4(o[0], o[1], o[2], o[3]);
     }
     if (blockIdx.x == gridDim.x - 1) {
         for (int64_t i = (nchunk << 4) + threadIdx.x; i < n; i += blockDim.x) {
             const float v = load1<BF16>(x, i);
             out[i] = static_cast<uint8_t>(cvt_pair<FMT>(__fmul_rn(v, scale), 0.0f) & 0xFFu);
-            am = max_ignore_nan(am, fabsf(v));
+            am = fmaxf(am, fabsf(v));
         }
     }
     if (amax_p != nullptr) block_amax_atomic(am, amax_p);
@@ -146,12 +202,13 @@ cast_rows_t_kernel(const void *__restrict__ x, int64_t rows, int64_t cols, const
             for (int q = 0; q < 4; ++q) {
                 float f[8];
                 load8<BF16>(x, cols, r + q, c, f);
-                lo[q] = cvt_quad<FMT>(__fmul_rn(f[0], scale), __fmul_rn(f[1], scale),
-                                      __fmul_rn(f[2], scale), __fmul_rn(f[3], scale));
-                hi[q] = cvt_quad<FMT>(__fmul_rn(f[4], scale), __fmul_rn(f[5], scale),
-                                      __fmul_rn(f[6], scale), __fmul_rn(f[7], scale));
-#pragma unroll
-                for (int j = 0; j < 8; ++j) am = max_ignore_nan(am, fabsf(f[j]));
+                uint32_t probe = 0;
+                lo[q] = cast4<FMT>(f[0], f[1], f[2], f[3], scale, am, probe);
+                hi[q] = cast4<FMT>(f[4], f[5], f[6], f[7], scale, am, probe);
+                if (probe & 0x80808080u) {
+                    lo[q] = canonical_nan<FMT>(lo[q]);
+                    hi[q] = canonical_nan<FMT>(hi[q]);
+                }
                 if constexpr (DBIAS) {
 #pragma unroll
                     for (int j = 0; j < 8; ++j) csum[j] = __fadd_rn(csum[j], f[j]);
@@ -267,10 +324,10 @@ amax_kernel(const void *__restrict__ x, int64_t n, float *__restrict__ amax_p) {
         float f[16];
         load16<BF16>(x, c, f);
 #pragma unroll
-        for (int j = 0; j < 16; ++j) am = max_ignore_nan(am, fabsf(f[j]));
+        for (int j = 0; j < 16; ++j) am = fmaxf(am, fabsf(f[j]));
     }
     if (blockIdx.x == gridDim.x - 1)
-        for (int64_t i = (nchunk << 4) + threadIdx.x; i < n; i += blockDim.x) am = max_ignore_nan(am, fabsf(load1<BF16>(x, i)));
+        for (int64_t i = (nchunk << 4) + threadIdx.x; i < n; i += blockDim.x) am = fmaxf(am, fabsf(load1<BF16>(x, i)));
     block_amax_atomic(am, amax_p);
 }
 

@@ -27,13 +27,38 @@ def run_quantize(fp8mp, x, fmt, scale, transpose, amax0=0.0):
 def test_every_bf16_pattern(cuda_lib, orc, fmt, transpose):
     bits = np.arange(65536, dtype=np.uint32).astype(np.uint16).reshape(256, 256)
     x = dev(bits.view(np.int16)).view(torch.bfloat16)
-    for scale in (1.0, 2.0 ** -7, 3.0, 0.1, 1e30):
+    # scale 0 turns the infinities into NaN products, which must give 0x7F
+    for scale in (1.0, 2.0 ** -7, 3.0, 0.1, 1e30, 0.0, -2.0):
         got, got_t, am = run_quantize(cuda_lib, x, fmt, scale, transpose)
         exp = orc.cast(bits, scale, fmt)
         assert_same_bits(got, exp, f"codes fmt={fmt} scale={scale}")
         if transpose:
             assert_same_bits(got_t, orc.transpose_u8(exp), "transposed codes")
         assert_same_bits(am, np.array([orc.amax(bits)], dtype=np.float32), "amax")
+
+
+@pytest.mark.parametrize("fmt", [E4M3, E5M2])
+@pytest.mark.parametrize("transpose", [False, True])
+def test_fp32_special_patterns(cuda_lib, orc, fmt, transpose):
+    """fp32 input: every bf16 pattern widened, plus payloads only fp32 has
+    (NaNs with low mantissa bits, the smallest subnormals, values just past
+    the rounding and saturation boundaries), under scales that include 0
+    (Inf * 0 is a NaN product) and a negative one."""
+    wide = np.arange(65536, dtype=np.uint32) << 16
+    rng = np.random.default_rng(20261202)
+    extra = np.array([0x7F800001, 0xFF800001, 0x7FBFFFFF, 0xFFFFFFFF, 0x7FC00001, 0x00000001, 0x80000001,
+                      0x007FFFFF, 0x43E00000, 0x43E00001, 0x43DFFFFF, 0x47600000, 0x47600001, 0x475FFFFF,
+                      0x3B000000, 0x3B000001, 0x3AFFFFFF, 0x37800000, 0x377FFFFF], dtype=np.uint32)
+    fill = rng.integers(0, 2 ** 32, size=4096 - extra.size, dtype=np.uint64).astype(np.uint32)
+    bits = np.concatenate([wide, extra, fill]).reshape(256, 272)
+    x = dev(bits.view(np.int32)).view(torch.float32)
+    for scale in (1.0, 2.0 ** -9, 0.0, -2.0):
+        got, got_t, am = run_quantize(cuda_lib, x, fmt, scale, transpose)
+        exp = orc.cast(bits.view(np.float32), scale, fmt)
+        assert_same_bits(got, exp, f"codes fmt={fmt} scale={scale}")
+        if transpose:
+            assert_same_bits(got_t, orc.transpose_u8(exp), "transposed codes")
+        assert_same_bits(am, np.array([orc.amax(bits.view(np.float32))], dtype=np.float32), "amax")
 
 
 @pytest.mark.slow
