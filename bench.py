@@ -639,6 +639,177 @@ def run_reference(args, world, rank):
     }
 
 
+# ------------------------------------------------------------ kernel table
+
+
+GEMM_SHAPES = (  # (name, M, K, N): the transformer block's and the MLP's linears
+    ("proj", 8192, 4096, 4096), ("qkv", 8192, 4096, 12288),
+    ("mlp_up", 16384, 4096, 14336), ("mlp_down", 16384, 14336, 4096))
+MASTER_PARAMS = 10 ** 9  # the optimizer-state workload
+
+
+def kernel_table(args):
+    """--kernels: every kernel of the path on its own, at the sizes of the
+    other workloads (the transformer block's and the MLP's GEMM shapes and
+    casts, the master step on 1e9 parameters), each against its roofline:
+    median device time of one launch with L2 flushed before it (3 warm-up
+    launches; the flush's own dirty lines are written back before the
+    launch), one JSON line per measurement, the clocks last. Inputs are
+    seeded and synthetic. cuBLASLt's FP8 GEMMs (torch._scaled_mm, E4M3/E5M2
+    in, bf16 out; the backward as its two launches on the transposed copies
+    they need) are timed the same way beside ours, as context."""
+    import torch
+
+    import fp8_mixed_precision_reduce_gb300 as fp8mp
+    import workloads
+
+    fp8mp.load()
+    peaks, peak_kind = load_peaks()
+    hbm = float(peaks["hbm_gbs"])
+    fp8_peak = float(peaks["bf16_tflops"]) * FP8_OVER_BF16
+    flush = torch.empty(int(2 * 129e6 // 4) + 1, dtype=torch.float32, device="cuda")
+    evict = torch.zeros_like(flush)
+    reps = max(3, args.steps)
+
+    def timed(fn, n=reps):
+        ts = []
+        for i in range(n + 3):
+            # L2 flushed by a 2x-L2 write, then that write's dirty lines
+            # evicted by a 2x-L2 read, so the timed launch starts from DRAM
+            # and pays for its own traffic only (as ncu's cache flush does)
+            flush.fill_(float(i))
+            evict.sum()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record()
+            fn()
+            b.record()
+            torch.cuda.synchronize()
+            if i >= 3:
+                ts.append(a.elapsed_time(b) * 1e3)
+        if fp8mp.fp8mp_check() != 0:
+            raise RuntimeError("a kernel's bounded wait ran out")
+        return statistics.median(ts)
+
+    def emit(kernel, workload, us, work, bound, **extra):
+        if bound == "tensor":
+            achieved, peak, unit = work / us / 1e6, fp8_peak, "TFLOP/s"
+        else:
+            achieved, peak, unit = work / us / 1e3, hbm, "GB/s"
+        line = {"kernel": kernel, "workload": workload, "us": round(us, 2), "value": round(achieved, 1),
+                "unit": unit, "roofline": {"bound": bound, "achieved": round(achieved, 1), "peak": round(peak, 1),
+                                           "unit": unit, "frac": round(achieved / peak, 4), "of": peak_kind}}
+        line.update(extra)
+        print(json.dumps(line), flush=True)
+
+    one = torch.ones(1, device="cuda")
+    one0 = torch.ones((), device="cuda")
+    g = workloads.gen(7, "cuda")
+    with ClockSampler(int(os.environ.get("LOCAL_RANK", "0"))) as clocks:
+        # ---- GEMMs: forward, fused backward (ours) and cuBLASLt's
+        for name, M, K, N in GEMM_SHAPES:
+            xf = (torch.randn(M, K, generator=g, device="cuda") * 4).to(torch.float8_e4m3fn)
+            wf = (torch.randn(N, K, generator=g, device="cuda") * 0.1).to(torch.float8_e4m3fn)
+            df = (torch.randn(M, N, generator=g, device="cuda") * 1e3).to(torch.float8_e5m2)
+            x8, w8, d8 = xf.view(torch.uint8), wf.view(torch.uint8), df.view(torch.uint8)
+            y = torch.empty(M, N, dtype=torch.bfloat16, device="cuda")
+            dx = torch.empty(M, K, dtype=torch.bfloat16, device="cuda")
+            dw = torch.empty(N, K, dtype=torch.bfloat16, device="cuda")
+            am = torch.zeros(1, device="cuda")
+            flag = torch.zeros(1, dtype=torch.int32, device="cuda")
+            fl = 2.0 * M * N * K
+            wl = f"{name} M={M} K={K} N={N}"
+            lt_f = timed(lambda: torch._scaled_mm(xf, wf.t(), scale_a=one0, scale_b=one0, out_dtype=torch.bfloat16))
+            us = timed(lambda: fp8mp.fp8_linear_fwd(x8, w8, one, one, y, y_amax=am))
+            emit("gemm_fp8_kernel fwd (bf16 out, amax)", wl, us, fl, "tensor",
+                 library={"cublaslt_us": round(lt_f, 2), "cublaslt_tflops": round(fl / lt_f / 1e6, 1)})
+            if name == "proj":
+                y8 = torch.empty(M, N, dtype=torch.uint8, device="cuda")
+                us = timed(lambda: fp8mp.fp8_linear_fwd_fp8out(x8, w8, one, one, one, y8, y_amax=am))
+                emit("gemm_fp8_kernel fwd (E4M3 out, amax)", wl, us, fl, "tensor")
+                del y8
+            wtf, dtf, xtf = wf.t().contiguous(), df.t().contiguous(), xf.t().contiguous()
+
+            def lt_bwd():
+                torch._scaled_mm(df, wtf.t(), scale_a=one0, scale_b=one0, out_dtype=torch.bfloat16)
+                torch._scaled_mm(dtf, xtf.t(), scale_a=one0, scale_b=one0, out_dtype=torch.bfloat16)
+
+            lt_b = timed(lt_bwd)
+            us = timed(lambda: fp8mp.fp8_linear_bwd_rowmajor(d8, w8, x8, one, one, one, dx, dw, dw_nonfinite=flag))
+            emit("gemm_fp8_kernel bwd (dgrad + wgrad, one launch, row-major copies)", wl, us, 2 * fl, "tensor",
+                 library={"cublaslt_two_launches_us": round(lt_b, 2),
+                          "cublaslt_tflops": round(2 * fl / lt_b / 1e6, 1)})
+            del xf, wf, df, x8, w8, d8, y, dx, dw, wtf, dtf, xtf
+            torch.cuda.empty_cache()
+        # ---- casts (bytes per element: 2 in + 1 out, + 1 for the transposed copy)
+        blk = workloads.transformer_block(device="cuda")
+        mlp = workloads.mlp(device="cuda")
+        for wl, x in (("transformer x 8192x4096 bf16", blk.x), ("mlp down input 16384x14336 bf16", mlp.x_down)):
+            rows, cols = x.shape
+            sc = torch.full((1,), 64.0, device="cuda")
+            am = torch.zeros(1, device="cuda")
+            q = torch.empty(rows, cols, dtype=torch.uint8, device="cuda")
+            qt = torch.empty(cols, rows, dtype=torch.uint8, device="cuda")
+            us = timed(lambda: fp8mp.fp8_quantize(x, fp8mp.E4M3, sc, q, None, am))
+            emit("cast_rows_kernel (E4M3, amax)", wl, us, 3.0 * x.numel(), "hbm")
+            us = timed(lambda: fp8mp.fp8_quantize(x, fp8mp.E4M3, sc, q, qt, am))
+            emit("cast_rows_t_kernel (E4M3 + transposed copy, amax)", wl, us, 4.0 * x.numel(), "hbm")
+            if rows == 8192:
+                sinv = torch.ones(1, device="cuda")
+                us = timed(lambda: fp8mp.fp8_quantize_current(x, fp8mp.E4M3, sc, sinv, am, q, None))
+                emit("current scaling: amax pass + scale + cast", wl, us, 5.0 * x.numel(), "hbm")
+            del q, qt
+        dy = blk.dy_proj
+        rows, cols = dy.shape
+        q = torch.empty(rows, cols, dtype=torch.uint8, device="cuda")
+        qt = torch.empty(cols, rows, dtype=torch.uint8, device="cuda")
+        db = torch.empty(cols, dtype=torch.float32, device="cuda")
+        ws = torch.empty(fp8mp.fp8_quantize_dbias_workspace_bytes(rows, cols), dtype=torch.uint8, device="cuda")
+        sc, am = torch.full((1,), 2.0 ** 10, device="cuda"), torch.zeros(1, device="cuda")
+        us = timed(lambda: fp8mp.fp8_quantize_dbias(dy, fp8mp.E5M2, sc, q, qt, db, ws, am))
+        emit("cast_rows_t_kernel<DBIAS> + dbias_reduce (E5M2 + transposed copy + bias gradient)",
+             "transformer dY 8192x4096 bf16", us, 4.0 * dy.numel(), "hbm")
+        del blk, mlp, dy, q, qt, db, ws
+        torch.cuda.empty_cache()
+        # ---- the master step on 1e9 parameters
+        n = MASTER_PARAMS
+        w = workloads.master_weights(n, device="cuda")
+        mom = torch.zeros(n, device="cuda")
+        w8 = torch.empty(n, dtype=torch.uint8, device="cuda")
+        grad = workloads.master_step(n, 0, device="cuda")
+        sw, amw = torch.full((1,), 256.0, device="cuda"), torch.zeros(1, device="cuda")
+        S, growth = torch.full((1,), S0, device="cuda"), torch.zeros(1, dtype=torch.int32, device="cuda")
+        found, flag = torch.zeros(1, dtype=torch.int32, device="cuda"), torch.zeros(1, dtype=torch.int32, device="cuda")
+        wl = f"optimizer state, {n:.0e} parameters"
+        us = timed(lambda: fp8mp.mp_master_step(grad, w, mom, w8, sw, amw, S, growth, found, LR, MU,
+                                                grad_nonfinite=flag), n=5)
+        emit("prescanned_step_kernel<SgdOpt> (flag from the gradients' producer)", wl, us, 19.0 * n, "hbm")
+        us = timed(lambda: fp8mp.mp_master_step(grad, w, mom, w8, sw, amw, S, growth, found, LR, MU), n=5)
+        emit("fused_step_kernel<SgdOpt> (scans the gradients itself)", wl, us, 21.0 * n, "hbm")
+        bad = grad.clone()
+        bad[12345] = float("inf")
+        us = timed(lambda: fp8mp.mp_master_step(bad, w, mom, w8, sw, amw, S, growth, found, LR, MU), n=5)
+        emit("fused_step_kernel<SgdOpt>, skipped step (an Inf in the gradients)", wl, us, 2.0 * n, "hbm")
+        del bad
+        S.fill_(S0)
+        v2 = torch.zeros(n, device="cuda")
+        bp = torch.ones(2, device="cuda")
+        us = timed(lambda: fp8mp.mp_master_step_adam(grad, w, mom, v2, w8, sw, amw, S, growth, found, bp, LR,
+                                                     grad_nonfinite=flag), n=5)
+        emit("prescanned_step_kernel<AdamOpt>", wl, us, 27.0 * n, "hbm")
+        us = timed(lambda: fp8mp.mp_master_step_adam(grad, w, mom, v2, w8, sw, amw, S, growth, found, bp, LR), n=5)
+        emit("fused_step_kernel<AdamOpt>", wl, us, 29.0 * n, "hbm")
+        del w, mom, w8, grad, v2
+        torch.cuda.empty_cache()
+        # ---- the scale update: latency only
+        metas = [fp8mp.Meta(HIST_LEN, f) for f in (fp8mp.E4M3, fp8mp.E4M3, fp8mp.E4M3, fp8mp.E5M2)]
+        us = timed(lambda: fp8mp.delayed_scaling_update(metas, fp8mp.AMAX_MOST_RECENT))
+        print(json.dumps({"kernel": "scale_update_kernel", "workload": f"4 metas, L={HIST_LEN}", "us": round(us, 2),
+                          "roofline": None}), flush=True)
+    print(json.dumps({"clocks": clocks.summary(),
+                      "l2": "flushed (2x L2 write, then a 2x L2 read that evicts its dirty lines) before each timed launch",
+                      "reps": reps, "warmup": 3}), flush=True)
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
     ap.add_argument("--gpus", type=int, default=1)
@@ -654,6 +825,9 @@ def main(argv=None):
                     help="the master step scans dW for Inf/NaN itself instead of reading the wgrad epilogue's flag")
     ap.add_argument("--eager", action="store_true",
                     help="launch every library call from Python in the timed steps instead of replaying graphs")
+    ap.add_argument("--kernels", action="store_true",
+                    help="instead of the step: each kernel alone at the other workloads' sizes against its "
+                         "roofline (one JSON line each; --steps sets the timed launches per kernel)")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
@@ -674,6 +848,9 @@ def main(argv=None):
     import fp8_mixed_precision_reduce_gb300 as fp8mp
 
     fp8mp.load()  # raises when the library is missing: no fallback
+    if args.kernels:
+        kernel_table(args)
+        return 0
     world, rank, local = dist_setup()
     out = run_ours(args, world, rank, local)
     if rank == 0:

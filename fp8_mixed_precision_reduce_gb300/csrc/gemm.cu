@@ -396,6 +396,18 @@ __device__ __forceinline__ bool has_nonfinite_bf16x2(uint32_t w) {
     return (t & 0xFFFFu) == 0u || (t >> 16) == 0u;
 }
 
+// max |v[j]| over 16 values as a pairwise tree (depth 4 instead of a chain
+// of 16); fmaxf ignores a NaN operand, so the result is the max of the
+// non-NaN |v| (or NaN when all are NaN, which fmaxf(am, .) then ignores).
+__device__ __forceinline__ float abs_max16(const float (&v)[16]) {
+    float t[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) t[j] = fmaxf(fabsf(v[2 * j]), fabsf(v[2 * j + 1]));
+#pragma unroll
+    for (int j = 0; j < 4; ++j) t[j] = fmaxf(t[2 * j], t[2 * j + 1]);
+    return fmaxf(fmaxf(t[0], t[1]), fmaxf(t[2], t[3]));
+}
+
 __device__ __forceinline__ uint32_t pack_bf16x2(float a, float b) {
     const __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
     return *reinterpret_cast<const uint32_t *>(&h);
@@ -660,10 +672,7 @@ gemm_fp8_kernel(const __grid_constant__ GemmBatch batch) {
                                 y[4 * j + 3] = __fmaf_rn(__uint_as_float(r32[16 * g + 4 * j + 3]), scale, bb.w);
                             }
                         }
-                        if (row_ok && col_ok) {
-#pragma unroll
-                            for (int j = 0; j < 16; ++j) am = max_ignore_nan(am, fabsf(y[j]));
-                        }
+                        if (row_ok && col_ok) am = fmaxf(am, abs_max16(y));
                         if (out_fp8) {
 #pragma unroll
                             for (int j = 0; j < 4; ++j) {
