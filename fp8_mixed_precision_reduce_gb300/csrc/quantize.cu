@@ -267,16 +267,30 @@ cast_rows_t_kernel(const void *__restrict__ x, int64_t rows, int64_t cols, const
     if (amax_p != nullptr) block_amax_atomic(am, amax_p);
 }
 
-// dbias[n] = sum over tile rows t (in order) of ws[t * cols + n].
-__global__ void __launch_bounds__(kThreads)
+// dbias[n] = the sum over tile rows t of ws[t * cols + n], in a fixed order:
+// each of a block's 8 row groups sums the tile rows g, g + 8, g + 16, ...
+// in increasing order, then the 8 group sums are added in group order. A
+// block covers 32 columns, so each warp reads 128 contiguous bytes of one
+// tile row and a thread has tile_rows / 8 independent loads in flight.
+constexpr int kReduceCols = 32, kReduceGroups = 8;
+__global__ void __launch_bounds__(kReduceCols * kReduceGroups)
 dbias_reduce_kernel(const float *__restrict__ ws, int64_t tile_rows, int64_t cols, void *__restrict__ dbias,
                     int bf16_out) {
     pdl_wait();
     pdl_launch_dependents();
-    const int64_t n = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
-    if (n >= cols) return;
+    __shared__ float part[kReduceGroups][kReduceCols];
+    const int tx = threadIdx.x % kReduceCols, g = threadIdx.x / kReduceCols;
+    const int64_t n = static_cast<int64_t>(blockIdx.x) * kReduceCols + tx;
     float t = 0.0f;
-    for (int64_t r = 0; r < tile_rows; ++r) t = __fadd_rn(t, ws[r * cols + n]);
+    if (n < cols) {
+#pragma unroll 4
+        for (int64_t r = g; r < tile_rows; r += kReduceGroups) t = __fadd_rn(t, ws[r * cols + n]);
+    }
+    part[g][tx] = t;
+    __syncthreads();
+    if (g != 0 || n >= cols) return;
+    t = part[0][tx];
+    for (int j = 1; j < kReduceGroups; ++j) t = __fadd_rn(t, part[j][tx]);
     if (bf16_out)
         static_cast<__nv_bfloat16 *>(dbias)[n] = __float2bfloat16_rn(t);
     else
@@ -378,8 +392,8 @@ int launch_quantize_dbias(const void *x, int x_dtype, int64_t rows, int64_t cols
                   : launch_typed<FP8MP_E5M2, false>(x, rows, cols, scale, out, out_t, amax, s, dev, ws);
     if (rc) return rc;
     const int64_t tile_rows = (rows + 127) >> 7;
-    launch_kernel(dbias_reduce_kernel, dim3(static_cast<unsigned>((cols + kThreads - 1) / kThreads)), dim3(kThreads),
-                  0, s, ws, tile_rows, cols, dbias, dbias_dtype == FP8MP_BF16 ? 1 : 0);
+    launch_kernel(dbias_reduce_kernel, dim3(static_cast<unsigned>((cols + kReduceCols - 1) / kReduceCols)),
+                  dim3(kReduceCols * kReduceGroups), 0, s, ws, tile_rows, cols, dbias, dbias_dtype == FP8MP_BF16 ? 1 : 0);
     const cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess)
         return fail(FP8MP_ERR_LAUNCH, "fp8_quantize_dbias: launch failed: %s", cudaGetErrorString(e));
