@@ -704,9 +704,12 @@ def kernel_table(args):
     one = torch.ones(1, device="cuda")
     one0 = torch.ones((), device="cuda")
     g = workloads.gen(7, "cuda")
+    only = args.only or ""
     with ClockSampler(int(os.environ.get("LOCAL_RANK", "0"))) as clocks:
         # ---- GEMMs: forward, fused backward (ours) and cuBLASLt's
         for name, M, K, N in GEMM_SHAPES:
+            if only not in f"{name} M={M} K={K} N={N}":
+                continue
             xf = (torch.randn(M, K, generator=g, device="cuda") * 4).to(torch.float8_e4m3fn)
             wf = (torch.randn(N, K, generator=g, device="cuda") * 0.1).to(torch.float8_e4m3fn)
             df = (torch.randn(M, N, generator=g, device="cuda") * 1e3).to(torch.float8_e5m2)
@@ -741,9 +744,12 @@ def kernel_table(args):
             del xf, wf, df, x8, w8, d8, y, dx, dw, wtf, dtf, xtf
             torch.cuda.empty_cache()
         # ---- casts (bytes per element: 2 in + 1 out, + 1 for the transposed copy)
-        blk = workloads.transformer_block(device="cuda")
-        mlp = workloads.mlp(device="cuda")
-        for wl, x in (("transformer x 8192x4096 bf16", blk.x), ("mlp down input 16384x14336 bf16", mlp.x_down)):
+        cast_wls = ("transformer x 8192x4096 bf16", "mlp down input 16384x14336 bf16", "transformer dY 8192x4096 bf16")
+        blk = workloads.transformer_block(device="cuda") if any(only in w for w in cast_wls) else None
+        mlp = workloads.mlp(device="cuda") if only in cast_wls[1] else None
+        for wl, x in ((cast_wls[0], blk.x if blk else None), (cast_wls[1], mlp.x_down if mlp else None)):
+            if x is None or only not in wl:
+                continue
             rows, cols = x.shape
             sc = torch.full((1,), 64.0, device="cuda")
             am = torch.zeros(1, device="cuda")
@@ -758,53 +764,59 @@ def kernel_table(args):
                 us = timed(lambda: fp8mp.fp8_quantize_current(x, fp8mp.E4M3, sc, sinv, am, q, None))
                 emit("current scaling: amax pass + scale + cast", wl, us, 5.0 * x.numel(), "hbm")
             del q, qt
-        dy = blk.dy_proj
-        rows, cols = dy.shape
-        q = torch.empty(rows, cols, dtype=torch.uint8, device="cuda")
-        qt = torch.empty(cols, rows, dtype=torch.uint8, device="cuda")
-        db = torch.empty(cols, dtype=torch.float32, device="cuda")
-        ws = torch.empty(fp8mp.fp8_quantize_dbias_workspace_bytes(rows, cols), dtype=torch.uint8, device="cuda")
-        sc, am = torch.full((1,), 2.0 ** 10, device="cuda"), torch.zeros(1, device="cuda")
-        us = timed(lambda: fp8mp.fp8_quantize_dbias(dy, fp8mp.E5M2, sc, q, qt, db, ws, am))
-        emit("cast_rows_t_kernel<DBIAS> + dbias_reduce (E5M2 + transposed copy + bias gradient)",
-             "transformer dY 8192x4096 bf16", us, 4.0 * dy.numel(), "hbm")
-        del blk, mlp, dy, q, qt, db, ws
+        if blk is not None and only in cast_wls[2]:
+            dy = blk.dy_proj
+            rows, cols = dy.shape
+            q = torch.empty(rows, cols, dtype=torch.uint8, device="cuda")
+            qt = torch.empty(cols, rows, dtype=torch.uint8, device="cuda")
+            db = torch.empty(cols, dtype=torch.float32, device="cuda")
+            ws = torch.empty(fp8mp.fp8_quantize_dbias_workspace_bytes(rows, cols), dtype=torch.uint8, device="cuda")
+            sc, am = torch.full((1,), 2.0 ** 10, device="cuda"), torch.zeros(1, device="cuda")
+            us = timed(lambda: fp8mp.fp8_quantize_dbias(dy, fp8mp.E5M2, sc, q, qt, db, ws, am))
+            emit("cast_rows_t_kernel<DBIAS> + dbias_reduce (E5M2 + transposed copy + bias gradient)",
+                 cast_wls[2], us, 4.0 * dy.numel(), "hbm")
+            del dy, q, qt, db, ws
+        del blk, mlp
         torch.cuda.empty_cache()
         # ---- the master step on 1e9 parameters
         n = MASTER_PARAMS
-        w = workloads.master_weights(n, device="cuda")
-        mom = torch.zeros(n, device="cuda")
-        w8 = torch.empty(n, dtype=torch.uint8, device="cuda")
-        grad = workloads.master_step(n, 0, device="cuda")
-        sw, amw = torch.full((1,), 256.0, device="cuda"), torch.zeros(1, device="cuda")
-        S, growth = torch.full((1,), S0, device="cuda"), torch.zeros(1, dtype=torch.int32, device="cuda")
-        found, flag = torch.zeros(1, dtype=torch.int32, device="cuda"), torch.zeros(1, dtype=torch.int32, device="cuda")
         wl = f"optimizer state, {n:.0e} parameters"
-        us = timed(lambda: fp8mp.mp_master_step(grad, w, mom, w8, sw, amw, S, growth, found, LR, MU,
-                                                grad_nonfinite=flag), n=5)
-        emit("prescanned_step_kernel<SgdOpt> (flag from the gradients' producer)", wl, us, 19.0 * n, "hbm")
-        us = timed(lambda: fp8mp.mp_master_step(grad, w, mom, w8, sw, amw, S, growth, found, LR, MU), n=5)
-        emit("fused_step_kernel<SgdOpt> (scans the gradients itself)", wl, us, 21.0 * n, "hbm")
-        bad = grad.clone()
-        bad[12345] = float("inf")
-        us = timed(lambda: fp8mp.mp_master_step(bad, w, mom, w8, sw, amw, S, growth, found, LR, MU), n=5)
-        emit("fused_step_kernel<SgdOpt>, skipped step (an Inf in the gradients)", wl, us, 2.0 * n, "hbm")
-        del bad
-        S.fill_(S0)
-        v2 = torch.zeros(n, device="cuda")
-        bp = torch.ones(2, device="cuda")
-        us = timed(lambda: fp8mp.mp_master_step_adam(grad, w, mom, v2, w8, sw, amw, S, growth, found, bp, LR,
-                                                     grad_nonfinite=flag), n=5)
-        emit("prescanned_step_kernel<AdamOpt>", wl, us, 27.0 * n, "hbm")
-        us = timed(lambda: fp8mp.mp_master_step_adam(grad, w, mom, v2, w8, sw, amw, S, growth, found, bp, LR), n=5)
-        emit("fused_step_kernel<AdamOpt>", wl, us, 29.0 * n, "hbm")
-        del w, mom, w8, grad, v2
-        torch.cuda.empty_cache()
+        if only not in wl:
+            n = 0
+        if n > 0:
+            w = workloads.master_weights(n, device="cuda")
+            mom = torch.zeros(n, device="cuda")
+            w8 = torch.empty(n, dtype=torch.uint8, device="cuda")
+            grad = workloads.master_step(n, 0, device="cuda")
+            sw, amw = torch.full((1,), 256.0, device="cuda"), torch.zeros(1, device="cuda")
+            S, growth = torch.full((1,), S0, device="cuda"), torch.zeros(1, dtype=torch.int32, device="cuda")
+            found, flag = torch.zeros(1, dtype=torch.int32, device="cuda"), torch.zeros(1, dtype=torch.int32, device="cuda")
+            us = timed(lambda: fp8mp.mp_master_step(grad, w, mom, w8, sw, amw, S, growth, found, LR, MU,
+                                                    grad_nonfinite=flag), n=5)
+            emit("prescanned_step_kernel<SgdOpt> (flag from the gradients' producer)", wl, us, 19.0 * n, "hbm")
+            us = timed(lambda: fp8mp.mp_master_step(grad, w, mom, w8, sw, amw, S, growth, found, LR, MU), n=5)
+            emit("fused_step_kernel<SgdOpt> (scans the gradients itself)", wl, us, 21.0 * n, "hbm")
+            bad = grad.clone()
+            bad[12345] = float("inf")
+            us = timed(lambda: fp8mp.mp_master_step(bad, w, mom, w8, sw, amw, S, growth, found, LR, MU), n=5)
+            emit("fused_step_kernel<SgdOpt>, skipped step (an Inf in the gradients)", wl, us, 2.0 * n, "hbm")
+            del bad
+            S.fill_(S0)
+            v2 = torch.zeros(n, device="cuda")
+            bp = torch.ones(2, device="cuda")
+            us = timed(lambda: fp8mp.mp_master_step_adam(grad, w, mom, v2, w8, sw, amw, S, growth, found, bp, LR,
+                                                         grad_nonfinite=flag), n=5)
+            emit("prescanned_step_kernel<AdamOpt>", wl, us, 27.0 * n, "hbm")
+            us = timed(lambda: fp8mp.mp_master_step_adam(grad, w, mom, v2, w8, sw, amw, S, growth, found, bp, LR), n=5)
+            emit("fused_step_kernel<AdamOpt>", wl, us, 29.0 * n, "hbm")
+            del w, mom, w8, grad, v2
+            torch.cuda.empty_cache()
         # ---- the scale update: latency only
-        metas = [fp8mp.Meta(HIST_LEN, f) for f in (fp8mp.E4M3, fp8mp.E4M3, fp8mp.E4M3, fp8mp.E5M2)]
-        us = timed(lambda: fp8mp.delayed_scaling_update(metas, fp8mp.AMAX_MOST_RECENT))
-        print(json.dumps({"kernel": "scale_update_kernel", "workload": f"4 metas, L={HIST_LEN}", "us": round(us, 2),
-                          "roofline": None}), flush=True)
+        if only in f"4 metas, L={HIST_LEN}":
+            metas = [fp8mp.Meta(HIST_LEN, f) for f in (fp8mp.E4M3, fp8mp.E4M3, fp8mp.E4M3, fp8mp.E5M2)]
+            us = timed(lambda: fp8mp.delayed_scaling_update(metas, fp8mp.AMAX_MOST_RECENT))
+            print(json.dumps({"kernel": "scale_update_kernel", "workload": f"4 metas, L={HIST_LEN}",
+                              "us": round(us, 2), "roofline": None}), flush=True)
     print(json.dumps({"clocks": clocks.summary(),
                       "l2": "flushed (2x L2 write, then a 2x L2 read that evicts its dirty lines) before each timed launch",
                       "reps": reps, "warmup": 3}), flush=True)
@@ -828,6 +840,8 @@ def main(argv=None):
     ap.add_argument("--kernels", action="store_true",
                     help="instead of the step: each kernel alone at the other workloads' sizes against its "
                          "roofline (one JSON line each; --steps sets the timed launches per kernel)")
+    ap.add_argument("--only", default=None,
+                    help="with --kernels: only the workloads whose name contains this text (e.g. mlp_up)")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
