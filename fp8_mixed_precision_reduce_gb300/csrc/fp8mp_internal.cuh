@@ -80,7 +80,7 @@ struct GemmDesc {
     const float *out_scale;  // non-null: FP8 output of out_fmt under *out_scale
     int out_fmt;
     int a_mn, b_mn;
-    int32_t *out_nonfinite;  // non-null (bf16 / fp32 output): |= 1 when a stored element is Inf or NaN
+    int32_t *out_nonfinite = nullptr;  // non-null (bf16 / fp32 output): |= 1 when a stored element is Inf or NaN
 };
 // Runs 1 or 2 independent GEMMs in one persistent launch.
 int launch_gemms(const GemmDesc *descs, int n, cudaStream_t s, const DeviceInfo &dev);
