@@ -205,6 +205,8 @@ int fp8_quantize_dbias_noalloc(const void *x, int32_t x_dtype, int64_t rows, int
  *   y[m, n] = (sum_k x8[m, k] * w8[n, k]) * sinv_x[0] * sinv_w[0] + bias[n]
  * accumulated in fp32 on the tensor cores, rounded once to y_dtype.
  *   *y_amax = max(*y_amax, max |y as stored|)                (when y_amax != NULL)
+ * NaN elements are left out of the amax (an E4M3 NaN code in x8 or w8 makes
+ * NaN outputs); an output that overflows to +-Inf counts as Inf.
  *
  * x8  [M x K] E4M3 codes;  w8 [N x K] E4M3 codes (the weight, K contiguous).
  * sinv_x, sinv_w  device pointers to one fp32 each (metas' scale_inv).

@@ -72,6 +72,32 @@ def test_fwd_bias_and_output_amax(cuda_lib, orc, engine, bias_dt, out):
     assert abs(am.item() - np.abs(ref).max()) <= 2.0 ** -8 * np.abs(ref).max() + 1e-5 * ab.max()
 
 
+@pytest.mark.parametrize("out", ["bf16", "f32"])
+def test_fwd_output_amax_leaves_out_nan_and_keeps_inf(cuda_lib, engine, out):
+    """NaN outputs (rows of x8 holding an E4M3 NaN code, and one 16-column
+    group made NaN by a NaN code in w8) are left out of the output amax,
+    which then equals the largest finite |y| stored; outputs that overflow
+    to +-Inf (a row of +448 codes under a large scale product) make it Inf.
+    Ragged tiles (1040 x 784), so masked rows and columns are in play."""
+    M, N, K = 1040, 784, 512
+    rng = np.random.default_rng(11)
+    A = finite_codes(rng, (M, K), E4M3)
+    B = finite_codes(rng, (N, K), E4M3)
+    A[3, 5] = 0x7F     # row 3 of y is NaN
+    A[1031, 0] = 0xFF  # a row in the last, ragged row tile
+    B[40, 7] = 0x7F    # column 40 of y is NaN
+    y, am = fwd(cuda_lib, A, B, 2.0 ** -6, 0.37, out=out, amax0=0.0)
+    yh = np.abs(np_view(y.float()))
+    assert np.isnan(yh[3]).all() and np.isnan(yh[:, 40]).all()
+    assert np.isfinite(np.nanmax(yh)) and am.item() == np.nanmax(yh)
+    # a row of the largest code pushes its outputs past the output type's range
+    A[700, :] = 0x7E   # +448
+    y, am = fwd(cuda_lib, A, B, 2.0 ** 60, 2.0 ** 60, out=out, amax0=0.0)
+    yh = np.abs(np_view(y.float()))
+    assert np.isinf(yh[700]).any()
+    assert am.item() == np.inf and np.nanmax(yh) == np.inf
+
+
 @pytest.mark.parametrize("dy_fmt", [E5M2, E4M3])
 @pytest.mark.parametrize("M,N,K", [(256, 512, 256), (1040, 784, 784), (1024, 768, 768)])
 def test_dgrad_and_wgrad(cuda_lib, orc, engine, dy_fmt, M, N, K):
