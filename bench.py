@@ -863,7 +863,9 @@ def main(argv=None):
 
     fp8mp.load()  # raises when the library is missing: no fallback
     if args.kernels:
-        kernel_table(args)
+        # one GPU's table: under torchrun only rank 0 measures, the others exit
+        if int(os.environ.get("RANK", "0")) == 0:
+            kernel_table(args)
         return 0
     world, rank, local = dist_setup()
     out = run_ours(args, world, rank, local)
