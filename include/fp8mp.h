@@ -151,8 +151,10 @@ int fp8_quantize_current(const void *x, int32_t x_dtype, int64_t rows, int64_t c
  *                        fp8_linear_bwd_rowmajor needs no transposed copy);
  *   dbias[c] = sum_r x[r, c]  over the unscaled input, fp32 accumulation in
  *                             a fixed order (deterministic): each 128-row
- *                             block's column sums, then the blocks in order;
- *                             rounded once to dbias_dtype.
+ *                             block's column sums; those of every 8th block
+ *                             (blocks g, g + 8, ...) added in order, then the
+ *                             8 partial sums in order of g; rounded once to
+ *                             dbias_dtype.
  * workspace  device scratch of at least fp8_quantize_dbias_workspace_bytes
  *            (rows, cols) bytes, 16-byte aligned, owned by the caller; its
  *            contents on entry do not matter and on exit are unspecified.
