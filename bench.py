@@ -243,7 +243,8 @@ class LinearStep:
         # the weight's first E4M3 copy (and its amax for the first update)
         fp8mp.fp8_quantize(self.master, E4, self.mw.scale, self.W8, None, self.mw.cur_amax)
         # 2 casts, the fwd GEMM, the fused dgrad + wgrad GEMM, 1 scale update, and the master step: one
-        # kernel after a 4-byte memset (three kernels when it scans dW itself with FP8MP_FUSED_MASTER=0)
+        # kernel on the epilogue's flag (scanning dW itself: a 4-byte memset and one kernel, or three
+        # kernels with FP8MP_FUSED_MASTER=0)
         self.launches_per_step = 6 if prescanned or os.environ.get("FP8MP_FUSED_MASTER", "1") != "0" else 8
 
     def step(self, gemm_events=None, io=None):

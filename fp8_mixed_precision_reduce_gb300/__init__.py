@@ -292,9 +292,10 @@ def mp_master_step(grad_bf16: torch.Tensor, master: torch.Tensor, momentum: torc
                    lr: float, momentum_coef: float, backoff: float = 0.5, growth_factor: float = 2.0,
                    growth_interval: int = 2000, stream=None, grad_nonfinite: torch.Tensor | None = None) -> None:
     """Unscale, overflow skip, FP32 SGD-momentum update and E4M3 re-cast, in place.
-    With grad_nonfinite (int32[1] on the device, set by the gradients' producer,
-    e.g. fp8_linear_bwd_rowmajor's dw_nonfinite) the step reads that flag
-    instead of scanning the gradients, and resets it to 0."""
+    With grad_nonfinite (int32[1] on the device holding 0 or 1, set by the
+    gradients' producer, e.g. fp8_linear_bwd_rowmajor's dw_nonfinite) the step
+    reads that flag instead of scanning the gradients, writes it to found_inf
+    and resets it to 0."""
     n = grad_bf16.numel()
     if grad_nonfinite is not None:
         _check(load().mp_master_step_prescanned(_ptr(grad_bf16), n, _ptr(master), _ptr(momentum), _ptr(w8),

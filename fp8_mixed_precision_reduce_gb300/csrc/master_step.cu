@@ -371,19 +371,19 @@ __global__ void __launch_bounds__(kThreads) fused_step_kernel(const StepCommon c
 // FP8MP_FUSED_MASTER=0 selects the three-launch version (read per call, so
 // tests can run both).
 // The step when the gradients' producer has already looked for Inf/NaN
-// (*grad_nonfinite nonzero iff it found one, e.g. the wgrad GEMM epilogue):
-// no scan pass and no barrier, so a plain launch. found_inf is 0 on entry
-// (zeroed on the stream); each block adds 2 when it is done, and the last
-// block does the bookkeeping, sets found_inf to the flag and resets
-// *grad_nonfinite to 0 for the next producer (every block read it before
-// its own arrival).
+// (*grad_nonfinite is 1 iff it found one, else 0, e.g. the wgrad GEMM
+// epilogue's flag): no scan pass and no barrier, so a plain launch, and no
+// memset before it. Each block reads bit 0 of the flag word and adds 2 to
+// the word when it is done (the count never touches bit 0); the last block
+// does the bookkeeping, writes found_inf and resets the word to 0 for the
+// next producer.
 template <class Opt, class Args, class Extra>
 __global__ void __launch_bounds__(kThreads)
 prescanned_step_kernel(const StepCommon c, const Args a, const Extra x, int32_t *grad_nonfinite) {
     pdl_wait();
     pdl_launch_dependents();
     __shared__ int s_skip;
-    if (threadIdx.x == 0) s_skip = *reinterpret_cast<volatile int32_t *>(grad_nonfinite) != 0;
+    if (threadIdx.x == 0) s_skip = (*reinterpret_cast<volatile int32_t *>(grad_nonfinite) & 1) != 0;
     __syncthreads();
     float am = 0.0f;
     if (!s_skip) {
@@ -393,7 +393,7 @@ prescanned_step_kernel(const StepCommon c, const Args a, const Extra x, int32_t 
     block_amax_atomic(am, c.amax_w);
     if (threadIdx.x == 0) {
         __threadfence();
-        const int32_t prev = atomicAdd(c.found_inf, 2);
+        const int32_t prev = atomicAdd(grad_nonfinite, 2);
         if ((prev >> 1) == static_cast<int32_t>(gridDim.x) - 1) {
             __threadfence();
             const int found = s_skip;
@@ -431,8 +431,11 @@ FusedGrid g_fused[64];
 template <class Opt, class Args, class Extra>
 int launch_step(const StepCommon &c, const Args &a, const Extra &x, int which, cudaStream_t s, const DeviceInfo &dev,
                 const char *fn, int32_t *grad_nonfinite = nullptr) {
-    cudaError_t e = cudaMemsetAsync(c.found_inf, 0, sizeof(int32_t), s);
-    if (e != cudaSuccess) return fail(FP8MP_ERR_LAUNCH, "%s: memset failed: %s", fn, cudaGetErrorString(e));
+    cudaError_t e = cudaSuccess;
+    if (grad_nonfinite == nullptr) {  // the scanning steps count arrivals in found_inf
+        e = cudaMemsetAsync(c.found_inf, 0, sizeof(int32_t), s);
+        if (e != cudaSuccess) return fail(FP8MP_ERR_LAUNCH, "%s: memset failed: %s", fn, cudaGetErrorString(e));
+    }
     const int64_t nvec = c.n >> 3;
     int64_t blocks = (nvec + kThreads - 1) / kThreads;
     if (blocks < 1) blocks = 1;

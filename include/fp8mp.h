@@ -398,10 +398,13 @@ int mp_master_step_adam(const uint16_t *grad_bf16, int64_t n, float *master, flo
  * (fp8_linear_bwd_rowmajor's dw_nonfinite): the same results bit for bit,
  * with found_inf taken from the flag instead of a scan of the gradients
  * (which saves a 2-byte-per-parameter pass and the grid barrier).
- *   grad_nonfinite  device int32, in/out: nonzero iff some gradient element
- *                   is Inf or NaN. The step copies it (as 0 / 1) into
- *                   *found_inf and then sets it to 0 for the next producer.
- *                   It must not be found_inf itself.
+ *   grad_nonfinite  device int32, in/out: 1 iff some gradient element is
+ *                   Inf or NaN, else 0 (the producer ORs 1 into a word that
+ *                   was 0). During the launch the step counts its blocks in
+ *                   the word's upper bits; it writes the flag into
+ *                   *found_inf (whatever that held: no memset precedes
+ *                   this step) and leaves the word at 0 for the next
+ *                   producer. It must not be found_inf itself.
  * Other arguments and results as mp_master_step / mp_master_step_adam.
  */
 int mp_master_step_prescanned(const uint16_t *grad_bf16, int64_t n, float *master, float *momentum,

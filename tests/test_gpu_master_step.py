@@ -152,6 +152,7 @@ def test_prescanned_steps_bit_exact(cuda_lib, orc, opt, n):
         g = workloads.master_step(n, step, seed=n + 7, inject=(step == 1), inject_frac=1e-3)
         gb = np_view(g)
         flag.fill_(int(((gb & 0x7F80) == 0x7F80).any()))
+        ds.found.fill_(0x5A5A)  # no memset precedes this step: found_inf is written whatever it held
         ds.scale_w.fill_(32.0)
         if opt == "sgd":
             cuda_lib.mp_master_step(g.cuda(), ds.w, ds.v, ds.w8, ds.scale_w, ds.amax_w, ds.S, ds.growth, ds.found,
