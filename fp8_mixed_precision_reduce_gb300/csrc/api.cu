@@ -13,6 +13,19 @@
 namespace fp8mp {
 
 namespace {
+__global__ void zero_word_kernel(uint32_t *word) {
+    pdl_wait();  // the previous kernel may still read or write the word
+    *word = 0u;
+    pdl_launch_dependents();
+}
+}  // namespace
+
+cudaError_t launch_zero_word(void *word, cudaStream_t s) {
+    return launch_kernel(zero_word_kernel, dim3(1), dim3(1), 0, s, static_cast<uint32_t *>(word));
+}
+
+
+namespace {
 thread_local char g_last_error[512] = {0};
 }
 

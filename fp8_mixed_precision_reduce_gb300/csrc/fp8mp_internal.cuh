@@ -52,6 +52,11 @@ cudaError_t launch_kernel(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_
     return cudaLaunchKernelEx(&cfg, kernel, static_cast<Args &&>(args)...);
 }
 
+// Zeroes one 32-bit word on the stream with a one-thread kernel launched like
+// the library's others, so a programmatic-launch chain is not broken the way
+// a memset node breaks it (the kernel waits for the previous grid first).
+cudaError_t launch_zero_word(void *word, cudaStream_t s);
+
 // Launchers (return FP8MP_* codes; arguments already validated).
 int launch_quantize_current(const void *x, int x_dtype, int64_t rows, int64_t cols, int fmt, int margin,
                             float *scale, float *scale_inv, float *amax, uint8_t *out, uint8_t *out_t,

@@ -432,9 +432,9 @@ template <class Opt, class Args, class Extra>
 int launch_step(const StepCommon &c, const Args &a, const Extra &x, int which, cudaStream_t s, const DeviceInfo &dev,
                 const char *fn, int32_t *grad_nonfinite = nullptr) {
     cudaError_t e = cudaSuccess;
-    if (grad_nonfinite == nullptr) {  // the scanning steps count arrivals in found_inf
-        e = cudaMemsetAsync(c.found_inf, 0, sizeof(int32_t), s);
-        if (e != cudaSuccess) return fail(FP8MP_ERR_LAUNCH, "%s: memset failed: %s", fn, cudaGetErrorString(e));
+    if (grad_nonfinite == nullptr) {  // the scanning steps count arrivals in found_inf: zero it
+        e = launch_zero_word(c.found_inf, s);
+        if (e != cudaSuccess) return fail(FP8MP_ERR_LAUNCH, "%s: launch failed: %s", fn, cudaGetErrorString(e));
     }
     const int64_t nvec = c.n >> 3;
     int64_t blocks = (nvec + kThreads - 1) / kThreads;
