@@ -32,6 +32,8 @@ roofline come from K more steps with timing events around the GEMM launches
 (an event between two kernels serialises them and costs the step ~20 us).
 
 --impl reference times the CPU oracle on a bounded sample of the same step.
+--kernels prints, instead of the step's line, one line per kernel timed alone
+at the other workloads' sizes against its roofline (--only selects some).
 """
 
 from __future__ import annotations
