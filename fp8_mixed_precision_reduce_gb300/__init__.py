@@ -166,9 +166,10 @@ def fp8_quantize_dbias(dy: torch.Tensor, fmt: int, scale: torch.Tensor, out: tor
                        out_t: torch.Tensor | None, dbias: torch.Tensor, workspace: torch.Tensor,
                        amax: torch.Tensor | None = None, stream=None) -> None:
     """Cast of an output gradient (+ optional transposed copy, + amax) that
-    also writes the bias gradient dbias = column sums of dy. `workspace` is a
-    device buffer of at least fp8_quantize_dbias_workspace_bytes(rows, cols)
-    bytes."""
+    also writes the bias gradient dbias = column sums of dy, in one launch.
+    `workspace` is a device buffer of at least
+    fp8_quantize_dbias_workspace_bytes(rows, cols) bytes, zero-filled before
+    its first use; every call leaves it zero again."""
     rows, cols = _rows_cols(dy)
     _check(load().fp8_quantize_dbias(_ptr(dy), _dtype_code(dy), rows, cols, fmt, _ptr(scale), _ptr(out),
                                      _ptr(out_t), _ptr(amax), _ptr(dbias), _dtype_code(dbias),
@@ -183,9 +184,10 @@ def fp8_quantize_dbias_noalloc(dy: torch.Tensor, fmt: int, scale: torch.Tensor, 
                                out_t: torch.Tensor, dbias: torch.Tensor, amax: torch.Tensor | None = None,
                                stream=None) -> None:
     """fp8_quantize_dbias without a workspace, for callers that cannot
-    allocate device memory: the partial sums live in a fixed 4 MiB array in
-    the library (ceil(rows/128) * cols <= 2^20). The first call on a device
-    looks up that array's address; calls that overlap on the GPU race on it."""
+    allocate device memory: the partial sums and counters live in a fixed
+    4 MiB array in the library (fp8_quantize_dbias_workspace_bytes(rows, cols)
+    <= 4 MiB). The first call on a device looks up that array's address;
+    calls that overlap on the GPU race on it."""
     rows, cols = _rows_cols(dy)
     _check(load().fp8_quantize_dbias_noalloc(_ptr(dy), _dtype_code(dy), rows, cols, fmt, _ptr(scale), _ptr(out),
                                              _ptr(out_t), _ptr(amax), _ptr(dbias), _dtype_code(dbias),

@@ -200,7 +200,13 @@ int fp8_quantize_current(const void *x, int32_t x_dtype, int64_t rows, int64_t c
 
 int64_t fp8_quantize_dbias_workspace_bytes(int64_t rows, int64_t cols) {
     if (rows < 0 || cols < 0) return -1;
-    return ((rows + 127) / 128) * cols * static_cast<int64_t>(sizeof(float));
+    if (rows > (1ll << 40) / (cols > 0 ? cols : 1)) return -1;
+    // the column sums of each of the k CTAs of a strip, then one arrival
+    // counter per 128-column strip
+    const int64_t bytes = static_cast<int64_t>(dbias_ctas_per_strip(rows, cols)) * cols *
+                              static_cast<int64_t>(sizeof(float)) +
+                          ((cols + 127) / 128) * static_cast<int64_t>(sizeof(uint32_t));
+    return (bytes + 15) & ~static_cast<int64_t>(15);
 }
 
 int fp8_quantize_dbias(const void *x, int32_t x_dtype, int64_t rows, int64_t cols, int32_t fmt, const float *scale,
@@ -215,6 +221,7 @@ int fp8_quantize_dbias(const void *x, int32_t x_dtype, int64_t rows, int64_t col
     REQUIRE(rows <= (1ll << 40) / (cols > 0 ? cols : 1), "%s: tensor too large", fn);
     REQUIRE(rows % 16 == 0 && cols % 16 == 0, "%s: rows and cols must be multiples of 16 (got %lld x %lld)", fn,
             (long long)rows, (long long)cols);
+    REQUIRE(rows < (1ll << 31) && cols < (1ll << 31), "%s: rows and cols must be below 2^31", fn);
     if (cols == 0) return FP8MP_OK;
     CHECK_PTR(dbias, true);
     const int64_t need = fp8_quantize_dbias_workspace_bytes(rows, cols);
@@ -565,12 +572,16 @@ int fp8mp_check(void *stream) {
     clear_error();
     cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return fail(FP8MP_ERR_LAUNCH, "stream synchronize failed: %s", cudaGetErrorString(e));
-    unsigned int flag = 0, mflag = 0;
+    unsigned int flag = 0, mflag = 0, cflag = 0;
     int rc = read_and_clear_timeout_flag(&flag);
     if (rc) return rc;
     rc = read_and_clear_master_timeout_flag(&mflag);
     if (rc) return rc;
+    rc = read_and_clear_cast_timeout_flag(&cflag);
+    if (rc) return rc;
     if (flag) return fail(FP8MP_ERR_TIMEOUT, "a GEMM kernel's bounded wait expired; its output is undefined");
+    if (cflag)
+        return fail(FP8MP_ERR_TIMEOUT, "the bias-gradient cast's bounded wait expired; its outputs are undefined");
     if (mflag)
         return fail(FP8MP_ERR_TIMEOUT, "the master step's bounded grid barrier expired; the step's results are "
                                        "undefined");

@@ -61,6 +61,10 @@ cudaError_t launch_zero_word(void *word, cudaStream_t s);
 int launch_quantize_current(const void *x, int x_dtype, int64_t rows, int64_t cols, int fmt, int margin,
                             float *scale, float *scale_inv, float *amax, uint8_t *out, uint8_t *out_t,
                             cudaStream_t s, const DeviceInfo &dev);
+// CTAs per 128-column strip of the bias-gradient cast (a function of the
+// shape only, so the column sums' order is too): its workspace holds that
+// many rows of column sums, then one arrival counter per strip.
+int dbias_ctas_per_strip(int64_t rows, int64_t cols);
 int launch_quantize_dbias(const void *x, int x_dtype, int64_t rows, int64_t cols, int fmt, const float *scale,
                           uint8_t *out, uint8_t *out_t, float *amax, void *dbias, int dbias_dtype, float *ws,
                           cudaStream_t s, const DeviceInfo &dev);
@@ -112,6 +116,8 @@ int launch_timeout_selftest(cudaStream_t s);
 int read_and_clear_timeout_flag(unsigned int *value);
 // Enqueues the one-block kernel whose grid-barrier wait is meant to run out.
 int launch_barrier_selftest(cudaStream_t s);
+// Reads and clears the tiled casts' wait-timeout flag.
+int read_and_clear_cast_timeout_flag(unsigned int *value);
 // Reads and clears the fused master step's barrier-timeout flag.
 int read_and_clear_master_timeout_flag(unsigned int *value);
 const char *last_error_message();

@@ -48,15 +48,12 @@
 // device flag that fp8mp_check() reports, tells the other roles of its CTA
 // to stop, waits (bounded) for its own copies / MMAs in flight, and the CTA
 // frees its TMEM and returns.
-#include <cuda.h>
-#include <cudaTypedefs.h>
-
 #include <atomic>
 #include <cstdlib>
 #include <cstring>
 #include <mutex>
 
-#include "fp8mp_internal.cuh"
+#include "fp8mp_async.cuh"
 
 namespace fp8mp {
 
@@ -72,8 +69,6 @@ constexpr int NUM_EPI_WARPS = 4;
 constexpr int NUM_THREADS = 64 + 32 * NUM_EPI_WARPS;
 constexpr int GROUP_M = 16;       // tile raster: 16 row-blocks per group
 constexpr uint32_t TMEM_COLS = 2 * TILE_N;
-constexpr long long kWaitLimitCycles = 4000000000ll;  // about 2 s at the SM clock
-constexpr uint32_t kSuspendHintNs = 1000000u;          // longest single sleep inside try_wait
 
 template <bool PAIR>
 struct Cfg {
@@ -135,34 +130,9 @@ struct GemmBatch {
 
 // ------------------------------------------------------------ PTX wrappers
 
-__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
-    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
-}
-__device__ __forceinline__ void fence_mbar_init() {
-    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-}
-__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
-    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
-}
-__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
-    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
-}
 // Arrive on an mbarrier given by its shared::cluster address (any CTA of the cluster).
 __device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr) {
     asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
-}
-// Tests the phase; if it is not complete the thread sleeps in hardware until
-// it completes or kSuspendHintNs pass (no spinning on the issue slots).
-__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
-    uint32_t ok;
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
-        "selp.u32 %0, 1, 0, p;\n\t}"
-        : "=r"(ok)
-        : "r"(bar), "r"(parity), "r"(kSuspendHintNs)
-        : "memory");
-    return ok != 0;
 }
 __device__ __forceinline__ uint32_t cluster_ctarank() {
     uint32_t r;
@@ -179,24 +149,9 @@ __device__ __forceinline__ void cluster_sync_all() {
     asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
 
-// Waits until the phase of parity `parity` of `bar` has completed. Returns
-// false if another role has raised `abort_flag` or if about kWaitLimitCycles
-// SM cycles elapse (then raises both flags).
-__device__ __noinline__ bool wait_bounded_slow(uint32_t bar, uint32_t parity, volatile int *abort_flag) {
-    const long long t0 = clock64();
-    for (;;) {
-        if (mbar_try_wait(bar, parity)) return true;
-        if (*abort_flag) return false;
-        if (clock64() - t0 > kWaitLimitCycles) {
-            *abort_flag = 1;
-            atomicOr(&g_gemm_timeout_flag, 1u);
-            return false;
-        }
-    }
-}
+// The shared bounded wait, reporting through the GEMM's timeout flag.
 __device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity, volatile int *abort_flag) {
-    if (mbar_try_wait(bar, parity)) return true;
-    return wait_bounded_slow(bar, parity, abort_flag);
+    return fp8mp::wait_bounded(bar, parity, abort_flag, &g_gemm_timeout_flag);
 }
 
 // TMA 2-D tile load into this CTA's shared memory; completion is counted on
@@ -235,9 +190,6 @@ __device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wa
 __device__ __forceinline__ void fence_proxy_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
 __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
     asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d) : "memory");
-}
-__device__ __forceinline__ void prefetch_tmap(const CUtensorMap *map) {
-    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
 }
 
 template <bool PAIR>
@@ -803,24 +755,10 @@ __global__ void fill_bias_kernel(int64_t rows, int64_t cols, const void *bias, i
 
 // ------------------------------------------------------------- host side
 
-PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
-    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-    static std::once_flag once;
-    std::call_once(once, [] {
-        void *ptr = nullptr;
-        cudaDriverEntryPointQueryResult q;
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
-                cudaSuccess &&
-            q == cudaDriverEntryPointSuccess)
-            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
-    });
-    return fn;
-}
-
 // Output tensor [rows x cols] of bf16, fp32 or FP8 bytes, box 32 rows x 128
 // bytes, 128-byte swizzle.
 int make_out_tmap(CUtensorMap *map, void *ptr, uint64_t cols, uint64_t rows, bool bf16, bool fp8 = false) {
-    auto enc = encode_fn();
+    auto enc = tensor_map_encoder();
     if (enc == nullptr) return fail(FP8MP_ERR_LAUNCH, "cuTensorMapEncodeTiled is not available");
     const uint64_t esize = fp8 ? 1 : (bf16 ? 2 : 4);
     const cuuint64_t dims[2] = {cols, rows};
@@ -842,7 +780,7 @@ int make_out_tmap(CUtensorMap *map, void *ptr, uint64_t cols, uint64_t rows, boo
 // A K-major operand has inner = kc, outer = its rows (box: the tile's rows);
 // an MN-major one has inner = its rows, outer = kc (box: 128 k-rows).
 int make_tmap(CUtensorMap *map, const void *ptr, uint64_t inner, uint64_t outer, uint32_t box_outer) {
-    auto enc = encode_fn();
+    auto enc = tensor_map_encoder();
     if (enc == nullptr) return fail(FP8MP_ERR_LAUNCH, "cuTensorMapEncodeTiled is not available");
     const cuuint64_t dims[2] = {inner, outer};
     const cuuint64_t strides[1] = {inner};
@@ -1055,6 +993,20 @@ int read_and_clear_timeout_flag(unsigned int *value) {
     if (e != cudaSuccess) return fail(FP8MP_ERR_LAUNCH, "reading the timeout flag failed: %s", cudaGetErrorString(e));
     *value = v;
     return FP8MP_OK;
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *ptr = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+    });
+    return fn;
 }
 
 }  // namespace fp8mp

@@ -10,10 +10,14 @@
 // array compiled into the library instead of a caller-provided workspace.
 //
 // The scratch is the file-scope array below: 2^20 floats (4 MiB), held by
-// every GPU that loads the library until the process exits. On the host its
-// name is only a host-side stand-in, so the device address is looked up once
-// per device with cudaGetSymbolAddress (with that device current) on the
-// first call on that device, and passed to the kernels.
+// every GPU that loads the library until the process exits. It holds the
+// per-tile column sums and, after them, the column strips' arrival counters.
+// The loader zero-fills it, and every call leaves what it used zero again,
+// so the counters start at zero on every call. On the host its name is only
+// a host-side stand-in, so the device address is looked up once per device
+// with cudaGetSymbolAddress (with that device current) on the first call on
+// that device, and passed to the kernel. That cached address is not
+// refreshed after cudaDeviceReset (the header says so).
 #include <mutex>
 
 #include "fp8mp_internal.cuh"
@@ -53,12 +57,14 @@ extern "C" int fp8_quantize_dbias_noalloc(const void *x, int32_t x_dtype, int64_
     const char *fn = "fp8_quantize_dbias_noalloc";
     clear_error();
     if (rows < 0 || cols < 0) return fail(FP8MP_ERR_INVALID, "%s: negative size", fn);
+    // bound the shape before the size product can overflow (the workspace
+    // size is -1 for a tensor beyond 2^40 elements)
     const int64_t need = fp8_quantize_dbias_workspace_bytes(rows, cols);
     const int64_t have = static_cast<int64_t>(FP8MP_NOALLOC_DBIAS_SCRATCH_FLOATS) * static_cast<int64_t>(sizeof(float));
-    if (need > have)
+    if (need < 0 || need > have)
         return fail(FP8MP_ERR_INVALID,
-                    "%s: %lld x %lld needs %lld scratch bytes (ceil(rows/128) * cols floats) but the fixed "
-                    "scratch array holds %lld; use fp8_quantize_dbias with a workspace",
+                    "%s: %lld x %lld needs %lld scratch bytes (ceil(rows/128) * cols floats and ceil(cols/128) "
+                    "counters) but the fixed scratch array holds %lld; use fp8_quantize_dbias with a workspace",
                     fn, (long long)rows, (long long)cols, (long long)need, (long long)have);
     float *ws = nullptr;
     if (rows > 0 && cols > 0) {
@@ -68,8 +74,9 @@ extern "C" int fp8_quantize_dbias_noalloc(const void *x, int32_t x_dtype, int64_
         const int rs = scratch_address(dev.device, &ws);
         if (rs) return rs;
     }
-    // The cast kernel writes every partial sum the reduction reads, so the
-    // scratch needs no clearing; the validated entry point does the rest.
+    // The array is zero on entry (zero-filled at load, and every call leaves
+    // what it used zero), as the workspace contract asks; the validated entry
+    // point does the rest.
     return fp8_quantize_dbias(x, x_dtype, rows, cols, fmt, scale, out, out_t, amax, dbias, dbias_dtype, ws,
                               ws != nullptr ? have : 0, stream);
 }

@@ -11,9 +11,17 @@
 // 2 or 4, output 1, transposed output 1). Loads and stores are 16 bytes wide
 // and coalesced; the amax is a per-thread max, a warp-shuffle max and one
 // atomic max per block.
-#include "fp8mp_internal.cuh"
+#include <atomic>
+#include <mutex>
+
+#include "fp8mp_async.cuh"
 
 namespace fp8mp {
+
+// Raised by a tiled cast whose bounded mbarrier wait ran out; fp8mp_check()
+// reads and clears it.
+__device__ unsigned int g_cast_timeout_flag = 0;
+
 namespace {
 
 constexpr int kThreads = 256;
@@ -40,26 +48,6 @@ __device__ __forceinline__ void load16(const void *x, int64_t chunk, float f[16]
             f[4 * i + 2] = v.z;
             f[4 * i + 3] = v.w;
         }
-    }
-}
-
-// 8 consecutive elements of row `r` starting at column `c`.
-template <bool BF16>
-__device__ __forceinline__ void load8(const void *x, int64_t cols, int64_t r, int64_t c, float f[8]) {
-    const int64_t e = r * cols + c;
-    if constexpr (BF16) {
-        const uint4 a = __ldcs(reinterpret_cast<const uint4 *>(reinterpret_cast<const uint16_t *>(x) + e));
-        const uint32_t w[4] = {a.x, a.y, a.z, a.w};
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            f[2 * i] = __uint_as_float(w[i] << 16);
-            f[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
-        }
-    } else {
-        const float4 *p = reinterpret_cast<const float4 *>(reinterpret_cast<const float *>(x) + e);
-        const float4 a = __ldcs(p), b = __ldcs(p + 1);
-        f[0] = a.x; f[1] = a.y; f[2] = a.z; f[3] = a.w;
-        f[4] = b.x; f[5] = b.y; f[6] = b.z; f[7] = b.w;
     }
 }
 
@@ -116,11 +104,19 @@ __device__ __forceinline__ uint32_t cast4_bf16(uint32_t w0, uint32_t w1, float s
                       __uint_as_float(w1 & 0xFFFF0000u), scale, am, probe);
 }
 
-// Row-major cast of a flat array of n elements: chunks of 16 elements give
-// one 16-byte store; the n % 16 tail is done element by element. Eight
-// blocks of 256 threads fit an SM (32 registers a thread).
+// Row-major cast of a flat array of n elements in chunks of 16 elements (one
+// 16-byte store of codes each). Block b owns the kChunksPerThread * 256
+// consecutive chunks from b * kChunksPerThread * 256 on; thread t takes
+// chunks t, t + 256, ... of them (each load and store instruction of a warp
+// is one coalesced 512-byte (bf16) or 1 KB (fp32) access) and issues all of
+// its loads before it converts anything, so a resident block keeps 32 KB
+// (bf16) in flight. The grid has one block per such run: small, equal
+// blocks that the block scheduler deals out to SMs as they free up. The
+// n % 16 tail is done element by element by the last block.
+constexpr int kChunksPerThread = 4;
+
 template <int FMT, bool BF16>
-__global__ void __launch_bounds__(kThreads, 8)
+__global__ void __launch_bounds__(kThreads, 4)
 cast_rows_kernel(const void *__restrict__ x, int64_t n, const float *__restrict__ scale_p,
                  uint8_t *__restrict__ out, float *__restrict__ amax_p) {
     pdl_wait();
@@ -128,29 +124,64 @@ cast_rows_kernel(const void *__restrict__ x, int64_t n, const float *__restrict_
     const float scale = __ldg(scale_p);
     float am = 0.0f;
     const int64_t nchunk = n >> 4;
-    const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
-    for (int64_t c = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; c < nchunk; c += stride) {
-        uint32_t o[4], probe = 0;
-        if constexpr (BF16) {
-            const uint4 *p = reinterpret_cast<const uint4 *>(x) + 2 * c;
-            const uint4 a = __ldcs(p), b = __ldcs(p + 1);
-            o[0] = cast4_bf16<FMT>(a.x, a.y, scale, am, probe);
-            o[1] = cast4_bf16<FMT>(a.z, a.w, scale, am, probe);
-            o[2] = cast4_bf16<FMT>(b.x, b.y, scale, am, probe);
-            o[3] = cast4_bf16<FMT>(b.z, b.w, scale, am, probe);
-        } else {
-            const float4 *p = reinterpret_cast<const float4 *>(x) + 4 * c;
+    const int64_t c0 = static_cast<int64_t>(blockIdx.x) * (kChunksPerThread * kThreads) + threadIdx.x;
+    if constexpr (BF16) {
+        uint4 raw[kChunksPerThread][2];
 #pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                const float4 v = __ldcs(p + j);
-                o[j] = cast4<FMT>(v.x, v.y, v.z, v.w, scale, am, probe);
+        for (int u = 0; u < kChunksPerThread; ++u) {
+            const int64_t c = c0 + u * kThreads;
+            if (c < nchunk) {
+                const uint4 *p = reinterpret_cast<const uint4 *>(x) + 2 * c;
+                raw[u][0] = __ldcs(p);
+                raw[u][1] = __ldcs(p + 1);
             }
         }
-        if (probe & 0x80808080u) {
 #pragma unroll
-            for (int j = 0; j < 4; ++j) o[j] = canonical_nan<FMT>(o[j]);
+        for (int u = 0; u < kChunksPerThread; ++u) {
+            const int64_t c = c0 + u * kThreads;
+            if (c < nchunk) {
+                uint32_t o[4], probe = 0;
+                o[0] = cast4_bf16<FMT>(raw[u][0].x, raw[u][0].y, scale, am, probe);
+                o[1] = cast4_bf16<FMT>(raw[u][0].z, raw[u][0].w, scale, am, probe);
+                o[2] = cast4_bf16<FMT>(raw[u][1].x, raw[u][1].y, scale, am, probe);
+                o[3] = cast4_bf16<FMT>(raw[u][1].z, raw[u][1].w, scale, am, probe);
+                if (probe & 0x80808080u) {
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) o[j] = canonical_nan<FMT>(o[j]);
+                }
+                reinterpret_cast<uint4 *>(out)[c] = make_uint4(o[0], o[1], o[2], o[3]);
+            }
         }
-        reinterpret_cast<uint4 *>(out)[c] = make_uint4(o[0], o[1], o[2], o[3]);
+    } else {
+        // fp32: two chunks (eight 16-byte loads) at a time
+#pragma unroll
+        for (int h = 0; h < kChunksPerThread; h += 2) {
+            float4 raw[2][4];
+#pragma unroll
+            for (int u = 0; u < 2; ++u) {
+                const int64_t c = c0 + (h + u) * kThreads;
+                if (c < nchunk) {
+                    const float4 *p = reinterpret_cast<const float4 *>(x) + 4 * c;
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) raw[u][j] = __ldcs(p + j);
+                }
+            }
+#pragma unroll
+            for (int u = 0; u < 2; ++u) {
+                const int64_t c = c0 + (h + u) * kThreads;
+                if (c < nchunk) {
+                    uint32_t o[4], probe = 0;
+#pragma unroll
+                    for (int j = 0; j < 4; ++j)
+                        o[j] = cast4<FMT>(raw[u][j].x, raw[u][j].y, raw[u][j].z, raw[u][j].w, scale, am, probe);
+                    if (probe & 0x80808080u) {
+#pragma unroll
+                        for (int j = 0; j < 4; ++j) o[j] = canonical_nan<FMT>(o[j]);
+                    }
+                    reinterpret_cast<uint4 *>(out)[c] = make_uint4(o[0], o[1], o[2], o[3]);
+                }
+            }
+        }
     }
     if (blockIdx.x == gridDim.x - 1) {
         for (int64_t i = (nchunk << 4) + threadIdx.x; i < n; i += blockDim.x) {
@@ -162,185 +193,533 @@ cast_rows_kernel(const void *__restrict__ x, int64_t n, const float *__restrict_
     if (amax_p != nullptr) block_amax_atomic(am, amax_p);
 }
 
-// Row-major + transposed cast of one 128 x 128 tile per block.
-// Phase 1: each thread converts a 4-row x 8-column patch (16-byte loads),
-// stores its row-major bytes, transposes the 4 x 8 bytes in registers into
-// eight 4-byte column words and parks them in shared memory, where word
-// (column cc, row-group g) sits at index cc * 32 + (g ^ 2 * ((cc >> 3) & 15))
-// -- the XOR spreads one store instruction of a warp over all 32 banks.
-// Phase 2: each thread reads 16 consecutive row bytes of one column (one
-// 16-byte shared load, un-permuting the XOR) and writes them to out_t, so a
-// warp writes four full 128-byte rows of out_t.
-// With DBIAS the kernel also sums its 128 rows per column (fp32, fixed order:
-// each thread its 8 rows in row order, then the 16 row groups in order) and
-// writes the 128 column sums of its tile to ws[tile_row * cols + col]; then
-// out_t may be NULL (no transposed copy: phase 2 is skipped).
-template <int FMT, bool BF16, bool DBIAS>
-__global__ void __launch_bounds__(kThreads)
+// Blocks of cast_rows_kernel / amax_kernel for n elements: one per run of
+// kChunksPerThread * 256 chunks, at least one (the last block also does the
+// n % 16 tail).
+inline int64_t row_blocks(int64_t n) {
+    const int64_t per_block = static_cast<int64_t>(kChunksPerThread) * kThreads;
+    const int64_t blocks = ((n >> 4) + per_block - 1) / per_block;
+    return blocks < 1 ? 1 : blocks;
+}
+
+// Row-major + transposed cast of one 128 x 128 tile per block of 256 threads.
+// Thread t covers rows r0 + 4 * (t >> 3) .. + 3 and columns c0 + 16 * (t & 7)
+// .. + 15: it issues the loads of its whole 4 x 16 patch first (eight 16-byte
+// loads for bf16, sixteen for fp32), converts it, and writes the four 16-byte
+// row segments of codes (eight threads write one 128-byte row segment). For
+// the transposed copy it turns the 4 x 16 codes into sixteen 4-byte column
+// words (4 consecutive rows of one column, by byte permutes) and parks them
+// in shared memory, where word (column cc, row group g) sits at index
+// cc * 32 + (g ^ 4 * ((cc >> 4) & 7)): one store instruction of a warp then
+// touches 32 distinct banks, and the four words of 16 consecutive rows stay
+// adjacent, so phase 2 moves 16 rows of one column with one 16-byte shared
+// load and one 16-byte store to out_t (eight threads write one 128-byte row
+// segment of out_t).
+template <int FMT, bool BF16>
+__global__ void __launch_bounds__(kThreads, BF16 ? 4 : 3)
 cast_rows_t_kernel(const void *__restrict__ x, int64_t rows, int64_t cols, const float *__restrict__ scale_p,
-                   uint8_t *__restrict__ out, uint8_t *__restrict__ out_t, float *__restrict__ amax_p,
-                   float *__restrict__ ws) {
+                   uint8_t *__restrict__ out, uint8_t *__restrict__ out_t, float *__restrict__ amax_p) {
     pdl_wait();
     pdl_launch_dependents();
     __shared__ __align__(16) uint32_t sT[128 * 32];
-    __shared__ float s_colsum[DBIAS ? 16 * 128 : 1];
-    float csum[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
     const int64_t tiles_c = (cols + 127) >> 7;
-    const int64_t r0 = (blockIdx.x / tiles_c) * 128, c0 = (blockIdx.x % tiles_c) * 128;
-    const int tx = threadIdx.x & 15, ty = threadIdx.x >> 4;
+    const int64_t tr = blockIdx.x / tiles_c, tc = blockIdx.x - tr * tiles_c;
+    const int64_t r0 = tr * 128, c0 = tc * 128;
+    const int tx = threadIdx.x & 7, ty = threadIdx.x >> 3;
+    const int64_t r = r0 + 4 * ty, c = c0 + 16 * tx;
     const float scale = __ldg(scale_p);
     float am = 0.0f;
-    const int64_t c = c0 + 8 * tx;
-    const int sw1 = 2 * tx;
+    if (r < rows && c < cols) {
+        uint32_t q[4][4];  // codes of row i, word k = columns 4k .. 4k+3
+        if constexpr (BF16) {
+            uint4 raw[4][2];
 #pragma unroll
-    for (int it = 0; it < 2; ++it) {
-        const int g = ty + 16 * it;  // 4-row group within the tile
-        const int64_t r = r0 + 4 * g;
-        if (c < cols && r < rows) {
-            uint32_t lo[4], hi[4];
+            for (int i = 0; i < 4; ++i) {
+                const uint4 *p = reinterpret_cast<const uint4 *>(reinterpret_cast<const uint16_t *>(x) +
+                                                                 (r + i) * cols + c);
+                raw[i][0] = __ldcs(p);
+                raw[i][1] = __ldcs(p + 1);
+            }
 #pragma unroll
-            for (int q = 0; q < 4; ++q) {
-                float f[8];
-                load8<BF16>(x, cols, r + q, c, f);
+            for (int i = 0; i < 4; ++i) {
+                const uint32_t w[8] = {raw[i][0].x, raw[i][0].y, raw[i][0].z, raw[i][0].w,
+                                       raw[i][1].x, raw[i][1].y, raw[i][1].z, raw[i][1].w};
                 uint32_t probe = 0;
-                lo[q] = cast4<FMT>(f[0], f[1], f[2], f[3], scale, am, probe);
-                hi[q] = cast4<FMT>(f[4], f[5], f[6], f[7], scale, am, probe);
+#pragma unroll
+                for (int k = 0; k < 4; ++k) q[i][k] = cast4_bf16<FMT>(w[2 * k], w[2 * k + 1], scale, am, probe);
                 if (probe & 0x80808080u) {
-                    lo[q] = canonical_nan<FMT>(lo[q]);
-                    hi[q] = canonical_nan<FMT>(hi[q]);
-                }
-                if constexpr (DBIAS) {
 #pragma unroll
-                    for (int j = 0; j < 8; ++j) csum[j] = __fadd_rn(csum[j], f[j]);
+                    for (int k = 0; k < 4; ++k) q[i][k] = canonical_nan<FMT>(q[i][k]);
                 }
-                *reinterpret_cast<uint2 *>(out + (r + q) * cols + c) = make_uint2(lo[q], hi[q]);
             }
-            // 4 x 4 byte transposes: word j holds column (c + j), rows r .. r+3.
-            uint32_t wcol[8];
-            {
-                const uint32_t t0 = __byte_perm(lo[0], lo[1], 0x5140), t1 = __byte_perm(lo[0], lo[1], 0x7362);
-                const uint32_t t2 = __byte_perm(lo[2], lo[3], 0x5140), t3 = __byte_perm(lo[2], lo[3], 0x7362);
-                wcol[0] = __byte_perm(t0, t2, 0x5410);
-                wcol[1] = __byte_perm(t0, t2, 0x7632);
-                wcol[2] = __byte_perm(t1, t3, 0x5410);
-                wcol[3] = __byte_perm(t1, t3, 0x7632);
-            }
-            {
-                const uint32_t t0 = __byte_perm(hi[0], hi[1], 0x5140), t1 = __byte_perm(hi[0], hi[1], 0x7362);
-                const uint32_t t2 = __byte_perm(hi[2], hi[3], 0x5140), t3 = __byte_perm(hi[2], hi[3], 0x7362);
-                wcol[4] = __byte_perm(t0, t2, 0x5410);
-                wcol[5] = __byte_perm(t0, t2, 0x7632);
-                wcol[6] = __byte_perm(t1, t3, 0x5410);
-                wcol[7] = __byte_perm(t1, t3, 0x7632);
-            }
-            if (out_t != nullptr) {
+        } else {
+            float4 raw[4][4];
 #pragma unroll
-                for (int j = 0; j < 8; ++j) sT[(8 * tx + j) * 32 + (g ^ sw1)] = wcol[j];
+            for (int i = 0; i < 4; ++i) {
+                const float4 *p = reinterpret_cast<const float4 *>(reinterpret_cast<const float *>(x) +
+                                                                   (r + i) * cols + c);
+#pragma unroll
+                for (int k = 0; k < 4; ++k) raw[i][k] = __ldcs(p + k);
+            }
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                uint32_t probe = 0;
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    const float4 v = raw[i][k];
+                    q[i][k] = cast4<FMT>(v.x, v.y, v.z, v.w, scale, am, probe);
+                }
+                if (probe & 0x80808080u) {
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) q[i][k] = canonical_nan<FMT>(q[i][k]);
+                }
             }
         }
-    }
-    if constexpr (DBIAS) {
 #pragma unroll
-        for (int j = 0; j < 8; ++j) s_colsum[ty * 128 + 8 * tx + j] = csum[j];
+        for (int i = 0; i < 4; ++i)
+            *reinterpret_cast<uint4 *>(out + (r + i) * cols + c) = make_uint4(q[i][0], q[i][1], q[i][2], q[i][3]);
+        if (out_t != nullptr) {
+            const int sw = ty ^ (4 * tx);  // row group ty, XOR-swizzled by the column's 16-wide group tx
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                // 4 x 4 byte transpose: rows r .. r+3 of columns c + 4k .. c + 4k + 3
+                const uint32_t t0 = __byte_perm(q[0][k], q[1][k], 0x5140), t1 = __byte_perm(q[0][k], q[1][k], 0x7362);
+                const uint32_t t2 = __byte_perm(q[2][k], q[3][k], 0x5140), t3 = __byte_perm(q[2][k], q[3][k], 0x7362);
+                uint32_t *col = &sT[(16 * tx + 4 * k) * 32 + sw];
+                col[0] = __byte_perm(t0, t2, 0x5410);
+                col[32] = __byte_perm(t0, t2, 0x7632);
+                col[64] = __byte_perm(t1, t3, 0x5410);
+                col[96] = __byte_perm(t1, t3, 0x7632);
+            }
+        }
     }
     __syncthreads();
-    if constexpr (DBIAS) {
-        if (threadIdx.x < 128 && c0 + threadIdx.x < cols) {
-            float t = 0.0f;
-            for (int g = 0; g < 16; ++g) t = __fadd_rn(t, s_colsum[g * 128 + threadIdx.x]);
-            ws[(r0 >> 7) * cols + c0 + threadIdx.x] = t;
-        }
-    }
+    if (out_t != nullptr) {
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        if (out_t == nullptr) break;
-        const int id = threadIdx.x + kThreads * i;  // 0 .. 1023
-        const int cc = id >> 3, k = id & 7;          // tile column, 16-row chunk
-        const int64_t col = c0 + cc, row = r0 + 16 * k;
-        if (col < cols && row < rows) {
-            const int sw = 2 * ((cc >> 3) & 15);
-            const uint4 P = *reinterpret_cast<const uint4 *>(&sT[cc * 32 + ((4 * k) ^ (sw & ~3))]);
-            const uint4 o = (sw & 2) ? make_uint4(P.z, P.w, P.x, P.y) : P;
-            *reinterpret_cast<uint4 *>(out_t + col * rows + row) = o;
+        for (int i = 0; i < 4; ++i) {
+            const int id = threadIdx.x + kThreads * i;  // 0 .. 1023
+            const int cc = id >> 3, k = id & 7;          // tile column, 16-row chunk
+            const int64_t col = c0 + cc, row = r0 + 16 * k;
+            if (col < cols && row < rows) {
+                const uint4 P = *reinterpret_cast<const uint4 *>(&sT[cc * 32 + 4 * (k ^ ((cc >> 4) & 7))]);
+                *reinterpret_cast<uint4 *>(out_t + col * rows + row) = P;
+            }
         }
     }
     if (amax_p != nullptr) block_amax_atomic(am, amax_p);
 }
 
-// dbias[n] = the sum over tile rows t of ws[t * cols + n], in a fixed order:
-// each of a block's 8 row groups sums the tile rows g, g + 8, g + 16, ...
-// in increasing order, then the 8 group sums are added in group order. A
-// block covers 32 columns, so each warp reads 128 contiguous bytes of one
-// tile row and a thread has tile_rows / 8 independent loads in flight.
-constexpr int kReduceCols = 32, kReduceGroups = 8;
-__global__ void __launch_bounds__(kReduceCols * kReduceGroups)
-dbias_reduce_kernel(const float *__restrict__ ws, int64_t tile_rows, int64_t cols, void *__restrict__ dbias,
-                    int bf16_out) {
+// ---------------------------------------------------------------------------
+// The bias-gradient cast: a persistent, TMA-fed version of the tile cast.
+//
+// The grid has k CTAs per 128-column strip (k = dbias_ctas_per_strip(), a
+// function of the shape only: 4 at 8192 x 4096, so 128 CTAs); CTA j of a
+// strip converts the strip's tile rows j, j + k, j + 2k, ..., so at any
+// moment the grid works on a band of k tile rows across the whole width.
+// Warp 8 (one lane) streams those 128 x 128 input tiles into a ring of
+// shared-memory stages with TMA (two or four 128-byte-swizzled boxes of 128
+// rows per tile) and re-arms a stage when the consumers have used it; warps
+// 0-7 read each tile from shared memory (each thread a 4 x 16 patch, as in
+// cast_rows_t_kernel), write the 16-byte row segments of codes, optionally
+// the transposed copy through sT, and add their rows to column sums they keep
+// in registers across all their tiles. The loads of the next tiles are in
+// flight while a tile is converted, and the CTA publishes its column sums,
+// fences and counts its arrival once, at the end. The arithmetic runs on
+// pairs of fp32 lanes (mul/add .f32x2: one instruction per two elements, each
+// lane rounded as its own fp32 operation).
+//
+// Column-sum order (fixed by the shape): each thread adds its 4 rows of each
+// of its CTA's tiles, tile after tile, in row order; the four threads of a
+// warp that share columns are combined by a butterfly (xor 8, then xor 16);
+// the 8 warps in warp order; then the strip's k CTA sums in order of j, by
+// the CTA that arrives last on the strip's counter, which writes dbias and
+// sets the k sums and the counter back to zero, so a workspace that is zero
+// before a call is zero after it.
+constexpr int kTileThreads = 288;       // 8 consumer warps + 1 producer warp
+constexpr int kBoxBytes = 128 * 128;    // one box: 128 rows x 128 bytes
+constexpr int kDbiasTargetCtas = 152;   // the split aims at this many CTAs
+
+template <bool BF16>
+struct TileCfg {
+    static constexpr int ESIZE = BF16 ? 2 : 4;
+    static constexpr int BOX_COLS = 128 / ESIZE;      // elements per box row
+    static constexpr int BOXES = 128 / BOX_COLS;      // boxes per 128-column tile
+    static constexpr int STAGE_BYTES = BOXES * kBoxBytes;
+    static constexpr int STAGES = BF16 ? 4 : 2;
+    static constexpr int ST_OFFSET = STAGES * STAGE_BYTES;
+    static constexpr int PART_OFFSET = ST_OFFSET + 128 * 32 * 4;
+    static constexpr int BAR_OFFSET = PART_OFFSET + 8 * 128 * 4;
+    static constexpr int MISC_OFFSET = BAR_OFFSET + 16 * STAGES;
+    static constexpr int SMEM_BYTES = MISC_OFFSET + 64 + 1024;  // + the 1024-byte alignment pad
+};
+
+__device__ __forceinline__ void consumer_sync() { asm volatile("bar.sync 1, 256;" ::: "memory"); }
+
+// Pairs of fp32 values in one 64-bit register (low lane first) and the
+// two-lane fp32 arithmetic of sm_100-class GPUs: each lane is one IEEE
+// round-to-nearest-even operation, bit-identical to the scalar one.
+__device__ __forceinline__ uint64_t f2_from_bits(uint32_t lo, uint32_t hi) {
+    uint64_t d;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(d) : "r"(lo), "r"(hi));
+    return d;
+}
+__device__ __forceinline__ void f2_split(uint64_t v, float &lo, float &hi) {
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+__device__ __forceinline__ uint64_t f2_mul(uint64_t a, uint64_t b) {
+    uint64_t d;
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+__device__ __forceinline__ uint64_t f2_add(uint64_t a, uint64_t b) {
+    uint64_t d;
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+
+// Two (lo, hi) pairs -> four codes under scale2 = (scale, scale); the pairs
+// join the column sums and their |x| the running amax. NaN inputs give NaN
+// codes here; the caller canonicalises them (they also make the column sums
+// NaN, which is how it notices).
+template <int FMT>
+__device__ __forceinline__ uint32_t cast_pairs(uint64_t p0, uint64_t p1, uint64_t scale2, uint64_t &s0, uint64_t &s1,
+                                               float &am) {
+    float a, b, c, d;
+    f2_split(f2_mul(p0, scale2), a, b);
+    f2_split(f2_mul(p1, scale2), c, d);
+    s0 = f2_add(s0, p0);
+    s1 = f2_add(s1, p1);
+    float x0, x1, x2, x3;
+    f2_split(p0, x0, x1);
+    f2_split(p1, x2, x3);
+    am = fmaxf(fmaxf(am, fabsf(x0)), fmaxf(fabsf(x1), fmaxf(fabsf(x2), fabsf(x3))));
+    return cvt_pair_raw<FMT>(a, b) | (cvt_pair_raw<FMT>(c, d) << 16);
+}
+
+template <int FMT, bool BF16>
+__global__ void __launch_bounds__(kTileThreads, 1)
+cast_dbias_kernel(const __grid_constant__ CUtensorMap tmap, int64_t rows, int64_t cols, int k_per_strip,
+                  const float *__restrict__ scale_p, uint8_t *__restrict__ out, uint8_t *__restrict__ out_t,
+                  float *__restrict__ amax_p, float *__restrict__ ws, uint32_t *__restrict__ counters,
+                  void *__restrict__ dbias, int dbias_bf16) {
+    using C = TileCfg<BF16>;
+    extern __shared__ uint8_t smem_raw[];
+    uint32_t base = smem_u32(smem_raw);
+    const uint32_t pad = (1024u - (base & 1023u)) & 1023u;
+    uint8_t *smem = smem_raw + pad;
+    base += pad;
+    uint32_t *sT = reinterpret_cast<uint32_t *>(smem + C::ST_OFFSET);
+    float *s_part = reinterpret_cast<float *>(smem + C::PART_OFFSET);
+    const uint32_t bar0 = base + C::BAR_OFFSET;
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + C::MISC_OFFSET);
+    int *s_last = reinterpret_cast<int *>(smem + C::MISC_OFFSET + 4);
+    float *s_red = reinterpret_cast<float *>(smem + C::MISC_OFFSET + 32);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int64_t tiles_r = (rows + 127) >> 7, tiles_c = (cols + 127) >> 7;
+    const int64_t strip = blockIdx.x % tiles_c;
+    const int64_t j = blockIdx.x / tiles_c;
+    const int64_t c0 = strip * 128;
+    const int64_t ntile = j < tiles_r ? (tiles_r - 1 - j) / k_per_strip + 1 : 0;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < C::STAGES; ++s) {
+            mbar_init(bar0 + 8u * s, 1);                  // full: the producer's arrival + the TMA bytes
+            mbar_init(bar0 + 8u * (C::STAGES + s), 8);    // empty: one arrival per consumer warp
+        }
+        *abort_flag = 0;
+        fence_mbar_init();
+        prefetch_tmap(&tmap);
+    }
+    __syncthreads();
     pdl_wait();
     pdl_launch_dependents();
-    __shared__ float part[kReduceGroups][kReduceCols];
-    const int tx = threadIdx.x % kReduceCols, g = threadIdx.x / kReduceCols;
-    const int64_t n = static_cast<int64_t>(blockIdx.x) * kReduceCols + tx;
-    float t = 0.0f;
-    if (n < cols) {
-#pragma unroll 4
-        for (int64_t r = g; r < tile_rows; r += kReduceGroups) t = __fadd_rn(t, ws[r * cols + n]);
+
+    if (warp == 8) {
+        if (lane == 0) {
+            // ---------------- TMA producer
+            int64_t i = 0;
+            for (; i < ntile; ++i) {
+                const int s = static_cast<int>(i % C::STAGES);
+                const uint32_t ph = static_cast<uint32_t>(i / C::STAGES) & 1u;
+                if (!wait_bounded(bar0 + 8u * (C::STAGES + s), ph ^ 1u, abort_flag, &g_cast_timeout_flag)) break;
+                mbar_arrive_expect_tx(bar0 + 8u * s, C::STAGE_BYTES);
+                const int32_t r0 = static_cast<int32_t>((j + i * k_per_strip) * 128);
+#pragma unroll
+                for (int bx = 0; bx < C::BOXES; ++bx)
+                    tma_load_2d_cta(base + s * C::STAGE_BYTES + bx * kBoxBytes, &tmap, bar0 + 8u * s,
+                                    static_cast<int32_t>(c0) + bx * C::BOX_COLS, r0);
+            }
+            if (i < ntile) {
+                // aborted: let the loads already issued land before the CTA goes away
+                volatile int never = 0;
+                for (int64_t q = i - 1; q >= 0 && q >= i - C::STAGES; --q)
+                    wait_bounded(bar0 + 8u * static_cast<uint32_t>(q % C::STAGES),
+                                 static_cast<uint32_t>(q / C::STAGES) & 1u, &never, &g_cast_timeout_flag);
+            }
+        }
+        return;
     }
-    part[g][tx] = t;
-    __syncthreads();
-    if (g != 0 || n >= cols) return;
-    t = part[0][tx];
-    for (int j = 1; j < kReduceGroups; ++j) t = __fadd_rn(t, part[j][tx]);
-    if (bf16_out)
-        static_cast<__nv_bfloat16 *>(dbias)[n] = __float2bfloat16_rn(t);
-    else
-        static_cast<float *>(dbias)[n] = t;
+
+    // ---------------- consumers: warps 0-7, thread (tx, ty) = 4 rows x 16 columns
+    const int tx = threadIdx.x & 7, ty = threadIdx.x >> 3;
+    const int64_t c = c0 + 16 * tx;
+    const float scale = __ldg(scale_p);
+    const uint64_t scale2 = f2_from_bits(__float_as_uint(scale), __float_as_uint(scale));
+    float am = 0.0f;
+    uint64_t csum[8];  // column pairs (2q, 2q + 1) of the thread's 16 columns
+#pragma unroll
+    for (int q = 0; q < 8; ++q) csum[q] = 0ull;
+    for (int64_t i = 0; i < ntile; ++i) {
+        const int s = static_cast<int>(i % C::STAGES);
+        const uint32_t ph = static_cast<uint32_t>(i / C::STAGES) & 1u;
+        // lane 0 waits for the stage; the warp follows its verdict (uniform
+        // per warp, so the __syncwarp below is never divergent)
+        int okw = 0;
+        if (lane == 0) okw = wait_bounded(bar0 + 8u * s, ph, abort_flag, &g_cast_timeout_flag) ? 1 : 0;
+        const bool ok = __shfl_sync(0xffffffffu, okw, 0) != 0;
+        __syncwarp();
+        const int64_t r0 = (j + i * k_per_strip) * 128;
+        const int64_t r = r0 + 4 * ty;
+        if (ok) {
+            const uint8_t *stage = smem + s * C::STAGE_BYTES;
+            uint32_t q4[4][4];  // codes of row rr, word w = columns 4w .. 4w+3
+#pragma unroll
+            for (int rr = 0; rr < 4; ++rr) {
+                const int row = 4 * ty + rr;
+                uint64_t p[8];  // the row's 16 values as pairs
+                if constexpr (BF16) {
+                    const uint8_t *box = stage + (tx >> 2) * kBoxBytes + row * 128;
+#pragma unroll
+                    for (int h = 0; h < 2; ++h) {
+                        const uint4 v = *reinterpret_cast<const uint4 *>(box + (((2 * (tx & 3) + h) ^ (row & 7)) << 4));
+                        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) p[4 * h + e] = f2_from_bits(w[e] << 16, w[e] & 0xFFFF0000u);
+                    }
+                } else {
+                    const uint8_t *box = stage + (tx >> 1) * kBoxBytes + row * 128;
+#pragma unroll
+                    for (int h = 0; h < 4; ++h) {
+                        const uint4 v = *reinterpret_cast<const uint4 *>(box + (((4 * (tx & 1) + h) ^ (row & 7)) << 4));
+                        p[2 * h] = f2_from_bits(v.x, v.y);
+                        p[2 * h + 1] = f2_from_bits(v.z, v.w);
+                    }
+                }
+#pragma unroll
+                for (int w = 0; w < 4; ++w)
+                    q4[rr][w] = cast_pairs<FMT>(p[2 * w], p[2 * w + 1], scale2, csum[2 * w], csum[2 * w + 1], am);
+            }
+            // Release the stage only now that every loaded value has been used:
+            // a shared-memory load whose value is consumed has been performed,
+            // so the refill cannot overwrite data the warp has not read yet (a
+            // release right after the loads let the next tile's TMA write reach
+            // a few 16-byte chunks first, about once in tens of launches).
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar0 + 8u * (C::STAGES + s));
+            // a NaN input makes its column sum NaN (and so, from then on, does
+            // nothing else: Inf - Inf also gives NaN, and canonicalising codes
+            // that hold no NaN changes nothing)
+            bool any_nan = false;
+#pragma unroll
+            for (int q = 0; q < 8; ++q) {
+                float lo, hi;
+                f2_split(csum[q], lo, hi);
+                any_nan |= (lo != lo) | (hi != hi);
+            }
+            if (any_nan) {
+#pragma unroll
+                for (int rr = 0; rr < 4; ++rr)
+#pragma unroll
+                    for (int w = 0; w < 4; ++w) q4[rr][w] = canonical_nan<FMT>(q4[rr][w]);
+            }
+            if (r < rows && c < cols) {
+#pragma unroll
+                for (int rr = 0; rr < 4; ++rr)
+                    *reinterpret_cast<uint4 *>(out + (r + rr) * cols + c) =
+                        make_uint4(q4[rr][0], q4[rr][1], q4[rr][2], q4[rr][3]);
+                if (out_t != nullptr) {
+                    const int sw = ty ^ (4 * tx);
+#pragma unroll
+                    for (int w = 0; w < 4; ++w) {
+                        const uint32_t t0 = __byte_perm(q4[0][w], q4[1][w], 0x5140), t1 = __byte_perm(q4[0][w], q4[1][w], 0x7362);
+                        const uint32_t t2 = __byte_perm(q4[2][w], q4[3][w], 0x5140), t3 = __byte_perm(q4[2][w], q4[3][w], 0x7362);
+                        uint32_t *col = &sT[(16 * tx + 4 * w) * 32 + sw];
+                        col[0] = __byte_perm(t0, t2, 0x5410);
+                        col[32] = __byte_perm(t0, t2, 0x7632);
+                        col[64] = __byte_perm(t1, t3, 0x5410);
+                        col[96] = __byte_perm(t1, t3, 0x7632);
+                    }
+                }
+            }
+        }
+        if (out_t != nullptr) {
+            // every consumer thread passes both barriers on every tile, aborted or not
+            consumer_sync();
+            if (ok) {
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    const int id = threadIdx.x + 256 * q;
+                    const int cc = id >> 3, kk = id & 7;
+                    const int64_t col = c0 + cc, row = r0 + 16 * kk;
+                    if (col < cols && row < rows) {
+                        const uint4 P = *reinterpret_cast<const uint4 *>(&sT[cc * 32 + 4 * (kk ^ ((cc >> 4) & 7))]);
+                        *reinterpret_cast<uint4 *>(out_t + col * rows + row) = P;
+                    }
+                }
+            }
+            consumer_sync();  // sT is free for the next tile
+        }
+    }
+    // ---------------- the CTA's amax and column sums
+    float cs[16];
+#pragma unroll
+    for (int q = 0; q < 8; ++q) f2_split(csum[q], cs[2 * q], cs[2 * q + 1]);
+#pragma unroll
+    for (int q = 0; q < 16; ++q) {
+        cs[q] = __fadd_rn(cs[q], __shfl_xor_sync(0xffffffffu, cs[q], 8));
+        cs[q] = __fadd_rn(cs[q], __shfl_xor_sync(0xffffffffu, cs[q], 16));
+    }
+    if (lane < 8) {
+        float *dst = &s_part[warp * 128 + 16 * tx];
+#pragma unroll
+        for (int q = 0; q < 16; q += 4)
+            *reinterpret_cast<float4 *>(dst + q) = make_float4(cs[q], cs[q + 1], cs[q + 2], cs[q + 3]);
+    }
+    am = warp_max(am);
+    if (lane == 0) s_red[warp] = am;
+    consumer_sync();
+    if (threadIdx.x == 0 && amax_p != nullptr) {
+        float t = s_red[0];
+        for (int w = 1; w < 8; ++w) t = fmaxf(t, s_red[w]);
+        atomicMax(reinterpret_cast<int *>(amax_p), __float_as_int(t));
+    }
+    if (threadIdx.x < 128) {
+        const int64_t col = c0 + threadIdx.x;
+        if (col < cols) {
+            float t = s_part[threadIdx.x];
+#pragma unroll
+            for (int w = 1; w < 8; ++w) t = __fadd_rn(t, s_part[w * 128 + threadIdx.x]);
+            ws[j * cols + col] = t;
+        }
+        __threadfence();  // the CTA's column sums are visible before its arrival is
+    }
+    consumer_sync();
+    if (threadIdx.x == 0) *s_last = atomicAdd(&counters[strip], 1u) == static_cast<uint32_t>(k_per_strip - 1);
+    consumer_sync();
+    if (*s_last) {
+        __threadfence();
+        if (threadIdx.x < 128 && c0 + threadIdx.x < cols) {
+            const int64_t col = c0 + threadIdx.x;
+            float t = __ldcg(ws + col);
+            for (int jj = 1; jj < k_per_strip; ++jj) t = __fadd_rn(t, __ldcg(ws + jj * cols + col));
+            for (int jj = 0; jj < k_per_strip; ++jj) __stcg(ws + jj * cols + col, 0.0f);
+            if (dbias_bf16)
+                static_cast<__nv_bfloat16 *>(dbias)[col] = __float2bfloat16_rn(t);
+            else
+                static_cast<float *>(dbias)[col] = t;
+        }
+        if (threadIdx.x == 0) counters[strip] = 0u;
+    }
 }
 
 template <int FMT, bool BF16>
 int launch_typed(const void *x, int64_t rows, int64_t cols, const float *scale, uint8_t *out,
-                 uint8_t *out_t, float *amax, cudaStream_t s, const DeviceInfo &dev, float *ws = nullptr) {
-    if (out_t == nullptr && ws == nullptr) {
+                 uint8_t *out_t, float *amax, cudaStream_t s) {
+    if (out_t == nullptr) {
         const int64_t n = rows * cols;
-        const int64_t nchunk = n >> 4;
-        // up to 32 blocks per SM (8 resident): smaller shares let the block
-        // scheduler even out the tail, measured faster than one resident wave
-        int64_t blocks = (nchunk + kThreads - 1) / kThreads;
-        const int64_t cap = static_cast<int64_t>(dev.num_sms) * 32;
-        if (blocks > cap) blocks = cap;
-        if (blocks < 1) blocks = 1;
+        const int64_t blocks = row_blocks(n);
+        if (blocks > 0x7FFFFFFF) return fail(FP8MP_ERR_INVALID, "fp8_quantize: tensor too large");
         launch_kernel(cast_rows_kernel<FMT, BF16>, dim3(static_cast<unsigned>(blocks)), dim3(kThreads), 0, s, x, n,
                       scale, out, amax);
     } else {
         const int64_t tiles = ((rows + 127) >> 7) * ((cols + 127) >> 7);
         if (tiles > 0x7FFFFFFF) return fail(FP8MP_ERR_INVALID, "fp8_quantize: tensor too large");
-        if (ws != nullptr)
-            launch_kernel(cast_rows_t_kernel<FMT, BF16, true>, dim3(static_cast<unsigned>(tiles)), dim3(kThreads), 0,
-                          s, x, rows, cols, scale, out, out_t, amax, ws);
-        else
-            launch_kernel(cast_rows_t_kernel<FMT, BF16, false>, dim3(static_cast<unsigned>(tiles)), dim3(kThreads), 0,
-                          s, x, rows, cols, scale, out, out_t, amax, nullptr);
+        launch_kernel(cast_rows_t_kernel<FMT, BF16>, dim3(static_cast<unsigned>(tiles)), dim3(kThreads), 0, s, x,
+                      rows, cols, scale, out, out_t, amax);
     }
     const cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return fail(FP8MP_ERR_LAUNCH, "fp8_quantize: launch failed: %s", cudaGetErrorString(e));
     return FP8MP_OK;
 }
 
+// The bias-gradient cast's launch: tensor map of x (boxes of 128 rows x 128
+// bytes, 128-byte swizzle, zero fill outside the tensor), k CTAs per strip.
+template <int FMT, bool BF16>
+int launch_dbias_typed(const void *x, int64_t rows, int64_t cols, const float *scale, uint8_t *out,
+                       uint8_t *out_t, float *amax, void *dbias, int dbias_bf16, float *ws, cudaStream_t s,
+                       const DeviceInfo &dev) {
+    using C = TileCfg<BF16>;
+    static std::atomic<bool> ready[64];
+    static std::mutex m;
+    if (dev.device < 0 || dev.device >= 64) return fail(FP8MP_ERR_DEVICE, "device index %d out of range", dev.device);
+    if (!ready[dev.device].load(std::memory_order_acquire)) {
+        std::lock_guard<std::mutex> lock(m);
+        if (!ready[dev.device].load(std::memory_order_relaxed)) {
+            const cudaError_t e = cudaFuncSetAttribute(cast_dbias_kernel<FMT, BF16>,
+                                                       cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
+            if (e != cudaSuccess)
+                return fail(FP8MP_ERR_LAUNCH, "fp8_quantize_dbias: shared-memory attribute: %s", cudaGetErrorString(e));
+            ready[dev.device].store(true, std::memory_order_release);
+        }
+    }
+    auto enc = tensor_map_encoder();
+    if (enc == nullptr) return fail(FP8MP_ERR_LAUNCH, "cuTensorMapEncodeTiled is not available");
+    CUtensorMap tmap;
+    const cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
+    const cuuint64_t strides[1] = {static_cast<cuuint64_t>(cols) * C::ESIZE};
+    const cuuint32_t box[2] = {static_cast<cuuint32_t>(C::BOX_COLS), 128};
+    const cuuint32_t estr[2] = {1, 1};
+    const CUresult r = enc(&tmap, BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2,
+                           const_cast<void *>(x), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                           CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS)
+        return fail(FP8MP_ERR_LAUNCH, "fp8_quantize_dbias: cuTensorMapEncodeTiled failed (%d)", static_cast<int>(r));
+    const int k = dbias_ctas_per_strip(rows, cols);
+    const int64_t grid = k * ((cols + 127) >> 7);
+    if (grid > 0x7FFFFFFF) return fail(FP8MP_ERR_INVALID, "fp8_quantize_dbias: tensor too large");
+    uint32_t *counters = reinterpret_cast<uint32_t *>(ws + static_cast<int64_t>(k) * cols);
+    launch_kernel(cast_dbias_kernel<FMT, BF16>, dim3(static_cast<unsigned>(grid)), dim3(kTileThreads), C::SMEM_BYTES,
+                  s, tmap, rows, cols, k, scale, out, out_t, amax, ws, counters, dbias, dbias_bf16);
+    const cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return fail(FP8MP_ERR_LAUNCH, "fp8_quantize_dbias: launch failed: %s", cudaGetErrorString(e));
+    return FP8MP_OK;
+}
+
 // amax pass of current scaling: max |x| over a flat array, one atomic max
-// per block into *amax (zeroed by the caller's stream just before).
+// per block into *amax (zeroed by the caller's stream just before). Same
+// work split as cast_rows_kernel: a block per run of kChunksPerThread * 256
+// chunks, all of a thread's loads issued first.
 template <bool BF16>
-__global__ void __launch_bounds__(kThreads)
+__global__ void __launch_bounds__(kThreads, 4)
 amax_kernel(const void *__restrict__ x, int64_t n, float *__restrict__ amax_p) {
     pdl_wait();
     pdl_launch_dependents();
     float am = 0.0f;
     const int64_t nchunk = n >> 4;
-    const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
-    for (int64_t c = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; c < nchunk; c += stride) {
-        float f[16];
-        load16<BF16>(x, c, f);
+    const int64_t c0 = static_cast<int64_t>(blockIdx.x) * (kChunksPerThread * kThreads) + threadIdx.x;
 #pragma unroll
-        for (int j = 0; j < 16; ++j) am = fmaxf(am, fabsf(f[j]));
+    for (int h = 0; h < kChunksPerThread; h += (BF16 ? kChunksPerThread : 2)) {
+        constexpr int U = BF16 ? kChunksPerThread : 2;
+        float f[U][16];
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const int64_t c = c0 + (h + u) * kThreads;
+            if (c < nchunk) {
+                load16<BF16>(x, c, f[u]);
+            } else {
+#pragma unroll
+                for (int j = 0; j < 16; ++j) f[u][j] = 0.0f;
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+#pragma unroll
+            for (int j = 0; j < 16; j += 4)
+                am = fmaxf(fmaxf(am, fabsf(f[u][j])),
+                           fmaxf(fabsf(f[u][j + 1]), fmaxf(fabsf(f[u][j + 2]), fabsf(f[u][j + 3]))));
+        }
     }
     if (blockIdx.x == gridDim.x - 1)
         for (int64_t i = (nchunk << 4) + threadIdx.x; i < n; i += blockDim.x) am = fmaxf(am, fabsf(load1<BF16>(x, i)));
@@ -365,10 +744,8 @@ int launch_quantize_current(const void *x, int x_dtype, int64_t rows, int64_t co
     cudaError_t e = cudaMemsetAsync(amax, 0, sizeof(float), s);
     if (e != cudaSuccess) return fail(FP8MP_ERR_LAUNCH, "fp8_quantize_current: memset failed: %s", cudaGetErrorString(e));
     const int64_t n = rows * cols;
-    int64_t blocks = ((n >> 4) + kThreads - 1) / kThreads;
-    const int64_t cap = static_cast<int64_t>(dev.num_sms) * 8;
-    if (blocks > cap) blocks = cap;
-    if (blocks < 1) blocks = 1;
+    const int64_t blocks = row_blocks(n);
+    if (blocks > 0x7FFFFFFF) return fail(FP8MP_ERR_INVALID, "fp8_quantize_current: tensor too large");
     if (x_dtype == FP8MP_BF16)
         launch_kernel(amax_kernel<true>, dim3(static_cast<unsigned>(blocks)), dim3(kThreads), 0, s, x, n, amax);
     else
@@ -381,35 +758,43 @@ int launch_quantize_current(const void *x, int x_dtype, int64_t rows, int64_t co
     return launch_quantize(x, x_dtype, rows, cols, fmt, scale, out, out_t, nullptr, s, dev);
 }
 
+int dbias_ctas_per_strip(int64_t rows, int64_t cols) {
+    const int64_t tiles_r = (rows + 127) >> 7, tiles_c = (cols + 127) >> 7;
+    int64_t k = tiles_c > 0 ? kDbiasTargetCtas / tiles_c : 1;
+    if (k > tiles_r) k = tiles_r;
+    if (k < 1) k = 1;
+    return static_cast<int>(k);
+}
+
 int launch_quantize_dbias(const void *x, int x_dtype, int64_t rows, int64_t cols, int fmt, const float *scale,
                           uint8_t *out, uint8_t *out_t, float *amax, void *dbias, int dbias_dtype, float *ws,
                           cudaStream_t s, const DeviceInfo &dev) {
     const bool bf16 = x_dtype == FP8MP_BF16;
-    int rc;
+    const int db16 = dbias_dtype == FP8MP_BF16 ? 1 : 0;
     if (fmt == FP8MP_E4M3)
-        rc = bf16 ? launch_typed<FP8MP_E4M3, true>(x, rows, cols, scale, out, out_t, amax, s, dev, ws)
-                  : launch_typed<FP8MP_E4M3, false>(x, rows, cols, scale, out, out_t, amax, s, dev, ws);
-    else
-        rc = bf16 ? launch_typed<FP8MP_E5M2, true>(x, rows, cols, scale, out, out_t, amax, s, dev, ws)
-                  : launch_typed<FP8MP_E5M2, false>(x, rows, cols, scale, out, out_t, amax, s, dev, ws);
-    if (rc) return rc;
-    const int64_t tile_rows = (rows + 127) >> 7;
-    launch_kernel(dbias_reduce_kernel, dim3(static_cast<unsigned>((cols + kReduceCols - 1) / kReduceCols)),
-                  dim3(kReduceCols * kReduceGroups), 0, s, ws, tile_rows, cols, dbias, dbias_dtype == FP8MP_BF16 ? 1 : 0);
-    const cudaError_t e = cudaGetLastError();
-    if (e != cudaSuccess)
-        return fail(FP8MP_ERR_LAUNCH, "fp8_quantize_dbias: launch failed: %s", cudaGetErrorString(e));
-    return FP8MP_OK;
+        return bf16 ? launch_dbias_typed<FP8MP_E4M3, true>(x, rows, cols, scale, out, out_t, amax, dbias, db16, ws, s, dev)
+                    : launch_dbias_typed<FP8MP_E4M3, false>(x, rows, cols, scale, out, out_t, amax, dbias, db16, ws, s, dev);
+    return bf16 ? launch_dbias_typed<FP8MP_E5M2, true>(x, rows, cols, scale, out, out_t, amax, dbias, db16, ws, s, dev)
+                : launch_dbias_typed<FP8MP_E5M2, false>(x, rows, cols, scale, out, out_t, amax, dbias, db16, ws, s, dev);
 }
 
 int launch_quantize(const void *x, int x_dtype, int64_t rows, int64_t cols, int fmt, const float *scale,
-                    uint8_t *out, uint8_t *out_t, float *amax, cudaStream_t s, const DeviceInfo &dev) {
+                    uint8_t *out, uint8_t *out_t, float *amax, cudaStream_t s, const DeviceInfo &) {
     const bool bf16 = x_dtype == FP8MP_BF16;
     if (fmt == FP8MP_E4M3)
-        return bf16 ? launch_typed<FP8MP_E4M3, true>(x, rows, cols, scale, out, out_t, amax, s, dev)
-                    : launch_typed<FP8MP_E4M3, false>(x, rows, cols, scale, out, out_t, amax, s, dev);
-    return bf16 ? launch_typed<FP8MP_E5M2, true>(x, rows, cols, scale, out, out_t, amax, s, dev)
-                : launch_typed<FP8MP_E5M2, false>(x, rows, cols, scale, out, out_t, amax, s, dev);
+        return bf16 ? launch_typed<FP8MP_E4M3, true>(x, rows, cols, scale, out, out_t, amax, s)
+                    : launch_typed<FP8MP_E4M3, false>(x, rows, cols, scale, out, out_t, amax, s);
+    return bf16 ? launch_typed<FP8MP_E5M2, true>(x, rows, cols, scale, out, out_t, amax, s)
+                : launch_typed<FP8MP_E5M2, false>(x, rows, cols, scale, out, out_t, amax, s);
+}
+
+int read_and_clear_cast_timeout_flag(unsigned int *value) {
+    unsigned int v = 0, zero = 0;
+    cudaError_t e = cudaMemcpyFromSymbol(&v, g_cast_timeout_flag, sizeof v);
+    if (e == cudaSuccess) e = cudaMemcpyToSymbol(g_cast_timeout_flag, &zero, sizeof zero);
+    if (e != cudaSuccess) return fail(FP8MP_ERR_LAUNCH, "reading the timeout flag failed: %s", cudaGetErrorString(e));
+    *value = v;
+    return FP8MP_OK;
 }
 
 }  // namespace fp8mp

@@ -68,8 +68,7 @@ class _FP8LinearFn(torch.autograd.Function):
         db = None
         if b_dtype is not None and ctx.needs_input_grad[2]:
             db = torch.empty(N, dtype=b_dtype, device=dev)
-            ws = torch.empty(max(1, fp8_quantize_dbias_workspace_bytes(M, N) // 4), dtype=torch.float32, device=dev)
-            fp8_quantize_dbias(dy2, E5M2, md.scale, D8, None, db, ws, amax=md.cur_amax)
+            fp8_quantize_dbias(dy2, E5M2, md.scale, D8, None, db, layer.dbias_workspace(M, N), amax=md.cur_amax)
         else:
             fp8_quantize(dy2, E5M2, md.scale, D8, None, md.cur_amax)
         sinv_dy = md.scale_inv.clone()
@@ -111,9 +110,20 @@ class FP8Linear(torch.nn.Module):
         # every backward); a master step given it as grad_nonfinite reads and
         # clears it instead of scanning the gradient again
         self.dw_nonfinite = torch.zeros(1, dtype=torch.int32, device=device)
+        # the bias gradient's workspace: zero-filled once, and every call of
+        # fp8_quantize_dbias leaves it zero, so it is reused without clearing
+        self._dbias_ws = torch.zeros(0, dtype=torch.float32, device=device)
 
     def metas(self):
         return [self.meta_x, self.meta_w, self.meta_y, self.meta_dy]
+
+    def dbias_workspace(self, rows: int, cols: int) -> torch.Tensor:
+        """The zero-filled workspace of the bias-gradient cast, grown when a
+        larger shape needs more."""
+        need = (fp8_quantize_dbias_workspace_bytes(rows, cols) + 3) // 4
+        if self._dbias_ws.numel() < need:
+            self._dbias_ws = torch.zeros(need, dtype=torch.float32, device=self._dbias_ws.device)
+        return self._dbias_ws
 
     def forward(self, x: torch.Tensor) -> torch.Tensor:
         return _FP8LinearFn.apply(x, self.weight, self.bias, self)

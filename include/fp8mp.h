@@ -150,21 +150,37 @@ int fp8_quantize_current(const void *x, int32_t x_dtype, int64_t rows, int64_t c
  *                        layer whose backward reads dY8 row-major through
  *                        fp8_linear_bwd_rowmajor needs no transposed copy);
  *   dbias[c] = sum_r x[r, c]  over the unscaled input, fp32 accumulation in
- *                             a fixed order (deterministic): each 128-row
- *                             block's column sums; those of every 8th block
- *                             (blocks g, g + 8, ...) added in order, then the
- *                             8 partial sums in order of g; rounded once to
- *                             dbias_dtype.
+ *                             a fixed order (deterministic, set by the shape
+ *                             alone): the rows are split among k CTAs per
+ *                             128-column strip, k = max(1, min(ceil(rows/128),
+ *                             152 / ceil(cols/128))), CTA j taking the 128-row
+ *                             tiles j, j + k, ...; each CTA adds, per column,
+ *                             its tiles' rows in 4-row runs (each run in row
+ *                             order, runs tile after tile), combines the four
+ *                             runs of each 16 rows pairwise ((a + b) + (c + d))
+ *                             and the eight 16-row sums in order; the strip's
+ *                             k CTA sums are added in order of j; rounded once
+ *                             to dbias_dtype.
+ * One launch: each CTA writes its column sums to the workspace and counts
+ * itself in a per-strip word there; the last CTA of a strip to finish adds
+ * the strip's sums, writes dbias, and sets the words it used back to zero.
  * workspace  device scratch of at least fp8_quantize_dbias_workspace_bytes
- *            (rows, cols) bytes, 16-byte aligned, owned by the caller; its
- *            contents on entry do not matter and on exit are unspecified.
+ *            (rows, cols) bytes, 16-byte aligned, owned by the caller. It
+ *            must be ZERO-FILLED before its first use (e.g. cudaMemset or
+ *            torch.zeros); every call leaves the bytes it used zero again,
+ *            so one workspace serves later calls of any shape that fits
+ *            without clearing. Calls that share a workspace must not overlap
+ *            on the GPU (keep them on one stream).
  * rows, cols multiples of 16; rows == 0 gives dbias = 0.
  */
 int fp8_quantize_dbias(const void *x, int32_t x_dtype, int64_t rows, int64_t cols, int32_t fmt,
                        const float *scale, uint8_t *out, uint8_t *out_t, float *amax, void *dbias,
                        int32_t dbias_dtype, float *workspace, int64_t workspace_bytes, void *stream);
 
-/* Workspace bytes fp8_quantize_dbias needs: ceil(rows / 128) * cols * 4. */
+/* Workspace bytes fp8_quantize_dbias needs: k * cols * 4 for the CTAs'
+ * column sums (k as above) plus ceil(cols / 128) * 4 for the strips' arrival
+ * counters, rounded up to a multiple of 16; -1 for a negative or too large
+ * shape. */
 int64_t fp8_quantize_dbias_workspace_bytes(int64_t rows, int64_t cols);
 
 /* Floats in the fixed scratch array of fp8_quantize_dbias_noalloc (4 MiB). */
@@ -179,20 +195,25 @@ int64_t fp8_quantize_dbias_workspace_bytes(int64_t rows, int64_t cols);
  * take the implicit device synchronisation of cudaMalloc / cudaFree.
  *
  * Same arguments and results as fp8_quantize_dbias, minus the workspace:
- * the per-block partial sums live in a file-scope device array of
- * FP8MP_NOALLOC_DBIAS_SCRATCH_FLOATS floats inside the library, which every
- * GPU that loads the library holds until the process exits. The call
- * allocates nothing (no cudaMalloc, cudaFree or allocating library routine).
- *   - Limit: ceil(rows / 128) * cols <= FP8MP_NOALLOC_DBIAS_SCRATCH_FLOATS
- *     (for example rows 16384 with cols up to 8192); larger shapes return
- *     FP8MP_ERR_INVALID with a message naming the limit.
+ * the per-tile column sums and the strips' arrival counters live in a
+ * file-scope device array of FP8MP_NOALLOC_DBIAS_SCRATCH_FLOATS floats
+ * inside the library, which every GPU that loads the library holds until
+ * the process exits. The call allocates nothing (no cudaMalloc, cudaFree or
+ * allocating library routine).
+ *   - Limit: fp8_quantize_dbias_workspace_bytes(rows, cols) <=
+ *     4 * FP8MP_NOALLOC_DBIAS_SCRATCH_FLOATS (any rows with cols up to
+ *     1040432); larger shapes return FP8MP_ERR_INVALID with a message
+ *     naming the limit.
  *   - The first call on a device looks up the array's device address
- *     (cudaGetSymbolAddress, with that device current) and caches it; make
- *     that first call before any stream capture.
- *   - Every call shares the one array and leaves its partial sums there
- *     (each call writes every entry it reads, so nothing needs clearing).
- *     Calls whose work overlaps on the GPU (other streams, other threads)
- *     race on the array: serialise them, e.g. on one stream.
+ *     (cudaGetSymbolAddress, with that device current) and caches it for
+ *     the life of the process; make that first call before any stream
+ *     capture. The cache does not survive cudaDeviceReset: after a reset of
+ *     a device that has called this function, do not call it again in that
+ *     process.
+ *   - The array starts zero-filled (the loader clears it) and every call
+ *     leaves it zero again, which is what the counters need. Calls whose
+ *     work overlaps on the GPU (other streams, other threads) race on the
+ *     array: serialise them, e.g. on one stream.
  */
 int fp8_quantize_dbias_noalloc(const void *x, int32_t x_dtype, int64_t rows, int64_t cols, int32_t fmt,
                                const float *scale, uint8_t *out, uint8_t *out_t, float *amax, void *dbias,

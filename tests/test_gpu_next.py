@@ -58,7 +58,7 @@ def dbias_check(got, ref, ab, rows, bf16):
     assert (err <= bound).all(), (err / bound).max()
 
 
-@pytest.mark.parametrize("rows,cols", [(16, 16), (144, 272), (1040, 784), (8192, 4096)])
+@pytest.mark.parametrize("rows,cols", [(16, 16), (144, 272), (1040, 784), (16, 4096), (4112, 16), (8192, 4096)])
 @pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
 @pytest.mark.parametrize("db_dtype", [torch.float32, torch.bfloat16])
 def test_dbias_fused_in_gradient_cast(cuda_lib, orc, rows, cols, dtype, db_dtype):
@@ -70,7 +70,7 @@ def test_dbias_fused_in_gradient_cast(cuda_lib, orc, rows, cols, dtype, db_dtype
     out_t = torch.empty((cols, rows), dtype=torch.uint8, device="cuda")
     am = torch.zeros(1, device="cuda")
     db = torch.empty(cols, dtype=db_dtype, device="cuda")
-    ws = torch.empty(cuda_lib.fp8_quantize_dbias_workspace_bytes(rows, cols) // 4, dtype=torch.float32,
+    ws = torch.zeros(cuda_lib.fp8_quantize_dbias_workspace_bytes(rows, cols) // 4, dtype=torch.float32,
                      device="cuda")
     cuda_lib.fp8_quantize_dbias(dy.cuda(), E5M2, scale, out, out_t, db, ws, amax=am)
     assert cuda_lib.fp8mp_check() == 0
@@ -94,7 +94,7 @@ def test_dbias_without_transposed_copy(cuda_lib, orc, rows, cols):
     g = workloads.gen(3 * rows + cols)
     dy = (torch.randn((rows, cols), generator=g) * 1e-3).to(torch.bfloat16).cuda()
     scale = torch.tensor([8192.0], device="cuda")
-    ws = torch.empty(cuda_lib.fp8_quantize_dbias_workspace_bytes(rows, cols) // 4, dtype=torch.float32,
+    ws = torch.zeros(cuda_lib.fp8_quantize_dbias_workspace_bytes(rows, cols) // 4, dtype=torch.float32,
                      device="cuda")
     out, am, db = (torch.empty((rows, cols), dtype=torch.uint8, device="cuda"), torch.zeros(1, device="cuda"),
                    torch.empty(cols, device="cuda"))
@@ -108,6 +108,37 @@ def test_dbias_without_transposed_copy(cuda_lib, orc, rows, cols):
     assert torch.equal(out, out2) and torch.equal(am, am2) and torch.equal(db, db2)
     ref, ab = orc.dbias(dyn)
     dbias_check(np_view(db), ref, ab, rows, False)
+
+
+def test_dbias_leaves_its_workspace_zero_across_shapes(cuda_lib, orc):
+    """One zero-filled workspace serves calls of different shapes in turn:
+    every call sets the tile sums and arrival counters it used back to zero
+    (the last tile of each column strip does), so each call starts from a
+    zero workspace and gets the oracle's codes and a bias gradient within the
+    summation bound."""
+    shapes = [(1040, 784), (144, 2064), (4112, 16), (2064, 1552), (1040, 784)]
+    need = max(cuda_lib.fp8_quantize_dbias_workspace_bytes(r, c) for r, c in shapes)
+    ws = torch.zeros(need // 4, dtype=torch.float32, device="cuda")
+    scale = torch.tensor([1024.0], device="cuda")
+    for i, (rows, cols) in enumerate(shapes):
+        g = workloads.gen(1000 + i)
+        dy = (torch.randn((rows, cols), generator=g) * 1e-3 - 3e-4 * i).to(torch.bfloat16)
+        dyn = np_view(dy)
+        out = torch.empty((rows, cols), dtype=torch.uint8, device="cuda")
+        out_t = torch.empty((cols, rows), dtype=torch.uint8, device="cuda") if i % 2 == 0 else None
+        db = torch.empty(cols, dtype=torch.float32, device="cuda")
+        am = torch.zeros(1, device="cuda")
+        cuda_lib.fp8_quantize_dbias(dy.cuda(), E5M2, scale, out, out_t, db, ws, amax=am)
+        assert cuda_lib.fp8mp_check() == 0
+        torch.cuda.synchronize()
+        assert int(torch.count_nonzero(ws)) == 0, f"call {i}: workspace not left zero"
+        q = orc.cast(dyn, 1024.0, E5M2)
+        assert_same_bits(out.cpu().numpy(), q, f"codes {i}")
+        if out_t is not None:
+            assert_same_bits(out_t.cpu().numpy(), orc.transpose_u8(q), f"transposed {i}")
+        assert_same_bits(np_view(am), np.array([orc.amax(dyn)], np.float32), f"amax {i}")
+        ref, ab = orc.dbias(dyn)
+        dbias_check(np_view(db), ref, ab, rows, False)
 
 
 def test_dbias_rejects_small_workspace(cuda_lib):

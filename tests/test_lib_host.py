@@ -185,3 +185,33 @@ def test_missing_library_fails_loudly(tmp_path):
             fp8mp.load(str(tmp_path / "nope.so"))
         finally:
             fp8mp._lib = saved
+
+
+def test_dbias_workspace_size_and_noalloc_limit(lib):
+    """The workspace holds the column sums of each of the k CTAs of a
+    128-column strip (k = min(ceil(rows / 128), max(1, 152 // strips))) plus
+    one arrival counter per strip, rounded up to 16 bytes; the allocation-free
+    variant refuses, before any CUDA call, shapes whose workspace exceeds its
+    fixed array -- including shapes whose size product would overflow."""
+    ws = fp8mp.fp8_quantize_dbias_workspace_bytes
+
+    def closed_form(rows, cols):
+        tr, tc = -(-rows // 128), -(-cols // 128)
+        k = max(1, min(tr, 152 // tc if tc else 1))
+        return (k * cols * 4 + tc * 4 + 15) // 16 * 16
+
+    for rows, cols in ((8192, 4096), (16, 16), (1040, 784), (16384, 14336), (1024, 768), (128, 16), (4112, 16),
+                       (0, 4096), (65536, 1 << 20)):
+        assert ws(rows, cols) == closed_form(rows, cols), (rows, cols)
+    assert ws(8192, 4096) == 4 * 4096 * 4 + 32 * 4  # 4 CTAs per strip
+    assert ws(16, 16) == 16 * 4 + 16  # one CTA's 16 sums and one counter, padded to 16
+    assert ws(-1, 16) == -1
+    assert ws(1 << 40, 1 << 20) == -1  # beyond 2^40 elements: no overflowing product
+    limit = 4 * fp8mp.NOALLOC_DBIAS_SCRATCH_FLOATS
+    assert ws(16384, 1040432) <= limit < ws(16384, 1040448)
+    assert ws(65536, 16384) <= limit
+    P = 4096  # fake aligned address, never dereferenced: validation fails first
+    for rows, cols in ((16384, 1040448), (1 << 40, 1 << 20), (1 << 62, 1 << 62)):
+        rc = lib.fp8_quantize_dbias_noalloc(P, 1, rows, cols, 1, P, P, None, None, P, 0, None)
+        assert rc == fp8mp.ERR_INVALID, (rows, cols)
+        assert "scratch" in fp8mp.last_error()
