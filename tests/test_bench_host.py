@@ -1,9 +1,10 @@
 """Host logic of bench.py on the CPU: the max-over-ranks timing reduction and
 barrier on a world-size-2 gloo group, rank gating of the reference arm, the
-clock-sample parsing, and the ncu-summary lookup that keys traffic to the
-GEMM source it was measured on."""
+clock-sample parsing, the ncu CSV ingest, and the traffic lookup that keys
+DRAM bytes to the GEMM source they were measured on."""
 
 import hashlib
+import json
 import os
 import socket
 
@@ -74,11 +75,50 @@ def test_clock_summary_flags_throttle():
 def test_traffic_lookup_is_keyed_to_the_gemm_source(tmp_path, monkeypatch):
     src = tmp_path / "gemm.cu"
     src.write_text("kernel v1")
-    prof = tmp_path / "prof.md"
+    rec = tmp_path / "traffic.json"
     sha = hashlib.sha256(b"kernel v1").hexdigest()
-    prof.write_text(f"- gemm_cu_sha256: `{sha}`\n- dram_bytes_per_launch: 123456\n")
+    rec.write_text(json.dumps({"gemm_cu_sha256": sha, "dram_bytes_per_launch": {"fwd": 100.0, "bwd": 300.0}}))
     monkeypatch.setattr(bench, "GEMM_SRC", str(src))
-    monkeypatch.setattr(bench, "PROFILE", str(prof))
-    assert bench.gemm_traffic_from_profile() == 123456.0
+    monkeypatch.setattr(bench, "TRAFFIC", str(rec))
+    assert bench.gemm_traffic("fwd") == 100.0 and bench.gemm_traffic("bwd") == 300.0
+    assert bench.gemm_traffic() == 200.0
     src.write_text("kernel v2")  # the kernel changed since the capture
-    assert bench.gemm_traffic_from_profile() is None
+    assert bench.gemm_traffic() is None and bench.gemm_traffic("fwd") is None
+    rec.unlink()
+    assert bench.gemm_traffic() is None
+
+
+RAW_CSV = """"ID","Process ID","Kernel Name","dram__bytes_read.sum","dram__bytes_write.sum","gpu__time_duration.sum"
+"","","","Mbyte","Kbyte","us"
+"0","7","void fp8mp::gemm_fp8_kernel<1>(fp8mp::Params)","59.25","31,600.5","78.0"
+"1","7","void fp8mp::cast_rows_kernel<1, 1>(const void *)","67.1","3,500.0","16.0"
+"2","7","void fp8mp::gemm_fp8_kernel<1>(fp8mp::Params)","110.4","63,200","152.8"
+"3","7","void fp8mp::gemm_fp8_kernel<1>(fp8mp::Params)","61.25","31,600.5","78.0"
+"""
+
+LONG_CSV = """"ID","Process ID","Process Name","Host Name","Kernel Name","Context","Stream","Section Name","Metric Name","Metric Unit","Metric Value"
+"4","7","python","box","gemm_fp8_kernel<1>","1","7","Command line profiler metrics","dram__bytes_read.sum","Gbyte","0.1104"
+"4","7","python","box","gemm_fp8_kernel<1>","1","7","Command line profiler metrics","dram__bytes_write.sum","Mbyte","63.2"
+"4","7","python","box","gemm_fp8_kernel<1>","1","7","Command line profiler metrics","gpu__time_duration.sum","us","152.8"
+"""
+
+
+def test_ncu_csv_ingest_both_exports(tmp_path, monkeypatch):
+    """The GEMM launches' DRAM bytes are read from either ncu CSV export,
+    units applied, other kernels skipped, launches labelled fwd / bwd in
+    capture order; the record is keyed to the current gemm.cu."""
+    raw = tmp_path / "raw.csv"
+    raw.write_text(RAW_CSV)
+    by, launches = bench.parse_ncu_dram_csv(str(raw))
+    assert [e["label"] for e in launches] == ["fwd", "bwd", "fwd"]
+    assert by["fwd"] == pytest.approx((59.25e6 + 31.6005e6 + 61.25e6 + 31.6005e6) / 2)
+    assert by["bwd"] == pytest.approx(110.4e6 + 63.2e6)
+    long = tmp_path / "long.csv"
+    long.write_text(LONG_CSV)
+    by2, launches2 = bench.parse_ncu_dram_csv(str(long), labels=("bwd",))
+    assert by2 == {"bwd": pytest.approx(110.4e6 + 63.2e6)} and launches2[0]["id"] == 4
+    out = tmp_path / "traffic.json"
+    monkeypatch.setattr(bench, "TRAFFIC", str(out))
+    rec = bench.ingest_ncu(str(raw), "ncu ... python bench.py")
+    assert rec["gemm_cu_sha256"] == bench.gemm_source_sha256()
+    assert bench.gemm_traffic("bwd") == pytest.approx(173.6e6)
