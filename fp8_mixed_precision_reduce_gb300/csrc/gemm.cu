@@ -67,7 +67,7 @@ constexpr int TILE_N = 256;       // output columns per tile (TMEM columns per a
 constexpr int ROWS_A = 128;       // rows of A each CTA stages (TMEM lanes)
 constexpr int NUM_EPI_WARPS = 4;
 constexpr int NUM_THREADS = 64 + 32 * NUM_EPI_WARPS;
-constexpr int GROUP_M = 16;       // tile raster: 16 row-blocks per group
+constexpr int GROUP_M = 16;       // tile raster: at most 16 row-blocks per group
 constexpr uint32_t TMEM_COLS = 2 * TILE_N;
 
 template <bool PAIR>
@@ -97,6 +97,7 @@ struct Cfg {
 struct GemmParams {
     int rows_a, rows_b, num_kb;
     int tiles_m, tiles_n;
+    int group_m;              // tile raster: row-blocks per group
     int a_mn, b_mn;           // operand stored MN-major ([kc x rows], contiguous along M / N)
     uint32_t idesc;           // tcgen05 instruction descriptor (operand formats, majors, M, N)
     const float *sinv_a, *sinv_b;
@@ -331,12 +332,12 @@ __device__ __forceinline__ int tile_problem(const GemmBatch &b, int t, int &loca
 }
 
 // Tile index -> (row-block of A, row-block of B), grouped so that the CTAs
-// working at the same time share GROUP_M A panels and a few B panels in L2.
-__device__ __forceinline__ void tile_coords(int t, int tiles_m, int tiles_n, int &mb, int &nb) {
-    const int group = GROUP_M * tiles_n;
+// working at the same time share group_m A panels and a few B panels in L2.
+__device__ __forceinline__ void tile_coords(int t, int tiles_m, int tiles_n, int group_m, int &mb, int &nb) {
+    const int group = group_m * tiles_n;
     const int g = t / group;
-    const int first = g * GROUP_M;
-    const int gm = min(tiles_m - first, GROUP_M);
+    const int first = g * group_m;
+    const int gm = min(tiles_m - first, group_m);
     const int local = t - g * group;
     mb = first + local % gm;
     nb = local / gm;
@@ -439,7 +440,7 @@ gemm_fp8_kernel(const __grid_constant__ GemmBatch batch) {
                 int local;
                 const GemmProblem &P = batch.prob[tile_problem(batch, tile, local)];
                 int mb, nb;
-                tile_coords(local, P.p.tiles_m, P.p.tiles_n, mb, nb);
+                tile_coords(local, P.p.tiles_m, P.p.tiles_n, P.p.group_m, mb, nb);
                 const int a_row = mb * C::TILE_M + static_cast<int>(rank) * ROWS_A;
                 const int b_row = nb * TILE_N + static_cast<int>(rank) * C::ROWS_B;
                 const int num_kb = P.p.num_kb;
@@ -576,7 +577,7 @@ gemm_fp8_kernel(const __grid_constant__ GemmBatch batch) {
             const int bias_bf16 = P.p.bias_bf16;
             const int rows_a = P.p.rows_a, rows_b = P.p.rows_b;
             int mb, nb;
-            tile_coords(local, P.p.tiles_m, P.p.tiles_n, mb, nb);
+            tile_coords(local, P.p.tiles_m, P.p.tiles_n, P.p.group_m, mb, nb);
             const int64_t m = static_cast<int64_t>(mb) * C::TILE_M + row_in_tile;
             const bool row_ok = m < rows_a;
             const int warp_row0 = mb * C::TILE_M + static_cast<int>(rank) * ROWS_A + q * 32;
@@ -793,6 +794,19 @@ int make_tmap(CUtensorMap *map, const void *ptr, uint64_t inner, uint64_t outer,
     return FP8MP_OK;
 }
 
+// Row-blocks per raster group of a problem with contraction length kc: as
+// many A panels (tile_m rows x kc bytes) as fit in 32 MB, at most GROUP_M.
+// Long contractions (the MLP's 14336- and 16384-long ones) get groups of 8-9
+// row-blocks, the others stay at 16: measured, the MLP-down forward launch
+// 560 against 588 us, the other workload shapes within noise.
+int raster_group(int64_t kc, int tile_m) {
+    const int64_t panel = static_cast<int64_t>(tile_m) * kc;
+    int64_t g = (32ll << 20) / (panel > 0 ? panel : 1);
+    if (g > GROUP_M) g = GROUP_M;
+    if (g < 1) g = 1;
+    return static_cast<int>(g);
+}
+
 constexpr uint32_t make_idesc(int fmt_a, int fmt_b, int m, int a_mn, int b_mn) {
     return (1u << 4)                                    // accumulator: f32
            | (static_cast<uint32_t>(fmt_a) << 7)        // A: 0 = E4M3, 1 = E5M2
@@ -930,6 +944,7 @@ int launch_gemms(const GemmDesc *descs, int n, cudaStream_t s, const DeviceInfo 
         p.num_kb = static_cast<int>((d.kc + BK - 1) / BK);
         p.tiles_n = static_cast<int>((d.rows_b + TILE_N - 1) / TILE_N);
         p.tiles_m = static_cast<int>(pair ? (d.rows_a + 255) / 256 : (d.rows_a + 127) / 128);
+        p.group_m = raster_group(d.kc, pair ? 256 : 128);
         p.a_mn = d.a_mn;
         p.b_mn = d.b_mn;
         p.idesc = make_idesc(d.fmt_a, d.fmt_b, pair ? 256 : 128, d.a_mn, d.b_mn);
