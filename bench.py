@@ -869,7 +869,13 @@ def kernel_table(args):
             if rows == 8192:
                 sinv = torch.ones(1, device="cuda")
                 us = timed(lambda: fp8mp.fp8_quantize_current(x, fp8mp.E4M3, sc, sinv, am, q, None))
-                emit("current scaling: amax pass + scale + cast", wl, us, 5.0 * x.numel(), "hbm")
+                # the operation reads x twice (amax pass, then the cast) and
+                # writes the codes: 5 B/elem. It runs as one cooperative launch
+                # whose second read of x comes from L2 when x fits there, so
+                # the fraction of the 3 B/elem that must cross the DRAM
+                # interface is reported beside it.
+                emit("current scaling: amax, grid barrier, scale and cast in one launch", wl, us, 5.0 * x.numel(),
+                     "hbm", dram_minimum_frac=round(3.0 * x.numel() / us / 1e3 / hbm, 4))
             del q, qt
         if blk is not None and only in cast_wls[2]:
             dy = blk.dy_proj

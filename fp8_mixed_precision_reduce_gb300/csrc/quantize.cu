@@ -726,6 +726,148 @@ amax_kernel(const void *__restrict__ x, int64_t n, float *__restrict__ amax_p) {
     block_amax_atomic(am, amax_p);
 }
 
+// Current scaling in one cooperative launch (row-major output): every block
+// takes the amax of its grid-stride share of x, loading it with an L2
+// evict-last policy; the blocks meet at a grid barrier counted in the
+// caller's scale_inv word (the arrival count; zeroed, with *amax, by a
+// one-thread kernel just before); every block then derives the same scale
+// from the tensor's amax and the old scale it read before arriving, and casts
+// the same share again -- now read from L2 when x fits there -- and the last
+// block to finish writes scale and scale_inv. The barrier wait is bounded
+// (about 2 s); on expiry the block raises the casts' timeout flag and skips
+// its cast (the outputs are then undefined; fp8mp_check() reports it).
+constexpr long long kGridWaitCycles = 4000000000ll;
+
+__device__ __forceinline__ uint64_t l2_evict_last_policy() {
+    uint64_t p;
+    asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
+    return p;
+}
+__device__ __forceinline__ uint4 ld_keep_in_l2(const uint4 *ptr, uint64_t pol) {
+    uint4 r;
+    asm volatile("ld.global.L2::cache_hint.v4.u32 {%0, %1, %2, %3}, [%4], %5;"
+                 : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+                 : "l"(ptr), "l"(pol)
+                 : "memory");
+    return r;
+}
+
+template <int FMT, bool BF16>
+__global__ void __launch_bounds__(kThreads, 4)
+current_cast_kernel(const void *__restrict__ x, int64_t n, int margin, float *__restrict__ scale_p,
+                    float *__restrict__ scale_inv_p, float *__restrict__ amax_p, uint8_t *__restrict__ out) {
+    pdl_wait();
+    __shared__ float s_scale;
+    __shared__ int s_ok;
+    const float old_scale = *scale_p;  // read before this block arrives at the barrier
+    const int64_t nchunk = n >> 4;
+    const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+    const int64_t t0 = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+    constexpr int V = BF16 ? 2 : 4;  // 16-byte vectors per 16-element chunk
+    const uint4 *x4 = reinterpret_cast<const uint4 *>(x);
+    const uint64_t pol = l2_evict_last_policy();
+    float am = 0.0f;
+    // ---- phase 1: amax, two chunks' loads in flight per thread
+    for (int64_t c = t0; c < nchunk; c += 2 * stride) {
+        uint4 v[2][V];
+#pragma unroll
+        for (int u = 0; u < 2; ++u) {
+            const int64_t cc = c + u * stride;
+            if (cc < nchunk) {
+#pragma unroll
+                for (int k = 0; k < V; ++k) v[u][k] = ld_keep_in_l2(x4 + V * cc + k, pol);
+            } else {
+#pragma unroll
+                for (int k = 0; k < V; ++k) v[u][k] = make_uint4(0u, 0u, 0u, 0u);
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < 2; ++u) {
+#pragma unroll
+            for (int k = 0; k < V; ++k) {
+                const uint32_t w[4] = {v[u][k].x, v[u][k].y, v[u][k].z, v[u][k].w};
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    if constexpr (BF16)
+                        am = fmaxf(am, fmaxf(fabsf(__uint_as_float(w[e] << 16)), fabsf(__uint_as_float(w[e] & 0xFFFF0000u))));
+                    else
+                        am = fmaxf(am, fabsf(__uint_as_float(w[e])));
+                }
+            }
+        }
+    }
+    if (blockIdx.x == gridDim.x - 1)
+        for (int64_t i = (nchunk << 4) + threadIdx.x; i < n; i += blockDim.x) am = fmaxf(am, fabsf(load1<BF16>(x, i)));
+    block_amax_atomic(am, amax_p);
+    // ---- grid barrier: arrivals counted in the scale_inv word
+    uint32_t *counter = reinterpret_cast<uint32_t *>(scale_inv_p);
+    if (threadIdx.x == 0) {
+        __threadfence();
+        atomicAdd(counter, 1u);
+        const volatile uint32_t *vc = counter;
+        const long long start = clock64();
+        int ok = 1;
+        while (*vc < gridDim.x) {
+            if (clock64() - start > kGridWaitCycles) {
+                atomicOr(&g_cast_timeout_flag, 1u);
+                ok = 0;
+                break;
+            }
+            __nanosleep(64);
+        }
+        __threadfence();
+        s_ok = ok;
+        s_scale = scale_from_amax(*reinterpret_cast<volatile float *>(amax_p), old_scale, FMT, margin);
+    }
+    __syncthreads();
+    pdl_launch_dependents();
+    const float sc = s_scale;
+    // ---- phase 2: the cast of the same share
+    if (s_ok) {
+        for (int64_t c = t0; c < nchunk; c += stride) {
+            uint32_t o[4], probe = 0;
+            float dummy = 0.0f;
+            if constexpr (BF16) {
+                const uint4 a = __ldcs(x4 + 2 * c), b = __ldcs(x4 + 2 * c + 1);
+                o[0] = cast4_bf16<FMT>(a.x, a.y, sc, dummy, probe);
+                o[1] = cast4_bf16<FMT>(a.z, a.w, sc, dummy, probe);
+                o[2] = cast4_bf16<FMT>(b.x, b.y, sc, dummy, probe);
+                o[3] = cast4_bf16<FMT>(b.z, b.w, sc, dummy, probe);
+            } else {
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    const float4 f = __ldcs(reinterpret_cast<const float4 *>(x4 + 4 * c + j));
+                    o[j] = cast4<FMT>(f.x, f.y, f.z, f.w, sc, dummy, probe);
+                }
+            }
+            if (probe & 0x80808080u) {
+#pragma unroll
+                for (int j = 0; j < 4; ++j) o[j] = canonical_nan<FMT>(o[j]);
+            }
+            reinterpret_cast<uint4 *>(out)[c] = make_uint4(o[0], o[1], o[2], o[3]);
+        }
+        if (blockIdx.x == gridDim.x - 1)
+            for (int64_t i = (nchunk << 4) + threadIdx.x; i < n; i += blockDim.x)
+                out[i] = static_cast<uint8_t>(cvt_pair<FMT>(__fmul_rn(load1<BF16>(x, i), sc), 0.0f) & 0xFFu);
+    }
+    // ---- the last block to finish publishes the scale
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        __threadfence();
+        if (atomicAdd(counter, 1u) == 2u * gridDim.x - 1u) {
+            *scale_p = sc;
+            *scale_inv_p = __fdiv_rn(1.0f, sc);
+        }
+    }
+}
+
+__global__ void zero_two_words_kernel(uint32_t *a, uint32_t *b) {
+    pdl_wait();
+    *a = 0u;
+    *b = 0u;
+    pdl_launch_dependents();
+}
+
 // scale and scale_inv from this tensor's amax (the current-scaling rule).
 __global__ void current_scale_kernel(const float *__restrict__ amax, float *__restrict__ scale,
                                      float *__restrict__ scale_inv, int fmt, int margin) {
@@ -738,9 +880,65 @@ __global__ void current_scale_kernel(const float *__restrict__ amax, float *__re
 
 }  // namespace
 
+// The cooperative current-scaling cast: blocks per SM that fit (queried once
+// per device and instantiation), times the SMs, at most one per 16-element
+// chunk group of 256 threads.
+template <int FMT, bool BF16>
+int launch_current_fused(const void *x, int64_t n, int margin, float *scale, float *scale_inv, float *amax,
+                         uint8_t *out, cudaStream_t s, const DeviceInfo &dev) {
+    static std::atomic<int> per_sm_cache[64];
+    if (dev.device < 0 || dev.device >= 64) return fail(FP8MP_ERR_DEVICE, "device index %d out of range", dev.device);
+    int per_sm = per_sm_cache[dev.device].load(std::memory_order_relaxed);
+    if (per_sm < 1) {
+        const cudaError_t e =
+            cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, current_cast_kernel<FMT, BF16>, kThreads, 0);
+        if (e != cudaSuccess || per_sm < 1)
+            return fail(FP8MP_ERR_LAUNCH, "fp8_quantize_current: occupancy query failed: %s", cudaGetErrorString(e));
+        per_sm_cache[dev.device].store(per_sm, std::memory_order_relaxed);
+    }
+    int64_t blocks = ((n >> 4) + kThreads - 1) / kThreads;
+    const int64_t cap = static_cast<int64_t>(dev.num_sms) * per_sm;
+    if (blocks > cap) blocks = cap;
+    if (blocks < 1) blocks = 1;
+    cudaError_t e = launch_kernel(zero_two_words_kernel, dim3(1), dim3(1), 0, s, reinterpret_cast<uint32_t *>(amax),
+                                  reinterpret_cast<uint32_t *>(scale_inv));
+    if (e != cudaSuccess) return fail(FP8MP_ERR_LAUNCH, "fp8_quantize_current: launch failed: %s", cudaGetErrorString(e));
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(blocks));
+    cfg.blockDim = dim3(kThreads);
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeCooperative;  // every block resident: the grid barrier cannot wait forever
+    attr[0].val.cooperative = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    e = cudaLaunchKernelEx(&cfg, current_cast_kernel<FMT, BF16>, x, n, margin, scale, scale_inv, amax, out);
+    if (e == cudaErrorCooperativeLaunchTooLarge) {
+        cudaGetLastError();  // not sticky: the grid did not fit at once; the caller takes the three-pass path
+        return 1;
+    }
+    if (e != cudaSuccess) return fail(FP8MP_ERR_LAUNCH, "fp8_quantize_current: launch failed: %s", cudaGetErrorString(e));
+    return FP8MP_OK;
+}
+
 int launch_quantize_current(const void *x, int x_dtype, int64_t rows, int64_t cols, int fmt, int margin,
                             float *scale, float *scale_inv, float *amax, uint8_t *out, uint8_t *out_t,
                             cudaStream_t s, const DeviceInfo &dev) {
+    if (out_t == nullptr && rows * cols > 0) {
+        // one cooperative launch; 1 = its grid did not fit at once (nothing
+        // read or written yet beyond *amax and *scale_inv, which the
+        // three-pass path below sets again)
+        const int64_t n = rows * cols;
+        const bool bf16 = x_dtype == FP8MP_BF16;
+        int rc;
+        if (fmt == FP8MP_E4M3)
+            rc = bf16 ? launch_current_fused<FP8MP_E4M3, true>(x, n, margin, scale, scale_inv, amax, out, s, dev)
+                      : launch_current_fused<FP8MP_E4M3, false>(x, n, margin, scale, scale_inv, amax, out, s, dev);
+        else
+            rc = bf16 ? launch_current_fused<FP8MP_E5M2, true>(x, n, margin, scale, scale_inv, amax, out, s, dev)
+                      : launch_current_fused<FP8MP_E5M2, false>(x, n, margin, scale, scale_inv, amax, out, s, dev);
+        if (rc != 1) return rc;
+    }
     cudaError_t e = cudaMemsetAsync(amax, 0, sizeof(float), s);
     if (e != cudaSuccess) return fail(FP8MP_ERR_LAUNCH, "fp8_quantize_current: memset failed: %s", cudaGetErrorString(e));
     const int64_t n = rows * cols;

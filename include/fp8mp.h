@@ -134,7 +134,13 @@ int fp8_quantize(const void *x, int32_t x_dtype, int64_t rows, int64_t cols, int
  * Arguments as fp8_quantize, plus: margin 0..126; scale (in/out, device fp32,
  * the fallback when the amax is zero or not finite); scale_inv and amax
  * (out, device fp32; *amax is overwritten, not max-merged).
- * Traffic: the amax pass reads x once more (bf16 + transpose: 6 B/elem).
+ * Without out_t the three passes are one cooperative launch (after a
+ * one-thread kernel that zeroes *amax and *scale_inv, the latter then
+ * counting the blocks at a bounded grid barrier): every block casts the
+ * share it measured, whose second read comes from L2 when x fits there. If
+ * the device cannot run that grid at once, the three passes run as separate
+ * launches. Traffic: the amax pass reads x once more (bf16: 5 B/elem; with
+ * the transposed copy 6 B/elem).
  */
 int fp8_quantize_current(const void *x, int32_t x_dtype, int64_t rows, int64_t cols, int32_t fmt,
                          int32_t margin, float *scale, float *scale_inv, float *amax, uint8_t *out,

@@ -34,6 +34,36 @@ def test_current_scaling(cuda_lib, orc, rows, cols, dtype, fmt):
         assert_same_bits(np_view(am), m.cur_amax, "amax")
 
 
+@pytest.mark.parametrize("rows,cols", [(1, 7), (16, 16), (1000, 333), (4096, 4096), (8192, 4096)])
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
+@pytest.mark.parametrize("fmt", [E4M3, E5M2])
+def test_current_scaling_row_only(cuda_lib, orc, rows, cols, dtype, fmt):
+    """Without a transposed copy the whole current-scaling cast is one
+    cooperative launch (amax, grid barrier, scale, cast of the same share):
+    codes, scale, scale_inv and amax bit-exact against the oracle, on sizes
+    from a tail-only 7 elements to several grid-stride passes, twice in a row
+    (the second call starts from the first call's scale)."""
+    g = workloads.gen(3 * rows + cols + fmt)
+    x = (torch.randn((rows, cols), generator=g) * 3).to(dtype)
+    xn = np_view(x)
+    xd = x.cuda()
+    for margin in (0, 2):
+        scale = torch.tensor([0.5], device="cuda")
+        sinv = torch.full((1,), 7.0, device="cuda")
+        am = torch.full((1,), 123.0, device="cuda")
+        out = torch.empty((rows, cols), dtype=torch.uint8, device="cuda")
+        scale0 = 0.5
+        for call in range(2):
+            cuda_lib.fp8_quantize_current(xd, fmt, scale, sinv, am, out, None, margin=margin)
+            assert cuda_lib.fp8mp_check() == 0
+            q, m = orc.cast_current(xn, fmt, margin=margin, scale0=scale0)
+            assert_same_bits(out.cpu().numpy(), q, f"codes call {call}")
+            assert_same_bits(np_view(scale), m.scale, "scale")
+            assert_same_bits(np_view(sinv), m.scale_inv, "scale_inv")
+            assert_same_bits(np_view(am), m.cur_amax, "amax")
+            scale0 = float(m.scale[0])
+
+
 def test_current_scaling_degenerate(cuda_lib, orc):
     for fill in (0.0, float("inf"), float("nan")):
         x = torch.full((32, 32), fill, dtype=torch.float32)
