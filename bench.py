@@ -7,7 +7,9 @@ transformer workload (M = 8192 tokens, K = N = 4096, bf16 activations with
 through the library's entry points on one CUDA stream:
   fp8_quantize(x -> X8, amax)                    E4M3, row-major only
   fp8_linear_fwd(X8, W8 -> Y bf16, amax_y)       W8: the weight's E4M3 copy
-  fp8_quantize(dY -> dY8, amax)                  E5M2, row-major only
+  fp8_quantize_ex(dY -> dY8, amax,               E5M2, row-major only; dY is an
+                  FP8MP_OVERLAP_PREVIOUS)        input of the step, so its cast runs
+                                                 beside the forward GEMM
   fp8_linear_bwd_rowmajor(dY8, W8, X8            dgrad and wgrad GEMMs in one
                           -> dX bf16, dW bf16)   launch, no transposed copies;
                                                  the wgrad epilogue flags an
@@ -283,13 +285,14 @@ def max_over_ranks(value: float, world: int) -> float:
 class LinearStep:
     """Device state and the step of the proj linear, through the library."""
 
-    def __init__(self, m=M_TOK, k=K_IN, n=N_OUT, seed=3, prescanned=True):
+    def __init__(self, m=M_TOK, k=K_IN, n=N_OUT, seed=3, prescanned=True, overlap_dy_cast=True):
         import torch
 
         import fp8_mixed_precision_reduce_gb300 as fp8mp
         import workloads
 
         self.fp8mp = fp8mp
+        self.overlap_dy_cast = overlap_dy_cast
         self.m, self.k, self.n = m, k, n
         dev = "cuda"
         tb = workloads.transformer_block(seed=seed, m=m, d=k, device=dev)
@@ -334,7 +337,12 @@ class LinearStep:
         f.fp8_linear_fwd(self.X8, self.W8, self.mx.scale_inv, self.mw.scale_inv, y, y_amax=self.my.cur_amax)
         if ev is not None:
             ev[1].record()
-        f.fp8_quantize(dy, f.E5M2, self.md.scale, self.D8, None, self.md.cur_amax)
+        if self.overlap_dy_cast:
+            # dY is an input of the step, not the forward GEMM's result: its
+            # cast may run beside the GEMM (it still completes after it)
+            f.fp8_quantize_ex(dy, f.E5M2, self.md.scale, self.D8, None, self.md.cur_amax, flags=f.OVERLAP_PREVIOUS)
+        else:
+            f.fp8_quantize(dy, f.E5M2, self.md.scale, self.D8, None, self.md.cur_amax)
         if ev is not None:
             ev[2].record()
         f.fp8_linear_bwd_rowmajor(self.D8, self.W8, self.X8, self.md.scale_inv, self.mw.scale_inv,
@@ -477,7 +485,7 @@ def run_ours(args, world, rank, local):
 
     peaks, peak_kind = load_peaks()
     lib_fp8 = library_fp8_gemm_tflops()
-    st = LinearStep(prescanned=not args.master_scans_dw)
+    st = LinearStep(prescanned=not args.master_scans_dw, overlap_dy_cast=not args.no_overlap)
     torch.cuda.synchronize()
     flush = torch.empty(int(2 * 129e6 // 4) + 1, dtype=torch.float32, device="cuda")  # > 2x L2
 
@@ -590,7 +598,9 @@ def run_ours(args, world, rank, local):
                    "amax_compute_algo": "most_recent", "recipe": "HYBRID", "parallelism": f"replicas x{world}",
                    "l2": "flushed (2x L2 write) between timed steps", "launch": launch,
                    "overflow_check": "master step scans dW" if args.master_scans_dw
-                   else "wgrad epilogue flags Inf/NaN in the stored dW; the master step reads the flag"},
+                   else "wgrad epilogue flags Inf/NaN in the stored dW; the master step reads the flag",
+                   "dy_cast": "plain, after the forward GEMM" if args.no_overlap
+                   else "enqueued after the forward GEMM with FP8MP_OVERLAP_PREVIOUS: runs beside it"},
         "gemm_only": {"tflops": round(world * fl / (gemm_step_ms * 1e-3) / 1e12, 2), "ms_per_step": round(gemm_step_ms, 5),
                       "fwd_ms": round(fwd_ms, 5), "bwd_ms": round(bwd_ms, 5),
                       "from": "a second pass of K steps with timing events around the GEMM launches",
@@ -959,6 +969,8 @@ def main(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--master-scans-dw", action="store_true",
                     help="the master step scans dW for Inf/NaN itself instead of reading the wgrad epilogue's flag")
+    ap.add_argument("--no-overlap", action="store_true",
+                    help="cast dY with a plain fp8_quantize instead of letting it run beside the forward GEMM")
     ap.add_argument("--eager", action="store_true",
                     help="launch every library call from Python in the timed steps instead of replaying graphs")
     ap.add_argument("--kernels", action="store_true",

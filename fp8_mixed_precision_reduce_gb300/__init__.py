@@ -24,7 +24,7 @@ OK, ERR_INVALID, ERR_DEVICE, ERR_LAUNCH, ERR_TIMEOUT = 0, -1, -2, -3, -4
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "libfp8mp.so")
-EXPORTS = ("fp8_quantize", "fp8_quantize_current", "fp8_quantize_dbias",
+EXPORTS = ("fp8_quantize", "fp8_quantize_ex", "fp8_quantize_current", "fp8_quantize_dbias",
            "fp8_quantize_dbias_workspace_bytes", "fp8_quantize_dbias_noalloc", "fp8_linear_fwd", "fp8_linear_fwd_fp8out", "fp8_linear_dgrad", "fp8_linear_wgrad",
            "fp8_linear_bwd", "fp8_linear_bwd_rowmajor", "delayed_scaling_update", "mp_master_step", "mp_master_step_adam", "mp_master_step_prescanned",
            "mp_master_step_adam_prescanned", "fp8mp_check", "fp8mp_last_error",
@@ -65,6 +65,7 @@ def load(path: str | None = None):
     L = ctypes.CDLL(path)
     P, I64, I32, F = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int32, ctypes.c_float
     L.fp8_quantize.argtypes = [P, I32, I64, I64, I32, P, P, P, P, P]
+    L.fp8_quantize_ex.argtypes = [P, I32, I64, I64, I32, P, P, P, P, ctypes.c_uint32, P]
     L.fp8_quantize_current.argtypes = [P, I32, I64, I64, I32, I32, P, P, P, P, P, P]
     L.fp8_quantize_dbias.argtypes = [P, I32, I64, I64, I32, P, P, P, P, P, I32, P, I64, P]
     L.fp8_quantize_dbias_noalloc.argtypes = [P, I32, I64, I64, I32, P, P, P, P, P, I32, P]
@@ -86,7 +87,7 @@ def load(path: str | None = None):
     L.fp8mp_selftest_barrier_timeout.argtypes = [P]
     L.fp8mp_last_error.restype = ctypes.c_char_p
     L.fp8mp_version.restype = I32
-    for name in ("fp8_quantize", "fp8_quantize_current", "fp8_quantize_dbias", "fp8_quantize_dbias_noalloc",
+    for name in ("fp8_quantize", "fp8_quantize_ex", "fp8_quantize_current", "fp8_quantize_dbias", "fp8_quantize_dbias_noalloc",
                  "fp8_linear_fwd", "fp8_linear_fwd_fp8out", "fp8_linear_dgrad", "fp8_linear_wgrad",
                  "fp8_linear_bwd", "fp8_linear_bwd_rowmajor", "delayed_scaling_update", "mp_master_step", "mp_master_step_adam",
                  "mp_master_step_prescanned", "mp_master_step_adam_prescanned", "fp8mp_check",
@@ -146,6 +147,21 @@ def fp8_quantize(x: torch.Tensor, fmt: int, scale: torch.Tensor, out: torch.Tens
     rows, cols = _rows_cols(x)
     _check(load().fp8_quantize(_ptr(x), _dtype_code(x), rows, cols, fmt, _ptr(scale), _ptr(out),
                                _ptr(out_t), _ptr(amax), _stream(stream)))
+
+
+OVERLAP_PREVIOUS = 1  # fp8_quantize_ex flag
+
+
+def fp8_quantize_ex(x: torch.Tensor, fmt: int, scale: torch.Tensor, out: torch.Tensor,
+                    out_t: torch.Tensor | None = None, amax: torch.Tensor | None = None, flags: int = 0,
+                    stream=None) -> None:
+    """fp8_quantize with flags. OVERLAP_PREVIOUS: the caller guarantees that the
+    work enqueued before this call neither writes nor reads x, out, out_t or
+    amax, so the cast may run while the previous kernel is still running; the
+    call still completes after it."""
+    rows, cols = _rows_cols(x)
+    _check(load().fp8_quantize_ex(_ptr(x), _dtype_code(x), rows, cols, fmt, _ptr(scale), _ptr(out),
+                                  _ptr(out_t), _ptr(amax), flags, _stream(stream)))
 
 
 def fp8_quantize_current(x: torch.Tensor, fmt: int, scale: torch.Tensor, scale_inv: torch.Tensor,

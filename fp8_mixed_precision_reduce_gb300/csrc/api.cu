@@ -145,12 +145,13 @@ int32_t fp8mp_version(void) { return 1; }
 
 const char *fp8mp_last_error(void) { return last_error_message(); }
 
-int fp8_quantize(const void *x, int32_t x_dtype, int64_t rows, int64_t cols, int32_t fmt, const float *scale,
-                 uint8_t *out, uint8_t *out_t, float *amax, void *stream) {
-    const char *fn = "fp8_quantize";
+static int quantize_entry(const char *fn, const void *x, int32_t x_dtype, int64_t rows, int64_t cols, int32_t fmt,
+                          const float *scale, uint8_t *out, uint8_t *out_t, float *amax, uint32_t flags,
+                          void *stream) {
     clear_error();
     REQUIRE(valid_dtype(x_dtype), "%s: x_dtype %d is not FP8MP_F32 or FP8MP_BF16", fn, x_dtype);
     REQUIRE(valid_fmt(fmt), "%s: fmt %d is not FP8MP_E4M3 or FP8MP_E5M2", fn, fmt);
+    REQUIRE((flags & ~static_cast<uint32_t>(FP8MP_OVERLAP_PREVIOUS)) == 0u, "%s: unknown flags 0x%x", fn, flags);
     REQUIRE(rows >= 0 && cols >= 0, "%s: negative size", fn);
     REQUIRE(rows <= (1ll << 40) / (cols > 0 ? cols : 1), "%s: tensor too large", fn);
     if (out_t != nullptr)
@@ -167,7 +168,17 @@ int fp8_quantize(const void *x, int32_t x_dtype, int64_t rows, int64_t cols, int
     int rc = current_device(&dev);
     if (rc) return rc;
     return launch_quantize(x, x_dtype, rows, cols, fmt, scale, out, out_t, amax, static_cast<cudaStream_t>(stream),
-                           dev);
+                           dev, (flags & FP8MP_OVERLAP_PREVIOUS) != 0u);
+}
+
+int fp8_quantize(const void *x, int32_t x_dtype, int64_t rows, int64_t cols, int32_t fmt, const float *scale,
+                 uint8_t *out, uint8_t *out_t, float *amax, void *stream) {
+    return quantize_entry("fp8_quantize", x, x_dtype, rows, cols, fmt, scale, out, out_t, amax, 0u, stream);
+}
+
+int fp8_quantize_ex(const void *x, int32_t x_dtype, int64_t rows, int64_t cols, int32_t fmt, const float *scale,
+                    uint8_t *out, uint8_t *out_t, float *amax, uint32_t flags, void *stream) {
+    return quantize_entry("fp8_quantize_ex", x, x_dtype, rows, cols, fmt, scale, out, out_t, amax, flags, stream);
 }
 
 int fp8_quantize_current(const void *x, int32_t x_dtype, int64_t rows, int64_t cols, int32_t fmt, int32_t margin,

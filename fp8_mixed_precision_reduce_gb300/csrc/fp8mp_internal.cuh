@@ -68,9 +68,11 @@ int dbias_ctas_per_strip(int64_t rows, int64_t cols);
 int launch_quantize_dbias(const void *x, int x_dtype, int64_t rows, int64_t cols, int fmt, const float *scale,
                           uint8_t *out, uint8_t *out_t, float *amax, void *dbias, int dbias_dtype, float *ws,
                           cudaStream_t s, const DeviceInfo &dev);
+// early: the cast's blocks start without waiting for the previous kernel on
+// the stream (its buffers do not interact with it; FP8MP_OVERLAP_PREVIOUS).
 int launch_quantize(const void *x, int x_dtype, int64_t rows, int64_t cols, int fmt,
                     const float *scale, uint8_t *out, uint8_t *out_t, float *amax,
-                    cudaStream_t s, const DeviceInfo &dev);
+                    cudaStream_t s, const DeviceInfo &dev, bool early = false);
 // One GEMM out[rows_a x rows_b] = (A B^T) * sinv_a * sinv_b (+ bias) over a
 // contraction of length kc. A is [rows_a x kc] (K-major) or, with a_mn,
 // [kc x rows_a] (MN-major); likewise B with rows_b and b_mn.

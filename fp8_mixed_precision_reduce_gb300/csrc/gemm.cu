@@ -431,6 +431,12 @@ gemm_fp8_kernel(const __grid_constant__ GemmBatch batch) {
     if (warp == 0) {
         if (lane == 0) {
             // ---------------- TMA producer (both CTAs of a pair)
+            // The next kernel on the stream may be scheduled from now on: an
+            // ordinary one waits in griddepcontrol.wait for this grid to
+            // complete; one whose buffers this launch does not touch (a cast
+            // enqueued with FP8MP_OVERLAP_PREVIOUS) runs in the registers and
+            // threads this CTA leaves free, during the mainloop.
+            pdl_launch_dependents();
             uint32_t it = 0;
             int issued_stages = 0;
             bool ok = true;
@@ -472,8 +478,6 @@ gemm_fp8_kernel(const __grid_constant__ GemmBatch batch) {
                     if (issued_stages < C::STAGES) ++issued_stages;
                 }
             }
-            // the last loads are issued: the next kernel may be scheduled
-            pdl_launch_dependents();
             if (!ok && rank == 0) {
                 // let the loads already issued land before the CTA goes away
                 for (int j = 1; j <= issued_stages && j <= static_cast<int>(it); ++j) {

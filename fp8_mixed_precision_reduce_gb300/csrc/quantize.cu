@@ -115,11 +115,17 @@ __device__ __forceinline__ uint32_t cast4_bf16(uint32_t w0, uint32_t w1, float s
 // n % 16 tail is done element by element by the last block.
 constexpr int kChunksPerThread = 4;
 
-template <int FMT, bool BF16>
+//
+// EARLY (FP8MP_OVERLAP_PREVIOUS): the caller guarantees that the kernel still
+// running before this one on the stream neither writes nor reads x, out or
+// *amax, so the blocks start without waiting for it (they use what it leaves
+// free of the SMs); block 0 waits for it at its very end, so the grid still
+// completes after it and whatever follows on the stream sees both.
+template <int FMT, bool BF16, bool EARLY>
 __global__ void __launch_bounds__(kThreads, 4)
 cast_rows_kernel(const void *__restrict__ x, int64_t n, const float *__restrict__ scale_p,
                  uint8_t *__restrict__ out, float *__restrict__ amax_p) {
-    pdl_wait();
+    if constexpr (!EARLY) pdl_wait();
     pdl_launch_dependents();
     const float scale = __ldg(scale_p);
     float am = 0.0f;
@@ -191,6 +197,9 @@ cast_rows_kernel(const void *__restrict__ x, int64_t n, const float *__restrict_
         }
     }
     if (amax_p != nullptr) block_amax_atomic(am, amax_p);
+    if constexpr (EARLY) {
+        if (blockIdx.x == 0) pdl_wait();
+    }
 }
 
 // Blocks of cast_rows_kernel / amax_kernel for n elements: one per run of
@@ -215,11 +224,12 @@ inline int64_t row_blocks(int64_t n) {
 // adjacent, so phase 2 moves 16 rows of one column with one 16-byte shared
 // load and one 16-byte store to out_t (eight threads write one 128-byte row
 // segment of out_t).
-template <int FMT, bool BF16>
+// EARLY: as for cast_rows_kernel.
+template <int FMT, bool BF16, bool EARLY>
 __global__ void __launch_bounds__(kThreads, BF16 ? 4 : 3)
 cast_rows_t_kernel(const void *__restrict__ x, int64_t rows, int64_t cols, const float *__restrict__ scale_p,
                    uint8_t *__restrict__ out, uint8_t *__restrict__ out_t, float *__restrict__ amax_p) {
-    pdl_wait();
+    if constexpr (!EARLY) pdl_wait();
     pdl_launch_dependents();
     __shared__ __align__(16) uint32_t sT[128 * 32];
     const int64_t tiles_c = (cols + 127) >> 7;
@@ -307,6 +317,9 @@ cast_rows_t_kernel(const void *__restrict__ x, int64_t rows, int64_t cols, const
         }
     }
     if (amax_p != nullptr) block_amax_atomic(am, amax_p);
+    if constexpr (EARLY) {
+        if (blockIdx.x == 0) pdl_wait();
+    }
 }
 
 // ---------------------------------------------------------------------------
@@ -623,20 +636,20 @@ cast_dbias_kernel(const __grid_constant__ CUtensorMap tmap, int64_t rows, int64_
     }
 }
 
-template <int FMT, bool BF16>
+template <int FMT, bool BF16, bool EARLY>
 int launch_typed(const void *x, int64_t rows, int64_t cols, const float *scale, uint8_t *out,
                  uint8_t *out_t, float *amax, cudaStream_t s) {
     if (out_t == nullptr) {
         const int64_t n = rows * cols;
         const int64_t blocks = row_blocks(n);
         if (blocks > 0x7FFFFFFF) return fail(FP8MP_ERR_INVALID, "fp8_quantize: tensor too large");
-        launch_kernel(cast_rows_kernel<FMT, BF16>, dim3(static_cast<unsigned>(blocks)), dim3(kThreads), 0, s, x, n,
-                      scale, out, amax);
+        launch_kernel(cast_rows_kernel<FMT, BF16, EARLY>, dim3(static_cast<unsigned>(blocks)), dim3(kThreads), 0, s,
+                      x, n, scale, out, amax);
     } else {
         const int64_t tiles = ((rows + 127) >> 7) * ((cols + 127) >> 7);
         if (tiles > 0x7FFFFFFF) return fail(FP8MP_ERR_INVALID, "fp8_quantize: tensor too large");
-        launch_kernel(cast_rows_t_kernel<FMT, BF16>, dim3(static_cast<unsigned>(tiles)), dim3(kThreads), 0, s, x,
-                      rows, cols, scale, out, out_t, amax);
+        launch_kernel(cast_rows_t_kernel<FMT, BF16, EARLY>, dim3(static_cast<unsigned>(tiles)), dim3(kThreads), 0, s,
+                      x, rows, cols, scale, out, out_t, amax);
     }
     const cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return fail(FP8MP_ERR_LAUNCH, "fp8_quantize: launch failed: %s", cudaGetErrorString(e));
@@ -977,13 +990,20 @@ int launch_quantize_dbias(const void *x, int x_dtype, int64_t rows, int64_t cols
 }
 
 int launch_quantize(const void *x, int x_dtype, int64_t rows, int64_t cols, int fmt, const float *scale,
-                    uint8_t *out, uint8_t *out_t, float *amax, cudaStream_t s, const DeviceInfo &) {
+                    uint8_t *out, uint8_t *out_t, float *amax, cudaStream_t s, const DeviceInfo &, bool early) {
     const bool bf16 = x_dtype == FP8MP_BF16;
+    if (early) {
+        if (fmt == FP8MP_E4M3)
+            return bf16 ? launch_typed<FP8MP_E4M3, true, true>(x, rows, cols, scale, out, out_t, amax, s)
+                        : launch_typed<FP8MP_E4M3, false, true>(x, rows, cols, scale, out, out_t, amax, s);
+        return bf16 ? launch_typed<FP8MP_E5M2, true, true>(x, rows, cols, scale, out, out_t, amax, s)
+                    : launch_typed<FP8MP_E5M2, false, true>(x, rows, cols, scale, out, out_t, amax, s);
+    }
     if (fmt == FP8MP_E4M3)
-        return bf16 ? launch_typed<FP8MP_E4M3, true>(x, rows, cols, scale, out, out_t, amax, s)
-                    : launch_typed<FP8MP_E4M3, false>(x, rows, cols, scale, out, out_t, amax, s);
-    return bf16 ? launch_typed<FP8MP_E5M2, true>(x, rows, cols, scale, out, out_t, amax, s)
-                : launch_typed<FP8MP_E5M2, false>(x, rows, cols, scale, out, out_t, amax, s);
+        return bf16 ? launch_typed<FP8MP_E4M3, true, false>(x, rows, cols, scale, out, out_t, amax, s)
+                    : launch_typed<FP8MP_E4M3, false, false>(x, rows, cols, scale, out, out_t, amax, s);
+    return bf16 ? launch_typed<FP8MP_E5M2, true, false>(x, rows, cols, scale, out, out_t, amax, s)
+                : launch_typed<FP8MP_E5M2, false, false>(x, rows, cols, scale, out, out_t, amax, s);
 }
 
 int read_and_clear_cast_timeout_flag(unsigned int *value) {

@@ -120,6 +120,28 @@ typedef struct fp8mp_meta {
 int fp8_quantize(const void *x, int32_t x_dtype, int64_t rows, int64_t cols, int32_t fmt,
                  const float *scale, uint8_t *out, uint8_t *out_t, float *amax, void *stream);
 
+/* Flags of fp8_quantize_ex. */
+#define FP8MP_OVERLAP_PREVIOUS 1u
+
+/*
+ * fp8_quantize_ex -- fp8_quantize with flags. The results are exactly
+ * fp8_quantize's; the flags only change how the work is scheduled.
+ *
+ * FP8MP_OVERLAP_PREVIOUS: the caller guarantees that the work enqueued on
+ *   `stream` before this call neither writes nor reads x, out, out_t or
+ *   *amax (for example the dY cast of a layer's backward pass enqueued right
+ *   after its forward GEMM, when dY does not come from that GEMM). The
+ *   cast's blocks then do not wait for the previous kernel to finish: they
+ *   start as soon as it lets the next kernel be scheduled (the library's
+ *   GEMMs do so at the start of their mainloop) and run in the SM resources
+ *   it leaves free. The call as a whole still completes only after the
+ *   previous kernel, so everything enqueued after it sees the writes of
+ *   both. Without programmatic launch (FP8MP_PDL=0) the flag has no effect.
+ * Other flag bits: FP8MP_ERR_INVALID.
+ */
+int fp8_quantize_ex(const void *x, int32_t x_dtype, int64_t rows, int64_t cols, int32_t fmt,
+                    const float *scale, uint8_t *out, uint8_t *out_t, float *amax, uint32_t flags, void *stream);
+
 /*
  * fp8_quantize_current -- the same cast under just-in-time ("current")
  * scaling ([TE-FP8] "Scaling factor 선택 전략", the just-in-time strategy:

@@ -215,3 +215,10 @@ def test_dbias_workspace_size_and_noalloc_limit(lib):
         rc = lib.fp8_quantize_dbias_noalloc(P, 1, rows, cols, 1, P, P, None, None, P, 0, None)
         assert rc == fp8mp.ERR_INVALID, (rows, cols)
         assert "scratch" in fp8mp.last_error()
+
+
+def test_quantize_ex_rejects_unknown_flags(lib):
+    P = 4096  # fake aligned address, never dereferenced: validation fails first
+    assert lib.fp8_quantize_ex(P, 1, 16, 16, 0, P, P, None, None, 2, None) == fp8mp.ERR_INVALID
+    assert "flags" in fp8mp.last_error()
+    assert lib.fp8_quantize_ex(P, 1, 16, 16, 0, P, P, None, None, 1 << 31, None) == fp8mp.ERR_INVALID
