@@ -10,24 +10,30 @@ through the library's entry points on one CUDA stream:
   fp8_quantize_ex(dY -> dY8, amax,               E5M2, row-major only; dY is an
                   FP8MP_OVERLAP_PREVIOUS)        input of the step, so its cast runs
                                                  beside the forward GEMM
-  fp8_linear_bwd_rowmajor(dY8, W8, X8            dgrad and wgrad GEMMs in one
-                          -> dX bf16, dW bf16)   launch, no transposed copies;
-                                                 the wgrad epilogue flags an
-                                                 Inf/NaN in the stored dW
-  delayed_scaling_update(x, w, y, dy metas)      L = 1024, most_recent
-  mp_master_step(dW -> master, momentum, W8)     SGD-momentum, loss scale 2^16,
-                                                 skip decided by that flag;
-                                                 re-casts W8 under the updated
-                                                 weight scale for the next step
+  delayed_scaling_update_ex(x, w, y, dy metas    L = 1024, most_recent; keeps the
+                            -> prev scale_inv)   scale_inv factors the casts used
+  fp8_linear_bwd_rowmajor(dY8, X8 -> dW bf16)    wgrad, from the row-major copies
+                                                 (no transposed ones); its epilogue
+                                                 flags an Inf/NaN in the stored dW
+  fp8_linear_bwd_rowmajor(dY8, W8 -> dX bf16)    dgrad
+  mp_master_step_prescanned_ex(dW -> master,     SGD-momentum, loss scale 2^16,
+      momentum, next W8; FP8MP_OVERLAP_PREVIOUS) skip decided by that flag;
+                                                 re-casts the weight under the
+                                                 updated scale into the other of
+                                                 two W8 buffers while dgrad still
+                                                 reads this step's
 The weight's first E4M3 copy is cast once before the first step; from then
 on each step's master step writes the next step's W8 (and records the amax
 of the new master weights for the next scale update), so the weight is cast
-once per optimizer step, inside the fused update pass.
+once per optimizer step, inside the fused update pass. The results are
+bitwise those of the serial order (one-launch backward, then the update,
+then the master step in place), which --no-overlap times.
 The metric counts the FLOPs the FP8 tensor cores perform, 3 * 2 * M * N * K,
 per step time. Multi-GPU runs are independent replicas (weak scaling).
 
-The timed steps replay a CUDA graph of those library calls (captured after the
-eager warm-up), as a training loop that captures its step would; --eager
+The timed steps replay CUDA graphs of those library calls (captured after the
+eager warm-up; one per W8 buffer, replayed in turn), as a training loop that
+captures its step would; --eager
 launches every call from Python instead. The step time comes from K steps
 with nothing between the step's kernels; the GEMM launch durations of the
 roofline come from K more steps with timing events around the GEMM launches
@@ -283,16 +289,29 @@ def max_over_ranks(value: float, world: int) -> float:
 
 
 class LinearStep:
-    """Device state and the step of the proj linear, through the library."""
+    """Device state and the step of the proj linear, through the library.
 
-    def __init__(self, m=M_TOK, k=K_IN, n=N_OUT, seed=3, prescanned=True, overlap_dy_cast=True):
+    With `overlap` (the default) two kernels run beside a GEMM instead of
+    after it: the dY cast beside the forward GEMM (dY is an input of the
+    step, not that GEMM's result), and the master step beside the dgrad GEMM.
+    For the latter the backward runs as two launches, wgrad first (dW and its
+    overflow flag are all the master step needs), the delayed-scaling update
+    moves before them (keeping the scale_inv factors this step's casts used,
+    which the backward GEMMs take), and the weight's E4M3 copy is double
+    buffered: dgrad reads the current copy while the master step writes the
+    next one. Every result is bitwise that of the serial order. Without it:
+    the one-launch backward, the update, the master step in place."""
+
+    def __init__(self, m=M_TOK, k=K_IN, n=N_OUT, seed=3, prescanned=True, overlap=True):
         import torch
 
         import fp8_mixed_precision_reduce_gb300 as fp8mp
         import workloads
 
         self.fp8mp = fp8mp
-        self.overlap_dy_cast = overlap_dy_cast
+        self.overlap = overlap
+        # the master step beside dgrad needs the epilogue's overflow flag
+        self.split_bwd = overlap and prescanned
         self.m, self.k, self.n = m, k, n
         dev = "cuda"
         tb = workloads.transformer_block(seed=seed, m=m, d=k, device=dev)
@@ -302,7 +321,8 @@ class LinearStep:
         del tb
         u8 = torch.uint8
         self.X8 = torch.empty((m, k), dtype=u8, device=dev)
-        self.W8 = torch.empty((n, k), dtype=u8, device=dev)
+        self.W8s = [torch.empty((n, k), dtype=u8, device=dev) for _ in range(2 if self.split_bwd else 1)]
+        self.cur = 0  # index of the copy the next step reads
         self.D8 = torch.empty((m, n), dtype=u8, device=dev)
         self.y = torch.empty((m, n), dtype=torch.bfloat16, device=dev)
         self.dx = torch.empty((m, k), dtype=torch.bfloat16, device=dev)
@@ -311,6 +331,8 @@ class LinearStep:
         self.S = torch.tensor([S0], dtype=torch.float32, device=dev)
         self.growth = torch.zeros(1, dtype=torch.int32, device=dev)
         self.found = torch.zeros(1, dtype=torch.int32, device=dev)
+        # scale_inv of x, w, y, dY as this step's casts used them (kept by the update)
+        self.snap = torch.zeros(4, dtype=torch.float32, device=dev)
         # dW's overflow flag: set by the wgrad epilogue, read and reset by the
         # master step (with prescanned=False the master step scans dW itself)
         self.prescanned = prescanned
@@ -320,71 +342,126 @@ class LinearStep:
         self.md = fp8mp.Meta(HIST_LEN, E5)
         # the weight's first E4M3 copy (and its amax for the first update)
         fp8mp.fp8_quantize(self.master, E4, self.mw.scale, self.W8, None, self.mw.cur_amax)
-        # 2 casts, the fwd GEMM, the fused dgrad + wgrad GEMM, 1 scale update, and the master step: one
-        # kernel on the epilogue's flag (scanning dW itself: a 4-byte memset and one kernel, or three
-        # kernels with FP8MP_FUSED_MASTER=0)
-        self.launches_per_step = 6 if prescanned or os.environ.get("FP8MP_FUSED_MASTER", "1") != "0" else 8
+        # split: 2 casts, the fwd GEMM, the update, wgrad, dgrad, the master step. Serial: 2 casts, the fwd
+        # GEMM, the fused dgrad + wgrad GEMM, the update, and the master step: one kernel on the epilogue's
+        # flag (scanning dW itself: a 4-byte memset and one kernel, or three kernels with FP8MP_FUSED_MASTER=0)
+        if self.split_bwd:
+            self.launches_per_step = 7
+        else:
+            self.launches_per_step = 6 if prescanned or os.environ.get("FP8MP_FUSED_MASTER", "1") != "0" else 8
+
+    @property
+    def W8(self):
+        """The weight's E4M3 copy the next step reads."""
+        return self.W8s[self.cur]
 
     def step(self, gemm_events=None, io=None):
         """One training step. `io` = (x, dy, y, dx) device buffers to use
-        instead of the step's own (the end-to-end leg double-buffers them)."""
+        instead of the step's own (the end-to-end leg double-buffers them).
+        `gemm_events`: four events recorded before and after the forward
+        GEMM and before and after the backward GEMM launches."""
         f = self.fp8mp
         x, dy, y, dx = io if io is not None else (self.x, self.dy, self.y, self.dx)
+        metas = [self.mx, self.mw, self.my, self.md]
+        W8 = self.W8
         f.fp8_quantize(x, f.E4M3, self.mx.scale, self.X8, None, self.mx.cur_amax)
         ev = gemm_events
         if ev is not None:
             ev[0].record()
-        f.fp8_linear_fwd(self.X8, self.W8, self.mx.scale_inv, self.mw.scale_inv, y, y_amax=self.my.cur_amax)
+        f.fp8_linear_fwd(self.X8, W8, self.mx.scale_inv, self.mw.scale_inv, y, y_amax=self.my.cur_amax)
         if ev is not None:
             ev[1].record()
-        if self.overlap_dy_cast:
+        if self.overlap:
             # dY is an input of the step, not the forward GEMM's result: its
             # cast may run beside the GEMM (it still completes after it)
             f.fp8_quantize_ex(dy, f.E5M2, self.md.scale, self.D8, None, self.md.cur_amax, flags=f.OVERLAP_PREVIOUS)
         else:
             f.fp8_quantize(dy, f.E5M2, self.md.scale, self.D8, None, self.md.cur_amax)
+        if not self.split_bwd:
+            if ev is not None:
+                ev[2].record()
+            f.fp8_linear_bwd_rowmajor(self.D8, W8, self.X8, self.md.scale_inv, self.mw.scale_inv,
+                                      self.mx.scale_inv, dx, self.dw,
+                                      dw_nonfinite=self.gnf if self.prescanned else None)
+            if ev is not None:
+                ev[3].record()
+            f.delayed_scaling_update(metas, f.AMAX_MOST_RECENT, 0)
+            f.mp_master_step(self.dw, self.master, self.mom, W8, self.mw.scale, self.mw.cur_amax, self.S,
+                             self.growth, self.found, LR, MU, grad_nonfinite=self.gnf if self.prescanned else None)
+            return
+        f.delayed_scaling_update(metas, f.AMAX_MOST_RECENT, 0, prev_scale_inv=self.snap)
+        sx, sw, sd = self.snap[0:1], self.snap[1:2], self.snap[3:4]
         if ev is not None:
             ev[2].record()
-        f.fp8_linear_bwd_rowmajor(self.D8, self.W8, self.X8, self.md.scale_inv, self.mw.scale_inv,
-                                  self.mx.scale_inv, dx, self.dw,
-                                  dw_nonfinite=self.gnf if self.prescanned else None)
+        f.fp8_linear_bwd_rowmajor(self.D8, None, self.X8, sd, None, sx, None, self.dw, dw_nonfinite=self.gnf)
+        f.fp8_linear_bwd_rowmajor(self.D8, W8, None, sd, sw, None, dx, None)
         if ev is not None:
             ev[3].record()
-        f.delayed_scaling_update([self.mx, self.mw, self.my, self.md], f.AMAX_MOST_RECENT, 0)
-        f.mp_master_step(self.dw, self.master, self.mom, self.W8, self.mw.scale, self.mw.cur_amax, self.S,
-                         self.growth, self.found, LR, MU, grad_nonfinite=self.gnf if self.prescanned else None)
+        nxt = self.cur ^ 1
+        # the next copy, written while dgrad still reads this one
+        f.mp_master_step(self.dw, self.master, self.mom, self.W8s[nxt], self.mw.scale, self.mw.cur_amax, self.S,
+                         self.growth, self.found, LR, MU, grad_nonfinite=self.gnf, w8_in=W8,
+                         flags=f.OVERLAP_PREVIOUS)
+        self.cur = nxt
 
 
-def capture_step_graphs(st, count):
-    """(replay of a plain graph of one step, ([count graphs of one step each
-    with four event-record nodes around the GEMM launches], [their events])).
-    The timed graphs need one graph per step because an event node records
-    into the same event at every replay. Capture runs on a side stream after
-    the eager warm-up (which made the library's one-time attribute and
-    occupancy queries); every graph is replayed once here, untimed (its
-    upload)."""
-    import torch
+class StepGraphs:
+    """The step as CUDA graphs: one per copy of the weight the step reads
+    (the step alternates between them), replayed in turn by `replay()`, and
+    `count` graphs of one step each with four event-record nodes around the
+    GEMM launches (an event node records into the same event at every
+    replay, so the timed pass needs one graph per step), replayed in order
+    by `replay_timed(i)`. Capture runs on a side stream after the eager
+    warm-up (which made the library's one-time attribute and occupancy
+    queries); every graph is replayed once here, untimed (its upload),
+    unless `upload` is False."""
 
-    side = torch.cuda.Stream()
-    side.wait_stream(torch.cuda.current_stream())
-    plain = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(plain, stream=side):
-        st.step()
-    graphs, events = [], []
-    for _ in range(count):
-        ev = [torch.cuda.Event(enable_timing=True, external=True) for _ in range(4)]
-        g = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(g, stream=side):
-            st.step(ev)
-        graphs.append(g)
-        events.append(ev)
-    torch.cuda.current_stream().wait_stream(side)
-    torch.cuda.synchronize()
-    plain.replay()
-    for g in graphs:
+    def __init__(self, st, count, upload=True):
+        import torch
+
+        self.st = st
+        c = st.cur
+        side = torch.cuda.Stream()
+        side.wait_stream(torch.cuda.current_stream())
+        self.by_copy = {}
+        for p in range(len(st.W8s)):
+            st.cur = (c + p) % len(st.W8s)
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=side):
+                st.step()
+            self.by_copy[(c + p) % len(st.W8s)] = g
+        self.timed, self.events, self.timed_copy = [], [], []
+        for i in range(count):
+            st.cur = (c + i) % len(st.W8s)
+            self.timed_copy.append(st.cur)
+            ev = [torch.cuda.Event(enable_timing=True, external=True) for _ in range(4)]
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=side):
+                st.step(ev)
+            self.timed.append(g)
+            self.events.append(ev)
+        st.cur = c  # capture ran nothing
+        torch.cuda.current_stream().wait_stream(side)
+        torch.cuda.synchronize()
+        if upload:
+            for _ in self.by_copy:
+                self.replay()
+            for i in range(count):
+                self.replay_timed(i)
+            torch.cuda.synchronize()
+
+    def replay(self):
+        st = self.st
+        g = self.by_copy[st.cur]
+        st.cur = (st.cur + 1) % len(st.W8s)
         g.replay()
-    torch.cuda.synchronize()
-    return plain.replay, (graphs, events)
+
+    def replay_timed(self, i):
+        st = self.st
+        while st.cur != self.timed_copy[i]:  # untimed: bring the weight copy in line
+            self.replay()
+        st.cur = (st.cur + 1) % len(st.W8s)
+        self.timed[i].replay()
 
 
 def run_e2e(st, steps, world, with_outputs=False):
@@ -485,7 +562,7 @@ def run_ours(args, world, rank, local):
 
     peaks, peak_kind = load_peaks()
     lib_fp8 = library_fp8_gemm_tflops()
-    st = LinearStep(prescanned=not args.master_scans_dw, overlap_dy_cast=not args.no_overlap)
+    st = LinearStep(prescanned=not args.master_scans_dw, overlap=not args.no_overlap)
     torch.cuda.synchronize()
     flush = torch.empty(int(2 * 129e6 // 4) + 1, dtype=torch.float32, device="cuda")  # > 2x L2
 
@@ -507,7 +584,8 @@ def run_ours(args, world, rank, local):
         plain, timed = st.step, None
         launch = "eager (one host launch per library call, programmatic dependent launch)"
     else:
-        plain, timed = capture_step_graphs(st, args.steps)
+        graphs = StepGraphs(st, args.steps)
+        plain, timed = graphs.replay, graphs
         launch = "CUDA graph of the step's library calls, captured once and replayed"
     starts = [E(enable_timing=True) for _ in range(args.steps)]
     ends = [E(enable_timing=True) for _ in range(args.steps)]
@@ -536,16 +614,19 @@ def run_ours(args, world, rank, local):
             torch.cuda.synchronize()
             repeat_means.append(statistics.mean(s.elapsed_time(e) for s, e in zip(rs, re_)))
         # pass 2
-        gev = [[E(enable_timing=True) for _ in range(4)] for _ in range(args.steps)] if timed is None else timed[1]
+        gev = [[E(enable_timing=True) for _ in range(4)] for _ in range(args.steps)] if timed is None else timed.events
         starts2 = [E(enable_timing=True) for _ in range(args.steps)]
         ends2 = [E(enable_timing=True) for _ in range(args.steps)]
+        if timed is not None:
+            while st.cur != timed.timed_copy[0]:  # the copy the first timed graph reads (untimed step)
+                plain()
         for i in range(args.steps):
             flush.fill_(float(i))
             starts2[i].record()
             if timed is None:
                 st.step(gev[i])
             else:
-                timed[0][i].replay()
+                timed.replay_timed(i)
             ends2[i].record()
         torch.cuda.synchronize()
     barrier(world)
@@ -554,7 +635,7 @@ def run_ours(args, world, rank, local):
         raise RuntimeError(f"timed steps failed: {st.fp8mp.last_error()}")
     step_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
     step2_ms = [s.elapsed_time(e) for s, e in zip(starts2, ends2)]
-    gemm_ms = [[g[0].elapsed_time(g[1]), g[2].elapsed_time(g[3])] for g in gev]  # fwd, fused bwd
+    gemm_ms = [[g[0].elapsed_time(g[1]), g[2].elapsed_time(g[3])] for g in gev]  # fwd, bwd (wgrad + dgrad)
     ms_per_step = max_over_ranks(statistics.mean(step_ms), world)
     ms_instrumented = max_over_ranks(statistics.mean(step2_ms), world)
     gemm_step_ms = max_over_ranks(statistics.mean(sum(g) for g in gemm_ms), world)
@@ -569,8 +650,9 @@ def run_ours(args, world, rank, local):
     fl = flops_per_step()
     value = world * fl / (ms_per_step * 1e-3) / 1e12
     fp8_nominal = float(peaks["bf16_tflops"]) * FP8_OVER_BF16
-    # the GEMM kernel's two launches per step do 2MNK (fwd) and 4MNK (dgrad +
-    # wgrad) FLOPs: achieved = their FLOPs / their summed device time
+    # the GEMM kernel's launches per step do 2MNK (fwd) and 4MNK (dgrad +
+    # wgrad: one launch, or two back to back) FLOPs: achieved = their FLOPs /
+    # their summed device time
     achieved = fl / ((fwd_ms + bwd_ms) * 1e-3) / 1e12
     # the FP8 peak actually reached on this GPU in this run: the best of
     # cuBLASLt's FP8 GEMM at 8192^3 and this library's fastest GEMM launch;
@@ -600,7 +682,10 @@ def run_ours(args, world, rank, local):
                    "overflow_check": "master step scans dW" if args.master_scans_dw
                    else "wgrad epilogue flags Inf/NaN in the stored dW; the master step reads the flag",
                    "dy_cast": "plain, after the forward GEMM" if args.no_overlap
-                   else "enqueued after the forward GEMM with FP8MP_OVERLAP_PREVIOUS: runs beside it"},
+                   else "enqueued after the forward GEMM with FP8MP_OVERLAP_PREVIOUS: runs beside it",
+                   "backward": ("wgrad launch, dgrad launch, then the master step with FP8MP_OVERLAP_PREVIOUS "
+                                "beside dgrad (scale update before them, weight copy double-buffered)")
+                   if st.split_bwd else "dgrad + wgrad in one launch, the scale update, the master step"},
         "gemm_only": {"tflops": round(world * fl / (gemm_step_ms * 1e-3) / 1e12, 2), "ms_per_step": round(gemm_step_ms, 5),
                       "fwd_ms": round(fwd_ms, 5), "bwd_ms": round(bwd_ms, 5),
                       "from": "a second pass of K steps with timing events around the GEMM launches",
@@ -970,7 +1055,8 @@ def main(argv=None):
     ap.add_argument("--master-scans-dw", action="store_true",
                     help="the master step scans dW for Inf/NaN itself instead of reading the wgrad epilogue's flag")
     ap.add_argument("--no-overlap", action="store_true",
-                    help="cast dY with a plain fp8_quantize instead of letting it run beside the forward GEMM")
+                    help="the serial step: cast dY after the forward GEMM, one-launch backward, then the update "
+                         "and the master step (no kernel runs beside a GEMM)")
     ap.add_argument("--eager", action="store_true",
                     help="launch every library call from Python in the timed steps instead of replaying graphs")
     ap.add_argument("--kernels", action="store_true",

@@ -26,8 +26,9 @@ _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "libfp8mp.so")
 EXPORTS = ("fp8_quantize", "fp8_quantize_ex", "fp8_quantize_current", "fp8_quantize_dbias",
            "fp8_quantize_dbias_workspace_bytes", "fp8_quantize_dbias_noalloc", "fp8_linear_fwd", "fp8_linear_fwd_fp8out", "fp8_linear_dgrad", "fp8_linear_wgrad",
-           "fp8_linear_bwd", "fp8_linear_bwd_rowmajor", "delayed_scaling_update", "mp_master_step", "mp_master_step_adam", "mp_master_step_prescanned",
-           "mp_master_step_adam_prescanned", "fp8mp_check", "fp8mp_last_error",
+           "fp8_linear_bwd", "fp8_linear_bwd_rowmajor", "delayed_scaling_update", "delayed_scaling_update_ex",
+           "mp_master_step", "mp_master_step_adam", "mp_master_step_prescanned", "mp_master_step_adam_prescanned",
+           "mp_master_step_prescanned_ex", "mp_master_step_adam_prescanned_ex", "fp8mp_check", "fp8mp_last_error",
            "fp8mp_version", "fp8mp_selftest_timeout", "fp8mp_selftest_barrier_timeout")
 
 _lib = None
@@ -78,10 +79,15 @@ def load(path: str | None = None):
     L.fp8_linear_bwd.argtypes = [P, P, P, P, I64, I64, I64, I32, P, P, P, P, I32, P, I32, P]
     L.fp8_linear_bwd_rowmajor.argtypes = [P, P, P, I64, I64, I64, I32, P, P, P, P, I32, P, I32, P, P]
     L.delayed_scaling_update.argtypes = [ctypes.POINTER(fp8mp_meta), I32, I32, I32, P]
+    L.delayed_scaling_update_ex.argtypes = [ctypes.POINTER(fp8mp_meta), I32, I32, I32, P, P]
     L.mp_master_step.argtypes = [P, I64, P, P, P, P, P, P, P, P, F, F, F, F, I32, P]
     L.mp_master_step_adam.argtypes = [P, I64, P, P, P, P, P, P, P, P, P, P, F, F, F, F, F, F, I32, P]
     L.mp_master_step_prescanned.argtypes = [P, I64, P, P, P, P, P, P, P, P, P, F, F, F, F, I32, P]
     L.mp_master_step_adam_prescanned.argtypes = [P, I64, P, P, P, P, P, P, P, P, P, P, P, F, F, F, F, F, F, I32, P]
+    U32 = ctypes.c_uint32
+    L.mp_master_step_prescanned_ex.argtypes = [P, I64, P, P, P, P, P, P, P, P, P, P, F, F, F, F, I32, U32, P]
+    L.mp_master_step_adam_prescanned_ex.argtypes = [P, I64, P, P, P, P, P, P, P, P, P, P, P, P, F, F, F, F, F, F,
+                                                    I32, U32, P]
     L.fp8mp_check.argtypes = [P]
     L.fp8mp_selftest_timeout.argtypes = [P]
     L.fp8mp_selftest_barrier_timeout.argtypes = [P]
@@ -89,8 +95,9 @@ def load(path: str | None = None):
     L.fp8mp_version.restype = I32
     for name in ("fp8_quantize", "fp8_quantize_ex", "fp8_quantize_current", "fp8_quantize_dbias", "fp8_quantize_dbias_noalloc",
                  "fp8_linear_fwd", "fp8_linear_fwd_fp8out", "fp8_linear_dgrad", "fp8_linear_wgrad",
-                 "fp8_linear_bwd", "fp8_linear_bwd_rowmajor", "delayed_scaling_update", "mp_master_step", "mp_master_step_adam",
-                 "mp_master_step_prescanned", "mp_master_step_adam_prescanned", "fp8mp_check",
+                 "fp8_linear_bwd", "fp8_linear_bwd_rowmajor", "delayed_scaling_update", "delayed_scaling_update_ex",
+                 "mp_master_step", "mp_master_step_adam", "mp_master_step_prescanned", "mp_master_step_adam_prescanned",
+                 "mp_master_step_prescanned_ex", "mp_master_step_adam_prescanned_ex", "fp8mp_check",
                  "fp8mp_selftest_timeout", "fp8mp_selftest_barrier_timeout"):
         getattr(L, name).restype = ctypes.c_int
     _lib = L
@@ -297,10 +304,19 @@ class Meta:
                           self.history_len, self.fmt)
 
 
-def delayed_scaling_update(metas, algo: int, margin: int = 0, stream=None) -> None:
-    """Rolls each meta's history, picks the amax and refreshes scale/scale_inv."""
+def delayed_scaling_update(metas, algo: int, margin: int = 0, stream=None,
+                           prev_scale_inv: torch.Tensor | None = None) -> None:
+    """Rolls each meta's history, picks the amax and refreshes scale/scale_inv.
+    With prev_scale_inv (fp32[len(metas)] on the device) each meta's
+    scale_inv from before the update is kept there (delayed_scaling_update_ex)."""
     metas = list(metas)
     arr = (fp8mp_meta * max(1, len(metas)))(*[m.c_struct() for m in metas])
+    if prev_scale_inv is not None:
+        if prev_scale_inv.numel() < len(metas) or prev_scale_inv.dtype != torch.float32:
+            raise Fp8mpError(ERR_INVALID, "prev_scale_inv must be float32 with one entry per meta")
+        _check(load().delayed_scaling_update_ex(arr, len(metas), algo, margin, _ptr(prev_scale_inv),
+                                                _stream(stream)))
+        return
     _check(load().delayed_scaling_update(arr, len(metas), algo, margin, _stream(stream)))
 
 
@@ -308,13 +324,25 @@ def mp_master_step(grad_bf16: torch.Tensor, master: torch.Tensor, momentum: torc
                    w8: torch.Tensor, scale_w: torch.Tensor, amax_w: torch.Tensor,
                    loss_scale: torch.Tensor, growth_tracker: torch.Tensor, found_inf: torch.Tensor,
                    lr: float, momentum_coef: float, backoff: float = 0.5, growth_factor: float = 2.0,
-                   growth_interval: int = 2000, stream=None, grad_nonfinite: torch.Tensor | None = None) -> None:
+                   growth_interval: int = 2000, stream=None, grad_nonfinite: torch.Tensor | None = None,
+                   w8_in: torch.Tensor | None = None, flags: int = 0) -> None:
     """Unscale, overflow skip, FP32 SGD-momentum update and E4M3 re-cast, in place.
     With grad_nonfinite (int32[1] on the device holding 0 or 1, set by the
     gradients' producer, e.g. fp8_linear_bwd_rowmajor's dw_nonfinite) the step
     reads that flag instead of scanning the gradients, writes it to found_inf
-    and resets it to 0."""
+    and resets it to 0. With it, w8_in (the current E4M3 copy; the new one goes
+    to w8, which a skipped step fills with w8_in) and flags
+    (OVERLAP_PREVIOUS) select mp_master_step_prescanned_ex."""
     n = grad_bf16.numel()
+    if w8_in is not None or flags:
+        if grad_nonfinite is None:
+            raise Fp8mpError(ERR_INVALID, "w8_in and flags need grad_nonfinite (the prescanned step)")
+        _check(load().mp_master_step_prescanned_ex(
+            _ptr(grad_bf16), n, _ptr(master), _ptr(momentum), _ptr(w8_in), _ptr(w8), _ptr(scale_w), _ptr(amax_w),
+            _ptr(loss_scale), _ptr(growth_tracker), _ptr(found_inf), _ptr(grad_nonfinite), float(lr),
+            float(momentum_coef), float(backoff), float(growth_factor), int(growth_interval), int(flags),
+            _stream(stream)))
+        return
     if grad_nonfinite is not None:
         _check(load().mp_master_step_prescanned(_ptr(grad_bf16), n, _ptr(master), _ptr(momentum), _ptr(w8),
                                                 _ptr(scale_w), _ptr(amax_w), _ptr(loss_scale), _ptr(growth_tracker),
@@ -333,10 +361,20 @@ def mp_master_step_adam(grad_bf16: torch.Tensor, master: torch.Tensor, exp_avg: 
                         loss_scale: torch.Tensor, growth_tracker: torch.Tensor, found_inf: torch.Tensor,
                         beta_pows: torch.Tensor, lr: float, beta1: float = 0.9, beta2: float = 0.999,
                         eps: float = 1e-8, backoff: float = 0.5, growth_factor: float = 2.0,
-                        growth_interval: int = 2000, stream=None, grad_nonfinite: torch.Tensor | None = None) -> None:
+                        growth_interval: int = 2000, stream=None, grad_nonfinite: torch.Tensor | None = None,
+                        w8_in: torch.Tensor | None = None, flags: int = 0) -> None:
     """Unscale, overflow skip, FP32 Adam update and E4M3 re-cast, in place
-    (grad_nonfinite: as mp_master_step)."""
+    (grad_nonfinite, w8_in, flags: as mp_master_step)."""
     n = grad_bf16.numel()
+    if w8_in is not None or flags:
+        if grad_nonfinite is None:
+            raise Fp8mpError(ERR_INVALID, "w8_in and flags need grad_nonfinite (the prescanned step)")
+        _check(load().mp_master_step_adam_prescanned_ex(
+            _ptr(grad_bf16), n, _ptr(master), _ptr(exp_avg), _ptr(exp_avg_sq), _ptr(w8_in), _ptr(w8),
+            _ptr(scale_w), _ptr(amax_w), _ptr(loss_scale), _ptr(growth_tracker), _ptr(found_inf),
+            _ptr(grad_nonfinite), _ptr(beta_pows), float(lr), float(beta1), float(beta2), float(eps),
+            float(backoff), float(growth_factor), int(growth_interval), int(flags), _stream(stream)))
+        return
     if grad_nonfinite is not None:
         _check(load().mp_master_step_adam_prescanned(
             _ptr(grad_bf16), n, _ptr(master), _ptr(exp_avg), _ptr(exp_avg_sq), _ptr(w8), _ptr(scale_w),

@@ -447,14 +447,15 @@ int fp8_linear_bwd_rowmajor(const uint8_t *dy8, const uint8_t *w8, const uint8_t
     return launch_gemms(d, n, static_cast<cudaStream_t>(stream), dev);
 }
 
-int delayed_scaling_update(const fp8mp_meta *metas, int32_t n, int32_t algo, int32_t margin, void *stream) {
-    const char *fn = "delayed_scaling_update";
+static int scale_update_entry(const char *fn, const fp8mp_meta *metas, int32_t n, int32_t algo, int32_t margin,
+                              float *prev_scale_inv, void *stream) {
     clear_error();
     REQUIRE(n >= 0, "%s: negative count", fn);
     if (n == 0) return FP8MP_OK;
     REQUIRE(metas != nullptr, "%s: metas is NULL", fn);
     REQUIRE(algo == FP8MP_AMAX_MAX || algo == FP8MP_AMAX_MOST_RECENT, "%s: algo %d invalid", fn, algo);
     REQUIRE(margin >= 0 && margin <= 126, "%s: margin %d outside 0..126", fn, margin);
+    CHECK_SCALAR(prev_scale_inv, false);
     for (int32_t i = 0; i < n; ++i) {
         const fp8mp_meta &m = metas[i];
         REQUIRE(m.history_len >= 1 && m.history_len <= FP8MP_MAX_HISTORY, "%s: meta %d history_len %d outside 1..%d",
@@ -465,14 +466,34 @@ int delayed_scaling_update(const fp8mp_meta *metas, int32_t n, int32_t algo, int
     DeviceInfo dev;
     const int rc = current_device(&dev);
     if (rc) return rc;
-    return launch_scale_update(metas, n, algo, margin, static_cast<cudaStream_t>(stream));
+    return launch_scale_update(metas, n, algo, margin, static_cast<cudaStream_t>(stream), prev_scale_inv);
+}
+
+int delayed_scaling_update(const fp8mp_meta *metas, int32_t n, int32_t algo, int32_t margin, void *stream) {
+    return scale_update_entry("delayed_scaling_update", metas, n, algo, margin, nullptr, stream);
+}
+
+int delayed_scaling_update_ex(const fp8mp_meta *metas, int32_t n, int32_t algo, int32_t margin,
+                              float *prev_scale_inv, void *stream) {
+    return scale_update_entry("delayed_scaling_update_ex", metas, n, algo, margin, prev_scale_inv, stream);
+}
+
+// w8_in and the flags of the _ex forms: the current E4M3 copy (NULL or w8
+// itself: in place) and FP8MP_OVERLAP_PREVIOUS.
+static int check_w8_pair(const char *fn, const uint8_t *w8_in, const uint8_t *w8, int64_t n, uint32_t flags) {
+    REQUIRE((flags & ~static_cast<uint32_t>(FP8MP_OVERLAP_PREVIOUS)) == 0u, "%s: unknown flags 0x%x", fn, flags);
+    CHECK_PTR(w8_in, false);
+    if (w8_in != nullptr && w8_in != w8 && n > 0)
+        REQUIRE(w8_in + n <= w8 || w8 + n <= w8_in, "%s: w8_in and w8_out overlap without being equal", fn);
+    return FP8MP_OK;
 }
 
 static int master_step_entry(const char *fn, const uint16_t *grad_bf16, int64_t n, float *master,
                              float *momentum, uint8_t *w8, const float *scale_w, float *amax_w, float *loss_scale,
                              int32_t *growth_tracker, int32_t *found_inf, int32_t *grad_nonfinite, bool prescanned,
                              float lr, float momentum_coef, float backoff, float growth_factor,
-                             int32_t growth_interval, void *stream) {
+                             int32_t growth_interval, void *stream, const uint8_t *w8_in = nullptr,
+                             uint32_t flags = 0u) {
     clear_error();
     REQUIRE(n >= 0 && n <= (1ll << 40), "%s: n = %lld out of range", fn, (long long)n);
     REQUIRE(growth_interval >= 1, "%s: growth_interval must be >= 1", fn);
@@ -480,6 +501,10 @@ static int master_step_entry(const char *fn, const uint16_t *grad_bf16, int64_t 
     CHECK_PTR(master, n > 0);
     CHECK_PTR(momentum, n > 0);
     CHECK_PTR(w8, n > 0);
+    {
+        const int rc_ = check_w8_pair(fn, w8_in, w8, n, flags);
+        if (rc_) return rc_;
+    }
     CHECK_SCALAR(scale_w, true);
     CHECK_SCALAR(amax_w, true);
     CHECK_SCALAR(loss_scale, true);
@@ -492,7 +517,8 @@ static int master_step_entry(const char *fn, const uint16_t *grad_bf16, int64_t 
     if (rc) return rc;
     return launch_master_step(grad_bf16, n, master, momentum, w8, scale_w, amax_w, loss_scale, growth_tracker,
                               found_inf, lr, momentum_coef, backoff, growth_factor, growth_interval,
-                              static_cast<cudaStream_t>(stream), dev, grad_nonfinite);
+                              static_cast<cudaStream_t>(stream), dev, grad_nonfinite, w8_in,
+                              (flags & FP8MP_OVERLAP_PREVIOUS) != 0u);
 }
 
 int mp_master_step(const uint16_t *grad_bf16, int64_t n, float *master, float *momentum, uint8_t *w8,
@@ -517,7 +543,8 @@ static int adam_step_entry(const char *fn, const uint16_t *grad_bf16, int64_t n,
                            float *exp_avg_sq, uint8_t *w8, const float *scale_w, float *amax_w, float *loss_scale,
                            int32_t *growth_tracker, int32_t *found_inf, int32_t *grad_nonfinite, bool prescanned,
                            float *beta_pows, float lr, float beta1, float beta2, float eps, float backoff,
-                           float growth_factor, int32_t growth_interval, void *stream) {
+                           float growth_factor, int32_t growth_interval, void *stream,
+                           const uint8_t *w8_in = nullptr, uint32_t flags = 0u) {
     clear_error();
     REQUIRE(n >= 0 && n <= (1ll << 40), "%s: n = %lld out of range", fn, (long long)n);
     REQUIRE(growth_interval >= 1, "%s: growth_interval must be >= 1", fn);
@@ -535,12 +562,17 @@ static int adam_step_entry(const char *fn, const uint16_t *grad_bf16, int64_t n,
     CHECK_SCALAR(beta_pows, true);
     CHECK_SCALAR(grad_nonfinite, prescanned);
     REQUIRE(grad_nonfinite != found_inf, "%s: grad_nonfinite and found_inf must be different words", fn);
+    {
+        const int rc_ = check_w8_pair(fn, w8_in, w8, n, flags);
+        if (rc_) return rc_;
+    }
     DeviceInfo dev;
     const int rc = current_device(&dev);
     if (rc) return rc;
     return launch_adam_step(grad_bf16, n, master, exp_avg, exp_avg_sq, w8, scale_w, amax_w, loss_scale,
                             growth_tracker, found_inf, beta_pows, lr, beta1, beta2, eps, backoff, growth_factor,
-                            growth_interval, static_cast<cudaStream_t>(stream), dev, grad_nonfinite);
+                            growth_interval, static_cast<cudaStream_t>(stream), dev, grad_nonfinite, w8_in,
+                            (flags & FP8MP_OVERLAP_PREVIOUS) != 0u);
 }
 
 int mp_master_step_adam(const uint16_t *grad_bf16, int64_t n, float *master, float *exp_avg, float *exp_avg_sq,
@@ -561,6 +593,27 @@ int mp_master_step_adam_prescanned(const uint16_t *grad_bf16, int64_t n, float *
     return adam_step_entry("mp_master_step_adam_prescanned", grad_bf16, n, master, exp_avg, exp_avg_sq, w8, scale_w,
                            amax_w, loss_scale, growth_tracker, found_inf, grad_nonfinite, true, beta_pows, lr, beta1,
                            beta2, eps, backoff, growth_factor, growth_interval, stream);
+}
+
+int mp_master_step_prescanned_ex(const uint16_t *grad_bf16, int64_t n, float *master, float *momentum,
+                                 const uint8_t *w8_in, uint8_t *w8_out, const float *scale_w, float *amax_w,
+                                 float *loss_scale, int32_t *growth_tracker, int32_t *found_inf,
+                                 int32_t *grad_nonfinite, float lr, float momentum_coef, float backoff,
+                                 float growth_factor, int32_t growth_interval, uint32_t flags, void *stream) {
+    return master_step_entry("mp_master_step_prescanned_ex", grad_bf16, n, master, momentum, w8_out, scale_w, amax_w,
+                             loss_scale, growth_tracker, found_inf, grad_nonfinite, true, lr, momentum_coef, backoff,
+                             growth_factor, growth_interval, stream, w8_in, flags);
+}
+
+int mp_master_step_adam_prescanned_ex(const uint16_t *grad_bf16, int64_t n, float *master, float *exp_avg,
+                                      float *exp_avg_sq, const uint8_t *w8_in, uint8_t *w8_out,
+                                      const float *scale_w, float *amax_w, float *loss_scale,
+                                      int32_t *growth_tracker, int32_t *found_inf, int32_t *grad_nonfinite,
+                                      float *beta_pows, float lr, float beta1, float beta2, float eps, float backoff,
+                                      float growth_factor, int32_t growth_interval, uint32_t flags, void *stream) {
+    return adam_step_entry("mp_master_step_adam_prescanned_ex", grad_bf16, n, master, exp_avg, exp_avg_sq, w8_out,
+                           scale_w, amax_w, loss_scale, growth_tracker, found_inf, grad_nonfinite, true, beta_pows,
+                           lr, beta1, beta2, eps, backoff, growth_factor, growth_interval, stream, w8_in, flags);
 }
 
 int fp8mp_selftest_timeout(void *stream) {

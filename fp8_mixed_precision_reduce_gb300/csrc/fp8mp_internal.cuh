@@ -100,18 +100,28 @@ int launch_gemm(const uint8_t *a, int fmt_a, const uint8_t *b, int fmt_b, int64_
                 const void *bias, int bias_dtype, void *out, int out_dtype, float *out_amax,
                 cudaStream_t s, const DeviceInfo &dev, const float *out_scale = nullptr,
                 int out_fmt = FP8MP_E4M3);
+// Registers one warp of the persistent (pair) GEMM holds, as allocated (8
+// per thread at a time), and in *warps its warps per CTA; 0 if the attribute
+// query fails.
+int gemm_warp_registers(int *warps);
+// prev_scale_inv (n floats or NULL) receives each meta's scale_inv as it
+// was before the update.
 int launch_scale_update(const fp8mp_meta *metas, int32_t n, int32_t algo, int32_t margin,
-                        cudaStream_t s);
+                        cudaStream_t s, float *prev_scale_inv = nullptr);
+// w8_in: the current E4M3 copy when the new one goes to a different buffer
+// w8 (copied there on a skipped step), NULL for in place. early (prescanned
+// steps only): start without waiting for the previous kernel on the stream
+// (FP8MP_OVERLAP_PREVIOUS), complete after it.
 int launch_master_step(const uint16_t *g, int64_t n, float *w, float *v, uint8_t *w8,
                        const float *scale_w, float *amax_w, float *loss_scale, int32_t *growth,
                        int32_t *found_inf, float lr, float mu, float backoff, float growth_factor,
                        int32_t growth_interval, cudaStream_t s, const DeviceInfo &dev,
-                       int32_t *grad_nonfinite = nullptr);
+                       int32_t *grad_nonfinite = nullptr, const uint8_t *w8_in = nullptr, bool early = false);
 int launch_adam_step(const uint16_t *g, int64_t n, float *w, float *m, float *v, uint8_t *w8, const float *scale_w,
                      float *amax_w, float *loss_scale, int32_t *growth, int32_t *found_inf, float *beta_pows,
                      float lr, float b1, float b2, float eps, float backoff, float growth_factor,
                      int32_t growth_interval, cudaStream_t s, const DeviceInfo &dev,
-                     int32_t *grad_nonfinite = nullptr);
+                     int32_t *grad_nonfinite = nullptr, const uint8_t *w8_in = nullptr, bool early = false);
 // Enqueues the one-thread kernel whose bounded wait is meant to run out.
 int launch_timeout_selftest(cudaStream_t s);
 // Reads and clears the GEMM wait-timeout flag (after a stream sync).
@@ -131,7 +141,10 @@ const char *last_error_message();
 // the kernel was launched without programmatic serialization.
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 // Lets the next kernel on the stream be scheduled (it still waits in
-// pdl_wait for this grid to complete before touching memory).
+// pdl_wait for this grid to complete before touching memory). Every kernel
+// of the library calls it only after its own pdl_wait has returned, so the
+// next kernel starting means every kernel before this one has completed
+// (which a kernel launched with FP8MP_OVERLAP_PREVIOUS relies on).
 __device__ __forceinline__ void pdl_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 
 // Largest finite value of each format.

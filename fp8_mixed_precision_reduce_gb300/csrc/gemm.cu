@@ -891,6 +891,18 @@ int prepare_engine(const DeviceInfo &dev) {
 
 }  // namespace
 
+int gemm_warp_registers(int *warps) {
+    static std::atomic<int> cached{0};
+    *warps = NUM_THREADS / 32;
+    int r = cached.load(std::memory_order_relaxed);
+    if (r > 0) return r;
+    cudaFuncAttributes fa;
+    if (cudaFuncGetAttributes(&fa, gemm_fp8_kernel<true>) != cudaSuccess) return 0;
+    r = 32 * ((fa.numRegs + 7) & ~7);
+    cached.store(r, std::memory_order_relaxed);
+    return r;
+}
+
 int launch_gemms(const GemmDesc *descs, int n, cudaStream_t s, const DeviceInfo &dev) {
     if (n < 1 || n > MAX_PROBLEMS) return fail(FP8MP_ERR_INVALID, "a GEMM launch takes 1 or 2 problems");
     const GemmDesc *work[MAX_PROBLEMS];

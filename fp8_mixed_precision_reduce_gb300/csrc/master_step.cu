@@ -38,6 +38,9 @@ __device__ unsigned int g_master_timeout_flag = 0;
 namespace {
 
 constexpr int kThreads = 256;
+// Early (FP8MP_OVERLAP_PREVIOUS) grid: one block per SM, of as many warps
+// (at most this many threads) as the registers a GEMM CTA leaves free allow.
+constexpr int kEarlyMaxThreads = 768;
 constexpr long long kBarrierLimitCycles = 4000000000ll;  // about 2 s at the SM clock
 
 __device__ __forceinline__ bool has_nonfinite_bf16x2(uint32_t w) {
@@ -221,6 +224,17 @@ __device__ __forceinline__ AdamOpt make_opt(const AdamArgs &a, float inv_s) {
     return o;
 }
 
+// This thread's grid-stride share of an n-byte copy (16-byte vectors, the
+// n % 16 tail by the last block).
+__device__ __forceinline__ void copy_share(const uint8_t *__restrict__ src, uint8_t *__restrict__ dst, int64_t n) {
+    const int64_t nvec = n >> 4;
+    const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+    for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < nvec; i += stride)
+        reinterpret_cast<uint4 *>(dst)[i] = __ldcs(reinterpret_cast<const uint4 *>(src) + i);
+    if (blockIdx.x == gridDim.x - 1)
+        for (int64_t i = (nvec << 4) + threadIdx.x; i < n; i += blockDim.x) dst[i] = src[i];
+}
+
 // The update pass over this thread's grid-stride share: the optimizer, the
 // E4M3 re-cast of the new master weights under *scale_w, their max |w|.
 template <class Opt>
@@ -290,6 +304,7 @@ struct StepCommon {
     const uint16_t *g;
     int64_t n;
     uint8_t *w8;
+    const uint8_t *w8_in;  // the current copy when w8 is another buffer, else NULL (in place)
     const float *scale_w;
     float *amax_w;
     float *loss_scale;
@@ -377,11 +392,28 @@ __global__ void __launch_bounds__(kThreads) fused_step_kernel(const StepCommon c
 // the word when it is done (the count never touches bit 0); the last block
 // does the bookkeeping, writes found_inf and resets the word to 0 for the
 // next producer.
-template <class Opt, class Args, class Extra>
-__global__ void __launch_bounds__(kThreads)
+//
+// With c.w8_in the new E4M3 copy goes to another buffer than the current
+// one, and a skipped step copies the current one there. EARLY
+// (FP8MP_OVERLAP_PREVIOUS): the caller guarantees that the kernel still
+// running before this one on the stream neither writes nor reads anything
+// the step touches (for example the dgrad GEMM of the same backward pass,
+// which reads the current E4M3 copy while the step writes the other one), so
+// the blocks start without waiting for it; block 0 waits for it at its very
+// end, so the grid completes after it. What the step reads from the kernels
+// before that one (the wgrad GEMM's dW and flag, the scale update's scale)
+// is complete: the previous kernel let this one start only after its own
+// wait on them had returned. The early grid is one block per SM,
+// sized to fit beside a CTA of the GEMM (whose shared memory leaves room for
+// one more block): every block runs from the start, so the whole update
+// overlaps the GEMM instead of the few blocks that find room first.
+template <class Opt, class Args, class Extra, bool EARLY>
+__global__ void __launch_bounds__(EARLY ? kEarlyMaxThreads : kThreads, EARLY ? 1 : 0)
 prescanned_step_kernel(const StepCommon c, const Args a, const Extra x, int32_t *grad_nonfinite) {
-    pdl_wait();
-    pdl_launch_dependents();
+    if constexpr (!EARLY) {
+        pdl_wait();
+        pdl_launch_dependents();
+    }
     __shared__ int s_skip;
     if (threadIdx.x == 0) s_skip = (*reinterpret_cast<volatile int32_t *>(grad_nonfinite) & 1) != 0;
     __syncthreads();
@@ -389,6 +421,8 @@ prescanned_step_kernel(const StepCommon c, const Args a, const Extra x, int32_t 
     if (!s_skip) {
         const Opt opt = make_opt(a, __fdiv_rn(1.0f, *c.loss_scale));
         am = update_share(opt, c.g, c.n, c.w8, *c.scale_w);
+    } else if (c.w8_in != nullptr && c.w8_in != c.w8) {
+        copy_share(c.w8_in, c.w8, c.n);  // skipped: the next copy is the current one
     }
     block_amax_atomic(am, c.amax_w);
     if (threadIdx.x == 0) {
@@ -401,6 +435,12 @@ prescanned_step_kernel(const StepCommon c, const Args a, const Extra x, int32_t 
             loss_scale_update(c.loss_scale, c.growth, found, c.backoff, c.growth_factor, c.interval);
             *c.found_inf = found;
             *grad_nonfinite = 0;
+        }
+    }
+    if constexpr (EARLY) {  // the next kernel may start once this wait has returned (as for the casts)
+        if (blockIdx.x == 0 && threadIdx.x == 0) {
+            pdl_wait();
+            pdl_launch_dependents();
         }
     }
 }
@@ -428,9 +468,40 @@ struct FusedGrid {
 };
 FusedGrid g_fused[64];
 
+// Threads of an early block: as many warps as fit in the register file
+// beside one CTA of the GEMM. The file is split between the SM's four
+// schedulers, and the warps of a CTA are dealt to them in turn, so the
+// bound is per scheduler: its quarter of the file, less the registers of the
+// GEMM warps it holds (at most ceil(warps / 4)), over the registers of one
+// warp of this kernel (allocated 8 per thread at a time), times four.
+// Queried once per optimizer.
+std::atomic<int> g_early_threads[2];
+
+template <class Opt, class Args, class Extra>
+int early_block_threads(int which, const DeviceInfo &dev) {
+    int t = g_early_threads[which].load(std::memory_order_relaxed);
+    if (t >= 32) return t;
+    cudaFuncAttributes fa;
+    int file = 0;
+    if (cudaFuncGetAttributes(&fa, prescanned_step_kernel<Opt, Args, Extra, true>) != cudaSuccess ||
+        cudaDeviceGetAttribute(&file, cudaDevAttrMaxRegistersPerMultiprocessor, dev.device) != cudaSuccess)
+        return 0;
+    int gemm_warps = 0;
+    const int gemm_warp = gemm_warp_registers(&gemm_warps);
+    if (gemm_warp <= 0) return 0;
+    const int per_warp = 32 * ((fa.numRegs + 7) & ~7);
+    const int free_per_scheduler = file / 4 - ((gemm_warps + 3) / 4) * gemm_warp;
+    int warps = 4 * (free_per_scheduler > 0 ? free_per_scheduler / per_warp : 0);
+    if (warps > kEarlyMaxThreads / 32) warps = kEarlyMaxThreads / 32;
+    if (warps < 4) warps = 4;  // no room beside the GEMM: the blocks wait for it, still one per SM
+    t = warps * 32;
+    g_early_threads[which].store(t, std::memory_order_relaxed);
+    return t;
+}
+
 template <class Opt, class Args, class Extra>
 int launch_step(const StepCommon &c, const Args &a, const Extra &x, int which, cudaStream_t s, const DeviceInfo &dev,
-                const char *fn, int32_t *grad_nonfinite = nullptr) {
+                const char *fn, int32_t *grad_nonfinite = nullptr, bool early = false) {
     cudaError_t e = cudaSuccess;
     if (grad_nonfinite == nullptr) {  // the scanning steps count arrivals in found_inf: zero it
         e = launch_zero_word(c.found_inf, s);
@@ -445,8 +516,16 @@ int launch_step(const StepCommon &c, const Args &a, const Extra &x, int which, c
         // than a grid of resident blocks
         const int64_t cap = static_cast<int64_t>(dev.num_sms) * 32;
         if (blocks > cap) blocks = cap;
-        e = launch_kernel(prescanned_step_kernel<Opt, Args, Extra>, dim3(static_cast<unsigned>(blocks)),
-                          dim3(kThreads), 0, s, c, a, x, grad_nonfinite);
+        if (early) {
+            const int threads = early_block_threads<Opt, Args, Extra>(which, dev);
+            if (threads < 32) return fail(FP8MP_ERR_LAUNCH, "%s: kernel attribute query failed", fn);
+            int64_t eb = (nvec + threads - 1) / threads;
+            eb = eb < 1 ? 1 : (eb > dev.num_sms ? dev.num_sms : eb);
+            e = launch_kernel(prescanned_step_kernel<Opt, Args, Extra, true>, dim3(static_cast<unsigned>(eb)),
+                              dim3(threads), 0, s, c, a, x, grad_nonfinite);
+        } else
+            e = launch_kernel(prescanned_step_kernel<Opt, Args, Extra, false>, dim3(static_cast<unsigned>(blocks)),
+                              dim3(kThreads), 0, s, c, a, x, grad_nonfinite);
         if (e != cudaSuccess) return fail(FP8MP_ERR_LAUNCH, "%s: launch failed: %s", fn, cudaGetErrorString(e));
         return FP8MP_OK;
     }
@@ -493,25 +572,27 @@ int launch_step(const StepCommon &c, const Args &a, const Extra &x, int which, c
 int launch_adam_step(const uint16_t *g, int64_t n, float *w, float *m, float *v, uint8_t *w8, const float *scale_w,
                      float *amax_w, float *loss_scale, int32_t *growth, int32_t *found_inf, float *beta_pows,
                      float lr, float b1, float b2, float eps, float backoff, float growth_factor,
-                     int32_t growth_interval, cudaStream_t s, const DeviceInfo &dev, int32_t *grad_nonfinite) {
-    const StepCommon c = {g, n, w8, scale_w, amax_w, loss_scale, growth, found_inf, backoff, growth_factor,
+                     int32_t growth_interval, cudaStream_t s, const DeviceInfo &dev, int32_t *grad_nonfinite,
+                     const uint8_t *w8_in, bool early) {
+    const StepCommon c = {g, n, w8, w8_in, scale_w, amax_w, loss_scale, growth, found_inf, backoff, growth_factor,
                           growth_interval};
     const AdamArgs a = {w, m, v, beta_pows, lr, b1, b2, eps};
     const AdamExtra x = {beta_pows, b1, b2};
     return launch_step<AdamOpt>(c, a, x, 1, s, dev, grad_nonfinite ? "mp_master_step_adam_prescanned"
                                                                    : "mp_master_step_adam",
-                                grad_nonfinite);
+                                grad_nonfinite, early);
 }
 
 int launch_master_step(const uint16_t *g, int64_t n, float *w, float *v, uint8_t *w8, const float *scale_w,
                        float *amax_w, float *loss_scale, int32_t *growth, int32_t *found_inf, float lr, float mu,
                        float backoff, float growth_factor, int32_t growth_interval, cudaStream_t s,
-                       const DeviceInfo &dev, int32_t *grad_nonfinite) {
-    const StepCommon c = {g, n, w8, scale_w, amax_w, loss_scale, growth, found_inf, backoff, growth_factor,
+                       const DeviceInfo &dev, int32_t *grad_nonfinite, const uint8_t *w8_in, bool early) {
+    const StepCommon c = {g, n, w8, w8_in, scale_w, amax_w, loss_scale, growth, found_inf, backoff, growth_factor,
                           growth_interval};
     const SgdArgs a = {w, v, lr, mu};
     return launch_step<SgdOpt>(c, a, NoExtra{}, 0, s, dev,
-                               grad_nonfinite ? "mp_master_step_prescanned" : "mp_master_step", grad_nonfinite);
+                               grad_nonfinite ? "mp_master_step_prescanned" : "mp_master_step", grad_nonfinite,
+                               early);
 }
 
 int launch_barrier_selftest(cudaStream_t s) {

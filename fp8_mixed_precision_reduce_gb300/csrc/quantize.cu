@@ -120,13 +120,19 @@ constexpr int kChunksPerThread = 4;
 // running before this one on the stream neither writes nor reads x, out or
 // *amax, so the blocks start without waiting for it (they use what it leaves
 // free of the SMs); block 0 waits for it at its very end, so the grid still
-// completes after it and whatever follows on the stream sees both.
+// completes after it and whatever follows on the stream sees both. Like
+// every kernel of the library it lets the next kernel start only after its
+// own wait has returned (here: block 0's, at the end; the other blocks let
+// it by exiting), so a kernel that starts early behind this one still knows
+// every kernel before this one complete.
 template <int FMT, bool BF16, bool EARLY>
 __global__ void __launch_bounds__(kThreads, 4)
 cast_rows_kernel(const void *__restrict__ x, int64_t n, const float *__restrict__ scale_p,
                  uint8_t *__restrict__ out, float *__restrict__ amax_p) {
-    if constexpr (!EARLY) pdl_wait();
-    pdl_launch_dependents();
+    if constexpr (!EARLY) {
+        pdl_wait();
+        pdl_launch_dependents();
+    }
     const float scale = __ldg(scale_p);
     float am = 0.0f;
     const int64_t nchunk = n >> 4;
@@ -198,7 +204,10 @@ cast_rows_kernel(const void *__restrict__ x, int64_t n, const float *__restrict_
     }
     if (amax_p != nullptr) block_amax_atomic(am, amax_p);
     if constexpr (EARLY) {
-        if (blockIdx.x == 0) pdl_wait();
+        if (blockIdx.x == 0) {
+            pdl_wait();
+            pdl_launch_dependents();
+        }
     }
 }
 
@@ -229,8 +238,10 @@ template <int FMT, bool BF16, bool EARLY>
 __global__ void __launch_bounds__(kThreads, BF16 ? 4 : 3)
 cast_rows_t_kernel(const void *__restrict__ x, int64_t rows, int64_t cols, const float *__restrict__ scale_p,
                    uint8_t *__restrict__ out, uint8_t *__restrict__ out_t, float *__restrict__ amax_p) {
-    if constexpr (!EARLY) pdl_wait();
-    pdl_launch_dependents();
+    if constexpr (!EARLY) {
+        pdl_wait();
+        pdl_launch_dependents();
+    }
     __shared__ __align__(16) uint32_t sT[128 * 32];
     const int64_t tiles_c = (cols + 127) >> 7;
     const int64_t tr = blockIdx.x / tiles_c, tc = blockIdx.x - tr * tiles_c;
@@ -318,7 +329,10 @@ cast_rows_t_kernel(const void *__restrict__ x, int64_t rows, int64_t cols, const
     }
     if (amax_p != nullptr) block_amax_atomic(am, amax_p);
     if constexpr (EARLY) {
-        if (blockIdx.x == 0) pdl_wait();
+        if (blockIdx.x == 0) {
+            pdl_wait();
+            pdl_launch_dependents();
+        }
     }
 }
 

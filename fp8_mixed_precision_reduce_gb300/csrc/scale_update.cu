@@ -27,6 +27,7 @@ struct MetaArgs {
     float *scale;
     float *scale_inv;
     float *cur_amax;
+    float *prev_scale_inv;  // receives scale_inv as it was before the update, or NULL
     int32_t len;
     int32_t fmt;
 };
@@ -44,8 +45,9 @@ __global__ void __launch_bounds__(kThreads) scale_update_kernel(const __grid_con
     const MetaArgs &m = b.m[blockIdx.x];
     const int L = m.len;
     const float cur = *m.cur_amax;
-    // the old scale, loaded with the rest so the final step waits on nothing
+    // the old scale (and scale_inv), loaded with the rest so the final step waits on nothing
     const float old_scale = threadIdx.x == 0 ? *m.scale : 0.0f;
+    const float old_sinv = (threadIdx.x == 0 && m.prev_scale_inv != nullptr) ? *m.scale_inv : 0.0f;
     for (int j = threadIdx.x; j < L; j += blockDim.x) old_hist[j] = m.hist[j];
     __syncthreads();
     // roll by one, newest first, and take the max of the new window
@@ -64,6 +66,7 @@ __global__ void __launch_bounds__(kThreads) scale_update_kernel(const __grid_con
         for (int w = 0; w < kThreads / 32; ++w) all = fmaxf(all, red[w]);
         const float a = (b.algo == FP8MP_AMAX_MAX) ? all : cur;
         const float sc = scale_from_amax(a, old_scale, m.fmt, b.margin);
+        if (m.prev_scale_inv != nullptr) *m.prev_scale_inv = old_sinv;
         *m.scale = sc;
         *m.scale_inv = __fdiv_rn(1.0f, sc);
         *m.cur_amax = 0.0f;
@@ -72,7 +75,8 @@ __global__ void __launch_bounds__(kThreads) scale_update_kernel(const __grid_con
 
 }  // namespace
 
-int launch_scale_update(const fp8mp_meta *metas, int32_t n, int32_t algo, int32_t margin, cudaStream_t s) {
+int launch_scale_update(const fp8mp_meta *metas, int32_t n, int32_t algo, int32_t margin, cudaStream_t s,
+                        float *prev_scale_inv) {
     for (int32_t first = 0; first < n; first += kMetasPerLaunch) {
         const int32_t cnt = (n - first < kMetasPerLaunch) ? (n - first) : kMetasPerLaunch;
         MetaBatch b;
@@ -80,7 +84,9 @@ int launch_scale_update(const fp8mp_meta *metas, int32_t n, int32_t algo, int32_
         int32_t max_len = 1;
         for (int32_t i = 0; i < cnt; ++i) {
             const fp8mp_meta &src = metas[first + i];
-            b.m[i] = MetaArgs{src.amax_history, src.scale, src.scale_inv, src.cur_amax, src.history_len, src.fmt};
+            b.m[i] = MetaArgs{src.amax_history, src.scale, src.scale_inv, src.cur_amax,
+                              prev_scale_inv != nullptr ? prev_scale_inv + first + i : nullptr, src.history_len,
+                              src.fmt};
             if (src.history_len > max_len) max_len = src.history_len;
         }
         b.algo = algo;

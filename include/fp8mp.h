@@ -387,6 +387,21 @@ int delayed_scaling_update(const fp8mp_meta *metas, int32_t n, int32_t algo, int
                            void *stream);
 
 /*
+ * delayed_scaling_update_ex -- delayed_scaling_update that also keeps the
+ * scale_inv each tensor had before the update:
+ *   prev_scale_inv[i] = metas[i].scale_inv as it was on entry
+ * prev_scale_inv  device float[n] (4-byte aligned) or NULL (then this is
+ *   delayed_scaling_update). With it the update may run before the backward
+ *   GEMMs of the step: they take their scale_inv factors from
+ *   prev_scale_inv, which are the factors the step's casts used ([TE-FP8]
+ *   "Scaling factor 선택 전략": the step's tensors are cast with the scale of
+ *   the previous steps' history; the new scale applies from the next cast on),
+ *   so the results are bitwise those of the update run after them.
+ */
+int delayed_scaling_update_ex(const fp8mp_meta *metas, int32_t n, int32_t algo, int32_t margin,
+                              float *prev_scale_inv, void *stream);
+
+/*
  * mp_master_step -- one mixed-precision optimizer step on a flat parameter
  * buffer: loss unscale, overflow check with dynamic loss scaling, FP32
  * master-weight SGD-momentum update and E4M3 re-cast ([MP] "FP32 Master Copy
@@ -467,6 +482,46 @@ int mp_master_step_adam_prescanned(const uint16_t *grad_bf16, int64_t n, float *
                                    int32_t *grad_nonfinite, float *beta_pows, float lr, float beta1, float beta2,
                                    float eps, float backoff, float growth_factor, int32_t growth_interval,
                                    void *stream);
+
+/*
+ * mp_master_step_prescanned_ex, mp_master_step_adam_prescanned_ex -- the
+ * prescanned steps with the new E4M3 copy of the weight written to another
+ * buffer than the one the current step's GEMMs read, so that the update can
+ * run while a GEMM still reads the current copy:
+ *   w8_in   [n] E4M3 codes: the current copy, read only when the step is
+ *           skipped (found_inf): then w8_out = w8_in, so w8_out always holds
+ *           the copy the next step uses. NULL or equal to w8_out: in place,
+ *           as the calls without _ex. Otherwise w8_in and w8_out must not
+ *           overlap.
+ *   w8_out  [n] E4M3 codes (written): the w8 of the calls without _ex.
+ *   flags   0 or FP8MP_OVERLAP_PREVIOUS: the caller guarantees that the work
+ *           enqueued on `stream` before this call, other than what completed
+ *           before the last kernel started, neither writes nor reads anything
+ *           this step reads or writes. The typical case is the dgrad GEMM
+ *           (fp8_linear_bwd_rowmajor with dw = NULL) enqueued right after the
+ *           wgrad GEMM that produced grad_bf16 and grad_nonfinite: it reads
+ *           w8_in while the step writes w8_out. The step then starts without
+ *           waiting for that GEMM, as one block per SM whose registers fit
+ *           beside the GEMM's CTA, and still completes only after it. The
+ *           kernel before that one (the wgrad GEMM) must have finished
+ *           before the previous kernel started (the library's kernels wait
+ *           for their predecessor before they let the next one start).
+ *           Without programmatic launch (FP8MP_PDL=0) the flag has no
+ *           effect. Other bits: FP8MP_ERR_INVALID.
+ * Every other argument and every result as the calls without _ex (w8 there
+ * is w8_out here).
+ */
+int mp_master_step_prescanned_ex(const uint16_t *grad_bf16, int64_t n, float *master, float *momentum,
+                                 const uint8_t *w8_in, uint8_t *w8_out, const float *scale_w, float *amax_w,
+                                 float *loss_scale, int32_t *growth_tracker, int32_t *found_inf,
+                                 int32_t *grad_nonfinite, float lr, float momentum_coef, float backoff,
+                                 float growth_factor, int32_t growth_interval, uint32_t flags, void *stream);
+int mp_master_step_adam_prescanned_ex(const uint16_t *grad_bf16, int64_t n, float *master, float *exp_avg,
+                                      float *exp_avg_sq, const uint8_t *w8_in, uint8_t *w8_out,
+                                      const float *scale_w, float *amax_w, float *loss_scale,
+                                      int32_t *growth_tracker, int32_t *found_inf, int32_t *grad_nonfinite,
+                                      float *beta_pows, float lr, float beta1, float beta2, float eps, float backoff,
+                                      float growth_factor, int32_t growth_interval, uint32_t flags, void *stream);
 
 /*
  * fp8mp_check -- synchronises `stream`, then reports and clears the device

@@ -1,15 +1,19 @@
 """The benchmark's training step (bench.LinearStep) against the oracle: a
 small instance over three steps, and the full proj-linear workload (M = 8192,
-K = N = 4096) over an eager step and a step replayed from a CUDA graph, the
-launch configuration bench.py times.
+K = N = 4096) over an eager step and steps replayed from the CUDA graphs
+bench.py times.
 
 The step casts x and dY row-major only, runs the forward GEMM on the weight's
-E4M3 copy, both backward GEMMs from the row-major copies in one launch, the
-delayed-scaling update, then the master step, which re-casts the weight's
-E4M3 copy under the just-updated weight scale for the next step. Checked
-here: every code and every meta bit-exact; every GEMM output within the GEMM
-tolerance; the master step bit-exact on the GPU's own bf16 dW (dW is the
-master step's input, and its rounding is not unique)."""
+E4M3 copy, the backward GEMMs from the row-major copies, the delayed-scaling
+update and the master step, which re-casts the weight's E4M3 copy under the
+just-updated weight scale for the next step. Both schedules are checked: the
+serial one (one-launch backward, update, master step in place) and the
+overlapped one the bench times (update first, keeping the casts' scale_inv
+for the backward; wgrad, dgrad, then the master step beside dgrad writing
+the other of two weight copies). Checked here: every code and every meta
+bit-exact; every GEMM output within the GEMM tolerance; the master step
+bit-exact on the GPU's own bf16 dW (dW is the master step's input, and its
+rounding is not unique)."""
 
 import numpy as np
 import pytest
@@ -85,9 +89,11 @@ class OracleRun:
         assert st.gnf.item() == 0  # dW's overflow flag, consumed and reset by the master step
 
 
-def test_bench_step_matches_oracle(cuda_lib, orc):
+@pytest.mark.parametrize("overlap", [True, False])
+def test_bench_step_matches_oracle(cuda_lib, orc, overlap):
     M, K, N = 384, 512, 256  # N <= K: the step takes dY's first N columns
-    st = bench.LinearStep(m=M, k=K, n=N)
+    st = bench.LinearStep(m=M, k=K, n=N, overlap=overlap)
+    assert st.split_bwd == overlap
     run = OracleRun(orc, st)
     for step in range(3):
         st.step()
@@ -96,24 +102,24 @@ def test_bench_step_matches_oracle(cuda_lib, orc):
 
 
 @pytest.mark.slow
-def test_bench_step_full_size_eager_then_graph(cuda_lib, orc):
-    """M = 8192, K = N = 4096, every output: one eager step, then one step
-    replayed from a CUDA graph captured on a side stream (the bench's timed
-    launches)."""
+def test_bench_step_full_size_eager_then_graphs(cuda_lib, orc):
+    """M = 8192, K = N = 4096, every output: one eager step, then steps
+    replayed through bench.StepGraphs, the timed launches: the graph of each
+    weight copy in turn (the master step beside dgrad writes the copy the
+    other graph reads), then a graph with the GEMM timing events."""
     st = bench.LinearStep()
     run = OracleRun(orc, st)
     st.step()
     assert cuda_lib.fp8mp_check() == 0
     run.check_step("eager step")
-    side = torch.cuda.Stream()
-    side.wait_stream(torch.cuda.current_stream())
-    g = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(g, stream=side):
-        st.step()
-    torch.cuda.current_stream().wait_stream(side)
-    g.replay()
+    graphs = bench.StepGraphs(st, 1, upload=False)
+    for label in ("graph of one copy", "graph of the other copy"):
+        graphs.replay()
+        assert cuda_lib.fp8mp_check() == 0
+        run.check_step(label)
+    graphs.replay_timed(0)
     assert cuda_lib.fp8mp_check() == 0
-    run.check_step("graph step")
+    run.check_step("timed graph")
 
 
 def test_bench_step_skips_on_a_nan_gradient(cuda_lib):
@@ -121,6 +127,7 @@ def test_bench_step_skips_on_a_nan_gradient(cuda_lib):
     wgrad epilogue flags it and the master step skips on the flag: master
     weights, momentum and W8 unchanged, S halved, growth reset, flag reset."""
     st = bench.LinearStep(m=256, k=512, n=256)
+    assert st.split_bwd
     st.step()
     assert cuda_lib.fp8mp_check() == 0
     master, mom, w8 = st.master.clone(), st.mom.clone(), st.W8.clone()

@@ -222,3 +222,62 @@ def test_quantize_ex_rejects_unknown_flags(lib):
     assert lib.fp8_quantize_ex(P, 1, 16, 16, 0, P, P, None, None, 2, None) == fp8mp.ERR_INVALID
     assert "flags" in fp8mp.last_error()
     assert lib.fp8_quantize_ex(P, 1, 16, 16, 0, P, P, None, None, 1 << 31, None) == fp8mp.ERR_INVALID
+
+
+def test_scale_update_ex_rejects_a_misaligned_snapshot(lib):
+    P = 4096
+    arr = (fp8mp.fp8mp_meta * 1)(fp8mp.fp8mp_meta(P, P, P, P, 16, 0))
+    assert lib.delayed_scaling_update_ex(arr, 0, 0, 0, P + 2, None) == fp8mp.OK  # n == 0: no-op
+    assert lib.delayed_scaling_update_ex(arr, 1, 0, 0, P + 2, None) == fp8mp.ERR_INVALID
+    assert "prev_scale_inv" in fp8mp.last_error()
+    assert lib.delayed_scaling_update_ex(arr, 1, 2, 0, None, None) == fp8mp.ERR_INVALID  # the same checks
+
+
+def test_master_step_ex_rejects_bad_copies_and_flags(lib):
+    """The two-buffer steps: unknown flags, a misaligned w8_in and a w8_in
+    that overlaps w8_out without being it are refused before any CUDA call."""
+    P, n = 1 << 20, 1024
+    # grad, n, master, momentum, w8_in, w8_out, scale_w, amax_w, S, growth, found, gnf, lr, mu, bo, gf, gi, flags
+    sgd = [P, n, P, P, 8 * P, 4 * P, P, P, P, P, P, 2 * P, 1e-4, 0.9, 0.5, 2.0, 2000, 0, None]
+    for i, v, word in ((17, 2, "flags"), (17, 1 << 31, "flags"), (4, 8 * P + 8, "w8_in"),
+                       (4, 4 * P + 512, "overlap"), (4, 4 * P - 512, "overlap"), (11, None, "grad_nonfinite")):
+        bad = list(sgd)
+        bad[i] = v
+        assert lib.mp_master_step_prescanned_ex(*bad) == fp8mp.ERR_INVALID, (i, v)
+        assert word in fp8mp.last_error(), (i, v, fp8mp.last_error())
+    # adam: grad, n, master, m, v, w8_in, w8_out, scale_w, amax_w, S, growth, found, gnf, beta_pows, lr, b1, b2,
+    # eps, bo, gf, gi, flags
+    adam = [P, n, P, P, P, 8 * P, 4 * P, P, P, P, P, P, 2 * P, P, 1e-4, 0.9, 0.999, 1e-8, 0.5, 2.0, 2000, 4, None]
+    assert lib.mp_master_step_adam_prescanned_ex(*adam) == fp8mp.ERR_INVALID and "flags" in fp8mp.last_error()
+    adam[21], adam[5] = 1, 4 * P + 16
+    assert lib.mp_master_step_adam_prescanned_ex(*adam) == fp8mp.ERR_INVALID and "overlap" in fp8mp.last_error()
+
+
+def test_binding_routes_the_two_buffer_step(monkeypatch):
+    """mp_master_step(w8_in=..., flags=...) calls the _ex entry point with
+    the current copy before the new one, and refuses without grad_nonfinite."""
+    import torch
+
+    calls = []
+
+    class FakeLib:
+        def __getattr__(self, name):
+            def f(*a):
+                calls.append((name, a))
+                return 0
+            return f
+
+    monkeypatch.setattr(fp8mp, "_lib", FakeLib())
+    t = {k: torch.zeros(16, dtype=torch.float32) for k in ("g", "w", "v", "s", "a", "S", "gr", "f", "nf")}
+    w8, w8_in = torch.zeros(16, dtype=torch.uint8), torch.ones(16, dtype=torch.uint8)
+    fp8mp.mp_master_step(t["g"], t["w"], t["v"], w8, t["s"], t["a"], t["S"], t["gr"], t["f"], 0.1, 0.9,
+                         stream=0, grad_nonfinite=t["nf"], w8_in=w8_in, flags=fp8mp.OVERLAP_PREVIOUS)
+    name, a = calls[-1]
+    assert name == "mp_master_step_prescanned_ex"
+    assert a[4] == w8_in.data_ptr() and a[5] == w8.data_ptr() and a[17] == fp8mp.OVERLAP_PREVIOUS
+    with pytest.raises(fp8mp.Fp8mpError):
+        fp8mp.mp_master_step(t["g"], t["w"], t["v"], w8, t["s"], t["a"], t["S"], t["gr"], t["f"], 0.1, 0.9,
+                             stream=0, w8_in=w8_in)
+    snap = torch.zeros(4, dtype=torch.float32)
+    fp8mp.delayed_scaling_update([], fp8mp.AMAX_MAX, 0, stream=0, prev_scale_inv=snap)
+    assert calls[-1][0] == "delayed_scaling_update_ex" and calls[-1][1][4] == snap.data_ptr()
