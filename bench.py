@@ -12,22 +12,24 @@ through the library's entry points on one CUDA stream:
                                                  beside the forward GEMM
   delayed_scaling_update_ex(x, w, y, dy metas    L = 1024, most_recent; keeps the
                             -> prev scale_inv)   scale_inv factors the casts used
-  fp8_linear_bwd_rowmajor(dY8, X8 -> dW bf16)    wgrad, from the row-major copies
-                                                 (no transposed ones); its epilogue
-                                                 flags an Inf/NaN in the stored dW
-  fp8_linear_bwd_rowmajor(dY8, W8 -> dX bf16)    dgrad
+  fp8_linear_bwd_rowmajor_ex(dY8, W8, X8          dgrad and wgrad GEMMs in one launch
+      -> dX bf16, dW bf16; SIGNAL_DW_DONE)       from the row-major copies, wgrad
+                                                 tiles first; the epilogue flags an
+                                                 Inf/NaN in the stored dW and signals
+                                                 when dW is complete
   mp_master_step_prescanned_ex(dW -> master,     SGD-momentum, loss scale 2^16,
-      momentum, next W8; FP8MP_OVERLAP_PREVIOUS) skip decided by that flag;
-                                                 re-casts the weight under the
-                                                 updated scale into the other of
-                                                 two W8 buffers while dgrad still
-                                                 reads this step's
+      momentum, next W8; OVERLAP_PREVIOUS        started beside the backward launch,
+      | WAIT_DW_DONE)                            waits for that signal; skip decided
+                                                 by the flag; re-casts the weight
+                                                 under the updated scale into the
+                                                 other of two W8 buffers while dgrad
+                                                 still reads this step's
 The weight's first E4M3 copy is cast once before the first step; from then
 on each step's master step writes the next step's W8 (and records the amax
 of the new master weights for the next scale update), so the weight is cast
 once per optimizer step, inside the fused update pass. The results are
-bitwise those of the serial order (one-launch backward, then the update,
-then the master step in place), which --no-overlap times.
+bitwise those of the serial order (the backward, then the update, then the
+master step in place), which --no-overlap times.
 The metric counts the FLOPs the FP8 tensor cores perform, 3 * 2 * M * N * K,
 per step time. Multi-GPU runs are independent replicas (weak scaling).
 
@@ -293,14 +295,16 @@ class LinearStep:
 
     With `overlap` (the default) two kernels run beside a GEMM instead of
     after it: the dY cast beside the forward GEMM (dY is an input of the
-    step, not that GEMM's result), and the master step beside the dgrad GEMM.
-    For the latter the backward runs as two launches, wgrad first (dW and its
-    overflow flag are all the master step needs), the delayed-scaling update
-    moves before them (keeping the scale_inv factors this step's casts used,
-    which the backward GEMMs take), and the weight's E4M3 copy is double
-    buffered: dgrad reads the current copy while the master step writes the
-    next one. Every result is bitwise that of the serial order. Without it:
-    the one-launch backward, the update, the master step in place."""
+    step, not that GEMM's result), and the master step beside the dgrad
+    tiles of the one-launch backward. For the latter the backward launch runs
+    its wgrad tiles first and signals in dW's overflow word when dW is
+    stored; the master step, started beside it, waits for that signal. The
+    delayed-scaling update moves before the backward (keeping the scale_inv
+    factors this step's casts used, which the backward GEMMs take), and the
+    weight's E4M3 copy is double buffered: dgrad reads the current copy while
+    the master step writes the next one. Every result is bitwise that of the
+    serial order. Without it: the backward, the update, the master step in
+    place."""
 
     def __init__(self, m=M_TOK, k=K_IN, n=N_OUT, seed=3, prescanned=True, overlap=True):
         import torch
@@ -310,8 +314,8 @@ class LinearStep:
 
         self.fp8mp = fp8mp
         self.overlap = overlap
-        # the master step beside dgrad needs the epilogue's overflow flag
-        self.split_bwd = overlap and prescanned
+        # the master step beside the backward needs the epilogue's overflow word
+        self.overlap_master = overlap and prescanned
         self.m, self.k, self.n = m, k, n
         dev = "cuda"
         tb = workloads.transformer_block(seed=seed, m=m, d=k, device=dev)
@@ -321,7 +325,7 @@ class LinearStep:
         del tb
         u8 = torch.uint8
         self.X8 = torch.empty((m, k), dtype=u8, device=dev)
-        self.W8s = [torch.empty((n, k), dtype=u8, device=dev) for _ in range(2 if self.split_bwd else 1)]
+        self.W8s = [torch.empty((n, k), dtype=u8, device=dev) for _ in range(2 if self.overlap_master else 1)]
         self.cur = 0  # index of the copy the next step reads
         self.D8 = torch.empty((m, n), dtype=u8, device=dev)
         self.y = torch.empty((m, n), dtype=torch.bfloat16, device=dev)
@@ -342,13 +346,10 @@ class LinearStep:
         self.md = fp8mp.Meta(HIST_LEN, E5)
         # the weight's first E4M3 copy (and its amax for the first update)
         fp8mp.fp8_quantize(self.master, E4, self.mw.scale, self.W8, None, self.mw.cur_amax)
-        # split: 2 casts, the fwd GEMM, the update, wgrad, dgrad, the master step. Serial: 2 casts, the fwd
-        # GEMM, the fused dgrad + wgrad GEMM, the update, and the master step: one kernel on the epilogue's
-        # flag (scanning dW itself: a 4-byte memset and one kernel, or three kernels with FP8MP_FUSED_MASTER=0)
-        if self.split_bwd:
-            self.launches_per_step = 7
-        else:
-            self.launches_per_step = 6 if prescanned or os.environ.get("FP8MP_FUSED_MASTER", "1") != "0" else 8
+        # 2 casts, the fwd GEMM, the fused dgrad + wgrad GEMM, the update, and the master step: one kernel
+        # on the epilogue's flag (scanning dW itself: a 4-byte memset and one kernel, or three kernels with
+        # FP8MP_FUSED_MASTER=0)
+        self.launches_per_step = 6 if prescanned or os.environ.get("FP8MP_FUSED_MASTER", "1") != "0" else 8
 
     @property
     def W8(self):
@@ -377,7 +378,7 @@ class LinearStep:
             f.fp8_quantize_ex(dy, f.E5M2, self.md.scale, self.D8, None, self.md.cur_amax, flags=f.OVERLAP_PREVIOUS)
         else:
             f.fp8_quantize(dy, f.E5M2, self.md.scale, self.D8, None, self.md.cur_amax)
-        if not self.split_bwd:
+        if not self.overlap_master:
             if ev is not None:
                 ev[2].record()
             f.fp8_linear_bwd_rowmajor(self.D8, W8, self.X8, self.md.scale_inv, self.mw.scale_inv,
@@ -393,15 +394,16 @@ class LinearStep:
         sx, sw, sd = self.snap[0:1], self.snap[1:2], self.snap[3:4]
         if ev is not None:
             ev[2].record()
-        f.fp8_linear_bwd_rowmajor(self.D8, None, self.X8, sd, None, sx, None, self.dw, dw_nonfinite=self.gnf)
-        f.fp8_linear_bwd_rowmajor(self.D8, W8, None, sd, sw, None, dx, None)
+        # wgrad tiles first; dW's word gets its completion bit while dgrad runs
+        f.fp8_linear_bwd_rowmajor(self.D8, W8, self.X8, sd, sw, sx, dx, self.dw, dw_nonfinite=self.gnf,
+                                  flags=f.SIGNAL_DW_DONE)
         if ev is not None:
             ev[3].record()
         nxt = self.cur ^ 1
-        # the next copy, written while dgrad still reads this one
+        # the next copy, written beside the backward launch (which still reads this one)
         f.mp_master_step(self.dw, self.master, self.mom, self.W8s[nxt], self.mw.scale, self.mw.cur_amax, self.S,
                          self.growth, self.found, LR, MU, grad_nonfinite=self.gnf, w8_in=W8,
-                         flags=f.OVERLAP_PREVIOUS)
+                         flags=f.OVERLAP_PREVIOUS | f.WAIT_DW_DONE)
         self.cur = nxt
 
 
@@ -683,9 +685,10 @@ def run_ours(args, world, rank, local):
                    else "wgrad epilogue flags Inf/NaN in the stored dW; the master step reads the flag",
                    "dy_cast": "plain, after the forward GEMM" if args.no_overlap
                    else "enqueued after the forward GEMM with FP8MP_OVERLAP_PREVIOUS: runs beside it",
-                   "backward": ("wgrad launch, dgrad launch, then the master step with FP8MP_OVERLAP_PREVIOUS "
-                                "beside dgrad (scale update before them, weight copy double-buffered)")
-                   if st.split_bwd else "dgrad + wgrad in one launch, the scale update, the master step"},
+                   "backward": ("dgrad + wgrad in one launch (wgrad tiles first, FP8MP_SIGNAL_DW_DONE), the master "
+                                "step beside it (FP8MP_OVERLAP_PREVIOUS | FP8MP_WAIT_DW_DONE); scale update before "
+                                "the backward, weight copy double-buffered")
+                   if st.overlap_master else "dgrad + wgrad in one launch, the scale update, the master step"},
         "gemm_only": {"tflops": round(world * fl / (gemm_step_ms * 1e-3) / 1e12, 2), "ms_per_step": round(gemm_step_ms, 5),
                       "fwd_ms": round(fwd_ms, 5), "bwd_ms": round(bwd_ms, 5),
                       "from": "a second pass of K steps with timing events around the GEMM launches",

@@ -26,8 +26,8 @@ _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "libfp8mp.so")
 EXPORTS = ("fp8_quantize", "fp8_quantize_ex", "fp8_quantize_current", "fp8_quantize_dbias",
            "fp8_quantize_dbias_workspace_bytes", "fp8_quantize_dbias_noalloc", "fp8_linear_fwd", "fp8_linear_fwd_fp8out", "fp8_linear_dgrad", "fp8_linear_wgrad",
-           "fp8_linear_bwd", "fp8_linear_bwd_rowmajor", "delayed_scaling_update", "delayed_scaling_update_ex",
-           "mp_master_step", "mp_master_step_adam", "mp_master_step_prescanned", "mp_master_step_adam_prescanned",
+           "fp8_linear_bwd", "fp8_linear_bwd_rowmajor", "fp8_linear_bwd_rowmajor_ex", "delayed_scaling_update",
+           "delayed_scaling_update_ex", "mp_master_step", "mp_master_step_adam", "mp_master_step_prescanned", "mp_master_step_adam_prescanned",
            "mp_master_step_prescanned_ex", "mp_master_step_adam_prescanned_ex", "fp8mp_check", "fp8mp_last_error",
            "fp8mp_version", "fp8mp_selftest_timeout", "fp8mp_selftest_barrier_timeout")
 
@@ -78,6 +78,8 @@ def load(path: str | None = None):
     L.fp8_linear_wgrad.argtypes = [P, P, I64, I64, I64, I32, P, P, P, I32, P]
     L.fp8_linear_bwd.argtypes = [P, P, P, P, I64, I64, I64, I32, P, P, P, P, I32, P, I32, P]
     L.fp8_linear_bwd_rowmajor.argtypes = [P, P, P, I64, I64, I64, I32, P, P, P, P, I32, P, I32, P, P]
+    L.fp8_linear_bwd_rowmajor_ex.argtypes = [P, P, P, I64, I64, I64, I32, P, P, P, P, I32, P, I32, P,
+                                             ctypes.c_uint32, P]
     L.delayed_scaling_update.argtypes = [ctypes.POINTER(fp8mp_meta), I32, I32, I32, P]
     L.delayed_scaling_update_ex.argtypes = [ctypes.POINTER(fp8mp_meta), I32, I32, I32, P, P]
     L.mp_master_step.argtypes = [P, I64, P, P, P, P, P, P, P, P, F, F, F, F, I32, P]
@@ -95,8 +97,8 @@ def load(path: str | None = None):
     L.fp8mp_version.restype = I32
     for name in ("fp8_quantize", "fp8_quantize_ex", "fp8_quantize_current", "fp8_quantize_dbias", "fp8_quantize_dbias_noalloc",
                  "fp8_linear_fwd", "fp8_linear_fwd_fp8out", "fp8_linear_dgrad", "fp8_linear_wgrad",
-                 "fp8_linear_bwd", "fp8_linear_bwd_rowmajor", "delayed_scaling_update", "delayed_scaling_update_ex",
-                 "mp_master_step", "mp_master_step_adam", "mp_master_step_prescanned", "mp_master_step_adam_prescanned",
+                 "fp8_linear_bwd", "fp8_linear_bwd_rowmajor", "fp8_linear_bwd_rowmajor_ex", "delayed_scaling_update",
+                 "delayed_scaling_update_ex", "mp_master_step", "mp_master_step_adam", "mp_master_step_prescanned", "mp_master_step_adam_prescanned",
                  "mp_master_step_prescanned_ex", "mp_master_step_adam_prescanned_ex", "fp8mp_check",
                  "fp8mp_selftest_timeout", "fp8mp_selftest_barrier_timeout"):
         getattr(L, name).restype = ctypes.c_int
@@ -156,7 +158,9 @@ def fp8_quantize(x: torch.Tensor, fmt: int, scale: torch.Tensor, out: torch.Tens
                                _ptr(out_t), _ptr(amax), _stream(stream)))
 
 
-OVERLAP_PREVIOUS = 1  # fp8_quantize_ex flag
+OVERLAP_PREVIOUS = 1  # FP8MP_OVERLAP_PREVIOUS: fp8_quantize_ex, mp_master_step(_adam) with w8_in
+SIGNAL_DW_DONE = 2  # FP8MP_SIGNAL_DW_DONE: fp8_linear_bwd_rowmajor
+WAIT_DW_DONE = 4  # FP8MP_WAIT_DW_DONE: mp_master_step(_adam) with grad_nonfinite and OVERLAP_PREVIOUS
 
 
 def fp8_quantize_ex(x: torch.Tensor, fmt: int, scale: torch.Tensor, out: torch.Tensor,
@@ -273,18 +277,21 @@ def fp8_linear_bwd(dy8: torch.Tensor, dy8t: torch.Tensor, w8t: torch.Tensor, x8t
 def fp8_linear_bwd_rowmajor(dy8: torch.Tensor, w8: torch.Tensor | None, x8: torch.Tensor | None,
                             sinv_dy: torch.Tensor, sinv_w: torch.Tensor | None, sinv_x: torch.Tensor | None,
                             dx: torch.Tensor | None, dw: torch.Tensor | None, dy_fmt: int = E5M2,
-                            dw_nonfinite: torch.Tensor | None = None, stream=None) -> None:
+                            dw_nonfinite: torch.Tensor | None = None, stream=None, flags: int = 0) -> None:
     """Both backward GEMMs from the forward's row-major FP8 copies, one launch:
     dx[M, K] = (dy8 . w8) * sinv_dy * sinv_w, dw[N, K] = (dy8^T . x8) * sinv_dy * sinv_x.
     dx or dw may be None to skip that gradient. dw_nonfinite (int32[1] on the
-    device) gets 1 OR-ed in when a stored element of dw is Inf or NaN."""
+    device) gets 1 OR-ed in when a stored element of dw is Inf or NaN. flags
+    (SIGNAL_DW_DONE) selects fp8_linear_bwd_rowmajor_ex."""
     M, N = dy8.shape
     K = (w8 if w8 is not None else x8).shape[1]
-    _check(load().fp8_linear_bwd_rowmajor(_ptr(dy8), _ptr(w8), _ptr(x8), M, N, K, dy_fmt, _ptr(sinv_dy),
-                                          _ptr(sinv_w), _ptr(sinv_x), _ptr(dx),
-                                          _dtype_code(dx) if dx is not None else F32, _ptr(dw),
-                                          _dtype_code(dw) if dw is not None else F32, _ptr(dw_nonfinite),
-                                          _stream(stream)))
+    args = (_ptr(dy8), _ptr(w8), _ptr(x8), M, N, K, dy_fmt, _ptr(sinv_dy), _ptr(sinv_w), _ptr(sinv_x), _ptr(dx),
+            _dtype_code(dx) if dx is not None else F32, _ptr(dw), _dtype_code(dw) if dw is not None else F32,
+            _ptr(dw_nonfinite))
+    if flags:
+        _check(load().fp8_linear_bwd_rowmajor_ex(*args, int(flags), _stream(stream)))
+    else:
+        _check(load().fp8_linear_bwd_rowmajor(*args, _stream(stream)))
 
 
 class Meta:

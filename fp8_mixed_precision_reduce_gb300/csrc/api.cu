@@ -18,7 +18,18 @@ __global__ void zero_word_kernel(uint32_t *word) {
     *word = 0u;
     pdl_launch_dependents();
 }
+// Sets the completion bit of an overflow word (an empty output is complete).
+__global__ void signal_done_kernel(uint32_t *word) {
+    pdl_wait();
+    pdl_launch_dependents();
+    __threadfence();
+    atomicOr(word, kDoneBit);
+}
 }  // namespace
+
+cudaError_t launch_signal_done(int32_t *word, cudaStream_t s) {
+    return launch_kernel(signal_done_kernel, dim3(1), dim3(1), 0, s, reinterpret_cast<uint32_t *>(word));
+}
 
 cudaError_t launch_zero_word(void *word, cudaStream_t s) {
     return launch_kernel(zero_word_kernel, dim3(1), dim3(1), 0, s, static_cast<uint32_t *>(word));
@@ -400,12 +411,14 @@ int fp8_linear_bwd(const uint8_t *dy8, const uint8_t *dy8t, const uint8_t *w8t, 
     return launch_gemms(d, 2, static_cast<cudaStream_t>(stream), dev);
 }
 
-int fp8_linear_bwd_rowmajor(const uint8_t *dy8, const uint8_t *w8, const uint8_t *x8, int64_t M, int64_t N,
-                            int64_t K, int32_t dy_fmt, const float *sinv_dy, const float *sinv_w,
-                            const float *sinv_x, void *dx, int32_t dx_dtype, void *dw, int32_t dw_dtype,
-                            int32_t *dw_nonfinite, void *stream) {
-    const char *fn = "fp8_linear_bwd_rowmajor";
+static int bwd_rowmajor_entry(const char *fn, const uint8_t *dy8, const uint8_t *w8, const uint8_t *x8, int64_t M,
+                              int64_t N, int64_t K, int32_t dy_fmt, const float *sinv_dy, const float *sinv_w,
+                              const float *sinv_x, void *dx, int32_t dx_dtype, void *dw, int32_t dw_dtype,
+                              int32_t *dw_nonfinite, uint32_t flags, void *stream) {
     clear_error();
+    REQUIRE((flags & ~static_cast<uint32_t>(FP8MP_SIGNAL_DW_DONE)) == 0u, "%s: unknown flags 0x%x", fn, flags);
+    if (flags & FP8MP_SIGNAL_DW_DONE)
+        REQUIRE(dw != nullptr && dw_nonfinite != nullptr, "%s: FP8MP_SIGNAL_DW_DONE needs dw and dw_nonfinite", fn);
     int rc = check_gemm_dims(fn, M, N, K);
     if (rc) return rc;
     REQUIRE(valid_fmt(dy_fmt), "%s: dy_fmt %d invalid", fn, dy_fmt);
@@ -413,13 +426,22 @@ int fp8_linear_bwd_rowmajor(const uint8_t *dy8, const uint8_t *w8, const uint8_t
     REQUIRE(dw == nullptr || valid_dtype(dw_dtype), "%s: dw_dtype %d invalid", fn, dw_dtype);
     const bool want_dx = dx != nullptr && M > 0 && K > 0;
     const bool want_dw = dw != nullptr && N > 0 && K > 0;
-    if (!want_dx && !want_dw) return FP8MP_OK;
+    const bool signal = (flags & FP8MP_SIGNAL_DW_DONE) != 0u;
+    if (!want_dx && !want_dw && !signal) return FP8MP_OK;
     CHECK_PTR(dx, false);
     CHECK_PTR(dw, false);
+    CHECK_SCALAR(dw_nonfinite, false);
+    if (!want_dx && !want_dw) {  // an empty dW is complete at once
+        DeviceInfo dev;
+        rc = current_device(&dev);
+        if (rc) return rc;
+        const cudaError_t e = launch_signal_done(dw_nonfinite, static_cast<cudaStream_t>(stream));
+        if (e != cudaSuccess) return fail(FP8MP_ERR_LAUNCH, "%s: launch failed: %s", fn, cudaGetErrorString(e));
+        return FP8MP_OK;
+    }
     CHECK_SCALAR(sinv_dy, true);
     if (want_dx) CHECK_SCALAR(sinv_w, true);
     if (want_dw) CHECK_SCALAR(sinv_x, true);
-    CHECK_SCALAR(dw_nonfinite, false);
     if (M > 0 && N > 0) {
         CHECK_PTR(dy8, true);
         if (want_dx) CHECK_PTR(w8, true);
@@ -442,9 +464,30 @@ int fp8_linear_bwd_rowmajor(const uint8_t *dy8, const uint8_t *w8, const uint8_t
                   nullptr, FP8MP_E4M3, 0, 1};
     // wgrad: A = dY8 [M x N] read MN-major (rows_a = N, kc = M), B = X8 [M x K] read MN-major
     if (want_dw)
-        d[n++] = {dy8, dy_fmt, x8, FP8MP_E4M3, N, K, M, sinv_dy, sinv_x, nullptr, FP8MP_F32, dw, dw_dtype, nullptr,
-                  nullptr, FP8MP_E4M3, 1, 1, dw_nonfinite};
+        d[n++] = {dy8,     dy_fmt,    x8,  FP8MP_E4M3, N,     K,       M,          sinv_dy, sinv_x, nullptr,
+                  FP8MP_F32, dw,      dw_dtype, nullptr, nullptr, FP8MP_E4M3, 1, 1, dw_nonfinite,
+                  signal};
+    if (!want_dw && signal) {  // dx only: dW is empty, complete before the GEMM
+        const cudaError_t e = launch_signal_done(dw_nonfinite, static_cast<cudaStream_t>(stream));
+        if (e != cudaSuccess) return fail(FP8MP_ERR_LAUNCH, "%s: launch failed: %s", fn, cudaGetErrorString(e));
+    }
     return launch_gemms(d, n, static_cast<cudaStream_t>(stream), dev);
+}
+
+int fp8_linear_bwd_rowmajor(const uint8_t *dy8, const uint8_t *w8, const uint8_t *x8, int64_t M, int64_t N,
+                            int64_t K, int32_t dy_fmt, const float *sinv_dy, const float *sinv_w,
+                            const float *sinv_x, void *dx, int32_t dx_dtype, void *dw, int32_t dw_dtype,
+                            int32_t *dw_nonfinite, void *stream) {
+    return bwd_rowmajor_entry("fp8_linear_bwd_rowmajor", dy8, w8, x8, M, N, K, dy_fmt, sinv_dy, sinv_w, sinv_x, dx,
+                              dx_dtype, dw, dw_dtype, dw_nonfinite, 0u, stream);
+}
+
+int fp8_linear_bwd_rowmajor_ex(const uint8_t *dy8, const uint8_t *w8, const uint8_t *x8, int64_t M, int64_t N,
+                               int64_t K, int32_t dy_fmt, const float *sinv_dy, const float *sinv_w,
+                               const float *sinv_x, void *dx, int32_t dx_dtype, void *dw, int32_t dw_dtype,
+                               int32_t *dw_nonfinite, uint32_t flags, void *stream) {
+    return bwd_rowmajor_entry("fp8_linear_bwd_rowmajor_ex", dy8, w8, x8, M, N, K, dy_fmt, sinv_dy, sinv_w, sinv_x,
+                              dx, dx_dtype, dw, dw_dtype, dw_nonfinite, flags, stream);
 }
 
 static int scale_update_entry(const char *fn, const fp8mp_meta *metas, int32_t n, int32_t algo, int32_t margin,
@@ -481,7 +524,10 @@ int delayed_scaling_update_ex(const fp8mp_meta *metas, int32_t n, int32_t algo, 
 // w8_in and the flags of the _ex forms: the current E4M3 copy (NULL or w8
 // itself: in place) and FP8MP_OVERLAP_PREVIOUS.
 static int check_w8_pair(const char *fn, const uint8_t *w8_in, const uint8_t *w8, int64_t n, uint32_t flags) {
-    REQUIRE((flags & ~static_cast<uint32_t>(FP8MP_OVERLAP_PREVIOUS)) == 0u, "%s: unknown flags 0x%x", fn, flags);
+    REQUIRE((flags & ~static_cast<uint32_t>(FP8MP_OVERLAP_PREVIOUS | FP8MP_WAIT_DW_DONE)) == 0u,
+            "%s: unknown flags 0x%x", fn, flags);
+    REQUIRE(!(flags & FP8MP_WAIT_DW_DONE) || (flags & FP8MP_OVERLAP_PREVIOUS),
+            "%s: FP8MP_WAIT_DW_DONE needs FP8MP_OVERLAP_PREVIOUS", fn);
     CHECK_PTR(w8_in, false);
     if (w8_in != nullptr && w8_in != w8 && n > 0)
         REQUIRE(w8_in + n <= w8 || w8 + n <= w8_in, "%s: w8_in and w8_out overlap without being equal", fn);
@@ -518,7 +564,7 @@ static int master_step_entry(const char *fn, const uint16_t *grad_bf16, int64_t 
     return launch_master_step(grad_bf16, n, master, momentum, w8, scale_w, amax_w, loss_scale, growth_tracker,
                               found_inf, lr, momentum_coef, backoff, growth_factor, growth_interval,
                               static_cast<cudaStream_t>(stream), dev, grad_nonfinite, w8_in,
-                              (flags & FP8MP_OVERLAP_PREVIOUS) != 0u);
+                              (flags & FP8MP_OVERLAP_PREVIOUS) != 0u, (flags & FP8MP_WAIT_DW_DONE) != 0u);
 }
 
 int mp_master_step(const uint16_t *grad_bf16, int64_t n, float *master, float *momentum, uint8_t *w8,
@@ -572,7 +618,7 @@ static int adam_step_entry(const char *fn, const uint16_t *grad_bf16, int64_t n,
     return launch_adam_step(grad_bf16, n, master, exp_avg, exp_avg_sq, w8, scale_w, amax_w, loss_scale,
                             growth_tracker, found_inf, beta_pows, lr, beta1, beta2, eps, backoff, growth_factor,
                             growth_interval, static_cast<cudaStream_t>(stream), dev, grad_nonfinite, w8_in,
-                            (flags & FP8MP_OVERLAP_PREVIOUS) != 0u);
+                            (flags & FP8MP_OVERLAP_PREVIOUS) != 0u, (flags & FP8MP_WAIT_DW_DONE) != 0u);
 }
 
 int mp_master_step_adam(const uint16_t *grad_bf16, int64_t n, float *master, float *exp_avg, float *exp_avg_sq,

@@ -92,7 +92,20 @@ struct GemmDesc {
     int out_fmt;
     int a_mn, b_mn;
     int32_t *out_nonfinite = nullptr;  // non-null (bf16 / fp32 output): |= 1 when a stored element is Inf or NaN
+    // with out_nonfinite: also count each stored tile part in that word and
+    // set kDoneBit once the whole output is stored (see the word's layout)
+    bool signal_done = false;
 };
+// The overflow word of a gradient (fp8_linear_bwd_rowmajor's dw_nonfinite,
+// the prescanned master step's grad_nonfinite), bit by bit: bit 0 the
+// Inf/NaN flag; bits 1-15 the master step's block arrivals (2 each); bits
+// 16-29 the GEMM's stored tile parts when it signals completion; bit 30 set
+// once every part is stored. The prescanned master step resets it to 0.
+constexpr uint32_t kArrivalShift = 1, kArrivalMask = 0x7FFFu;
+constexpr uint32_t kPartShift = 16, kPartMask = 0x3FFFu;
+constexpr uint32_t kDoneBit = 1u << 30;
+// One-thread kernel that ORs kDoneBit into the word.
+cudaError_t launch_signal_done(int32_t *word, cudaStream_t s);
 // Runs 1 or 2 independent GEMMs in one persistent launch.
 int launch_gemms(const GemmDesc *descs, int n, cudaStream_t s, const DeviceInfo &dev);
 int launch_gemm(const uint8_t *a, int fmt_a, const uint8_t *b, int fmt_b, int64_t rows_a,
@@ -111,17 +124,21 @@ int launch_scale_update(const fp8mp_meta *metas, int32_t n, int32_t algo, int32_
 // w8_in: the current E4M3 copy when the new one goes to a different buffer
 // w8 (copied there on a skipped step), NULL for in place. early (prescanned
 // steps only): start without waiting for the previous kernel on the stream
-// (FP8MP_OVERLAP_PREVIOUS), complete after it.
+// (FP8MP_OVERLAP_PREVIOUS), complete after it. wait_done (with early):
+// that kernel produces the gradients and signals their completion in the
+// word (FP8MP_WAIT_DW_DONE).
 int launch_master_step(const uint16_t *g, int64_t n, float *w, float *v, uint8_t *w8,
                        const float *scale_w, float *amax_w, float *loss_scale, int32_t *growth,
                        int32_t *found_inf, float lr, float mu, float backoff, float growth_factor,
                        int32_t growth_interval, cudaStream_t s, const DeviceInfo &dev,
-                       int32_t *grad_nonfinite = nullptr, const uint8_t *w8_in = nullptr, bool early = false);
+                       int32_t *grad_nonfinite = nullptr, const uint8_t *w8_in = nullptr, bool early = false,
+                       bool wait_done = false);
 int launch_adam_step(const uint16_t *g, int64_t n, float *w, float *m, float *v, uint8_t *w8, const float *scale_w,
                      float *amax_w, float *loss_scale, int32_t *growth, int32_t *found_inf, float *beta_pows,
                      float lr, float b1, float b2, float eps, float backoff, float growth_factor,
                      int32_t growth_interval, cudaStream_t s, const DeviceInfo &dev,
-                     int32_t *grad_nonfinite = nullptr, const uint8_t *w8_in = nullptr, bool early = false);
+                     int32_t *grad_nonfinite = nullptr, const uint8_t *w8_in = nullptr, bool early = false,
+                     bool wait_done = false);
 // Enqueues the one-thread kernel whose bounded wait is meant to run out.
 int launch_timeout_selftest(cudaStream_t s);
 // Reads and clears the GEMM wait-timeout flag (after a stream sync).

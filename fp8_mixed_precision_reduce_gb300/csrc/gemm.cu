@@ -110,6 +110,7 @@ struct GemmParams {
     const float *out_scale;
     float *out_amax;
     int32_t *out_nonfinite;   // bf16 / fp32 output: |= 1 when a stored element is Inf or NaN
+    int signal_parts;         // > 0: stored tile parts to count in *out_nonfinite before kDoneBit
 };
 
 // One GEMM of a launch: its operand and output tensor maps and parameters.
@@ -682,6 +683,24 @@ gemm_fp8_kernel(const __grid_constant__ GemmBatch batch) {
                 am1 = max_ignore_nan(am1, am);
                 bad1 |= bad;
             }
+            if (P.p.signal_parts > 0) {
+                // this warp's part of the tile is stored: its flag first, then
+                // its count, once the stores are complete and visible
+                const bool bad_part = __any_sync(0xffffffffu, bad);
+                if (lane == 0) {
+                    bulk_wait_all();
+                    asm volatile("fence.proxy.async.global;" ::: "memory");
+                    __threadfence();
+                    if (bad_part) atomicOr(P.p.out_nonfinite, 1);
+                    const uint32_t old =
+                        atomicAdd(reinterpret_cast<unsigned int *>(P.p.out_nonfinite), 1u << kPartShift);
+                    if (((old >> kPartShift) & kPartMask) + 1u == static_cast<uint32_t>(P.p.signal_parts)) {
+                        __threadfence();
+                        atomicOr(reinterpret_cast<unsigned int *>(P.p.out_nonfinite), kDoneBit);
+                    }
+                }
+                __syncwarp();
+            }
             tc_fence_before();
             __syncwarp();
             if (lane == 0) {
@@ -694,7 +713,10 @@ gemm_fp8_kernel(const __grid_constant__ GemmBatch batch) {
         if (lane == 0) bulk_wait_all();  // stores done before the CTA's shared memory goes away
         for (int i = 0; i < batch.nprob; ++i) {
             const GemmParams &pp = batch.prob[i].p;
-            if (pp.out_nonfinite != nullptr && __any_sync(0xffffffffu, i == 0 ? bad0 : bad1) && lane == 0)
+            // (a signalling problem flagged each part before counting it: the
+            // word's consumer may already have reset it by now)
+            if (pp.out_nonfinite != nullptr && pp.signal_parts == 0 &&
+                __any_sync(0xffffffffu, i == 0 ? bad0 : bad1) && lane == 0)
                 atomicOr(pp.out_nonfinite, 1);
             if (pp.out_amax == nullptr) continue;
             float a = warp_max(i == 0 ? am0 : am1);
@@ -920,6 +942,11 @@ int launch_gemms(const GemmDesc *descs, int n, cudaStream_t s, const DeviceInfo 
                                                 d.out, d.out_dtype == FP8MP_BF16 ? 1 : 0, d.out_amax, d.out_scale,
                                                 d.out_fmt);
             if (e != cudaSuccess) return fail(FP8MP_ERR_LAUNCH, "GEMM fill launch failed: %s", cudaGetErrorString(e));
+            if (d.signal_done && d.out_nonfinite != nullptr) {  // the filled output is complete
+                const cudaError_t e2 = launch_signal_done(d.out_nonfinite, s);
+                if (e2 != cudaSuccess)
+                    return fail(FP8MP_ERR_LAUNCH, "GEMM signal launch failed: %s", cudaGetErrorString(e2));
+            }
             continue;
         }
         work[nw++] = &d;
@@ -975,6 +1002,15 @@ int launch_gemms(const GemmDesc *descs, int n, cudaStream_t s, const DeviceInfo 
         p.out_scale = d.out_scale;
         p.out_amax = d.out_amax;
         p.out_nonfinite = d.out_nonfinite;
+        p.signal_parts = 0;
+        if (d.signal_done && d.out_nonfinite != nullptr) {
+            // each tile is stored in parts by the epilogue warps of its CTA(s)
+            const int64_t parts = static_cast<int64_t>(p.tiles_m) * p.tiles_n * (pair ? 2 : 1) * NUM_EPI_WARPS;
+            if (parts > static_cast<int64_t>(kPartMask))
+                return fail(FP8MP_ERR_INVALID, "GEMM: %lld tile parts are too many to signal completion",
+                            static_cast<long long>(parts));
+            p.signal_parts = static_cast<int>(parts);
+        }
         const uint64_t kc = static_cast<uint64_t>(d.kc);
         const uint64_t ra = static_cast<uint64_t>(d.rows_a), rb = static_cast<uint64_t>(d.rows_b);
         rc = d.a_mn ? make_tmap(&P.ta, d.a, ra, kc, BK) : make_tmap(&P.ta, d.a, kc, ra, ROWS_A);

@@ -237,14 +237,17 @@ __device__ __forceinline__ void copy_share(const uint8_t *__restrict__ src, uint
 
 // The update pass over this thread's grid-stride share: the optimizer, the
 // E4M3 re-cast of the new master weights under *scale_w, their max |w|.
-template <class Opt>
+// CG: the gradients are read through L2 only (ld.global.cg): a step that
+// starts before their producer has finished must not see lines its SM's L1
+// kept from an earlier kernel.
+template <class Opt, bool CG = false>
 __device__ __forceinline__ float update_share(const Opt &opt, const uint16_t *__restrict__ g, int64_t n,
                                               uint8_t *__restrict__ w8, float sw) {
     float am = 0.0f;
     const int64_t nvec = n >> 3;
     const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
     for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < nvec; i += stride) {
-        const uint4 gd = __ldcs(reinterpret_cast<const uint4 *>(g) + i);
+        const uint4 gd = CG ? __ldcg(reinterpret_cast<const uint4 *>(g) + i) : __ldcs(reinterpret_cast<const uint4 *>(g) + i);
         const uint32_t gw[4] = {gd.x, gd.y, gd.z, gd.w};
         float gf[8], wf[8];
 #pragma unroll
@@ -263,7 +266,7 @@ __device__ __forceinline__ float update_share(const Opt &opt, const uint16_t *__
     }
     if (blockIdx.x == gridDim.x - 1) {
         for (int64_t i = (nvec << 3) + threadIdx.x; i < n; i += blockDim.x) {
-            const float wn = opt.scalar(i, bf16_bits_to_f32(g[i]));
+            const float wn = opt.scalar(i, bf16_bits_to_f32(CG ? __ldcg(g + i) : g[i]));
             w8[i] = static_cast<uint8_t>(cvt_pair<FP8MP_E4M3>(__fmul_rn(wn, sw), 0.0f) & 0xFFu);
             am = max_ignore_nan(am, fabsf(wn));
         }
@@ -407,7 +410,14 @@ __global__ void __launch_bounds__(kThreads) fused_step_kernel(const StepCommon c
 // sized to fit beside a CTA of the GEMM (whose shared memory leaves room for
 // one more block): every block runs from the start, so the whole update
 // overlaps the GEMM instead of the few blocks that find room first.
-template <class Opt, class Args, class Extra, bool EARLY>
+//
+// WAIT (with EARLY; FP8MP_WAIT_DW_DONE): the gradients' producer is the
+// kernel still running (a backward GEMM launch that signals completion, its
+// dW tiles first): thread 0 of each block waits, bounded by about 2 s, for
+// the word's completion bit before the flag is read, and the gradients are
+// read through L2 only. A wait that runs out raises the device timeout flag
+// and the block updates nothing.
+template <class Opt, class Args, class Extra, bool EARLY, bool WAIT>
 __global__ void __launch_bounds__(EARLY ? kEarlyMaxThreads : kThreads, EARLY ? 1 : 0)
 prescanned_step_kernel(const StepCommon c, const Args a, const Extra x, int32_t *grad_nonfinite) {
     if constexpr (!EARLY) {
@@ -415,20 +425,41 @@ prescanned_step_kernel(const StepCommon c, const Args a, const Extra x, int32_t 
         pdl_launch_dependents();
     }
     __shared__ int s_skip;
-    if (threadIdx.x == 0) s_skip = (*reinterpret_cast<volatile int32_t *>(grad_nonfinite) & 1) != 0;
+    if (threadIdx.x == 0) {
+        if constexpr (WAIT) {
+            const long long t0 = clock64();
+            uint32_t w;
+            int skip = 1;
+            for (;;) {
+                asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(w) : "l"(grad_nonfinite) : "memory");
+                if (w & kDoneBit) {
+                    skip = (w & 1u) != 0;
+                    break;
+                }
+                if (clock64() - t0 > kBarrierLimitCycles) {
+                    atomicOr(&g_master_timeout_flag, 1u);
+                    break;
+                }
+                __nanosleep(256);
+            }
+            s_skip = skip;
+        } else {
+            s_skip = (*reinterpret_cast<volatile int32_t *>(grad_nonfinite) & 1) != 0;
+        }
+    }
     __syncthreads();
     float am = 0.0f;
     if (!s_skip) {
         const Opt opt = make_opt(a, __fdiv_rn(1.0f, *c.loss_scale));
-        am = update_share(opt, c.g, c.n, c.w8, *c.scale_w);
+        am = update_share<Opt, WAIT>(opt, c.g, c.n, c.w8, *c.scale_w);
     } else if (c.w8_in != nullptr && c.w8_in != c.w8) {
         copy_share(c.w8_in, c.w8, c.n);  // skipped: the next copy is the current one
     }
     block_amax_atomic(am, c.amax_w);
     if (threadIdx.x == 0) {
         __threadfence();
-        const int32_t prev = atomicAdd(grad_nonfinite, 2);
-        if ((prev >> 1) == static_cast<int32_t>(gridDim.x) - 1) {
+        const uint32_t prev = atomicAdd(reinterpret_cast<unsigned int *>(grad_nonfinite), 1u << kArrivalShift);
+        if (((prev >> kArrivalShift) & kArrivalMask) == gridDim.x - 1) {
             __threadfence();
             const int found = s_skip;
             if (!found) x.clean_step();
@@ -483,7 +514,7 @@ int early_block_threads(int which, const DeviceInfo &dev) {
     if (t >= 32) return t;
     cudaFuncAttributes fa;
     int file = 0;
-    if (cudaFuncGetAttributes(&fa, prescanned_step_kernel<Opt, Args, Extra, true>) != cudaSuccess ||
+    if (cudaFuncGetAttributes(&fa, prescanned_step_kernel<Opt, Args, Extra, true, true>) != cudaSuccess ||
         cudaDeviceGetAttribute(&file, cudaDevAttrMaxRegistersPerMultiprocessor, dev.device) != cudaSuccess)
         return 0;
     int gemm_warps = 0;
@@ -501,7 +532,7 @@ int early_block_threads(int which, const DeviceInfo &dev) {
 
 template <class Opt, class Args, class Extra>
 int launch_step(const StepCommon &c, const Args &a, const Extra &x, int which, cudaStream_t s, const DeviceInfo &dev,
-                const char *fn, int32_t *grad_nonfinite = nullptr, bool early = false) {
+                const char *fn, int32_t *grad_nonfinite = nullptr, bool early = false, bool wait_done = false) {
     cudaError_t e = cudaSuccess;
     if (grad_nonfinite == nullptr) {  // the scanning steps count arrivals in found_inf: zero it
         e = launch_zero_word(c.found_inf, s);
@@ -521,11 +552,16 @@ int launch_step(const StepCommon &c, const Args &a, const Extra &x, int which, c
             if (threads < 32) return fail(FP8MP_ERR_LAUNCH, "%s: kernel attribute query failed", fn);
             int64_t eb = (nvec + threads - 1) / threads;
             eb = eb < 1 ? 1 : (eb > dev.num_sms ? dev.num_sms : eb);
-            e = launch_kernel(prescanned_step_kernel<Opt, Args, Extra, true>, dim3(static_cast<unsigned>(eb)),
-                              dim3(threads), 0, s, c, a, x, grad_nonfinite);
-        } else
-            e = launch_kernel(prescanned_step_kernel<Opt, Args, Extra, false>, dim3(static_cast<unsigned>(blocks)),
-                              dim3(kThreads), 0, s, c, a, x, grad_nonfinite);
+            if (wait_done)
+                e = launch_kernel(prescanned_step_kernel<Opt, Args, Extra, true, true>,
+                                  dim3(static_cast<unsigned>(eb)), dim3(threads), 0, s, c, a, x, grad_nonfinite);
+            else
+                e = launch_kernel(prescanned_step_kernel<Opt, Args, Extra, true, false>,
+                                  dim3(static_cast<unsigned>(eb)), dim3(threads), 0, s, c, a, x, grad_nonfinite);
+        } else {
+            e = launch_kernel(prescanned_step_kernel<Opt, Args, Extra, false, false>,
+                              dim3(static_cast<unsigned>(blocks)), dim3(kThreads), 0, s, c, a, x, grad_nonfinite);
+        }
         if (e != cudaSuccess) return fail(FP8MP_ERR_LAUNCH, "%s: launch failed: %s", fn, cudaGetErrorString(e));
         return FP8MP_OK;
     }
@@ -573,26 +609,27 @@ int launch_adam_step(const uint16_t *g, int64_t n, float *w, float *m, float *v,
                      float *amax_w, float *loss_scale, int32_t *growth, int32_t *found_inf, float *beta_pows,
                      float lr, float b1, float b2, float eps, float backoff, float growth_factor,
                      int32_t growth_interval, cudaStream_t s, const DeviceInfo &dev, int32_t *grad_nonfinite,
-                     const uint8_t *w8_in, bool early) {
+                     const uint8_t *w8_in, bool early, bool wait_done) {
     const StepCommon c = {g, n, w8, w8_in, scale_w, amax_w, loss_scale, growth, found_inf, backoff, growth_factor,
                           growth_interval};
     const AdamArgs a = {w, m, v, beta_pows, lr, b1, b2, eps};
     const AdamExtra x = {beta_pows, b1, b2};
     return launch_step<AdamOpt>(c, a, x, 1, s, dev, grad_nonfinite ? "mp_master_step_adam_prescanned"
                                                                    : "mp_master_step_adam",
-                                grad_nonfinite, early);
+                                grad_nonfinite, early, wait_done);
 }
 
 int launch_master_step(const uint16_t *g, int64_t n, float *w, float *v, uint8_t *w8, const float *scale_w,
                        float *amax_w, float *loss_scale, int32_t *growth, int32_t *found_inf, float lr, float mu,
                        float backoff, float growth_factor, int32_t growth_interval, cudaStream_t s,
-                       const DeviceInfo &dev, int32_t *grad_nonfinite, const uint8_t *w8_in, bool early) {
+                       const DeviceInfo &dev, int32_t *grad_nonfinite, const uint8_t *w8_in, bool early,
+                       bool wait_done) {
     const StepCommon c = {g, n, w8, w8_in, scale_w, amax_w, loss_scale, growth, found_inf, backoff, growth_factor,
                           growth_interval};
     const SgdArgs a = {w, v, lr, mu};
     return launch_step<SgdOpt>(c, a, NoExtra{}, 0, s, dev,
                                grad_nonfinite ? "mp_master_step_prescanned" : "mp_master_step", grad_nonfinite,
-                               early);
+                               early, wait_done);
 }
 
 int launch_barrier_selftest(cudaStream_t s) {

@@ -122,6 +122,11 @@ int fp8_quantize(const void *x, int32_t x_dtype, int64_t rows, int64_t cols, int
 
 /* Flags of fp8_quantize_ex. */
 #define FP8MP_OVERLAP_PREVIOUS 1u
+/* fp8_linear_bwd_rowmajor_ex: signal in dw_nonfinite when dW is stored. */
+#define FP8MP_SIGNAL_DW_DONE 2u
+/* mp_master_step(_adam)_prescanned_ex: wait for that signal (with
+ * FP8MP_OVERLAP_PREVIOUS). */
+#define FP8MP_WAIT_DW_DONE 4u
 
 /*
  * fp8_quantize_ex -- fp8_quantize with flags. The results are exactly
@@ -367,6 +372,32 @@ int fp8_linear_bwd_rowmajor(const uint8_t *dy8, const uint8_t *w8, const uint8_t
                             int32_t *dw_nonfinite, void *stream);
 
 /*
+ * fp8_linear_bwd_rowmajor_ex -- fp8_linear_bwd_rowmajor with flags:
+ *   0                     the call without _ex.
+ *   FP8MP_SIGNAL_DW_DONE  (needs dw and dw_nonfinite) the launch also tells a
+ *                         master step that runs beside it when dW is
+ *                         complete: each epilogue warp, once its part of a
+ *                         dW tile is stored and visible, ORs that part's
+ *                         Inf/NaN flag into bit 0 of *dw_nonfinite and adds
+ *                         1 << 16 to the word; the last part sets bit 30.
+ *                         (Bits 1-15 are the prescanned master step's block
+ *                         count; at most 16383 parts: dW of up to 2047 tiles
+ *                         of 256 x 256.) The word must hold only bit 0 or
+ *                         nothing before the call (the prescanned master step
+ *                         leaves it 0), and its consumer must be
+ *                         mp_master_step(_adam)_prescanned_ex, which resets
+ *                         it; an empty dW sets bit 30 at once. The launch
+ *                         runs the dW tiles first when dW's contraction (M)
+ *                         is the longer one, so the signal comes while the
+ *                         dX tiles are still being computed.
+ * Other bits: FP8MP_ERR_INVALID.
+ */
+int fp8_linear_bwd_rowmajor_ex(const uint8_t *dy8, const uint8_t *w8, const uint8_t *x8, int64_t M, int64_t N,
+                               int64_t K, int32_t dy_fmt, const float *sinv_dy, const float *sinv_w,
+                               const float *sinv_x, void *dx, int32_t dx_dtype, void *dw, int32_t dw_dtype,
+                               int32_t *dw_nonfinite, uint32_t flags, void *stream);
+
+/*
  * delayed_scaling_update -- the DelayedScaling bookkeeping of one step for a
  * batch of tensors ([TE-FP8] "Scaling factor 선택 전략", "FP8 사용방안(recipe)":
  * amax_history_len, amax_compute_algo; [PT-FP8] amax and scale history
@@ -507,7 +538,17 @@ int mp_master_step_adam_prescanned(const uint16_t *grad_bf16, int64_t n, float *
  *           before the previous kernel started (the library's kernels wait
  *           for their predecessor before they let the next one start).
  *           Without programmatic launch (FP8MP_PDL=0) the flag has no
- *           effect. Other bits: FP8MP_ERR_INVALID.
+ *           effect.
+ *           FP8MP_WAIT_DW_DONE (only with FP8MP_OVERLAP_PREVIOUS): the
+ *           kernel running before this one is the backward GEMM launch that
+ *           produces grad_bf16 and signals its completion
+ *           (fp8_linear_bwd_rowmajor_ex with FP8MP_SIGNAL_DW_DONE, on the
+ *           same word as grad_nonfinite). The step then starts beside that
+ *           launch, each block waits (bounded, about 2 s) for bit 30 of
+ *           *grad_nonfinite before it reads the flag and the gradients, and
+ *           reads them through L2. A wait that runs out raises the flag
+ *           fp8mp_check reports (FP8MP_ERR_TIMEOUT) and the step is skipped.
+ *           Other bits: FP8MP_ERR_INVALID.
  * Every other argument and every result as the calls without _ex (w8 there
  * is w8_out here).
  */

@@ -9,8 +9,9 @@ update and the master step, which re-casts the weight's E4M3 copy under the
 just-updated weight scale for the next step. Both schedules are checked: the
 serial one (one-launch backward, update, master step in place) and the
 overlapped one the bench times (update first, keeping the casts' scale_inv
-for the backward; wgrad, dgrad, then the master step beside dgrad writing
-the other of two weight copies). Checked here: every code and every meta
+for the backward; the backward launch signals when dW is stored, and the
+master step, started beside it, waits for that signal and writes the other
+of two weight copies). Checked here: every code and every meta
 bit-exact; every GEMM output within the GEMM tolerance; the master step
 bit-exact on the GPU's own bf16 dW (dW is the master step's input, and its
 rounding is not unique)."""
@@ -93,7 +94,7 @@ class OracleRun:
 def test_bench_step_matches_oracle(cuda_lib, orc, overlap):
     M, K, N = 384, 512, 256  # N <= K: the step takes dY's first N columns
     st = bench.LinearStep(m=M, k=K, n=N, overlap=overlap)
-    assert st.split_bwd == overlap
+    assert st.overlap_master == overlap
     run = OracleRun(orc, st)
     for step in range(3):
         st.step()
@@ -127,7 +128,7 @@ def test_bench_step_skips_on_a_nan_gradient(cuda_lib):
     wgrad epilogue flags it and the master step skips on the flag: master
     weights, momentum and W8 unchanged, S halved, growth reset, flag reset."""
     st = bench.LinearStep(m=256, k=512, n=256)
-    assert st.split_bwd
+    assert st.overlap_master
     st.step()
     assert cuda_lib.fp8mp_check() == 0
     master, mom, w8 = st.master.clone(), st.mom.clone(), st.W8.clone()

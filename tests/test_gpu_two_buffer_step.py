@@ -152,3 +152,51 @@ def test_two_buffer_step_in_place_is_the_plain_step(cuda_lib, orc):
         orc.master_step(gb, hw, hv, h8, 32.0, ham, st, 1e-4, 0.9)
         assert_same_bits(np_view(ds.w), hw, f"step {step} master")
         assert_same_bits(ds.w8[0].cpu().numpy(), h8, f"step {step} copy")  # a skip leaves it as it was
+
+
+@pytest.mark.parametrize("shape", [(384, 256, 512), (2048, 1024, 1024), (0, 256, 512)])
+def test_backward_signals_dw_completion(cuda_lib, shape):
+    """fp8_linear_bwd_rowmajor_ex with FP8MP_SIGNAL_DW_DONE: the same dX and
+    dW as the plain launch, bit 30 of the word set once dW is stored (at once
+    for an empty contraction), bit 0 the overflow flag of the stored dW."""
+    f = cuda_lib
+    M, N, K = shape
+    g = torch.Generator(device="cuda").manual_seed(M + N + K)
+    d8 = (torch.randn(M, N, generator=g, device="cuda") * 8).to(torch.float8_e5m2).view(torch.uint8)
+    w8 = torch.randn(N, K, generator=g, device="cuda").to(torch.float8_e4m3fn).view(torch.uint8)
+    x8 = torch.randn(M, K, generator=g, device="cuda").to(torch.float8_e4m3fn).view(torch.uint8)
+    if M > 0:
+        d8[M // 2, N // 3] = 0x7F  # an E5M2 NaN code: NaN in one dW row
+    one = torch.ones(1, device="cuda")
+    outs = []
+    for flags in (0, f.SIGNAL_DW_DONE):
+        dx = torch.full((M, K), 7.0, dtype=torch.bfloat16, device="cuda")
+        dw = torch.full((N, K), 7.0, dtype=torch.bfloat16, device="cuda")
+        word = torch.zeros(1, dtype=torch.int32, device="cuda")
+        f.fp8_linear_bwd_rowmajor(d8, w8, x8, one, one, one, dx, dw, dw_nonfinite=word, flags=flags)
+        assert f.fp8mp_check() == 0
+        outs.append((dx, dw, int(word.item())))
+    (dx0, dw0, w0), (dx1, dw1, w1) = outs
+    assert torch.equal(dx0.view(torch.int16), dx1.view(torch.int16))
+    assert torch.equal(dw0.view(torch.int16), dw1.view(torch.int16))
+    bad = int(not torch.isfinite(dw0.float()).all())
+    assert w0 == bad
+    assert w1 & (1 << 30) and (w1 & 1) == bad
+    assert (w1 >> 1) & 0x7FFF == 0  # no master step counted in it
+
+
+def test_waiting_master_step_times_out_without_a_signal(cuda_lib):
+    """FP8MP_WAIT_DW_DONE behind a kernel that never signals: each block's
+    bounded wait runs out (about 2 s), fp8mp_check reports the timeout, the
+    step updates nothing and the word is left at 0."""
+    f = cuda_lib
+    n = 4096
+    ds = State(workloads.master_weights(n, seed=9), "sgd")
+    w_before = ds.w.clone()
+    torch.zeros(16, device="cuda").add_(1.0)  # some earlier kernel on the stream
+    ds.step(f, torch.zeros(n, dtype=torch.int16, device="cuda"), ds.w8[0], ds.w8[1],
+            f.OVERLAP_PREVIOUS | f.WAIT_DW_DONE)
+    assert f.fp8mp_check() == f.ERR_TIMEOUT
+    assert torch.equal(ds.w.view(torch.int32), w_before.view(torch.int32))
+    assert ds.flag.item() == 0
+    assert f.fp8mp_check() == 0  # the flag was cleared by the first check

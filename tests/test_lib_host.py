@@ -247,8 +247,11 @@ def test_master_step_ex_rejects_bad_copies_and_flags(lib):
         assert word in fp8mp.last_error(), (i, v, fp8mp.last_error())
     # adam: grad, n, master, m, v, w8_in, w8_out, scale_w, amax_w, S, growth, found, gnf, beta_pows, lr, b1, b2,
     # eps, bo, gf, gi, flags
-    adam = [P, n, P, P, P, 8 * P, 4 * P, P, P, P, P, P, 2 * P, P, 1e-4, 0.9, 0.999, 1e-8, 0.5, 2.0, 2000, 4, None]
+    adam = [P, n, P, P, P, 8 * P, 4 * P, P, P, P, P, P, 2 * P, P, 1e-4, 0.9, 0.999, 1e-8, 0.5, 2.0, 2000, 8, None]
     assert lib.mp_master_step_adam_prescanned_ex(*adam) == fp8mp.ERR_INVALID and "flags" in fp8mp.last_error()
+    adam[21] = fp8mp.WAIT_DW_DONE  # the wait only makes sense beside the producer
+    assert lib.mp_master_step_adam_prescanned_ex(*adam) == fp8mp.ERR_INVALID
+    assert "OVERLAP_PREVIOUS" in fp8mp.last_error()
     adam[21], adam[5] = 1, 4 * P + 16
     assert lib.mp_master_step_adam_prescanned_ex(*adam) == fp8mp.ERR_INVALID and "overlap" in fp8mp.last_error()
 
@@ -281,3 +284,18 @@ def test_binding_routes_the_two_buffer_step(monkeypatch):
     snap = torch.zeros(4, dtype=torch.float32)
     fp8mp.delayed_scaling_update([], fp8mp.AMAX_MAX, 0, stream=0, prev_scale_inv=snap)
     assert calls[-1][0] == "delayed_scaling_update_ex" and calls[-1][1][4] == snap.data_ptr()
+
+
+def test_bwd_rowmajor_ex_rejects_bad_flags(lib):
+    """Unknown flags, and the completion signal without dW or without its
+    overflow word, are refused before any CUDA call."""
+    P = 4096
+    args = [P, P, P, 256, 256, 256, 1, P, P, P, P, 1, 2 * P, 1, 3 * P]
+    assert lib.fp8_linear_bwd_rowmajor_ex(*args, 8, None) == fp8mp.ERR_INVALID and "flags" in fp8mp.last_error()
+    no_word = list(args)
+    no_word[14] = None
+    assert lib.fp8_linear_bwd_rowmajor_ex(*no_word, fp8mp.SIGNAL_DW_DONE, None) == fp8mp.ERR_INVALID
+    assert "dw_nonfinite" in fp8mp.last_error()
+    no_dw = list(args)
+    no_dw[12] = None
+    assert lib.fp8_linear_bwd_rowmajor_ex(*no_dw, fp8mp.SIGNAL_DW_DONE, None) == fp8mp.ERR_INVALID
