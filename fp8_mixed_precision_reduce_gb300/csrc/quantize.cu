@@ -500,7 +500,7 @@ cast_dbias_kernel(const __grid_constant__ CUtensorMap tmap, int64_t rows, int64_
     for (int64_t i = 0; i < ntile; ++i) {
         const int s = static_cast<int>(i % C::STAGES);
         const uint32_t ph = static_cast<uint32_t>(i / C::STAGES) & 1u;
-        // lane 0 waits for the stage; the warp follows its verdict (uniform
+        // lane 0 waits for the stage; the warp follows its result (uniform
         // per warp, so the __syncwarp below is never divergent)
         int okw = 0;
         if (lane == 0) okw = wait_bounded(bar0 + 8u * s, ph, abort_flag, &g_cast_timeout_flag) ? 1 : 0;
