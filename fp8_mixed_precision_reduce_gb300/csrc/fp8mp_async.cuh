@@ -77,6 +77,31 @@ __device__ __forceinline__ void prefetch_tmap(const CUtensorMap *map) {
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
 }
 
+// Thread-block clusters: this CTA's rank, the shared::cluster address of the
+// variable at local shared address `addr` in CTA `rank`, a load through such
+// an address (distributed shared memory), and a barrier over every thread of
+// every CTA of the cluster (release / acquire: the shared-memory writes made
+// before it are seen by the loads made after it, in any CTA of the cluster;
+// all threads of a warp execute it together).
+__device__ __forceinline__ uint32_t cluster_ctarank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+__device__ __forceinline__ uint32_t mapa_shared(uint32_t addr, uint32_t rank) {
+    uint32_t r;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(addr), "r"(rank));
+    return r;
+}
+__device__ __forceinline__ float ld_shared_cluster_f32(uint32_t cluster_addr) {
+    float v;
+    asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(cluster_addr) : "memory");
+    return v;
+}
+__device__ __forceinline__ void cluster_sync_all() {
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
 // The driver's cuTensorMapEncodeTiled, looked up once through the runtime
 // (no link against libcuda); NULL when the driver does not provide it.
 PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder();

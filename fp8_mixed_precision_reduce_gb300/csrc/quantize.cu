@@ -362,6 +362,15 @@ cast_rows_t_kernel(const void *__restrict__ x, int64_t rows, int64_t cols, const
 // the CTA that arrives last on the strip's counter, which writes dbias and
 // sets the k sums and the counter back to zero, so a workspace that is zero
 // before a call is zero after it.
+//
+// CL: the strip's k CTAs are one thread-block cluster (k <= 8, launched only
+// when the device holds all the strips' clusters at once): blocks
+// strip * k .. strip * k + k - 1, CTA j being cluster rank j. Each CTA leaves
+// its column sums in its own shared memory, and after a cluster barrier CTA
+// 0 reads the others' through distributed shared memory and adds them in
+// the same order of j; a second barrier keeps every CTA resident until it
+// has. No workspace, counter, fence or global atomic: the same sums, bit for
+// bit, without the round trips through L2 at the end of the launch.
 constexpr int kTileThreads = 288;       // 8 consumer warps + 1 producer warp
 constexpr int kBoxBytes = 128 * 128;    // one box: 128 rows x 128 bytes
 constexpr int kDbiasTargetCtas = 152;   // the split aims at this many CTAs
@@ -423,7 +432,7 @@ __device__ __forceinline__ uint32_t cast_pairs(uint64_t p0, uint64_t p1, uint64_
     return cvt_pair_raw<FMT>(a, b) | (cvt_pair_raw<FMT>(c, d) << 16);
 }
 
-template <int FMT, bool BF16>
+template <int FMT, bool BF16, bool CL>
 __global__ void __launch_bounds__(kTileThreads, 1)
 cast_dbias_kernel(const __grid_constant__ CUtensorMap tmap, int64_t rows, int64_t cols, int k_per_strip,
                   const float *__restrict__ scale_p, uint8_t *__restrict__ out, uint8_t *__restrict__ out_t,
@@ -444,8 +453,8 @@ cast_dbias_kernel(const __grid_constant__ CUtensorMap tmap, int64_t rows, int64_
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int64_t tiles_r = (rows + 127) >> 7, tiles_c = (cols + 127) >> 7;
-    const int64_t strip = blockIdx.x % tiles_c;
-    const int64_t j = blockIdx.x / tiles_c;
+    const int64_t strip = CL ? blockIdx.x / k_per_strip : blockIdx.x % tiles_c;
+    const int64_t j = CL ? blockIdx.x % k_per_strip : blockIdx.x / tiles_c;
     const int64_t c0 = strip * 128;
     const int64_t ntile = j < tiles_r ? (tiles_r - 1 - j) / k_per_strip + 1 : 0;
 
@@ -483,6 +492,14 @@ cast_dbias_kernel(const __grid_constant__ CUtensorMap tmap, int64_t rows, int64_
                 for (int64_t q = i - 1; q >= 0 && q >= i - C::STAGES; --q)
                     wait_bounded(bar0 + 8u * static_cast<uint32_t>(q % C::STAGES),
                                  static_cast<uint32_t>(q / C::STAGES) & 1u, &never, &g_cast_timeout_flag);
+            }
+        }
+        if constexpr (CL) {
+            // the producer warp takes part in the cluster's two barriers too
+            __syncwarp();
+            if (k_per_strip > 1) {
+                cluster_sync_all();
+                cluster_sync_all();
             }
         }
         return;
@@ -621,6 +638,37 @@ cast_dbias_kernel(const __grid_constant__ CUtensorMap tmap, int64_t rows, int64_
         for (int w = 1; w < 8; ++w) t = fmaxf(t, s_red[w]);
         atomicMax(reinterpret_cast<int *>(amax_p), __float_as_int(t));
     }
+    if constexpr (CL) {
+        // the CTA's column sums in its shared memory (the transpose tile is
+        // free: every tile's reads of it ended before the last consumer_sync)
+        float *s_col = reinterpret_cast<float *>(sT);
+        if (threadIdx.x < 128) {
+            float t = s_part[threadIdx.x];
+#pragma unroll
+            for (int w = 1; w < 8; ++w) t = __fadd_rn(t, s_part[w * 128 + threadIdx.x]);
+            s_col[threadIdx.x] = t;
+        }
+        __syncwarp();
+        if (k_per_strip > 1) cluster_sync_all();  // every CTA's sums are written
+        if (j == 0 && threadIdx.x < 128 && c0 + threadIdx.x < cols) {
+            const uint32_t a = smem_u32(s_col + threadIdx.x);
+            float v[8];
+#pragma unroll
+            for (int r = 1; r < 8; ++r) v[r] = r < k_per_strip ? ld_shared_cluster_f32(mapa_shared(a, r)) : 0.0f;
+            float t = s_col[threadIdx.x];
+#pragma unroll
+            for (int r = 1; r < 8; ++r)
+                if (r < k_per_strip) t = __fadd_rn(t, v[r]);
+            const int64_t col = c0 + threadIdx.x;
+            if (dbias_bf16)
+                static_cast<__nv_bfloat16 *>(dbias)[col] = __float2bfloat16_rn(t);
+            else
+                static_cast<float *>(dbias)[col] = t;
+        }
+        __syncwarp();
+        if (k_per_strip > 1) cluster_sync_all();  // CTA 0 has read them: the others may leave
+        return;
+    }
     if (threadIdx.x < 128) {
         const int64_t col = c0 + threadIdx.x;
         if (col < cols) {
@@ -672,19 +720,32 @@ int launch_typed(const void *x, int64_t rows, int64_t cols, const float *scale, 
 
 // The bias-gradient cast's launch: tensor map of x (boxes of 128 rows x 128
 // bytes, 128-byte swizzle, zero fill outside the tensor), k CTAs per strip.
+// The CL kernel runs when k = 1 (nothing to combine) and, without a
+// transposed copy, as clusters of k when 2 <= k <= 8 and the device holds
+// every strip's cluster at once (asked of the occupancy calculator once per
+// device and k); else the workspace kernel. At 8192 x 4096 bf16 the
+// clusters took 20.3-20.8 us against 21.3 without the transposed copy, but
+// 26.7-27.1 against 25.3-25.6 with it (presumably because a cluster's CTAs
+// must share one GPC, so 32 clusters of 4 load some GPCs with more busy SMs
+// than the 128 CTAs spread one per SM do, which costs the launch that moves
+// 4 B/elem more than the round trips it saves).
 template <int FMT, bool BF16>
 int launch_dbias_typed(const void *x, int64_t rows, int64_t cols, const float *scale, uint8_t *out,
                        uint8_t *out_t, float *amax, void *dbias, int dbias_bf16, float *ws, cudaStream_t s,
                        const DeviceInfo &dev) {
     using C = TileCfg<BF16>;
     static std::atomic<bool> ready[64];
+    static std::atomic<int> max_clusters[64][9];  // 0: not asked yet, else 1 + the answer
     static std::mutex m;
     if (dev.device < 0 || dev.device >= 64) return fail(FP8MP_ERR_DEVICE, "device index %d out of range", dev.device);
     if (!ready[dev.device].load(std::memory_order_acquire)) {
         std::lock_guard<std::mutex> lock(m);
         if (!ready[dev.device].load(std::memory_order_relaxed)) {
-            const cudaError_t e = cudaFuncSetAttribute(cast_dbias_kernel<FMT, BF16>,
-                                                       cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
+            cudaError_t e = cudaFuncSetAttribute(cast_dbias_kernel<FMT, BF16, false>,
+                                                 cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
+            if (e == cudaSuccess)
+                e = cudaFuncSetAttribute(cast_dbias_kernel<FMT, BF16, true>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
             if (e != cudaSuccess)
                 return fail(FP8MP_ERR_LAUNCH, "fp8_quantize_dbias: shared-memory attribute: %s", cudaGetErrorString(e));
             ready[dev.device].store(true, std::memory_order_release);
@@ -704,12 +765,45 @@ int launch_dbias_typed(const void *x, int64_t rows, int64_t cols, const float *s
     if (r != CUDA_SUCCESS)
         return fail(FP8MP_ERR_LAUNCH, "fp8_quantize_dbias: cuTensorMapEncodeTiled failed (%d)", static_cast<int>(r));
     const int k = dbias_ctas_per_strip(rows, cols);
-    const int64_t grid = k * ((cols + 127) >> 7);
+    const int64_t strips = (cols + 127) >> 7;
+    const int64_t grid = k * strips;
     if (grid > 0x7FFFFFFF) return fail(FP8MP_ERR_INVALID, "fp8_quantize_dbias: tensor too large");
-    uint32_t *counters = reinterpret_cast<uint32_t *>(ws + static_cast<int64_t>(k) * cols);
-    launch_kernel(cast_dbias_kernel<FMT, BF16>, dim3(static_cast<unsigned>(grid)), dim3(kTileThreads), C::SMEM_BYTES,
-                  s, tmap, rows, cols, k, scale, out, out_t, amax, ws, counters, dbias, dbias_bf16);
-    const cudaError_t e = cudaGetLastError();
+    bool cl = k == 1;
+    if (out_t == nullptr && k >= 2 && k <= 8) {
+        int n = max_clusters[dev.device][k].load(std::memory_order_relaxed) - 1;
+        if (n < 0) {
+            cudaLaunchConfig_t cfg = {};
+            cudaLaunchAttribute attr[1];
+            cfg.gridDim = dim3(static_cast<unsigned>(k * ((dev.num_sms + k - 1) / k)));
+            cfg.blockDim = dim3(kTileThreads);
+            cfg.dynamicSmemBytes = C::SMEM_BYTES;
+            attr[0].id = cudaLaunchAttributeClusterDimension;
+            attr[0].val.clusterDim.x = static_cast<unsigned>(k);
+            attr[0].val.clusterDim.y = 1;
+            attr[0].val.clusterDim.z = 1;
+            cfg.attrs = attr;
+            cfg.numAttrs = 1;
+            if (cudaOccupancyMaxActiveClusters(&n, cast_dbias_kernel<FMT, BF16, true>, &cfg) != cudaSuccess) {
+                (void)cudaGetLastError();  // an unanswered query only means the workspace kernel
+                n = 0;
+            }
+            max_clusters[dev.device][k].store(n + 1, std::memory_order_relaxed);
+        }
+        cl = n >= strips;
+    }
+    cudaError_t e;
+    if (cl) {
+        e = launch_kernel_cluster(cast_dbias_kernel<FMT, BF16, true>, dim3(static_cast<unsigned>(grid)),
+                                  dim3(kTileThreads), C::SMEM_BYTES, s, static_cast<unsigned>(k), tmap, rows, cols,
+                                  k, scale, out, out_t, amax, ws, static_cast<uint32_t *>(nullptr), dbias,
+                                  dbias_bf16);
+    } else {
+        uint32_t *counters = reinterpret_cast<uint32_t *>(ws + static_cast<int64_t>(k) * cols);
+        e = launch_kernel(cast_dbias_kernel<FMT, BF16, false>, dim3(static_cast<unsigned>(grid)),
+                          dim3(kTileThreads), C::SMEM_BYTES, s, tmap, rows, cols, k, scale, out, out_t, amax, ws,
+                          counters, dbias, dbias_bf16);
+    }
+    if (e == cudaSuccess) e = cudaGetLastError();
     if (e != cudaSuccess) return fail(FP8MP_ERR_LAUNCH, "fp8_quantize_dbias: launch failed: %s", cudaGetErrorString(e));
     return FP8MP_OK;
 }

@@ -171,6 +171,60 @@ def test_dbias_leaves_its_workspace_zero_across_shapes(cuda_lib, orc):
         dbias_check(np_view(db), ref, ab, rows, False)
 
 
+def dbias_in_documented_order(x):
+    """The bias gradient summed in the order the library documents for its
+    fused cast, restated in numpy fp32 (each addition one IEEE round to
+    nearest): k = max(1, min(tile rows, 152 // strips)) CTAs per 128-column
+    strip, CTA j taking tile rows j, j + k, ...; per column, 32 running sums
+    of 4-row runs (thread row ty adds rows 4ty .. 4ty + 3 of each of its
+    tiles, tile after tile); the four runs of a warp combined pairwise (ty ^ 1,
+    then ty ^ 2); the 8 warps in order; then the k CTA sums in order of j."""
+    rows, cols = x.shape
+    tr, tc = -(-rows // 128), -(-cols // 128)
+    k = max(1, min(tr, 152 // tc))
+    xp = np.zeros((tr * 128, tc * 128), np.float32)
+    xp[:rows, :cols] = x
+    ctas = []
+    for j in range(k):
+        s = np.zeros((32, tc * 128), np.float32)
+        for t in range(j, tr, k):
+            blk = xp[t * 128:(t + 1) * 128].reshape(32, 4, -1)
+            for rr in range(4):
+                s = s + blk[:, rr, :]
+        s = s.reshape(8, 4, -1)
+        w = (s[:, 0] + s[:, 1]) + (s[:, 2] + s[:, 3])
+        t_sum = w[0]
+        for ww in range(1, 8):
+            t_sum = t_sum + w[ww]
+        ctas.append(t_sum)
+    tot = ctas[0]
+    for j in range(1, k):
+        tot = tot + ctas[j]
+    return tot[:cols], k
+
+
+@pytest.mark.parametrize("with_t", [False, True])
+@pytest.mark.parametrize("rows,cols", [(8192, 4096), (144, 272), (1040, 784), (4112, 16), (16, 4096), (2064, 1552)])
+def test_dbias_follows_its_documented_order(cuda_lib, rows, cols, with_t):
+    """Bit for bit the fp32 sums of the documented order, whichever way the
+    launch combined the CTAs of a strip (without a transposed copy and for
+    2 <= k <= 8 a cluster reading its CTAs' sums from distributed shared
+    memory, else the workspace and the strip's last arriver; nothing to
+    combine at k = 1)."""
+    g = workloads.gen(11 * rows + cols)
+    dy = (torch.randn((rows, cols), generator=g) * 1e-2 + 1e-3).to(torch.bfloat16)
+    want, k = dbias_in_documented_order(np_view(dy.float()))
+    ws = torch.zeros(cuda_lib.fp8_quantize_dbias_workspace_bytes(rows, cols) // 4, dtype=torch.float32,
+                     device="cuda")
+    out = torch.empty((rows, cols), dtype=torch.uint8, device="cuda")
+    out_t = torch.empty((cols, rows), dtype=torch.uint8, device="cuda") if with_t else None
+    db = torch.empty(cols, dtype=torch.float32, device="cuda")
+    cuda_lib.fp8_quantize_dbias(dy.cuda(), E5M2, torch.ones(1, device="cuda"), out, out_t, db, ws)
+    assert cuda_lib.fp8mp_check() == 0
+    assert int(torch.count_nonzero(ws)) == 0
+    assert_same_bits(np_view(db), want, f"dbias, k={k}")
+
+
 def test_dbias_rejects_small_workspace(cuda_lib):
     dy = torch.ones((256, 64), dtype=torch.bfloat16, device="cuda")
     out = torch.empty((256, 64), dtype=torch.uint8, device="cuda")
