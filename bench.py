@@ -860,7 +860,8 @@ def kernel_table(args):
     """--kernels: every kernel of the path on its own, at the sizes of the
     other workloads (the transformer block's and the MLP's GEMM shapes and
     casts, the master step on 1e9 parameters), each against its roofline:
-    median device time of one launch with L2 flushed before it (3 warm-up
+    device time of one launch (the mean of the middle 80 % of the timed
+    launches) with L2 flushed before it (3 warm-up
     launches; the flush's own dirty lines are written back before the
     launch), one JSON line per measurement, the clocks last. Inputs are
     seeded and synthetic. cuBLASLt's FP8 GEMMs (torch._scaled_mm, E4M3/E5M2
@@ -896,7 +897,13 @@ def kernel_table(args):
                 ts.append(a.elapsed_time(b) * 1e3)
         if fp8mp.fp8mp_check() != 0:
             raise RuntimeError("a kernel's bounded wait ran out")
-        return statistics.median(ts)
+        # the mean of the middle 80 %: the event durations of a ~20 us launch
+        # cluster at a few values about 1 us apart, so their median jumps
+        # between those values; the trimmed mean resolves finer and still
+        # drops the outliers
+        ts.sort()
+        cut = len(ts) // 10
+        return statistics.mean(ts[cut:len(ts) - cut])
 
     def emit(kernel, workload, us, work, bound, **extra):
         if bound == "tensor":
