@@ -197,6 +197,11 @@ int fp8_quantize_current(const void *x, int32_t x_dtype, int64_t rows, int64_t c
  * One launch: each CTA writes its column sums to the workspace and counts
  * itself in a per-strip word there; the last CTA of a strip to finish adds
  * the strip's sums, writes dbias, and sets the words it used back to zero.
+ * Without a transposed copy, when 2 <= k <= 8 and the device holds every
+ * strip's k CTAs as one thread-block cluster at once, CTA 0 of each strip
+ * reads the others' sums from their shared memory instead (the same sums,
+ * bit for bit; the workspace is not touched); at k = 1 a CTA writes dbias
+ * itself.
  * workspace  device scratch of at least fp8_quantize_dbias_workspace_bytes
  *            (rows, cols) bytes, 16-byte aligned, owned by the caller. It
  *            must be ZERO-FILLED before its first use (e.g. cudaMemset or
