@@ -97,7 +97,8 @@ struct Cfg {
 struct GemmParams {
     int rows_a, rows_b, num_kb;
     int tiles_m, tiles_n;
-    int group_m;              // tile raster: row-blocks per group
+    int group_m;              // tile raster: row-blocks per group, or
+    int group_n;              //   when group_n > 0, column-blocks per group
     int a_mn, b_mn;           // operand stored MN-major ([kc x rows], contiguous along M / N)
     uint32_t idesc;           // tcgen05 instruction descriptor (operand formats, majors, M, N)
     const float *sinv_a, *sinv_b;
@@ -319,8 +320,22 @@ __device__ __forceinline__ int tile_problem(const GemmBatch &b, int t, int &loca
 }
 
 // Tile index -> (row-block of A, row-block of B), grouped so that the CTAs
-// working at the same time share group_m A panels and a few B panels in L2.
-__device__ __forceinline__ void tile_coords(int t, int tiles_m, int tiles_n, int group_m, int &mb, int &nb) {
+// working at the same time share group_m A panels and a few B panels in L2
+// (row-block fastest within a group); with group_n > 0 the other way round:
+// groups of group_n B panels, column-block fastest, every A panel streamed
+// past them once per group.
+__device__ __forceinline__ void tile_coords(int t, int tiles_m, int tiles_n, int group_m, int group_n, int &mb,
+                                            int &nb) {
+    if (group_n > 0) {
+        const int group = group_n * tiles_m;
+        const int g = t / group;
+        const int first = g * group_n;
+        const int gn = min(tiles_n - first, group_n);
+        const int local = t - g * group;
+        nb = first + local % gn;
+        mb = local / gn;
+        return;
+    }
     const int group = group_m * tiles_n;
     const int g = t / group;
     const int first = g * group_m;
@@ -433,7 +448,7 @@ gemm_fp8_kernel(const __grid_constant__ GemmBatch batch) {
                 int local;
                 const GemmProblem &P = batch.prob[tile_problem(batch, tile, local)];
                 int mb, nb;
-                tile_coords(local, P.p.tiles_m, P.p.tiles_n, P.p.group_m, mb, nb);
+                tile_coords(local, P.p.tiles_m, P.p.tiles_n, P.p.group_m, P.p.group_n, mb, nb);
                 const int a_row = mb * C::TILE_M + static_cast<int>(rank) * ROWS_A;
                 const int b_row = nb * TILE_N + static_cast<int>(rank) * C::ROWS_B;
                 const int num_kb = P.p.num_kb;
@@ -568,7 +583,7 @@ gemm_fp8_kernel(const __grid_constant__ GemmBatch batch) {
             const int bias_bf16 = P.p.bias_bf16;
             const int rows_a = P.p.rows_a, rows_b = P.p.rows_b;
             int mb, nb;
-            tile_coords(local, P.p.tiles_m, P.p.tiles_n, P.p.group_m, mb, nb);
+            tile_coords(local, P.p.tiles_m, P.p.tiles_n, P.p.group_m, P.p.group_n, mb, nb);
             const int64_t m = static_cast<int64_t>(mb) * C::TILE_M + row_in_tile;
             const bool row_ok = m < rows_a;
             const int warp_row0 = mb * C::TILE_M + static_cast<int>(rank) * ROWS_A + q * 32;
@@ -819,6 +834,23 @@ int raster_group(int64_t kc, int tile_m) {
     return static_cast<int>(g);
 }
 
+// Which way to group the raster of a problem whose operands do not fit in
+// L2 together (more than 64 MB): the DRAM bytes each order needs when the
+// group's panels stay in L2 and the other operand streams past them are
+// about A + ceil(tiles_m / gm) * B (row-block groups, B read once per
+// group) and B + ceil(tiles_n / gn) * A (column-block groups); the order
+// with fewer is taken. Returns group_n, 0 for row-block groups. The MLP's
+// backward GEMMs and its down projection's forward stream their 235 MB
+// operand twice instead of re-reading the 59-67 MB one 7-8 times.
+int raster_columns(int64_t rows_a, int64_t rows_b, int64_t kc, int tiles_m, int tiles_n, int gm) {
+    const int64_t a = rows_a * kc, b = rows_b * kc;
+    if (a + b <= (64ll << 20)) return 0;
+    const int gn = raster_group(kc, TILE_N);
+    const int64_t by_rows = a + ((tiles_m + gm - 1) / gm) * b;
+    const int64_t by_cols = b + ((tiles_n + gn - 1) / gn) * a;
+    return by_cols < by_rows ? gn : 0;
+}
+
 constexpr uint32_t make_idesc(int fmt_a, int fmt_b, int m, int a_mn, int b_mn) {
     return (1u << 4)                                    // accumulator: f32
            | (static_cast<uint32_t>(fmt_a) << 7)        // A: 0 = E4M3, 1 = E5M2
@@ -974,6 +1006,7 @@ int launch_gemms(const GemmDesc *descs, int n, cudaStream_t s, const DeviceInfo 
         p.tiles_n = static_cast<int>((d.rows_b + TILE_N - 1) / TILE_N);
         p.tiles_m = static_cast<int>(pair ? (d.rows_a + 255) / 256 : (d.rows_a + 127) / 128);
         p.group_m = raster_group(d.kc, pair ? 256 : 128);
+        p.group_n = raster_columns(d.rows_a, d.rows_b, d.kc, p.tiles_m, p.tiles_n, p.group_m);
         p.a_mn = d.a_mn;
         p.b_mn = d.b_mn;
         p.idesc = make_idesc(d.fmt_a, d.fmt_b, pair ? 256 : 128, d.a_mn, d.b_mn);
