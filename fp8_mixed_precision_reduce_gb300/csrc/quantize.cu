@@ -888,11 +888,11 @@ current_cast_kernel(const void *__restrict__ x, int64_t n, int margin, float *__
     const uint4 *x4 = reinterpret_cast<const uint4 *>(x);
     const uint64_t pol = l2_evict_last_policy();
     float am = 0.0f;
-    // ---- phase 1: amax, two chunks' loads in flight per thread
-    for (int64_t c = t0; c < nchunk; c += 2 * stride) {
-        uint4 v[2][V];
+    // ---- phase 1: amax, four chunks' loads in flight per thread
+    for (int64_t c = t0; c < nchunk; c += 4 * stride) {
+        uint4 v[4][V];
 #pragma unroll
-        for (int u = 0; u < 2; ++u) {
+        for (int u = 0; u < 4; ++u) {
             const int64_t cc = c + u * stride;
             if (cc < nchunk) {
 #pragma unroll
@@ -903,7 +903,7 @@ current_cast_kernel(const void *__restrict__ x, int64_t n, int margin, float *__
             }
         }
 #pragma unroll
-        for (int u = 0; u < 2; ++u) {
+        for (int u = 0; u < 4; ++u) {
 #pragma unroll
             for (int k = 0; k < V; ++k) {
                 const uint32_t w[4] = {v[u][k].x, v[u][k].y, v[u][k].z, v[u][k].w};
@@ -1028,11 +1028,15 @@ int launch_current_fused(const void *x, int64_t n, int margin, float *scale, flo
     cfg.gridDim = dim3(static_cast<unsigned>(blocks));
     cfg.blockDim = dim3(kThreads);
     cfg.stream = s;
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeCooperative;  // every block resident: the grid barrier cannot wait forever
     attr[0].val.cooperative = 1;
+    // and launched like the library's other kernels: its blocks wait in
+    // griddepcontrol.wait, before the grid barrier, for the zeroing kernel
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = pdl_enabled() ? 2 : 1;
     e = cudaLaunchKernelEx(&cfg, current_cast_kernel<FMT, BF16>, x, n, margin, scale, scale_inv, amax, out);
     if (e == cudaErrorCooperativeLaunchTooLarge) {
         cudaGetLastError();  // not sticky: the grid did not fit at once; the caller takes the three-pass path
