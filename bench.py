@@ -10,20 +10,23 @@ through the library's entry points on one CUDA stream:
   fp8_quantize_ex(dY -> dY8, amax,               E5M2, row-major only; dY is an
                   FP8MP_OVERLAP_PREVIOUS)        input of the step, so its cast runs
                                                  beside the forward GEMM
-  delayed_scaling_update_ex(x, w, y, dy metas    L = 1024, most_recent; keeps the
-                            -> prev scale_inv)   scale_inv factors the casts used
   fp8_linear_bwd_rowmajor_ex(dY8, W8, X8          dgrad and wgrad GEMMs in one launch
       -> dX bf16, dW bf16; SIGNAL_DW_DONE)       from the row-major copies, wgrad
                                                  tiles first; the epilogue flags an
                                                  Inf/NaN in the stored dW and signals
                                                  when dW is complete
-  mp_master_step_prescanned_ex(dW -> master,     SGD-momentum, loss scale 2^16,
-      momentum, next W8; OVERLAP_PREVIOUS        started beside the backward launch,
-      | WAIT_DW_DONE)                            waits for that signal; skip decided
-                                                 by the flag; re-casts the weight
-                                                 under the updated scale into the
-                                                 other of two W8 buffers while dgrad
-                                                 still reads this step's
+  mp_master_step_prescanned_scaling_ex(dW ->     SGD-momentum, loss scale 2^16,
+      master, momentum, next W8; x, w, y, dy     started beside the backward launch;
+      metas; OVERLAP_PREVIOUS | WAIT_DW_DONE)    its blocks first run the delayed-
+                                                 scaling update of the four metas
+                                                 (L = 1024, most_recent; the new
+                                                 scale_inv written once the backward
+                                                 launch, which reads the old ones, is
+                                                 complete), then wait for that signal;
+                                                 skip decided by the flag; re-casts the
+                                                 weight under the updated scale into
+                                                 the other of two W8 buffers while
+                                                 dgrad still reads this step's
 The weight's first E4M3 copy is cast once before the first step; from then
 on each step's master step writes the next step's W8 (and records the amax
 of the new master weights for the next scale update), so the weight is cast
@@ -299,12 +302,12 @@ class LinearStep:
     tiles of the one-launch backward. For the latter the backward launch runs
     its wgrad tiles first and signals in dW's overflow word when dW is
     stored; the master step, started beside it, waits for that signal. The
-    delayed-scaling update moves before the backward (keeping the scale_inv
-    factors this step's casts used, which the backward GEMMs take), and the
-    weight's E4M3 copy is double buffered: dgrad reads the current copy while
-    the master step writes the next one. Every result is bitwise that of the
-    serial order. Without it: the backward, the update, the master step in
-    place."""
+    master step also runs the delayed-scaling update of the four metas while
+    it waits (writing the new scale_inv factors only once the backward
+    launch, which reads the old ones, has completed), and the weight's E4M3
+    copy is double buffered: dgrad reads the current copy while the master
+    step writes the next one. Every result is bitwise that of the serial
+    order. Without it: the backward, the update, the master step in place."""
 
     def __init__(self, m=M_TOK, k=K_IN, n=N_OUT, seed=3, prescanned=True, overlap=True):
         import torch
@@ -335,8 +338,6 @@ class LinearStep:
         self.S = torch.tensor([S0], dtype=torch.float32, device=dev)
         self.growth = torch.zeros(1, dtype=torch.int32, device=dev)
         self.found = torch.zeros(1, dtype=torch.int32, device=dev)
-        # scale_inv of x, w, y, dY as this step's casts used them (kept by the update)
-        self.snap = torch.zeros(4, dtype=torch.float32, device=dev)
         # dW's overflow flag: set by the wgrad epilogue, read and reset by the
         # master step (with prescanned=False the master step scans dW itself)
         self.prescanned = prescanned
@@ -348,8 +349,10 @@ class LinearStep:
         fp8mp.fp8_quantize(self.master, E4, self.mw.scale, self.W8, None, self.mw.cur_amax)
         # 2 casts, the fwd GEMM, the fused dgrad + wgrad GEMM, the update, and the master step: one kernel
         # on the epilogue's flag (scanning dW itself: a 4-byte memset and one kernel, or three kernels with
-        # FP8MP_FUSED_MASTER=0)
+        # FP8MP_FUSED_MASTER=0); overlapped, the update runs inside the master step
         self.launches_per_step = 6 if prescanned or os.environ.get("FP8MP_FUSED_MASTER", "1") != "0" else 8
+        if self.overlap_master:
+            self.launches_per_step = 5
 
     @property
     def W8(self):
@@ -390,20 +393,21 @@ class LinearStep:
             f.mp_master_step(self.dw, self.master, self.mom, W8, self.mw.scale, self.mw.cur_amax, self.S,
                              self.growth, self.found, LR, MU, grad_nonfinite=self.gnf if self.prescanned else None)
             return
-        f.delayed_scaling_update(metas, f.AMAX_MOST_RECENT, 0, prev_scale_inv=self.snap)
-        sx, sw, sd = self.snap[0:1], self.snap[1:2], self.snap[3:4]
         if ev is not None:
             ev[2].record()
         # wgrad tiles first; dW's word gets its completion bit while dgrad runs
-        f.fp8_linear_bwd_rowmajor(self.D8, W8, self.X8, sd, sw, sx, dx, self.dw, dw_nonfinite=self.gnf,
-                                  flags=f.SIGNAL_DW_DONE)
+        f.fp8_linear_bwd_rowmajor(self.D8, W8, self.X8, self.md.scale_inv, self.mw.scale_inv, self.mx.scale_inv,
+                                  dx, self.dw, dw_nonfinite=self.gnf, flags=f.SIGNAL_DW_DONE)
         if ev is not None:
             ev[3].record()
         nxt = self.cur ^ 1
-        # the next copy, written beside the backward launch (which still reads this one)
+        # the next copy, written beside the backward launch (which still reads
+        # this one), and the metas' update, whose new scale_inv factors are
+        # written once that launch has completed
         f.mp_master_step(self.dw, self.master, self.mom, self.W8s[nxt], self.mw.scale, self.mw.cur_amax, self.S,
                          self.growth, self.found, LR, MU, grad_nonfinite=self.gnf, w8_in=W8,
-                         flags=f.OVERLAP_PREVIOUS | f.WAIT_DW_DONE)
+                         flags=f.OVERLAP_PREVIOUS | f.WAIT_DW_DONE, metas=metas, amax_algo=f.AMAX_MOST_RECENT,
+                         margin=0)
         self.cur = nxt
 
 
@@ -689,8 +693,8 @@ def run_ours(args, world, rank, local):
                    "dy_cast": "plain, after the forward GEMM" if args.no_overlap
                    else "enqueued after the forward GEMM with FP8MP_OVERLAP_PREVIOUS: runs beside it",
                    "backward": ("dgrad + wgrad in one launch (wgrad tiles first, FP8MP_SIGNAL_DW_DONE), the master "
-                                "step beside it (FP8MP_OVERLAP_PREVIOUS | FP8MP_WAIT_DW_DONE); scale update before "
-                                "the backward, weight copy double-buffered")
+                                "step beside it (FP8MP_OVERLAP_PREVIOUS | FP8MP_WAIT_DW_DONE) running the scale update "
+                                "of the four metas too, weight copy double-buffered")
                    if st.overlap_master else "dgrad + wgrad in one launch, the scale update, the master step"},
         "gemm_only": {"tflops": round(world * fl / (gemm_step_ms * 1e-3) / 1e12, 2), "ms_per_step": round(gemm_step_ms, 5),
                       "fwd_ms": round(fwd_ms, 5), "bwd_ms": round(bwd_ms, 5),

@@ -90,6 +90,11 @@ def load(path: str | None = None):
     L.mp_master_step_prescanned_ex.argtypes = [P, I64, P, P, P, P, P, P, P, P, P, P, F, F, F, F, I32, U32, P]
     L.mp_master_step_adam_prescanned_ex.argtypes = [P, I64, P, P, P, P, P, P, P, P, P, P, P, P, F, F, F, F, F, F,
                                                     I32, U32, P]
+    M = ctypes.POINTER(fp8mp_meta)
+    L.mp_master_step_prescanned_scaling_ex.argtypes = [P, I64, P, P, P, P, P, P, P, P, P, P, F, F, F, F, I32,
+                                                       M, I32, I32, I32, U32, P]
+    L.mp_master_step_adam_prescanned_scaling_ex.argtypes = [P, I64, P, P, P, P, P, P, P, P, P, P, P, P, F, F, F,
+                                                            F, F, F, I32, M, I32, I32, I32, U32, P]
     L.fp8mp_check.argtypes = [P]
     L.fp8mp_selftest_timeout.argtypes = [P]
     L.fp8mp_selftest_barrier_timeout.argtypes = [P]
@@ -332,15 +337,30 @@ def mp_master_step(grad_bf16: torch.Tensor, master: torch.Tensor, momentum: torc
                    loss_scale: torch.Tensor, growth_tracker: torch.Tensor, found_inf: torch.Tensor,
                    lr: float, momentum_coef: float, backoff: float = 0.5, growth_factor: float = 2.0,
                    growth_interval: int = 2000, stream=None, grad_nonfinite: torch.Tensor | None = None,
-                   w8_in: torch.Tensor | None = None, flags: int = 0) -> None:
+                   w8_in: torch.Tensor | None = None, flags: int = 0, metas=None, amax_algo: int = AMAX_MOST_RECENT,
+                   margin: int = 0) -> None:
     """Unscale, overflow skip, FP32 SGD-momentum update and E4M3 re-cast, in place.
     With grad_nonfinite (int32[1] on the device holding 0 or 1, set by the
     gradients' producer, e.g. fp8_linear_bwd_rowmajor's dw_nonfinite) the step
     reads that flag instead of scanning the gradients, writes it to found_inf
     and resets it to 0. With it, w8_in (the current E4M3 copy; the new one goes
     to w8, which a skipped step fills with w8_in) and flags
-    (OVERLAP_PREVIOUS) select mp_master_step_prescanned_ex."""
+    (OVERLAP_PREVIOUS) select mp_master_step_prescanned_ex; metas (with
+    amax_algo, margin; flags OVERLAP_PREVIOUS | WAIT_DW_DONE) select
+    mp_master_step_prescanned_scaling_ex, which also runs the metas'
+    delayed-scaling update."""
     n = grad_bf16.numel()
+    if metas is not None:
+        if grad_nonfinite is None:
+            raise Fp8mpError(ERR_INVALID, "metas need grad_nonfinite (the prescanned step)")
+        metas = list(metas)
+        arr = (fp8mp_meta * max(1, len(metas)))(*[m.c_struct() for m in metas])
+        _check(load().mp_master_step_prescanned_scaling_ex(
+            _ptr(grad_bf16), n, _ptr(master), _ptr(momentum), _ptr(w8_in), _ptr(w8), _ptr(scale_w), _ptr(amax_w),
+            _ptr(loss_scale), _ptr(growth_tracker), _ptr(found_inf), _ptr(grad_nonfinite), float(lr),
+            float(momentum_coef), float(backoff), float(growth_factor), int(growth_interval), arr, len(metas),
+            int(amax_algo), int(margin), int(flags), _stream(stream)))
+        return
     if w8_in is not None or flags:
         if grad_nonfinite is None:
             raise Fp8mpError(ERR_INVALID, "w8_in and flags need grad_nonfinite (the prescanned step)")
@@ -369,10 +389,23 @@ def mp_master_step_adam(grad_bf16: torch.Tensor, master: torch.Tensor, exp_avg: 
                         beta_pows: torch.Tensor, lr: float, beta1: float = 0.9, beta2: float = 0.999,
                         eps: float = 1e-8, backoff: float = 0.5, growth_factor: float = 2.0,
                         growth_interval: int = 2000, stream=None, grad_nonfinite: torch.Tensor | None = None,
-                        w8_in: torch.Tensor | None = None, flags: int = 0) -> None:
+                        w8_in: torch.Tensor | None = None, flags: int = 0, metas=None, amax_algo: int = AMAX_MOST_RECENT,
+                        margin: int = 0) -> None:
     """Unscale, overflow skip, FP32 Adam update and E4M3 re-cast, in place
-    (grad_nonfinite, w8_in, flags: as mp_master_step)."""
+    (grad_nonfinite, w8_in, flags, metas, amax_algo, margin: as mp_master_step)."""
     n = grad_bf16.numel()
+    if metas is not None:
+        if grad_nonfinite is None:
+            raise Fp8mpError(ERR_INVALID, "metas need grad_nonfinite (the prescanned step)")
+        metas = list(metas)
+        arr = (fp8mp_meta * max(1, len(metas)))(*[m.c_struct() for m in metas])
+        _check(load().mp_master_step_adam_prescanned_scaling_ex(
+            _ptr(grad_bf16), n, _ptr(master), _ptr(exp_avg), _ptr(exp_avg_sq), _ptr(w8_in), _ptr(w8),
+            _ptr(scale_w), _ptr(amax_w), _ptr(loss_scale), _ptr(growth_tracker), _ptr(found_inf),
+            _ptr(grad_nonfinite), _ptr(beta_pows), float(lr), float(beta1), float(beta2), float(eps),
+            float(backoff), float(growth_factor), int(growth_interval), arr, len(metas), int(amax_algo),
+            int(margin), int(flags), _stream(stream)))
+        return
     if w8_in is not None or flags:
         if grad_nonfinite is None:
             raise Fp8mpError(ERR_INVALID, "w8_in and flags need grad_nonfinite (the prescanned step)")

@@ -534,12 +534,46 @@ static int check_w8_pair(const char *fn, const uint8_t *w8_in, const uint8_t *w8
     return FP8MP_OK;
 }
 
+// The metas of a master step that also runs the step's delayed-scaling
+// update (the _scaling_ex entries): validated as delayed_scaling_update
+// validates them, at most kMaxFoldMetas, the weight's meta found by its
+// scale pointer (it must then also hold amax_w); the step must start beside
+// the backward launch and wait for its dW signal.
+static int build_fold(const char *fn, const fp8mp_meta *metas, int32_t n_metas, int32_t algo, int32_t margin,
+                      const float *scale_w, const float *amax_w, uint32_t flags, FoldBatch *fb) {
+    std::memset(fb, 0, sizeof *fb);
+    fb->w_index = -1;
+    REQUIRE(n_metas >= 0 && n_metas <= kMaxFoldMetas, "%s: n_metas = %d outside 0..%d", fn, n_metas, kMaxFoldMetas);
+    REQUIRE(n_metas == 0 || metas != nullptr, "%s: metas is NULL", fn);
+    REQUIRE(algo == FP8MP_AMAX_MAX || algo == FP8MP_AMAX_MOST_RECENT, "%s: algo %d invalid", fn, algo);
+    REQUIRE(margin >= 0 && margin <= 126, "%s: margin %d outside 0..126", fn, margin);
+    REQUIRE(flags == (FP8MP_OVERLAP_PREVIOUS | FP8MP_WAIT_DW_DONE),
+            "%s: flags must be FP8MP_OVERLAP_PREVIOUS | FP8MP_WAIT_DW_DONE", fn);
+    for (int32_t i = 0; i < n_metas; ++i) {
+        const fp8mp_meta &m = metas[i];
+        REQUIRE(m.history_len >= 1 && m.history_len <= FP8MP_MAX_HISTORY, "%s: meta %d history_len %d outside 1..%d",
+                fn, i, m.history_len, FP8MP_MAX_HISTORY);
+        REQUIRE(valid_fmt(m.fmt), "%s: meta %d fmt %d invalid", fn, i, m.fmt);
+        REQUIRE(m.amax_history && m.scale && m.scale_inv && m.cur_amax, "%s: meta %d has a NULL pointer", fn, i);
+        if (m.scale == scale_w) {
+            REQUIRE(fb->w_index < 0, "%s: two metas hold scale_w", fn);
+            REQUIRE(m.cur_amax == amax_w, "%s: the meta holding scale_w must hold amax_w as its cur_amax", fn);
+            fb->w_index = i;
+        }
+        fb->m[i] = FoldMeta{m.amax_history, m.scale, m.scale_inv, m.cur_amax, m.history_len, m.fmt};
+    }
+    fb->n = n_metas;
+    fb->algo = algo;
+    fb->margin = margin;
+    return FP8MP_OK;
+}
+
 static int master_step_entry(const char *fn, const uint16_t *grad_bf16, int64_t n, float *master,
                              float *momentum, uint8_t *w8, const float *scale_w, float *amax_w, float *loss_scale,
                              int32_t *growth_tracker, int32_t *found_inf, int32_t *grad_nonfinite, bool prescanned,
                              float lr, float momentum_coef, float backoff, float growth_factor,
                              int32_t growth_interval, void *stream, const uint8_t *w8_in = nullptr,
-                             uint32_t flags = 0u) {
+                             uint32_t flags = 0u, const FoldBatch *fold = nullptr) {
     clear_error();
     REQUIRE(n >= 0 && n <= (1ll << 40), "%s: n = %lld out of range", fn, (long long)n);
     REQUIRE(growth_interval >= 1, "%s: growth_interval must be >= 1", fn);
@@ -564,7 +598,7 @@ static int master_step_entry(const char *fn, const uint16_t *grad_bf16, int64_t 
     return launch_master_step(grad_bf16, n, master, momentum, w8, scale_w, amax_w, loss_scale, growth_tracker,
                               found_inf, lr, momentum_coef, backoff, growth_factor, growth_interval,
                               static_cast<cudaStream_t>(stream), dev, grad_nonfinite, w8_in,
-                              (flags & FP8MP_OVERLAP_PREVIOUS) != 0u, (flags & FP8MP_WAIT_DW_DONE) != 0u);
+                              (flags & FP8MP_OVERLAP_PREVIOUS) != 0u, (flags & FP8MP_WAIT_DW_DONE) != 0u, fold);
 }
 
 int mp_master_step(const uint16_t *grad_bf16, int64_t n, float *master, float *momentum, uint8_t *w8,
@@ -590,7 +624,7 @@ static int adam_step_entry(const char *fn, const uint16_t *grad_bf16, int64_t n,
                            int32_t *growth_tracker, int32_t *found_inf, int32_t *grad_nonfinite, bool prescanned,
                            float *beta_pows, float lr, float beta1, float beta2, float eps, float backoff,
                            float growth_factor, int32_t growth_interval, void *stream,
-                           const uint8_t *w8_in = nullptr, uint32_t flags = 0u) {
+                           const uint8_t *w8_in = nullptr, uint32_t flags = 0u, const FoldBatch *fold = nullptr) {
     clear_error();
     REQUIRE(n >= 0 && n <= (1ll << 40), "%s: n = %lld out of range", fn, (long long)n);
     REQUIRE(growth_interval >= 1, "%s: growth_interval must be >= 1", fn);
@@ -618,7 +652,7 @@ static int adam_step_entry(const char *fn, const uint16_t *grad_bf16, int64_t n,
     return launch_adam_step(grad_bf16, n, master, exp_avg, exp_avg_sq, w8, scale_w, amax_w, loss_scale,
                             growth_tracker, found_inf, beta_pows, lr, beta1, beta2, eps, backoff, growth_factor,
                             growth_interval, static_cast<cudaStream_t>(stream), dev, grad_nonfinite, w8_in,
-                            (flags & FP8MP_OVERLAP_PREVIOUS) != 0u, (flags & FP8MP_WAIT_DW_DONE) != 0u);
+                            (flags & FP8MP_OVERLAP_PREVIOUS) != 0u, (flags & FP8MP_WAIT_DW_DONE) != 0u, fold);
 }
 
 int mp_master_step_adam(const uint16_t *grad_bf16, int64_t n, float *master, float *exp_avg, float *exp_avg_sq,
@@ -660,6 +694,41 @@ int mp_master_step_adam_prescanned_ex(const uint16_t *grad_bf16, int64_t n, floa
     return adam_step_entry("mp_master_step_adam_prescanned_ex", grad_bf16, n, master, exp_avg, exp_avg_sq, w8_out,
                            scale_w, amax_w, loss_scale, growth_tracker, found_inf, grad_nonfinite, true, beta_pows,
                            lr, beta1, beta2, eps, backoff, growth_factor, growth_interval, stream, w8_in, flags);
+}
+
+int mp_master_step_prescanned_scaling_ex(const uint16_t *grad_bf16, int64_t n, float *master, float *momentum,
+                                         const uint8_t *w8_in, uint8_t *w8_out, const float *scale_w,
+                                         float *amax_w, float *loss_scale, int32_t *growth_tracker,
+                                         int32_t *found_inf, int32_t *grad_nonfinite, float lr, float momentum_coef,
+                                         float backoff, float growth_factor, int32_t growth_interval,
+                                         const fp8mp_meta *metas, int32_t n_metas, int32_t amax_algo,
+                                         int32_t margin, uint32_t flags, void *stream) {
+    const char *fn = "mp_master_step_prescanned_scaling_ex";
+    clear_error();
+    FoldBatch fb;
+    const int rc = build_fold(fn, metas, n_metas, amax_algo, margin, scale_w, amax_w, flags, &fb);
+    if (rc) return rc;
+    return master_step_entry(fn, grad_bf16, n, master, momentum, w8_out, scale_w, amax_w, loss_scale, growth_tracker,
+                             found_inf, grad_nonfinite, true, lr, momentum_coef, backoff, growth_factor,
+                             growth_interval, stream, w8_in, flags, &fb);
+}
+
+int mp_master_step_adam_prescanned_scaling_ex(const uint16_t *grad_bf16, int64_t n, float *master, float *exp_avg,
+                                              float *exp_avg_sq, const uint8_t *w8_in, uint8_t *w8_out,
+                                              const float *scale_w, float *amax_w, float *loss_scale,
+                                              int32_t *growth_tracker, int32_t *found_inf, int32_t *grad_nonfinite,
+                                              float *beta_pows, float lr, float beta1, float beta2, float eps,
+                                              float backoff, float growth_factor, int32_t growth_interval,
+                                              const fp8mp_meta *metas, int32_t n_metas, int32_t amax_algo,
+                                              int32_t margin, uint32_t flags, void *stream) {
+    const char *fn = "mp_master_step_adam_prescanned_scaling_ex";
+    clear_error();
+    FoldBatch fb;
+    const int rc = build_fold(fn, metas, n_metas, amax_algo, margin, scale_w, amax_w, flags, &fb);
+    if (rc) return rc;
+    return adam_step_entry(fn, grad_bf16, n, master, exp_avg, exp_avg_sq, w8_out, scale_w, amax_w, loss_scale,
+                           growth_tracker, found_inf, grad_nonfinite, true, beta_pows, lr, beta1, beta2, eps, backoff,
+                           growth_factor, growth_interval, stream, w8_in, flags, &fb);
 }
 
 int fp8mp_selftest_timeout(void *stream) {

@@ -127,10 +127,27 @@ struct GemmDesc {
 // the prescanned master step's grad_nonfinite), bit by bit: bit 0 the
 // Inf/NaN flag; bits 1-15 the master step's block arrivals (2 each); bits
 // 16-29 the GEMM's stored tile parts when it signals completion; bit 30 set
-// once every part is stored. The prescanned master step resets it to 0.
+// once every part is stored; bit 31 set by the master step that runs the
+// delayed-scaling update as well, once the weight's new scale is written.
+// The prescanned master step resets it to 0.
 constexpr uint32_t kArrivalShift = 1, kArrivalMask = 0x7FFFu;
 constexpr uint32_t kPartShift = 16, kPartMask = 0x3FFFu;
 constexpr uint32_t kDoneBit = 1u << 30;
+constexpr uint32_t kMetaBit = 1u << 31;
+
+// The delayed-scaling update of up to kMaxFoldMetas tensors run by the
+// blocks of a master step (mp_master_step_prescanned_scaling_ex): the
+// metas' arrays, which of them is the weight's (its new scale is the one the
+// step casts with; -1 if none), the recipe's algorithm and margin.
+constexpr int kMaxFoldMetas = 8;
+struct FoldMeta {
+    float *hist, *scale, *scale_inv, *cur_amax;
+    int32_t len, fmt;
+};
+struct FoldBatch {
+    FoldMeta m[kMaxFoldMetas];
+    int32_t n, w_index, algo, margin;
+};
 // One-thread kernel that ORs kDoneBit into the word.
 cudaError_t launch_signal_done(int32_t *word, cudaStream_t s);
 // Runs 1 or 2 independent GEMMs in one persistent launch.
@@ -159,13 +176,13 @@ int launch_master_step(const uint16_t *g, int64_t n, float *w, float *v, uint8_t
                        int32_t *found_inf, float lr, float mu, float backoff, float growth_factor,
                        int32_t growth_interval, cudaStream_t s, const DeviceInfo &dev,
                        int32_t *grad_nonfinite = nullptr, const uint8_t *w8_in = nullptr, bool early = false,
-                       bool wait_done = false);
+                       bool wait_done = false, const FoldBatch *fold = nullptr);
 int launch_adam_step(const uint16_t *g, int64_t n, float *w, float *m, float *v, uint8_t *w8, const float *scale_w,
                      float *amax_w, float *loss_scale, int32_t *growth, int32_t *found_inf, float *beta_pows,
                      float lr, float b1, float b2, float eps, float backoff, float growth_factor,
                      int32_t growth_interval, cudaStream_t s, const DeviceInfo &dev,
                      int32_t *grad_nonfinite = nullptr, const uint8_t *w8_in = nullptr, bool early = false,
-                     bool wait_done = false);
+                     bool wait_done = false, const FoldBatch *fold = nullptr);
 // Enqueues the one-thread kernel whose bounded wait is meant to run out.
 int launch_timeout_selftest(cudaStream_t s);
 // Reads and clears the GEMM wait-timeout flag (after a stream sync).

@@ -411,20 +411,90 @@ __global__ void __launch_bounds__(kThreads) fused_step_kernel(const StepCommon c
 // one more block): every block runs from the start, so the whole update
 // overlaps the GEMM instead of the few blocks that find room first.
 //
+// One tensor's delayed-scaling update by a whole block, as
+// scale_update_kernel computes it (roll the history one place, newest at
+// index 0; the max of the new window, or the newest amax with the
+// most-recent algorithm; the scale from it), without staging the history in
+// shared memory, of which a block beside a GEMM CTA has almost none: the
+// history moves one place towards its end in chunks of blockDim elements,
+// the highest chunk first, every old value of a chunk read before any of the
+// chunk is written (a block barrier between), so nothing is overwritten
+// before it is read. Returns the new scale in thread 0.
+__device__ float fold_meta_update(const FoldMeta &m, int algo, int margin, float *red) {
+    const int L = m.len;
+    const int T = static_cast<int>(blockDim.x);
+    const float cur = __ldcg(m.cur_amax);
+    float mx = 0.0f;
+    for (int base = ((L - 1) / T) * T; base >= 0; base -= T) {
+        const int j = base + static_cast<int>(threadIdx.x);
+        float v = 0.0f;
+        if (j < L) v = (j == 0) ? cur : __ldcg(m.hist + j - 1);
+        __syncthreads();
+        if (j < L) {
+            m.hist[j] = v;
+            mx = max_ignore_nan(mx, v);
+        }
+    }
+    mx = warp_max(mx);
+    if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = mx;
+    __syncthreads();
+    float sc = 0.0f;
+    if (threadIdx.x == 0) {
+        float all = 0.0f;
+        for (int w = 0; w < T / 32; ++w) all = fmaxf(all, red[w]);
+        const float a = (algo == FP8MP_AMAX_MAX) ? all : cur;
+        sc = scale_from_amax(a, __ldcg(m.scale), m.fmt, margin);
+    }
+    return sc;
+}
+
 // WAIT (with EARLY; FP8MP_WAIT_DW_DONE): the gradients' producer is the
 // kernel still running (a backward GEMM launch that signals completion, its
 // dW tiles first): thread 0 of each block waits, bounded by about 2 s, for
 // the word's completion bit before the flag is read, and the gradients are
 // read through L2 only. A wait that runs out raises the device timeout flag
 // and the block updates nothing.
-template <class Opt, class Args, class Extra, bool EARLY, bool WAIT>
+//
+// FOLD (with EARLY and WAIT; mp_master_step_prescanned_scaling_ex): the
+// blocks also run the step's delayed-scaling update of fb's metas, block b
+// the metas b, b + gridDim.x, ..., before they wait for the gradients: each
+// history rolled and each new scale and zeroed amax written at once, the
+// weight's scale followed by bit 31 of the word, which every block waits
+// for too before it casts with that scale (and adds to the weight's amax,
+// zeroed just before). The new scale_inv values, which the still running
+// backward GEMMs read in their old form, are written only after the block's
+// griddepcontrol.wait at its end. Every result is that of the update
+// launched before the backward with the scale_inv snapshot.
+template <class Opt, class Args, class Extra, bool EARLY, bool WAIT, bool FOLD>
 __global__ void __launch_bounds__(EARLY ? kEarlyMaxThreads : kThreads, EARLY ? 1 : 0)
-prescanned_step_kernel(const StepCommon c, const Args a, const Extra x, int32_t *grad_nonfinite) {
+prescanned_step_kernel(const StepCommon c, const Args a, const Extra x, int32_t *grad_nonfinite,
+                       const __grid_constant__ FoldBatch fb) {
     if constexpr (!EARLY) {
         pdl_wait();
         pdl_launch_dependents();
     }
     __shared__ int s_skip;
+    __shared__ float s_sinv[kMaxFoldMetas];  // FOLD: the new scale_inv of the metas this block updated
+    if constexpr (FOLD) {
+        __shared__ float s_red[32];
+#pragma unroll 1
+        for (int k = 0; k < kMaxFoldMetas; ++k) {
+            const int mi = static_cast<int>(blockIdx.x) + k * static_cast<int>(gridDim.x);
+            if (mi >= fb.n) break;
+            const FoldMeta &m = fb.m[mi];
+            const float sc = fold_meta_update(m, fb.algo, fb.margin, s_red);
+            if (threadIdx.x == 0) {
+                *m.scale = sc;
+                *m.cur_amax = 0.0f;
+                s_sinv[k] = __fdiv_rn(1.0f, sc);
+                if (mi == fb.w_index) {
+                    __threadfence();  // the scale and the zeroed amax before the bit
+                    atomicOr(reinterpret_cast<unsigned int *>(grad_nonfinite), kMetaBit);
+                }
+            }
+            __syncthreads();  // s_red is free for the next meta
+        }
+    }
     if (threadIdx.x == 0) {
         if constexpr (WAIT) {
             const long long t0 = clock64();
@@ -432,7 +502,7 @@ prescanned_step_kernel(const StepCommon c, const Args a, const Extra x, int32_t 
             int skip = 1;
             for (;;) {
                 asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(w) : "l"(grad_nonfinite) : "memory");
-                if (w & kDoneBit) {
+                if ((w & kDoneBit) && (!FOLD || fb.w_index < 0 || (w & kMetaBit))) {
                     skip = (w & 1u) != 0;
                     break;
                 }
@@ -451,7 +521,7 @@ prescanned_step_kernel(const StepCommon c, const Args a, const Extra x, int32_t 
     float am = 0.0f;
     if (!s_skip) {
         const Opt opt = make_opt(a, __fdiv_rn(1.0f, *c.loss_scale));
-        am = update_share<Opt, WAIT>(opt, c.g, c.n, c.w8, *c.scale_w);
+        am = update_share<Opt, WAIT>(opt, c.g, c.n, c.w8, FOLD ? __ldcg(c.scale_w) : *c.scale_w);
     } else if (c.w8_in != nullptr && c.w8_in != c.w8) {
         copy_share(c.w8_in, c.w8, c.n);  // skipped: the next copy is the current one
     }
@@ -466,6 +536,16 @@ prescanned_step_kernel(const StepCommon c, const Args a, const Extra x, int32_t 
             loss_scale_update(c.loss_scale, c.growth, found, c.backoff, c.growth_factor, c.interval);
             *c.found_inf = found;
             *grad_nonfinite = 0;
+        }
+    }
+    if constexpr (FOLD) {
+        if (threadIdx.x == 0 && static_cast<int>(blockIdx.x) < fb.n) {
+            pdl_wait();  // the backward launch, which reads the old scale_inv, is complete
+            for (int k = 0; k < kMaxFoldMetas; ++k) {
+                const int mi = static_cast<int>(blockIdx.x) + k * static_cast<int>(gridDim.x);
+                if (mi >= fb.n) break;
+                *fb.m[mi].scale_inv = s_sinv[k];
+            }
         }
     }
     if constexpr (EARLY) {  // the next kernel may start once this wait has returned (as for the casts)
@@ -506,15 +586,16 @@ FusedGrid g_fused[64];
 // GEMM warps it holds (at most ceil(warps / 4)), over the registers of one
 // warp of this kernel (allocated 8 per thread at a time), times four.
 // Queried once per optimizer.
-std::atomic<int> g_early_threads[2];
+std::atomic<int> g_early_threads[4];  // [which + 2 * FOLD]
 
-template <class Opt, class Args, class Extra>
+template <class Opt, class Args, class Extra, bool FOLD>
 int early_block_threads(int which, const DeviceInfo &dev) {
+    which += FOLD ? 2 : 0;
     int t = g_early_threads[which].load(std::memory_order_relaxed);
     if (t >= 32) return t;
     cudaFuncAttributes fa;
     int file = 0;
-    if (cudaFuncGetAttributes(&fa, prescanned_step_kernel<Opt, Args, Extra, true, true>) != cudaSuccess ||
+    if (cudaFuncGetAttributes(&fa, prescanned_step_kernel<Opt, Args, Extra, true, true, FOLD>) != cudaSuccess ||
         cudaDeviceGetAttribute(&file, cudaDevAttrMaxRegistersPerMultiprocessor, dev.device) != cudaSuccess)
         return 0;
     int gemm_warps = 0;
@@ -532,7 +613,11 @@ int early_block_threads(int which, const DeviceInfo &dev) {
 
 template <class Opt, class Args, class Extra>
 int launch_step(const StepCommon &c, const Args &a, const Extra &x, int which, cudaStream_t s, const DeviceInfo &dev,
-                const char *fn, int32_t *grad_nonfinite = nullptr, bool early = false, bool wait_done = false) {
+                const char *fn, int32_t *grad_nonfinite = nullptr, bool early = false, bool wait_done = false,
+                const FoldBatch *fold = nullptr) {
+    FoldBatch none;
+    std::memset(&none, 0, sizeof none);
+    none.w_index = -1;
     cudaError_t e = cudaSuccess;
     if (grad_nonfinite == nullptr) {  // the scanning steps count arrivals in found_inf: zero it
         e = launch_zero_word(c.found_inf, s);
@@ -548,19 +633,28 @@ int launch_step(const StepCommon &c, const Args &a, const Extra &x, int which, c
         const int64_t cap = static_cast<int64_t>(dev.num_sms) * 32;
         if (blocks > cap) blocks = cap;
         if (early) {
-            const int threads = early_block_threads<Opt, Args, Extra>(which, dev);
+            const bool folded = fold != nullptr && wait_done;
+            const int threads = folded ? early_block_threads<Opt, Args, Extra, true>(which, dev)
+                                       : early_block_threads<Opt, Args, Extra, false>(which, dev);
             if (threads < 32) return fail(FP8MP_ERR_LAUNCH, "%s: kernel attribute query failed", fn);
             int64_t eb = (nvec + threads - 1) / threads;
             eb = eb < 1 ? 1 : (eb > dev.num_sms ? dev.num_sms : eb);
-            if (wait_done)
-                e = launch_kernel(prescanned_step_kernel<Opt, Args, Extra, true, true>,
-                                  dim3(static_cast<unsigned>(eb)), dim3(threads), 0, s, c, a, x, grad_nonfinite);
+            if (folded)
+                e = launch_kernel(prescanned_step_kernel<Opt, Args, Extra, true, true, true>,
+                                  dim3(static_cast<unsigned>(eb)), dim3(threads), 0, s, c, a, x, grad_nonfinite,
+                                  *fold);
+            else if (wait_done)
+                e = launch_kernel(prescanned_step_kernel<Opt, Args, Extra, true, true, false>,
+                                  dim3(static_cast<unsigned>(eb)), dim3(threads), 0, s, c, a, x, grad_nonfinite,
+                                  none);
             else
-                e = launch_kernel(prescanned_step_kernel<Opt, Args, Extra, true, false>,
-                                  dim3(static_cast<unsigned>(eb)), dim3(threads), 0, s, c, a, x, grad_nonfinite);
+                e = launch_kernel(prescanned_step_kernel<Opt, Args, Extra, true, false, false>,
+                                  dim3(static_cast<unsigned>(eb)), dim3(threads), 0, s, c, a, x, grad_nonfinite,
+                                  none);
         } else {
-            e = launch_kernel(prescanned_step_kernel<Opt, Args, Extra, false, false>,
-                              dim3(static_cast<unsigned>(blocks)), dim3(kThreads), 0, s, c, a, x, grad_nonfinite);
+            e = launch_kernel(prescanned_step_kernel<Opt, Args, Extra, false, false, false>,
+                              dim3(static_cast<unsigned>(blocks)), dim3(kThreads), 0, s, c, a, x, grad_nonfinite,
+                              none);
         }
         if (e != cudaSuccess) return fail(FP8MP_ERR_LAUNCH, "%s: launch failed: %s", fn, cudaGetErrorString(e));
         return FP8MP_OK;
@@ -609,27 +703,27 @@ int launch_adam_step(const uint16_t *g, int64_t n, float *w, float *m, float *v,
                      float *amax_w, float *loss_scale, int32_t *growth, int32_t *found_inf, float *beta_pows,
                      float lr, float b1, float b2, float eps, float backoff, float growth_factor,
                      int32_t growth_interval, cudaStream_t s, const DeviceInfo &dev, int32_t *grad_nonfinite,
-                     const uint8_t *w8_in, bool early, bool wait_done) {
+                     const uint8_t *w8_in, bool early, bool wait_done, const FoldBatch *fold) {
     const StepCommon c = {g, n, w8, w8_in, scale_w, amax_w, loss_scale, growth, found_inf, backoff, growth_factor,
                           growth_interval};
     const AdamArgs a = {w, m, v, beta_pows, lr, b1, b2, eps};
     const AdamExtra x = {beta_pows, b1, b2};
     return launch_step<AdamOpt>(c, a, x, 1, s, dev, grad_nonfinite ? "mp_master_step_adam_prescanned"
                                                                    : "mp_master_step_adam",
-                                grad_nonfinite, early, wait_done);
+                                grad_nonfinite, early, wait_done, fold);
 }
 
 int launch_master_step(const uint16_t *g, int64_t n, float *w, float *v, uint8_t *w8, const float *scale_w,
                        float *amax_w, float *loss_scale, int32_t *growth, int32_t *found_inf, float lr, float mu,
                        float backoff, float growth_factor, int32_t growth_interval, cudaStream_t s,
                        const DeviceInfo &dev, int32_t *grad_nonfinite, const uint8_t *w8_in, bool early,
-                       bool wait_done) {
+                       bool wait_done, const FoldBatch *fold) {
     const StepCommon c = {g, n, w8, w8_in, scale_w, amax_w, loss_scale, growth, found_inf, backoff, growth_factor,
                           growth_interval};
     const SgdArgs a = {w, v, lr, mu};
     return launch_step<SgdOpt>(c, a, NoExtra{}, 0, s, dev,
                                grad_nonfinite ? "mp_master_step_prescanned" : "mp_master_step", grad_nonfinite,
-                               early, wait_done);
+                               early, wait_done, fold);
 }
 
 int launch_barrier_selftest(cudaStream_t s) {

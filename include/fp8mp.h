@@ -570,6 +570,48 @@ int mp_master_step_adam_prescanned_ex(const uint16_t *grad_bf16, int64_t n, floa
                                       float growth_factor, int32_t growth_interval, uint32_t flags, void *stream);
 
 /*
+ * mp_master_step_prescanned_scaling_ex, mp_master_step_adam_prescanned_scaling_ex
+ * -- the _ex steps that also run the step's delayed-scaling update of up to
+ * 8 tensors, as delayed_scaling_update does it ([TE-FP8] "Scaling factor
+ * 선택 전략" and "FP8 사용방안(recipe)"; [H100-Q] section 3), so that the
+ * update needs no launch of its own in the training step: the step's blocks
+ * run it while they wait for the backward launch's dW signal.
+ *   metas, n_metas   0..8 metas (NULL when 0), amax_algo and margin as for
+ *                    delayed_scaling_update. The meta whose scale is scale_w
+ *                    (if any) is the weight's: it must have amax_w as its
+ *                    cur_amax, and the step casts the new weight copy with
+ *                    its NEW scale (the update's), then adds the new copy's
+ *                    amax to the zeroed cur_amax -- as delayed_scaling_update
+ *                    followed by the _ex step would.
+ *   flags            must be FP8MP_OVERLAP_PREVIOUS | FP8MP_WAIT_DW_DONE
+ *                    (the step starts beside the backward launch that signals
+ *                    dW's completion).
+ * Histories, scales and cur_amax are written as the step starts; each
+ * meta's scale_inv keeps its old value until the backward launch the step
+ * started beside has completed, so that launch may read the metas' scale_inv
+ * (the step's factors, as the snapshot of delayed_scaling_update_ex gives
+ * them) while the update runs. Results equal, bit for bit, those of
+ * delayed_scaling_update_ex enqueued before the backward launch followed by
+ * the _ex step. Every other argument as the _ex calls; FP8MP_ERR_INVALID for
+ * a bad meta, a bad count, two metas holding scale_w, or other flags.
+ */
+int mp_master_step_prescanned_scaling_ex(const uint16_t *grad_bf16, int64_t n, float *master, float *momentum,
+                                         const uint8_t *w8_in, uint8_t *w8_out, const float *scale_w,
+                                         float *amax_w, float *loss_scale, int32_t *growth_tracker,
+                                         int32_t *found_inf, int32_t *grad_nonfinite, float lr, float momentum_coef,
+                                         float backoff, float growth_factor, int32_t growth_interval,
+                                         const fp8mp_meta *metas, int32_t n_metas, int32_t amax_algo,
+                                         int32_t margin, uint32_t flags, void *stream);
+int mp_master_step_adam_prescanned_scaling_ex(const uint16_t *grad_bf16, int64_t n, float *master, float *exp_avg,
+                                              float *exp_avg_sq, const uint8_t *w8_in, uint8_t *w8_out,
+                                              const float *scale_w, float *amax_w, float *loss_scale,
+                                              int32_t *growth_tracker, int32_t *found_inf, int32_t *grad_nonfinite,
+                                              float *beta_pows, float lr, float beta1, float beta2, float eps,
+                                              float backoff, float growth_factor, int32_t growth_interval,
+                                              const fp8mp_meta *metas, int32_t n_metas, int32_t amax_algo,
+                                              int32_t margin, uint32_t flags, void *stream);
+
+/*
  * fp8mp_check -- synchronises `stream`, then reports and clears the device
  * flags a kernel sets when one of its bounded waits runs out (a GEMM's
  * mbarrier wait, the master step's grid barrier): FP8MP_ERR_TIMEOUT if one

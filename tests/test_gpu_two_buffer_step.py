@@ -200,3 +200,109 @@ def test_waiting_master_step_times_out_without_a_signal(cuda_lib):
     assert torch.equal(ds.w.view(torch.int32), w_before.view(torch.int32))
     assert ds.flag.item() == 0
     assert f.fp8mp_check() == 0  # the flag was cleared by the first check
+
+
+DONE_BIT = 1 << 30
+
+
+def make_metas(f, lens, fmts, seed):
+    g = torch.Generator(device="cuda").manual_seed(seed)
+    ms = []
+    for L, fm in zip(lens, fmts):
+        m = f.Meta(L, fm)
+        m.amax_history.copy_(torch.rand(L, generator=g, device="cuda") * 100.0)
+        m.scale.copy_(torch.rand(1, generator=g, device="cuda") * 8.0 + 0.5)
+        m.scale_inv.copy_(1.0 / m.scale)
+        m.cur_amax.copy_(torch.rand(1, generator=g, device="cuda") * 50.0)
+        ms.append(m)
+    return ms
+
+
+def clone_metas(f, ms):
+    out = []
+    for m in ms:
+        c = f.Meta(m.amax_history.numel(), m.fmt)
+        for name in ("amax_history", "scale", "scale_inv", "cur_amax"):
+            getattr(c, name).copy_(getattr(m, name))
+        out.append(c)
+    return out
+
+
+@pytest.mark.parametrize("opt", ["sgd", "adam"])
+@pytest.mark.parametrize("n,lens,w_at,skip", [
+    (1 << 20, (1024, 1024, 1024, 1024), 1, False),   # the bench step's four metas, the weight's second
+    (1 << 20, (1024, 1024, 1024, 1024), 1, True),    # a skipped step still updates the metas
+    (4096, (1, 3, 8192, 513, 7, 1024, 2, 600), 5, False),  # one block runs all eight metas
+    (9, (5,), -1, False),                            # no weight meta: the step casts with scale_w as it is
+    ((1 << 20) + 3, (), -1, False),                  # no metas: the _ex step
+])
+def test_folded_update_is_the_separate_update_then_the_step(cuda_lib, opt, n, lens, w_at, skip):
+    """mp_master_step_prescanned_scaling_ex (and its Adam form) against
+    delayed_scaling_update_ex followed by the _ex step on copies of the same
+    state, both behind a word that already holds the completion bit: every
+    history, scale, scale_inv and cur_amax, the master weights and moments,
+    the new E4M3 copy, the loss scale, growth counter and found_inf agree bit
+    for bit, and the word is back at 0."""
+    f = cuda_lib
+    fmts = tuple(E5M2 if i % 4 == 3 else E4M3 for i in range(len(lens)))
+    w = workloads.master_weights(n, seed=n + 5)
+    g = workloads.master_step(n, 1, seed=n + 5, inject=skip, inject_frac=1e-3).cuda()
+    bad = int(((np_view(g.cpu()) & 0x7F80) == 0x7F80).any())
+    assert bad == int(skip)
+    runs = []
+    for fold in (False, True):
+        ds = State(w, opt)
+        metas = make_metas(f, lens, fmts, seed=17)
+        if w_at >= 0:  # the weight's meta holds the step's scale_w and amax_w
+            ds.scale_w = metas[w_at].scale
+            ds.amax_w = metas[w_at].cur_amax
+        ds.flag.fill_(DONE_BIT | bad)
+        flags = f.OVERLAP_PREVIOUS | f.WAIT_DW_DONE
+        if fold:
+            if opt == "sgd":
+                f.mp_master_step(g, ds.w, ds.v, ds.w8[1], ds.scale_w, ds.amax_w, ds.S, ds.growth, ds.found, 1e-4,
+                                 0.9, grad_nonfinite=ds.flag, w8_in=ds.w8[0], flags=flags, metas=metas,
+                                 amax_algo=f.AMAX_MAX, margin=1)
+            else:
+                f.mp_master_step_adam(g, ds.w, ds.m, ds.v, ds.w8[1], ds.scale_w, ds.amax_w, ds.S, ds.growth,
+                                      ds.found, ds.bp, lr=1e-3, grad_nonfinite=ds.flag, w8_in=ds.w8[0], flags=flags,
+                                      metas=metas, amax_algo=f.AMAX_MAX, margin=1)
+        else:
+            if metas:
+                snap = torch.zeros(len(metas), device="cuda")
+                f.delayed_scaling_update(metas, f.AMAX_MAX, 1, prev_scale_inv=snap)
+            ds.step(f, g, ds.w8[0], ds.w8[1], flags)
+        assert f.fp8mp_check() == 0, f.last_error()
+        runs.append((ds, metas))
+    (a, ma), (b, mb) = runs
+    for name in ("w", "v", "m", "bp", "S", "growth", "found", "amax_w", "flag"):
+        assert_same_bits(np_view(getattr(b, name)), np_view(getattr(a, name)), name)
+    assert int(b.flag.item()) == 0 and int(b.found.item()) == int(skip)
+    assert torch.equal(b.w8[1], a.w8[1]) and torch.equal(b.w8[0], a.w8[0])
+    for i, (x, y) in enumerate(zip(mb, ma)):
+        for name in ("amax_history", "scale", "scale_inv", "cur_amax"):
+            assert_same_bits(np_view(getattr(x, name)), np_view(getattr(y, name)), f"meta {i} {name}")
+
+
+def test_folded_update_validation(cuda_lib):
+    f = cuda_lib
+    ds = State(workloads.master_weights(64, seed=1), "sgd")
+    g = torch.zeros(64, dtype=torch.bfloat16, device="cuda")
+    metas = make_metas(f, (4, 4), (E4M3, E4M3), seed=3)
+    both = f.OVERLAP_PREVIOUS | f.WAIT_DW_DONE
+
+    def call(ms, flags, scale_w=None, amax_w=None):
+        f.mp_master_step(g, ds.w, ds.v, ds.w8[1], ds.scale_w if scale_w is None else scale_w,
+                         ds.amax_w if amax_w is None else amax_w, ds.S, ds.growth, ds.found, 1e-4, 0.9,
+                         grad_nonfinite=ds.flag, w8_in=ds.w8[0], flags=flags, metas=ms)
+
+    with pytest.raises(cuda_lib.Fp8mpError, match="flags must be"):
+        call(metas, f.OVERLAP_PREVIOUS)
+    with pytest.raises(cuda_lib.Fp8mpError, match="n_metas"):
+        call(make_metas(f, (2,) * 9, (E4M3,) * 9, seed=4), both)
+    with pytest.raises(cuda_lib.Fp8mpError, match="must hold amax_w"):
+        call(metas, both, scale_w=metas[0].scale)
+    twin = make_metas(f, (4,), (E4M3,), seed=5)[0]
+    twin.scale = metas[0].scale
+    with pytest.raises(cuda_lib.Fp8mpError, match="two metas"):
+        call([metas[0], twin], both, scale_w=metas[0].scale, amax_w=metas[0].cur_amax)

@@ -299,3 +299,73 @@ def test_bwd_rowmajor_ex_rejects_bad_flags(lib):
     no_dw = list(args)
     no_dw[12] = None
     assert lib.fp8_linear_bwd_rowmajor_ex(*no_dw, fp8mp.SIGNAL_DW_DONE, None) == fp8mp.ERR_INVALID
+
+
+def test_scaling_master_step_validation(lib):
+    """mp_master_step_prescanned_scaling_ex and its Adam form refuse, before
+    any CUDA call: other flags than OVERLAP_PREVIOUS | WAIT_DW_DONE, more than
+    8 metas, a bad meta, a weight meta (the one holding scale_w) whose
+    cur_amax is not amax_w, and two metas holding scale_w."""
+    P = 4096  # fake aligned addresses, never dereferenced: validation fails first
+    both = fp8mp.OVERLAP_PREVIOUS | fp8mp.WAIT_DW_DONE
+    scale_w, amax_w = 64 * P, 65 * P
+
+    def metas(*specs):
+        arr = (fp8mp.fp8mp_meta * max(1, len(specs)))()
+        for i, (scale, amax, L) in enumerate(specs):
+            arr[i] = fp8mp.fp8mp_meta(P * (100 + 8 * i), scale, P * (102 + 8 * i), amax, L, fp8mp.E4M3)
+        return arr
+
+    def sgd(arr, n_metas, flags=both, algo=fp8mp.AMAX_MOST_RECENT, margin=0):
+        return lib.mp_master_step_prescanned_scaling_ex(P, 64, P, P, 8 * P, 4 * P, scale_w, amax_w, P, P, 9 * P,
+                                                        10 * P, 1e-4, 0.9, 0.5, 2.0, 2000, arr, n_metas, algo,
+                                                        margin, flags, None)
+
+    ok = metas((P * 200, P * 201, 16), (scale_w, amax_w, 16))
+    cases = [
+        (lambda: sgd(ok, 2, flags=fp8mp.OVERLAP_PREVIOUS), "flags must be"),
+        (lambda: sgd(ok, 9), "n_metas"),
+        (lambda: sgd(ok, 2, algo=5), "algo"),
+        (lambda: sgd(ok, 2, margin=200), "margin"),
+        (lambda: sgd(metas((P * 200, P * 201, 0)), 1), "history_len"),
+        (lambda: sgd(metas((scale_w, P * 201, 16)), 1), "must hold amax_w"),
+        (lambda: sgd(metas((scale_w, amax_w, 16), (scale_w, amax_w, 16)), 2), "two metas"),
+    ]
+    for i, (fn, word) in enumerate(cases):
+        assert fn() == fp8mp.ERR_INVALID, i
+        assert word in fp8mp.last_error(), (i, fp8mp.last_error())
+    adam = lib.mp_master_step_adam_prescanned_scaling_ex(P, 64, P, P, P, 8 * P, 4 * P, scale_w, amax_w, P, P, 9 * P,
+                                                          10 * P, P, 1e-4, 0.9, 0.999, 1e-8, 0.5, 2.0, 2000, ok, 9,
+                                                          fp8mp.AMAX_MOST_RECENT, 0, both, None)
+    assert adam == fp8mp.ERR_INVALID and "n_metas" in fp8mp.last_error()
+
+
+def test_binding_routes_the_scaling_step(monkeypatch):
+    """mp_master_step(metas=...) calls mp_master_step_prescanned_scaling_ex
+    with the metas' array, their count, the algorithm, margin and flags."""
+    import torch
+
+    calls = []
+
+    class FakeLib:
+        def __getattr__(self, name):
+            def f(*a):
+                calls.append((name, a))
+                return 0
+            return f
+
+    monkeypatch.setattr(fp8mp, "_lib", FakeLib())
+    t = {k: torch.zeros(16, dtype=torch.float32) for k in ("g", "w", "v", "s", "a", "S", "gr", "f", "nf")}
+    w8, w8_in = torch.zeros(16, dtype=torch.uint8), torch.ones(16, dtype=torch.uint8)
+    ms = [fp8mp.Meta(4, fp8mp.E4M3, device="cpu") for _ in range(3)]
+    flags = fp8mp.OVERLAP_PREVIOUS | fp8mp.WAIT_DW_DONE
+    fp8mp.mp_master_step(t["g"], t["w"], t["v"], w8, t["s"], t["a"], t["S"], t["gr"], t["f"], 0.1, 0.9,
+                         stream=0, grad_nonfinite=t["nf"], w8_in=w8_in, flags=flags, metas=ms,
+                         amax_algo=fp8mp.AMAX_MAX, margin=2)
+    name, a = calls[-1]
+    assert name == "mp_master_step_prescanned_scaling_ex"
+    assert a[4] == w8_in.data_ptr() and a[5] == w8.data_ptr()
+    assert a[17][1].scale == ms[1].scale.data_ptr() and a[18:22] == (3, fp8mp.AMAX_MAX, 2, flags)
+    with pytest.raises(fp8mp.Fp8mpError):
+        fp8mp.mp_master_step(t["g"], t["w"], t["v"], w8, t["s"], t["a"], t["S"], t["gr"], t["f"], 0.1, 0.9,
+                             stream=0, metas=ms)
