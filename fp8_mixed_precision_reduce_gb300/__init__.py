@@ -28,7 +28,9 @@ EXPORTS = ("fp8_quantize", "fp8_quantize_ex", "fp8_quantize_current", "fp8_quant
            "fp8_quantize_dbias_workspace_bytes", "fp8_quantize_dbias_noalloc", "fp8_linear_fwd", "fp8_linear_fwd_fp8out", "fp8_linear_dgrad", "fp8_linear_wgrad",
            "fp8_linear_bwd", "fp8_linear_bwd_rowmajor", "fp8_linear_bwd_rowmajor_ex", "delayed_scaling_update",
            "delayed_scaling_update_ex", "mp_master_step", "mp_master_step_adam", "mp_master_step_prescanned", "mp_master_step_adam_prescanned",
-           "mp_master_step_prescanned_ex", "mp_master_step_adam_prescanned_ex", "fp8mp_check", "fp8mp_last_error",
+           "mp_master_step_prescanned_ex", "mp_master_step_adam_prescanned_ex",
+           "mp_master_step_prescanned_scaling_ex", "mp_master_step_adam_prescanned_scaling_ex", "fp8mp_check",
+           "fp8mp_last_error",
            "fp8mp_version", "fp8mp_selftest_timeout", "fp8mp_selftest_barrier_timeout")
 
 _lib = None
