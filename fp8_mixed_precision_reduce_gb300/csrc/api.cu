@@ -560,6 +560,10 @@ static int build_fold(const char *fn, const fp8mp_meta *metas, int32_t n_metas, 
             REQUIRE(m.cur_amax == amax_w, "%s: the meta holding scale_w must hold amax_w as its cur_amax", fn);
             fb->w_index = i;
         }
+        // the step adds to amax_w only after the weight's meta (found by
+        // scale_w) has zeroed it: a meta holding amax_w under another scale
+        // would zero it while the step's blocks add to it
+        REQUIRE(m.cur_amax != amax_w || m.scale == scale_w, "%s: meta %d holds amax_w but not scale_w", fn, i);
         fb->m[i] = FoldMeta{m.amax_history, m.scale, m.scale_inv, m.cur_amax, m.history_len, m.fmt};
     }
     fb->n = n_metas;

@@ -593,7 +593,8 @@ int mp_master_step_adam_prescanned_ex(const uint16_t *grad_bf16, int64_t n, floa
  * them) while the update runs. Results equal, bit for bit, those of
  * delayed_scaling_update_ex enqueued before the backward launch followed by
  * the _ex step. Every other argument as the _ex calls; FP8MP_ERR_INVALID for
- * a bad meta, a bad count, two metas holding scale_w, or other flags.
+ * a bad meta, a bad count, two metas holding scale_w, a meta holding amax_w
+ * but not scale_w, or other flags.
  */
 int mp_master_step_prescanned_scaling_ex(const uint16_t *grad_bf16, int64_t n, float *master, float *momentum,
                                          const uint8_t *w8_in, uint8_t *w8_out, const float *scale_w,

@@ -330,6 +330,7 @@ def test_scaling_master_step_validation(lib):
         (lambda: sgd(metas((P * 200, P * 201, 0)), 1), "history_len"),
         (lambda: sgd(metas((scale_w, P * 201, 16)), 1), "must hold amax_w"),
         (lambda: sgd(metas((scale_w, amax_w, 16), (scale_w, amax_w, 16)), 2), "two metas"),
+        (lambda: sgd(metas((P * 200, amax_w, 16)), 1), "holds amax_w but not scale_w"),
     ]
     for i, (fn, word) in enumerate(cases):
         assert fn() == fp8mp.ERR_INVALID, i
