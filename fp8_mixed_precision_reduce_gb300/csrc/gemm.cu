@@ -552,14 +552,17 @@ gemm_fp8_kernel(const __grid_constant__ GemmBatch batch) {
         // scale, bias and rounding in registers, the row written into a
         // 128-byte-swizzled 32 x 128 B staging box, then one TMA store per
         // box. Two boxes per warp alternate so the next chunk overlaps the
-        // store.
+        // store; they alternate by committed store, not by chunk, because a
+        // chunk past a ragged edge stores nothing (and commits no bulk group),
+        // and "at most one group still reading" only protects the box the
+        // newest group does not read.
         const int q = warp & 3;  // this warp may access TMEM lanes 32q .. 32q+31
         const int row_in_tile = static_cast<int>(rank) * ROWS_A + q * 32 + lane;
         const uint32_t stage_box = base + C::EPI_OFFSET + static_cast<uint32_t>((warp - 2) * 2 * C::EPI_BOX_BYTES);
         float am0 = 0.0f, am1 = 0.0f;  // max |y| of problem 0 / 1
         bool bad0 = false, bad1 = false;  // a stored element of problem 0 / 1 is Inf or NaN
         int lt = 0;
-        uint32_t chunk_no = 0;
+        uint32_t stored = 0;  // TMA stores this warp has committed
         for (int r = 0; r < rounds; ++r) {
             const int tile = serpentine_tile(r, cluster_id, num_clusters);
             if (tile >= num_tiles) continue;
@@ -591,7 +594,7 @@ gemm_fp8_kernel(const __grid_constant__ GemmBatch batch) {
             float am = 0.0f;
             bool bad = false;
 #pragma unroll 1
-            for (int c = 0; c < TILE_N; c += box_cols, ++chunk_no) {
+            for (int c = 0; c < TILE_N; c += box_cols) {
                 uint32_t packed[32];  // this lane's 128-byte row of the box
 #pragma unroll
                 for (int half = 0; half < 4; ++half) {
@@ -660,9 +663,12 @@ gemm_fp8_kernel(const __grid_constant__ GemmBatch batch) {
                         for (int j = 0; j < 32; ++j) bad |= (packed[j] & 0x7F800000u) == 0x7F800000u;
                     }
                 }
-                // the staging box written two chunks ago must have been read by its TMA store
-                const uint32_t box = stage_box + (chunk_no & 1u) * C::EPI_BOX_BYTES;
-                if (lane == 0 && chunk_no >= 2) bulk_wait_read_le1();
+                // boxes that start outside the output (ragged last tiles) are
+                // neither staged nor stored
+                if (nb * TILE_N + c >= rows_b || warp_row0 >= rows_a) continue;
+                // the staging box of the store before last must have been read
+                const uint32_t box = stage_box + (stored & 1u) * C::EPI_BOX_BYTES;
+                if (lane == 0 && stored >= 2) bulk_wait_read_le1();
                 __syncwarp();
                 const uint32_t row_addr = box + static_cast<uint32_t>(lane) * 128u;
 #pragma unroll
@@ -671,11 +677,11 @@ gemm_fp8_kernel(const __grid_constant__ GemmBatch batch) {
                                  packed[4 * j], packed[4 * j + 1], packed[4 * j + 2], packed[4 * j + 3]);
                 fence_proxy_async_smem();
                 __syncwarp();
-                // boxes that start outside the output (ragged last tiles) are not stored
-                if (lane == 0 && nb * TILE_N + c < rows_b && warp_row0 < rows_a) {
+                if (lane == 0) {
                     tma_store_2d(&P.to, box, nb * TILE_N + c, warp_row0);
                     bulk_commit_group();
                 }
+                ++stored;
             }
             if (pi == 0) {
                 am0 = max_ignore_nan(am0, am);
