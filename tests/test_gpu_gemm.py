@@ -197,6 +197,38 @@ def test_backward_from_rowmajor_copies(cuda_lib, orc, engine, M, N, K, dy_fmt, d
     assert torch.equal(dx.float(), dx1.float()) and torch.equal(dw.float(), dw1.float())
 
 
+@pytest.mark.parametrize("M,N,K", [(256, 2048, 528), (4096, 1024, 48), (2048, 512, 80)])
+def test_ragged_edge_outputs_repeat_bitwise(cuda_lib, orc, engine, M, N, K):
+    """Output widths that end inside a tile column (528 = 2 x 256 + 16, 48,
+    80), so the epilogue stages and stores only some chunks of the last one:
+    40 more launches of the fused backward give bitwise the first one's dX
+    and dW, which is within the GEMM tolerance of the oracle. A staging box
+    rewritten while its TMA store still read it would show as rows of
+    another chunk's values (or zeros) in one of the repeats."""
+    rng = np.random.default_rng(M + 3 * N + 5 * K)
+    dy8 = finite_codes(rng, (M, N), E5M2)
+    w8 = finite_codes(rng, (N, K), E4M3)
+    x8 = finite_codes(rng, (M, K), E4M3)
+    s_dy, s_w, s_x = 2.0 ** -9, 0.625, 0.125
+    ops = (dev(dy8), dev(w8), dev(x8), sc(s_dy), sc(s_w), sc(s_x))
+    dx = torch.empty((M, K), dtype=torch.bfloat16, device="cuda")
+    dw = torch.empty((N, K), dtype=torch.float32, device="cuda")
+    cuda_lib.fp8_linear_bwd_rowmajor(*ops, dx, dw, dy_fmt=E5M2)
+    assert cuda_lib.fp8mp_check() == 0
+    w8t, x8t, dy8t = (np.ascontiguousarray(a.T) for a in (w8, x8, dy8))
+    ref, ab = orc.gemm_ref(dy8, E5M2, w8t, E4M3, s_dy, s_w)
+    gemm_tolerance_check(np_view(dx.float()).astype(np.float64), ref, ab, f"ragged dx {M}x{N}x{K}")
+    ref, ab = orc.gemm_ref(dy8t, E5M2, x8t, E4M3, s_dy, s_x)
+    gemm_tolerance_check(np_view(dw).astype(np.float64), ref, ab, f"ragged dw {M}x{N}x{K}")
+    dx0, dw0 = dx.clone(), dw.clone()
+    for i in range(40):
+        dx.fill_(7.0)
+        dw.fill_(7.0)
+        cuda_lib.fp8_linear_bwd_rowmajor(*ops, dx, dw, dy_fmt=E5M2)
+        assert torch.equal(dx, dx0) and torch.equal(dw, dw0), f"repeat {i + 1} differs from the first launch"
+    assert cuda_lib.fp8mp_check() == 0
+
+
 def test_backward_from_rowmajor_copies_one_side(cuda_lib, orc, engine):
     """dx or dw None: only the other gradient is computed (and written)."""
     M, N, K = 272, 400, 528
