@@ -40,13 +40,25 @@ def test_fp8linear_two_steps(cuda_lib, orc):
         ref, ab = orc.gemm_ref(qx, E4M3, qw, E4M3, sx, sw, bias=base.b.double().numpy())
         yh = np_view(y.detach())
         gemm_tolerance_check(yh.astype(np.float64), ref, ab, f"t={t} y")
+        # the three gradients are all checked before any failure is raised:
+        # which of them agree tells a wrong E5M2 copy of dY (dx, dw and the
+        # codes behind them) from a wrong store of one output
+        failed = []
         ref, ab = orc.gemm_ref(qd, E5M2, orc.transpose_u8(qw), E4M3, sd, sw)
-        gemm_tolerance_check(np_view(x.grad).astype(np.float64), ref, ab, f"t={t} dx")
+        try:
+            gemm_tolerance_check(np_view(x.grad).astype(np.float64), ref, ab, f"t={t} dx")
+        except AssertionError as e:
+            failed.append(str(e))
         ref, ab = orc.gemm_ref(orc.transpose_u8(qd), E5M2, orc.transpose_u8(qx), E4M3, sd, sx)
-        gemm_tolerance_check(np_view(layer.weight.grad).astype(np.float64), ref, ab, f"t={t} dw")
+        try:
+            gemm_tolerance_check(np_view(layer.weight.grad).astype(np.float64), ref, ab, f"t={t} dw")
+        except AssertionError as e:
+            failed.append(str(e))
         db_ref, db_abs = orc.dbias(dyn)
         err = np.abs(np_view(layer.bias.grad).astype(np.float64) - db_ref)
-        assert (err <= 1024 * 2.0 ** -24 * db_abs + 1e-30).all()
+        if not (err <= 1024 * 2.0 ** -24 * db_abs + 1e-30).all():
+            failed.append(f"t={t} dbias: {int((err > 1024 * 2.0 ** -24 * db_abs + 1e-30).sum())} columns out of bound")
+        assert not failed, "\n".join(failed)
 
         om["x"].record_amax(orc.amax(xn))
         om["w"].record_amax(orc.amax(wn))
